@@ -1,0 +1,313 @@
+#!/usr/bin/env python
+"""Benchmark of the relative-position memory attention hot path.
+
+Workload: one layer's forward + backward at B=16, H=16, L=512, M=512 (memory
+full), d_h=64, bf16 inputs with fp32 accumulation; synthetic seeded inputs
+with the distributions of that configuration. A step = rxl_attn_fwd +
+rxl_attn_bwd over that batch.
+
+Throughput counts algorithmic work only: visible pairs N = B*H*(L*m +
+L(L+1)/2); forward 6*d_h = 384 flop per pair (three d_h-long products: the
+content score, the position score, P.V), backward 12*d_h = 768 flop per pair
+(dV, dP, dQ-content, dQ-position, dK, dR); recomputation is not counted.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream, with the L2 flushed (a 256 MiB write) between steps
+outside the events; barrier + synchronize around the timed region, max over
+ranks. Under torchrun every rank runs its own copy of the workload (the
+path's (b,h) units are independent: weak scaling, no collective).
+
+--impl reference times the float64 CPU oracle on a bounded sample of the
+same workload (the only comparison program this path has).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "rel-pos mem-attention fwd+bwd TFLOP/s & tokens/s vs bf16 tensor-core peak"
+WORKLOAD = "cfg3_bf16_B16H16_L512M512_dh64_fwd+bwd"
+B, H, L, M, DH = 16, 16, 512, 512, 64
+SCALE = 1.0 / math.sqrt(DH)
+FLOP_FWD_PAIR, FLOP_BWD_PAIR = 6 * DH, 12 * DH
+
+
+def visible_pairs(b, h, l, m):
+    return b * h * (l * m + l * (l + 1) // 2)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.lines, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        time.sleep(0.3)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_inputs(seed=0):
+    import rxl_inputs as gen
+    w = gen.CFG3
+    p, s, mem = gen.layer_params(w), gen.segment_inputs(w), gen.initial_memory(w)
+    return dict(q=s["q"], k_mem=mem["k_mem"], k_cur=s["k_cur"], v_mem=mem["v_mem"], v_cur=s["v_cur"],
+                u=p["u"], vb=p["vb"], r=p["r"], do=s["do"])
+
+
+def cpu_sample(x, units_heads, nthreads):
+    """Oracle fwd+bwd on the heads `units_heads` (all batch rows); returns
+    (seconds, algorithmic flop of the sample)."""
+    import numpy as np
+    import oracle
+    k = np.concatenate([x["k_mem"], x["k_cur"]], 2)
+    v = np.concatenate([x["v_mem"], x["v_cur"]], 2)
+    hs = slice(units_heads[0], units_heads[1])
+    t0 = time.perf_counter()
+    oracle.fwd(x["q"][:, hs], k[:, hs], v[:, hs], x["r"][hs], x["u"][hs], x["vb"][hs], SCALE, nthreads=nthreads)
+    oracle.bwd(x["q"][:, hs], k[:, hs], v[:, hs], x["r"][hs], x["u"][hs], x["vb"][hs], x["do"][:, hs], SCALE,
+               nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    nh = units_heads[1] - units_heads[0]
+    return dt, visible_pairs(B, nh, L, M) * (FLOP_FWD_PAIR + FLOP_BWD_PAIR)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    x = make_inputs()
+    nthreads = os.cpu_count() or 1
+    heads = (0, 1)                  # one head, all 16 batch rows: 16 (b,h) units per step
+    for _ in range(args.warmup):
+        cpu_sample(x, heads, nthreads)
+    tot_s, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = cpu_sample(x, heads, nthreads)
+        tot_s += dt
+        tot_f += fl
+    value = tot_f / tot_s / 1e12
+    pairs = visible_pairs(B, 1, L, M)
+    sample = f"fwd+bwd of 1 head x {B} batch rows ({pairs} visible pairs) of the workload per step"
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "tokens_per_s": args.steps * B * L / 16 / tot_s,
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "L": L, "M": M, "dh": DH, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": min(nthreads, B), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import long_context_lm_rel_gb300 as rxl
+    from tests._harness import AttnCall, place_kv
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    rxl.lib()
+    x = make_inputs()
+    cap = m = M
+    c = AttnCall(x["q"], place_kv(x["k_mem"], x["k_cur"], cap, 0), place_kv(x["v_mem"], x["v_cur"], cap, 0),
+                 x["r"], x["u"], x["vb"], cap=cap, m=m, head=0, dtype="bf16", scale=SCALE).alloc_bwd(x["do"])
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def step():
+        c.fwd(stream)
+        n = rxl.rxl_last_launch_count()
+        c.bwd(stream)
+        return n + rxl.rxl_last_launch_count()
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    launches = 0
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        for e in ev:
+            flush.zero_()                 # L2 flush, outside the timed events
+            e[0].record(stream)
+            c.fwd(stream)
+            launches += rxl.rxl_last_launch_count()
+            e[1].record(stream)
+            c.bwd(stream)
+            launches += rxl.rxl_last_launch_count()
+            e[2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    tot_ms = sum(fwd_ms) + sum(bwd_ms)
+    t = torch.tensor([tot_ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    tot_ms = float(t.item())
+
+    pairs = visible_pairs(B, H, L, m)
+    flop_step = pairs * (FLOP_FWD_PAIR + FLOP_BWD_PAIR)
+    value = world * args.steps * flop_step / (tot_ms * 1e-3) / 1e12
+    tokens = world * args.steps * B * L / (tot_ms * 1e-3)
+
+    # end to end through the C ABI from pinned host buffers: inputs H2D, fwd,
+    # bwd, every output D2H, each step
+    host_in = {n: getattr(c, n).cpu().pin_memory() for n in ("q", "k", "v", "r", "u", "vb", "do")}
+    host_out = {n: torch.empty_like(getattr(c, n), device="cpu").pin_memory()
+                for n in ("o", "lse", "dq", "dk", "dv", "dr", "du", "dvb")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n, t in host_in.items():
+            getattr(c, n).copy_(t, non_blocking=True)
+        c.fwd(stream)
+        c.bwd(stream)
+        for n, t in host_out.items():
+            t.copy_(getattr(c, n), non_blocking=True)
+
+    for _ in range(max(args.warmup, 1)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_value = world * args.steps * flop_step / (float(t.item()) * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    peak_tf, _, peak_kind = peaks()
+    bwd_avg = sum(bwd_ms) / len(bwd_ms)
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    achieved = pairs * FLOP_BWD_PAIR / (bwd_avg * 1e-3) / 1e12
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": tokens, "fwd_ms": fwd_avg, "bwd_ms": bwd_avg,
+        "fwd_tflops": pairs * FLOP_FWD_PAIR / (fwd_avg * 1e-3) / 1e12,
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "L": L, "M": M, "mem_len": m, "dh": DH,
+                   "flop_per_step": flop_step, "l2": "flushed between steps (256 MiB write, outside events)",
+                   "parallelism": f"{world} independent replicas (one per GPU)"},
+        "roofline": {"bound": "tensor", "kernel": "rxl_attn_bwd", "achieved": achieved, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+                     "peak_kind": f"{peak_kind} bf16 burst"},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        dt, fl = cpu_sample(x, (0, 4), nthreads)
+        out["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": min(nthreads, 4 * B),
+                               "kind": "oracle",
+                               "sample": f"fwd+bwd of 4 heads x {B} batch rows (64 of 256 (b,h) units), {dt:.1f} s"}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world)
+    finally:
+        if world > 1 and args.impl == "ours":
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

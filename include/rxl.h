@@ -1,0 +1,170 @@
+/*
+ * rxl.h -- C ABI of librxl: Transformer-XL relative-position memory attention
+ * on one GB300 (sm_103a).
+ *
+ * The operation (Transformer-XL page, zty624.github.io ch4_transformer/xl.html):
+ *   - "Segment-Level Recurrence": the L queries of the current segment attend
+ *     over [SG(memory); current]; keys/values have memory+current rows,
+ *     queries only the current ones ("Batched Tensor Contract").
+ *   - "Causal Mask With Memory", eq. allow: key positions -m..-1 (memory)
+ *     are always visible, current key j is visible to query i iff j <= i.
+ *   - "Relative Positional Encoding", four-term score:
+ *        A_ij = (q_i + u).k_j + (q_i + v).r_{i-j}
+ *     (the regrouped form is printed on the iopencloud page, section 2.2).
+ *   - "Dimension Walkthrough": O = softmax((A + M_causal)/sqrt(d_h)) V; the
+ *     scale applies to the whole of A; R has (M+L) rows, one per distance.
+ *   - "Why Stop Gradient": gradients reach the K/V rows of the memory block
+ *     (and R, u, v) but nothing flows back into the cached states.
+ *   - eq. Tail_M and update_mems ("Batched Tensor Contract"): after each
+ *     segment every layer keeps the last M states; the Polish glossary page
+ *     (robocikowo.com) describes it as a FIFO buffer on the GPU whose oldest
+ *     entries are overwritten.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The
+ *     library allocates no device memory and keeps no device state between
+ *     calls; a call only reads its inputs and writes its outputs/workspace.
+ *   - Row-major, contiguous, d_h innermost. Element type = desc.dtype for
+ *     q, k, v, r, u, vbias, o, dout, dq, dk, dv; float32 for lse, dr, du,
+ *     dvbias and workspace.
+ *   - Every pointer must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *     and never synchronise. Arguments are checked before anything is
+ *     launched; on any error nothing is launched and no output is touched.
+ *     Device faults surface at the caller's next synchronisation.
+ *   - Thread safety: calls may be made from several host threads; the only
+ *     shared host state is a cache of TMA descriptors guarded by a mutex.
+ */
+#ifndef RXL_H
+#define RXL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *rxl_stream_t;
+
+typedef enum {
+  RXL_OK = 0,
+  RXL_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative or inconsistent size */
+  RXL_ERR_UNSUPPORTED = 2,        /* valid request this build does not implement (d_h != 64, dtype) */
+  RXL_ERR_MISALIGNED = 3,         /* pointer or row stride not 16-byte aligned */
+  RXL_ERR_WORKSPACE_TOO_SMALL = 4,
+  RXL_ERR_CUDA = 5                /* a CUDA call or launch failed (see rxl_last_cuda_error) */
+} rxl_status;
+
+typedef enum { RXL_DTYPE_F32 = 0, RXL_DTYPE_BF16 = 1 } rxl_dtype;
+
+/*
+ * Shape of one attention call.
+ *   B, H, L   batch, heads, current-segment rows (queries), all >= 1
+ *   dh        head width; must be 64
+ *   mem_cap   M: rows reserved for memory in K/V (>= 0)
+ *   mem_len   m: valid memory rows, 0 <= m <= M (memory fills up over the
+ *             first segments of a stream)
+ *   mem_head  physical row of the OLDEST memory row, 0 <= head < M (0 if M==0)
+ *   scale     multiplies the whole score A (1/sqrt(dh) in the paper)
+ *
+ * K and V have M+L rows per (b,h): rows [0, M) are the memory ring, and
+ * logical memory row t (t = 0 oldest, t < m) lives at physical row
+ * (mem_head + t) mod M; rows [M, M+L) are the current segment. Logical key
+ * position of memory row t is t - m; of current row i it is i. R has M+L rows
+ * per head; row d embeds the distance d; rows 0..m+L-1 are read.
+ */
+typedef struct {
+  int B, H, L, dh;
+  int mem_cap;
+  int mem_len;
+  int mem_head;
+  float scale;
+  rxl_dtype dtype;
+} rxl_attn_desc;
+
+/*
+ * Forward (Transformer-XL page, "Relative Positional Encoding" and
+ * "Dimension Walkthrough"):
+ *   O_i   = sum_j softmax_j(scale * A_ij | allow(i,j)) V_j
+ *   lse_i = log sum_j exp(scale * A_ij)   (natural log, allowed j only)
+ * q [B,H,L,dh]; k, v [B,H,M+L,dh]; r [H,M+L,dh]; u, vbias [H,dh];
+ * o [B,H,L,dh] (written); lse [B,H,L] float32 (written).
+ * The L x (m+L) score matrix is never written to memory.
+ */
+rxl_status rxl_attn_fwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                        const void *r, const void *u, const void *vbias, void *o, float *lse,
+                        rxl_stream_t stream);
+
+/* Workspace bytes rxl_attn_bwd needs for this shape (0 on invalid desc). */
+size_t rxl_attn_bwd_workspace_bytes(const rxl_attn_desc *desc);
+
+/*
+ * Backward of the forward above for upstream gradient dout [B,H,L,dh], given
+ * the forward's o and lse. With dA_ij = scale * P_ij (dout_i.V_j - D_i) and
+ * D_i = dout_i . o_i:
+ *   dq_i  = sum_j dA_ij (k_j + r_{i-j})            [B,H,L,dh]
+ *   dk_j  = sum_i dA_ij (q_i + u)                  [B,H,M+L,dh]
+ *   dv_j  = sum_i P_ij dout_i                      [B,H,M+L,dh]
+ *   dr_d  = sum_b sum_{i-j=d} dA_ij (q_i + v)      [H,M+L,dh] float32
+ *   du    = sum_{b,i,j} dA_ij k_j                  [H,dh]     float32
+ *   dvbias= sum_{b,i,j} dA_ij r_{i-j}              [H,dh]     float32
+ * dk/dv use the physical row layout of k/v: memory rows get their K/V
+ * gradient (stop-gradient stops only the path into the cached states, which
+ * this call never writes); ring rows that hold no valid memory get zeros, as
+ * do dr rows d >= m+L. k and v are read-only here.
+ * workspace: device scratch of at least rxl_attn_bwd_workspace_bytes(desc)
+ * bytes (16-byte aligned), owned by the caller; contents on entry ignored.
+ */
+rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                        const void *r, const void *u, const void *vbias, const void *o,
+                        const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                        float *dr, float *du, float *dvbias, void *workspace,
+                        size_t workspace_bytes, rxl_stream_t stream);
+
+/*
+ * FIFO memory ring (eq. Tail_M; update_mems with mem_len == cap).
+ *   data         device pointer to plane 0, row 0
+ *   planes       independent rings (e.g. B*H), >= 1
+ *   cap          capacity M in rows (>= 0; 0 keeps nothing)
+ *   D            elements per row (D * elem_size must be a multiple of 16)
+ *   plane_stride elements between planes (>= cap*D, 16-byte multiple)
+ *   head, len    oldest row's physical index and number of valid rows;
+ *                logical row t lives at physical (head + t) mod cap
+ */
+typedef struct {
+  void *data;
+  int planes, cap, D;
+  long long plane_stride;
+  rxl_dtype dtype;
+  int head, len;
+} rxl_ring;
+
+/*
+ * Append L rows per plane and keep the last cap rows:
+ *   ring <- Tail_cap([ring_logical; src]).
+ * src plane p starts at src + p * src_plane_stride (elements) and holds L
+ * contiguous rows of D elements; src must not overlap the rows written.
+ * Only the last min(L, cap) rows of src are copied (bit-exact); nothing
+ * else in the ring moves. On success ring->head and ring->len are advanced
+ * on the host (the struct is caller-owned host memory); on error the ring
+ * struct and the device data are unchanged.
+ */
+rxl_status rxl_mem_update(rxl_ring *ring, const void *src, long long src_plane_stride, int L,
+                          rxl_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *rxl_status_string(rxl_status status);
+
+/* The CUDA error code behind the most recent RXL_ERR_CUDA on this thread. */
+int rxl_last_cuda_error(void);
+
+/* Number of kernels the most recent successful call on this thread launched. */
+int rxl_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RXL_H */

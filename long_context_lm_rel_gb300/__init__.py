@@ -1,0 +1,130 @@
+"""Python binding of librxl (include/rxl.h): argument marshalling only.
+
+Every function has the name and the argument order of its C entry point.
+Tensors may be torch tensors (their data_ptr() is passed) or raw integer
+device addresses. Each call raises RxlError on a non-OK status. The library
+must have been built (``build()``); nothing here computes anything, and
+there is no fallback when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB, build  # noqa: F401
+
+RXL_OK = 0
+RXL_ERR_INVALID_ARGUMENT = 1
+RXL_ERR_UNSUPPORTED = 2
+RXL_ERR_MISALIGNED = 3
+RXL_ERR_WORKSPACE_TOO_SMALL = 4
+RXL_ERR_CUDA = 5
+RXL_DTYPE_F32 = 0
+RXL_DTYPE_BF16 = 1
+
+
+class rxl_attn_desc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int), ("dh", ctypes.c_int),
+                ("mem_cap", ctypes.c_int), ("mem_len", ctypes.c_int), ("mem_head", ctypes.c_int),
+                ("scale", ctypes.c_float), ("dtype", ctypes.c_int)]
+
+
+class rxl_ring(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("planes", ctypes.c_int), ("cap", ctypes.c_int),
+                ("D", ctypes.c_int), ("plane_stride", ctypes.c_longlong), ("dtype", ctypes.c_int),
+                ("head", ctypes.c_int), ("len", ctypes.c_int)]
+
+
+class RxlError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {rxl_status_string(status)}"
+                         + (f" (cuda error {lib().rxl_last_cuda_error()})" if status == RXL_ERR_CUDA else ""))
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded librxl (ctypes). Raises if the library was not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError(f"librxl.so is not built ({LIB}); call long_context_lm_rel_gb300.build()")
+            L = ctypes.CDLL(LIB)
+            P, vp = ctypes.POINTER, ctypes.c_void_p
+            L.rxl_attn_fwd.argtypes = [P(rxl_attn_desc)] + [vp] * 8 + [vp]
+            L.rxl_attn_fwd.restype = ctypes.c_int
+            L.rxl_attn_bwd_workspace_bytes.argtypes = [P(rxl_attn_desc)]
+            L.rxl_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+            L.rxl_attn_bwd.argtypes = [P(rxl_attn_desc)] + [vp] * 16 + [ctypes.c_size_t, vp]
+            L.rxl_attn_bwd.restype = ctypes.c_int
+            L.rxl_mem_update.argtypes = [P(rxl_ring), vp, ctypes.c_longlong, ctypes.c_int, vp]
+            L.rxl_mem_update.restype = ctypes.c_int
+            L.rxl_status_string.argtypes = [ctypes.c_int]
+            L.rxl_status_string.restype = ctypes.c_char_p
+            L.rxl_last_cuda_error.argtypes = []
+            L.rxl_last_cuda_error.restype = ctypes.c_int
+            L.rxl_last_launch_count.argtypes = []
+            L.rxl_last_launch_count.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != RXL_OK:
+        raise RxlError(status, where)
+
+
+def make_desc(B, H, L, mem_cap, mem_len, mem_head=0, scale=0.125, dtype=RXL_DTYPE_BF16, dh=64):
+    return rxl_attn_desc(B, H, L, dh, mem_cap, mem_len, mem_head, scale, dtype)
+
+
+def rxl_attn_fwd(desc, q, k, v, r, u, vbias, o, lse, stream=None):
+    _check(lib().rxl_attn_fwd(ctypes.byref(desc), *map(_ptr, (q, k, v, r, u, vbias, o, lse)),
+                              _stream(stream)), "rxl_attn_fwd")
+
+
+def rxl_attn_bwd_workspace_bytes(desc) -> int:
+    return int(lib().rxl_attn_bwd_workspace_bytes(ctypes.byref(desc)))
+
+
+def rxl_attn_bwd(desc, q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr, du, dvbias,
+                 workspace, workspace_bytes, stream=None):
+    _check(lib().rxl_attn_bwd(ctypes.byref(desc),
+                              *map(_ptr, (q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr, du,
+                                          dvbias, workspace)),
+                              int(workspace_bytes), _stream(stream)), "rxl_attn_bwd")
+
+
+def rxl_mem_update(ring: rxl_ring, src, src_plane_stride: int, L: int, stream=None):
+    _check(lib().rxl_mem_update(ctypes.byref(ring), _ptr(src), int(src_plane_stride), int(L),
+                                _stream(stream)), "rxl_mem_update")
+
+
+def rxl_status_string(status: int) -> str:
+    return lib().rxl_status_string(int(status)).decode()
+
+
+def rxl_last_launch_count() -> int:
+    return int(lib().rxl_last_launch_count())

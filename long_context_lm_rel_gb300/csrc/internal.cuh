@@ -1,0 +1,46 @@
+// Internal declarations shared by the translation units of librxl.
+// Not part of the public ABI (include/rxl.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/rxl.h"
+
+namespace rxl {
+
+// Validated shape of one attention call, as the kernels see it.
+struct AttnShape {
+  int B, H, L;
+  int cap;        // M: memory rows reserved in K/V
+  int m;          // valid memory rows
+  int head;       // physical row of the oldest memory row
+  float scale;
+  int kv_rows;    // cap + L
+};
+
+// Workspace layout of the backward (offsets in bytes from the base).
+struct BwdWorkspace {
+  size_t d_off, dqu_off, dqv_off, total;
+};
+BwdWorkspace simt_bwd_workspace(const AttnShape &s);
+
+// Launchers return cudaSuccess or the launch error; `launches` is
+// incremented by the number of kernels put on the stream.
+cudaError_t launch_mem_update(void *data, int planes, int cap, int D, long long plane_stride,
+                              int elem_bytes, const void *src, long long src_plane_stride,
+                              int src_row0, int nrows, int dst_row0, cudaStream_t st,
+                              int *launches);
+
+cudaError_t launch_simt_fwd(const AttnShape &s, rxl_dtype dt, const void *q, const void *k,
+                            const void *v, const void *r, const void *u, const void *vb,
+                            void *o, float *lse, cudaStream_t st, int *launches);
+
+cudaError_t launch_simt_bwd(const AttnShape &s, rxl_dtype dt, const void *q, const void *k,
+                            const void *v, const void *r, const void *u, const void *vb,
+                            const void *o, const float *lse, const void *dout, void *dq,
+                            void *dk, void *dv, float *dr, float *du, float *dvb, void *ws,
+                            cudaStream_t st, int *launches);
+
+}  // namespace rxl

@@ -1,0 +1,152 @@
+// C ABI of librxl: argument validation, dispatch and status reporting.
+// See include/rxl.h for the contract of every entry point.
+#include <math.h>
+#include <stdint.h>
+
+#include <initializer_list>
+
+#include "internal.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+thread_local int g_last_launches = 0;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+rxl_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return RXL_OK;
+  g_last_cuda_error = (int)e;
+  return RXL_ERR_CUDA;
+}
+
+// Checks the descriptor; on success fills the kernel-side shape.
+rxl_status check_desc(const rxl_attn_desc *d, rxl::AttnShape *s) {
+  if (!d) return RXL_ERR_INVALID_ARGUMENT;
+  if (d->B < 1 || d->H < 1 || d->L < 1 || d->dh < 1) return RXL_ERR_INVALID_ARGUMENT;
+  if (d->mem_cap < 0 || d->mem_len < 0 || d->mem_len > d->mem_cap) return RXL_ERR_INVALID_ARGUMENT;
+  if (d->mem_cap == 0 ? d->mem_head != 0 : (d->mem_head < 0 || d->mem_head >= d->mem_cap))
+    return RXL_ERR_INVALID_ARGUMENT;
+  if (!isfinite(d->scale)) return RXL_ERR_INVALID_ARGUMENT;
+  // int32 row indexing inside the kernels: keep every per-(b,h) extent and
+  // the grid sizes far from overflow
+  const long long rows = (long long)d->mem_cap + d->L;
+  if (rows > (1LL << 24) || (long long)d->B * d->H > (1LL << 24) ||
+      (long long)d->B * d->H * rows > (1LL << 34))
+    return RXL_ERR_INVALID_ARGUMENT;
+  if (d->dtype != RXL_DTYPE_F32 && d->dtype != RXL_DTYPE_BF16) return RXL_ERR_UNSUPPORTED;
+  if (d->dh != 64) return RXL_ERR_UNSUPPORTED;
+  s->B = d->B; s->H = d->H; s->L = d->L;
+  s->cap = d->mem_cap; s->m = d->mem_len; s->head = d->mem_head;
+  s->scale = d->scale;
+  s->kv_rows = d->mem_cap + d->L;
+  return RXL_OK;
+}
+
+rxl_status check_ptrs(std::initializer_list<const void *> ps) {
+  for (const void *p : ps)
+    if (!p) return RXL_ERR_INVALID_ARGUMENT;
+  for (const void *p : ps)
+    if (!aligned16(p)) return RXL_ERR_MISALIGNED;
+  return RXL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *rxl_status_string(rxl_status s) {
+  switch (s) {
+    case RXL_OK: return "RXL_OK";
+    case RXL_ERR_INVALID_ARGUMENT: return "RXL_ERR_INVALID_ARGUMENT";
+    case RXL_ERR_UNSUPPORTED: return "RXL_ERR_UNSUPPORTED";
+    case RXL_ERR_MISALIGNED: return "RXL_ERR_MISALIGNED";
+    case RXL_ERR_WORKSPACE_TOO_SMALL: return "RXL_ERR_WORKSPACE_TOO_SMALL";
+    case RXL_ERR_CUDA: return "RXL_ERR_CUDA";
+  }
+  return "RXL_ERR_UNKNOWN";
+}
+
+int rxl_last_cuda_error(void) { return g_last_cuda_error; }
+
+int rxl_last_launch_count(void) { return g_last_launches; }
+
+rxl_status rxl_attn_fwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                        const void *r, const void *u, const void *vbias, void *o, float *lse,
+                        rxl_stream_t stream) {
+  rxl::AttnShape s;
+  rxl_status st = check_desc(desc, &s);
+  if (st != RXL_OK) return st;
+  if ((st = check_ptrs({q, k, v, r, u, vbias, o, lse})) != RXL_OK) return st;
+  int launches = 0;
+  const cudaError_t e = rxl::launch_simt_fwd(s, desc->dtype, q, k, v, r, u, vbias, o, lse,
+                                             (cudaStream_t)stream, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
+size_t rxl_attn_bwd_workspace_bytes(const rxl_attn_desc *desc) {
+  rxl::AttnShape s;
+  if (check_desc(desc, &s) != RXL_OK) return 0;
+  return rxl::simt_bwd_workspace(s).total;
+}
+
+rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                        const void *r, const void *u, const void *vbias, const void *o,
+                        const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                        float *dr, float *du, float *dvbias, void *workspace,
+                        size_t workspace_bytes, rxl_stream_t stream) {
+  rxl::AttnShape s;
+  rxl_status st = check_desc(desc, &s);
+  if (st != RXL_OK) return st;
+  if ((st = check_ptrs({q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr, du, dvbias,
+                        workspace})) != RXL_OK)
+    return st;
+  if (workspace_bytes < rxl::simt_bwd_workspace(s).total) return RXL_ERR_WORKSPACE_TOO_SMALL;
+  int launches = 0;
+  const cudaError_t e =
+      rxl::launch_simt_bwd(s, desc->dtype, q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr,
+                           du, dvbias, workspace, (cudaStream_t)stream, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
+rxl_status rxl_mem_update(rxl_ring *ring, const void *src, long long src_plane_stride, int L,
+                          rxl_stream_t stream) {
+  if (!ring || L < 0) return RXL_ERR_INVALID_ARGUMENT;
+  if (ring->dtype != RXL_DTYPE_F32 && ring->dtype != RXL_DTYPE_BF16) return RXL_ERR_UNSUPPORTED;
+  if (ring->planes < 1 || ring->cap < 0 || ring->D < 1) return RXL_ERR_INVALID_ARGUMENT;
+  if (ring->len < 0 || ring->len > ring->cap) return RXL_ERR_INVALID_ARGUMENT;
+  if (ring->cap == 0 ? ring->head != 0 : (ring->head < 0 || ring->head >= ring->cap))
+    return RXL_ERR_INVALID_ARGUMENT;
+  const int es = ring->dtype == RXL_DTYPE_F32 ? 4 : 2;
+  if (ring->plane_stride < (long long)ring->cap * ring->D) return RXL_ERR_INVALID_ARGUMENT;
+  if (src_plane_stride < (long long)L * ring->D) return RXL_ERR_INVALID_ARGUMENT;
+  g_last_launches = 0;
+  if (ring->cap == 0 || L == 0) return RXL_OK;  // nothing kept / nothing appended
+  if (!ring->data || !src) return RXL_ERR_INVALID_ARGUMENT;
+  if (!aligned16(ring->data) || !aligned16(src) || ((long long)ring->D * es) % 16 != 0 ||
+      (ring->plane_stride * es) % 16 != 0 || (src_plane_stride * es) % 16 != 0)
+    return RXL_ERR_MISALIGNED;
+  const int cap = ring->cap;
+  const int nwrite = L < cap ? L : cap;          // only the last min(L, cap) rows survive
+  const int src_row0 = L - nwrite;
+  const int dst_row0 = (int)(((long long)ring->head + ring->len + src_row0) % cap);
+  int launches = 0;
+  const cudaError_t e = rxl::launch_mem_update(ring->data, ring->planes, cap, ring->D,
+                                               ring->plane_stride, es, src, src_plane_stride,
+                                               src_row0, nwrite, dst_row0,
+                                               (cudaStream_t)stream, &launches);
+  g_last_launches = launches;
+  if (e != cudaSuccess) return cuda_status(e);
+  const long long total = (long long)ring->len + L;
+  if (total > cap) {
+    ring->head = (int)(((long long)ring->head + total - cap) % cap);
+    ring->len = cap;
+  } else {
+    ring->len = (int)total;
+  }
+  return RXL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,315 @@
+"""Parity of rxl_attn_fwd / rxl_attn_bwd (called through the C ABI) with the
+float64 oracle on the same seeded inputs.
+
+* every element at sizes the oracle finishes in seconds (several tiles,
+  ragged tails, rotated and wrapping rings, empty memory);
+* the five configurations of the path at full size: cfg1 and cfg2 in full,
+  cfg3/cfg4 on sampled forward rows plus the whole backward of one head
+  (all batch rows), cfg5 as the 32-segment stream on its first and last layer
+  with sampled rows at fill, wrap and steady-state segments;
+* skew-sensitive closed-form probes (distance labels) on tile boundaries;
+* stop-gradient: the cache is never written by the backward.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import rxl_inputs as gen
+from tests._harness import AttnCall, assert_close, logical_kv, place_kv, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def make_inputs(B, H, L, cap, m, dtype, seed=0, tid0=900000, D_model=1024):
+    """Synthetic inputs with the distributions of the configurations:
+    Q, K, V ~ N(0,1)/sqrt(dh), u, v ~ N(0, 0.02^2), R sinusoid x W_R, dO ~ N(0,1)."""
+    dh, sd = 64, 0.125
+    n = lambda i, shape, std: gen.round_to(gen.normal(seed, tid0 + i, shape, std), dtype)
+    return dict(
+        q=n(1, (B, H, L, dh), sd), k_mem=n(2, (B, H, m, dh), sd), k_cur=n(3, (B, H, L, dh), sd),
+        v_mem=n(4, (B, H, m, dh), sd), v_cur=n(5, (B, H, L, dh), sd), u=n(6, (H, dh), 0.02),
+        vb=n(7, (H, dh), 0.02), do=n(8, (B, H, L, dh), 1.0),
+        r=gen.round_to(gen.rel_table(cap + L, D_model, H, dh, seed, tid0 + 9), dtype))
+
+
+def run_gpu(x, cap, m, head, dtype, bwd=True, scale=0.125):
+    k_phys = place_kv(x["k_mem"], x["k_cur"], cap, head, fill=7.0)   # junk in unused ring rows
+    v_phys = place_kv(x["v_mem"], x["v_cur"], cap, head, fill=-7.0)
+    c = AttnCall(x["q"], k_phys, v_phys, x["r"], x["u"], x["vb"], cap=cap, m=m, head=head,
+                 dtype=dtype, scale=scale).fwd()
+    if bwd:
+        c.alloc_bwd(x["do"]).bwd()
+    return c
+
+
+def logical(x):
+    return (np.concatenate([x["k_mem"], x["k_cur"]], 2), np.concatenate([x["v_mem"], x["v_cur"]], 2))
+
+
+def compare_full(x, c, cap, m, head, dtype, bwd=True, scale=0.125, tag=""):
+    import torch
+    torch.cuda.synchronize()
+    k, v = logical(x)
+    o, lse = oracle.fwd(x["q"], k, v, x["r"], x["u"], x["vb"], scale)
+    assert_close("O", to_host(c.o), o, dtype, tag)
+    assert_close("LSE", to_host(c.lse), lse, dtype, tag)
+    if not bwd:
+        return
+    g = oracle.bwd(x["q"], k, v, x["r"], x["u"], x["vb"], x["do"], scale)
+    L = x["q"].shape[2]
+    assert_close("dQ", to_host(c.dq), g["dq"], dtype, tag)
+    dk, dv = to_host(c.dk), to_host(c.dv)
+    assert_close("dK", logical_kv(dk, cap, head, m), g["dk"], dtype, tag)
+    assert_close("dV", logical_kv(dv, cap, head, m), g["dv"], dtype, tag)
+    unused = np.setdiff1d(np.arange(cap), (head + np.arange(m)) % cap if m else [])
+    assert np.all(dk[:, :, unused] == 0) and np.all(dv[:, :, unused] == 0), "ring rows without memory"
+    dr = to_host(c.dr)
+    assert_close("dR", dr[:, :m + L], g["dr"], dtype, tag)
+    assert np.all(dr[:, m + L:] == 0)
+    assert_close("du", to_host(c.du), g["du"], dtype, tag)
+    assert_close("dv", to_host(c.dvb), g["dvb"], dtype, tag)
+
+
+# ---------------------------------------------------- small full-oracle cases
+
+SMALL = [  # B, H, L, cap, m, head
+    (2, 2, 200, 300, 250, 123),   # several tiles, ragged, rotated ring that wraps
+    (1, 3, 129, 0, 0, 0),         # no memory at all: plain causal attention
+    (2, 1, 64, 1600, 1600, 1550), # long full ring that wraps mid-tile
+    (3, 2, 1, 5, 5, 2),           # one query row
+    (1, 2, 130, 128, 127, 0),     # tile edges +-1
+    (2, 2, 128, 256, 0, 0),       # memory capacity but still empty
+]
+
+
+@pytest.mark.parametrize("B,H,L,cap,m,head", SMALL)
+def test_small_bf16_full_parity(B, H, L, cap, m, head):
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=B * 1000 + L + m)
+    c = run_gpu(x, cap, m, head, "bf16")
+    compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head)))
+
+
+def test_small_f32_full_parity():
+    x = make_inputs(2, 2, 37, 50, 41, "f32", seed=3, D_model=64)
+    c = run_gpu(x, 50, 41, 17, "f32")
+    compare_full(x, c, 50, 41, 17, "f32")
+
+
+# ---------------------------------------------- configuration 1 (fp32, 4x12)
+
+def test_cfg1_f32_fwd_bwd_and_memory_update():
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    w = gen.CFG1
+    p, s, mem = gen.layer_params(w), gen.segment_inputs(w), gen.initial_memory(w)
+    x = dict(q=s["q"], k_mem=mem["k_mem"], k_cur=s["k_cur"], v_mem=mem["v_mem"], v_cur=s["v_cur"],
+             u=p["u"], vb=p["vb"], r=p["r"], do=s["do"])
+    c = run_gpu(x, w.M, w.M, 0, "f32", scale=w.scale)
+    compare_full(x, c, w.M, w.M, 0, "f32", scale=w.scale)
+    # one memory update: ring <- last 8 of [8 memory rows; 4 current rows]
+    ring = rxl.rxl_ring(c.k.data_ptr(), w.B * w.H, w.M, w.dh, (w.M + w.L) * w.dh, rxl.RXL_DTYPE_F32, 0, w.M)
+    rxl.rxl_mem_update(ring, c.k.data_ptr() + w.M * w.dh * 4, (w.M + w.L) * w.dh, w.L)
+    torch.cuda.synchronize()
+    want = oracle.tail_m(x["k_mem"], x["k_cur"], w.M)
+    got = c.k.cpu().numpy()[:, :, (ring.head + np.arange(ring.len)) % w.M]
+    assert (ring.head, ring.len) == (4, 8)
+    assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32))
+
+
+# -------------------------------- configuration 2 (4-segment stream, fwd+bwd)
+
+def test_cfg2_stream_fwd_bwd():
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    w = gen.CFG2
+    p = gen.layer_params(w)
+    cap, L = w.M, w.L
+    mem_k = np.zeros((w.B, w.H, 0, w.dh), np.float32)
+    mem_v = mem_k.copy()
+    head = 0
+    k_dev = v_dev = None
+    for seg in range(w.segments):
+        s = gen.segment_inputs(w, seg)
+        m = mem_k.shape[2]
+        assert m == min(cap, seg * L)
+        x = dict(q=s["q"], k_mem=mem_k, k_cur=s["k_cur"], v_mem=mem_v, v_cur=s["v_cur"],
+                 u=p["u"], vb=p["vb"], r=p["r"], do=s["do"])
+        c = run_gpu(x, cap, m, head, "bf16", scale=w.scale)
+        if k_dev is not None:   # device rings carried over from the previous segment
+            c.k[:, :, :cap] = k_dev[:, :, :cap]
+            c.v[:, :, :cap] = v_dev[:, :, :cap]
+            c.fwd().bwd()
+        compare_full(x, c, cap, m, head, "bf16", scale=w.scale, tag=f"segment {seg}")
+        rk = rxl.rxl_ring(c.k.data_ptr(), w.B * w.H, cap, w.dh, (cap + L) * w.dh, rxl.RXL_DTYPE_BF16, head, m)
+        rv = rxl.rxl_ring(c.v.data_ptr(), w.B * w.H, cap, w.dh, (cap + L) * w.dh, rxl.RXL_DTYPE_BF16, head, m)
+        rxl.rxl_mem_update(rk, c.k.data_ptr() + cap * w.dh * 2, (cap + L) * w.dh, L)
+        rxl.rxl_mem_update(rv, c.v.data_ptr() + cap * w.dh * 2, (cap + L) * w.dh, L)
+        torch.cuda.synchronize()
+        mem_k = oracle.tail_m(mem_k, s["k_cur"], cap)
+        mem_v = oracle.tail_m(mem_v, s["v_cur"], cap)
+        head = rk.head
+        k_dev, v_dev = c.k.clone(), c.v.clone()
+
+
+# ---------------------------------- configurations 3 and 4 (full size, sampled)
+
+def sample_rows(B, H, L, n, rng):
+    fixed = [0, 1, 63, 64, 127, 128, L - 1]
+    sel = set()
+    for b, h in [(0, 0), (B - 1, H - 1), (B // 2, H // 3)]:
+        for i in fixed:
+            if i < L:
+                sel.add((b, h, i))
+    while len(sel) < n:
+        sel.add((int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(L))))
+    return np.array(sorted(sel), dtype=np.int32)
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+def test_full_size_config(cfg):
+    import torch
+    w = gen.CONFIGS[cfg]
+    p = gen.layer_params(w)
+    s = gen.segment_inputs(w)
+    mem = gen.initial_memory(w)
+    x = dict(q=s["q"], k_mem=mem["k_mem"], k_cur=s["k_cur"], v_mem=mem["v_mem"], v_cur=s["v_cur"],
+             u=p["u"], vb=p["vb"], r=p["r"], do=s["do"])
+    cap = m = w.M
+    c = run_gpu(x, cap, m, 0, "bf16", scale=w.scale)
+    torch.cuda.synchronize()
+    k, v = logical(x)
+    rng = np.random.default_rng(cfg)
+    sel = sample_rows(w.B, w.H, w.L, 96, rng)
+    o_ref, lse_ref = oracle.fwd_rows(x["q"], k, v, x["r"], x["u"], x["vb"], w.scale, sel)
+    o, lse = to_host(c.o), to_host(c.lse)
+    assert_close("O(sampled)", o[sel[:, 0], sel[:, 1], sel[:, 2]], o_ref, "bf16")
+    assert_close("LSE(sampled)", lse[sel[:, 0], sel[:, 1], sel[:, 2]], lse_ref, "bf16")
+    # the whole backward of one head, all batch rows (dR/du/dv sum over b)
+    h = w.H // 2
+    hs = slice(h, h + 1)
+    g = oracle.bwd(x["q"][:, hs], k[:, hs], v[:, hs], x["r"][hs], x["u"][hs], x["vb"][hs],
+                   x["do"][:, hs], w.scale)
+    assert_close("dQ", to_host(c.dq)[:, hs], g["dq"], "bf16")
+    assert_close("dK", logical_kv(to_host(c.dk)[:, hs], cap, 0, m), g["dk"], "bf16")
+    assert_close("dV", logical_kv(to_host(c.dv)[:, hs], cap, 0, m), g["dv"], "bf16")
+    assert_close("dR", to_host(c.dr)[hs], g["dr"], "bf16")
+    assert_close("du", to_host(c.du)[hs], g["du"], "bf16")
+    assert_close("dv", to_host(c.dvb)[hs], g["dvb"], "bf16")
+
+
+# ------------------------- configuration 5 (16-layer evaluation stream, fwd)
+
+def test_cfg5_stream_first_and_last_layer():
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    w = gen.CFG5
+    cap, L, dh = w.M, w.L, w.dh
+    check_at = {0, 1, 11, 12, 13, 31}   # empty, partial, last partial, wrap, full, steady
+    rng = np.random.default_rng(55)
+    for layer in (0, w.layers - 1):
+        p = gen.layer_params(w, layer)
+        k = torch.zeros((w.B, w.H, cap + L, dh), device="cuda", dtype=torch.bfloat16)
+        v = torch.zeros_like(k)
+        r_dev = AttnCall(np.zeros((w.B, w.H, L, dh), np.float32), np.zeros((w.B, w.H, cap + L, dh), np.float32),
+                         np.zeros((w.B, w.H, cap + L, dh), np.float32), p["r"], p["u"], p["vb"],
+                         cap=cap, m=0, head=0, dtype="bf16", scale=w.scale)
+        rk = rxl.rxl_ring(k.data_ptr(), w.B * w.H, cap, dh, (cap + L) * dh, rxl.RXL_DTYPE_BF16, 0, 0)
+        rv = rxl.rxl_ring(v.data_ptr(), w.B * w.H, cap, dh, (cap + L) * dh, rxl.RXL_DTYPE_BF16, 0, 0)
+        mem_k = np.zeros((w.B, w.H, 0, dh), np.float32)
+        mem_v = mem_k.copy()
+        from tests._harness import to_dev
+        for seg in range(w.segments):
+            s = gen.segment_inputs(w, seg, layer)
+            k[:, :, cap:] = to_dev(s["k_cur"], "bf16")
+            v[:, :, cap:] = to_dev(s["v_cur"], "bf16")
+            q = to_dev(s["q"], "bf16")
+            desc = rxl.make_desc(w.B, w.H, L, cap, rk.len, rk.head, w.scale, rxl.RXL_DTYPE_BF16)
+            rxl.rxl_attn_fwd(desc, q, k, v, r_dev.r, r_dev.u, r_dev.vb, r_dev.o, r_dev.lse)
+            if seg in check_at:
+                torch.cuda.synchronize()
+                kl = np.concatenate([mem_k, s["k_cur"]], 2)
+                vl = np.concatenate([mem_v, s["v_cur"]], 2)
+                sel = sample_rows(w.B, w.H, L, 48, rng)
+                o_ref, lse_ref = oracle.fwd_rows(s["q"], kl, vl, p["r"], p["u"], p["vb"], w.scale, sel)
+                o, lse = to_host(r_dev.o), to_host(r_dev.lse)
+                tag = f"layer {layer} segment {seg} m={rk.len} head={rk.head}"
+                assert_close("O", o[sel[:, 0], sel[:, 1], sel[:, 2]], o_ref, "bf16", tag)
+                assert_close("LSE", lse[sel[:, 0], sel[:, 1], sel[:, 2]], lse_ref, "bf16", tag)
+            rxl.rxl_mem_update(rk, k.data_ptr() + cap * dh * 2, (cap + L) * dh, L)
+            rxl.rxl_mem_update(rv, v.data_ptr() + cap * dh * 2, (cap + L) * dh, L)
+            mem_k = oracle.tail_m(mem_k, s["k_cur"], cap)
+            mem_v = oracle.tail_m(mem_v, s["v_cur"], cap)
+        assert (rk.len, rk.head) == (cap, (32 * L - cap) % cap)
+
+
+# ------------------------------------------- skew-sensitive closed-form probes
+
+@pytest.mark.parametrize("L,cap,m,head", [(4, 8, 8, 0), (127, 129, 129, 5), (128, 128, 128, 0),
+                                           (129, 127, 127, 100), (128, 1600, 1600, 1550), (257, 0, 0, 0)])
+def test_distance_probe_on_gpu(L, cap, m, head):
+    """Q=K=u=0, v = alpha*(64 e0 + e1), R_d = (d // 64, d % 64, 0...): the
+    logits are s*alpha*(i-j), exact in bf16, so P is a truncated geometric
+    law over the distance i-j. V_j carries small labels of its logical
+    position p = j+m: (1, p % 8, (p // 8) % 8, p // 64). O_i is then the
+    expected label under that law and LSE_i a closed form; a key or a
+    distance off by one moves the expected labels by ~1."""
+    B, H, dh, s, alpha = 2, 2, 64, 0.125, -16.0   # s*alpha = -2
+    q = np.zeros((B, H, L, dh), np.float32)
+    n = m + L
+    kk = np.zeros((B, H, cap + L, dh), np.float32)
+    lab = np.arange(n)
+    feats = [np.ones(n), lab % 8, (lab // 8) % 8, lab // 64]
+    vlog = np.zeros((B, H, n, dh), np.float32)
+    for ch, f in enumerate(feats):
+        vlog[..., ch] = f
+    vv = place_kv(vlog[:, :, :m], vlog[:, :, m:], cap, head, fill=1000.0)
+    r = np.zeros((H, cap + L, dh), np.float32)
+    d = np.arange(cap + L)
+    r[:, :, 0], r[:, :, 1] = d // 64, d % 64
+    vb = np.zeros((H, dh), np.float32)
+    vb[:, 0], vb[:, 1] = 64 * alpha, alpha
+    c = AttnCall(q, kk, vv, r, np.zeros((H, dh), np.float32), vb, cap=cap, m=m, head=head,
+                 dtype="bf16", scale=s).fwd()
+    import torch
+    torch.cuda.synchronize()
+    o, lse = to_host(c.o), to_host(c.lse)
+    rho = math.exp(s * alpha)
+    for i in range(L):
+        w = rho ** np.arange(i + m + 1)           # weight of distance d = 0..i+m
+        tot = w.sum()
+        pos = i + m - np.arange(i + m + 1)        # logical position of the key at distance d
+        assert np.abs(lse[:, :, i] - math.log(tot)).max() < 2e-3, i
+        for ch, f in enumerate(feats):
+            want = (w * f[pos]).sum() / tot
+            err = np.abs(o[:, :, i, ch] - want).max()
+            assert err <= 0.01 + 2 ** -8 * abs(want), (i, ch, float(err), want)
+
+
+def test_ring_rotation_gives_same_outputs():
+    """Translation invariance on the device: the same logical memory stored
+    at another ring head gives the same O and LSE."""
+    B, H, L, cap, m = 2, 2, 100, 300, 260
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=77)
+    outs = []
+    for head in (0, 41, 299):
+        c = run_gpu(x, cap, m, head, "bf16", bwd=False)
+        outs.append((to_host(c.o), to_host(c.lse)))
+    for o, l in outs[1:]:
+        np.testing.assert_allclose(o, outs[0][0], rtol=0, atol=2e-3)
+        np.testing.assert_allclose(l, outs[0][1], rtol=0, atol=1e-5)
+
+
+def test_backward_never_writes_the_cache():
+    import torch
+    B, H, L, cap, m = 2, 2, 96, 160, 150
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=13)
+    c = run_gpu(x, cap, m, 37, "bf16", bwd=False)
+    k0, v0 = c.k.clone(), c.v.clone()
+    c.alloc_bwd(x["do"]).bwd()
+    torch.cuda.synchronize()
+    assert torch.equal(c.k, k0) and torch.equal(c.v, v0)
+    mem_rows = (37 + np.arange(m)) % cap
+    dk = to_host(c.dk)[:, :, mem_rows]
+    assert np.all(np.abs(dk).sum(-1) > 0), "memory rows must receive K gradients"
