@@ -1,0 +1,453 @@
+// Fused relative-position memory attention forward on sm_103a tensor cores.
+//
+// Math (Transformer-XL page, "Relative Positional Encoding", "Dimension
+// Walkthrough", "Causal Mask With Memory"):
+//   A_ij = (q_i+u).k_j + (q_i+v).r_{i-j},  O_i = softmax_j(scale*A_ij | allow) V
+// The L x (m+L) score matrix never leaves the SM.
+//
+// One CTA owns (b, h, 128 query rows). It walks the visible keys in tiles of
+// 128 physically contiguous K/V rows (the ring's two runs and the current
+// block; a tile never straddles the ring's wrap). For every key tile:
+//   * TMA loads K, V (128 x 64) and the band of 256 R rows the tile needs:
+//     distances d0 .. d0+255 with d0 = i0 - j0 - 127 (rows outside R read as
+//     zero and are masked anyway);
+//   * tcgen05: S = (Q+u) K^T   -> TMEM cols [0,128)     (M=128, N=128)
+//              G = (Q+v) Rb^T  -> TMEM cols [128,384)   (M=128, N=256)
+//     so G[ii][t] = (q_ii+v).r_{d0+t}; the relative shift the pages do by
+//     pad/reshape/slice is an index skew here: S_p[ii][jj] = G[ii][ii-jj+127];
+//   * the 4 softmax warps (one thread per query row, TMEM lane = row) load S
+//     and their skewed G window, mask, run the fp32 online softmax (exp2),
+//     write P (bf16) to shared memory and rescale O in TMEM;
+//   * tcgen05: O += P V -> TMEM cols [384,448)          (M=128, N=64)
+// Warp 4 is the producer: one thread issues the TMA loads (two stages) and
+// every MMA; tcgen05.commit signals completion through mbarriers.
+//
+// The skew: thread (warp w, lane l) owns row ii = 32w+l and needs G columns
+// ii..ii+127. Per chunk of 32 keys it loads a warp-uniform 64-column window
+// and shifts it by l with a 5-stage predicated barrel shift.
+#include <math.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "internal.cuh"
+#include "sm103.cuh"
+
+namespace rxl {
+namespace {
+
+using namespace sm103;
+
+constexpr int BQ = 128, BK = 128, DH = 64, NB = 256;
+constexpr int kThreads = 160;                  // 4 softmax warps + 1 producer warp
+constexpr uint32_t SM_QU = 0;                  // [128][64] bf16, sw128
+constexpr uint32_t SM_QV = 16384;
+constexpr uint32_t SM_K = 32768;               // 2 stages x 16 KB
+constexpr uint32_t SM_V = 65536;               // 2 stages x 16 KB
+constexpr uint32_t SM_R = 98304;               // 2 stages x 32 KB
+constexpr uint32_t SM_P = 163840;              // 2 x [128][64] bf16 (keys 0-63, 64-127)
+constexpr uint32_t SM_BAR = 196608;            // mbarriers, TMEM slot, abort flag
+constexpr uint32_t SMEM_BYTES = SM_BAR + 128 + 1024;  // + alignment slack
+constexpr uint32_t STAGE_TX = 16384 + 16384 + 32768;
+constexpr uint32_t TM_S = 0, TM_G = 128, TM_O = 384, TM_COLS = 512;
+
+constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+constexpr uint32_t IDESC_G = idesc_bf16(128, 256, false, false);
+constexpr uint32_t IDESC_O = idesc_bf16(128, 64, false, true);   // V is MN-major (d contiguous)
+
+__device__ int g_fwd_error;
+
+struct Params {
+  int B, H, L, cap, m, head, nq;
+  float scale_log2;  // scale * log2(e)
+  const __nv_bfloat16 *q, *u, *vb;
+  __nv_bfloat16 *o;
+  float *lse;
+};
+
+struct Tile {
+  int phys0;   // first physical K/V row
+  int jlog0;   // logical key position of that row (-m .. L-1)
+  int nvalid;  // rows of the tile that are keys of this run
+};
+
+// Key tiles of query tile i0: ring run A (head .. cap), ring run B (0 ..),
+// then current rows 0 .. min(i0+BQ, L).
+struct TileList {
+  int lenA, lenB, lenC, nA, nB, nC;
+  __device__ TileList(const Params &p, int i0) {
+    lenA = min(p.m, p.cap - p.head);
+    lenB = p.m - lenA;
+    lenC = min(i0 + BQ, p.L);
+    nA = (lenA + BK - 1) / BK;
+    nB = (lenB + BK - 1) / BK;
+    nC = (lenC + BK - 1) / BK;
+  }
+  __device__ int count() const { return nA + nB + nC; }
+  __device__ Tile get(const Params &p, int t) const {
+    Tile x;
+    if (t < nA) {
+      x.phys0 = p.head + t * BK;
+      x.jlog0 = -p.m + t * BK;
+      x.nvalid = min(BK, lenA - t * BK);
+    } else if (t < nA + nB) {
+      const int u = t - nA;
+      x.phys0 = u * BK;
+      x.jlog0 = -p.m + lenA + u * BK;
+      x.nvalid = min(BK, lenB - u * BK);
+    } else {
+      const int u = t - nA - nB;
+      x.phys0 = p.cap + u * BK;
+      x.jlog0 = u * BK;
+      x.nvalid = min(BK, lenC - u * BK);
+    }
+    return x;
+  }
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_r, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = p.nq - 1 - (int)(blockIdx.x % p.nq);  // long query tiles first
+  const int bh = (int)(blockIdx.x / p.nq);
+  const int h = bh % p.H;
+  const int i0 = qt * BQ;
+
+  const uint32_t bar_full0 = sbase + SM_BAR, bar_full1 = bar_full0 + 8;
+  const uint32_t bar_sg = bar_full0 + 16, bar_p = bar_full0 + 24, bar_pv = bar_full0 + 32;
+  const uint32_t bar_drain = bar_full0 + 40;
+  uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 48);
+  volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 56);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_full0, 1);
+    mbar_init(bar_full1, 1);
+    mbar_init(bar_sg, 1);
+    mbar_init(bar_p, 4 * 32);
+    mbar_init(bar_pv, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(tmem_slot), TM_COLS);
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_r);
+    }
+  } else {
+    // (Q+u) and (Q+v) in bf16, 128-byte swizzled K-major tiles.
+    const int ii = warp * 32 + lane;
+    const int i = i0 + ii;
+    const uint4 *qrow = (const uint4 *)(p.q + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
+    const uint4 *urow = (const uint4 *)(p.u + (size_t)h * DH);
+    const uint4 *vrow = (const uint4 *)(p.vb + (size_t)h * DH);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 qv4 = i < p.L ? qrow[c] : make_uint4(0, 0, 0, 0);
+      const uint4 u4 = urow[c], v4 = vrow[c];
+      const __nv_bfloat162 *q2 = (const __nv_bfloat162 *)&qv4;
+      const __nv_bfloat162 *u2 = (const __nv_bfloat162 *)&u4;
+      const __nv_bfloat162 *v2 = (const __nv_bfloat162 *)&v4;
+      uint32_t a[4], b[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 qf = __bfloat1622float2(q2[e]);
+        const float2 uf = __bfloat1622float2(u2[e]);
+        const float2 vf = __bfloat1622float2(v2[e]);
+        a[e] = pack_bf16(qf.x + uf.x, qf.y + uf.y);
+        b[e] = pack_bf16(qf.x + vf.x, qf.y + vf.y);
+      }
+      st_shared_v4(sbase + SM_QU + sw128_offset(ii, c), a[0], a[1], a[2], a[3]);
+      st_shared_v4(sbase + SM_QV + sw128_offset(ii, c), b[0], b[1], b[2], b[3]);
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const TileList tl(p, i0);
+  const int T = tl.count();
+
+  if (warp == 4) {
+    // ------------------------------------------------ producer / MMA issuer
+    if (lane == 0) {
+      bool pending[2] = {false, false};
+      int nissued[2] = {0, 0};
+      auto issue_tma = [&](int t) {
+        const int s = t & 1;
+        const Tile x = tl.get(p, t);
+        const uint32_t bar = s ? bar_full1 : bar_full0;
+        mbar_expect_tx(bar, STAGE_TX);
+        tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, bh, bar);
+        tma_load_3d(sbase + SM_V + s * 16384, &tm_v, 0, x.phys0, bh, bar);
+        tma_load_3d(sbase + SM_R + s * 32768, &tm_r, 0, i0 - x.jlog0 - (BK - 1), h, bar);
+        pending[s] = true;
+        ++nissued[s];
+      };
+      auto issue_sg = [&](int t) {
+        const int s = t & 1;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t a = sdesc_sw128(sbase + SM_QU + k * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(sbase + SM_K + s * 16384 + k * 32, 16, 1024);
+          mma_bf16(tmem + TM_S, a, b, IDESC_S, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t a = sdesc_sw128(sbase + SM_QV + k * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(sbase + SM_R + s * 32768 + k * 32, 16, 1024);
+          mma_bf16(tmem + TM_G, a, b, IDESC_G, k > 0);
+        }
+        mma_commit(bar_sg);
+      };
+      bool ok = true;
+      if (T > 0) issue_tma(0);
+      if (T > 1) issue_tma(1);
+      if (T > 0) {
+        ok = mbar_wait(bar_full0, 0, abort_flag);
+        pending[0] = false;
+        if (ok) issue_sg(0);
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        if (!(ok = mbar_wait(bar_p, t & 1, abort_flag))) break;
+        tc_fence_after();
+        const int s = t & 1;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = sdesc_sw128(sbase + SM_P + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(sbase + SM_V + s * 16384 + k * 2048, 16, 1024);
+          mma_bf16(tmem + TM_O, a, b, IDESC_O, (t > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(bar_pv);
+        if (t + 1 < T) {
+          const int s1 = (t + 1) & 1;
+          if (!(ok = mbar_wait(s1 ? bar_full1 : bar_full0, ((t + 1) >> 1) & 1, abort_flag))) break;
+          pending[s1] = false;
+          issue_sg(t + 1);
+        }
+        if (t + 2 < T) {
+          if (!(ok = mbar_wait(bar_pv, t & 1, abort_flag))) break;
+          issue_tma(t + 2);
+        }
+      }
+      if (!ok) {
+        // wind down: let in-flight copies and MMAs land before TMEM and
+        // shared memory are released
+        volatile int no_abort = 0;
+        for (int s = 0; s < 2; ++s)
+          if (pending[s]) mbar_wait(s ? bar_full1 : bar_full0, (nissued[s] - 1) & 1, &no_abort);
+        mma_commit(bar_drain);
+        mbar_wait(bar_drain, 0, &no_abort);
+        atomicExch(&g_fwd_error, 1);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------- softmax warps
+    const int ii = warp * 32 + lane;
+    const int i = i0 + ii;
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int s = t & 1;
+      ok = mbar_wait(bar_sg, t & 1, abort_flag) &&
+           mbar_wait(s ? bar_full1 : bar_full0, (t >> 1) & 1, abort_flag);
+      // tcgen05.ld/st below are warp-collective: keep every decision warp-uniform
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      tc_fence_after();
+      const Tile x = tl.get(p, t);
+      float y[BK];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32], w0[32], w1[32];
+        tmem_ld32(trow + TM_S + 32 * c, sr);
+        const uint32_t gcol = TM_G + 32 * warp + 96 - 32 * c;
+        tmem_ld32(trow + gcol, w0);
+        tmem_ld32(trow + gcol + 32, w1);
+        tmem_wait_ld();
+        float win[64];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          win[e] = __uint_as_float(w0[e]);
+          win[32 + e] = __uint_as_float(w1[e]);
+        }
+        // win[x] <- win[x + lane]: shifts by 16, 8, 4, 2, 1 under the lane's bits
+#pragma unroll
+        for (int b = 4; b >= 0; --b) {
+          const int sh = 1 << b;
+          const bool take = (lane >> b) & 1;
+          // fixed trip count so the loop unrolls and win[] stays in registers
+#pragma unroll
+          for (int e = 0; e < 63; ++e)
+            if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int jj = 32 * c + k;
+          const float a = __uint_as_float(sr[k]) + win[31 - k];
+          const bool valid = jj < x.nvalid && x.jlog0 + jj <= i;
+          y[jj] = valid ? a * p.scale_log2 : -INFINITY;
+        }
+      }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < BK; ++k) mt = fmaxf(mt, y[k]);
+      const float m_new = fmaxf(m_run, mt);
+      const float ref = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2(m_run - ref);  // 0 on the first visible tile
+      float sum = 0.f;
+      uint32_t pk[BK / 2];
+#pragma unroll
+      for (int k = 0; k < BK; k += 2) {
+        const float p0 = ex2(y[k] - ref), p1 = ex2(y[k + 1] - ref);
+        sum += p0 + p1;
+        pk[k / 2] = pack_bf16(p0, p1);
+      }
+      l_run = l_run * alpha + sum;
+      m_run = m_new;
+      // P -> shared memory (the previous P.V finished: bar_sg of this tile
+      // was committed after it)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t addr = sbase + SM_P + (c >> 3) * 16384 + sw128_offset(ii, c & 7);
+        st_shared_v4(addr, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+      // rows of V past the run hold another run's (or junk) data: zero them
+      // so that 0 * junk cannot leak into O
+      if (ii >= x.nvalid) {
+        const uint32_t vrow = sbase + SM_V + s * 16384 + ii * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_shared_v4(vrow + 16 * c, 0, 0, 0, 0);
+      }
+      if (__any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t o[32];
+          tmem_ld32(trow + TM_O + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(trow + TM_O + 32 * c, o);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+    // epilogue: O / l, LSE (natural log)
+    if (ok && T > 0) ok = mbar_wait(bar_pv, (T - 1) & 1, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      uint4 *orow = (uint4 *)(p.o + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        tmem_ld32(trow + TM_O + 32 * c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+          v.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+          v.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+          v.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+          if (i < p.L) orow[4 * c + e] = v;
+        }
+      }
+      if (i < p.L) p.lse[(size_t)bh * p.L + i] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+    } else {
+      atomicExch(&g_fwd_error, 1);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) tmem_dealloc(tmem, TM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  });
+  return fn;
+}
+
+// [planes][rows][64] bf16 tensor, box of `box_rows` rows, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, int planes, int rows, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)rows * 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, const void *v,
+                          const void *r, const void *u, const void *vb, void *o, float *lse,
+                          cudaStream_t st, int *launches) {
+  CUtensorMap tk, tv, tr;
+  if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
+      !make_map(&tr, r, s.H, s.kv_rows, NB))
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(rxl_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  Params p;
+  p.B = s.B; p.H = s.H; p.L = s.L; p.cap = s.cap; p.m = s.m; p.head = s.head;
+  p.nq = (s.L + BQ - 1) / BQ;
+  p.scale_log2 = s.scale * 1.4426950408889634f;
+  p.q = (const __nv_bfloat16 *)q; p.u = (const __nv_bfloat16 *)u; p.vb = (const __nv_bfloat16 *)vb;
+  p.o = (__nv_bfloat16 *)o; p.lse = lse;
+  const unsigned grid = (unsigned)(s.B * s.H * p.nq);
+  rxl_fwd_tc_kernel<<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t tc_fwd_read_error(int *flag) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_fwd_error, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fwd_error, &zero, sizeof(int));
+  return e;
+}
+
+}  // namespace rxl

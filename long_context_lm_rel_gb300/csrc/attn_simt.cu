@@ -96,14 +96,39 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(
   if (lane == 0) lse[row] = mx + logf(l);
 }
 
-// D_i = dO_i . O_i
+// D_i = dO_i . O_i with O_i recomputed in fp32: D_i = sum_j P_ij (dO_i . V_j).
+// The stored O is rounded to the input type; taking D from it would put that
+// rounding error into every dS_ij of the row.
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) simt_bwd_d_kernel(
-    long long nrows, const T *__restrict__ o, const T *__restrict__ dout, float *__restrict__ D) {
+    AttnShape s, const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+    const T *__restrict__ r, const T *__restrict__ u, const T *__restrict__ vb,
+    const float *__restrict__ lse, const T *__restrict__ dout, float *__restrict__ D) {
   const long long row = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= nrows) return;
-  const float d = warp_sum(dot2(ld2(o + row * kDh + 2 * lane), ld2(dout + row * kDh + 2 * lane)));
+  if (row >= (long long)s.B * s.H * s.L) return;
+  const int i = (int)(row % s.L);
+  const long long bh = row / s.L;
+  const int h = (int)(bh % s.H);
+  const float2 qq = ld2(q + row * kDh + 2 * lane);
+  const float2 uu = ld2(u + h * kDh + 2 * lane), vv = ld2(vb + h * kDh + 2 * lane);
+  const float2 qu = make_float2(qq.x + uu.x, qq.y + uu.y);
+  const float2 qv = make_float2(qq.x + vv.x, qq.y + vv.y);
+  const float2 dO = ld2(dout + row * kDh + 2 * lane);
+  const float lse_i = lse[row];
+  const T *kb = k + bh * s.kv_rows * kDh, *vbase = v + bh * s.kv_rows * kDh;
+  const T *rh = r + (long long)h * s.kv_rows * kDh;
+  float2 acc = make_float2(0.f, 0.f);
+  for (int j = -s.m; j <= i; ++j) {
+    const long long pr = phys_row(s, j);
+    const float a = warp_sum(dot2(qu, ld2(kb + pr * kDh + 2 * lane)) +
+                             dot2(qv, ld2(rh + (long long)(i - j) * kDh + 2 * lane)));
+    const float p = expf(a * s.scale - lse_i);
+    const float2 vj = ld2(vbase + pr * kDh + 2 * lane);
+    acc.x += p * vj.x;
+    acc.y += p * vj.y;
+  }
+  const float d = warp_sum(acc.x * dO.x + acc.y * dO.y);
   if (lane == 0) D[row] = d;
 }
 
@@ -280,7 +305,7 @@ cudaError_t bwd_impl(const AttnShape &s, const void *q, const void *k, const voi
   const long long rows = (long long)s.B * s.H * s.L;
   const T *Q = (const T *)q, *K = (const T *)k, *V = (const T *)v, *R = (const T *)r;
   const T *U = (const T *)u, *VB = (const T *)vb, *DO = (const T *)dout;
-  simt_bwd_d_kernel<T><<<blocks_for(rows), kWarps * 32, 0, st>>>(rows, (const T *)o, DO, D);
+  simt_bwd_d_kernel<T><<<blocks_for(rows), kWarps * 32, 0, st>>>(s, Q, K, V, R, U, VB, lse, DO, D);
   simt_bwd_dq_kernel<T><<<blocks_for(rows), kWarps * 32, 0, st>>>(s, Q, K, V, R, U, VB, lse, DO,
                                                                  D, (T *)dq, dqu, dqv);
   simt_bwd_dkv_kernel<T><<<blocks_for((long long)s.B * s.H * s.kv_rows), kWarps * 32, 0, st>>>(

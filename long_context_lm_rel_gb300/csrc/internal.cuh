@@ -43,4 +43,11 @@ cudaError_t launch_simt_bwd(const AttnShape &s, rxl_dtype dt, const void *q, con
                             void *dk, void *dv, float *dr, float *du, float *dvb, void *ws,
                             cudaStream_t st, int *launches);
 
+// sm_103a tensor-core forward (bf16).
+cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, const void *v,
+                          const void *r, const void *u, const void *vb, void *o, float *lse,
+                          cudaStream_t st, int *launches);
+// Reads and clears the forward kernel's wait-timeout flag (synchronous).
+cudaError_t tc_fwd_read_error(int *flag);
+
 }  // namespace rxl

@@ -71,6 +71,12 @@ int rxl_last_cuda_error(void) { return g_last_cuda_error; }
 
 int rxl_last_launch_count(void) { return g_last_launches; }
 
+int rxl_device_error_flags(void) {
+  int fwd = 0;
+  if (rxl::tc_fwd_read_error(&fwd) != cudaSuccess) return -1;
+  return fwd ? 1 : 0;
+}
+
 rxl_status rxl_attn_fwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
                         const void *r, const void *u, const void *vbias, void *o, float *lse,
                         rxl_stream_t stream) {
@@ -79,8 +85,11 @@ rxl_status rxl_attn_fwd(const rxl_attn_desc *desc, const void *q, const void *k,
   if (st != RXL_OK) return st;
   if ((st = check_ptrs({q, k, v, r, u, vbias, o, lse})) != RXL_OK) return st;
   int launches = 0;
-  const cudaError_t e = rxl::launch_simt_fwd(s, desc->dtype, q, k, v, r, u, vbias, o, lse,
-                                             (cudaStream_t)stream, &launches);
+  const cudaError_t e =
+      desc->dtype == RXL_DTYPE_BF16
+          ? rxl::launch_tc_fwd(s, q, k, v, r, u, vbias, o, lse, (cudaStream_t)stream, &launches)
+          : rxl::launch_simt_fwd(s, desc->dtype, q, k, v, r, u, vbias, o, lse,
+                                 (cudaStream_t)stream, &launches);
   g_last_launches = launches;
   return cuda_status(e);
 }
