@@ -168,8 +168,8 @@ int rxl_last_launch_count(void);
  * bounded (about two seconds); a kernel that gives up records it in a device
  * word instead of hanging, drains its in-flight copies, frees its tensor
  * memory and exits with its outputs undefined. This call synchronises the
- * current device, returns the recorded bits (bit 0: forward kernel) and
- * clears them; -1 if the device could not be read.
+ * current device, returns the recorded bits (bit 0: forward kernel, bit 1:
+ * backward kernels) and clears them; -1 if the device could not be read.
  */
 int rxl_device_error_flags(void);
 

@@ -63,7 +63,14 @@ struct Params {
   const __nv_bfloat16 *q, *u, *vb;
   __nv_bfloat16 *o;
   float *lse;
+  // backward preparation (kPrep): dO in, D = dO.O (fp32 O) and the bf16
+  // (Q+u), (Q+v) rows out
+  const __nv_bfloat16 *dout;
+  float *delta;
+  __nv_bfloat16 *qu_out, *qv_out;
 };
+
+constexpr int kFwd = 0, kPrep = 1;
 
 struct Tile {
   int phys0;   // first physical K/V row
@@ -109,6 +116,7 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_r, const Params p) {
@@ -169,6 +177,11 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       }
       st_shared_v4(sbase + SM_QU + sw128_offset(ii, c), a[0], a[1], a[2], a[3]);
       st_shared_v4(sbase + SM_QV + sw128_offset(ii, c), b[0], b[1], b[2], b[3]);
+      if (MODE == kPrep && i < p.L) {
+        const size_t off = ((size_t)bh * p.L + i) * DH;
+        ((uint4 *)(p.qu_out + off))[c] = make_uint4(a[0], a[1], a[2], a[3]);
+        ((uint4 *)(p.qv_out + off))[c] = make_uint4(b[0], b[1], b[2], b[3]);
+      }
     }
     fence_proxy_async_smem();
   }
@@ -351,7 +364,30 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // epilogue: O / l, LSE (natural log)
     if (ok && T > 0) ok = mbar_wait(bar_pv, (T - 1) & 1, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    if (ok && MODE == kPrep) {
+      // D_i = dO_i . O_i with O_i still in fp32
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      const uint4 *drow = (const uint4 *)(p.dout + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        tmem_ld32(trow + TM_O + 32 * c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint4 d4 = drow[4 * c + e];
+          const __nv_bfloat162 *d2 = (const __nv_bfloat162 *)&d4;
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const float2 df = __bfloat1622float2(d2[f]);
+            acc += __uint_as_float(o[8 * e + 2 * f]) * df.x + __uint_as_float(o[8 * e + 2 * f + 1]) * df.y;
+          }
+        }
+      }
+      if (i < p.L) p.delta[(size_t)bh * p.L + i] = acc * inv;
+    } else if (ok) {
       tc_fence_after();
       const float inv = 1.f / l_run;
       uint4 *orow = (uint4 *)(p.o + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
@@ -415,11 +451,11 @@ bool make_map(CUtensorMap *m, const void *base, int planes, int rows, int box_ro
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, const void *v,
-                          const void *r, const void *u, const void *vb, void *o, float *lse,
-                          cudaStream_t st, int *launches) {
+template <int MODE>
+cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const void *v,
+                        const void *r, const void *u, const void *vb, void *o, float *lse,
+                        const void *dout, float *delta, void *qu_out, void *qv_out,
+                        cudaStream_t st, int *launches) {
   CUtensorMap tk, tv, tr;
   if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
       !make_map(&tr, r, s.H, s.kv_rows, NB))
@@ -427,20 +463,39 @@ cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, cons
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(rxl_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(rxl_fwd_tc_kernel<MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   Params p;
+  p.dout = (const __nv_bfloat16 *)dout; p.delta = delta;
+  p.qu_out = (__nv_bfloat16 *)qu_out; p.qv_out = (__nv_bfloat16 *)qv_out;
   p.B = s.B; p.H = s.H; p.L = s.L; p.cap = s.cap; p.m = s.m; p.head = s.head;
   p.nq = (s.L + BQ - 1) / BQ;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.q = (const __nv_bfloat16 *)q; p.u = (const __nv_bfloat16 *)u; p.vb = (const __nv_bfloat16 *)vb;
   p.o = (__nv_bfloat16 *)o; p.lse = lse;
   const unsigned grid = (unsigned)(s.B * s.H * p.nq);
-  rxl_fwd_tc_kernel<<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p);
+  rxl_fwd_tc_kernel<MODE><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p);
   ++*launches;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, const void *v,
+                          const void *r, const void *u, const void *vb, void *o, float *lse,
+                          cudaStream_t st, int *launches) {
+  return launch_mode<kFwd>(s, q, k, v, r, u, vb, o, lse, nullptr, nullptr, nullptr, nullptr, st,
+                           launches);
+}
+
+cudaError_t launch_tc_bwd_prep(const AttnShape &s, const void *q, const void *k, const void *v,
+                               const void *r, const void *u, const void *vb, const void *dout,
+                               float *delta, void *qu_out, void *qv_out, cudaStream_t st,
+                               int *launches) {
+  return launch_mode<kPrep>(s, q, k, v, r, u, vb, nullptr, nullptr, dout, delta, qu_out, qv_out,
+                            st, launches);
 }
 
 cudaError_t tc_fwd_read_error(int *flag) {

@@ -50,4 +50,19 @@ cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, cons
 // Reads and clears the forward kernel's wait-timeout flag (synchronous).
 cudaError_t tc_fwd_read_error(int *flag);
 
+// Forward kernel in backward-preparation mode: D = dO.O (fp32 O) and the
+// bf16 (Q+u), (Q+v) rows.
+cudaError_t launch_tc_bwd_prep(const AttnShape &s, const void *q, const void *k, const void *v,
+                               const void *r, const void *u, const void *vb, const void *dout,
+                               float *delta, void *qu_out, void *qv_out, cudaStream_t st,
+                               int *launches);
+
+// sm_103a tensor-core backward (bf16).
+BwdWorkspace tc_bwd_workspace(const AttnShape &s);
+cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, const void *v,
+                          const void *r, const void *u, const void *vb, const float *lse,
+                          const void *dout, void *dq, void *dk, void *dv, float *dr, float *du,
+                          float *dvb, void *ws, cudaStream_t st, int *launches);
+cudaError_t tc_bwd_read_error(int *flag);
+
 }  // namespace rxl

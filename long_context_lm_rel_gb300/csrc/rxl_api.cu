@@ -72,9 +72,10 @@ int rxl_last_cuda_error(void) { return g_last_cuda_error; }
 int rxl_last_launch_count(void) { return g_last_launches; }
 
 int rxl_device_error_flags(void) {
-  int fwd = 0;
-  if (rxl::tc_fwd_read_error(&fwd) != cudaSuccess) return -1;
-  return fwd ? 1 : 0;
+  int fwd = 0, bwd = 0;
+  if (rxl::tc_fwd_read_error(&fwd) != cudaSuccess || rxl::tc_bwd_read_error(&bwd) != cudaSuccess)
+    return -1;
+  return (fwd ? 1 : 0) | (bwd ? 2 : 0);
 }
 
 rxl_status rxl_attn_fwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
@@ -97,7 +98,8 @@ rxl_status rxl_attn_fwd(const rxl_attn_desc *desc, const void *q, const void *k,
 size_t rxl_attn_bwd_workspace_bytes(const rxl_attn_desc *desc) {
   rxl::AttnShape s;
   if (check_desc(desc, &s) != RXL_OK) return 0;
-  return rxl::simt_bwd_workspace(s).total;
+  return desc->dtype == RXL_DTYPE_BF16 ? rxl::tc_bwd_workspace(s).total
+                                       : rxl::simt_bwd_workspace(s).total;
 }
 
 rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
@@ -111,11 +113,15 @@ rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k,
   if ((st = check_ptrs({q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr, du, dvbias,
                         workspace})) != RXL_OK)
     return st;
-  if (workspace_bytes < rxl::simt_bwd_workspace(s).total) return RXL_ERR_WORKSPACE_TOO_SMALL;
+  const bool tc = desc->dtype == RXL_DTYPE_BF16;
+  if (workspace_bytes < (tc ? rxl::tc_bwd_workspace(s).total : rxl::simt_bwd_workspace(s).total))
+    return RXL_ERR_WORKSPACE_TOO_SMALL;
   int launches = 0;
   const cudaError_t e =
-      rxl::launch_simt_bwd(s, desc->dtype, q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr,
-                           du, dvbias, workspace, (cudaStream_t)stream, &launches);
+      tc ? rxl::launch_tc_bwd(s, q, k, v, r, u, vbias, lse, dout, dq, dk, dv, dr, du, dvbias,
+                              workspace, (cudaStream_t)stream, &launches)
+         : rxl::launch_simt_bwd(s, desc->dtype, q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr,
+                                du, dvbias, workspace, (cudaStream_t)stream, &launches);
   g_last_launches = launches;
   return cuda_status(e);
 }

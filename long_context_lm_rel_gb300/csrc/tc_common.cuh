@@ -1,0 +1,115 @@
+// Shared pieces of the sm_103a attention kernels: key-tile enumeration over
+// the memory ring, the skewed position-score read-out and small TMEM helpers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "sm103.cuh"
+
+namespace rxl {
+namespace tc {
+
+using namespace sm103;
+
+constexpr int BQ = 128, BK = 128, DH = 64, NB = 256;
+
+// A run of 128 physically contiguous K/V rows.
+struct KeyTile {
+  int phys0;   // first physical K/V row
+  int jlog0;   // logical key position of that row (-m .. L-1)
+  int nvalid;  // rows of the tile that belong to this run
+};
+
+// Key tiles over ring run A (head .. cap), ring run B (0 .. ), then the
+// current rows 0 .. lenC. A tile never straddles the ring's wrap, so its
+// rows are consecutive logical keys and one R band serves the whole tile.
+struct KeyTiles {
+  int m, cap, head, lenA, lenB, lenC, nA, nB, nC;
+  __device__ KeyTiles(int m_, int cap_, int head_, int lenC_) {
+    m = m_; cap = cap_; head = head_;
+    lenA = min(m, cap - head);
+    lenB = m - lenA;
+    lenC = lenC_;
+    nA = (lenA + BK - 1) / BK;
+    nB = (lenB + BK - 1) / BK;
+    nC = (lenC + BK - 1) / BK;
+  }
+  __device__ int count() const { return nA + nB + nC; }
+  __device__ KeyTile get(int t) const {
+    KeyTile x;
+    if (t < nA) {
+      x.phys0 = head + t * BK;
+      x.jlog0 = -m + t * BK;
+      x.nvalid = min(BK, lenA - t * BK);
+    } else if (t < nA + nB) {
+      const int u = t - nA;
+      x.phys0 = u * BK;
+      x.jlog0 = -m + lenA + u * BK;
+      x.nvalid = min(BK, lenB - u * BK);
+    } else {
+      const int u = t - nA - nB;
+      x.phys0 = cap + u * BK;
+      x.jlog0 = u * BK;
+      x.nvalid = min(BK, lenC - u * BK);
+    }
+    return x;
+  }
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+// Scaled logits (log2 domain) of one 128x128 tile for the calling thread's
+// query row ii = 32*warp + lane, key jj = 0..127:
+//   y[jj] = (S[ii][jj] + G[ii][ii - jj + 127]) * scale_log2, -inf if masked.
+// S sits at TMEM columns s_col.., the 256-column band G at g_col.. of the
+// warp's lane quadrant `trow`. Warp-collective (TMEM loads).
+__device__ __forceinline__ void tile_logits(uint32_t trow, uint32_t s_col, uint32_t g_col,
+                                            int warp, int lane, int i, const KeyTile &x,
+                                            float scale_log2, float (&y)[BK]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t sr[32], w0[32], w1[32];
+    tmem_ld32(trow + s_col + 32 * c, sr);
+    const uint32_t gcol = g_col + 32 * warp + 96 - 32 * c;
+    tmem_ld32(trow + gcol, w0);
+    tmem_ld32(trow + gcol + 32, w1);
+    tmem_wait_ld();
+    float win[64];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      win[e] = __uint_as_float(w0[e]);
+      win[32 + e] = __uint_as_float(w1[e]);
+    }
+    // win[x] <- win[x + lane] (5 predicated stages; fixed trip counts keep
+    // the array in registers)
+#pragma unroll
+    for (int b = 4; b >= 0; --b) {
+      const int sh = 1 << b;
+      const bool take = (lane >> b) & 1;
+#pragma unroll
+      for (int e = 0; e < 63; ++e)
+        if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int jj = 32 * c + k;
+      const float a = __uint_as_float(sr[k]) + win[31 - k];
+      const bool valid = jj < x.nvalid && x.jlog0 + jj <= i;
+      y[jj] = valid ? a * scale_log2 : -INFINITY;
+    }
+  }
+}
+
+// Vector float atomic add (sm_90+): 4 consecutive floats, 16-byte aligned.
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+}  // namespace tc
+}  // namespace rxl
