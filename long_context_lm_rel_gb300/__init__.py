@@ -70,6 +70,8 @@ def lib():
             L.rxl_last_cuda_error.restype = ctypes.c_int
             L.rxl_last_launch_count.argtypes = []
             L.rxl_last_launch_count.restype = ctypes.c_int
+            L.rxl_device_error_flags.argtypes = []
+            L.rxl_device_error_flags.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -128,3 +130,7 @@ def rxl_status_string(status: int) -> str:
 
 def rxl_last_launch_count() -> int:
     return int(lib().rxl_last_launch_count())
+
+
+def rxl_device_error_flags() -> int:
+    return int(lib().rxl_device_error_flags())

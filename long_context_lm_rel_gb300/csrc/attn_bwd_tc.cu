@@ -18,7 +18,11 @@
 //   q      : one CTA per (b, h, 128-query tile), loops over key tiles:
 //            S, G -> P, dP -> dA, and the sheared dG[ii][t] = dA[ii][ii+127-t];
 //            dQ_content += dA K and dQ_position += dG Rband accumulate in TMEM;
-//            dR_band = dG^T (Q+v) per tile pair, added into dR (fp32 atomics)
+//            dR_band = dG^T (Q+v) per tile pair, added into dR (fp32 atomics).
+//            The position products run in fp16 (dG scaled by a CTA-wide power
+//            of two, R band and (Q+v) converted in place): R rows are several
+//            times larger than K rows, and bf16 rounding of dA in that term
+//            alone can exceed 1% of max|dQ| on short contexts.
 //   finish : du, dv = fixed-order sums of the per-CTA column sums of the two
 //            dQ parts
 // Both main kernels keep the score tile in TMEM (lanes = query rows), so the
@@ -41,6 +45,8 @@ constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
 constexpr uint32_t IDESC_G = idesc_bf16(128, 256, false, false);
 constexpr uint32_t IDESC_MN_MN = idesc_bf16(128, 64, true, true);   // A^T . B, both d/row-major tiles
 constexpr uint32_t IDESC_K_MN = idesc_bf16(128, 64, false, true);
+constexpr uint32_t IDESC_K_MN_F16 = idesc_f16(128, 64, false, true);
+constexpr uint32_t IDESC_MN_MN_F16 = idesc_f16(128, 64, true, true);
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ int g_bwd_error;
@@ -79,15 +85,18 @@ __device__ __forceinline__ void store_row_bf16(uint32_t base, int ii, const floa
 // With rev[x] = a[127 - x], output column chunk D (32 columns from
 // 32*warp + 32*D) holds rev[32D + y - lane]; the lane shift is a 5-stage
 // barrel shift of a 64-value window.
+// Values are multiplied by `scale` and stored as fp16.
 __device__ __forceinline__ void store_sheared_row(uint32_t base, int ii, int warp, int lane,
-                                                  const float (&a)[BK]) {
+                                                  const float (&a)[BK], float scale) {
   auto put32 = [&](int col0, const float (&v)[32]) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int col = col0 + 8 * e;
       const uint32_t addr = base + (col >> 6) * 16384 + sw128_offset(ii, (col & 63) >> 3);
-      st_shared_v4(addr, pack_bf16(v[8 * e + 0], v[8 * e + 1]), pack_bf16(v[8 * e + 2], v[8 * e + 3]),
-                   pack_bf16(v[8 * e + 4], v[8 * e + 5]), pack_bf16(v[8 * e + 6], v[8 * e + 7]));
+      st_shared_v4(addr, pack_f16(scale * v[8 * e + 0], scale * v[8 * e + 1]),
+                   pack_f16(scale * v[8 * e + 2], scale * v[8 * e + 3]),
+                   pack_f16(scale * v[8 * e + 4], scale * v[8 * e + 5]),
+                   pack_f16(scale * v[8 * e + 6], scale * v[8 * e + 7]));
     }
   };
   // column chunks outside [32*warp, 32*warp + 160) are zero for every lane
@@ -325,13 +334,13 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
   const uint32_t bar_q = sb + Q_BAR, bar_k = bar_q + 8, bar_sg = bar_q + 16, bar_p = bar_q + 24;
   const uint32_t bar_dp = bar_q + 32, bar_ds = bar_q + 40, bar_dr = bar_q + 48, bar_fl = bar_q + 56;
-  const uint32_t bar_drain = bar_q + 64;
+  const uint32_t bar_drain = bar_q + 64, bar_red = bar_q + 88;
   uint32_t *tmem_slot = (uint32_t *)(smem + Q_BAR + 72);
   volatile int *abort_flag = (volatile int *)(smem + Q_BAR + 80);
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1); mbar_init(bar_k, 1); mbar_init(bar_sg, 1); mbar_init(bar_p, 128);
     mbar_init(bar_dp, 1); mbar_init(bar_ds, 128); mbar_init(bar_dr, 1); mbar_init(bar_fl, 128);
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, 1); mbar_init(bar_red, 4);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -346,16 +355,18 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       int k_issued = 0;
       auto issue_k = [&](int t) {
         const KeyTile x = tiles.get(t);
-        mbar_expect_tx(bar_k, 2 * 16384 + 32768);
+        // (Q+v) is reloaded with every key tile: the previous copy was
+        // converted to fp16 in place
+        mbar_expect_tx(bar_k, 3 * 16384 + 32768);
         tma_load_3d(sb + Q_K, &tm_k, 0, x.phys0, bh, bar_k);
         tma_load_3d(sb + Q_V, &tm_v, 0, x.phys0, bh, bar_k);
         tma_load_3d(sb + Q_R, &tm_r, 0, i0 - x.jlog0 - (BK - 1), h, bar_k);
+        tma_load_3d(sb + Q_QV, &tm_qv, 0, i0, bh, bar_k);
         ++k_issued;
       };
       bool ok = true;
-      mbar_expect_tx(bar_q, 3 * 16384);
+      mbar_expect_tx(bar_q, 2 * 16384);
       tma_load_3d(sb + Q_QU, &tm_qu, 0, i0, bh, bar_q);
-      tma_load_3d(sb + Q_QV, &tm_qv, 0, i0, bh, bar_q);
       tma_load_3d(sb + Q_DO, &tm_do, 0, i0, bh, bar_q);
       issue_k(0);
       ok = mbar_wait(bar_q, 0, abort_flag);
@@ -381,15 +392,15 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           mma_bf16(tmem + TM_A, kdesc(sb + Q_DA, k), mndesc(sb + Q_K, k), IDESC_K_MN,
                    (t > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < 16; ++k)  // dQ_position += dG . Rband
-          mma_bf16(tmem + TM_B, kdesc(sb + Q_DG, k), mndesc(sb + Q_R, k), IDESC_K_MN,
+        for (int k = 0; k < 16; ++k)  // dQ_position += dG . Rband (fp16)
+          mma_bf16(tmem + TM_B, kdesc(sb + Q_DG, k), mndesc(sb + Q_R, k), IDESC_K_MN_F16,
                    (t > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb)  // dR band = dG^T . (Q+v), two 128-distance blocks
+        for (int mb = 0; mb < 2; ++mb)  // dR band = dG^T . (Q+v), two 128-distance blocks (fp16)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             mma_bf16(tmem + TM_G + 64 * mb, mndesc(sb + Q_DG + 2 * mb * 16384, k),
-                     mndesc(sb + Q_QV, k), IDESC_MN_MN, k > 0);
+                     mndesc(sb + Q_QV, k), IDESC_MN_MN_F16, k > 0);
         mma_commit(bar_dr);
         if (!(ok = mbar_wait(bar_fl, t & 1, abort_flag))) break;
         if (t + 1 < T) issue_k(t + 1);
@@ -412,12 +423,22 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.f;
     const float Di = row_ok ? p.delta[row] : 0.f;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    volatile float *wmax = (volatile float *)(smem + Q_BAR + 96);  // [2][4] per-warp maxima
+    float sig = 1.0e30f;  // fp16 scale of the position products (power of two, non-increasing)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const KeyTile x = tiles.get(t);
-      ok = mbar_wait(bar_sg, t & 1, abort_flag);
+      ok = mbar_wait(bar_sg, t & 1, abort_flag) && mbar_wait(bar_k, t & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
+      // S and G are done with the bf16 R band and (Q+v): convert them to fp16
+      // for the position-gradient products of this tile pair
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        chunk_bf16_to_f16(sb + Q_R + sw128_offset(ii, c));
+        chunk_bf16_to_f16(sb + Q_R + 16384 + sw128_offset(ii, c));
+        chunk_bf16_to_f16(sb + Q_QV + sw128_offset(ii, c));
+      }
       float y[BK];
       tile_logits(trow, TM_S, TM_G, warp, lane, i, x, p.scale_log2, y);
 #pragma unroll
@@ -439,7 +460,40 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
       }
       store_row_bf16(sb + Q_DA, ii, y);
-      store_sheared_row(sb + Q_DG, ii, warp, lane, y);
+      // CTA-wide max |dA| of this tile pair -> power-of-two fp16 scale
+      float am = 0.f;
+#pragma unroll
+      for (int k = 0; k < BK; ++k) am = fmaxf(am, fabsf(y[k]));
+      am = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(am)));
+      if (lane == 0) {
+        wmax[(t & 1) * 4 + warp] = am;
+        mbar_arrive(bar_red);
+      }
+      ok = mbar_wait(bar_red, t & 1, abort_flag);  // bounded, unlike a named barrier
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      am = fmaxf(fmaxf(wmax[(t & 1) * 4 + 0], wmax[(t & 1) * 4 + 1]),
+                 fmaxf(wmax[(t & 1) * 4 + 2], wmax[(t & 1) * 4 + 3]));
+      if (am > 0.f) {
+        const float want = exp2f(14.f - ceilf(log2f(am)));  // max |scaled dA| <= 2^14
+        if (want < sig) {
+          if (t > 0) {
+            // rescale the fp16-scaled dQ_position accumulator
+            const float f = want / sig;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t g[32];
+              tmem_ld32(trow + TM_B + 32 * c, g);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) g[e] = __float_as_uint(__uint_as_float(g[e]) * f);
+              tmem_st32(trow + TM_B + 32 * c, g);
+            }
+            tmem_wait_st();
+          }
+          sig = want;
+        }
+      }
+      store_sheared_row(sb + Q_DG, ii, warp, lane, y, sig);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_ds);
@@ -458,10 +512,11 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           tmem_ld32(trow + TM_G + 64 * mb + 32 * c, g);
           tmem_wait_ld();
           if (d >= 0 && d < p.m + p.L) {
+            const float f = 1.f / sig;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              red_add_v4(dst + 32 * c + 4 * e, __uint_as_float(g[4 * e]), __uint_as_float(g[4 * e + 1]),
-                         __uint_as_float(g[4 * e + 2]), __uint_as_float(g[4 * e + 3]));
+              red_add_v4(dst + 32 * c + 4 * e, f * __uint_as_float(g[4 * e]), f * __uint_as_float(g[4 * e + 1]),
+                         f * __uint_as_float(g[4 * e + 2]), f * __uint_as_float(g[4 * e + 3]));
           }
         }
       }
@@ -480,6 +535,9 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         tmem_ld32(trow + TM_A + 32 * c, a);
         tmem_ld32(trow + TM_B + 32 * c, b);
         tmem_wait_ld();
+        const float f = sig < 1.0e29f ? 1.f / sig : 0.f;  // undo the fp16 scale
+#pragma unroll
+        for (int e = 0; e < 32; ++e) b[e] = __float_as_uint(__uint_as_float(b[e]) * f);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           red[ii * 64 + 32 * c + e] = __uint_as_float(a[e]);

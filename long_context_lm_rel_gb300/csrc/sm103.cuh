@@ -141,6 +141,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+// Same, fp16 A and B.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10));
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T, issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -203,6 +208,28 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two floats to fp16x2 (round to nearest, saturating to the finite range).
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// In place: 8 bf16 of a 16-byte shared-memory chunk become 8 fp16.
+__device__ __forceinline__ void chunk_bf16_to_f16(uint32_t addr) {
+  uint32_t a, b, c, d;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr));
+  auto cv = [](uint32_t x) {
+    const float lo = __uint_as_float(x << 16), hi = __uint_as_float(x & 0xFFFF0000u);
+    return pack_f16(lo, hi);
+  };
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(cv(a)), "r"(cv(b)),
+               "r"(cv(c)), "r"(cv(d))
+               : "memory");
 }
 
 __device__ __forceinline__ float ex2(float x) {

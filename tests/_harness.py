@@ -65,6 +65,13 @@ def logical_kv(phys: np.ndarray, cap: int, head: int, m: int) -> np.ndarray:
     return np.concatenate([phys[:, :, ring_rows(cap, head, m)], phys[:, :, cap:]], axis=2)
 
 
+def assert_no_device_error():
+    """No tensor-core kernel gave up on a bounded wait since the last check."""
+    import long_context_lm_rel_gb300 as rxl
+    flags = rxl.lib().rxl_device_error_flags()
+    assert flags == 0, f"device-side wait timeout flags: {flags}"
+
+
 def assert_close(name: str, got: np.ndarray, ref: np.ndarray, dtype: str, extra=""):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

@@ -17,7 +17,7 @@ import pytest
 
 import oracle
 import rxl_inputs as gen
-from tests._harness import AttnCall, assert_close, logical_kv, place_kv, to_host
+from tests._harness import AttnCall, assert_close, assert_no_device_error, logical_kv, place_kv, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +51,7 @@ def logical(x):
 def compare_full(x, c, cap, m, head, dtype, bwd=True, scale=0.125, tag=""):
     import torch
     torch.cuda.synchronize()
+    assert_no_device_error()
     k, v = logical(x)
     o, lse = oracle.fwd(x["q"], k, v, x["r"], x["u"], x["vb"], scale)
     assert_close("O", to_host(c.o), o, dtype, tag)
@@ -179,6 +180,7 @@ def test_full_size_config(cfg):
     cap = m = w.M
     c = run_gpu(x, cap, m, 0, "bf16", scale=w.scale)
     torch.cuda.synchronize()
+    assert_no_device_error()
     k, v = logical(x)
     rng = np.random.default_rng(cfg)
     sel = sample_rows(w.B, w.H, w.L, 96, rng)
