@@ -124,6 +124,37 @@ rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k,
                         size_t workspace_bytes, rxl_stream_t stream);
 
 /*
+ * rxl_attn_bwd_noalloc -- rxl_attn_bwd without a caller-supplied workspace.
+ * The paper has no counterpart: this is a deployment convenience.
+ *
+ * For callers that cannot allocate device memory when they run the backward:
+ * plugin-style hosts that pass in only pre-allocated inputs and outputs and
+ * provide no allocator, or latency-critical loops that must not pay for a
+ * cudaMalloc. The scratch is a fixed array inside the library
+ * (rxl_attn_bwd_noalloc_max_scratch_bytes() bytes, 16 MiB), held on every GPU
+ * that loads the library until the process exits; this call itself allocates
+ * nothing.
+ *  - Same arguments, outputs and checks as rxl_attn_bwd minus the workspace.
+ *  - Shapes whose backward needs more than the fixed scratch
+ *    (rxl_attn_bwd_workspace_bytes(desc) > max) return
+ *    RXL_ERR_WORKSPACE_TOO_SMALL without launching anything.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array per device and it keeps the last call's
+ *    contents (nothing in it has to start at zero). Calls that overlap on the
+ *    GPU, e.g. on two streams, race on it: serialise them.
+ */
+rxl_status rxl_attn_bwd_noalloc(const rxl_attn_desc *desc, const void *q, const void *k,
+                                const void *v, const void *r, const void *u, const void *vbias,
+                                const void *o, const float *lse, const void *dout, void *dq,
+                                void *dk, void *dv, float *dr, float *du, float *dvbias,
+                                rxl_stream_t stream);
+
+/* Size in bytes of the fixed scratch rxl_attn_bwd_noalloc uses. */
+size_t rxl_attn_bwd_noalloc_max_scratch_bytes(void);
+
+/*
  * FIFO memory ring (eq. Tail_M; update_mems with mem_len == cap).
  *   data         device pointer to plane 0, row 0
  *   planes       independent rings (e.g. B*H), >= 1

@@ -72,6 +72,10 @@ def lib():
             L.rxl_last_launch_count.restype = ctypes.c_int
             L.rxl_device_error_flags.argtypes = []
             L.rxl_device_error_flags.restype = ctypes.c_int
+            L.rxl_attn_bwd_noalloc.argtypes = [P(rxl_attn_desc)] + [vp] * 15 + [vp]
+            L.rxl_attn_bwd_noalloc.restype = ctypes.c_int
+            L.rxl_attn_bwd_noalloc_max_scratch_bytes.argtypes = []
+            L.rxl_attn_bwd_noalloc_max_scratch_bytes.restype = ctypes.c_size_t
             _lib = L
     return _lib
 
@@ -117,6 +121,20 @@ def rxl_attn_bwd(desc, q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr, du, d
                               *map(_ptr, (q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr, du,
                                           dvbias, workspace)),
                               int(workspace_bytes), _stream(stream)), "rxl_attn_bwd")
+
+
+def rxl_attn_bwd_noalloc(desc, q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr, du, dvbias,
+                         stream=None):
+    """rxl_attn_bwd for callers that cannot allocate: the scratch is a fixed
+    array inside the library (see include/rxl.h for its size and rules)."""
+    _check(lib().rxl_attn_bwd_noalloc(ctypes.byref(desc),
+                                      *map(_ptr, (q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv,
+                                                  dr, du, dvbias)),
+                                      _stream(stream)), "rxl_attn_bwd_noalloc")
+
+
+def rxl_attn_bwd_noalloc_max_scratch_bytes() -> int:
+    return int(lib().rxl_attn_bwd_noalloc_max_scratch_bytes())
 
 
 def rxl_mem_update(ring: rxl_ring, src, src_plane_stride: int, L: int, stream=None):
