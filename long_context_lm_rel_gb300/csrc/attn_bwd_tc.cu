@@ -40,7 +40,9 @@ namespace {
 using namespace sm103;
 using namespace tc;
 
-constexpr int kThreads = 160;
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each owning 64 of a row's keys
+constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
+constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
 constexpr uint32_t IDESC_G = idesc_bf16(128, 256, false, false);
 constexpr uint32_t IDESC_MN_MN = idesc_bf16(128, 64, true, true);   // A^T . B, both d/row-major tiles
@@ -69,70 +71,76 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {
   return sdesc_sw128(base + kk * 2048, 16384, 1024);
 }
 
-// Writes 128 fp32 values of row `ii` as bf16 into a [128][128] K-major
-// 128-byte-swizzled tile pair (columns 0-63 | 64-127, 16 KB apart).
-__device__ __forceinline__ void store_row_bf16(uint32_t base, int ii, const float (&a)[BK]) {
+// 64 fp32 values (keys 64*hf ..) of row ii as bf16 into column block hf of a
+// [128][128] K-major 128-byte-swizzled tile pair (blocks 16 KB apart).
+__device__ __forceinline__ void store_half_bf16(uint32_t base, int ii, int hf, const float (&a)[64]) {
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    const uint32_t addr = base + (c >> 3) * 16384 + sw128_offset(ii, c & 7);
-    st_shared_v4(addr, pack_bf16(a[8 * c + 0], a[8 * c + 1]), pack_bf16(a[8 * c + 2], a[8 * c + 3]),
-                 pack_bf16(a[8 * c + 4], a[8 * c + 5]), pack_bf16(a[8 * c + 6], a[8 * c + 7]));
+  for (int c = 0; c < 8; ++c)
+    st_shared_v4(base + hf * 16384 + sw128_offset(ii, c), pack_bf16(a[8 * c + 0], a[8 * c + 1]),
+                 pack_bf16(a[8 * c + 2], a[8 * c + 3]), pack_bf16(a[8 * c + 4], a[8 * c + 5]),
+                 pack_bf16(a[8 * c + 6], a[8 * c + 7]));
+}
+
+// Bounded rendezvous of the two warps of a lane quadrant (mbarrier, count 2).
+__device__ __forceinline__ bool pair_sync(uint32_t bar, int lane, uint32_t &phase,
+                                          volatile int *abort_flag) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, phase & 1, abort_flag));
+  ++phase;
+  return ok;
+}
+
+// Output chunk D of the sheared dG row ii: columns 32*quad + 32*D + y hold
+// v[ii + 127 - col] = w1[y + u] with w1[z] = v[158 - 32D - z] and u = 31 - lane
+// (5-stage barrel shift), stored as fp16 into a [128][256] K-major tile set
+// (four 16 KB column blocks).
+__device__ __forceinline__ void shear_put(uint32_t base, int ii, int quad, int lane, int D,
+                                          float (&w1)[63]) {
+  const int u = 31 - lane;
+#pragma unroll
+  for (int b = 4; b >= 0; --b) {
+    const int sh = 1 << b;
+    const bool take = (u >> b) & 1;
+#pragma unroll
+    for (int e = 0; e < 62; ++e)
+      if (e < 32 + sh - 1 && e + sh < 63) w1[e] = take ? w1[e + sh] : w1[e];
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int col = 32 * (quad + D) + 8 * e;
+    st_shared_v4(base + (col >> 6) * 16384 + sw128_offset(ii, (col & 63) >> 3),
+                 pack_f16(w1[8 * e + 0], w1[8 * e + 1]), pack_f16(w1[8 * e + 2], w1[8 * e + 3]),
+                 pack_f16(w1[8 * e + 4], w1[8 * e + 5]), pack_f16(w1[8 * e + 6], w1[8 * e + 7]));
   }
 }
 
-// Sheared row of dG: dG[ii][t] = a[ii + 127 - t] for t in [ii, ii+127], 0
-// elsewhere, into a [128][256] K-major tile set (four 16 KB column blocks).
-// With rev[x] = a[127 - x], output column chunk D (32 columns from
-// 32*warp + 32*D) holds rev[32D + y - lane]; the lane shift is a 5-stage
-// barrel shift of a 64-value window.
-// Values are multiplied by `scale` and stored as fp16.
-__device__ __forceinline__ void store_sheared_row(uint32_t base, int ii, int warp, int lane,
-                                                  const float (&a)[BK], float scale) {
-  auto put32 = [&](int col0, const float (&v)[32]) {
+// Half 0 of a row writes chunks D = 2, 3, 4 from its keys 0..63 (y) and keys
+// 64..95 received from half 1 (xk, already scaled); half 1 writes D = 0, 1
+// from its keys 64..127. Values are scaled by sig (a power of two).
+template <int D>
+__device__ __forceinline__ void shear_chunk_lo(uint32_t base, int ii, int quad, int lane,
+                                               const float (&y)[64], const float (&xk)[32], float sig) {
+  float w1[63];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int col = col0 + 8 * e;
-      const uint32_t addr = base + (col >> 6) * 16384 + sw128_offset(ii, (col & 63) >> 3);
-      st_shared_v4(addr, pack_f16(scale * v[8 * e + 0], scale * v[8 * e + 1]),
-                   pack_f16(scale * v[8 * e + 2], scale * v[8 * e + 3]),
-                   pack_f16(scale * v[8 * e + 4], scale * v[8 * e + 5]),
-                   pack_f16(scale * v[8 * e + 6], scale * v[8 * e + 7]));
-    }
-  };
-  // column chunks outside [32*warp, 32*warp + 160) are zero for every lane
-  for (int C = 0; C < 8; ++C) {
-    if (C < warp || C > warp + 4) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = 32 * C + 8 * e;
-        st_shared_v4(base + (col >> 6) * 16384 + sw128_offset(ii, (col & 63) >> 3), 0, 0, 0, 0);
-      }
-    }
+  for (int z = 0; z < 63; ++z) {
+    const int key = 158 - 32 * D - z;
+    w1[z] = (key >= 0 && key < 64) ? sig * y[(key >= 0 && key < 64) ? key : 0]
+            : (key >= 64 && key < 96) ? xk[(key >= 64 && key < 96) ? key - 64 : 0]
+                                      : 0.f;
   }
-  const int u = 31 - lane;
+  shear_put(base, ii, quad, lane, D, w1);
+}
+template <int D>
+__device__ __forceinline__ void shear_chunk_hi(uint32_t base, int ii, int quad, int lane,
+                                               const float (&y)[64], float sig) {
+  float w1[63];
 #pragma unroll
-  for (int D = 0; D < 5; ++D) {
-    // w1[z] = rev[32(D-1) + 1 + z] = a[158 - 32D - z], 0 outside [0,128)
-    float w1[63];
-#pragma unroll
-    for (int z = 0; z < 63; ++z) {
-      const int idx = 158 - 32 * D - z;
-      w1[z] = (idx >= 0 && idx < BK) ? a[(idx >= 0 && idx < BK) ? idx : 0] : 0.f;
-    }
-    // w1[z] <- w1[z + u]
-#pragma unroll
-    for (int b = 4; b >= 0; --b) {
-      const int sh = 1 << b;
-      const bool take = (u >> b) & 1;
-#pragma unroll
-      for (int e = 0; e < 62; ++e)
-        if (e < 32 + sh - 1 && e + sh < 63) w1[e] = take ? w1[e + sh] : w1[e];
-    }
-    float out[32];
-#pragma unroll
-    for (int y = 0; y < 32; ++y) out[y] = w1[y];
-    put32(32 * (warp + D), out);
+  for (int z = 0; z < 63; ++z) {
+    const int key = 158 - 32 * D - z;
+    w1[z] = (key >= 64 && key < 128) ? sig * y[(key >= 64 && key < 128) ? key - 64 : 0] : 0.f;
   }
+  shear_put(base, ii, quad, lane, D, w1);
 }
 
 // ------------------------------------------------------------- dK / dV kernel
@@ -164,18 +172,19 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   uint32_t *tmem_slot = (uint32_t *)(smem + KV_BAR + 64);
   volatile int *abort_flag = (volatile int *)(smem + KV_BAR + 72);
   if (threadIdx.x == 0) {
-    mbar_init(bar_kv, 1); mbar_init(bar_q, 1); mbar_init(bar_sg, 1); mbar_init(bar_p, 128);
-    mbar_init(bar_dp, 1); mbar_init(bar_ds, 128); mbar_init(bar_pair, 1); mbar_init(bar_drain, 1);
+    mbar_init(bar_kv, 1); mbar_init(bar_q, 1); mbar_init(bar_sg, 1);
+    mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_dp, 1);
+    mbar_init(bar_ds, kSoftmaxWarps * 32); mbar_init(bar_pair, 1); mbar_init(bar_drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 4) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == kProducerWarp) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     if (lane == 0) {
       int q_issued = 0;
       auto issue_q = [&](int n) {
@@ -235,8 +244,9 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
     __syncwarp();
   } else {
-    const int ii = warp * 32 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const int quad = warp & 3, hf = warp >> 2;
+    const int ii = quad * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
     for (int n = 0; n < NQ; ++n) {
       const int i = (qlo + n) * BQ + ii;
@@ -247,11 +257,11 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       ok = mbar_wait(bar_sg, n & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      float y[BK];
-      tile_logits(trow, TM_S, TM_G, warp, lane, i, x, p.scale_log2, y);
+      float y[64];
+      half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, x, p.scale_log2, y);
 #pragma unroll
-      for (int k = 0; k < BK; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
-      store_row_bf16(sb + KV_P, ii, y);
+      for (int k = 0; k < 64; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
+      store_half_bf16(sb + KV_P, ii, hf, y);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_p);
@@ -259,17 +269,17 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dp[32];
-        tmem_ld32(trow + TM_S + 32 * c, dp);
+        tmem_ld32(trow + TM_S + 64 * hf + 32 * cc, dp);
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float pv = y[32 * c + k];
-          y[32 * c + k] = pv != 0.f ? p.scale * pv * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
+          const float pv = y[32 * cc + k];
+          y[32 * cc + k] = pv != 0.f ? p.scale * pv * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
         }
       }
-      store_row_bf16(sb + KV_DA, ii, y);
+      store_half_bf16(sb + KV_DA, ii, hf, y);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_ds);
@@ -277,27 +287,25 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (ok && NQ > 0) ok = mbar_wait(bar_pair, (NQ - 1) & 1, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
-      // TMEM lanes of the dV / dK accumulators are key rows
+      // TMEM lanes of the dV / dK accumulators are key rows; half 0 writes
+      // dV, half 1 dK
       tc_fence_after();
       const int kk = ii;
       const size_t krow = (size_t)bh * p.kv_rows + x.phys0 + (kk < x.nvalid ? kk : 0);
+      __nv_bfloat16 *dst = (hf ? p.dk : p.dv) + krow * DH;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16 *dst = (which ? p.dk : p.dv) + krow * DH;
+      for (int c = 0; c < 2; ++c) {
+        uint32_t g[32];
+        tmem_ld32(trow + (hf ? TM_B : TM_A) + 32 * c, g);
+        tmem_wait_ld();
+        if (kk < x.nvalid) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t g[32];
-          tmem_ld32(trow + (which ? TM_B : TM_A) + 32 * c, g);
-          tmem_wait_ld();
-          if (kk < x.nvalid) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              ((uint4 *)dst)[4 * c + e] = make_uint4(
-                  pack_bf16(__uint_as_float(g[8 * e + 0]), __uint_as_float(g[8 * e + 1])),
-                  pack_bf16(__uint_as_float(g[8 * e + 2]), __uint_as_float(g[8 * e + 3])),
-                  pack_bf16(__uint_as_float(g[8 * e + 4]), __uint_as_float(g[8 * e + 5])),
-                  pack_bf16(__uint_as_float(g[8 * e + 6]), __uint_as_float(g[8 * e + 7])));
-          }
+          for (int e = 0; e < 4; ++e)
+            ((uint4 *)dst)[4 * c + e] = make_uint4(
+                pack_bf16(__uint_as_float(g[8 * e + 0]), __uint_as_float(g[8 * e + 1])),
+                pack_bf16(__uint_as_float(g[8 * e + 2]), __uint_as_float(g[8 * e + 3])),
+                pack_bf16(__uint_as_float(g[8 * e + 4]), __uint_as_float(g[8 * e + 5])),
+                pack_bf16(__uint_as_float(g[8 * e + 6]), __uint_as_float(g[8 * e + 7])));
         }
       }
     } else {
@@ -307,14 +315,14 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, 512);
+  if (warp == kProducerWarp) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------- dQ / dR / du / dv kernel
 
 constexpr uint32_t Q_QU = 0, Q_QV = 16384, Q_DO = 32768, Q_K = 49152, Q_V = 65536;
-constexpr uint32_t Q_R = 81920, Q_DA = 114688, Q_DG = 147456, Q_BAR = 212992;
-constexpr uint32_t Q_SMEM = Q_BAR + 128 + 1024;
+constexpr uint32_t Q_R = 81920, Q_DA = 114688, Q_DG = 147456, Q_X = 212992, Q_BAR = 221184;
+constexpr uint32_t Q_SMEM = Q_BAR + 256 + 1024;  // barriers, TMEM slot, flags, [2][8] warp maxima
 
 __global__ void __launch_bounds__(kThreads, 1)
 rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -334,23 +342,26 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
   const uint32_t bar_q = sb + Q_BAR, bar_k = bar_q + 8, bar_sg = bar_q + 16, bar_p = bar_q + 24;
   const uint32_t bar_dp = bar_q + 32, bar_ds = bar_q + 40, bar_dr = bar_q + 48, bar_fl = bar_q + 56;
-  const uint32_t bar_drain = bar_q + 64, bar_red = bar_q + 88;
-  uint32_t *tmem_slot = (uint32_t *)(smem + Q_BAR + 72);
-  volatile int *abort_flag = (volatile int *)(smem + Q_BAR + 80);
+  const uint32_t bar_drain = bar_q + 64, bar_red = bar_q + 72, bar_x0 = bar_q + 80;  // + 4 pair barriers
+  uint32_t *tmem_slot = (uint32_t *)(smem + Q_BAR + 112);
+  volatile int *abort_flag = (volatile int *)(smem + Q_BAR + 116);
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1); mbar_init(bar_k, 1); mbar_init(bar_sg, 1); mbar_init(bar_p, 128);
-    mbar_init(bar_dp, 1); mbar_init(bar_ds, 128); mbar_init(bar_dr, 1); mbar_init(bar_fl, 128);
-    mbar_init(bar_drain, 1); mbar_init(bar_red, 4);
+    mbar_init(bar_q, 1); mbar_init(bar_k, 1); mbar_init(bar_sg, 1);
+    mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_dp, 1);
+    mbar_init(bar_ds, kSoftmaxWarps * 32); mbar_init(bar_dr, 1);
+    mbar_init(bar_fl, kSoftmaxWarps * 32); mbar_init(bar_drain, 1);
+    mbar_init(bar_red, kSoftmaxWarps);
+    for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 4) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == kProducerWarp) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     if (lane == 0) {
       int k_issued = 0;
       auto issue_k = [&](int t) {
@@ -416,14 +427,17 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
     __syncwarp();
   } else {
-    const int ii = warp * 32 + lane;
+    const int quad = warp & 3, hf = warp >> 2;
+    const int ii = quad * 32 + lane;
     const int i = i0 + ii;
     const bool row_ok = i < p.L;
     const size_t row = (size_t)bh * p.L + (row_ok ? i : 0);
     const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.f;
     const float Di = row_ok ? p.delta[row] : 0.f;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    volatile float *wmax = (volatile float *)(smem + Q_BAR + 96);  // [2][4] per-warp maxima
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t bar_x = bar_x0 + 8 * quad;
+    volatile float *wmax = (volatile float *)(smem + Q_BAR + 96 + 32);  // [2][8] in the slack
+    uint32_t xphase = 0;
     float sig = 1.0e30f;  // fp16 scale of the position products (power of two, non-increasing)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -434,85 +448,124 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       // S and G are done with the bf16 R band and (Q+v): convert them to fp16
       // for the position-gradient products of this tile pair
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        chunk_bf16_to_f16(sb + Q_R + sw128_offset(ii, c));
-        chunk_bf16_to_f16(sb + Q_R + 16384 + sw128_offset(ii, c));
-        chunk_bf16_to_f16(sb + Q_QV + sw128_offset(ii, c));
-      }
-      float y[BK];
-      tile_logits(trow, TM_S, TM_G, warp, lane, i, x, p.scale_log2, y);
+      for (int c = 0; c < 8; ++c) chunk_bf16_to_f16(sb + Q_R + hf * 16384 + sw128_offset(ii, c));
 #pragma unroll
-      for (int k = 0; k < BK; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
+      for (int c = 0; c < 4; ++c) chunk_bf16_to_f16(sb + Q_QV + sw128_offset(ii, 4 * hf + c));
+      float y[64];
+      half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, x, p.scale_log2, y);
+#pragma unroll
+      for (int k = 0; k < 64; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
       tc_fence_before();
       mbar_arrive(bar_p);
       ok = mbar_wait(bar_dp, t & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dp[32];
-        tmem_ld32(trow + TM_S + 32 * c, dp);
+        tmem_ld32(trow + TM_S + 64 * hf + 32 * cc, dp);
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float pv = y[32 * c + k];
-          y[32 * c + k] = pv != 0.f ? p.scale * pv * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
+          const float pv = y[32 * cc + k];
+          y[32 * cc + k] = pv != 0.f ? p.scale * pv * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
         }
       }
-      store_row_bf16(sb + Q_DA, ii, y);
+      store_half_bf16(sb + Q_DA, ii, hf, y);
       // CTA-wide max |dA| of this tile pair -> power-of-two fp16 scale
       float am = 0.f;
 #pragma unroll
-      for (int k = 0; k < BK; ++k) am = fmaxf(am, fabsf(y[k]));
+      for (int k = 0; k < 64; ++k) am = fmaxf(am, fabsf(y[k]));
       am = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(am)));
       if (lane == 0) {
-        wmax[(t & 1) * 4 + warp] = am;
+        wmax[(t & 1) * 8 + warp] = am;
         mbar_arrive(bar_red);
       }
       ok = mbar_wait(bar_red, t & 1, abort_flag);  // bounded, unlike a named barrier
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      am = fmaxf(fmaxf(wmax[(t & 1) * 4 + 0], wmax[(t & 1) * 4 + 1]),
-                 fmaxf(wmax[(t & 1) * 4 + 2], wmax[(t & 1) * 4 + 3]));
+      am = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSoftmaxWarps; ++w) am = fmaxf(am, wmax[(t & 1) * 8 + w]);
       if (am > 0.f) {
         const float want = exp2f(14.f - ceilf(log2f(am)));  // max |scaled dA| <= 2^14
         if (want < sig) {
           if (t > 0) {
-            // rescale the fp16-scaled dQ_position accumulator
+            // rescale this half's columns of the fp16-scaled dQ_position accumulator
             const float f = want / sig;
+            uint32_t g[32];
+            tmem_ld32(trow + TM_B + 32 * hf, g);
+            tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              uint32_t g[32];
-              tmem_ld32(trow + TM_B + 32 * c, g);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) g[e] = __float_as_uint(__uint_as_float(g[e]) * f);
-              tmem_st32(trow + TM_B + 32 * c, g);
-            }
+            for (int e = 0; e < 32; ++e) g[e] = __float_as_uint(__uint_as_float(g[e]) * f);
+            tmem_st32(trow + TM_B + 32 * hf, g);
             tmem_wait_st();
           }
           sig = want;
         }
       }
-      store_sheared_row(sb + Q_DG, ii, warp, lane, y, sig);
+      // sheared dG (fp16, scaled by sig): half 1 hands keys 64..95 to half 0
+      const uint32_t xrow = sb + Q_X + ii * 64;
+      if (hf == 1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          st_shared_v4(xrow + 16 * e, pack_f16(sig * y[8 * e + 0], sig * y[8 * e + 1]),
+                       pack_f16(sig * y[8 * e + 2], sig * y[8 * e + 3]),
+                       pack_f16(sig * y[8 * e + 4], sig * y[8 * e + 5]),
+                       pack_f16(sig * y[8 * e + 6], sig * y[8 * e + 7]));
+      }
+      if (!(ok = pair_sync(bar_x, lane, xphase, abort_flag))) break;
+      // column chunks outside [32*quad, 32*quad + 160) are zero for every lane
+      for (int C = 0; C < 8; ++C) {
+        if (hf == 0 ? C < quad : C > quad + 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = 32 * C + 8 * e;
+            st_shared_v4(sb + Q_DG + (col >> 6) * 16384 + sw128_offset(ii, (col & 63) >> 3), 0, 0, 0, 0);
+          }
+        }
+      }
+      if (hf == 0) {
+        float xk[32];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t a, b, c, d;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                       : "r"(xrow + 16 * e));
+          const uint32_t w[4] = {a, b, c, d};
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const __half2 hv = *reinterpret_cast<const __half2 *>(&w[f]);
+            const float2 fv = __half22float2(hv);
+            xk[8 * e + 2 * f] = fv.x;
+            xk[8 * e + 2 * f + 1] = fv.y;
+          }
+        }
+        shear_chunk_lo<2>(sb + Q_DG, ii, quad, lane, y, xk, sig);
+        shear_chunk_lo<3>(sb + Q_DG, ii, quad, lane, y, xk, sig);
+        shear_chunk_lo<4>(sb + Q_DG, ii, quad, lane, y, xk, sig);
+      } else {
+        shear_chunk_hi<0>(sb + Q_DG, ii, quad, lane, y, sig);
+        shear_chunk_hi<1>(sb + Q_DG, ii, quad, lane, y, sig);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_ds);
       ok = mbar_wait(bar_dr, t & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      // dR rows of this tile pair: TMEM lane = band row, distance d0 + row
+      // dR rows of this tile pair: TMEM lane = band row, half hf reads block hf
       const int d0 = i0 - x.jlog0 - (BK - 1);
-#pragma unroll
-      for (int mb = 0; mb < 2; ++mb) {
-        const int d = d0 + 128 * mb + ii;
+      {
+        const int d = d0 + 128 * hf + ii;
         float *dst = p.dr + ((size_t)h * p.kv_rows + (d >= 0 ? d : 0)) * DH;
+        const float f = 1.f / sig;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t g[32];
-          tmem_ld32(trow + TM_G + 64 * mb + 32 * c, g);
+          tmem_ld32(trow + TM_G + 64 * hf + 32 * c, g);
           tmem_wait_ld();
           if (d >= 0 && d < p.m + p.L) {
-            const float f = 1.f / sig;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               red_add_v4(dst + 32 * c + 4 * e, f * __uint_as_float(g[4 * e]), f * __uint_as_float(g[4 * e + 1]),
@@ -526,41 +579,39 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
-      // dQ = content + position parts; du, dv partials = column sums of the parts
+      // dQ = content + position parts; du, dv partials = column sums of the
+      // parts. This thread owns columns 32*hf .. 32*hf+31 of its row.
       float *red = (float *)(smem + Q_DG);  // [2][128][64] fp32, reuses the dG tile
       uint4 *qrow = (uint4 *)(p.dq + row * DH);
+      uint32_t a[32], b[32];
+      tmem_ld32(trow + TM_A + 32 * hf, a);
+      tmem_ld32(trow + TM_B + 32 * hf, b);
+      tmem_wait_ld();
+      const float f = sig < 1.0e29f ? 1.f / sig : 0.f;  // undo the fp16 scale
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t a[32], b[32];
-        tmem_ld32(trow + TM_A + 32 * c, a);
-        tmem_ld32(trow + TM_B + 32 * c, b);
-        tmem_wait_ld();
-        const float f = sig < 1.0e29f ? 1.f / sig : 0.f;  // undo the fp16 scale
+      for (int e = 0; e < 32; ++e) b[e] = __float_as_uint(__uint_as_float(b[e]) * f);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) b[e] = __float_as_uint(__uint_as_float(b[e]) * f);
+      for (int e = 0; e < 32; ++e) {
+        red[ii * 64 + 32 * hf + e] = __uint_as_float(a[e]);
+        red[128 * 64 + ii * 64 + 32 * hf + e] = __uint_as_float(b[e]);
+      }
+      if (row_ok) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          red[ii * 64 + 32 * c + e] = __uint_as_float(a[e]);
-          red[128 * 64 + ii * 64 + 32 * c + e] = __uint_as_float(b[e]);
-        }
-        if (row_ok) {
+        for (int e = 0; e < 4; ++e) {
+          float s8[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float s[8];
-#pragma unroll
-            for (int f = 0; f < 8; ++f) s[f] = __uint_as_float(a[8 * e + f]) + __uint_as_float(b[8 * e + f]);
-            qrow[4 * c + e] = make_uint4(pack_bf16(s[0], s[1]), pack_bf16(s[2], s[3]),
-                                         pack_bf16(s[4], s[5]), pack_bf16(s[6], s[7]));
-          }
+          for (int g = 0; g < 8; ++g) s8[g] = __uint_as_float(a[8 * e + g]) + __uint_as_float(b[8 * e + g]);
+          qrow[4 * hf + e] = make_uint4(pack_bf16(s8[0], s8[1]), pack_bf16(s8[2], s8[3]),
+                                        pack_bf16(s8[4], s8[5]), pack_bf16(s8[6], s8[7]));
         }
       }
     } else {
       atomicExch(&g_bwd_error, 8);
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");  // the 4 softmax warps only
-    if (ok) {
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // the softmax warps only
+    if (ok && threadIdx.x < 128) {
       const float *red = (const float *)(smem + Q_DG);
-      const int part = ii >> 6, col = ii & 63;  // 128 threads: (part, column)
+      const int part = threadIdx.x >> 6, col = threadIdx.x & 63;  // (part, column)
       float acc = 0.f;
       for (int r = 0; r < BQ; ++r) acc += red[part * 128 * 64 + r * 64 + col];
       p.duv_part[(((size_t)bh * p.nq + qt) * 2 + part) * DH + col] = acc;
@@ -569,7 +620,7 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, 512);
+  if (warp == kProducerWarp) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------- small kernels

@@ -15,31 +15,43 @@
 //              G = (Q+v) Rb^T  -> TMEM cols [128,384)   (M=128, N=256)
 //     so G[ii][t] = (q_ii+v).r_{d0+t}; the relative shift the pages do by
 //     pad/reshape/slice is an index skew here: S_p[ii][jj] = G[ii][ii-jj+127];
-//   * the 4 softmax warps (one thread per query row, TMEM lane = row) load S
-//     and their skewed G window, mask, run the fp32 online softmax (exp2),
-//     write P (bf16) to shared memory and rescale O in TMEM;
+//     (Q+u) and (Q+v) are stored prescaled by scale*log2(e), so S + S_p is
+//     already the base-2 logit;
+//   * 8 softmax warps, two per TMEM lane quadrant: the thread of (row ii,
+//     half hf) handles keys 64*hf .. 64*hf+63 of row ii. It loads S and its
+//     skewed G window, masks, and runs the fp32 online softmax (exp2); the two
+//     halves of a row exchange their maxima (and at the end their sums)
+//     through shared memory. P goes to shared memory (bf16), O is rescaled in
+//     TMEM;
 //   * tcgen05: O += P V -> TMEM cols [384,448)          (M=128, N=64)
-// Warp 4 is the producer: one thread issues the TMA loads (two stages) and
+// Warp 8 is the producer: one thread issues the TMA loads (two stages) and
 // every MMA; tcgen05.commit signals completion through mbarriers.
 //
-// The skew: thread (warp w, lane l) owns row ii = 32w+l and needs G columns
-// ii..ii+127. Per chunk of 32 keys it loads a warp-uniform 64-column window
-// and shifts it by l with a 5-stage predicated barrel shift.
+// The skew: thread of row ii = 32*quad + lane needs G columns ii..ii+127. Per
+// chunk of 32 keys it loads a warp-uniform 64-column window and shifts it by
+// its lane with a 5-stage predicated barrel shift.
 #include <math.h>
 #include <stdio.h>
 
 #include <mutex>
 
 #include "internal.cuh"
-#include "sm103.cuh"
+#include "tc_common.cuh"
 
 namespace rxl {
 namespace {
 
 using namespace sm103;
+using tc::BQ;
+using tc::BK;
+using tc::DH;
+using tc::NB;
+using tc::KeyTile;
+using tc::KeyTiles;
 
-constexpr int BQ = 128, BK = 128, DH = 64, NB = 256;
-constexpr int kThreads = 160;                  // 4 softmax warps + 1 producer warp
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
+constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr uint32_t SM_QU = 0;                  // [128][64] bf16, sw128
 constexpr uint32_t SM_QV = 16384;
 constexpr uint32_t SM_K = 32768;               // 2 stages x 16 KB
@@ -47,7 +59,8 @@ constexpr uint32_t SM_V = 65536;               // 2 stages x 16 KB
 constexpr uint32_t SM_R = 98304;               // 2 stages x 32 KB
 constexpr uint32_t SM_P = 163840;              // 2 x [128][64] bf16 (keys 0-63, 64-127)
 constexpr uint32_t SM_BAR = 196608;            // mbarriers, TMEM slot, abort flag
-constexpr uint32_t SMEM_BYTES = SM_BAR + 128 + 1024;  // + alignment slack
+constexpr uint32_t SM_X = SM_BAR + 128;        // row-half exchange: [2][2][128] floats
+constexpr uint32_t SMEM_BYTES = SM_X + 2048 + 1024;  // + alignment slack
 constexpr uint32_t STAGE_TX = 16384 + 16384 + 32768;
 constexpr uint32_t TM_S = 0, TM_G = 128, TM_O = 384, TM_COLS = 512;
 
@@ -64,7 +77,7 @@ struct Params {
   __nv_bfloat16 *o;
   float *lse;
   // backward preparation (kPrep): dO in, D = dO.O (fp32 O) and the bf16
-  // (Q+u), (Q+v) rows out
+  // (Q+u), (Q+v) rows (unscaled) out
   const __nv_bfloat16 *dout;
   float *delta;
   __nv_bfloat16 *qu_out, *qv_out;
@@ -72,48 +85,19 @@ struct Params {
 
 constexpr int kFwd = 0, kPrep = 1;
 
-struct Tile {
-  int phys0;   // first physical K/V row
-  int jlog0;   // logical key position of that row (-m .. L-1)
-  int nvalid;  // rows of the tile that are keys of this run
-};
-
-// Key tiles of query tile i0: ring run A (head .. cap), ring run B (0 ..),
-// then current rows 0 .. min(i0+BQ, L).
-struct TileList {
-  int lenA, lenB, lenC, nA, nB, nC;
-  __device__ TileList(const Params &p, int i0) {
-    lenA = min(p.m, p.cap - p.head);
-    lenB = p.m - lenA;
-    lenC = min(i0 + BQ, p.L);
-    nA = (lenA + BK - 1) / BK;
-    nB = (lenB + BK - 1) / BK;
-    nC = (lenC + BK - 1) / BK;
-  }
-  __device__ int count() const { return nA + nB + nC; }
-  __device__ Tile get(const Params &p, int t) const {
-    Tile x;
-    if (t < nA) {
-      x.phys0 = p.head + t * BK;
-      x.jlog0 = -p.m + t * BK;
-      x.nvalid = min(BK, lenA - t * BK);
-    } else if (t < nA + nB) {
-      const int u = t - nA;
-      x.phys0 = u * BK;
-      x.jlog0 = -p.m + lenA + u * BK;
-      x.nvalid = min(BK, lenB - u * BK);
-    } else {
-      const int u = t - nA - nB;
-      x.phys0 = p.cap + u * BK;
-      x.jlog0 = u * BK;
-      x.nvalid = min(BK, lenC - u * BK);
-    }
-    return x;
-  }
-};
-
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-  return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+// Exchange of one float per row between the two warps of a lane quadrant
+// (bounded wait): returns the partner's value.
+__device__ __forceinline__ bool pair_exchange(float mine, float *out, volatile float *xbuf,
+                                              uint32_t bar, int hf, int ii, int lane,
+                                              uint32_t &phase, volatile int *abort_flag) {
+  volatile float *slot = xbuf + (phase & 1) * 256;
+  slot[hf * 128 + ii] = mine;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, phase & 1, abort_flag));
+  ++phase;
+  *out = slot[(1 - hf) * 128 + ii];
+  return ok;
 }
 
 template <int MODE>
@@ -121,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_r, const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = align1024(smem_raw);
+  uint8_t *smem = tc::align1024(smem_raw);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = p.nq - 1 - (int)(blockIdx.x % p.nq);  // long query tiles first
@@ -134,18 +118,21 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   const uint32_t bar_drain = bar_full0 + 40;
   uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 48);
   volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 56);
+  const uint32_t bar_x0 = bar_full0 + 64;  // 4 quadrant exchange barriers
+  volatile float *xbuf = (volatile float *)(smem + SM_X);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_full0, 1);
     mbar_init(bar_full1, 1);
     mbar_init(bar_sg, 1);
-    mbar_init(bar_p, 4 * 32);
+    mbar_init(bar_p, kSoftmaxWarps * 32);
     mbar_init(bar_pv, 1);
     mbar_init(bar_drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     tmem_alloc(smem_u32(tmem_slot), TM_COLS);
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
@@ -153,34 +140,40 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       tma_prefetch_desc(&tm_r);
     }
   } else {
-    // (Q+u) and (Q+v) in bf16, 128-byte swizzled K-major tiles.
-    const int ii = warp * 32 + lane;
+    // (Q+u)*c and (Q+v)*c in bf16, c = scale*log2(e), as 128-byte swizzled
+    // K-major tiles; the row's two warps split its 8 chunks.
+    const int quad = warp & 3, hf = warp >> 2;
+    const int ii = quad * 32 + lane;
     const int i = i0 + ii;
+    const float c2 = p.scale_log2;
     const uint4 *qrow = (const uint4 *)(p.q + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
     const uint4 *urow = (const uint4 *)(p.u + (size_t)h * DH);
     const uint4 *vrow = (const uint4 *)(p.vb + (size_t)h * DH);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int cc = 0; cc < 4; ++cc) {
+      const int c = 4 * hf + cc;
       uint4 qv4 = i < p.L ? qrow[c] : make_uint4(0, 0, 0, 0);
       const uint4 u4 = urow[c], v4 = vrow[c];
-      const __nv_bfloat162 *q2 = (const __nv_bfloat162 *)&qv4;
-      const __nv_bfloat162 *u2 = (const __nv_bfloat162 *)&u4;
-      const __nv_bfloat162 *v2 = (const __nv_bfloat162 *)&v4;
-      uint32_t a[4], b[4];
+      const uint32_t qw[4] = {qv4.x, qv4.y, qv4.z, qv4.w};
+      const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+      const uint32_t vw[4] = {v4.x, v4.y, v4.z, v4.w};
+      uint32_t a[4], b[4], a1[4], b1[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 qf = __bfloat1622float2(q2[e]);
-        const float2 uf = __bfloat1622float2(u2[e]);
-        const float2 vf = __bfloat1622float2(v2[e]);
-        a[e] = pack_bf16(qf.x + uf.x, qf.y + uf.y);
-        b[e] = pack_bf16(qf.x + vf.x, qf.y + vf.y);
+        const float q0 = __uint_as_float(qw[e] << 16), q1 = __uint_as_float(qw[e] & 0xFFFF0000u);
+        const float u0 = __uint_as_float(uw[e] << 16), u1 = __uint_as_float(uw[e] & 0xFFFF0000u);
+        const float v0 = __uint_as_float(vw[e] << 16), v1 = __uint_as_float(vw[e] & 0xFFFF0000u);
+        a[e] = pack_bf16((q0 + u0) * c2, (q1 + u1) * c2);
+        b[e] = pack_bf16((q0 + v0) * c2, (q1 + v1) * c2);
+        a1[e] = pack_bf16(q0 + u0, q1 + u1);
+        b1[e] = pack_bf16(q0 + v0, q1 + v1);
       }
       st_shared_v4(sbase + SM_QU + sw128_offset(ii, c), a[0], a[1], a[2], a[3]);
       st_shared_v4(sbase + SM_QV + sw128_offset(ii, c), b[0], b[1], b[2], b[3]);
       if (MODE == kPrep && i < p.L) {
         const size_t off = ((size_t)bh * p.L + i) * DH;
-        ((uint4 *)(p.qu_out + off))[c] = make_uint4(a[0], a[1], a[2], a[3]);
-        ((uint4 *)(p.qv_out + off))[c] = make_uint4(b[0], b[1], b[2], b[3]);
+        ((uint4 *)(p.qu_out + off))[c] = make_uint4(a1[0], a1[1], a1[2], a1[3]);
+        ((uint4 *)(p.qv_out + off))[c] = make_uint4(b1[0], b1[1], b1[2], b1[3]);
       }
     }
     fence_proxy_async_smem();
@@ -190,17 +183,17 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const TileList tl(p, i0);
+  const KeyTiles tl(p.m, p.cap, p.head, min(i0 + BQ, p.L));
   const int T = tl.count();
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------ producer / MMA issuer
     if (lane == 0) {
       bool pending[2] = {false, false};
       int nissued[2] = {0, 0};
       auto issue_tma = [&](int t) {
         const int s = t & 1;
-        const Tile x = tl.get(p, t);
+        const KeyTile x = tl.get(t);
         const uint32_t bar = s ? bar_full1 : bar_full0;
         mbar_expect_tx(bar, STAGE_TX);
         tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, bh, bar);
@@ -269,10 +262,13 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __syncwarp();
   } else {
     // ----------------------------------------------------- softmax warps
-    const int ii = warp * 32 + lane;
+    const int quad = warp & 3, hf = warp >> 2;
+    const int ii = quad * 32 + lane;
     const int i = i0 + ii;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    float m_run = -INFINITY, l_run = 0.f;
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t bar_x = bar_x0 + 8 * quad;
+    uint32_t xphase = 0;
+    float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's part of the row sum
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t & 1;
@@ -281,121 +277,82 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       // tcgen05.ld/st below are warp-collective: keep every decision warp-uniform
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      const Tile x = tl.get(p, t);
-      float y[BK];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], w0[32], w1[32];
-        tmem_ld32(trow + TM_S + 32 * c, sr);
-        const uint32_t gcol = TM_G + 32 * warp + 96 - 32 * c;
-        tmem_ld32(trow + gcol, w0);
-        tmem_ld32(trow + gcol + 32, w1);
-        tmem_wait_ld();
-        float win[64];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          win[e] = __uint_as_float(w0[e]);
-          win[32 + e] = __uint_as_float(w1[e]);
-        }
-        // win[x] <- win[x + lane]: shifts by 16, 8, 4, 2, 1 under the lane's bits
-#pragma unroll
-        for (int b = 4; b >= 0; --b) {
-          const int sh = 1 << b;
-          const bool take = (lane >> b) & 1;
-          // fixed trip count so the loop unrolls and win[] stays in registers
-#pragma unroll
-          for (int e = 0; e < 63; ++e)
-            if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
-        }
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int jj = 32 * c + k;
-          const float a = __uint_as_float(sr[k]) + win[31 - k];
-          const bool valid = jj < x.nvalid && x.jlog0 + jj <= i;
-          y[jj] = valid ? a * p.scale_log2 : -INFINITY;
-        }
-      }
+      const KeyTile x = tl.get(t);
+      float y[64];
+      tc::half_tile_logits<false>(trow, TM_S, TM_G, quad, lane, hf, i, x, 1.f, y);
       float mt = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < BK; ++k) mt = fmaxf(mt, y[k]);
-      const float m_new = fmaxf(m_run, mt);
+      for (int k = 0; k < 64; ++k) mt = fmaxf(mt, y[k]);
+      float other;
+      if (!(ok = pair_exchange(mt, &other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
+      const float m_new = fmaxf(m_run, fmaxf(mt, other));
       const float ref = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = ex2(m_run - ref);  // 0 on the first visible tile
       float sum = 0.f;
-      uint32_t pk[BK / 2];
+      uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < BK; k += 2) {
+      for (int k = 0; k < 64; k += 2) {
         const float p0 = ex2(y[k] - ref), p1 = ex2(y[k + 1] - ref);
         sum += p0 + p1;
         pk[k / 2] = pack_bf16(p0, p1);
       }
       l_run = l_run * alpha + sum;
       m_run = m_new;
-      // P -> shared memory (the previous P.V finished: bar_sg of this tile
-      // was committed after it)
+      // P (keys 64*hf ..) -> its shared-memory column block; the previous
+      // P.V finished (bar_sg of this tile was committed after it)
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint32_t addr = sbase + SM_P + (c >> 3) * 16384 + sw128_offset(ii, c & 7);
-        st_shared_v4(addr, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      }
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(sbase + SM_P + hf * 16384 + sw128_offset(ii, c), pk[4 * c], pk[4 * c + 1],
+                     pk[4 * c + 2], pk[4 * c + 3]);
       // rows of V past the run hold another run's (or junk) data: zero them
       // so that 0 * junk cannot leak into O
       if (ii >= x.nvalid) {
         const uint32_t vrow = sbase + SM_V + s * 16384 + ii * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) st_shared_v4(vrow + 16 * c, 0, 0, 0, 0);
+        for (int c = 0; c < 4; ++c) st_shared_v4(vrow + 16 * (4 * hf + c), 0, 0, 0, 0);
       }
       if (__any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
+        uint32_t o[32];
+        tmem_ld32(trow + TM_O + 32 * hf, o);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t o[32];
-          tmem_ld32(trow + TM_O + 32 * c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(trow + TM_O + 32 * c, o);
-        }
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st32(trow + TM_O + 32 * hf, o);
         tmem_wait_st();
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_p);
     }
-    // epilogue: O / l, LSE (natural log)
+    // epilogue: O / l, LSE (natural log); this thread owns O columns 32*hf..
     if (ok && T > 0) ok = mbar_wait(bar_pv, (T - 1) & 1, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && MODE == kPrep) {
-      // D_i = dO_i . O_i with O_i still in fp32
+    float l_other = 0.f;
+    if (ok) ok = pair_exchange(l_run, &l_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
+    if (ok) {
       tc_fence_after();
-      const float inv = 1.f / l_run;
-      const uint4 *drow = (const uint4 *)(p.dout + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
-      float acc = 0.f;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        tmem_ld32(trow + TM_O + 32 * c, o);
-        tmem_wait_ld();
+      const float inv = 1.f / (l_run + l_other);
+      uint32_t o[32];
+      tmem_ld32(trow + TM_O + 32 * hf, o);
+      tmem_wait_ld();
+      if (MODE == kPrep) {
+        // D_i = dO_i . O_i with O_i still in fp32
+        const uint4 *drow = (const uint4 *)(p.dout + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
+        float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const uint4 d4 = drow[4 * c + e];
-          const __nv_bfloat162 *d2 = (const __nv_bfloat162 *)&d4;
+          const uint4 d4 = drow[4 * hf + e];
+          const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-          for (int f = 0; f < 4; ++f) {
-            const float2 df = __bfloat1622float2(d2[f]);
-            acc += __uint_as_float(o[8 * e + 2 * f]) * df.x + __uint_as_float(o[8 * e + 2 * f + 1]) * df.y;
-          }
+          for (int f = 0; f < 4; ++f)
+            acc += __uint_as_float(o[8 * e + 2 * f]) * __uint_as_float(dw[f] << 16) +
+                   __uint_as_float(o[8 * e + 2 * f + 1]) * __uint_as_float(dw[f] & 0xFFFF0000u);
         }
-      }
-      if (i < p.L) p.delta[(size_t)bh * p.L + i] = acc * inv;
-    } else if (ok) {
-      tc_fence_after();
-      const float inv = 1.f / l_run;
-      uint4 *orow = (uint4 *)(p.o + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        tmem_ld32(trow + TM_O + 32 * c, o);
-        tmem_wait_ld();
+        float acc_other = 0.f;
+        ok = pair_exchange(acc, &acc_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
+        if (ok && hf == 0 && i < p.L) p.delta[(size_t)bh * p.L + i] = (acc + acc_other) * inv;
+      } else {
+        uint4 *orow = (uint4 *)(p.o + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           uint4 v;
@@ -403,18 +360,18 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           v.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
           v.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
           v.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-          if (i < p.L) orow[4 * c + e] = v;
+          if (i < p.L) orow[4 * hf + e] = v;
         }
+        if (hf == 0 && i < p.L)
+          p.lse[(size_t)bh * p.L + i] = (m_run + log2f(l_run + l_other)) * 0.69314718055994531f;
       }
-      if (i < p.L) p.lse[(size_t)bh * p.L + i] = (m_run + log2f(l_run)) * 0.69314718055994531f;
-    } else {
-      atomicExch(&g_fwd_error, 1);
     }
+    if (!ok) atomicExch(&g_fwd_error, 1);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, TM_COLS);
+  if (warp == kProducerWarp) tmem_dealloc(tmem, TM_COLS);
 }
 
 // ------------------------------------------------------------------ host side

@@ -104,6 +104,48 @@ __device__ __forceinline__ void tile_logits(uint32_t trow, uint32_t s_col, uint3
   }
 }
 
+// Half-tile variant for two warps per TMEM lane quadrant: the calling thread
+// (quadrant `quad`, half `hf`) produces the logits of keys jj = 64*hf + k,
+// k = 0..63, of its row ii = 32*quad + lane: y[k] = (S + G_skewed) * scale,
+// -inf where masked. kScaled = false skips the multiply (operands prescaled).
+template <bool kScaled>
+__device__ __forceinline__ void half_tile_logits(uint32_t trow, uint32_t s_col, uint32_t g_col,
+                                                 int quad, int lane, int hf, int i,
+                                                 const KeyTile &x, float scale, float (&y)[64]) {
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int c = 2 * hf + cc;
+    uint32_t sr[32], w0[32], w1[32];
+    tmem_ld32(trow + s_col + 32 * c, sr);
+    const uint32_t gcol = g_col + 32 * quad + 96 - 32 * c;
+    tmem_ld32(trow + gcol, w0);
+    tmem_ld32(trow + gcol + 32, w1);
+    tmem_wait_ld();
+    float win[64];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      win[e] = __uint_as_float(w0[e]);
+      win[32 + e] = __uint_as_float(w1[e]);
+    }
+#pragma unroll
+    for (int b = 4; b >= 0; --b) {
+      const int sh = 1 << b;
+      const bool take = (lane >> b) & 1;
+#pragma unroll
+      for (int e = 0; e < 63; ++e)
+        if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
+    }
+    // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i
+    const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      float a = __uint_as_float(sr[k]) + win[31 - k];
+      if (kScaled) a *= scale;
+      y[32 * cc + k] = k <= lim ? a : -INFINITY;
+    }
+  }
+}
+
 // Vector float atomic add (sm_90+): 4 consecutive floats, 16-byte aligned.
 __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
