@@ -40,7 +40,7 @@ namespace {
 using namespace sm103;
 using namespace tc;
 
-constexpr int kSoftmaxWarps = 16;  // four per TMEM lane quadrant, each owning 32 of a row's keys
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each owning 64 of a row's keys
 constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
@@ -71,18 +71,18 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {
   return sdesc_sw128(base + kk * 2048, 16384, 1024);
 }
 
-// 32 fp32 values (keys 32*c ..) of row ii as bf16 into a [128][128] K-major
-// 128-byte-swizzled tile pair (column blocks of 64 keys, 16 KB apart).
-__device__ __forceinline__ void store_chunk_bf16(uint32_t base, int ii, int c, const float (&a)[32]) {
+// 64 fp32 values (keys 64*hf ..) of row ii as bf16 into column block hf of a
+// [128][128] K-major 128-byte-swizzled tile pair (blocks 16 KB apart).
+__device__ __forceinline__ void store_half_bf16(uint32_t base, int ii, int hf, const float (&a)[64]) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e)
-    st_shared_v4(base + (c >> 1) * 16384 + sw128_offset(ii, 4 * (c & 1) + e),
-                 pack_bf16(a[8 * e + 0], a[8 * e + 1]), pack_bf16(a[8 * e + 2], a[8 * e + 3]),
-                 pack_bf16(a[8 * e + 4], a[8 * e + 5]), pack_bf16(a[8 * e + 6], a[8 * e + 7]));
+  for (int c = 0; c < 8; ++c)
+    st_shared_v4(base + hf * 16384 + sw128_offset(ii, c), pack_bf16(a[8 * c + 0], a[8 * c + 1]),
+                 pack_bf16(a[8 * c + 2], a[8 * c + 3]), pack_bf16(a[8 * c + 4], a[8 * c + 5]),
+                 pack_bf16(a[8 * c + 6], a[8 * c + 7]));
 }
 
-// Bounded rendezvous of the four warps of a lane quadrant (mbarrier, count 4).
-__device__ __forceinline__ bool quad_sync(uint32_t bar, int lane, uint32_t &phase,
+// Bounded rendezvous of the two warps of a lane quadrant (mbarrier, count 2).
+__device__ __forceinline__ bool pair_sync(uint32_t bar, int lane, uint32_t &phase,
                                           volatile int *abort_flag) {
   __syncwarp();
   if (lane == 0) mbar_arrive(bar);
@@ -92,9 +92,11 @@ __device__ __forceinline__ bool quad_sync(uint32_t bar, int lane, uint32_t &phas
 }
 
 // Output chunk D of the sheared dG row ii: columns 32*quad + 32*D + y hold
-// v[ii + 127 - col] = w1[y + u] with u = 31 - lane (5-stage barrel shift),
-// stored as fp16 into a [128][256] K-major tile set (four 16 KB blocks).
-__device__ __forceinline__ void shear_put(uint32_t base, int ii, int col0, int lane, float (&w1)[63]) {
+// v[ii + 127 - col] = w1[y + u] with w1[z] = v[158 - 32D - z] and u = 31 - lane
+// (5-stage barrel shift), stored as fp16 into a [128][256] K-major tile set
+// (four 16 KB column blocks).
+__device__ __forceinline__ void shear_put(uint32_t base, int ii, int quad, int lane, int D,
+                                          float (&w1)[63]) {
   const int u = 31 - lane;
 #pragma unroll
   for (int b = 4; b >= 0; --b) {
@@ -106,11 +108,39 @@ __device__ __forceinline__ void shear_put(uint32_t base, int ii, int col0, int l
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const int col = col0 + 8 * e;
+    const int col = 32 * (quad + D) + 8 * e;
     st_shared_v4(base + (col >> 6) * 16384 + sw128_offset(ii, (col & 63) >> 3),
                  pack_f16(w1[8 * e + 0], w1[8 * e + 1]), pack_f16(w1[8 * e + 2], w1[8 * e + 3]),
                  pack_f16(w1[8 * e + 4], w1[8 * e + 5]), pack_f16(w1[8 * e + 6], w1[8 * e + 7]));
   }
+}
+
+// Half 0 of a row writes chunks D = 2, 3, 4 from its keys 0..63 (y) and keys
+// 64..95 received from half 1 (xk, already scaled); half 1 writes D = 0, 1
+// from its keys 64..127. Values are scaled by sig (a power of two).
+template <int D>
+__device__ __forceinline__ void shear_chunk_lo(uint32_t base, int ii, int quad, int lane,
+                                               const float (&y)[64], const float (&xk)[32], float sig) {
+  float w1[63];
+#pragma unroll
+  for (int z = 0; z < 63; ++z) {
+    const int key = 158 - 32 * D - z;
+    w1[z] = (key >= 0 && key < 64) ? sig * y[(key >= 0 && key < 64) ? key : 0]
+            : (key >= 64 && key < 96) ? xk[(key >= 64 && key < 96) ? key - 64 : 0]
+                                      : 0.f;
+  }
+  shear_put(base, ii, quad, lane, D, w1);
+}
+template <int D>
+__device__ __forceinline__ void shear_chunk_hi(uint32_t base, int ii, int quad, int lane,
+                                               const float (&y)[64], float sig) {
+  float w1[63];
+#pragma unroll
+  for (int z = 0; z < 63; ++z) {
+    const int key = 158 - 32 * D - z;
+    w1[z] = (key >= 64 && key < 128) ? sig * y[(key >= 64 && key < 128) ? key - 64 : 0] : 0.f;
+  }
+  shear_put(base, ii, quad, lane, D, w1);
 }
 
 // ------------------------------------------------------------- dK / dV kernel
@@ -214,7 +244,7 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
     __syncwarp();
   } else {
-    const int quad = warp & 3, ck = warp >> 2;  // TMEM lane quadrant, key chunk
+    const int quad = warp & 3, hf = warp >> 2;
     const int ii = quad * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
@@ -222,31 +252,34 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       const int i = (qlo + n) * BQ + ii;
       const bool row_ok = i < p.L;
       const size_t row = (size_t)bh * p.L + (row_ok ? i : 0);
-      const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.f;  // loaded before the wait
+      const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.f;
       const float Di = row_ok ? p.delta[row] : 0.f;
       ok = mbar_wait(bar_sg, n & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      float y[32];
-      chunk_logits<true>(trow, TM_S, TM_G, quad, lane, ck, i, x, p.scale_log2, y);
+      float y[64];
+      half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, x, p.scale_log2, y);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
-      store_chunk_bf16(sb + KV_P, ii, ck, y);
+      for (int k = 0; k < 64; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
+      store_half_bf16(sb + KV_P, ii, hf, y);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_p);
       ok = mbar_wait(bar_dp, n & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      {
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dp[32];
-        tmem_ld32(trow + TM_S + 32 * ck, dp);
+        tmem_ld32(trow + TM_S + 64 * hf + 32 * cc, dp);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          y[k] = y[k] != 0.f ? p.scale * y[k] * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
+        for (int k = 0; k < 32; ++k) {
+          const float pv = y[32 * cc + k];
+          y[32 * cc + k] = pv != 0.f ? p.scale * pv * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
+        }
       }
-      store_chunk_bf16(sb + KV_DA, ii, ck, y);
+      store_half_bf16(sb + KV_DA, ii, hf, y);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_ds);
@@ -254,23 +287,26 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (ok && NQ > 0) ok = mbar_wait(bar_pair, (NQ - 1) & 1, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
-      // TMEM lanes of the dV / dK accumulators are key rows; chunk warps 0/1
-      // write dV columns 0-31/32-63, warps 2/3 the same of dK
+      // TMEM lanes of the dV / dK accumulators are key rows; half 0 writes
+      // dV, half 1 dK
       tc_fence_after();
       const int kk = ii;
       const size_t krow = (size_t)bh * p.kv_rows + x.phys0 + (kk < x.nvalid ? kk : 0);
-      __nv_bfloat16 *dst = ((ck >> 1) ? p.dk : p.dv) + krow * DH + 32 * (ck & 1);
-      uint32_t g[32];
-      tmem_ld32(trow + ((ck >> 1) ? TM_B : TM_A) + 32 * (ck & 1), g);
-      tmem_wait_ld();
-      if (kk < x.nvalid) {
+      __nv_bfloat16 *dst = (hf ? p.dk : p.dv) + krow * DH;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          ((uint4 *)dst)[e] = make_uint4(
-              pack_bf16(__uint_as_float(g[8 * e + 0]), __uint_as_float(g[8 * e + 1])),
-              pack_bf16(__uint_as_float(g[8 * e + 2]), __uint_as_float(g[8 * e + 3])),
-              pack_bf16(__uint_as_float(g[8 * e + 4]), __uint_as_float(g[8 * e + 5])),
-              pack_bf16(__uint_as_float(g[8 * e + 6]), __uint_as_float(g[8 * e + 7])));
+      for (int c = 0; c < 2; ++c) {
+        uint32_t g[32];
+        tmem_ld32(trow + (hf ? TM_B : TM_A) + 32 * c, g);
+        tmem_wait_ld();
+        if (kk < x.nvalid) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            ((uint4 *)dst)[4 * c + e] = make_uint4(
+                pack_bf16(__uint_as_float(g[8 * e + 0]), __uint_as_float(g[8 * e + 1])),
+                pack_bf16(__uint_as_float(g[8 * e + 2]), __uint_as_float(g[8 * e + 3])),
+                pack_bf16(__uint_as_float(g[8 * e + 4]), __uint_as_float(g[8 * e + 5])),
+                pack_bf16(__uint_as_float(g[8 * e + 6]), __uint_as_float(g[8 * e + 7])));
+        }
       }
     } else {
       atomicExch(&g_bwd_error, 2);
@@ -286,7 +322,7 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
 constexpr uint32_t Q_QU = 0, Q_QV = 16384, Q_DO = 32768, Q_K = 49152, Q_V = 65536;
 constexpr uint32_t Q_R = 81920, Q_DA = 114688, Q_DG = 147456, Q_X = 212992, Q_BAR = 221184;
-constexpr uint32_t Q_SMEM = Q_BAR + 256 + 1024;  // barriers, TMEM slot, flags, [2][16] warp maxima
+constexpr uint32_t Q_SMEM = Q_BAR + 256 + 1024;  // barriers, TMEM slot, flags, [2][8] warp maxima
 
 __global__ void __launch_bounds__(kThreads, 1)
 rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -315,7 +351,7 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     mbar_init(bar_ds, kSoftmaxWarps * 32); mbar_init(bar_dr, 1);
     mbar_init(bar_fl, kSoftmaxWarps * 32); mbar_init(bar_drain, 1);
     mbar_init(bar_red, kSoftmaxWarps);
-    for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 4);
+    for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -391,7 +427,7 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
     __syncwarp();
   } else {
-    const int quad = warp & 3, ck = warp >> 2;  // TMEM lane quadrant, key chunk
+    const int quad = warp & 3, hf = warp >> 2;
     const int ii = quad * 32 + lane;
     const int i = i0 + ii;
     const bool row_ok = i < p.L;
@@ -400,12 +436,7 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const float Di = row_ok ? p.delta[row] : 0.f;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t bar_x = bar_x0 + 8 * quad;
-    volatile float *wmax = (volatile float *)(smem + Q_BAR + 128);  // [2][16]
-    // chunk ck+1 of every row, fp16 and scaled, for the shear of chunk ck:
-    // chunk 1 in the exchange area, chunks 2 and 3 in the V tile (V is dead
-    // once dP has been computed)
-    const uint32_t xnbr = ck == 0 ? sb + Q_X : sb + Q_V + (ck - 1) * 8192;   // chunk ck+1 (read)
-    const uint32_t xown = ck == 1 ? sb + Q_X : sb + Q_V + (ck - 2) * 8192;   // chunk ck (write)
+    volatile float *wmax = (volatile float *)(smem + Q_BAR + 96 + 32);  // [2][8] in the slack
     uint32_t xphase = 0;
     float sig = 1.0e30f;  // fp16 scale of the position products (power of two, non-increasing)
     bool ok = true;
@@ -417,115 +448,105 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       // S and G are done with the bf16 R band and (Q+v): convert them to fp16
       // for the position-gradient products of this tile pair
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        chunk_bf16_to_f16(sb + Q_R + (ck >> 1) * 16384 + sw128_offset(ii, 4 * (ck & 1) + c));
+      for (int c = 0; c < 8; ++c) chunk_bf16_to_f16(sb + Q_R + hf * 16384 + sw128_offset(ii, c));
 #pragma unroll
-      for (int c = 0; c < 2; ++c) chunk_bf16_to_f16(sb + Q_QV + sw128_offset(ii, 2 * ck + c));
-      float y[32];
-      chunk_logits<true>(trow, TM_S, TM_G, quad, lane, ck, i, x, p.scale_log2, y);
+      for (int c = 0; c < 4; ++c) chunk_bf16_to_f16(sb + Q_QV + sw128_offset(ii, 4 * hf + c));
+      float y[64];
+      half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, x, p.scale_log2, y);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
+      for (int k = 0; k < 64; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
       tc_fence_before();
       mbar_arrive(bar_p);
       ok = mbar_wait(bar_dp, t & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      {
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dp[32];
-        tmem_ld32(trow + TM_S + 32 * ck, dp);
+        tmem_ld32(trow + TM_S + 64 * hf + 32 * cc, dp);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          y[k] = y[k] != 0.f ? p.scale * y[k] * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
+        for (int k = 0; k < 32; ++k) {
+          const float pv = y[32 * cc + k];
+          y[32 * cc + k] = pv != 0.f ? p.scale * pv * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
+        }
       }
-      store_chunk_bf16(sb + Q_DA, ii, ck, y);
+      store_half_bf16(sb + Q_DA, ii, hf, y);
       // CTA-wide max |dA| of this tile pair -> power-of-two fp16 scale
       float am = 0.f;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) am = fmaxf(am, fabsf(y[k]));
+      for (int k = 0; k < 64; ++k) am = fmaxf(am, fabsf(y[k]));
       am = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(am)));
       if (lane == 0) {
-        wmax[(t & 1) * 16 + warp] = am;
+        wmax[(t & 1) * 8 + warp] = am;
         mbar_arrive(bar_red);
       }
       ok = mbar_wait(bar_red, t & 1, abort_flag);  // bounded, unlike a named barrier
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       am = 0.f;
 #pragma unroll
-      for (int w = 0; w < kSoftmaxWarps; ++w) am = fmaxf(am, wmax[(t & 1) * 16 + w]);
+      for (int w = 0; w < kSoftmaxWarps; ++w) am = fmaxf(am, wmax[(t & 1) * 8 + w]);
       if (am > 0.f) {
         const float want = exp2f(14.f - ceilf(log2f(am)));  // max |scaled dA| <= 2^14
         if (want < sig) {
           if (t > 0) {
-            // rescale this warp's columns of the fp16-scaled dQ_position accumulator
+            // rescale this half's columns of the fp16-scaled dQ_position accumulator
             const float f = want / sig;
-            uint32_t g[16];
-            tmem_ld16(trow + TM_B + 16 * ck, g);
+            uint32_t g[32];
+            tmem_ld32(trow + TM_B + 32 * hf, g);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) g[e] = __float_as_uint(__uint_as_float(g[e]) * f);
-            tmem_st16(trow + TM_B + 16 * ck, g);
+            for (int e = 0; e < 32; ++e) g[e] = __float_as_uint(__uint_as_float(g[e]) * f);
+            tmem_st32(trow + TM_B + 32 * hf, g);
             tmem_wait_st();
           }
           sig = want;
         }
       }
-      // sheared dG (fp16, scaled by sig). Output chunk D = 3 - ck (columns
-      // 32*(quad+D) ..) needs key chunks ck and ck+1: publish this chunk for
-      // warp ck-1, pick up chunk ck+1 from warp ck+1.
-      if (ck > 0) {
+      // sheared dG (fp16, scaled by sig): half 1 hands keys 64..95 to half 0
+      const uint32_t xrow = sb + Q_X + ii * 64;
+      if (hf == 1) {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          st_shared_v4(xown + ii * 64 + 16 * e, pack_f16(sig * y[8 * e + 0], sig * y[8 * e + 1]),
+          st_shared_v4(xrow + 16 * e, pack_f16(sig * y[8 * e + 0], sig * y[8 * e + 1]),
                        pack_f16(sig * y[8 * e + 2], sig * y[8 * e + 3]),
                        pack_f16(sig * y[8 * e + 4], sig * y[8 * e + 5]),
                        pack_f16(sig * y[8 * e + 6], sig * y[8 * e + 7]));
       }
-      if (!(ok = quad_sync(bar_x, lane, xphase, abort_flag))) break;
-      {
-        // column chunks outside [32*quad, 32*quad + 160) are zero for every
-        // lane: the k-th of those three goes to warp ck = k+1
-        if (ck > 0) {
-          const int k = ck - 1;
-          const int C = k < quad ? k : k + 5;
+      if (!(ok = pair_sync(bar_x, lane, xphase, abort_flag))) break;
+      // column chunks outside [32*quad, 32*quad + 160) are zero for every lane
+      for (int C = 0; C < 8; ++C) {
+        if (hf == 0 ? C < quad : C > quad + 4) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int col = 32 * C + 8 * e;
             st_shared_v4(sb + Q_DG + (col >> 6) * 16384 + sw128_offset(ii, (col & 63) >> 3), 0, 0, 0, 0);
           }
         }
-        // w1[z] = value of key 32*ck + 62 - z: own chunk for z >= 31, chunk
-        // ck+1 (absent for ck = 3) for z <= 30
-        float w1[63];
-        if (ck < 3) {
+      }
+      if (hf == 0) {
+        float xk[32];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint32_t a, b, c, d;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-                         : "r"(xnbr + ii * 64 + 16 * e));
-            const uint32_t w[4] = {a, b, c, d};
+        for (int e = 0; e < 4; ++e) {
+          uint32_t a, b, c, d;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                       : "r"(xrow + 16 * e));
+          const uint32_t w[4] = {a, b, c, d};
 #pragma unroll
-            for (int f = 0; f < 4; ++f) {
-              const float2 fv = __half22float2(*reinterpret_cast<const __half2 *>(&w[f]));
-              // neighbour key 8e+2f (+1) sits at z = 30 - (8e+2f) (-1)
-              if (30 - (8 * e + 2 * f) >= 0) w1[30 - (8 * e + 2 * f)] = fv.x;
-              if (29 - (8 * e + 2 * f) >= 0) w1[29 - (8 * e + 2 * f)] = fv.y;
-            }
+          for (int f = 0; f < 4; ++f) {
+            const __half2 hv = *reinterpret_cast<const __half2 *>(&w[f]);
+            const float2 fv = __half22float2(hv);
+            xk[8 * e + 2 * f] = fv.x;
+            xk[8 * e + 2 * f + 1] = fv.y;
           }
-        } else {
-#pragma unroll
-          for (int z = 0; z <= 30; ++z) w1[z] = 0.f;
         }
-#pragma unroll
-        for (int z = 31; z < 63; ++z) w1[z] = sig * y[62 - z];
-        shear_put(sb + Q_DG, ii, 32 * (quad + 3 - ck), lane, w1);
-        if (ck == 0) {
-          // output chunk D = 4: keys 30 - z of chunk 0 only
-#pragma unroll
-          for (int z = 0; z < 63; ++z) w1[z] = z <= 30 ? sig * y[z <= 30 ? 30 - z : 0] : 0.f;
-          shear_put(sb + Q_DG, ii, 32 * (quad + 4), lane, w1);
-        }
+        shear_chunk_lo<2>(sb + Q_DG, ii, quad, lane, y, xk, sig);
+        shear_chunk_lo<3>(sb + Q_DG, ii, quad, lane, y, xk, sig);
+        shear_chunk_lo<4>(sb + Q_DG, ii, quad, lane, y, xk, sig);
+      } else {
+        shear_chunk_hi<0>(sb + Q_DG, ii, quad, lane, y, sig);
+        shear_chunk_hi<1>(sb + Q_DG, ii, quad, lane, y, sig);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -533,21 +554,23 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       ok = mbar_wait(bar_dr, t & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      // dR rows of this tile pair: TMEM lane = band row; warp ck reads block
-      // ck>>1, columns 32*(ck&1) ..
+      // dR rows of this tile pair: TMEM lane = band row, half hf reads block hf
+      const int d0 = i0 - x.jlog0 - (BK - 1);
       {
-        const int mb = ck >> 1;
-        const int d = i0 - x.jlog0 - (BK - 1) + 128 * mb + ii;
-        float *dst = p.dr + ((size_t)h * p.kv_rows + (d >= 0 ? d : 0)) * DH + 32 * (ck & 1);
+        const int d = d0 + 128 * hf + ii;
+        float *dst = p.dr + ((size_t)h * p.kv_rows + (d >= 0 ? d : 0)) * DH;
         const float f = 1.f / sig;
-        uint32_t g[32];
-        tmem_ld32(trow + TM_G + 64 * mb + 32 * (ck & 1), g);
-        tmem_wait_ld();
-        if (d >= 0 && d < p.m + p.L) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            red_add_v4(dst + 4 * e, f * __uint_as_float(g[4 * e]), f * __uint_as_float(g[4 * e + 1]),
-                       f * __uint_as_float(g[4 * e + 2]), f * __uint_as_float(g[4 * e + 3]));
+        for (int c = 0; c < 2; ++c) {
+          uint32_t g[32];
+          tmem_ld32(trow + TM_G + 64 * hf + 32 * c, g);
+          tmem_wait_ld();
+          if (d >= 0 && d < p.m + p.L) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              red_add_v4(dst + 32 * c + 4 * e, f * __uint_as_float(g[4 * e]), f * __uint_as_float(g[4 * e + 1]),
+                         f * __uint_as_float(g[4 * e + 2]), f * __uint_as_float(g[4 * e + 3]));
+          }
         }
       }
       tc_fence_before();
@@ -557,35 +580,35 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (ok) {
       tc_fence_after();
       // dQ = content + position parts; du, dv partials = column sums of the
-      // parts. This thread owns columns 16*ck .. 16*ck+15 of its row.
+      // parts. This thread owns columns 32*hf .. 32*hf+31 of its row.
       float *red = (float *)(smem + Q_DG);  // [2][128][64] fp32, reuses the dG tile
       uint4 *qrow = (uint4 *)(p.dq + row * DH);
-      uint32_t a[16], b[16];
-      tmem_ld16(trow + TM_A + 16 * ck, a);
-      tmem_ld16(trow + TM_B + 16 * ck, b);
+      uint32_t a[32], b[32];
+      tmem_ld32(trow + TM_A + 32 * hf, a);
+      tmem_ld32(trow + TM_B + 32 * hf, b);
       tmem_wait_ld();
       const float f = sig < 1.0e29f ? 1.f / sig : 0.f;  // undo the fp16 scale
 #pragma unroll
-      for (int e = 0; e < 16; ++e) b[e] = __float_as_uint(__uint_as_float(b[e]) * f);
+      for (int e = 0; e < 32; ++e) b[e] = __float_as_uint(__uint_as_float(b[e]) * f);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        red[ii * 64 + 16 * ck + e] = __uint_as_float(a[e]);
-        red[128 * 64 + ii * 64 + 16 * ck + e] = __uint_as_float(b[e]);
+      for (int e = 0; e < 32; ++e) {
+        red[ii * 64 + 32 * hf + e] = __uint_as_float(a[e]);
+        red[128 * 64 + ii * 64 + 32 * hf + e] = __uint_as_float(b[e]);
       }
       if (row_ok) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
+        for (int e = 0; e < 4; ++e) {
           float s8[8];
 #pragma unroll
           for (int g = 0; g < 8; ++g) s8[g] = __uint_as_float(a[8 * e + g]) + __uint_as_float(b[8 * e + g]);
-          qrow[2 * ck + e] = make_uint4(pack_bf16(s8[0], s8[1]), pack_bf16(s8[2], s8[3]),
+          qrow[4 * hf + e] = make_uint4(pack_bf16(s8[0], s8[1]), pack_bf16(s8[2], s8[3]),
                                         pack_bf16(s8[4], s8[5]), pack_bf16(s8[6], s8[7]));
         }
       }
     } else {
       atomicExch(&g_bwd_error, 8);
     }
-    asm volatile("bar.sync 1, 512;" ::: "memory");  // the softmax warps only
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // the softmax warps only
     if (ok && threadIdx.x < 128) {
       const float *red = (const float *)(smem + Q_DG);
       const int part = threadIdx.x >> 6, col = threadIdx.x & 63;  // (part, column)

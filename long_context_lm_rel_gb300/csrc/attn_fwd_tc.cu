@@ -17,13 +17,12 @@
 //     pad/reshape/slice is an index skew here: S_p[ii][jj] = G[ii][ii-jj+127];
 //     (Q+u) and (Q+v) are stored prescaled by scale*log2(e), so S + S_p is
 //     already the base-2 logit;
-//   * 16 softmax warps, four per TMEM lane quadrant: the thread of (row ii,
-//     chunk c) handles keys 32*c .. 32*c+31 of row ii. It loads S and its
-//     skewed G window, masks, and runs the fp32 online softmax (exp2); the
-//     four chunks of a row exchange their maxima (and at the end their sums)
-//     through shared memory. P goes to shared memory (bf16). The running
-//     maximum used as the exponent reference only moves when the row max
-//     grows by more than 2^8 (then O is rescaled in TMEM), so P <= 256;
+//   * 8 softmax warps, two per TMEM lane quadrant: the thread of (row ii,
+//     half hf) handles keys 64*hf .. 64*hf+63 of row ii. It loads S and its
+//     skewed G window, masks, and runs the fp32 online softmax (exp2); the two
+//     halves of a row exchange their maxima (and at the end their sums)
+//     through shared memory. P goes to shared memory (bf16), O is rescaled in
+//     TMEM;
 //   * tcgen05: O += P V -> TMEM cols [384,448)          (M=128, N=64)
 // Warp 8 is the producer: one thread issues the TMA loads (two stages) and
 // every MMA; tcgen05.commit signals completion through mbarriers.
@@ -50,7 +49,7 @@ using tc::NB;
 using tc::KeyTile;
 using tc::KeyTiles;
 
-constexpr int kSoftmaxWarps = 16;
+constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr uint32_t SM_QU = 0;                  // [128][64] bf16, sw128
@@ -60,9 +59,8 @@ constexpr uint32_t SM_V = 65536;               // 2 stages x 16 KB
 constexpr uint32_t SM_R = 98304;               // 2 stages x 32 KB
 constexpr uint32_t SM_P = 163840;              // 2 x [128][64] bf16 (keys 0-63, 64-127)
 constexpr uint32_t SM_BAR = 196608;            // mbarriers, TMEM slot, abort flag
-constexpr uint32_t SM_X = SM_BAR + 128;        // row exchange: [2][4][128] floats
-constexpr uint32_t SMEM_BYTES = SM_X + 4096 + 1024;  // + alignment slack
-constexpr float kRescaleThreshold = 8.f;       // log2 units
+constexpr uint32_t SM_X = SM_BAR + 128;        // row-half exchange: [2][2][128] floats
+constexpr uint32_t SMEM_BYTES = SM_X + 2048 + 1024;  // + alignment slack
 constexpr uint32_t STAGE_TX = 16384 + 16384 + 32768;
 constexpr uint32_t TM_S = 0, TM_G = 128, TM_O = 384, TM_COLS = 512;
 
@@ -86,6 +84,21 @@ struct Params {
 };
 
 constexpr int kFwd = 0, kPrep = 1;
+
+// Exchange of one float per row between the two warps of a lane quadrant
+// (bounded wait): returns the partner's value.
+__device__ __forceinline__ bool pair_exchange(float mine, float *out, volatile float *xbuf,
+                                              uint32_t bar, int hf, int ii, int lane,
+                                              uint32_t &phase, volatile int *abort_flag) {
+  volatile float *slot = xbuf + (phase & 1) * 256;
+  slot[hf * 128 + ii] = mine;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, phase & 1, abort_flag));
+  ++phase;
+  *out = slot[(1 - hf) * 128 + ii];
+  return ok;
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -115,7 +128,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     mbar_init(bar_p, kSoftmaxWarps * 32);
     mbar_init(bar_pv, 1);
     mbar_init(bar_drain, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 4);
+    for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -129,7 +142,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   } else {
     // (Q+u)*c and (Q+v)*c in bf16, c = scale*log2(e), as 128-byte swizzled
     // K-major tiles; the row's two warps split its 8 chunks.
-    const int quad = warp & 3, ck = warp >> 2;
+    const int quad = warp & 3, hf = warp >> 2;
     const int ii = quad * 32 + lane;
     const int i = i0 + ii;
     const float c2 = p.scale_log2;
@@ -137,8 +150,8 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const uint4 *urow = (const uint4 *)(p.u + (size_t)h * DH);
     const uint4 *vrow = (const uint4 *)(p.vb + (size_t)h * DH);
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = 2 * ck + cc;
+    for (int cc = 0; cc < 4; ++cc) {
+      const int c = 4 * hf + cc;
       uint4 qv4 = i < p.L ? qrow[c] : make_uint4(0, 0, 0, 0);
       const uint4 u4 = urow[c], v4 = vrow[c];
       const uint32_t qw[4] = {qv4.x, qv4.y, qv4.z, qv4.w};
@@ -249,14 +262,13 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __syncwarp();
   } else {
     // ----------------------------------------------------- softmax warps
-    const int quad = warp & 3, ck = warp >> 2;  // TMEM lane quadrant, key chunk
+    const int quad = warp & 3, hf = warp >> 2;
     const int ii = quad * 32 + lane;
     const int i = i0 + ii;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t bar_x = bar_x0 + 8 * quad;
     uint32_t xphase = 0;
-    float m_ref = -INFINITY;  // exponent reference of the row (log2 units)
-    float l_run = 0.f;        // this chunk's part of the row sum
+    float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's part of the row sum
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t & 1;
@@ -266,97 +278,92 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const KeyTile x = tl.get(t);
-      float y[32];
-      tc::chunk_logits<false>(trow, TM_S, TM_G, quad, lane, ck, i, x, 1.f, y);
+      float y[64];
+      tc::half_tile_logits<false>(trow, TM_S, TM_G, quad, lane, hf, i, x, 1.f, y);
       float mt = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) mt = fmaxf(mt, y[k]);
-      float mv[4];
-      if (!(ok = tc::quad_exchange(mt, mv, xbuf, bar_x, ck, ii, lane, xphase, abort_flag))) break;
-      mt = fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3]));
-      // move the reference only when the row max outgrows it by 2^8
-      const bool move = mt > m_ref + kRescaleThreshold;
-      const float m_new = move ? mt : m_ref;
+      for (int k = 0; k < 64; ++k) mt = fmaxf(mt, y[k]);
+      float other;
+      if (!(ok = pair_exchange(mt, &other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
+      const float m_new = fmaxf(m_run, fmaxf(mt, other));
       const float ref = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = move ? ex2(m_ref - ref) : 1.f;  // 0 on the first visible tile
+      const float alpha = ex2(m_run - ref);  // 0 on the first visible tile
       float sum = 0.f;
-      uint32_t pk[16];
+      uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
+      for (int k = 0; k < 64; k += 2) {
         const float p0 = ex2(y[k] - ref), p1 = ex2(y[k + 1] - ref);
         sum += p0 + p1;
         pk[k / 2] = pack_bf16(p0, p1);
       }
       l_run = l_run * alpha + sum;
-      m_ref = m_new;
-      // P (keys 32*ck ..) -> its shared-memory chunks; the previous P.V
-      // finished (bar_sg of this tile was committed after it)
+      m_run = m_new;
+      // P (keys 64*hf ..) -> its shared-memory column block; the previous
+      // P.V finished (bar_sg of this tile was committed after it)
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        st_shared_v4(sbase + SM_P + (ck >> 1) * 16384 + sw128_offset(ii, 4 * (ck & 1) + c), pk[4 * c],
-                     pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(sbase + SM_P + hf * 16384 + sw128_offset(ii, c), pk[4 * c], pk[4 * c + 1],
+                     pk[4 * c + 2], pk[4 * c + 3]);
       // rows of V past the run hold another run's (or junk) data: zero them
       // so that 0 * junk cannot leak into O
       if (ii >= x.nvalid) {
         const uint32_t vrow = sbase + SM_V + s * 16384 + ii * 128;
-        st_shared_v4(vrow + 16 * (2 * ck), 0, 0, 0, 0);
-        st_shared_v4(vrow + 16 * (2 * ck + 1), 0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) st_shared_v4(vrow + 16 * (4 * hf + c), 0, 0, 0, 0);
       }
       if (__any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
-        uint32_t o[16];
-        tmem_ld16(trow + TM_O + 16 * ck, o);
+        uint32_t o[32];
+        tmem_ld32(trow + TM_O + 32 * hf, o);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-        tmem_st16(trow + TM_O + 16 * ck, o);
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st32(trow + TM_O + 32 * hf, o);
         tmem_wait_st();
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_p);
     }
-    // epilogue: O / l, LSE (natural log); this thread owns O columns 16*ck..
+    // epilogue: O / l, LSE (natural log); this thread owns O columns 32*hf..
     if (ok && T > 0) ok = mbar_wait(bar_pv, (T - 1) & 1, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    float lv[4] = {0.f, 0.f, 0.f, 0.f};
-    if (ok) ok = tc::quad_exchange(l_run, lv, xbuf, bar_x, ck, ii, lane, xphase, abort_flag);
+    float l_other = 0.f;
+    if (ok) ok = pair_exchange(l_run, &l_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
     if (ok) {
       tc_fence_after();
-      const float l_all = (lv[0] + lv[1]) + (lv[2] + lv[3]);
-      const float inv = 1.f / l_all;
-      uint32_t o[16];
-      tmem_ld16(trow + TM_O + 16 * ck, o);
+      const float inv = 1.f / (l_run + l_other);
+      uint32_t o[32];
+      tmem_ld32(trow + TM_O + 32 * hf, o);
       tmem_wait_ld();
       if (MODE == kPrep) {
         // D_i = dO_i . O_i with O_i still in fp32
         const uint4 *drow = (const uint4 *)(p.dout + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
         float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint4 d4 = drow[2 * ck + e];
+        for (int e = 0; e < 4; ++e) {
+          const uint4 d4 = drow[4 * hf + e];
           const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
           for (int f = 0; f < 4; ++f)
             acc += __uint_as_float(o[8 * e + 2 * f]) * __uint_as_float(dw[f] << 16) +
                    __uint_as_float(o[8 * e + 2 * f + 1]) * __uint_as_float(dw[f] & 0xFFFF0000u);
         }
-        float av[4];
-        ok = tc::quad_exchange(acc, av, xbuf, bar_x, ck, ii, lane, xphase, abort_flag);
-        if (ok && ck == 0 && i < p.L)
-          p.delta[(size_t)bh * p.L + i] = ((av[0] + av[1]) + (av[2] + av[3])) * inv;
+        float acc_other = 0.f;
+        ok = pair_exchange(acc, &acc_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
+        if (ok && hf == 0 && i < p.L) p.delta[(size_t)bh * p.L + i] = (acc + acc_other) * inv;
       } else {
         uint4 *orow = (uint4 *)(p.o + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
+        for (int e = 0; e < 4; ++e) {
           uint4 v;
           v.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
           v.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
           v.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
           v.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-          if (i < p.L) orow[2 * ck + e] = v;
+          if (i < p.L) orow[4 * hf + e] = v;
         }
-        if (ck == 0 && i < p.L)
-          p.lse[(size_t)bh * p.L + i] = (m_ref + log2f(l_all)) * 0.69314718055994531f;
+        if (hf == 0 && i < p.L)
+          p.lse[(size_t)bh * p.L + i] = (m_run + log2f(l_run + l_other)) * 0.69314718055994531f;
       }
     }
     if (!ok) atomicExch(&g_fwd_error, 1);

@@ -146,60 +146,6 @@ __device__ __forceinline__ void half_tile_logits(uint32_t trow, uint32_t s_col, 
   }
 }
 
-// One-chunk variant for four warps per TMEM lane quadrant: the calling
-// thread (quadrant `quad`, chunk c) produces the logits of keys
-// jj = 32*c + k, k = 0..31, of its row ii = 32*quad + lane.
-template <bool kScaled>
-__device__ __forceinline__ void chunk_logits(uint32_t trow, uint32_t s_col, uint32_t g_col, int quad,
-                                             int lane, int c, int i, const KeyTile &x, float scale,
-                                             float (&y)[32]) {
-  uint32_t sr[32], w0[32], w1[32];
-  tmem_ld32(trow + s_col + 32 * c, sr);
-  const uint32_t gcol = g_col + 32 * quad + 96 - 32 * c;
-  tmem_ld32(trow + gcol, w0);
-  tmem_ld32(trow + gcol + 32, w1);
-  tmem_wait_ld();
-  float win[64];
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    win[e] = __uint_as_float(w0[e]);
-    win[32 + e] = __uint_as_float(w1[e]);
-  }
-#pragma unroll
-  for (int b = 4; b >= 0; --b) {
-    const int sh = 1 << b;
-    const bool take = (lane >> b) & 1;
-#pragma unroll
-    for (int e = 0; e < 63; ++e)
-      if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
-  }
-  // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i
-  const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
-#pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    float a = __uint_as_float(sr[k]) + win[31 - k];
-    if (kScaled) a *= scale;
-    y[k] = k <= lim ? a : -INFINITY;
-  }
-}
-
-// Exchange of one float per row among the four warps of a lane quadrant
-// (bounded mbarrier wait, count 4 lane-0 arrivals). xbuf holds [2][4][128]
-// floats; on return v[w] is the value of the quadrant's warp with chunk w.
-__device__ __forceinline__ bool quad_exchange(float mine, float (&v)[4], volatile float *xbuf,
-                                              uint32_t bar, int c, int ii, int lane,
-                                              uint32_t &phase, volatile int *abort_flag) {
-  volatile float *slot = xbuf + (phase & 1) * 512;
-  slot[c * 128 + ii] = mine;
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, phase & 1, abort_flag));
-  ++phase;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) v[w] = slot[w * 128 + ii];
-  return ok;
-}
-
 // Vector float atomic add (sm_90+): 4 consecutive floats, 16-byte aligned.
 __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
