@@ -21,8 +21,9 @@
 //     half hf) handles keys 64*hf .. 64*hf+63 of row ii. It loads S and its
 //     skewed G window, masks, and runs the fp32 online softmax (exp2); the two
 //     halves of a row exchange their maxima (and at the end their sums)
-//     through shared memory. P goes to shared memory (bf16), O is rescaled in
-//     TMEM;
+//     through shared memory. P goes to shared memory (bf16). The running
+//     maximum used as the exponent reference only moves when the row max
+//     grows by more than 2^8 (then O is rescaled in TMEM), so P <= 256;
 //   * tcgen05: O += P V -> TMEM cols [384,448)          (M=128, N=64)
 // Warp 8 is the producer: one thread issues the TMA loads (two stages) and
 // every MMA; tcgen05.commit signals completion through mbarriers.
@@ -61,6 +62,7 @@ constexpr uint32_t SM_P = 163840;              // 2 x [128][64] bf16 (keys 0-63,
 constexpr uint32_t SM_BAR = 196608;            // mbarriers, TMEM slot, abort flag
 constexpr uint32_t SM_X = SM_BAR + 128;        // row-half exchange: [2][2][128] floats
 constexpr uint32_t SMEM_BYTES = SM_X + 2048 + 1024;  // + alignment slack
+constexpr float kRescaleThreshold = 8.f;       // log2 units
 constexpr uint32_t STAGE_TX = 16384 + 16384 + 32768;
 constexpr uint32_t TM_S = 0, TM_G = 128, TM_O = 384, TM_COLS = 512;
 
@@ -285,9 +287,13 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       for (int k = 0; k < 64; ++k) mt = fmaxf(mt, y[k]);
       float other;
       if (!(ok = pair_exchange(mt, &other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
-      const float m_new = fmaxf(m_run, fmaxf(mt, other));
+      // the exponent reference only moves when the row max outgrows it by
+      // 2^8 (P <= 256 otherwise), which skips most O rescales
+      const float mrow = fmaxf(mt, other);
+      const bool move = mrow > m_run + kRescaleThreshold;
+      const float m_new = move ? mrow : m_run;
       const float ref = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ex2(m_run - ref);  // 0 on the first visible tile
+      const float alpha = move ? ex2(m_run - ref) : 1.f;  // 0 on the first visible tile
       float sum = 0.f;
       uint32_t pk[32];
 #pragma unroll
