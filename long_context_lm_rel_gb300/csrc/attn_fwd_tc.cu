@@ -5,32 +5,32 @@
 //   A_ij = (q_i+u).k_j + (q_i+v).r_{i-j},  O_i = softmax_j(scale*A_ij | allow) V
 // The L x (m+L) score matrix never leaves the SM.
 //
-// One CTA owns (b, h, 128 query rows) and walks the visible keys in tiles of
-// 64 physically contiguous K/V rows (the ring's two runs and the current
-// block; a tile never straddles the ring's wrap). Tile t with first logical
-// key j0 needs the R band of distances d0 .. d0+190, d0 = i0 - j0 - 63, held
-// in TMEM as three 64-column chunks of G = (Q+v) R_band^T. The next tile of
-// the same run (j0 + 64) needs d0-64 .. d0+126: two of those chunks again.
-// So G lives in a ring of four 64-column TMEM slots and each such tile costs
-// one new N=64 position MMA (no band waste); a tile that starts a new run
-// recomputes all three chunks.
-//   * TMA loads K, V (64 x 64) and the new R chunk(s) (64 x 64 each);
-//   * tcgen05: S = (Q+u) K^T into one of two 64-column S slots, the new G
-//     chunk(s) into the ring, O += P V (M=128, N=64, K=64) into 64 O columns;
-//   * the relative shift the pages do by pad/reshape/slice is an index skew:
-//     S_p[ii][jj] = G[ii][ii - jj + 63] (band-relative column);
-//   * (Q+u) and (Q+v) are stored prescaled by scale*log2(e);
+// One CTA owns (b, h, 128 query rows). It walks the visible keys in tiles of
+// 128 physically contiguous K/V rows (the ring's two runs and the current
+// block; a tile never straddles the ring's wrap). For every key tile:
+//   * TMA loads K, V (128 x 64) and the band of 256 R rows the tile needs:
+//     distances d0 .. d0+255 with d0 = i0 - j0 - 127 (rows outside R read as
+//     zero and are masked anyway);
+//   * tcgen05: S = (Q+u) K^T   -> TMEM cols [0,128)     (M=128, N=128)
+//              G = (Q+v) Rb^T  -> TMEM cols [128,384)   (M=128, N=256)
+//     so G[ii][t] = (q_ii+v).r_{d0+t}; the relative shift the pages do by
+//     pad/reshape/slice is an index skew here: S_p[ii][jj] = G[ii][ii-jj+127];
+//     (Q+u) and (Q+v) are stored prescaled by scale*log2(e), so S + S_p is
+//     already the base-2 logit;
 //   * 8 softmax warps, two per TMEM lane quadrant: the thread of (row ii,
-//     half hf) handles keys 32*hf .. 32*hf+31 of row ii: S, its skewed
-//     64-column G window (5-stage barrel shift by the lane), mask, fp32
-//     softmax with exp2. The two halves exchange the row maximum; the
-//     exponent reference only moves when the row max grows by more than 2^8
-//     (then O is rescaled in TMEM), so P <= 256. P goes to one of two shared
-//     buffers.
-// With two S slots, two P buffers and the G ring, the producer issues the
-// MMAs of tile t+1 while the softmax warps work on tile t. Every mbarrier a
-// side waits on is duplicated per tile parity, so no waiter can fall two
-// phases behind. Warp 8 is the producer (one thread: TMA and every MMA).
+//     half hf) handles keys 64*hf .. 64*hf+63 of row ii. It loads S and its
+//     skewed G window, masks, and runs the fp32 online softmax (exp2); the two
+//     halves of a row exchange their maxima (and at the end their sums)
+//     through shared memory. P goes to shared memory (bf16). The running
+//     maximum used as the exponent reference only moves when the row max
+//     grows by more than 2^8 (then O is rescaled in TMEM), so P <= 256;
+//   * tcgen05: O += P V -> TMEM cols [384,448)          (M=128, N=64)
+// Warp 8 is the producer: one thread issues the TMA loads (two stages) and
+// every MMA; tcgen05.commit signals completion through mbarriers.
+//
+// The skew: thread of row ii = 32*quad + lane needs G columns ii..ii+127. Per
+// chunk of 32 keys it loads a warp-uniform 64-column window and shifts it by
+// its lane with a 5-stage predicated barrel shift.
 #include <math.h>
 #include <stdio.h>
 
@@ -44,27 +44,30 @@ namespace {
 
 using namespace sm103;
 using tc::BQ;
+using tc::BK;
 using tc::DH;
+using tc::NB;
 using tc::KeyTile;
+using tc::KeyTiles;
 
-constexpr int FK = 64;                         // keys per tile
-using FwdTiles = tc::KeyTilesW<FK>;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr uint32_t SM_QU = 0;                  // [128][64] bf16, sw128
 constexpr uint32_t SM_QV = 16384;
-constexpr uint32_t SM_K = 32768;               // 2 stages x [64][64] (8 KB)
-constexpr uint32_t SM_V = 49152;               // 2 stages x 8 KB
-constexpr uint32_t SM_R = 65536;               // 2 stages x 3 chunks x 8 KB
-constexpr uint32_t SM_P = 114688;              // 2 x [128][64] bf16
-constexpr uint32_t SM_BAR = 147456;            // mbarriers, TMEM slot, abort flag
-constexpr uint32_t SM_X = SM_BAR + 256;        // row-half exchange: [2][2][128] floats
+constexpr uint32_t SM_K = 32768;               // 2 stages x 16 KB
+constexpr uint32_t SM_V = 65536;               // 2 stages x 16 KB
+constexpr uint32_t SM_R = 98304;               // 2 stages x 32 KB
+constexpr uint32_t SM_P = 163840;              // 2 x [128][64] bf16 (keys 0-63, 64-127)
+constexpr uint32_t SM_BAR = 196608;            // mbarriers, TMEM slot, abort flag
+constexpr uint32_t SM_X = SM_BAR + 128;        // row-half exchange: [2][2][128] floats
 constexpr uint32_t SMEM_BYTES = SM_X + 2048 + 1024;  // + alignment slack
 constexpr float kRescaleThreshold = 8.f;       // log2 units
-constexpr uint32_t TM_S = 0, TM_G = 128, TM_O = 384, TM_COLS = 512;  // S: 2 x 64, G: 4 x 64
+constexpr uint32_t STAGE_TX = 16384 + 16384 + 32768;
+constexpr uint32_t TM_S = 0, TM_G = 128, TM_O = 384, TM_COLS = 512;
 
-constexpr uint32_t IDESC_64 = idesc_bf16(128, 64, false, false);
+constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+constexpr uint32_t IDESC_G = idesc_bf16(128, 256, false, false);
 constexpr uint32_t IDESC_O = idesc_bf16(128, 64, false, true);   // V is MN-major (d contiguous)
 
 __device__ int g_fwd_error;
@@ -99,13 +102,6 @@ __device__ __forceinline__ bool pair_exchange(float mine, float *out, volatile f
   return ok;
 }
 
-// Tile t continues the run of tile t-1 (its band shares two chunks).
-__device__ __forceinline__ bool adjacent(const FwdTiles &tl, int t) {
-  if (t == 0) return false;
-  const KeyTile a = tl.get(t - 1), b = tl.get(t);
-  return a.nvalid == FK && b.jlog0 == a.jlog0 + FK;
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -119,25 +115,20 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   const int h = bh % p.H;
   const int i0 = qt * BQ;
 
-  // barriers: full[2] (TMA), sg[2] (S/G MMAs), pr[2] (softmax done with a
-  // tile), pv[2] (P.V done), drain, exchange[4]
-  const uint32_t bar0 = sbase + SM_BAR;
-  auto bar_full = [&](int s) { return bar0 + 8 * s; };
-  auto bar_sg = [&](int s) { return bar0 + 16 + 8 * s; };
-  auto bar_pr = [&](int s) { return bar0 + 32 + 8 * s; };
-  auto bar_pv = [&](int s) { return bar0 + 48 + 8 * s; };
-  const uint32_t bar_drain = bar0 + 64, bar_x0 = bar0 + 72;
-  uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 104);
-  volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 108);
+  const uint32_t bar_full0 = sbase + SM_BAR, bar_full1 = bar_full0 + 8;
+  const uint32_t bar_sg = bar_full0 + 16, bar_p = bar_full0 + 24, bar_pv = bar_full0 + 32;
+  const uint32_t bar_drain = bar_full0 + 40;
+  uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 48);
+  volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 56);
+  const uint32_t bar_x0 = bar_full0 + 64;  // 4 quadrant exchange barriers
   volatile float *xbuf = (volatile float *)(smem + SM_X);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_full(s), 1);
-      mbar_init(bar_sg(s), 1);
-      mbar_init(bar_pr(s), kSoftmaxWarps * 32);
-      mbar_init(bar_pv(s), 1);
-    }
+    mbar_init(bar_full0, 1);
+    mbar_init(bar_full1, 1);
+    mbar_init(bar_sg, 1);
+    mbar_init(bar_p, kSoftmaxWarps * 32);
+    mbar_init(bar_pv, 1);
     mbar_init(bar_drain, 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     *abort_flag = 0;
@@ -194,77 +185,68 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const FwdTiles tl(p.m, p.cap, p.head, min(i0 + BQ, p.L));
+  const KeyTiles tl(p.m, p.cap, p.head, min(i0 + BQ, p.L));
   const int T = tl.count();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------ producer / MMA issuer
     if (lane == 0) {
-      int nissued[2] = {0, 0};
       bool pending[2] = {false, false};
+      int nissued[2] = {0, 0};
       auto issue_tma = [&](int t) {
         const int s = t & 1;
         const KeyTile x = tl.get(t);
-        const bool adj = adjacent(tl, t);
-        const uint32_t bar = bar_full(s);
-        mbar_expect_tx(bar, (adj ? 3 : 5) * 8192);
-        tma_load_3d(sbase + SM_K + s * 8192, &tm_k, 0, x.phys0, bh, bar);
-        tma_load_3d(sbase + SM_V + s * 8192, &tm_v, 0, x.phys0, bh, bar);
-        const int d0 = i0 - x.jlog0 - (FK - 1);
-        for (int c = 0; c < (adj ? 1 : 3); ++c)
-          tma_load_3d(sbase + SM_R + s * 24576 + c * 8192, &tm_r, 0, d0 + 64 * c, h, bar);
+        const uint32_t bar = s ? bar_full1 : bar_full0;
+        mbar_expect_tx(bar, STAGE_TX);
+        tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, bh, bar);
+        tma_load_3d(sbase + SM_V + s * 16384, &tm_v, 0, x.phys0, bh, bar);
+        tma_load_3d(sbase + SM_R + s * 32768, &tm_r, 0, i0 - x.jlog0 - (BK - 1), h, bar);
         pending[s] = true;
         ++nissued[s];
       };
-      int base = 0;  // ring slot of chunk 0 of the current tile's band
       auto issue_sg = [&](int t) {
         const int s = t & 1;
-        const bool adj = adjacent(tl, t);
-        if (t > 0) base = (base + 3) & 3;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_S + 64 * s, sdesc_sw128(sbase + SM_QU + k * 32, 16, 1024),
-                   sdesc_sw128(sbase + SM_K + s * 8192 + k * 32, 16, 1024), IDESC_64, k > 0);
-        for (int c = 0; c < (adj ? 1 : 3); ++c)
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t a = sdesc_sw128(sbase + SM_QU + k * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(sbase + SM_K + s * 16384 + k * 32, 16, 1024);
+          mma_bf16(tmem + TM_S, a, b, IDESC_S, k > 0);
+        }
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + TM_G + 64 * ((base + c) & 3), sdesc_sw128(sbase + SM_QV + k * 32, 16, 1024),
-                     sdesc_sw128(sbase + SM_R + s * 24576 + c * 8192 + k * 32, 16, 1024), IDESC_64, k > 0);
-        mma_commit(bar_sg(s));
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t a = sdesc_sw128(sbase + SM_QV + k * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(sbase + SM_R + s * 32768 + k * 32, 16, 1024);
+          mma_bf16(tmem + TM_G, a, b, IDESC_G, k > 0);
+        }
+        mma_commit(bar_sg);
       };
       bool ok = true;
-      issue_tma(0);
+      if (T > 0) issue_tma(0);
       if (T > 1) issue_tma(1);
-      ok = mbar_wait(bar_full(0), 0, abort_flag);
-      pending[0] = false;
-      if (ok) issue_sg(0);
+      if (T > 0) {
+        ok = mbar_wait(bar_full0, 0, abort_flag);
+        pending[0] = false;
+        if (ok) issue_sg(0);
+      }
       for (int t = 0; ok && t < T; ++t) {
+        if (!(ok = mbar_wait(bar_p, t & 1, abort_flag))) break;
+        tc_fence_after();
         const int s = t & 1;
-        bool waited_pr = false;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = sdesc_sw128(sbase + SM_P + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(sbase + SM_V + s * 16384 + k * 2048, 16, 1024);
+          mma_bf16(tmem + TM_O, a, b, IDESC_O, (t > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(bar_pv);
         if (t + 1 < T) {
           const int s1 = (t + 1) & 1;
-          if (!(ok = mbar_wait(bar_full(s1), ((t + 1) >> 1) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(s1 ? bar_full1 : bar_full0, ((t + 1) >> 1) & 1, abort_flag))) break;
           pending[s1] = false;
-          // an adjacent tile only overwrites the S slot and ring slot tile
-          // t-1 used (its softmax finished before P.V(t-1) was issued); a
-          // new run needs all three chunk slots, i.e. tile t's softmax done
-          if (!adjacent(tl, t + 1)) {
-            if (!(ok = mbar_wait(bar_pr(s), (t >> 1) & 1, abort_flag))) break;
-            waited_pr = true;
-          }
           issue_sg(t + 1);
         }
-        if (!waited_pr && !(ok = mbar_wait(bar_pr(s), (t >> 1) & 1, abort_flag))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_O, sdesc_sw128(sbase + SM_P + s * 16384 + k * 32, 16, 1024),
-                   sdesc_sw128(sbase + SM_V + s * 8192 + k * 2048, 16, 1024), IDESC_O,
-                   (t > 0 || k > 0) ? 1u : 0u);
-        mma_commit(bar_pv(s));
         if (t + 2 < T) {
-          // stage s is free once P.V(t) (and with it S/G(t)) completed
-          if (!(ok = mbar_wait(bar_pv(s), (t >> 1) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(bar_pv, t & 1, abort_flag))) break;
           issue_tma(t + 2);
         }
       }
@@ -273,7 +255,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // shared memory are released
         volatile int no_abort = 0;
         for (int s = 0; s < 2; ++s)
-          if (pending[s]) mbar_wait(bar_full(s), (nissued[s] - 1) & 1, &no_abort);
+          if (pending[s]) mbar_wait(s ? bar_full1 : bar_full0, (nissued[s] - 1) & 1, &no_abort);
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0, &no_abort);
         atomicExch(&g_fwd_error, 1);
@@ -289,88 +271,53 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const uint32_t bar_x = bar_x0 + 8 * quad;
     uint32_t xphase = 0;
     float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's part of the row sum
-    int base = 0;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t & 1;
-      if (t > 0) base = (base + 3) & 3;
-      ok = mbar_wait(bar_sg(s), (t >> 1) & 1, abort_flag) &&
-           mbar_wait(bar_full(s), (t >> 1) & 1, abort_flag);
-      // P buffer s was last read by P.V(t-2)
-      if (ok && t >= 2) ok = mbar_wait(bar_pv(s), ((t - 2) >> 1) & 1, abort_flag);
+      ok = mbar_wait(bar_sg, t & 1, abort_flag) &&
+           mbar_wait(s ? bar_full1 : bar_full0, (t >> 1) & 1, abort_flag);
       // tcgen05.ld/st below are warp-collective: keep every decision warp-uniform
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const KeyTile x = tl.get(t);
-      float y[32];
-      {
-        uint32_t sr[32], w0[32], w1[32];
-        tmem_ld32(trow + TM_S + 64 * s + 32 * hf, sr);
-        const int a0 = 32 * quad + 32 - 32 * hf;  // band column of the window
-        tmem_ld32(trow + TM_G + 64 * ((base + (a0 >> 6)) & 3) + (a0 & 63), w0);
-        const int a1 = a0 + 32;
-        tmem_ld32(trow + TM_G + 64 * ((base + (a1 >> 6)) & 3) + (a1 & 63), w1);
-        tmem_wait_ld();
-        float win[64];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          win[e] = __uint_as_float(w0[e]);
-          win[32 + e] = __uint_as_float(w1[e]);
-        }
-        // win[x] <- win[x + lane]
-#pragma unroll
-        for (int b = 4; b >= 0; --b) {
-          const int sh = 1 << b;
-          const bool take = (lane >> b) & 1;
-#pragma unroll
-          for (int e = 0; e < 63; ++e)
-            if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
-        }
-        // key jj = 32*hf + k is visible iff jj < nvalid and jlog0 + jj <= i
-        const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * hf;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float a = __uint_as_float(sr[k]) + win[31 - k];
-          y[k] = k <= lim ? a : -INFINITY;
-        }
-      }
+      float y[64];
+      tc::half_tile_logits<false>(trow, TM_S, TM_G, quad, lane, hf, i, x, 1.f, y);
       float mt = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) mt = fmaxf(mt, y[k]);
+      for (int k = 0; k < 64; ++k) mt = fmaxf(mt, y[k]);
       float other;
       if (!(ok = pair_exchange(mt, &other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
-      // the exponent reference only moves when the row max outgrows it by 2^8
+      // the exponent reference only moves when the row max outgrows it by
+      // 2^8 (P <= 256 otherwise), which skips most O rescales
       const float mrow = fmaxf(mt, other);
       const bool move = mrow > m_run + kRescaleThreshold;
       const float m_new = move ? mrow : m_run;
       const float ref = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = move ? ex2(m_run - ref) : 1.f;  // 0 on the first visible tile
       float sum = 0.f;
-      uint32_t pk[16];
+      uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
+      for (int k = 0; k < 64; k += 2) {
         const float p0 = ex2(y[k] - ref), p1 = ex2(y[k + 1] - ref);
         sum += p0 + p1;
         pk[k / 2] = pack_bf16(p0, p1);
       }
       l_run = l_run * alpha + sum;
       m_run = m_new;
+      // P (keys 64*hf ..) -> its shared-memory column block; the previous
+      // P.V finished (bar_sg of this tile was committed after it)
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        st_shared_v4(sbase + SM_P + s * 16384 + sw128_offset(ii, 4 * hf + c), pk[4 * c], pk[4 * c + 1],
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(sbase + SM_P + hf * 16384 + sw128_offset(ii, c), pk[4 * c], pk[4 * c + 1],
                      pk[4 * c + 2], pk[4 * c + 3]);
       // rows of V past the run hold another run's (or junk) data: zero them
       // so that 0 * junk cannot leak into O
-      if (ii < FK && ii >= x.nvalid) {
-        const uint32_t vrow = sbase + SM_V + s * 8192 + ii * 128;
+      if (ii >= x.nvalid) {
+        const uint32_t vrow = sbase + SM_V + s * 16384 + ii * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) st_shared_v4(vrow + 16 * (4 * hf + c), 0, 0, 0, 0);
       }
       if (__any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
-        // O holds P.V up to tile t-1: wait for it, then rescale this half's columns
-        const bool okw = mbar_wait(bar_pv((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag);
-        if (!(ok = __all_sync(0xffffffffu, okw))) break;
-        tc_fence_after();
         uint32_t o[32];
         tmem_ld32(trow + TM_O + 32 * hf, o);
         tmem_wait_ld();
@@ -381,10 +328,10 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar_pr(s));
+      mbar_arrive(bar_p);
     }
     // epilogue: O / l, LSE (natural log); this thread owns O columns 32*hf..
-    if (ok && T > 0) ok = mbar_wait(bar_pv((T - 1) & 1), ((T - 1) >> 1) & 1, abort_flag);
+    if (ok && T > 0) ok = mbar_wait(bar_pv, (T - 1) & 1, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     float l_other = 0.f;
     if (ok) ok = pair_exchange(l_run, &l_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
@@ -473,8 +420,8 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
                         const void *dout, float *delta, void *qu_out, void *qv_out,
                         cudaStream_t st, int *launches) {
   CUtensorMap tk, tv, tr;
-  if (!make_map(&tk, k, s.B * s.H, s.kv_rows, FK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, FK) ||
-      !make_map(&tr, r, s.H, s.kv_rows, 64))
+  if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
+      !make_map(&tr, r, s.H, s.kv_rows, NB))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;

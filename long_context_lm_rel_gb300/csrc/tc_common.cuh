@@ -22,43 +22,41 @@ struct KeyTile {
   int nvalid;  // rows of the tile that belong to this run
 };
 
-// Key tiles of W rows over ring run A (head .. cap), ring run B (0 .. ), then
-// the current rows 0 .. lenC. A tile never straddles the ring's wrap, so its
+// Key tiles over ring run A (head .. cap), ring run B (0 .. ), then the
+// current rows 0 .. lenC. A tile never straddles the ring's wrap, so its
 // rows are consecutive logical keys and one R band serves the whole tile.
-template <int W>
-struct KeyTilesW {
+struct KeyTiles {
   int m, cap, head, lenA, lenB, lenC, nA, nB, nC;
-  __device__ KeyTilesW(int m_, int cap_, int head_, int lenC_) {
+  __device__ KeyTiles(int m_, int cap_, int head_, int lenC_) {
     m = m_; cap = cap_; head = head_;
     lenA = min(m, cap - head);
     lenB = m - lenA;
     lenC = lenC_;
-    nA = (lenA + W - 1) / W;
-    nB = (lenB + W - 1) / W;
-    nC = (lenC + W - 1) / W;
+    nA = (lenA + BK - 1) / BK;
+    nB = (lenB + BK - 1) / BK;
+    nC = (lenC + BK - 1) / BK;
   }
   __device__ int count() const { return nA + nB + nC; }
   __device__ KeyTile get(int t) const {
     KeyTile x;
     if (t < nA) {
-      x.phys0 = head + t * W;
-      x.jlog0 = -m + t * W;
-      x.nvalid = min(W, lenA - t * W);
+      x.phys0 = head + t * BK;
+      x.jlog0 = -m + t * BK;
+      x.nvalid = min(BK, lenA - t * BK);
     } else if (t < nA + nB) {
       const int u = t - nA;
-      x.phys0 = u * W;
-      x.jlog0 = -m + lenA + u * W;
-      x.nvalid = min(W, lenB - u * W);
+      x.phys0 = u * BK;
+      x.jlog0 = -m + lenA + u * BK;
+      x.nvalid = min(BK, lenB - u * BK);
     } else {
       const int u = t - nA - nB;
-      x.phys0 = cap + u * W;
-      x.jlog0 = u * W;
-      x.nvalid = min(W, lenC - u * W);
+      x.phys0 = cap + u * BK;
+      x.jlog0 = u * BK;
+      x.nvalid = min(BK, lenC - u * BK);
     }
     return x;
   }
 };
-using KeyTiles = KeyTilesW<BK>;
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
