@@ -274,6 +274,12 @@ def run_ours(args, rank, world):
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
     }
+    if world == 1 and not args.no_stream:
+        stream, mu = stream_cfg5()
+        _, hbm, kind = peaks()
+        mu.update({"peak": hbm, "frac": mu["achieved"] / hbm, "peak_kind": f"{kind} copy"})
+        out["stream_cfg5"] = stream
+        out["mem_update_roofline"] = mu
     if world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         dt, fl = cpu_sample(x, (0, 4), nthreads)
@@ -283,6 +289,70 @@ def run_ours(args, rank, world):
     print(json.dumps(out), flush=True)
 
 
+def stream_cfg5(segments=32, layers=16, reps_update=200):
+    """The 16-layer evaluation stream (B4 H16 L128 M1600, fwd + ring update per
+    layer and segment, memory empty at the start) and the memory-update kernel
+    alone. Inputs: seeded device normals (timing only; parity is in tests)."""
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    B5, H5, L5, M5 = 4, 16, 128, 1600
+    kv = M5 + L5
+    g = torch.Generator(device="cuda").manual_seed(5)
+    bf = torch.bfloat16
+    mk = lambda *s, std=0.125: (torch.randn(*s, generator=g, device="cuda") * std).to(bf)
+    K = [mk(B5, H5, kv, DH) for _ in range(layers)]
+    V = [mk(B5, H5, kv, DH) for _ in range(layers)]
+    R = [mk(H5, kv, DH, std=0.7) for _ in range(layers)]
+    U = [mk(H5, DH, std=0.02) for _ in range(layers)]
+    VB = [mk(H5, DH, std=0.02) for _ in range(layers)]
+    Q = mk(B5, H5, L5, DH)
+    o = torch.empty(B5, H5, L5, DH, device="cuda", dtype=bf)
+    lse = torch.empty(B5, H5, L5, device="cuda", dtype=torch.float32)
+    cur = mk(B5, H5, L5, DH)
+    rings = [[rxl.rxl_ring(t.data_ptr(), B5 * H5, M5, DH, kv * DH, rxl.RXL_DTYPE_BF16, 0, 0) for t in (K[n], V[n])]
+             for n in range(layers)]
+    st = torch.cuda.current_stream()
+    launches = 0
+    pairs = 0
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for seg in range(segments):
+        for n in range(layers):
+            rk, rv = rings[n]
+            K[n][:, :, M5:].copy_(cur)
+            V[n][:, :, M5:].copy_(cur)
+            m = rk.len
+            pairs += B5 * H5 * (L5 * m + L5 * (L5 + 1) // 2)
+            d = rxl.make_desc(B5, H5, L5, M5, m, rk.head, SCALE, rxl.RXL_DTYPE_BF16)
+            rxl.rxl_attn_fwd(d, Q, K[n], V[n], R[n], U[n], VB[n], o, lse, st)
+            launches += rxl.rxl_last_launch_count()
+            for r_, t in ((rk, K[n]), (rv, V[n])):
+                rxl.rxl_mem_update(r_, t.data_ptr() + M5 * DH * 2, kv * DH, L5, st)
+                launches += rxl.rxl_last_launch_count()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    # the memory update alone: back-to-back calls on a full ring
+    rk = rxl.rxl_ring(K[0].data_ptr(), B5 * H5, M5, DH, kv * DH, rxl.RXL_DTYPE_BF16, 0, M5)
+    for _ in range(10):
+        rxl.rxl_mem_update(rk, K[0].data_ptr() + M5 * DH * 2, kv * DH, L5, st)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(reps_update):
+        rxl.rxl_mem_update(rk, K[0].data_ptr() + M5 * DH * 2, kv * DH, L5, st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / reps_update
+    bytes_call = 2 * B5 * H5 * min(L5, M5) * DH * 2   # read + write of the appended rows
+    return {"workload": "cfg5_bf16_B4H16_L128M1600_16layer_32seg_fwd", "segments": segments, "layers": layers,
+            "ms": ms, "tokens_per_s": B5 * L5 * segments / (ms * 1e-3),
+            "attn_tflops": pairs * FLOP_FWD_PAIR / (ms * 1e-3) / 1e12, "gpu_launches": launches,
+            "note": "per segment and layer: K/V current rows copied in (torch), rxl_attn_fwd, 2 x rxl_mem_update"}, \
+           {"kernel": "mem_update_kernel", "bound": "hbm", "unit": "GB/s", "us_per_call": us,
+            "bytes_per_call": bytes_call, "achieved": bytes_call / (us * 1e-6) / 1e9}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -290,6 +360,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stream", action="store_true", help="skip the cfg5 stream / memory-update timing")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
