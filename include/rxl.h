@@ -155,6 +155,27 @@ rxl_status rxl_attn_bwd_noalloc(const rxl_attn_desc *desc, const void *q, const 
 size_t rxl_attn_bwd_noalloc_max_scratch_bytes(void);
 
 /*
+ * Training pair: the same forward and backward, with one more output of the
+ * forward that the backward consumes. o_lo [B,H,L,dh] (bf16 only; NULL for
+ * f32, where O is exact) receives O - o, i.e. what rounding O to bf16
+ * dropped, itself rounded to bf16. With it the backward takes
+ * D_i = dout_i . (o_i + o_lo_i) from a streaming pass; with o_lo == NULL
+ * (also what rxl_attn_fwd / rxl_attn_bwd do) the backward recomputes the
+ * forward to obtain D from the unrounded O. D enters every dA_ij of the row,
+ * so it must be more accurate than a bf16 O. Other arguments, outputs and
+ * checks as in rxl_attn_fwd / rxl_attn_bwd.
+ */
+rxl_status rxl_attn_fwd_ex(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                           const void *r, const void *u, const void *vbias, void *o, void *o_lo,
+                           float *lse, rxl_stream_t stream);
+
+rxl_status rxl_attn_bwd_ex(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                           const void *r, const void *u, const void *vbias, const void *o,
+                           const void *o_lo, const float *lse, const void *dout, void *dq,
+                           void *dk, void *dv, float *dr, float *du, float *dvbias,
+                           void *workspace, size_t workspace_bytes, rxl_stream_t stream);
+
+/*
  * FIFO memory ring (eq. Tail_M; update_mems with mem_len == cap).
  *   data         device pointer to plane 0, row 0
  *   planes       independent rings (e.g. B*H), >= 1

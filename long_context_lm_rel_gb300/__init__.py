@@ -72,6 +72,10 @@ def lib():
             L.rxl_last_launch_count.restype = ctypes.c_int
             L.rxl_device_error_flags.argtypes = []
             L.rxl_device_error_flags.restype = ctypes.c_int
+            L.rxl_attn_fwd_ex.argtypes = [P(rxl_attn_desc)] + [vp] * 9 + [vp]
+            L.rxl_attn_fwd_ex.restype = ctypes.c_int
+            L.rxl_attn_bwd_ex.argtypes = [P(rxl_attn_desc)] + [vp] * 17 + [ctypes.c_size_t, vp]
+            L.rxl_attn_bwd_ex.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc.argtypes = [P(rxl_attn_desc)] + [vp] * 15 + [vp]
             L.rxl_attn_bwd_noalloc.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc_max_scratch_bytes.argtypes = []
@@ -109,6 +113,19 @@ def make_desc(B, H, L, mem_cap, mem_len, mem_head=0, scale=0.125, dtype=RXL_DTYP
 def rxl_attn_fwd(desc, q, k, v, r, u, vbias, o, lse, stream=None):
     _check(lib().rxl_attn_fwd(ctypes.byref(desc), *map(_ptr, (q, k, v, r, u, vbias, o, lse)),
                               _stream(stream)), "rxl_attn_fwd")
+
+
+def rxl_attn_fwd_ex(desc, q, k, v, r, u, vbias, o, o_lo, lse, stream=None):
+    _check(lib().rxl_attn_fwd_ex(ctypes.byref(desc), *map(_ptr, (q, k, v, r, u, vbias, o, o_lo, lse)),
+                                 _stream(stream)), "rxl_attn_fwd_ex")
+
+
+def rxl_attn_bwd_ex(desc, q, k, v, r, u, vbias, o, o_lo, lse, dout, dq, dk, dv, dr, du, dvbias,
+                    workspace, workspace_bytes, stream=None):
+    _check(lib().rxl_attn_bwd_ex(ctypes.byref(desc),
+                                 *map(_ptr, (q, k, v, r, u, vbias, o, o_lo, lse, dout, dq, dk, dv, dr,
+                                             du, dvbias, workspace)),
+                                 int(workspace_bytes), _stream(stream)), "rxl_attn_bwd_ex")
 
 
 def rxl_attn_bwd_workspace_bytes(desc) -> int:

@@ -645,6 +645,47 @@ __global__ void bwd_zero_kernel(float *dr, size_t n_dr, __nv_bfloat16 *dk, __nv_
   }
 }
 
+// Streaming preparation when the forward kept the low part of O: per row,
+// (Q+u) and (Q+v) in bf16 and D_i = dO_i . (o_i + o_lo_i). Eight threads
+// per row, 16 bytes each.
+__global__ void __launch_bounds__(256) bwd_light_prep_kernel(
+    long long rows, int L, int H, const __nv_bfloat16 *__restrict__ q,
+    const __nv_bfloat16 *__restrict__ u, const __nv_bfloat16 *__restrict__ vb,
+    const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ o_lo,
+    const __nv_bfloat16 *__restrict__ dout, __nv_bfloat16 *__restrict__ qu,
+    __nv_bfloat16 *__restrict__ qv, float *__restrict__ delta) {
+  const int sub = threadIdx.x & 7;
+  for (long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 3; row < rows;
+       row += ((long long)gridDim.x * blockDim.x) >> 3) {
+    const int h = (int)((row / L) % H);
+    const size_t off = (size_t)row * DH;
+    const uint4 q4 = ((const uint4 *)(q + off))[sub];
+    const uint4 u4 = ((const uint4 *)(u + (size_t)h * DH))[sub];
+    const uint4 v4 = ((const uint4 *)(vb + (size_t)h * DH))[sub];
+    const uint4 o4 = ((const uint4 *)(o + off))[sub];
+    const uint4 l4 = ((const uint4 *)(o_lo + off))[sub];
+    const uint4 d4 = ((const uint4 *)(dout + off))[sub];
+    const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
+    const uint32_t vw[4] = {v4.x, v4.y, v4.z, v4.w}, ow[4] = {o4.x, o4.y, o4.z, o4.w};
+    const uint32_t lw[4] = {l4.x, l4.y, l4.z, l4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
+    auto lo = [](uint32_t x) { return __uint_as_float(x << 16); };
+    auto hi = [](uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); };
+    uint32_t a[4], b[4];
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      a[e] = pack_bf16(lo(qw[e]) + lo(uw[e]), hi(qw[e]) + hi(uw[e]));
+      b[e] = pack_bf16(lo(qw[e]) + lo(vw[e]), hi(qw[e]) + hi(vw[e]));
+      acc += lo(dw[e]) * (lo(ow[e]) + lo(lw[e])) + hi(dw[e]) * (hi(ow[e]) + hi(lw[e]));
+    }
+    ((uint4 *)(qu + off))[sub] = make_uint4(a[0], a[1], a[2], a[3]);
+    ((uint4 *)(qv + off))[sub] = make_uint4(b[0], b[1], b[2], b[3]);
+#pragma unroll
+    for (int w = 4; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (sub == 0) delta[row] = acc;
+  }
+}
+
 __global__ void bwd_finish_kernel(const float *duv_part, float *du, float *dvb, int B, int H, int nq) {
   const int h = blockIdx.x, part = threadIdx.x >> 6, c = threadIdx.x & 63;
   float acc = 0.f;
@@ -704,7 +745,8 @@ BwdWorkspace tc_bwd_workspace(const AttnShape &s) {
 }
 
 cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, const void *v,
-                          const void *r, const void *u, const void *vb, const float *lse,
+                          const void *r, const void *u, const void *vb, const void *o,
+                          const void *o_lo, const float *lse,
                           const void *dout, void *dq, void *dk, void *dv, float *dr, float *du,
                           float *dvb, void *ws, cudaStream_t st, int *launches) {
   const BwdWorkspace w = tc_bwd_workspace(s);
@@ -735,8 +777,19 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   bwd_zero_kernel<<<sms * 4, 256, 0, st>>>(dr, n_dr, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv,
                                            s.B * s.H, s.cap, s.m, s.head, s.kv_rows);
   ++*launches;
-  cudaError_t e = launch_tc_bwd_prep(s, q, k, v, r, u, vb, dout, delta, qu, qv, st, launches);
-  if (e != cudaSuccess) return e;
+  if (o_lo) {
+    const long long rows = (long long)s.B * s.H * s.L;
+    long long blocks = (rows * 8 + 255) / 256;
+    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+    bwd_light_prep_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+        rows, s.L, s.H, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)u,
+        (const __nv_bfloat16 *)vb, (const __nv_bfloat16 *)o, (const __nv_bfloat16 *)o_lo,
+        (const __nv_bfloat16 *)dout, (__nv_bfloat16 *)qu, (__nv_bfloat16 *)qv, delta);
+    ++*launches;
+  } else {
+    cudaError_t e = launch_tc_bwd_prep(s, q, k, v, r, u, vb, dout, delta, qu, qv, st, launches);
+    if (e != cudaSuccess) return e;
+  }
 
   BwdParams p;
   p.B = s.B; p.H = s.H; p.L = s.L; p.cap = s.cap; p.m = s.m; p.head = s.head; p.nq = nq;

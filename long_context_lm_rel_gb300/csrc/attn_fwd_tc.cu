@@ -77,6 +77,7 @@ struct Params {
   float scale_log2;  // scale * log2(e)
   const __nv_bfloat16 *q, *u, *vb;
   __nv_bfloat16 *o;
+  __nv_bfloat16 *o_lo;  // optional: O - bf16(O), rounded to bf16 (exact D in the backward)
   float *lse;
   // backward preparation (kPrep): dO in, D = dO.O (fp32 O) and the bf16
   // (Q+u), (Q+v) rows (unscaled) out
@@ -358,15 +359,26 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         ok = pair_exchange(acc, &acc_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
         if (ok && hf == 0 && i < p.L) p.delta[(size_t)bh * p.L + i] = (acc + acc_other) * inv;
       } else {
-        uint4 *orow = (uint4 *)(p.o + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
+        const size_t orow_off = ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH;
+        uint4 *orow = (uint4 *)(p.o + orow_off);
+        uint4 *lorow = (uint4 *)(p.o_lo + orow_off);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          uint4 v;
-          v.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-          v.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-          v.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-          v.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-          if (i < p.L) orow[4 * hf + e] = v;
+          float f[8];
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) f[g] = __uint_as_float(o[8 * e + g]) * inv;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            hi[g] = pack_bf16(f[2 * g], f[2 * g + 1]);
+            // low part: what bf16 rounding of O dropped, itself in bf16
+            lo[g] = pack_bf16(f[2 * g] - __uint_as_float(hi[g] << 16),
+                              f[2 * g + 1] - __uint_as_float(hi[g] & 0xFFFF0000u));
+          }
+          if (i < p.L) {
+            orow[4 * hf + e] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            if (p.o_lo) lorow[4 * hf + e] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
         }
         if (hf == 0 && i < p.L)
           p.lse[(size_t)bh * p.L + i] = (m_run + log2f(l_run + l_other)) * 0.69314718055994531f;
@@ -416,7 +428,7 @@ bool make_map(CUtensorMap *m, const void *base, int planes, int rows, int box_ro
 
 template <int MODE>
 cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const void *v,
-                        const void *r, const void *u, const void *vb, void *o, float *lse,
+                        const void *r, const void *u, const void *vb, void *o, void *o_lo, float *lse,
                         const void *dout, float *delta, void *qu_out, void *qv_out,
                         cudaStream_t st, int *launches) {
   CUtensorMap tk, tv, tr;
@@ -437,7 +449,7 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   p.nq = (s.L + BQ - 1) / BQ;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.q = (const __nv_bfloat16 *)q; p.u = (const __nv_bfloat16 *)u; p.vb = (const __nv_bfloat16 *)vb;
-  p.o = (__nv_bfloat16 *)o; p.lse = lse;
+  p.o = (__nv_bfloat16 *)o; p.o_lo = (__nv_bfloat16 *)o_lo; p.lse = lse;
   const unsigned grid = (unsigned)(s.B * s.H * p.nq);
   rxl_fwd_tc_kernel<MODE><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p);
   ++*launches;
@@ -447,9 +459,9 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
 }  // namespace
 
 cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, const void *v,
-                          const void *r, const void *u, const void *vb, void *o, float *lse,
-                          cudaStream_t st, int *launches) {
-  return launch_mode<kFwd>(s, q, k, v, r, u, vb, o, lse, nullptr, nullptr, nullptr, nullptr, st,
+                          const void *r, const void *u, const void *vb, void *o, void *o_lo,
+                          float *lse, cudaStream_t st, int *launches) {
+  return launch_mode<kFwd>(s, q, k, v, r, u, vb, o, o_lo, lse, nullptr, nullptr, nullptr, nullptr, st,
                            launches);
 }
 
@@ -457,7 +469,7 @@ cudaError_t launch_tc_bwd_prep(const AttnShape &s, const void *q, const void *k,
                                const void *r, const void *u, const void *vb, const void *dout,
                                float *delta, void *qu_out, void *qv_out, cudaStream_t st,
                                int *launches) {
-  return launch_mode<kPrep>(s, q, k, v, r, u, vb, nullptr, nullptr, dout, delta, qu_out, qv_out,
+  return launch_mode<kPrep>(s, q, k, v, r, u, vb, nullptr, nullptr, nullptr, dout, delta, qu_out, qv_out,
                             st, launches);
 }
 

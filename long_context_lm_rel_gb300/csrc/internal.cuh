@@ -44,9 +44,10 @@ cudaError_t launch_simt_bwd(const AttnShape &s, rxl_dtype dt, const void *q, con
                             cudaStream_t st, int *launches);
 
 // sm_103a tensor-core forward (bf16).
+// o_lo (nullable) receives O - bf16(O) in bf16.
 cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, const void *v,
-                          const void *r, const void *u, const void *vb, void *o, float *lse,
-                          cudaStream_t st, int *launches);
+                          const void *r, const void *u, const void *vb, void *o, void *o_lo,
+                          float *lse, cudaStream_t st, int *launches);
 // Reads and clears the forward kernel's wait-timeout flag (synchronous).
 cudaError_t tc_fwd_read_error(int *flag);
 
@@ -59,8 +60,11 @@ cudaError_t launch_tc_bwd_prep(const AttnShape &s, const void *q, const void *k,
 
 // sm_103a tensor-core backward (bf16).
 BwdWorkspace tc_bwd_workspace(const AttnShape &s);
+// With o_lo (nullable), D comes from dO.(o + o_lo) in a streaming pass;
+// without it the forward is recomputed to obtain D from the fp32 O.
 cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, const void *v,
-                          const void *r, const void *u, const void *vb, const float *lse,
+                          const void *r, const void *u, const void *vb, const void *o,
+                          const void *o_lo, const float *lse,
                           const void *dout, void *dq, void *dk, void *dv, float *dr, float *du,
                           float *dvb, void *ws, cudaStream_t st, int *launches);
 cudaError_t tc_bwd_read_error(int *flag);

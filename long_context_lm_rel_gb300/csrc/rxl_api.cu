@@ -78,21 +78,29 @@ int rxl_device_error_flags(void) {
   return (fwd ? 1 : 0) | (bwd ? 2 : 0);
 }
 
-rxl_status rxl_attn_fwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
-                        const void *r, const void *u, const void *vbias, void *o, float *lse,
-                        rxl_stream_t stream) {
+rxl_status rxl_attn_fwd_ex(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                           const void *r, const void *u, const void *vbias, void *o, void *o_lo,
+                           float *lse, rxl_stream_t stream) {
   rxl::AttnShape s;
   rxl_status st = check_desc(desc, &s);
   if (st != RXL_OK) return st;
   if ((st = check_ptrs({q, k, v, r, u, vbias, o, lse})) != RXL_OK) return st;
+  if (o_lo && desc->dtype != RXL_DTYPE_BF16) return RXL_ERR_INVALID_ARGUMENT;
+  if (o_lo && !aligned16(o_lo)) return RXL_ERR_MISALIGNED;
   int launches = 0;
   const cudaError_t e =
       desc->dtype == RXL_DTYPE_BF16
-          ? rxl::launch_tc_fwd(s, q, k, v, r, u, vbias, o, lse, (cudaStream_t)stream, &launches)
+          ? rxl::launch_tc_fwd(s, q, k, v, r, u, vbias, o, o_lo, lse, (cudaStream_t)stream, &launches)
           : rxl::launch_simt_fwd(s, desc->dtype, q, k, v, r, u, vbias, o, lse,
                                  (cudaStream_t)stream, &launches);
   g_last_launches = launches;
   return cuda_status(e);
+}
+
+rxl_status rxl_attn_fwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                        const void *r, const void *u, const void *vbias, void *o, float *lse,
+                        rxl_stream_t stream) {
+  return rxl_attn_fwd_ex(desc, q, k, v, r, u, vbias, o, nullptr, lse, stream);
 }
 
 size_t rxl_attn_bwd_workspace_bytes(const rxl_attn_desc *desc) {
@@ -102,14 +110,16 @@ size_t rxl_attn_bwd_workspace_bytes(const rxl_attn_desc *desc) {
                                        : rxl::simt_bwd_workspace(s).total;
 }
 
-rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
-                        const void *r, const void *u, const void *vbias, const void *o,
-                        const float *lse, const void *dout, void *dq, void *dk, void *dv,
-                        float *dr, float *du, float *dvbias, void *workspace,
-                        size_t workspace_bytes, rxl_stream_t stream) {
+rxl_status rxl_attn_bwd_ex(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                           const void *r, const void *u, const void *vbias, const void *o,
+                           const void *o_lo, const float *lse, const void *dout, void *dq,
+                           void *dk, void *dv, float *dr, float *du, float *dvbias,
+                           void *workspace, size_t workspace_bytes, rxl_stream_t stream) {
   rxl::AttnShape s;
   rxl_status st = check_desc(desc, &s);
   if (st != RXL_OK) return st;
+  if (o_lo && desc->dtype != RXL_DTYPE_BF16) return RXL_ERR_INVALID_ARGUMENT;
+  if (o_lo && !aligned16(o_lo)) return RXL_ERR_MISALIGNED;
   if ((st = check_ptrs({q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr, du, dvbias,
                         workspace})) != RXL_OK)
     return st;
@@ -118,12 +128,21 @@ rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k,
     return RXL_ERR_WORKSPACE_TOO_SMALL;
   int launches = 0;
   const cudaError_t e =
-      tc ? rxl::launch_tc_bwd(s, q, k, v, r, u, vbias, lse, dout, dq, dk, dv, dr, du, dvbias,
-                              workspace, (cudaStream_t)stream, &launches)
+      tc ? rxl::launch_tc_bwd(s, q, k, v, r, u, vbias, o, o_lo, lse, dout, dq, dk, dv, dr, du,
+                              dvbias, workspace, (cudaStream_t)stream, &launches)
          : rxl::launch_simt_bwd(s, desc->dtype, q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr,
                                 du, dvbias, workspace, (cudaStream_t)stream, &launches);
   g_last_launches = launches;
   return cuda_status(e);
+}
+
+rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                        const void *r, const void *u, const void *vbias, const void *o,
+                        const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                        float *dr, float *du, float *dvbias, void *workspace,
+                        size_t workspace_bytes, rxl_stream_t stream) {
+  return rxl_attn_bwd_ex(desc, q, k, v, r, u, vbias, o, nullptr, lse, dout, dq, dk, dv, dr, du,
+                         dvbias, workspace, workspace_bytes, stream);
 }
 
 rxl_status rxl_mem_update(rxl_ring *ring, const void *src, long long src_plane_stride, int L,

@@ -113,6 +113,20 @@ class AttnCall:
                               self.lse, stream)
         return self
 
+    def fwd_ex(self, stream=None):
+        """Forward of the training pair: also keeps the low part of O."""
+        if not hasattr(self, "o_lo"):
+            self.o_lo = self.torch.empty_like(self.o)
+        self.rxl.rxl_attn_fwd_ex(self.desc, self.q, self.k, self.v, self.r, self.u, self.vb, self.o,
+                                 self.o_lo, self.lse, stream)
+        return self
+
+    def bwd_ex(self, stream=None):
+        self.rxl.rxl_attn_bwd_ex(self.desc, self.q, self.k, self.v, self.r, self.u, self.vb, self.o,
+                                 self.o_lo, self.lse, self.do, self.dq, self.dk, self.dv, self.dr,
+                                 self.du, self.dvb, self.ws, self.ws_bytes, stream)
+        return self
+
     def alloc_bwd(self, dout):
         torch = self.torch
         B, H, L, dh = self.shape

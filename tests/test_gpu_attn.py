@@ -34,13 +34,16 @@ def make_inputs(B, H, L, cap, m, dtype, seed=0, tid0=900000, D_model=1024):
         r=gen.round_to(gen.rel_table(cap + L, D_model, H, dh, seed, tid0 + 9), dtype))
 
 
-def run_gpu(x, cap, m, head, dtype, bwd=True, scale=0.125):
+def run_gpu(x, cap, m, head, dtype, bwd=True, scale=0.125, ex=False):
+    """ex=True runs the training pair (forward keeps the low part of O)."""
     k_phys = place_kv(x["k_mem"], x["k_cur"], cap, head, fill=7.0)   # junk in unused ring rows
     v_phys = place_kv(x["v_mem"], x["v_cur"], cap, head, fill=-7.0)
     c = AttnCall(x["q"], k_phys, v_phys, x["r"], x["u"], x["vb"], cap=cap, m=m, head=head,
-                 dtype=dtype, scale=scale).fwd()
+                 dtype=dtype, scale=scale)
+    c.fwd_ex() if ex else c.fwd()
     if bwd:
-        c.alloc_bwd(x["do"]).bwd()
+        c.alloc_bwd(x["do"])
+        c.bwd_ex() if ex else c.bwd()
     return c
 
 
@@ -85,11 +88,26 @@ SMALL = [  # B, H, L, cap, m, head
 ]
 
 
+@pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
 @pytest.mark.parametrize("B,H,L,cap,m,head", SMALL)
-def test_small_bf16_full_parity(B, H, L, cap, m, head):
+def test_small_bf16_full_parity(B, H, L, cap, m, head, ex):
     x = make_inputs(B, H, L, cap, m, "bf16", seed=B * 1000 + L + m)
-    c = run_gpu(x, cap, m, head, "bf16")
-    compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head)))
+    c = run_gpu(x, cap, m, head, "bf16", ex=ex)
+    compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head, ex)))
+
+
+def test_low_part_of_o_restores_the_unrounded_output():
+    import torch
+    B, H, L, cap, m = 2, 2, 150, 200, 180
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=31)
+    c = run_gpu(x, cap, m, 11, "bf16", bwd=False, ex=True)
+    torch.cuda.synchronize()
+    k, v = logical(x)
+    o_ref, _ = oracle.fwd(x["q"], k, v, x["r"], x["u"], x["vb"], 0.125)
+    hi, lo = to_host(c.o), to_host(c.o_lo)
+    err_hi = np.abs(hi - o_ref).max()
+    err_sum = np.abs(hi + lo - o_ref).max()
+    assert err_sum < 0.05 * err_hi, (err_sum, err_hi)   # far below bf16 rounding of O
 
 
 def test_small_f32_full_parity():
@@ -168,8 +186,9 @@ def sample_rows(B, H, L, n, rng):
     return np.array(sorted(sel), dtype=np.int32)
 
 
+@pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
 @pytest.mark.parametrize("cfg", [3, 4])
-def test_full_size_config(cfg):
+def test_full_size_config(cfg, ex):
     import torch
     w = gen.CONFIGS[cfg]
     p = gen.layer_params(w)
@@ -178,7 +197,7 @@ def test_full_size_config(cfg):
     x = dict(q=s["q"], k_mem=mem["k_mem"], k_cur=s["k_cur"], v_mem=mem["v_mem"], v_cur=s["v_cur"],
              u=p["u"], vb=p["vb"], r=p["r"], do=s["do"])
     cap = m = w.M
-    c = run_gpu(x, cap, m, 0, "bf16", scale=w.scale)
+    c = run_gpu(x, cap, m, 0, "bf16", scale=w.scale, ex=ex)
     torch.cuda.synchronize()
     assert_no_device_error()
     k, v = logical(x)
