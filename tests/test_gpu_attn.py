@@ -105,9 +105,12 @@ def test_low_part_of_o_restores_the_unrounded_output():
     k, v = logical(x)
     o_ref, _ = oracle.fwd(x["q"], k, v, x["r"], x["u"], x["vb"], 0.125)
     hi, lo = to_host(c.o), to_host(c.o_lo)
-    err_hi = np.abs(hi - o_ref).max()
-    err_sum = np.abs(hi + lo - o_ref).max()
-    assert err_sum < 0.05 * err_hi, (err_sum, err_hi)   # far below bf16 rounding of O
+    # o_lo is what rounding O to bf16 dropped: at most half a bf16 ulp of o
+    assert np.all(np.abs(lo) <= np.abs(hi) * 2.0 ** -8 + 1e-30)
+    # and o + o_lo is the unrounded (fp32) O, closer to the exact O than o
+    err_hi = np.abs(hi - o_ref).mean()
+    err_sum = np.abs(hi + lo - o_ref).mean()
+    assert err_sum < 0.75 * err_hi, (err_sum, err_hi)
 
 
 def test_small_f32_full_parity():
