@@ -103,33 +103,129 @@ __device__ __forceinline__ bool pair_exchange(float mine, float *out, volatile f
   return ok;
 }
 
+// A work item is one (b, h, 128-query tile). Items are numbered so that the
+// longest query tiles (most keys) come first. CTA c of G takes one item per
+// round r, in snake order: item r*G + c on even rounds, r*G + G-1-c on odd
+// ones, so that the CTAs' total key-tile counts stay within about one tile.
+struct Item {
+  int bh, h, i0, T;
+};
+
+__device__ __forceinline__ Item item_at(const Params &p, int w) {
+  const int BH = p.B * p.H;
+  Item it;
+  it.bh = w % BH;
+  it.h = it.bh % p.H;
+  it.i0 = (p.nq - 1 - w / BH) * BQ;
+  it.T = KeyTiles(p.m, p.cap, p.head, min(it.i0 + BQ, p.L)).count();
+  return it;
+}
+
+// Walks this CTA's tiles across its items: k counts the CTA's items, t the
+// key tiles of the current item.
+struct Cursor {
+  int k, w, t, nitems;
+  bool valid;
+  Item it;
+  __device__ __forceinline__ int item_of_round(int r) const {
+    const int G = gridDim.x, c = blockIdx.x;
+    return r * G + ((r & 1) ? G - 1 - c : c);
+  }
+  __device__ void init(const Params &p, int n) {
+    nitems = n;
+    k = 0;
+    t = 0;
+    w = item_of_round(0);
+    valid = w < nitems;
+    if (valid) it = item_at(p, w);
+  }
+  __device__ void next(const Params &p) {
+    if (++t == it.T) {
+      t = 0;
+      ++k;
+      w = item_of_round(k);
+      valid = w < nitems;
+      if (valid) it = item_at(p, w);
+    }
+  }
+};
+
+// (Q+u)*c and (Q+v)*c in bf16, c = scale*log2(e), as 128-byte swizzled
+// K-major tiles for the item's query rows; the row's two warps split its 8
+// chunks. In kPrep mode the unscaled rows also go to global memory.
+template <int MODE>
+__device__ __forceinline__ void q_prep(const Params &p, const Item &it, uint32_t sbase, int quad,
+                                       int hf, int lane) {
+  const int ii = quad * 32 + lane;
+  const int i = it.i0 + ii;
+  const float c2 = p.scale_log2;
+  const uint4 *qrow = (const uint4 *)(p.q + ((size_t)it.bh * p.L + (i < p.L ? i : 0)) * DH);
+  const uint4 *urow = (const uint4 *)(p.u + (size_t)it.h * DH);
+  const uint4 *vrow = (const uint4 *)(p.vb + (size_t)it.h * DH);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c = 4 * hf + cc;
+    uint4 qv4 = i < p.L ? qrow[c] : make_uint4(0, 0, 0, 0);
+    const uint4 u4 = urow[c], v4 = vrow[c];
+    const uint32_t qw[4] = {qv4.x, qv4.y, qv4.z, qv4.w};
+    const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+    const uint32_t vw[4] = {v4.x, v4.y, v4.z, v4.w};
+    uint32_t a[4], b[4], a1[4], b1[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float q0 = __uint_as_float(qw[e] << 16), q1 = __uint_as_float(qw[e] & 0xFFFF0000u);
+      const float u0 = __uint_as_float(uw[e] << 16), u1 = __uint_as_float(uw[e] & 0xFFFF0000u);
+      const float v0 = __uint_as_float(vw[e] << 16), v1 = __uint_as_float(vw[e] & 0xFFFF0000u);
+      a[e] = pack_bf16((q0 + u0) * c2, (q1 + u1) * c2);
+      b[e] = pack_bf16((q0 + v0) * c2, (q1 + v1) * c2);
+      a1[e] = pack_bf16(q0 + u0, q1 + u1);
+      b1[e] = pack_bf16(q0 + v0, q1 + v1);
+    }
+    st_shared_v4(sbase + SM_QU + sw128_offset(ii, c), a[0], a[1], a[2], a[3]);
+    st_shared_v4(sbase + SM_QV + sw128_offset(ii, c), b[0], b[1], b[2], b[3]);
+    if (MODE == kPrep && i < p.L) {
+      const size_t off = ((size_t)it.bh * p.L + i) * DH;
+      ((uint4 *)(p.qu_out + off))[c] = make_uint4(a1[0], a1[1], a1[2], a1[3]);
+      ((uint4 *)(p.qv_out + off))[c] = make_uint4(b1[0], b1[1], b1[2], b1[3]);
+    }
+  }
+}
+
+// Persistent kernel: gridDim.x CTAs walk all work items. Per CTA, tiles are
+// numbered g = 0, 1, ... across its items; every barrier phase follows g
+// (tile barriers) or the item counter k (q_ready, o_free).
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_r, const Params p) {
+                  const __grid_constant__ CUtensorMap tm_r, const Params p, int nitems) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = tc::align1024(smem_raw);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = p.nq - 1 - (int)(blockIdx.x % p.nq);  // long query tiles first
-  const int bh = (int)(blockIdx.x / p.nq);
-  const int h = bh % p.H;
-  const int i0 = qt * BQ;
 
-  const uint32_t bar_full0 = sbase + SM_BAR, bar_full1 = bar_full0 + 8;
-  const uint32_t bar_sg = bar_full0 + 16, bar_p = bar_full0 + 24, bar_pv = bar_full0 + 32;
-  const uint32_t bar_drain = bar_full0 + 40;
-  uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 48);
-  volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 56);
-  const uint32_t bar_x0 = bar_full0 + 64;  // 4 quadrant exchange barriers
+  const uint32_t b0 = sbase + SM_BAR;
+  const uint32_t bar_full0 = b0, bar_full1 = b0 + 8;
+  const uint32_t bar_sg = b0 + 16;       // S/G MMAs of a tile done (commit)
+  const uint32_t bar_sgfree = b0 + 24;   // softmax finished reading S/G of a tile (256)
+  const uint32_t bar_pr = b0 + 32;       // softmax finished a tile: P written (256)
+  const uint32_t bar_pv = b0 + 40;       // P.V of a tile done (commit)
+  const uint32_t bar_qready = b0 + 48;   // Q tiles of an item written (256)
+  const uint32_t bar_ofree = b0 + 56;    // epilogue of an item read O (256)
+  const uint32_t bar_drain = b0 + 64;
+  const uint32_t bar_x0 = b0 + 72;       // 4 quadrant exchange barriers
+  uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 104);
+  volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 108);
   volatile float *xbuf = (volatile float *)(smem + SM_X);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_full0, 1);
     mbar_init(bar_full1, 1);
     mbar_init(bar_sg, 1);
-    mbar_init(bar_p, kSoftmaxWarps * 32);
+    mbar_init(bar_sgfree, kSoftmaxWarps * 32);
+    mbar_init(bar_pr, kSoftmaxWarps * 32);
     mbar_init(bar_pv, 1);
+    mbar_init(bar_qready, kSoftmaxWarps * 32);
+    mbar_init(bar_ofree, kSoftmaxWarps * 32);
     mbar_init(bar_drain, 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     *abort_flag = 0;
@@ -142,71 +238,35 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_r);
     }
-  } else {
-    // (Q+u)*c and (Q+v)*c in bf16, c = scale*log2(e), as 128-byte swizzled
-    // K-major tiles; the row's two warps split its 8 chunks.
-    const int quad = warp & 3, hf = warp >> 2;
-    const int ii = quad * 32 + lane;
-    const int i = i0 + ii;
-    const float c2 = p.scale_log2;
-    const uint4 *qrow = (const uint4 *)(p.q + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
-    const uint4 *urow = (const uint4 *)(p.u + (size_t)h * DH);
-    const uint4 *vrow = (const uint4 *)(p.vb + (size_t)h * DH);
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      const int c = 4 * hf + cc;
-      uint4 qv4 = i < p.L ? qrow[c] : make_uint4(0, 0, 0, 0);
-      const uint4 u4 = urow[c], v4 = vrow[c];
-      const uint32_t qw[4] = {qv4.x, qv4.y, qv4.z, qv4.w};
-      const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
-      const uint32_t vw[4] = {v4.x, v4.y, v4.z, v4.w};
-      uint32_t a[4], b[4], a1[4], b1[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float q0 = __uint_as_float(qw[e] << 16), q1 = __uint_as_float(qw[e] & 0xFFFF0000u);
-        const float u0 = __uint_as_float(uw[e] << 16), u1 = __uint_as_float(uw[e] & 0xFFFF0000u);
-        const float v0 = __uint_as_float(vw[e] << 16), v1 = __uint_as_float(vw[e] & 0xFFFF0000u);
-        a[e] = pack_bf16((q0 + u0) * c2, (q1 + u1) * c2);
-        b[e] = pack_bf16((q0 + v0) * c2, (q1 + v1) * c2);
-        a1[e] = pack_bf16(q0 + u0, q1 + u1);
-        b1[e] = pack_bf16(q0 + v0, q1 + v1);
-      }
-      st_shared_v4(sbase + SM_QU + sw128_offset(ii, c), a[0], a[1], a[2], a[3]);
-      st_shared_v4(sbase + SM_QV + sw128_offset(ii, c), b[0], b[1], b[2], b[3]);
-      if (MODE == kPrep && i < p.L) {
-        const size_t off = ((size_t)bh * p.L + i) * DH;
-        ((uint4 *)(p.qu_out + off))[c] = make_uint4(a1[0], a1[1], a1[2], a1[3]);
-        ((uint4 *)(p.qv_out + off))[c] = make_uint4(b1[0], b1[1], b1[2], b1[3]);
-      }
-    }
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const KeyTiles tl(p.m, p.cap, p.head, min(i0 + BQ, p.L));
-  const int T = tl.count();
-
   if (warp == kProducerWarp) {
     // ------------------------------------------------ producer / MMA issuer
     if (lane == 0) {
       bool pending[2] = {false, false};
       int nissued[2] = {0, 0};
-      auto issue_tma = [&](int t) {
-        const int s = t & 1;
-        const KeyTile x = tl.get(t);
+      Cursor tc_;  // next tile to load
+      tc_.init(p, nitems);
+      int g_tma = 0;
+      auto issue_tma = [&]() {
+        const int s = g_tma & 1;
+        const KeyTile x = KeyTiles(p.m, p.cap, p.head, min(tc_.it.i0 + BQ, p.L)).get(tc_.t);
         const uint32_t bar = s ? bar_full1 : bar_full0;
         mbar_expect_tx(bar, STAGE_TX);
-        tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, bh, bar);
-        tma_load_3d(sbase + SM_V + s * 16384, &tm_v, 0, x.phys0, bh, bar);
-        tma_load_3d(sbase + SM_R + s * 32768, &tm_r, 0, i0 - x.jlog0 - (BK - 1), h, bar);
+        tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, tc_.it.bh, bar);
+        tma_load_3d(sbase + SM_V + s * 16384, &tm_v, 0, x.phys0, tc_.it.bh, bar);
+        tma_load_3d(sbase + SM_R + s * 32768, &tm_r, 0, tc_.it.i0 - x.jlog0 - (BK - 1), tc_.it.h, bar);
         pending[s] = true;
         ++nissued[s];
+        ++g_tma;
+        tc_.next(p);
       };
-      auto issue_sg = [&](int t) {
-        const int s = t & 1;
+      auto issue_sg = [&](int g) {
+        const int s = g & 1;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint64_t a = sdesc_sw128(sbase + SM_QU + k * 32, 16, 1024);
@@ -221,35 +281,58 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
         mma_commit(bar_sg);
       };
+      auto wait_full = [&](int g) {
+        const int s = g & 1;
+        const bool r = mbar_wait(s ? bar_full1 : bar_full0, (g >> 1) & 1, abort_flag);
+        pending[s] = false;
+        return r;
+      };
       bool ok = true;
-      if (T > 0) issue_tma(0);
-      if (T > 1) issue_tma(1);
-      if (T > 0) {
-        ok = mbar_wait(bar_full0, 0, abort_flag);
-        pending[0] = false;
+      Cursor mc;  // tile whose P.V is next
+      mc.init(p, nitems);
+      if (tc_.valid) issue_tma();
+      if (tc_.valid) issue_tma();
+      if (mc.valid) {
+        ok = mbar_wait(bar_qready, 0, abort_flag) && wait_full(0);
         if (ok) issue_sg(0);
       }
-      for (int t = 0; ok && t < T; ++t) {
-        if (!(ok = mbar_wait(bar_p, t & 1, abort_flag))) break;
+      for (int g = 0; ok && mc.valid; ++g) {
+        Cursor nx = mc;
+        nx.next(p);
+        const bool new_item = nx.valid && nx.t == 0;
+        // S/G of tile g+1 as soon as the softmax released S/G of tile g
+        // (same item: the Q tiles are unchanged)
+        if (nx.valid && !new_item) {
+          if (!(ok = mbar_wait(bar_sgfree, g & 1, abort_flag) && wait_full(g + 1))) break;
+          issue_sg(g + 1);
+        }
+        if (!(ok = mbar_wait(bar_pr, g & 1, abort_flag))) break;
+        // the first P.V of an item overwrites O: its epilogue must have read it
+        if (mc.t == 0 && mc.k > 0 && !(ok = mbar_wait(bar_ofree, (mc.k - 1) & 1, abort_flag))) break;
         tc_fence_after();
-        const int s = t & 1;
+        const int s = g & 1;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t a = sdesc_sw128(sbase + SM_P + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
           const uint64_t b = sdesc_sw128(sbase + SM_V + s * 16384 + k * 2048, 16, 1024);
-          mma_bf16(tmem + TM_O, a, b, IDESC_O, (t > 0 || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + TM_O, a, b, IDESC_O, (mc.t > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(bar_pv);
-        if (t + 1 < T) {
-          const int s1 = (t + 1) & 1;
-          if (!(ok = mbar_wait(s1 ? bar_full1 : bar_full0, ((t + 1) >> 1) & 1, abort_flag))) break;
-          pending[s1] = false;
-          issue_sg(t + 1);
+        if (new_item) {
+          // next item: its Q tiles are written once the softmax finished
+          // this item's last tile
+          if (!(ok = mbar_wait(bar_sgfree, g & 1, abort_flag) &&
+                     mbar_wait(bar_qready, nx.k & 1, abort_flag) && wait_full(g + 1)))
+            break;
+          tc_fence_after();
+          issue_sg(g + 1);
         }
-        if (t + 2 < T) {
-          if (!(ok = mbar_wait(bar_pv, t & 1, abort_flag))) break;
-          issue_tma(t + 2);
+        if (tc_.valid) {
+          // stage g&1 is free once P.V(g) (and with it S/G(g)) completed
+          if (!(ok = mbar_wait(bar_pv, g & 1, abort_flag))) break;
+          issue_tma();
         }
+        mc = nx;
       }
       if (!ok) {
         // wind down: let in-flight copies and MMAs land before TMEM and
@@ -267,29 +350,75 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // ----------------------------------------------------- softmax warps
     const int quad = warp & 3, hf = warp >> 2;
     const int ii = quad * 32 + lane;
-    const int i = i0 + ii;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t bar_x = bar_x0 + 8 * quad;
     uint32_t xphase = 0;
     float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's part of the row sum
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int s = t & 1;
-      ok = mbar_wait(bar_sg, t & 1, abort_flag) &&
-           mbar_wait(s ? bar_full1 : bar_full0, (t >> 1) & 1, abort_flag);
+    Cursor cur;
+    cur.init(p, nitems);
+    if (cur.valid) {
+      q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
+      fence_proxy_async_smem();
+      mbar_arrive(bar_qready);
+    }
+    for (int g = 0; cur.valid; ++g) {
+      const Item it = cur.it;
+      const int t = cur.t;
+      const int i = it.i0 + ii;
+      const int s = g & 1;
+      ok = mbar_wait(bar_sg, g & 1, abort_flag) &&
+           mbar_wait(s ? bar_full1 : bar_full0, (g >> 1) & 1, abort_flag);
+      // P buffer and O: P.V(g-1) must be done
+      if (ok && g > 0) ok = mbar_wait(bar_pv, (g - 1) & 1, abort_flag);
       // tcgen05.ld/st below are warp-collective: keep every decision warp-uniform
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      const KeyTile x = tl.get(t);
+      const KeyTile x = KeyTiles(p.m, p.cap, p.head, min(it.i0 + BQ, p.L)).get(t);
       float y[64];
-      tc::half_tile_logits<false>(trow, TM_S, TM_G, quad, lane, hf, i, x, 1.f, y);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hf + cc;
+        uint32_t sr[32], w0[32], w1[32];
+        tmem_ld32(trow + TM_S + 32 * c, sr);
+        const uint32_t gcol = TM_G + 32 * quad + 96 - 32 * c;
+        tmem_ld32(trow + gcol, w0);
+        tmem_ld32(trow + gcol + 32, w1);
+        tmem_wait_ld();
+        if (cc == 1) {
+          // done reading S and G: the next tile's S/G MMAs may start
+          tc_fence_before();
+          mbar_arrive(bar_sgfree);
+        }
+        float win[64];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          win[e] = __uint_as_float(w0[e]);
+          win[32 + e] = __uint_as_float(w1[e]);
+        }
+        // win[x] <- win[x + lane] (5 predicated stages)
+#pragma unroll
+        for (int b = 4; b >= 0; --b) {
+          const int sh = 1 << b;
+          const bool take = (lane >> b) & 1;
+#pragma unroll
+          for (int e = 0; e < 63; ++e)
+            if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
+        }
+        // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i
+        const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float a = __uint_as_float(sr[k]) + win[31 - k];
+          y[32 * cc + k] = k <= lim ? a : -INFINITY;
+        }
+      }
       float mt = -INFINITY;
 #pragma unroll
       for (int k = 0; k < 64; ++k) mt = fmaxf(mt, y[k]);
       float other;
       if (!(ok = pair_exchange(mt, &other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
-      // the exponent reference only moves when the row max outgrows it by
-      // 2^8 (P <= 256 otherwise), which skips most O rescales
+      // the exponent reference only moves when the row max outgrows it by 2^8
       const float mrow = fmaxf(mt, other);
       const bool move = mrow > m_run + kRescaleThreshold;
       const float m_new = move ? mrow : m_run;
@@ -305,8 +434,6 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       }
       l_run = l_run * alpha + sum;
       m_run = m_new;
-      // P (keys 64*hf ..) -> its shared-memory column block; the previous
-      // P.V finished (bar_sg of this tile was committed after it)
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         st_shared_v4(sbase + SM_P + hf * 16384 + sw128_offset(ii, c), pk[4 * c], pk[4 * c + 1],
@@ -329,22 +456,31 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar_p);
-    }
-    // epilogue: O / l, LSE (natural log); this thread owns O columns 32*hf..
-    if (ok && T > 0) ok = mbar_wait(bar_pv, (T - 1) & 1, abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    float l_other = 0.f;
-    if (ok) ok = pair_exchange(l_run, &l_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
-    if (ok) {
+      mbar_arrive(bar_pr);
+
+      cur.next(p);
+      if (t + 1 < it.T) continue;
+      // ---- last tile of the item: Q tiles of the next item, then epilogue
+      if (cur.valid) {
+        // the S/G MMAs of this item are all done (bar_sg waited above)
+        q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
+        fence_proxy_async_smem();
+        mbar_arrive(bar_qready);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, g & 1, abort_flag));
+      float l_other = 0.f;
+      if (ok) ok = pair_exchange(l_run, &l_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
+      if (!ok) break;
       tc_fence_after();
       const float inv = 1.f / (l_run + l_other);
       uint32_t o[32];
       tmem_ld32(trow + TM_O + 32 * hf, o);
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_ofree);
       if (MODE == kPrep) {
         // D_i = dO_i . O_i with O_i still in fp32
-        const uint4 *drow = (const uint4 *)(p.dout + ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH);
+        const uint4 *drow = (const uint4 *)(p.dout + ((size_t)it.bh * p.L + (i < p.L ? i : 0)) * DH);
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -356,10 +492,10 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                    __uint_as_float(o[8 * e + 2 * f + 1]) * __uint_as_float(dw[f] & 0xFFFF0000u);
         }
         float acc_other = 0.f;
-        ok = pair_exchange(acc, &acc_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
-        if (ok && hf == 0 && i < p.L) p.delta[(size_t)bh * p.L + i] = (acc + acc_other) * inv;
+        if (!(ok = pair_exchange(acc, &acc_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
+        if (hf == 0 && i < p.L) p.delta[(size_t)it.bh * p.L + i] = (acc + acc_other) * inv;
       } else {
-        const size_t orow_off = ((size_t)bh * p.L + (i < p.L ? i : 0)) * DH;
+        const size_t orow_off = ((size_t)it.bh * p.L + (i < p.L ? i : 0)) * DH;
         uint4 *orow = (uint4 *)(p.o + orow_off);
         uint4 *lorow = (uint4 *)(p.o_lo + orow_off);
 #pragma unroll
@@ -367,13 +503,13 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           float f[8];
           uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int g = 0; g < 8; ++g) f[g] = __uint_as_float(o[8 * e + g]) * inv;
+          for (int g2 = 0; g2 < 8; ++g2) f[g2] = __uint_as_float(o[8 * e + g2]) * inv;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            hi[g] = pack_bf16(f[2 * g], f[2 * g + 1]);
+          for (int g2 = 0; g2 < 4; ++g2) {
+            hi[g2] = pack_bf16(f[2 * g2], f[2 * g2 + 1]);
             // low part: what bf16 rounding of O dropped, itself in bf16
-            lo[g] = pack_bf16(f[2 * g] - __uint_as_float(hi[g] << 16),
-                              f[2 * g + 1] - __uint_as_float(hi[g] & 0xFFFF0000u));
+            lo[g2] = pack_bf16(f[2 * g2] - __uint_as_float(hi[g2] << 16),
+                               f[2 * g2 + 1] - __uint_as_float(hi[g2] & 0xFFFF0000u));
           }
           if (i < p.L) {
             orow[4 * hf + e] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -381,8 +517,10 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           }
         }
         if (hf == 0 && i < p.L)
-          p.lse[(size_t)bh * p.L + i] = (m_run + log2f(l_run + l_other)) * 0.69314718055994531f;
+          p.lse[(size_t)it.bh * p.L + i] = (m_run + log2f(l_run + l_other)) * 0.69314718055994531f;
       }
+      m_run = -INFINITY;
+      l_run = 0.f;
     }
     if (!ok) atomicExch(&g_fwd_error, 1);
   }
@@ -450,8 +588,12 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.q = (const __nv_bfloat16 *)q; p.u = (const __nv_bfloat16 *)u; p.vb = (const __nv_bfloat16 *)vb;
   p.o = (__nv_bfloat16 *)o; p.o_lo = (__nv_bfloat16 *)o_lo; p.lse = lse;
-  const unsigned grid = (unsigned)(s.B * s.H * p.nq);
-  rxl_fwd_tc_kernel<MODE><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p);
+  const int nitems = s.B * s.H * p.nq;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const unsigned grid = (unsigned)(nitems < sms ? nitems : sms);
+  rxl_fwd_tc_kernel<MODE><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
   ++*launches;
   return cudaGetLastError();
 }
