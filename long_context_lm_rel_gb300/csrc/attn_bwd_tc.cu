@@ -8,25 +8,29 @@
 //   dQ_i = sum_j dA_ij (k_j + r_{i-j})  dR_d = sum_b sum_{i-j=d} dA_ij (q_i+v)
 //   du   = sum dA_ij k_j               dv   = sum dA_ij r_{i-j}
 //
+// One pass over the visible (query tile, key tile) pairs computes every
+// gradient; the logits are formed once per pair.
+//
 // Kernels (all on the caller's stream):
-//   zero   : dR <- 0; dK/dV rows of ring slots without valid memory <- 0
-//   prep   : the forward kernel in preparation mode: D_i from the fp32 O, and
-//            the bf16 (Q+u), (Q+v) rows the two kernels below load by TMA
-//   kv     : one CTA per (b, h, 128-key tile), loops over query tiles:
-//            S, G -> P (skewed, masked), dP = dO V^T -> dA;
-//            dV += P^T dO and dK += dA^T (Q+u) accumulate in TMEM
-//   q      : one CTA per (b, h, 128-query tile), loops over key tiles:
-//            S, G -> P, dP -> dA, and the sheared dG[ii][t] = dA[ii][ii+127-t];
-//            dQ_content += dA K and dQ_position += dG Rband accumulate in TMEM;
-//            dR_band = dG^T (Q+v) per tile pair, added into dR (fp32 atomics).
-//            The position products run in fp16 (dG scaled by a CTA-wide power
-//            of two, R band and (Q+v) converted in place): R rows are several
-//            times larger than K rows, and bf16 rounding of dA in that term
-//            alone can exceed 1% of max|dQ| on short contexts.
-//   finish : du, dv = fixed-order sums of the per-CTA column sums of the two
-//            dQ parts
-// Both main kernels keep the score tile in TMEM (lanes = query rows), so the
-// skewed read of the position scores is the one the forward uses.
+//   zero   : dR, the fp32 dQ accumulator and the du/dv sums <- 0; dK/dV rows
+//            of ring slots without valid memory <- 0; R -> fp16 copy
+//   prep   : D_i and the (Q+u) (bf16) and (Q+v) (fp16) rows, either from
+//            dO.(o + o_lo) in a streaming pass or, without o_lo, from the
+//            forward kernel recomputing the fp32 O
+//   main   : persistent; a CTA takes one (b, h, 128-key tile) item at a time
+//            and loops over the query tiles that see it:
+//              S = (Q+u)K^T, G = (Q+v)Rband^T    -> P (skewed G, masked)
+//              dP = dO V^T, dV += P^T dO         -> dA, sheared dG
+//              dK += dA^T (Q+u), dQc = dA K, dQp = dG Rband, dRband = dG^T (Q+v)
+//            dV, dK stay in TMEM for the whole item; the pair's dQc + dQp
+//            and its two 128-distance dR blocks are added into fp32 global
+//            accumulators (vector reductions). The column sums of dQp over
+//            the rows give dv; du = (column sums of dQ) - dv.
+//            The position products run in fp16 with dG scaled by a power of
+//            two chosen per pair from max |dA|: R rows are several times
+//            larger than K rows, and bf16 rounding of dA in that term alone
+//            can exceed 1% of max|dQ| on short contexts.
+//   finish : dQ -> bf16 with per-head column sums; then du, dv
 #include <math.h>
 
 #include <mutex>
@@ -44,7 +48,7 @@ constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each owning 64 
 constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
-constexpr uint32_t IDESC_G = idesc_bf16(128, 256, false, false);
+constexpr uint32_t IDESC_G_F16 = idesc_f16(128, 256, false, false);
 constexpr uint32_t IDESC_MN_MN = idesc_bf16(128, 64, true, true);   // A^T . B, both d/row-major tiles
 constexpr uint32_t IDESC_K_MN = idesc_bf16(128, 64, false, true);
 constexpr uint32_t IDESC_K_MN_F16 = idesc_f16(128, 64, false, true);
@@ -54,12 +58,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 __device__ int g_bwd_error;
 
 struct BwdParams {
-  int B, H, L, cap, m, head, nq, kv_rows, nkt;
+  int B, H, L, cap, m, head, nq, kv_rows, nitems;
   float scale, scale_log2;
   const float *lse, *delta;
-  __nv_bfloat16 *dq, *dk, *dv;
-  float *dr;        // [H][kv_rows][64], zeroed by the zero kernel
-  float *duv_part;  // [B*H][nq][2][64]
+  __nv_bfloat16 *dk, *dv;
+  float *dq_acc;  // [B*H][L][64], zeroed
+  float *dr;      // [H][kv_rows][64], zeroed
+  float *dv_acc;  // [H][64] column sums of the position part of dQ, zeroed
 };
 
 // K-major operand: 128-byte swizzled [rows][64] tile, k-step kk of 16 elements.
@@ -91,152 +96,194 @@ __device__ __forceinline__ bool pair_sync(uint32_t bar, int lane, uint32_t &phas
   return ok;
 }
 
-// Output chunk D of the sheared dG row ii: columns 32*quad + 32*D + y hold
-// v[ii + 127 - col] = w1[y + u] with w1[z] = v[158 - 32D - z] and u = 31 - lane
-// (5-stage barrel shift), stored as fp16 into a [128][256] K-major tile set
-// (four 16 KB column blocks).
-__device__ __forceinline__ void shear_put(uint32_t base, int ii, int quad, int lane, int D,
-                                          float (&w1)[63]) {
-  const int u = 31 - lane;
-#pragma unroll
-  for (int b = 4; b >= 0; --b) {
-    const int sh = 1 << b;
-    const bool take = (u >> b) & 1;
-#pragma unroll
-    for (int e = 0; e < 62; ++e)
-      if (e < 32 + sh - 1 && e + sh < 63) w1[e] = take ? w1[e + sh] : w1[e];
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int col = 32 * (quad + D) + 8 * e;
-    st_shared_v4(base + (col >> 6) * 16384 + sw128_offset(ii, (col & 63) >> 3),
-                 pack_f16(w1[8 * e + 0], w1[8 * e + 1]), pack_f16(w1[8 * e + 2], w1[8 * e + 3]),
-                 pack_f16(w1[8 * e + 4], w1[8 * e + 5]), pack_f16(w1[8 * e + 6], w1[8 * e + 7]));
-  }
+// ------------------------------------------------------------ main kernel
+
+constexpr uint32_t F_K = 0, F_V = 16384, F_QU = 32768, F_QV = 49152, F_DO = 65536;
+constexpr uint32_t F_R = 81920, F_PA = 114688, F_DG = 147456, F_X = 212992, F_BAR = 215040;
+constexpr uint32_t F_SMEM = F_BAR + 256 + 1024;
+// TMEM columns: dV, dK accumulators; S (then dP); G (then dQc, dQp, dR blocks)
+constexpr uint32_t TM_DV = 0, TM_DK = 64, TM_S = 128, TM_G = 256;
+constexpr uint32_t TM_QC = 256, TM_QP = 320, TM_R0 = 384;
+
+// A work item is one (b, h, key tile); items are numbered key tile major, so
+// that the memory tiles and the early current tiles (seen by the most query
+// tiles) come first. CTA c of G takes one item per round, snake order.
+struct FItem {
+  int bh, h, qlo, NQ;
+  KeyTile x;
+};
+
+__device__ __forceinline__ FItem fitem(const BwdParams &p, const KeyTiles &tiles, int w) {
+  const int BH = p.B * p.H;
+  FItem it;
+  it.bh = w % BH;
+  it.h = it.bh % p.H;
+  it.x = tiles.get(w / BH);
+  it.qlo = it.x.jlog0 >= 0 ? it.x.jlog0 / BQ : 0;
+  it.NQ = p.nq - it.qlo;
+  return it;
 }
 
-// Half 0 of a row writes chunks D = 2, 3, 4 from its keys 0..63 (y) and keys
-// 64..95 received from half 1 (xk, already scaled); half 1 writes D = 0, 1
-// from its keys 64..127. Values are scaled by sig (a power of two).
-template <int D>
-__device__ __forceinline__ void shear_chunk_lo(uint32_t base, int ii, int quad, int lane,
-                                               const float (&y)[64], const float (&xk)[32], float sig) {
-  float w1[63];
-#pragma unroll
-  for (int z = 0; z < 63; ++z) {
-    const int key = 158 - 32 * D - z;
-    w1[z] = (key >= 0 && key < 64) ? sig * y[(key >= 0 && key < 64) ? key : 0]
-            : (key >= 64 && key < 96) ? xk[(key >= 64 && key < 96) ? key - 64 : 0]
-                                      : 0.f;
+// Walks this CTA's (item, query tile) pairs: k counts items, n query tiles.
+struct PairCursor {
+  int k, n;
+  bool valid;
+  FItem it;
+  __device__ __forceinline__ static int item_of_round(int r) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return r * G + ((r & 1) ? G - 1 - c : c);
   }
-  shear_put(base, ii, quad, lane, D, w1);
-}
-template <int D>
-__device__ __forceinline__ void shear_chunk_hi(uint32_t base, int ii, int quad, int lane,
-                                               const float (&y)[64], float sig) {
-  float w1[63];
-#pragma unroll
-  for (int z = 0; z < 63; ++z) {
-    const int key = 158 - 32 * D - z;
-    w1[z] = (key >= 64 && key < 128) ? sig * y[(key >= 64 && key < 128) ? key - 64 : 0] : 0.f;
+  __device__ void init(const BwdParams &p, const KeyTiles &tiles) {
+    k = 0;
+    n = 0;
+    const int w = item_of_round(0);
+    valid = w < p.nitems;
+    if (valid) it = fitem(p, tiles, w);
   }
-  shear_put(base, ii, quad, lane, D, w1);
-}
-
-// ------------------------------------------------------------- dK / dV kernel
-
-constexpr uint32_t KV_K = 0, KV_V = 16384, KV_QU = 32768, KV_QV = 49152, KV_DO = 65536;
-constexpr uint32_t KV_R = 81920, KV_P = 114688, KV_DA = 147456, KV_BAR = 180224;
-constexpr uint32_t KV_SMEM = KV_BAR + 128 + 1024;
-constexpr uint32_t TM_S = 0, TM_G = 128, TM_A = 384, TM_B = 448;  // A/B: dV/dK or dQc/dQp
+  __device__ void next(const BwdParams &p, const KeyTiles &tiles) {
+    if (++n == it.NQ) {
+      n = 0;
+      ++k;
+      const int w = item_of_round(k);
+      valid = w < p.nitems;
+      if (valid) it = fitem(p, tiles, w);
+    }
+  }
+  __device__ int i0() const { return (it.qlo + n) * BQ; }
+};
 
 __global__ void __launch_bounds__(kThreads, 1)
-rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_qu,
-                  const __grid_constant__ CUtensorMap tm_qv, const __grid_constant__ CUtensorMap tm_do,
-                  const BwdParams p) {
+rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_r16, const __grid_constant__ CUtensorMap tm_qu,
+                    const __grid_constant__ CUtensorMap tm_qv16, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / p.nkt, kt = blockIdx.x % p.nkt;
-  const int h = bh % p.H;
   const KeyTiles tiles(p.m, p.cap, p.head, p.L);
-  const KeyTile x = tiles.get(kt);
-  const int qlo = x.jlog0 >= 0 ? x.jlog0 / BQ : 0;
-  const int NQ = p.nq - qlo;
 
-  const uint32_t bar_kv = sb + KV_BAR, bar_q = bar_kv + 8, bar_sg = bar_kv + 16, bar_p = bar_kv + 24;
-  const uint32_t bar_dp = bar_kv + 32, bar_ds = bar_kv + 40, bar_pair = bar_kv + 48;
-  const uint32_t bar_drain = bar_kv + 56;
-  uint32_t *tmem_slot = (uint32_t *)(smem + KV_BAR + 64);
-  volatile int *abort_flag = (volatile int *)(smem + KV_BAR + 72);
+  const uint32_t b0 = sb + F_BAR;
+  const uint32_t bar_kv = b0, bar_ld = b0 + 8, bar_sg = b0 + 16, bar_p = b0 + 24;
+  const uint32_t bar_dp = b0 + 32, bar_ds = b0 + 40, bar_fin = b0 + 48, bar_fl = b0 + 56;
+  const uint32_t bar_acc = b0 + 64, bar_red = b0 + 72, bar_drain = b0 + 80, bar_x0 = b0 + 88;
+  uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 120);
+  volatile int *abort_flag = (volatile int *)(smem + F_BAR + 124);
+  volatile float *wmax = (volatile float *)(smem + F_BAR + 128);  // [2][8]
   if (threadIdx.x == 0) {
-    mbar_init(bar_kv, 1); mbar_init(bar_q, 1); mbar_init(bar_sg, 1);
+    mbar_init(bar_kv, 1); mbar_init(bar_ld, 1); mbar_init(bar_sg, 1);
     mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_dp, 1);
-    mbar_init(bar_ds, kSoftmaxWarps * 32); mbar_init(bar_pair, 1); mbar_init(bar_drain, 1);
+    mbar_init(bar_ds, kSoftmaxWarps * 32); mbar_init(bar_fin, 1);
+    mbar_init(bar_fl, kSoftmaxWarps * 32); mbar_init(bar_acc, kSoftmaxWarps * 32);
+    mbar_init(bar_red, kSoftmaxWarps); mbar_init(bar_drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == kProducerWarp) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == kProducerWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v); tma_prefetch_desc(&tm_r16);
+      tma_prefetch_desc(&tm_qu); tma_prefetch_desc(&tm_qv16); tma_prefetch_desc(&tm_do);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kProducerWarp) {
+    // ------------------------------------------------ producer / MMA issuer
     if (lane == 0) {
-      int q_issued = 0;
-      auto issue_q = [&](int n) {
-        const int i0 = (qlo + n) * BQ;
-        mbar_expect_tx(bar_q, 3 * 16384 + 32768);
-        tma_load_3d(sb + KV_QU, &tm_qu, 0, i0, bh, bar_q);
-        tma_load_3d(sb + KV_QV, &tm_qv, 0, i0, bh, bar_q);
-        tma_load_3d(sb + KV_DO, &tm_do, 0, i0, bh, bar_q);
-        tma_load_3d(sb + KV_R, &tm_r, 0, i0 - x.jlog0 - (BK - 1), h, bar_q);
-        ++q_issued;
+      bool pend_kv = false, pend_ld = false;
+      int n_kv = 0, n_ld = 0;
+      auto issue_loads = [&](const PairCursor &c) {
+        const FItem &it = c.it;
+        if (c.n == 0) {
+          mbar_expect_tx(bar_kv, 2 * 16384);
+          tma_load_3d(sb + F_K, &tm_k, 0, it.x.phys0, it.bh, bar_kv);
+          tma_load_3d(sb + F_V, &tm_v, 0, it.x.phys0, it.bh, bar_kv);
+          pend_kv = true;
+          ++n_kv;
+        }
+        const int i0 = c.i0();
+        mbar_expect_tx(bar_ld, 3 * 16384 + 32768);
+        tma_load_3d(sb + F_QU, &tm_qu, 0, i0, it.bh, bar_ld);
+        tma_load_3d(sb + F_QV, &tm_qv16, 0, i0, it.bh, bar_ld);
+        tma_load_3d(sb + F_DO, &tm_do, 0, i0, it.bh, bar_ld);
+        tma_load_3d(sb + F_R, &tm_r16, 0, i0 - it.x.jlog0 - (BK - 1), it.h, bar_ld);
+        pend_ld = true;
+        ++n_ld;
       };
       bool ok = true;
-      mbar_expect_tx(bar_kv, 2 * 16384);
-      tma_load_3d(sb + KV_K, &tm_k, 0, x.phys0, bh, bar_kv);
-      tma_load_3d(sb + KV_V, &tm_v, 0, x.phys0, bh, bar_kv);
-      issue_q(0);
-      ok = mbar_wait(bar_kv, 0, abort_flag);
-      for (int n = 0; ok && n < NQ; ++n) {
-        if (!(ok = mbar_wait(bar_q, n & 1, abort_flag))) break;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_S, kdesc(sb + KV_QU, k), kdesc(sb + KV_K, k), IDESC_S, k > 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_G, kdesc(sb + KV_QV, k), kdesc(sb + KV_R, k), IDESC_G, k > 0);
-        mma_commit(bar_sg);
-        if (!(ok = mbar_wait(bar_p, n & 1, abort_flag))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_S, kdesc(sb + KV_DO, k), kdesc(sb + KV_V, k), IDESC_S, k > 0);
-        mma_commit(bar_dp);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_bf16(tmem + TM_A, mndesc(sb + KV_P, k), mndesc(sb + KV_DO, k), IDESC_MN_MN,
-                   (n > 0 || k > 0) ? 1u : 0u);
-        if (!(ok = mbar_wait(bar_ds, n & 1, abort_flag))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_bf16(tmem + TM_B, mndesc(sb + KV_DA, k), mndesc(sb + KV_QU, k), IDESC_MN_MN,
-                   (n > 0 || k > 0) ? 1u : 0u);
-        mma_commit(bar_pair);
-        if (n + 1 < NQ) {
-          if (!(ok = mbar_wait(bar_pair, n & 1, abort_flag))) break;
-          issue_q(n + 1);
+      PairCursor c;
+      c.init(p, tiles);
+      if (c.valid) issue_loads(c);
+      for (int g = 0; ok && c.valid; ++g) {
+        const bool first = c.n == 0;
+        if (first) {
+          if (!(ok = mbar_wait(bar_kv, (c.k & 1), abort_flag))) break;
+          pend_kv = false;
         }
+        if (!(ok = mbar_wait(bar_ld, g & 1, abort_flag))) break;
+        pend_ld = false;
+        // G's columns hold the previous pair's dQ / dR until it was flushed
+        if (g > 0 && !(ok = mbar_wait(bar_fl, (g - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(tmem + TM_S, kdesc(sb + F_QU, k), kdesc(sb + F_K, k), IDESC_S, k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(tmem + TM_G, kdesc(sb + F_QV, k), kdesc(sb + F_R, k), IDESC_G_F16, k > 0);
+        mma_commit(bar_sg);
+        if (!(ok = mbar_wait(bar_p, g & 1, abort_flag))) break;
+        // the first dV of an item overwrites the accumulators: the previous
+        // item's epilogue must have read them
+        if (first && c.k > 0 && !(ok = mbar_wait(bar_acc, (c.k - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(tmem + TM_S, kdesc(sb + F_DO, k), kdesc(sb + F_V, k), IDESC_S, k > 0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // dV += P^T dO
+          mma_bf16(tmem + TM_DV, mndesc(sb + F_PA, k), mndesc(sb + F_DO, k), IDESC_MN_MN,
+                   (!first || k > 0) ? 1u : 0u);
+        mma_commit(bar_dp);
+        if (!(ok = mbar_wait(bar_ds, g & 1, abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // dK += dA^T (Q+u)
+          mma_bf16(tmem + TM_DK, mndesc(sb + F_PA, k), mndesc(sb + F_QU, k), IDESC_MN_MN,
+                   (!first || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // dQc = dA K
+          mma_bf16(tmem + TM_QC, kdesc(sb + F_PA, k), mndesc(sb + F_K, k), IDESC_K_MN, k > 0);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)  // dQp = dG Rband (fp16)
+          mma_bf16(tmem + TM_QP, kdesc(sb + F_DG, k), mndesc(sb + F_R, k), IDESC_K_MN_F16, k > 0);
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)  // dR band = dG^T (Q+v), two 128-distance blocks (fp16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_bf16(tmem + TM_R0 + 64 * mb, mndesc(sb + F_DG + 2 * mb * 16384, k),
+                     mndesc(sb + F_QV, k), IDESC_MN_MN_F16, k > 0);
+        mma_commit(bar_fin);
+        PairCursor nx = c;
+        nx.next(p, tiles);
+        if (nx.valid) {
+          // every operand of this pair has been consumed once its MMAs are done
+          if (!(ok = mbar_wait(bar_fin, g & 1, abort_flag))) break;
+          issue_loads(nx);
+        }
+        c = nx;
       }
       if (!ok) {
+        // wind down: let in-flight copies and MMAs land before TMEM and
+        // shared memory are released
         volatile int no_abort = 0;
-        mbar_wait(bar_kv, 0, &no_abort);
-        if (q_issued > 0) mbar_wait(bar_q, (q_issued - 1) & 1, &no_abort);
+        if (pend_kv) mbar_wait(bar_kv, (n_kv - 1) & 1, &no_abort);
+        if (pend_ld) mbar_wait(bar_ld, (n_ld - 1) & 1, &no_abort);
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0, &no_abort);
         atomicExch(&g_bwd_error, 1);
@@ -244,220 +291,41 @@ rxl_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
     __syncwarp();
   } else {
+    // ----------------------------------------------------- softmax warps
     const int quad = warp & 3, hf = warp >> 2;
     const int ii = quad * 32 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-    bool ok = true;
-    for (int n = 0; n < NQ; ++n) {
-      const int i = (qlo + n) * BQ + ii;
-      const bool row_ok = i < p.L;
-      const size_t row = (size_t)bh * p.L + (row_ok ? i : 0);
-      const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.f;
-      const float Di = row_ok ? p.delta[row] : 0.f;
-      ok = mbar_wait(bar_sg, n & 1, abort_flag);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      tc_fence_after();
-      float y[64];
-      half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, x, p.scale_log2, y);
-#pragma unroll
-      for (int k = 0; k < 64; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
-      store_half_bf16(sb + KV_P, ii, hf, y);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar_p);
-      ok = mbar_wait(bar_dp, n & 1, abort_flag);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t dp[32];
-        tmem_ld32(trow + TM_S + 64 * hf + 32 * cc, dp);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float pv = y[32 * cc + k];
-          y[32 * cc + k] = pv != 0.f ? p.scale * pv * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
-        }
-      }
-      store_half_bf16(sb + KV_DA, ii, hf, y);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar_ds);
-    }
-    if (ok && NQ > 0) ok = mbar_wait(bar_pair, (NQ - 1) & 1, abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      // TMEM lanes of the dV / dK accumulators are key rows; half 0 writes
-      // dV, half 1 dK
-      tc_fence_after();
-      const int kk = ii;
-      const size_t krow = (size_t)bh * p.kv_rows + x.phys0 + (kk < x.nvalid ? kk : 0);
-      __nv_bfloat16 *dst = (hf ? p.dk : p.dv) + krow * DH;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t g[32];
-        tmem_ld32(trow + (hf ? TM_B : TM_A) + 32 * c, g);
-        tmem_wait_ld();
-        if (kk < x.nvalid) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            ((uint4 *)dst)[4 * c + e] = make_uint4(
-                pack_bf16(__uint_as_float(g[8 * e + 0]), __uint_as_float(g[8 * e + 1])),
-                pack_bf16(__uint_as_float(g[8 * e + 2]), __uint_as_float(g[8 * e + 3])),
-                pack_bf16(__uint_as_float(g[8 * e + 4]), __uint_as_float(g[8 * e + 5])),
-                pack_bf16(__uint_as_float(g[8 * e + 6]), __uint_as_float(g[8 * e + 7])));
-        }
-      }
-    } else {
-      atomicExch(&g_bwd_error, 2);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == kProducerWarp) tmem_dealloc(tmem, 512);
-}
-
-// ---------------------------------------------------- dQ / dR / du / dv kernel
-
-constexpr uint32_t Q_QU = 0, Q_QV = 16384, Q_DO = 32768, Q_K = 49152, Q_V = 65536;
-constexpr uint32_t Q_R = 81920, Q_DA = 114688, Q_DG = 147456, Q_X = 212992, Q_BAR = 221184;
-constexpr uint32_t Q_SMEM = Q_BAR + 256 + 1024;  // barriers, TMEM slot, flags, [2][8] warp maxima
-
-__global__ void __launch_bounds__(kThreads, 1)
-rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_qu,
-                 const __grid_constant__ CUtensorMap tm_qv, const __grid_constant__ CUtensorMap tm_do,
-                 const BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = align1024(smem_raw);
-  const uint32_t sb = smem_u32(smem);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = p.nq - 1 - (int)(blockIdx.x % p.nq);
-  const int bh = (int)(blockIdx.x / p.nq);
-  const int h = bh % p.H;
-  const int i0 = qt * BQ;
-  const KeyTiles tiles(p.m, p.cap, p.head, min(i0 + BQ, p.L));
-  const int T = tiles.count();
-
-  const uint32_t bar_q = sb + Q_BAR, bar_k = bar_q + 8, bar_sg = bar_q + 16, bar_p = bar_q + 24;
-  const uint32_t bar_dp = bar_q + 32, bar_ds = bar_q + 40, bar_dr = bar_q + 48, bar_fl = bar_q + 56;
-  const uint32_t bar_drain = bar_q + 64, bar_red = bar_q + 72, bar_x0 = bar_q + 80;  // + 4 pair barriers
-  uint32_t *tmem_slot = (uint32_t *)(smem + Q_BAR + 112);
-  volatile int *abort_flag = (volatile int *)(smem + Q_BAR + 116);
-  if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1); mbar_init(bar_k, 1); mbar_init(bar_sg, 1);
-    mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_dp, 1);
-    mbar_init(bar_ds, kSoftmaxWarps * 32); mbar_init(bar_dr, 1);
-    mbar_init(bar_fl, kSoftmaxWarps * 32); mbar_init(bar_drain, 1);
-    mbar_init(bar_red, kSoftmaxWarps);
-    for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
-  if (warp == kProducerWarp) tmem_alloc(smem_u32(tmem_slot), 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == kProducerWarp) {
-    if (lane == 0) {
-      int k_issued = 0;
-      auto issue_k = [&](int t) {
-        const KeyTile x = tiles.get(t);
-        // (Q+v) is reloaded with every key tile: the previous copy was
-        // converted to fp16 in place
-        mbar_expect_tx(bar_k, 3 * 16384 + 32768);
-        tma_load_3d(sb + Q_K, &tm_k, 0, x.phys0, bh, bar_k);
-        tma_load_3d(sb + Q_V, &tm_v, 0, x.phys0, bh, bar_k);
-        tma_load_3d(sb + Q_R, &tm_r, 0, i0 - x.jlog0 - (BK - 1), h, bar_k);
-        tma_load_3d(sb + Q_QV, &tm_qv, 0, i0, bh, bar_k);
-        ++k_issued;
-      };
-      bool ok = true;
-      mbar_expect_tx(bar_q, 2 * 16384);
-      tma_load_3d(sb + Q_QU, &tm_qu, 0, i0, bh, bar_q);
-      tma_load_3d(sb + Q_DO, &tm_do, 0, i0, bh, bar_q);
-      issue_k(0);
-      ok = mbar_wait(bar_q, 0, abort_flag);
-      for (int t = 0; ok && t < T; ++t) {
-        if (!(ok = mbar_wait(bar_k, t & 1, abort_flag))) break;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_S, kdesc(sb + Q_QU, k), kdesc(sb + Q_K, k), IDESC_S, k > 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_G, kdesc(sb + Q_QV, k), kdesc(sb + Q_R, k), IDESC_G, k > 0);
-        mma_commit(bar_sg);
-        if (!(ok = mbar_wait(bar_p, t & 1, abort_flag))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_S, kdesc(sb + Q_DO, k), kdesc(sb + Q_V, k), IDESC_S, k > 0);
-        mma_commit(bar_dp);
-        if (!(ok = mbar_wait(bar_ds, t & 1, abort_flag))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)   // dQ_content += dA . K
-          mma_bf16(tmem + TM_A, kdesc(sb + Q_DA, k), mndesc(sb + Q_K, k), IDESC_K_MN,
-                   (t > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < 16; ++k)  // dQ_position += dG . Rband (fp16)
-          mma_bf16(tmem + TM_B, kdesc(sb + Q_DG, k), mndesc(sb + Q_R, k), IDESC_K_MN_F16,
-                   (t > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-        for (int mb = 0; mb < 2; ++mb)  // dR band = dG^T . (Q+v), two 128-distance blocks (fp16)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_bf16(tmem + TM_G + 64 * mb, mndesc(sb + Q_DG + 2 * mb * 16384, k),
-                     mndesc(sb + Q_QV, k), IDESC_MN_MN_F16, k > 0);
-        mma_commit(bar_dr);
-        if (!(ok = mbar_wait(bar_fl, t & 1, abort_flag))) break;
-        if (t + 1 < T) issue_k(t + 1);
-      }
-      if (!ok) {
-        volatile int no_abort = 0;
-        mbar_wait(bar_q, 0, &no_abort);
-        if (k_issued > 0) mbar_wait(bar_k, (k_issued - 1) & 1, &no_abort);
-        mma_commit(bar_drain);
-        mbar_wait(bar_drain, 0, &no_abort);
-        atomicExch(&g_bwd_error, 4);
-      }
-    }
-    __syncwarp();
-  } else {
-    const int quad = warp & 3, hf = warp >> 2;
-    const int ii = quad * 32 + lane;
-    const int i = i0 + ii;
-    const bool row_ok = i < p.L;
-    const size_t row = (size_t)bh * p.L + (row_ok ? i : 0);
-    const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.f;
-    const float Di = row_ok ? p.delta[row] : 0.f;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t bar_x = bar_x0 + 8 * quad;
-    volatile float *wmax = (volatile float *)(smem + Q_BAR + 96 + 32);  // [2][8] in the slack
+    const int c0 = ii >> 3;  // first 16-byte chunk of row ii's sheared values
     uint32_t xphase = 0;
-    float sig = 1.0e30f;  // fp16 scale of the position products (power of two, non-increasing)
+    // dG columns outside [ii, ii + 127] are zero for every pair: clear once
+    for (int C = 0; C < 32; ++C)
+      if (hf == 1 ? C < c0 : C > c0 + 16)
+        st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), 0, 0, 0, 0);
+    float dvp = 0.f;  // sum over this warp's rows of dQp, column 32*hf + lane
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const KeyTile x = tiles.get(t);
-      ok = mbar_wait(bar_sg, t & 1, abort_flag) && mbar_wait(bar_k, t & 1, abort_flag);
+    PairCursor c;
+    c.init(p, tiles);
+    for (int g = 0; c.valid; ++g) {
+      const FItem it = c.it;
+      const int i0 = c.i0();
+      const int i = i0 + ii;
+      const bool row_ok = i < p.L;
+      const size_t row = (size_t)it.bh * p.L + (row_ok ? i : 0);
+      const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.f;
+      const float Di = row_ok ? p.delta[row] : 0.f;
+      ok = mbar_wait(bar_sg, g & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      // S and G are done with the bf16 R band and (Q+v): convert them to fp16
-      // for the position-gradient products of this tile pair
-#pragma unroll
-      for (int c = 0; c < 8; ++c) chunk_bf16_to_f16(sb + Q_R + hf * 16384 + sw128_offset(ii, c));
-#pragma unroll
-      for (int c = 0; c < 4; ++c) chunk_bf16_to_f16(sb + Q_QV + sw128_offset(ii, 4 * hf + c));
       float y[64];
-      half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, x, p.scale_log2, y);
+      half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, y);
 #pragma unroll
       for (int k = 0; k < 64; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
+      store_half_bf16(sb + F_PA, ii, hf, y);
+      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_p);
-      ok = mbar_wait(bar_dp, t & 1, abort_flag);
+      ok = mbar_wait(bar_dp, g & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
 #pragma unroll
@@ -471,151 +339,168 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           y[32 * cc + k] = pv != 0.f ? p.scale * pv * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
         }
       }
-      store_half_bf16(sb + Q_DA, ii, hf, y);
-      // CTA-wide max |dA| of this tile pair -> power-of-two fp16 scale
+      // P is no longer read: dP and dV were committed together
+      store_half_bf16(sb + F_PA, ii, hf, y);
+      // CTA-wide max |dA| of this pair -> power-of-two fp16 scale of dG
       float am = 0.f;
 #pragma unroll
       for (int k = 0; k < 64; ++k) am = fmaxf(am, fabsf(y[k]));
       am = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(am)));
       if (lane == 0) {
-        wmax[(t & 1) * 8 + warp] = am;
+        wmax[(g & 1) * 8 + warp] = am;
         mbar_arrive(bar_red);
       }
-      ok = mbar_wait(bar_red, t & 1, abort_flag);  // bounded, unlike a named barrier
+      ok = mbar_wait(bar_red, g & 1, abort_flag);  // bounded, unlike a named barrier
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       am = 0.f;
 #pragma unroll
-      for (int w = 0; w < kSoftmaxWarps; ++w) am = fmaxf(am, wmax[(t & 1) * 8 + w]);
-      if (am > 0.f) {
-        const float want = exp2f(14.f - ceilf(log2f(am)));  // max |scaled dA| <= 2^14
-        if (want < sig) {
-          if (t > 0) {
-            // rescale this half's columns of the fp16-scaled dQ_position accumulator
-            const float f = want / sig;
-            uint32_t g[32];
-            tmem_ld32(trow + TM_B + 32 * hf, g);
-            tmem_wait_ld();
+      for (int w = 0; w < kSoftmaxWarps; ++w) am = fmaxf(am, wmax[(g & 1) * 8 + w]);
+      const float sig = am > 0.f ? exp2f(14.f - ceilf(log2f(am))) : 1.f;  // max |sig dA| <= 2^14
+      // Sheared dG row ii: key jj sits at column ii + 127 - jj. This half's
+      // keys fill columns s .. s+63 (s = ii + 64 - 64 hf) in reverse key
+      // order; z = those values shifted right by s mod 8 = ii mod 8 lines
+      // them up with 16-byte chunks (s >> 3) .. (s >> 3) + 8.
+      {
+        const int r = ii & 7;
+        float z[72];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) g[e] = __float_as_uint(__uint_as_float(g[e]) * f);
-            tmem_st32(trow + TM_B + 32 * hf, g);
-            tmem_wait_st();
-          }
-          sig = want;
+        for (int x = 0; x < 72; ++x) z[x] = x < 64 ? sig * y[63 - (x < 64 ? x : 0)] : 0.f;
+#pragma unroll
+        for (int b = 4; b >= 1; b >>= 1) {
+          const bool take = (r & b) != 0;
+#pragma unroll
+          for (int x = 71; x >= 0; --x) z[x] = take ? (x >= b ? z[x >= b ? x - b : 0] : 0.f) : z[x];
         }
-      }
-      // sheared dG (fp16, scaled by sig): half 1 hands keys 64..95 to half 0
-      const uint32_t xrow = sb + Q_X + ii * 64;
-      if (hf == 1) {
+        const int cbase = c0 + (hf ? 0 : 8);
+        const uint32_t xrow = sb + F_X + ii * 16;
+        if (hf == 1) {
+          // chunk cbase + 8 is shared with the other half: hand it over
+          st_shared_v4(xrow, pack_f16(z[64], z[65]), pack_f16(z[66], z[67]), pack_f16(z[68], z[69]),
+                       pack_f16(z[70], z[71]));
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          st_shared_v4(xrow + 16 * e, pack_f16(sig * y[8 * e + 0], sig * y[8 * e + 1]),
-                       pack_f16(sig * y[8 * e + 2], sig * y[8 * e + 3]),
-                       pack_f16(sig * y[8 * e + 4], sig * y[8 * e + 5]),
-                       pack_f16(sig * y[8 * e + 6], sig * y[8 * e + 7]));
-      }
-      if (!(ok = pair_sync(bar_x, lane, xphase, abort_flag))) break;
-      // column chunks outside [32*quad, 32*quad + 160) are zero for every lane
-      for (int C = 0; C < 8; ++C) {
-        if (hf == 0 ? C < quad : C > quad + 4) {
+          for (int t = 0; t < 8; ++t) {
+            const int C = cbase + t;
+            st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7),
+                         pack_f16(z[8 * t + 0], z[8 * t + 1]), pack_f16(z[8 * t + 2], z[8 * t + 3]),
+                         pack_f16(z[8 * t + 4], z[8 * t + 5]), pack_f16(z[8 * t + 6], z[8 * t + 7]));
+          }
+        } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = 32 * C + 8 * e;
-            st_shared_v4(sb + Q_DG + (col >> 6) * 16384 + sw128_offset(ii, (col & 63) >> 3), 0, 0, 0, 0);
+          for (int t = 1; t < 9; ++t) {
+            const int C = cbase + t;
+            st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7),
+                         pack_f16(z[8 * t + 0], z[8 * t + 1]), pack_f16(z[8 * t + 2], z[8 * t + 3]),
+                         pack_f16(z[8 * t + 4], z[8 * t + 5]), pack_f16(z[8 * t + 6], z[8 * t + 7]));
           }
         }
-      }
-      if (hf == 0) {
-        float xk[32];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint32_t a, b, c, d;
+        if (!(ok = pair_sync(bar_x, lane, xphase, abort_flag))) break;
+        if (hf == 0) {
+          // the two halves' values occupy complementary positions of the
+          // shared chunk (+0 elsewhere): OR merges them exactly
+          uint32_t a, b, cc, d;
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-                       : "r"(xrow + 16 * e));
-          const uint32_t w[4] = {a, b, c, d};
-#pragma unroll
-          for (int f = 0; f < 4; ++f) {
-            const __half2 hv = *reinterpret_cast<const __half2 *>(&w[f]);
-            const float2 fv = __half22float2(hv);
-            xk[8 * e + 2 * f] = fv.x;
-            xk[8 * e + 2 * f + 1] = fv.y;
-          }
+                       : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
+                       : "r"(xrow));
+          const int C = cbase;
+          st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7),
+                       a | pack_f16(z[0], z[1]), b | pack_f16(z[2], z[3]), cc | pack_f16(z[4], z[5]),
+                       d | pack_f16(z[6], z[7]));
         }
-        shear_chunk_lo<2>(sb + Q_DG, ii, quad, lane, y, xk, sig);
-        shear_chunk_lo<3>(sb + Q_DG, ii, quad, lane, y, xk, sig);
-        shear_chunk_lo<4>(sb + Q_DG, ii, quad, lane, y, xk, sig);
-      } else {
-        shear_chunk_hi<0>(sb + Q_DG, ii, quad, lane, y, sig);
-        shear_chunk_hi<1>(sb + Q_DG, ii, quad, lane, y, sig);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_ds);
-      ok = mbar_wait(bar_dr, t & 1, abort_flag);
+      ok = mbar_wait(bar_fin, g & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      // dR rows of this tile pair: TMEM lane = band row, half hf reads block hf
-      const int d0 = i0 - x.jlog0 - (BK - 1);
       {
-        const int d = d0 + 128 * hf + ii;
-        float *dst = p.dr + ((size_t)h * p.kv_rows + (d >= 0 ? d : 0)) * DH;
-        const float f = 1.f / sig;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t g[32];
-          tmem_ld32(trow + TM_G + 64 * hf + 32 * c, g);
+        // flush: dQ rows (this half's 32 columns) and dR rows of block hf
+        const float inv = 1.f / sig;
+        float v[32];
+        {
+          uint32_t qc[32], qp[32];
+          tmem_ld32(trow + TM_QC + 32 * hf, qc);
+          tmem_ld32(trow + TM_QP + 32 * hf, qp);
           tmem_wait_ld();
-          if (d >= 0 && d < p.m + p.L) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(qp[e]) * inv;
+          if (row_ok) {
+            float *dst = p.dq_acc + row * DH + 32 * hf;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              red_add_v4(dst + 32 * c + 4 * e, f * __uint_as_float(g[4 * e]), f * __uint_as_float(g[4 * e + 1]),
-                         f * __uint_as_float(g[4 * e + 2]), f * __uint_as_float(g[4 * e + 3]));
+              red_add_v4(dst + 4 * e, __uint_as_float(qc[4 * e]) + v[4 * e],
+                         __uint_as_float(qc[4 * e + 1]) + v[4 * e + 1],
+                         __uint_as_float(qc[4 * e + 2]) + v[4 * e + 2],
+                         __uint_as_float(qc[4 * e + 3]) + v[4 * e + 3]);
           }
         }
-      }
-      tc_fence_before();
-      mbar_arrive(bar_fl);
-    }
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after();
-      // dQ = content + position parts; du, dv partials = column sums of the
-      // parts. This thread owns columns 32*hf .. 32*hf+31 of its row.
-      float *red = (float *)(smem + Q_DG);  // [2][128][64] fp32, reuses the dG tile
-      uint4 *qrow = (uint4 *)(p.dq + row * DH);
-      uint32_t a[32], b[32];
-      tmem_ld32(trow + TM_A + 32 * hf, a);
-      tmem_ld32(trow + TM_B + 32 * hf, b);
-      tmem_wait_ld();
-      const float f = sig < 1.0e29f ? 1.f / sig : 0.f;  // undo the fp16 scale
+        {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(trow + TM_R0 + 64 * hf, ra);
+          tmem_ld32(trow + TM_R0 + 64 * hf + 32, rb);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar_fl);  // the G columns may take the next pair's logits
+          const int d = i0 - it.x.jlog0 - (BK - 1) + 128 * hf + ii;
+          if (d >= 0 && d < p.m + p.L) {
+            float *dst = p.dr + ((size_t)it.h * p.kv_rows + d) * DH;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) b[e] = __float_as_uint(__uint_as_float(b[e]) * f);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        red[ii * 64 + 32 * hf + e] = __uint_as_float(a[e]);
-        red[128 * 64 + ii * 64 + 32 * hf + e] = __uint_as_float(b[e]);
-      }
-      if (row_ok) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float s8[8];
-#pragma unroll
-          for (int g = 0; g < 8; ++g) s8[g] = __uint_as_float(a[8 * e + g]) + __uint_as_float(b[8 * e + g]);
-          qrow[4 * hf + e] = make_uint4(pack_bf16(s8[0], s8[1]), pack_bf16(s8[2], s8[3]),
-                                        pack_bf16(s8[4], s8[5]), pack_bf16(s8[6], s8[7]));
+            for (int e = 0; e < 8; ++e) {
+              red_add_v4(dst + 4 * e, inv * __uint_as_float(ra[4 * e]), inv * __uint_as_float(ra[4 * e + 1]),
+                         inv * __uint_as_float(ra[4 * e + 2]), inv * __uint_as_float(ra[4 * e + 3]));
+              red_add_v4(dst + 32 + 4 * e, inv * __uint_as_float(rb[4 * e]),
+                         inv * __uint_as_float(rb[4 * e + 1]), inv * __uint_as_float(rb[4 * e + 2]),
+                         inv * __uint_as_float(rb[4 * e + 3]));
+            }
+          }
         }
+        // column sums of dQp over the warp's 32 rows (recursive halving):
+        // afterwards lane l holds column 32*hf + l
+#pragma unroll
+        for (int h2 = 16; h2 >= 1; h2 >>= 1) {
+          const bool upper = (lane & h2) != 0;
+#pragma unroll
+          for (int k = 0; k < h2; ++k) {
+            const float send = upper ? v[k] : v[k + h2];
+            const float keep = upper ? v[k + h2] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, h2);
+          }
+        }
+        dvp += v[0];
       }
-    } else {
-      atomicExch(&g_bwd_error, 8);
+      c.next(p, tiles);
+      if (c.valid && c.n != 0) continue;
+      // ---- end of the item: dV (half 0) and dK (half 1) rows, dv sums
+      {
+        const int kk = ii;
+        const size_t krow = (size_t)it.bh * p.kv_rows + it.x.phys0 + (kk < it.x.nvalid ? kk : 0);
+        __nv_bfloat16 *dst = (hf ? p.dk : p.dv) + krow * DH;
+        uint32_t ga[32], gb[32];
+        tmem_ld32(trow + (hf ? TM_DK : TM_DV), ga);
+        tmem_ld32(trow + (hf ? TM_DK : TM_DV) + 32, gb);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_acc);
+        if (kk < it.x.nvalid) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ((uint4 *)dst)[e] = make_uint4(
+                pack_bf16(__uint_as_float(ga[8 * e + 0]), __uint_as_float(ga[8 * e + 1])),
+                pack_bf16(__uint_as_float(ga[8 * e + 2]), __uint_as_float(ga[8 * e + 3])),
+                pack_bf16(__uint_as_float(ga[8 * e + 4]), __uint_as_float(ga[8 * e + 5])),
+                pack_bf16(__uint_as_float(ga[8 * e + 6]), __uint_as_float(ga[8 * e + 7])));
+            ((uint4 *)dst)[4 + e] = make_uint4(
+                pack_bf16(__uint_as_float(gb[8 * e + 0]), __uint_as_float(gb[8 * e + 1])),
+                pack_bf16(__uint_as_float(gb[8 * e + 2]), __uint_as_float(gb[8 * e + 3])),
+                pack_bf16(__uint_as_float(gb[8 * e + 4]), __uint_as_float(gb[8 * e + 5])),
+                pack_bf16(__uint_as_float(gb[8 * e + 6]), __uint_as_float(gb[8 * e + 7])));
+          }
+        }
+        atomicAdd(p.dv_acc + it.h * DH + 32 * hf + lane, dvp);
+        dvp = 0.f;
+      }
     }
-    asm volatile("bar.sync 1, 256;" ::: "memory");  // the softmax warps only
-    if (ok && threadIdx.x < 128) {
-      const float *red = (const float *)(smem + Q_DG);
-      const int part = threadIdx.x >> 6, col = threadIdx.x & 63;  // (part, column)
-      float acc = 0.f;
-      for (int r = 0; r < BQ; ++r) acc += red[part * 128 * 64 + r * 64 + col];
-      p.duv_part[(((size_t)bh * p.nq + qt) * 2 + part) * DH + col] = acc;
-    }
+    if (!ok) atomicExch(&g_bwd_error, 2);
   }
   tc_fence_before();
   __syncthreads();
@@ -625,18 +510,33 @@ rxl_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
 // ---------------------------------------------------------- small kernels
 
-__global__ void bwd_zero_kernel(float *dr, size_t n_dr, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
-                                int BH, int cap, int m, int head, int kv_rows) {
+// dR, the dQ accumulator and the du/dv sums <- 0; dK/dV rows of ring slots
+// that hold no valid memory <- 0; R16 <- fp16(R) (satfinite).
+__global__ void bwd_zero_kernel(float *dr, size_t n_dr, float *dq_acc, size_t n_dq, float *sums,
+                                int n_sums, __nv_bfloat16 *dk, __nv_bfloat16 *dv, int BH, int cap,
+                                int m, int head, int kv_rows, const __nv_bfloat16 *r, __half *r16,
+                                size_t n_r) {
   const size_t tid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t e = tid; e < n_dr / 4; e += stride) ((float4 *)dr)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-  // dK/dV rows of ring slots that hold no valid memory: 8 x 16 B per row
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (size_t e = tid; e < n_dr / 4; e += stride) ((float4 *)dr)[e] = z4;
+  for (size_t e = tid; e < n_dq / 4; e += stride) ((float4 *)dq_acc)[e] = z4;
+  for (size_t e = tid; e < (size_t)n_sums; e += stride) sums[e] = 0.f;
+  for (size_t e = tid; e < n_r / 8; e += stride) {
+    const uint4 a = ((const uint4 *)r)[e];
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int f = 0; f < 4; ++f)
+      o[f] = pack_f16(__uint_as_float(w[f] << 16), __uint_as_float(w[f] & 0xFFFF0000u));
+    ((uint4 *)r16)[e] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
   const int empty = cap - m;
   const size_t n_rows = (size_t)BH * empty * 8;
   for (size_t e = tid; e < n_rows; e += stride) {
     const int c = (int)(e & 7);
-    const size_t r = e >> 3;
-    const int bh = (int)(r / empty), t = m + (int)(r % empty);  // logical slot t >= m
+    const size_t rr = e >> 3;
+    const int bh = (int)(rr / empty), t = m + (int)(rr % empty);  // logical slot t >= m
     int pr = head + t;
     if (pr >= cap) pr -= cap;
     const size_t off = ((size_t)bh * kv_rows + pr) * DH;
@@ -646,14 +546,14 @@ __global__ void bwd_zero_kernel(float *dr, size_t n_dr, __nv_bfloat16 *dk, __nv_
 }
 
 // Streaming preparation when the forward kept the low part of O: per row,
-// (Q+u) and (Q+v) in bf16 and D_i = dO_i . (o_i + o_lo_i). Eight threads
-// per row, 16 bytes each.
+// (Q+u) in bf16, (Q+v) in fp16 and D_i = dO_i . (o_i + o_lo_i). Eight
+// threads per row, 16 bytes each.
 __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
     long long rows, int L, int H, const __nv_bfloat16 *__restrict__ q,
     const __nv_bfloat16 *__restrict__ u, const __nv_bfloat16 *__restrict__ vb,
     const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ o_lo,
     const __nv_bfloat16 *__restrict__ dout, __nv_bfloat16 *__restrict__ qu,
-    __nv_bfloat16 *__restrict__ qv, float *__restrict__ delta) {
+    __half *__restrict__ qv, float *__restrict__ delta) {
   const int sub = threadIdx.x & 7;
   for (long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 3; row < rows;
        row += ((long long)gridDim.x * blockDim.x) >> 3) {
@@ -675,7 +575,7 @@ __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       a[e] = pack_bf16(lo(qw[e]) + lo(uw[e]), hi(qw[e]) + hi(uw[e]));
-      b[e] = pack_bf16(lo(qw[e]) + lo(vw[e]), hi(qw[e]) + hi(vw[e]));
+      b[e] = pack_f16(lo(qw[e]) + lo(vw[e]), hi(qw[e]) + hi(vw[e]));
       acc += lo(dw[e]) * (lo(ow[e]) + lo(lw[e])) + hi(dw[e]) * (hi(ow[e]) + hi(lw[e]));
     }
     ((uint4 *)(qu + off))[sub] = make_uint4(a[0], a[1], a[2], a[3]);
@@ -686,13 +586,45 @@ __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
   }
 }
 
-__global__ void bwd_finish_kernel(const float *duv_part, float *du, float *dvb, int B, int H, int nq) {
-  const int h = blockIdx.x, part = threadIdx.x >> 6, c = threadIdx.x & 63;
-  float acc = 0.f;
-  for (int b = 0; b < B; ++b)
-    for (int q = 0; q < nq; ++q)
-      acc += duv_part[((((size_t)b * H + h) * nq + q) * 2 + part) * DH + c];
-  (part ? dvb : du)[h * DH + c] = acc;
+// dq = bf16(dQ accumulator); per-head column sums of dQ into colsum[H][64].
+// Block (bh, chunk) covers 128 rows of one (b, h) plane: 8 threads per row,
+// 8 columns each.
+__global__ void __launch_bounds__(256) bwd_dq_finish_kernel(const float *__restrict__ dq_acc,
+                                                            __nv_bfloat16 *__restrict__ dq,
+                                                            float *colsum, int L, int H,
+                                                            int chunks) {
+  __shared__ float part[32][65];
+  const int bh = blockIdx.x / chunks, ch = blockIdx.x % chunks;
+  const int sub = threadIdx.x & 7, slot = threadIdx.x >> 3;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int r_end = min(L, (ch + 1) * 128);
+  for (int i = ch * 128 + slot; i < r_end; i += 32) {
+    const size_t off = ((size_t)bh * L + i) * DH + 8 * sub;
+    const float4 a = *(const float4 *)(dq_acc + off);
+    const float4 b = *(const float4 *)(dq_acc + off + 4);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    *(uint4 *)(dq + off) = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
+                                      pack_bf16(b.z, b.w));
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[slot][8 * sub + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    float s = 0.f;
+    for (int k = 0; k < 32; ++k) s += part[k][threadIdx.x];
+    atomicAdd(colsum + (bh % H) * DH + threadIdx.x, s);
+  }
+}
+
+// du = (column sums of dQ) - dv; dv = column sums of the position part.
+__global__ void bwd_duv_kernel(const float *colsum, const float *dv_acc, float *du, float *dvb,
+                               int n) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < n) {
+    dvb[e] = dv_acc[e];
+    du[e] = colsum[e] - dv_acc[e];
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -732,15 +664,18 @@ size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
+// Workspace: D [rows] f32 | (Q+u) [rows][64] bf16 | (Q+v) [rows][64] fp16 |
+// R fp16 [H][kv_rows][64] | dQ accumulator [rows][64] f32 | dv, colsum [H][64] f32
 BwdWorkspace tc_bwd_workspace(const AttnShape &s) {
   const size_t rows = (size_t)s.B * s.H * s.L;
-  const int nq = (s.L + BQ - 1) / BQ;
   BwdWorkspace w;
-  w.d_off = 0;                                              // D [B,H,L] f32
-  w.dqu_off = up256(rows * 4);                              // (Q+u) bf16
-  w.dqv_off = w.dqu_off + up256(rows * DH * 2);             // (Q+v) bf16
-  const size_t duv_off = w.dqv_off + up256(rows * DH * 2);  // du/dv partials
-  w.total = duv_off + up256((size_t)s.B * s.H * nq * 2 * DH * 4);
+  w.d_off = 0;
+  w.dqu_off = up256(rows * 4);
+  w.dqv_off = w.dqu_off + up256(rows * DH * 2);
+  const size_t r16_off = w.dqv_off + up256(rows * DH * 2);
+  const size_t dq_off = r16_off + up256((size_t)s.H * s.kv_rows * DH * 2);
+  const size_t sums_off = dq_off + up256(rows * DH * 4);
+  w.total = sums_off + up256((size_t)2 * s.H * DH * 4);
   return w;
 }
 
@@ -750,41 +685,46 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
                           const void *dout, void *dq, void *dk, void *dv, float *dr, float *du,
                           float *dvb, void *ws, cudaStream_t st, int *launches) {
   const BwdWorkspace w = tc_bwd_workspace(s);
+  const size_t rows = (size_t)s.B * s.H * s.L;
   float *delta = (float *)((char *)ws + w.d_off);
   void *qu = (char *)ws + w.dqu_off;
   void *qv = (char *)ws + w.dqv_off;
-  float *duv = (float *)((char *)ws + w.dqv_off + up256((size_t)s.B * s.H * s.L * DH * 2));
+  const size_t r16_off = w.dqv_off + up256(rows * DH * 2);
+  __half *r16 = (__half *)((char *)ws + r16_off);
+  const size_t dq_off = r16_off + up256((size_t)s.H * s.kv_rows * DH * 2);
+  float *dq_acc = (float *)((char *)ws + dq_off);
+  float *sums = (float *)((char *)ws + dq_off + up256(rows * DH * 4));  // dv_acc | colsum
   const int nq = (s.L + BQ - 1) / BQ;
 
-  CUtensorMap tk, tv, tr, tqu, tqv, tdo;
+  CUtensorMap tk, tv, tr16, tqu, tqv, tdo;
   if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
-      !make_map(&tr, r, s.H, s.kv_rows, NB) || !make_map(&tqu, qu, s.B * s.H, s.L, BQ) ||
+      !make_map(&tr16, r16, s.H, s.kv_rows, NB) || !make_map(&tqu, qu, s.B * s.H, s.L, BQ) ||
       !make_map(&tqv, qv, s.B * s.H, s.L, BQ) || !make_map(&tdo, dout, s.B * s.H, s.L, BQ))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(rxl_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(rxl_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM);
+    attr_err = cudaFuncSetAttribute(rxl_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    F_SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
 
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const size_t n_dr = (size_t)s.H * s.kv_rows * DH;
-  bwd_zero_kernel<<<sms * 4, 256, 0, st>>>(dr, n_dr, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv,
-                                           s.B * s.H, s.cap, s.m, s.head, s.kv_rows);
+  bwd_zero_kernel<<<sms * 4, 256, 0, st>>>(dr, (size_t)s.H * s.kv_rows * DH, dq_acc, rows * DH, sums,
+                                           2 * s.H * DH, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv,
+                                           s.B * s.H, s.cap, s.m, s.head, s.kv_rows,
+                                           (const __nv_bfloat16 *)r, r16,
+                                           (size_t)s.H * s.kv_rows * DH);
   ++*launches;
   if (o_lo) {
-    const long long rows = (long long)s.B * s.H * s.L;
-    long long blocks = (rows * 8 + 255) / 256;
+    long long blocks = ((long long)rows * 8 + 255) / 256;
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
     bwd_light_prep_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-        rows, s.L, s.H, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)u,
+        (long long)rows, s.L, s.H, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)u,
         (const __nv_bfloat16 *)vb, (const __nv_bfloat16 *)o, (const __nv_bfloat16 *)o_lo,
-        (const __nv_bfloat16 *)dout, (__nv_bfloat16 *)qu, (__nv_bfloat16 *)qv, delta);
+        (const __nv_bfloat16 *)dout, (__nv_bfloat16 *)qu, (__half *)qv, delta);
     ++*launches;
   } else {
     cudaError_t e = launch_tc_bwd_prep(s, q, k, v, r, u, vb, dout, delta, qu, qv, st, launches);
@@ -798,18 +738,22 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
     // key tiles per (b,h): ring runs A and B, then the current rows
     const int lenA = s.m < s.cap - s.head ? s.m : s.cap - s.head;
     const int lenB = s.m - lenA;
-    p.nkt = (lenA + BK - 1) / BK + (lenB + BK - 1) / BK + (s.L + BK - 1) / BK;
+    const int nkt = (lenA + BK - 1) / BK + (lenB + BK - 1) / BK + (s.L + BK - 1) / BK;
+    p.nitems = s.B * s.H * nkt;
   }
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;
   p.lse = lse; p.delta = delta;
-  p.dq = (__nv_bfloat16 *)dq; p.dk = (__nv_bfloat16 *)dk; p.dv = (__nv_bfloat16 *)dv;
-  p.dr = dr; p.duv_part = duv;
-  rxl_bwd_kv_kernel<<<(unsigned)(s.B * s.H * p.nkt), kThreads, KV_SMEM, st>>>(tk, tv, tr, tqu, tqv, tdo, p);
+  p.dk = (__nv_bfloat16 *)dk; p.dv = (__nv_bfloat16 *)dv;
+  p.dq_acc = dq_acc; p.dr = dr; p.dv_acc = sums;
+  const unsigned grid = (unsigned)(p.nitems < sms ? p.nitems : sms);
+  rxl_bwd_main_kernel<<<grid, kThreads, F_SMEM, st>>>(tk, tv, tr16, tqu, tqv, tdo, p);
   ++*launches;
-  rxl_bwd_q_kernel<<<(unsigned)(s.B * s.H * nq), kThreads, Q_SMEM, st>>>(tk, tv, tr, tqu, tqv, tdo, p);
+  const int chunks = (s.L + 127) / 128;
+  bwd_dq_finish_kernel<<<(unsigned)(s.B * s.H * chunks), 256, 0, st>>>(dq_acc, (__nv_bfloat16 *)dq,
+                                                                        sums + s.H * DH, s.L, s.H, chunks);
   ++*launches;
-  bwd_finish_kernel<<<s.H, 128, 0, st>>>(duv, du, dvb, s.B, s.H, nq);
+  bwd_duv_kernel<<<(s.H * DH + 255) / 256, 256, 0, st>>>(sums + s.H * DH, sums, du, dvb, s.H * DH);
   ++*launches;
   return cudaGetLastError();
 }

@@ -83,7 +83,8 @@ struct Params {
   // (Q+u), (Q+v) rows (unscaled) out
   const __nv_bfloat16 *dout;
   float *delta;
-  __nv_bfloat16 *qu_out, *qv_out;
+  __nv_bfloat16 *qu_out;
+  __half *qv_out;  // (Q+v) rows in fp16 for the backward's position products
 };
 
 constexpr int kFwd = 0, kPrep = 1;
@@ -152,7 +153,7 @@ struct Cursor {
 
 // (Q+u)*c and (Q+v)*c in bf16, c = scale*log2(e), as 128-byte swizzled
 // K-major tiles for the item's query rows; the row's two warps split its 8
-// chunks. In kPrep mode the unscaled rows also go to global memory.
+// chunks. In kPrep mode the unscaled rows also go to global memory ((Q+v) in fp16).
 template <int MODE>
 __device__ __forceinline__ void q_prep(const Params &p, const Item &it, uint32_t sbase, int quad,
                                        int hf, int lane) {
@@ -179,7 +180,7 @@ __device__ __forceinline__ void q_prep(const Params &p, const Item &it, uint32_t
       a[e] = pack_bf16((q0 + u0) * c2, (q1 + u1) * c2);
       b[e] = pack_bf16((q0 + v0) * c2, (q1 + v1) * c2);
       a1[e] = pack_bf16(q0 + u0, q1 + u1);
-      b1[e] = pack_bf16(q0 + v0, q1 + v1);
+      b1[e] = pack_f16(q0 + v0, q1 + v1);
     }
     st_shared_v4(sbase + SM_QU + sw128_offset(ii, c), a[0], a[1], a[2], a[3]);
     st_shared_v4(sbase + SM_QV + sw128_offset(ii, c), b[0], b[1], b[2], b[3]);
@@ -582,7 +583,7 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   if (attr_err != cudaSuccess) return attr_err;
   Params p;
   p.dout = (const __nv_bfloat16 *)dout; p.delta = delta;
-  p.qu_out = (__nv_bfloat16 *)qu_out; p.qv_out = (__nv_bfloat16 *)qv_out;
+  p.qu_out = (__nv_bfloat16 *)qu_out; p.qv_out = (__half *)qv_out;
   p.B = s.B; p.H = s.H; p.L = s.L; p.cap = s.cap; p.m = s.m; p.head = s.head;
   p.nq = (s.L + BQ - 1) / BQ;
   p.scale_log2 = s.scale * 1.4426950408889634f;

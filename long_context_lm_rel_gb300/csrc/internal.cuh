@@ -52,7 +52,7 @@ cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, cons
 cudaError_t tc_fwd_read_error(int *flag);
 
 // Forward kernel in backward-preparation mode: D = dO.O (fp32 O) and the
-// bf16 (Q+u), (Q+v) rows.
+// (Q+u) rows in bf16 and (Q+v) rows in fp16.
 cudaError_t launch_tc_bwd_prep(const AttnShape &s, const void *q, const void *k, const void *v,
                                const void *r, const void *u, const void *vb, const void *dout,
                                float *delta, void *qu_out, void *qv_out, cudaStream_t st,

@@ -19,8 +19,9 @@
 
 namespace {
 
-// 16 MiB: enough for B*H*L up to about 63,000 query rows (the backward needs
-// about 260 bytes of scratch per query row).
+// 16 MiB: enough for B*H*L up to about 32,000 query rows (the backward needs
+// about 520 bytes of scratch per query row, plus 128 bytes per head and K/V
+// row for an fp16 copy of R).
 constexpr size_t kScratchBytes = 16u << 20;
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
