@@ -23,14 +23,16 @@
 //              dP = dO V^T, dV += P^T dO         -> dA, sheared dG
 //              dK += dA^T (Q+u), dQc = dA K, dQp = dG Rband, dRband = dG^T (Q+v)
 //            dV, dK stay in TMEM for the whole item; the pair's dQc + dQp
-//            and its two 128-distance dR blocks are added into fp32 global
-//            accumulators (vector reductions). The column sums of dQp over
+//            and its two 128-distance dR blocks are staged in fp32 in the
+//            shared buffers its MMAs no longer need and added into fp32
+//            global accumulators by TMA tensor reductions, which run while the
+//            next pair proceeds. The column sums of dQp over
 //            the rows give dv; du = (column sums of dQ) - dv.
 //            The position products run in fp16 with dG scaled by a power of
 //            two chosen per pair from max |dA|: R rows are several times
 //            larger than K rows, and bf16 rounding of dA in that term alone
 //            can exceed 1% of max|dQ| on short contexts.
-//   finish : dQ -> bf16 with per-head column sums; then du, dv
+//   finish : dQ -> bf16 with per-head column sums; then dR copied out, du, dv
 #include <math.h>
 
 #include <mutex>
@@ -62,10 +64,13 @@ struct BwdParams {
   float scale, scale_log2;
   const float *lse, *delta;
   __nv_bfloat16 *dk, *dv;
-  float *dq_acc;  // [B*H][L][64], zeroed
-  float *dr;      // [H][kv_rows][64], zeroed
   float *dv_acc;  // [H][64] column sums of the position part of dQ, zeroed
 };
+
+// dR accumulates in [H][kDrPad + kv_rows][64] fp32 with kDrPad leading rows,
+// so that every 32-row box of a band starts at a non-negative row (the bands
+// start at distance >= -127; their rows below 0 only ever receive zeros).
+constexpr int kDrPad = 128;
 
 // K-major operand: 128-byte swizzled [rows][64] tile, k-step kk of 16 elements.
 __device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk) {
@@ -156,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_r16, const __grid_constant__ CUtensorMap tm_qu,
                     const __grid_constant__ CUtensorMap tm_qv16, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dr,
                     const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -185,6 +191,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     if (lane == 0) {
       tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v); tma_prefetch_desc(&tm_r16);
       tma_prefetch_desc(&tm_qu); tma_prefetch_desc(&tm_qv16); tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_dq); tma_prefetch_desc(&tm_dr);
     }
   }
   tc_fence_before();
@@ -298,10 +305,6 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const uint32_t bar_x = bar_x0 + 8 * quad;
     const int c0 = ii >> 3;  // first 16-byte chunk of row ii's sheared values
     uint32_t xphase = 0;
-    // dG columns outside [ii, ii + 127] are zero for every pair: clear once
-    for (int C = 0; C < 32; ++C)
-      if (hf == 1 ? C < c0 : C > c0 + 16)
-        st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), 0, 0, 0, 0);
     float dvp = 0.f;  // sum over this warp's rows of dQp, column 32*hf + lane
     bool ok = true;
     PairCursor c;
@@ -321,6 +324,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, y);
 #pragma unroll
       for (int k = 0; k < 64; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
+      // this warp's rows of the P buffer held its dQ staging of the previous pair
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
       store_half_bf16(sb + F_PA, ii, hf, y);
       fence_proxy_async_smem();
       tc_fence_before();
@@ -373,6 +379,17 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         const int cbase = c0 + (hf ? 0 : 8);
         const uint32_t xrow = sb + F_X + ii * 16;
+        // the quadrant's dG rows held both warps' dR staging of the previous
+        // pair (each warp waited for its own reads before its P store)
+        if (!(ok = pair_sync(bar_x, lane, xphase, abort_flag))) break;
+        // columns outside [ii, ii + 127] are zero (staging overwrote them)
+        if (hf == 1) {
+          for (int C = 0; C < 15; ++C)
+            if (C < c0) st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), 0, 0, 0, 0);
+        } else {
+          for (int C = 17; C < 32; ++C)
+            if (C > c0 + 16) st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), 0, 0, 0, 0);
+        }
         if (hf == 1) {
           // chunk cbase + 8 is shared with the other half: hand it over
           st_shared_v4(xrow, pack_f16(z[64], z[65]), pack_f16(z[66], z[67]), pack_f16(z[68], z[69]),
@@ -414,7 +431,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       {
-        // flush: dQ rows (this half's 32 columns) and dR rows of block hf
+        // flush: this half's 32 dQ columns of row ii and row ii of dR block
+        // hf, staged in fp32 (128-byte swizzled 32-column boxes) in the P/dA
+        // and dG buffers, then added into the accumulators by TMA
         const float inv = 1.f / sig;
         float v[32];
         {
@@ -424,15 +443,13 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(qp[e]) * inv;
-          if (row_ok) {
-            float *dst = p.dq_acc + row * DH + 32 * hf;
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              red_add_v4(dst + 4 * e, __uint_as_float(qc[4 * e]) + v[4 * e],
-                         __uint_as_float(qc[4 * e + 1]) + v[4 * e + 1],
-                         __uint_as_float(qc[4 * e + 2]) + v[4 * e + 2],
-                         __uint_as_float(qc[4 * e + 3]) + v[4 * e + 3]);
-          }
+          for (int e = 0; e < 8; ++e)
+            st_shared_v4(sb + F_PA + hf * 16384 + sw128_offset(ii, e),
+                         __float_as_uint(__uint_as_float(qc[4 * e]) + v[4 * e]),
+                         __float_as_uint(__uint_as_float(qc[4 * e + 1]) + v[4 * e + 1]),
+                         __float_as_uint(__uint_as_float(qc[4 * e + 2]) + v[4 * e + 2]),
+                         __float_as_uint(__uint_as_float(qc[4 * e + 3]) + v[4 * e + 3]));
         }
         {
           uint32_t ra[32], rb[32];
@@ -441,18 +458,32 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar_fl);  // the G columns may take the next pair's logits
-          const int d = i0 - it.x.jlog0 - (BK - 1) + 128 * hf + ii;
-          if (d >= 0 && d < p.m + p.L) {
-            float *dst = p.dr + ((size_t)it.h * p.kv_rows + d) * DH;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              red_add_v4(dst + 4 * e, inv * __uint_as_float(ra[4 * e]), inv * __uint_as_float(ra[4 * e + 1]),
-                         inv * __uint_as_float(ra[4 * e + 2]), inv * __uint_as_float(ra[4 * e + 3]));
-              red_add_v4(dst + 32 + 4 * e, inv * __uint_as_float(rb[4 * e]),
-                         inv * __uint_as_float(rb[4 * e + 1]), inv * __uint_as_float(rb[4 * e + 2]),
-                         inv * __uint_as_float(rb[4 * e + 3]));
-            }
+          for (int e = 0; e < 8; ++e) {
+            st_shared_v4(sb + F_DG + 2 * hf * 16384 + sw128_offset(ii, e),
+                         __float_as_uint(inv * __uint_as_float(ra[4 * e])),
+                         __float_as_uint(inv * __uint_as_float(ra[4 * e + 1])),
+                         __float_as_uint(inv * __uint_as_float(ra[4 * e + 2])),
+                         __float_as_uint(inv * __uint_as_float(ra[4 * e + 3])));
+            st_shared_v4(sb + F_DG + (2 * hf + 1) * 16384 + sw128_offset(ii, e),
+                         __float_as_uint(inv * __uint_as_float(rb[4 * e])),
+                         __float_as_uint(inv * __uint_as_float(rb[4 * e + 1])),
+                         __float_as_uint(inv * __uint_as_float(rb[4 * e + 2])),
+                         __float_as_uint(inv * __uint_as_float(rb[4 * e + 3])));
           }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int qrow = i0 + 32 * quad;
+          const int drow = kDrPad + i0 - it.x.jlog0 - (BK - 1) + 128 * hf + 32 * quad;  // >= 1
+          if (qrow < p.L)
+            tma_reduce_add_3d(&tm_dq, 32 * hf, qrow, it.bh, sb + F_PA + hf * 16384 + quad * 4096);
+          if (drow < kDrPad + p.kv_rows) {
+            tma_reduce_add_3d(&tm_dr, 0, drow, it.h, sb + F_DG + 2 * hf * 16384 + quad * 4096);
+            tma_reduce_add_3d(&tm_dr, 32, drow, it.h, sb + F_DG + (2 * hf + 1) * 16384 + quad * 4096);
+          }
+          bulk_commit();
         }
         // column sums of dQp over the warp's 32 rows (recursive halving):
         // afterwards lane l holds column 32*hf + l
@@ -501,6 +532,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
     }
     if (!ok) atomicExch(&g_bwd_error, 2);
+    // the TMA reductions must be complete before shared memory goes away
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -510,8 +544,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
 // ---------------------------------------------------------- small kernels
 
-// dR, the dQ accumulator and the du/dv sums <- 0; dK/dV rows of ring slots
-// that hold no valid memory <- 0; R16 <- fp16(R) (satfinite).
+// The dR and dQ accumulators and the du/dv sums <- 0; dK/dV rows of ring
+// slots that hold no valid memory <- 0; R16 <- fp16(R) (satfinite).
 __global__ void bwd_zero_kernel(float *dr, size_t n_dr, float *dq_acc, size_t n_dq, float *sums,
                                 int n_sums, __nv_bfloat16 *dk, __nv_bfloat16 *dv, int BH, int cap,
                                 int m, int head, int kv_rows, const __nv_bfloat16 *r, __half *r16,
@@ -617,13 +651,20 @@ __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(const float *__restr
   }
 }
 
-// du = (column sums of dQ) - dv; dv = column sums of the position part.
-__global__ void bwd_duv_kernel(const float *colsum, const float *dv_acc, float *du, float *dvb,
-                               int n) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e < n) {
+// dR rows out of the padded accumulator; du = (column sums of dQ) - dv,
+// dv = column sums of the position part.
+__global__ void bwd_tail_kernel(const float *colsum, const float *dv_acc, float *du, float *dvb,
+                                int n, const float *dr_acc, float *dr, int H, int kv_rows) {
+  const size_t tid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t e = tid; e < (size_t)n; e += stride) {
     dvb[e] = dv_acc[e];
     du[e] = colsum[e] - dv_acc[e];
+  }
+  const size_t per_h = (size_t)kv_rows * DH / 4;
+  for (size_t e = tid; e < (size_t)H * per_h; e += stride) {
+    const size_t h = e / per_h, o = e % per_h;
+    ((float4 *)dr)[e] = ((const float4 *)(dr_acc + (h * (kv_rows + kDrPad) + kDrPad) * DH))[o];
   }
 }
 
@@ -660,12 +701,27 @@ bool make_map(CUtensorMap *m, const void *base, int planes, int rows, int box_ro
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [planes][rows][64] with 32-row x 32-column boxes, 128-byte swizzle
+// (the reduction targets of the main kernel).
+bool make_map_f32(CUtensorMap *m, const void *base, int planes, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {256, (cuuint64_t)rows * 256};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
 // Workspace: D [rows] f32 | (Q+u) [rows][64] bf16 | (Q+v) [rows][64] fp16 |
-// R fp16 [H][kv_rows][64] | dQ accumulator [rows][64] f32 | dv, colsum [H][64] f32
+// R fp16 [H][kv_rows][64] | dQ accumulator [rows][64] f32 | dv, colsum [H][64] f32 |
+// dR accumulator [H][kDrPad + kv_rows][64] f32
 BwdWorkspace tc_bwd_workspace(const AttnShape &s) {
   const size_t rows = (size_t)s.B * s.H * s.L;
   BwdWorkspace w;
@@ -675,7 +731,8 @@ BwdWorkspace tc_bwd_workspace(const AttnShape &s) {
   const size_t r16_off = w.dqv_off + up256(rows * DH * 2);
   const size_t dq_off = r16_off + up256((size_t)s.H * s.kv_rows * DH * 2);
   const size_t sums_off = dq_off + up256(rows * DH * 4);
-  w.total = sums_off + up256((size_t)2 * s.H * DH * 4);
+  const size_t dr_off = sums_off + up256((size_t)2 * s.H * DH * 4);
+  w.total = dr_off + up256((size_t)s.H * (kDrPad + s.kv_rows) * DH * 4);
   return w;
 }
 
@@ -694,12 +751,16 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   const size_t dq_off = r16_off + up256((size_t)s.H * s.kv_rows * DH * 2);
   float *dq_acc = (float *)((char *)ws + dq_off);
   float *sums = (float *)((char *)ws + dq_off + up256(rows * DH * 4));  // dv_acc | colsum
+  float *dr_acc = (float *)((char *)sums + up256((size_t)2 * s.H * DH * 4));
+  const size_t n_dr_acc = (size_t)s.H * (kDrPad + s.kv_rows) * DH;
   const int nq = (s.L + BQ - 1) / BQ;
 
-  CUtensorMap tk, tv, tr16, tqu, tqv, tdo;
+  CUtensorMap tk, tv, tr16, tqu, tqv, tdo, tdq, tdr;
   if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
       !make_map(&tr16, r16, s.H, s.kv_rows, NB) || !make_map(&tqu, qu, s.B * s.H, s.L, BQ) ||
-      !make_map(&tqv, qv, s.B * s.H, s.L, BQ) || !make_map(&tdo, dout, s.B * s.H, s.L, BQ))
+      !make_map(&tqv, qv, s.B * s.H, s.L, BQ) || !make_map(&tdo, dout, s.B * s.H, s.L, BQ) ||
+      !make_map_f32(&tdq, dq_acc, s.B * s.H, s.L) ||
+      !make_map_f32(&tdr, dr_acc, s.H, kDrPad + s.kv_rows))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -712,7 +773,7 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  bwd_zero_kernel<<<sms * 4, 256, 0, st>>>(dr, (size_t)s.H * s.kv_rows * DH, dq_acc, rows * DH, sums,
+  bwd_zero_kernel<<<sms * 4, 256, 0, st>>>(dr_acc, n_dr_acc, dq_acc, rows * DH, sums,
                                            2 * s.H * DH, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv,
                                            s.B * s.H, s.cap, s.m, s.head, s.kv_rows,
                                            (const __nv_bfloat16 *)r, r16,
@@ -745,15 +806,16 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   p.scale_log2 = s.scale * kLog2e;
   p.lse = lse; p.delta = delta;
   p.dk = (__nv_bfloat16 *)dk; p.dv = (__nv_bfloat16 *)dv;
-  p.dq_acc = dq_acc; p.dr = dr; p.dv_acc = sums;
+  p.dv_acc = sums;
   const unsigned grid = (unsigned)(p.nitems < sms ? p.nitems : sms);
-  rxl_bwd_main_kernel<<<grid, kThreads, F_SMEM, st>>>(tk, tv, tr16, tqu, tqv, tdo, p);
+  rxl_bwd_main_kernel<<<grid, kThreads, F_SMEM, st>>>(tk, tv, tr16, tqu, tqv, tdo, tdq, tdr, p);
   ++*launches;
   const int chunks = (s.L + 127) / 128;
   bwd_dq_finish_kernel<<<(unsigned)(s.B * s.H * chunks), 256, 0, st>>>(dq_acc, (__nv_bfloat16 *)dq,
                                                                         sums + s.H * DH, s.L, s.H, chunks);
   ++*launches;
-  bwd_duv_kernel<<<(s.H * DH + 255) / 256, 256, 0, st>>>(sums + s.H * DH, sums, du, dvb, s.H * DH);
+  bwd_tail_kernel<<<sms * 2, 256, 0, st>>>(sums + s.H * DH, sums, du, dvb, s.H * DH, dr_acc, dr, s.H,
+                                           s.kv_rows);
   ++*launches;
   return cudaGetLastError();
 }
