@@ -25,8 +25,8 @@
 //            dV, dK stay in TMEM for the whole item; the pair's dQc + dQp
 //            and its two 128-distance dR blocks are staged in fp32 in the
 //            shared buffers its MMAs no longer need and added into fp32
-//            global accumulators by TMA tensor reductions, which run while the
-//            next pair proceeds. The column sums of dQp over
+//            global accumulators by TMA tensor reductions, issued by a warp of
+//            their own while the next pair proceeds. The column sums of dQp over
 //            the rows give dv; du = (column sums of dQ) - dv.
 //            The position products run in fp16 with dG scaled by a power of
 //            two chosen per pair from max |dA|: R rows are several times
@@ -47,8 +47,9 @@ using namespace sm103;
 using namespace tc;
 
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each owning 64 of a row's keys
-constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
-constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kProducerWarp = kSoftmaxWarps;   // TMA loads and MMA issue
+constexpr int kStoreWarp = kSoftmaxWarps + 1;  // TMA reductions of the staged dQ / dR rows
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
 constexpr uint32_t IDESC_G_F16 = idesc_f16(128, 256, false, false);
 constexpr uint32_t IDESC_MN_MN = idesc_bf16(128, 64, true, true);   // A^T . B, both d/row-major tiles
@@ -173,9 +174,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const uint32_t bar_kv = b0, bar_ld = b0 + 8, bar_sg = b0 + 16, bar_p = b0 + 24;
   const uint32_t bar_dp = b0 + 32, bar_ds = b0 + 40, bar_fin = b0 + 48, bar_fl = b0 + 56;
   const uint32_t bar_acc = b0 + 64, bar_red = b0 + 72, bar_drain = b0 + 80, bar_x0 = b0 + 88;
-  uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 120);
-  volatile int *abort_flag = (volatile int *)(smem + F_BAR + 124);
-  volatile float *wmax = (volatile float *)(smem + F_BAR + 128);  // [2][8]
+  const uint32_t bar_staged = b0 + 120;  // each softmax warp staged its rows of a pair (8)
+  const uint32_t bar_sfree = b0 + 128;   // the staging of a pair has been read (1)
+  uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 136);
+  volatile int *abort_flag = (volatile int *)(smem + F_BAR + 140);
+  volatile float *wmax = (volatile float *)(smem + F_BAR + 144);  // [2][8]
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1); mbar_init(bar_ld, 1); mbar_init(bar_sg, 1);
     mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_dp, 1);
@@ -183,6 +186,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     mbar_init(bar_fl, kSoftmaxWarps * 32); mbar_init(bar_acc, kSoftmaxWarps * 32);
     mbar_init(bar_red, kSoftmaxWarps); mbar_init(bar_drain, 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
+    mbar_init(bar_staged, kSoftmaxWarps);
+    mbar_init(bar_sfree, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -297,6 +302,39 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
     }
     __syncwarp();
+  } else if (warp == kStoreWarp) {
+    // --------------------------------------------------- reduction issuer
+    if (lane == 0) {
+      bool ok = true;
+      PairCursor c;
+      c.init(p, tiles);
+      for (int g = 0; c.valid; ++g) {
+        if (!(ok = mbar_wait(bar_staged, g & 1, abort_flag))) break;
+        const int i0 = c.i0();
+        const int d0 = kDrPad + i0 - c.it.x.jlog0 - (BK - 1);  // >= 1
+#pragma unroll 1
+        for (int w = 0; w < kSoftmaxWarps; ++w) {
+          // warp (quad, hf) staged its dQ box in the P/dA buffer and its dR
+          // block-hf rows in dG atoms 2hf, 2hf+1
+          const int quad = w & 3, hf = w >> 2;
+          const int qrow = i0 + 32 * quad, drow = d0 + 128 * hf + 32 * quad;
+          if (qrow < p.L)
+            tma_reduce_add_3d(&tm_dq, 32 * hf, qrow, c.it.bh, sb + F_PA + hf * 16384 + quad * 4096);
+          if (drow < kDrPad + p.kv_rows) {
+            tma_reduce_add_3d(&tm_dr, 0, drow, c.it.h, sb + F_DG + 2 * hf * 16384 + quad * 4096);
+            tma_reduce_add_3d(&tm_dr, 32, drow, c.it.h, sb + F_DG + (2 * hf + 1) * 16384 + quad * 4096);
+          }
+        }
+        bulk_commit();
+        bulk_wait_read();
+        mbar_arrive(bar_sfree);
+        c.next(p, tiles);
+      }
+      // the reductions must be complete before shared memory goes away
+      bulk_wait_all();
+      if (!ok) atomicExch(&g_bwd_error, 4);
+    }
+    __syncwarp();
   } else {
     // ----------------------------------------------------- softmax warps
     const int quad = warp & 3, hf = warp >> 2;
@@ -324,9 +362,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, y);
 #pragma unroll
       for (int k = 0; k < 64; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
-      // this warp's rows of the P buffer held its dQ staging of the previous pair
-      if (lane == 0) bulk_wait_read();
-      __syncwarp();
+      // the P/dA and dG buffers held the previous pair's staging
+      if (g > 0) {
+        ok = mbar_wait(bar_sfree, (g - 1) & 1, abort_flag);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      }
       store_half_bf16(sb + F_PA, ii, hf, y);
       fence_proxy_async_smem();
       tc_fence_before();
@@ -379,9 +419,6 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         const int cbase = c0 + (hf ? 0 : 8);
         const uint32_t xrow = sb + F_X + ii * 16;
-        // the quadrant's dG rows held both warps' dR staging of the previous
-        // pair (each warp waited for its own reads before its P store)
-        if (!(ok = pair_sync(bar_x, lane, xphase, abort_flag))) break;
         // columns outside [ii, ii + 127] are zero (staging overwrote them)
         if (hf == 1) {
           for (int C = 0; C < 15; ++C)
@@ -474,17 +511,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          const int qrow = i0 + 32 * quad;
-          const int drow = kDrPad + i0 - it.x.jlog0 - (BK - 1) + 128 * hf + 32 * quad;  // >= 1
-          if (qrow < p.L)
-            tma_reduce_add_3d(&tm_dq, 32 * hf, qrow, it.bh, sb + F_PA + hf * 16384 + quad * 4096);
-          if (drow < kDrPad + p.kv_rows) {
-            tma_reduce_add_3d(&tm_dr, 0, drow, it.h, sb + F_DG + 2 * hf * 16384 + quad * 4096);
-            tma_reduce_add_3d(&tm_dr, 32, drow, it.h, sb + F_DG + (2 * hf + 1) * 16384 + quad * 4096);
-          }
-          bulk_commit();
-        }
+        if (lane == 0) mbar_arrive(bar_staged);
         // column sums of dQp over the warp's 32 rows (recursive halving):
         // afterwards lane l holds column 32*hf + l
 #pragma unroll
@@ -532,9 +559,6 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
     }
     if (!ok) atomicExch(&g_bwd_error, 2);
-    // the TMA reductions must be complete before shared memory goes away
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
