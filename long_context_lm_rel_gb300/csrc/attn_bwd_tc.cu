@@ -176,9 +176,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const uint32_t bar_acc = b0 + 64, bar_red = b0 + 72, bar_drain = b0 + 80, bar_x0 = b0 + 88;
   const uint32_t bar_staged = b0 + 120;  // each softmax warp staged its rows of a pair (8)
   const uint32_t bar_sfree = b0 + 128;   // the staging of a pair has been read (1)
-  uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 136);
-  volatile int *abort_flag = (volatile int *)(smem + F_BAR + 140);
-  volatile float *wmax = (volatile float *)(smem + F_BAR + 144);  // [2][8]
+  const uint32_t bar_da = b0 + 136;      // softmax warps (256): dA written
+  const uint32_t bar_f0 = b0 + 144;      // dK and dQc done (commit)
+  uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 152);
+  volatile int *abort_flag = (volatile int *)(smem + F_BAR + 156);
+  volatile float *wmax = (volatile float *)(smem + F_BAR + 160);  // [2][8]
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1); mbar_init(bar_ld, 1); mbar_init(bar_sg, 1);
     mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_dp, 1);
@@ -188,6 +190,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     mbar_init(bar_staged, kSoftmaxWarps);
     mbar_init(bar_sfree, 1);
+    mbar_init(bar_da, kSoftmaxWarps * 32);
+    mbar_init(bar_f0, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -262,7 +266,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           mma_bf16(tmem + TM_DV, mndesc(sb + F_PA, k), mndesc(sb + F_DO, k), IDESC_MN_MN,
                    (!first || k > 0) ? 1u : 0u);
         mma_commit(bar_dp);
-        if (!(ok = mbar_wait(bar_ds, g & 1, abort_flag))) break;
+        // dK and dQc as soon as dA is written, while the softmax warps
+        // shear dG; then dQp and the dR blocks
+        if (!(ok = mbar_wait(bar_da, g & 1, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // dK += dA^T (Q+u)
@@ -271,6 +277,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // dQc = dA K
           mma_bf16(tmem + TM_QC, kdesc(sb + F_PA, k), mndesc(sb + F_K, k), IDESC_K_MN, k > 0);
+        mma_commit(bar_f0);
+        if (!(ok = mbar_wait(bar_ds, g & 1, abort_flag))) break;
+        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 16; ++k)  // dQp = dG Rband (fp16)
           mma_bf16(tmem + TM_QP, kdesc(sb + F_DG, k), mndesc(sb + F_R, k), IDESC_K_MN_F16, k > 0);
@@ -387,6 +396,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
       // P is no longer read: dP and dV were committed together
       store_half_bf16(sb + F_PA, ii, hf, y);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_da);
       // CTA-wide max |dA| of this pair -> power-of-two fp16 scale of dG
       float am = 0.f;
 #pragma unroll
