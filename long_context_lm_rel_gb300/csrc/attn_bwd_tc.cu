@@ -178,9 +178,10 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const uint32_t bar_sfree = b0 + 128;   // the staging of a pair has been read (1)
   const uint32_t bar_da = b0 + 136;      // softmax warps (256): dA written
   const uint32_t bar_f0 = b0 + 144;      // dK and dQc done (commit)
-  uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 152);
-  volatile int *abort_flag = (volatile int *)(smem + F_BAR + 156);
-  volatile float *wmax = (volatile float *)(smem + F_BAR + 160);  // [2][8]
+  const uint32_t bar_do = b0 + 152, bar_qu = b0 + 160;  // TMA: dO, (Q+u) of a pair
+  uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 168);
+  volatile int *abort_flag = (volatile int *)(smem + F_BAR + 172);
+  volatile float *wmax = (volatile float *)(smem + F_BAR + 176);  // [2][8]
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1); mbar_init(bar_ld, 1); mbar_init(bar_sg, 1);
     mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_dp, 1);
@@ -192,6 +193,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     mbar_init(bar_sfree, 1);
     mbar_init(bar_da, kSoftmaxWarps * 32);
     mbar_init(bar_f0, 1);
+    mbar_init(bar_do, 1);
+    mbar_init(bar_qu, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -211,38 +214,47 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   if (warp == kProducerWarp) {
     // ------------------------------------------------ producer / MMA issuer
     if (lane == 0) {
-      bool pend_kv = false, pend_ld = false;
-      int n_kv = 0, n_ld = 0;
+      int n_kv = 0, n_ld = 0, n_do = 0, n_qu = 0;  // copies issued per barrier
+      // dO of a pair is loaded once the previous pair's dP and dV are done,
+      // (Q+u) once its dK and dQc are done; the rest at the end of the pair
+      auto load_do = [&](const PairCursor &c) {
+        mbar_expect_tx(bar_do, 16384);
+        tma_load_3d(sb + F_DO, &tm_do, 0, c.i0(), c.it.bh, bar_do);
+        ++n_do;
+      };
+      auto load_qu = [&](const PairCursor &c) {
+        mbar_expect_tx(bar_qu, 16384);
+        tma_load_3d(sb + F_QU, &tm_qu, 0, c.i0(), c.it.bh, bar_qu);
+        ++n_qu;
+      };
       auto issue_loads = [&](const PairCursor &c) {
         const FItem &it = c.it;
         if (c.n == 0) {
           mbar_expect_tx(bar_kv, 2 * 16384);
           tma_load_3d(sb + F_K, &tm_k, 0, it.x.phys0, it.bh, bar_kv);
           tma_load_3d(sb + F_V, &tm_v, 0, it.x.phys0, it.bh, bar_kv);
-          pend_kv = true;
           ++n_kv;
         }
         const int i0 = c.i0();
-        mbar_expect_tx(bar_ld, 3 * 16384 + 32768);
-        tma_load_3d(sb + F_QU, &tm_qu, 0, i0, it.bh, bar_ld);
+        mbar_expect_tx(bar_ld, 16384 + 32768);
         tma_load_3d(sb + F_QV, &tm_qv16, 0, i0, it.bh, bar_ld);
-        tma_load_3d(sb + F_DO, &tm_do, 0, i0, it.bh, bar_ld);
         tma_load_3d(sb + F_R, &tm_r16, 0, i0 - it.x.jlog0 - (BK - 1), it.h, bar_ld);
-        pend_ld = true;
         ++n_ld;
       };
       bool ok = true;
       PairCursor c;
       c.init(p, tiles);
-      if (c.valid) issue_loads(c);
+      if (c.valid) {
+        load_qu(c);
+        load_do(c);
+        issue_loads(c);
+      }
       for (int g = 0; ok && c.valid; ++g) {
         const bool first = c.n == 0;
-        if (first) {
-          if (!(ok = mbar_wait(bar_kv, (c.k & 1), abort_flag))) break;
-          pend_kv = false;
-        }
-        if (!(ok = mbar_wait(bar_ld, g & 1, abort_flag))) break;
-        pend_ld = false;
+        PairCursor nx = c;
+        nx.next(p, tiles);
+        if (first && !(ok = mbar_wait(bar_kv, (c.k & 1), abort_flag))) break;
+        if (!(ok = mbar_wait(bar_qu, g & 1, abort_flag) && mbar_wait(bar_ld, g & 1, abort_flag))) break;
         // G's columns hold the previous pair's dQ / dR until it was flushed
         if (g > 0 && !(ok = mbar_wait(bar_fl, (g - 1) & 1, abort_flag))) break;
         tc_fence_after();
@@ -257,6 +269,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         // the first dV of an item overwrites the accumulators: the previous
         // item's epilogue must have read them
         if (first && c.k > 0 && !(ok = mbar_wait(bar_acc, (c.k - 1) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar_do, g & 1, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -266,6 +279,10 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           mma_bf16(tmem + TM_DV, mndesc(sb + F_PA, k), mndesc(sb + F_DO, k), IDESC_MN_MN,
                    (!first || k > 0) ? 1u : 0u);
         mma_commit(bar_dp);
+        if (nx.valid) {  // dO is free once dP and dV are done
+          if (!(ok = mbar_wait(bar_dp, g & 1, abort_flag))) break;
+          load_do(nx);
+        }
         // dK and dQc as soon as dA is written, while the softmax warps
         // shear dG; then dQp and the dR blocks
         if (!(ok = mbar_wait(bar_da, g & 1, abort_flag))) break;
@@ -278,6 +295,10 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int k = 0; k < 8; ++k)  // dQc = dA K
           mma_bf16(tmem + TM_QC, kdesc(sb + F_PA, k), mndesc(sb + F_K, k), IDESC_K_MN, k > 0);
         mma_commit(bar_f0);
+        if (nx.valid) {  // (Q+u) is free once dK is done
+          if (!(ok = mbar_wait(bar_f0, g & 1, abort_flag))) break;
+          load_qu(nx);
+        }
         if (!(ok = mbar_wait(bar_ds, g & 1, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
@@ -290,8 +311,6 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             mma_bf16(tmem + TM_R0 + 64 * mb, mndesc(sb + F_DG + 2 * mb * 16384, k),
                      mndesc(sb + F_QV, k), IDESC_MN_MN_F16, k > 0);
         mma_commit(bar_fin);
-        PairCursor nx = c;
-        nx.next(p, tiles);
         if (nx.valid) {
           // every operand of this pair has been consumed once its MMAs are done
           if (!(ok = mbar_wait(bar_fin, g & 1, abort_flag))) break;
@@ -302,9 +321,13 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       if (!ok) {
         // wind down: let in-flight copies and MMAs land before TMEM and
         // shared memory are released
+        // (the latest copy of each barrier; an earlier one completed before
+        // the latest was issued, and a completed phase returns at once)
         volatile int no_abort = 0;
-        if (pend_kv) mbar_wait(bar_kv, (n_kv - 1) & 1, &no_abort);
-        if (pend_ld) mbar_wait(bar_ld, (n_ld - 1) & 1, &no_abort);
+        if (n_kv > 0) mbar_wait(bar_kv, (n_kv - 1) & 1, &no_abort);
+        if (n_ld > 0) mbar_wait(bar_ld, (n_ld - 1) & 1, &no_abort);
+        if (n_do > 0) mbar_wait(bar_do, (n_do - 1) & 1, &no_abort);
+        if (n_qu > 0) mbar_wait(bar_qu, (n_qu - 1) & 1, &no_abort);
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0, &no_abort);
         atomicExch(&g_bwd_error, 1);
