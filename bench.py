@@ -110,8 +110,10 @@ class ClockSampler:
 
 
 def make_inputs(seed=0):
+    import dataclasses
+
     import rxl_inputs as gen
-    w = gen.CFG3
+    w = dataclasses.replace(gen.CFG3, seed=seed) if seed else gen.CFG3
     p, s, mem = gen.layer_params(w), gen.segment_inputs(w), gen.initial_memory(w)
     return dict(q=s["q"], k_mem=mem["k_mem"], k_cur=s["k_cur"], v_mem=mem["v_mem"], v_cur=s["v_cur"],
                 u=p["u"], vb=p["vb"], r=p["r"], do=s["do"])
@@ -170,12 +172,13 @@ def run_ours(args, rank, world):
     import torch.distributed as dist
 
     import long_context_lm_rel_gb300 as rxl
+    from long_context_lm_rel_gb300.multirank import max_over_ranks, replica_seed, whole_job_rate
     from tests._harness import AttnCall, place_kv
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     rxl.lib()
-    x = make_inputs()
+    x = make_inputs(replica_seed(0, rank))   # one independent replica per rank
     cap = m = M
     c = AttnCall(x["q"], place_kv(x["k_mem"], x["k_cur"], cap, 0), place_kv(x["v_mem"], x["v_cur"], cap, 0),
                  x["r"], x["u"], x["vb"], cap=cap, m=m, head=0, dtype="bf16", scale=SCALE).alloc_bwd(x["do"])
@@ -212,16 +215,12 @@ def run_ours(args, rank, world):
         dist.barrier()
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    tot_ms = sum(fwd_ms) + sum(bwd_ms)
-    t = torch.tensor([tot_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(fwd_ms) + sum(bwd_ms), world, device="cuda")
 
     pairs = visible_pairs(B, H, L, m)
     flop_step = pairs * (FLOP_FWD_PAIR + FLOP_BWD_PAIR)
-    value = world * args.steps * flop_step / (tot_ms * 1e-3) / 1e12
-    tokens = world * args.steps * B * L / (tot_ms * 1e-3)
+    value = whole_job_rate(args.steps * flop_step, world, tot_ms * 1e-3) / 1e12
+    tokens = whole_job_rate(args.steps * B * L, world, tot_ms * 1e-3)
 
     # end to end through the C ABI from pinned host buffers: inputs H2D, fwd,
     # bwd, every output D2H, each step
@@ -248,10 +247,8 @@ def run_ours(args, rank, world):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    t = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_value = world * args.steps * flop_step / (float(t.item()) * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device="cuda")
+    e2e_value = whole_job_rate(args.steps * flop_step, world, e2e_ms * 1e-3) / 1e12
 
     if rank != 0:
         return
