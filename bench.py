@@ -113,7 +113,7 @@ def make_inputs(seed=0):
     import dataclasses
 
     import rxl_inputs as gen
-    w = dataclasses.replace(gen.CFG3, seed=seed) if seed else gen.CFG3
+    w = dataclasses.replace(gen.CFG3, seed=seed, B=B)
     p, s, mem = gen.layer_params(w), gen.segment_inputs(w), gen.initial_memory(w)
     return dict(q=s["q"], k_mem=mem["k_mem"], k_cur=s["k_cur"], v_mem=mem["v_mem"], v_cur=s["v_cur"],
                 u=p["u"], vb=p["vb"], r=p["r"], do=s["do"])
@@ -238,17 +238,19 @@ def run_ours(args, rank, world):
         for n, t in host_out.items():
             t.copy_(getattr(c, n), non_blocking=True)
 
-    for _ in range(max(args.warmup, 1)):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device="cuda")
-    e2e_value = whole_job_rate(args.steps * flop_step, world, e2e_ms * 1e-3) / 1e12
+    e2e_value = None
+    if not args.no_e2e:
+        for _ in range(max(args.warmup, 1)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device="cuda")
+        e2e_value = whole_job_rate(args.steps * flop_step, world, e2e_ms * 1e-3) / 1e12
 
     if rank != 0:
         return
@@ -278,6 +280,7 @@ def run_ours(args, rank, world):
         mu.update({"peak": hbm, "frac": mu["achieved"] / hbm, "peak_kind": f"{kind} copy"})
         out["stream_cfg5"] = stream
         out["mem_update_roofline"] = mu
+        out["window_recompute"] = window_recompute()
     if world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         dt, fl = cpu_sample(x, (0, 4), nthreads)
@@ -351,6 +354,54 @@ def stream_cfg5(segments=32, layers=16, reps_update=200):
             "bytes_per_call": bytes_call, "achieved": bytes_call / (us * 1e-6) / 1e9}
 
 
+def window_recompute(reps=20):
+    """Evaluation with and without the memory, one layer (the reuse the pages
+    credit for Transformer-XL's evaluation speed): the segment-recurrent step
+    (L = 128 new queries over M = 1600 cached rows plus the segment) against
+    recomputing causal attention over the whole window of M + L = 1728
+    positions for every new position (m = 0), B4 H16 bf16, the same kernel.
+    Speed-up per evaluated position = L * t_window / t_segment. Warm L2,
+    back-to-back calls; parity of both shapes is in the GPU tests."""
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    B5, H5, L5, M5 = 4, 16, 128, 1600
+    W = M5 + L5
+    g = torch.Generator(device="cuda").manual_seed(7)
+    bf = torch.bfloat16
+    mk = lambda *s, std=0.125: (torch.randn(*s, generator=g, device="cuda") * std).to(bf)
+    st = torch.cuda.current_stream()
+
+    def timed(Lq, cap, m):
+        q, k, v = mk(B5, H5, Lq, DH), mk(B5, H5, cap + Lq, DH), mk(B5, H5, cap + Lq, DH)
+        r, u, vb = mk(H5, cap + Lq, DH, std=0.7), mk(H5, DH, std=0.02), mk(H5, DH, std=0.02)
+        o = torch.empty(B5, H5, Lq, DH, device="cuda", dtype=bf)
+        lse = torch.empty(B5, H5, Lq, device="cuda", dtype=torch.float32)
+        d = rxl.make_desc(B5, H5, Lq, cap, m, 0, SCALE, rxl.RXL_DTYPE_BF16)
+        for _ in range(3):
+            rxl.rxl_attn_fwd(d, q, k, v, r, u, vb, o, lse, st)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            rxl.rxl_attn_fwd(d, q, k, v, r, u, vb, o, lse, st)
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    t_seg = timed(L5, M5, M5)
+    t_win = timed(W, 0, 0)
+    pairs_seg = visible_pairs(B5, H5, L5, M5)
+    pairs_win = B5 * H5 * W * (W + 1) // 2
+    return {"workload": "cfg5 shape, one layer: B4 H16, L128 over M1600 vs window 1728 recomputed, fwd",
+            "segment_ms": t_seg, "window_ms": t_win,
+            "segment_positions_per_s": B5 * L5 / (t_seg * 1e-3),
+            "window_positions_per_s": B5 / (t_win * 1e-3),
+            "speedup_per_position": L5 * t_win / t_seg,
+            "segment_attn_tflops": pairs_seg * FLOP_FWD_PAIR / (t_seg * 1e-3) / 1e12,
+            "window_attn_tflops": pairs_win * FLOP_FWD_PAIR / (t_win * 1e-3) / 1e12,
+            "note": "attention of one layer only, warm L2; the pages' ~1800x refers to the whole model"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -359,7 +410,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stream", action="store_true", help="skip the cfg5 stream / memory-update timing")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) timing")
+    ap.add_argument("--batch", type=int, default=16,
+                    help="batch rows of the workload (16 = the benchmark; smaller = profiling case)")
     args = ap.parse_args()
+    global B, WORKLOAD
+    if args.batch != B:
+        B = args.batch
+        WORKLOAD = f"cfg3_shape_bf16_B{B}H16_L512M512_dh64_fwd+bwd (profiling case)"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and args.impl == "ours":

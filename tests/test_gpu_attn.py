@@ -223,6 +223,27 @@ def test_full_size_config(cfg, ex):
     assert_close("dv", to_host(c.dvb)[hs], g["dvb"], "bf16")
 
 
+# -------------------- recompute-the-window evaluation baseline (forward)
+
+def test_window_recompute_case():
+    """The evaluation baseline without a memory: every step recomputes causal
+    attention over the whole window of cfg5 (M + L = 1728 positions, m = 0),
+    B4 H16; sampled rows against the oracle."""
+    import torch
+    B, H, W = 4, 16, 1728
+    x = make_inputs(B, H, W, 0, 0, "bf16", seed=1728)
+    c = run_gpu(x, 0, 0, 0, "bf16", bwd=False)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    k, v = logical(x)
+    rng = np.random.default_rng(1728)
+    sel = sample_rows(B, H, W, 64, rng)
+    o_ref, lse_ref = oracle.fwd_rows(x["q"], k, v, x["r"], x["u"], x["vb"], 0.125, sel)
+    o, lse = to_host(c.o), to_host(c.lse)
+    assert_close("O(sampled)", o[sel[:, 0], sel[:, 1], sel[:, 2]], o_ref, "bf16")
+    assert_close("LSE(sampled)", lse[sel[:, 0], sel[:, 1], sel[:, 2]], lse_ref, "bf16")
+
+
 # ------------------------- configuration 5 (16-layer evaluation stream, fwd)
 
 def test_cfg5_stream_first_and_last_layer():
