@@ -76,6 +76,10 @@ def _bind(lib):
     lib.oracle_logits.restype = None
     lib.oracle_bwd.argtypes = [i, i, i, i, i, d, ll] + [_D] * 7 + [_D] * 6 + [i]
     lib.oracle_bwd.restype = ctypes.c_int
+    lib.oracle_fwd_reset.argtypes = [i, i, i, i, i, d, ll] + [_D] * 6 + [_I, _D, _D, i]
+    lib.oracle_fwd_reset.restype = None
+    lib.oracle_bwd_reset.argtypes = [i, i, i, i, i, d, ll] + [_D] * 6 + [_I] + [_D] * 7 + [i]
+    lib.oracle_bwd_reset.restype = ctypes.c_int
     return lib
 
 
@@ -104,17 +108,32 @@ def _r_rows(r, mL):
     return _f64(r[:, :mL, :])
 
 
-def fwd(q, k, v, r, u, vb, scale, pos0=0, nthreads=None, lib=None):
+def _mvis(mem_visible, B, m):
+    """Per batch row: newest memory rows visible (document reset), int32 [B]."""
+    a = np.ascontiguousarray(np.asarray(mem_visible, dtype=np.int32).reshape(B))
+    assert ((a >= 0) & (a <= m)).all(), "mem_visible must lie in [0, m]"
+    return a
+
+
+def fwd(q, k, v, r, u, vb, scale, pos0=0, nthreads=None, lib=None, mem_visible=None):
     """O [B,H,L,dh] and LSE [B,H,L] (float64). k, v: [B,H,m+L,dh] in logical
-    order (memory rows oldest first, then the current rows)."""
+    order (memory rows oldest first, then the current rows). mem_visible
+    (optional, [B]): batch row b sees only its newest mem_visible[b] memory
+    rows (per-row document reset)."""
     lib = lib or load()
     B, H, L, m, dh = _shapes(q, k, r)
     q, k, v, u, vb = map(_f64, (q, k, v, u, vb))
     r = _r_rows(r, m + L)
     o = np.zeros((B, H, L, dh))
     lse = np.zeros((B, H, L))
-    lib.oracle_fwd(B, H, L, m, dh, float(scale), int(pos0), _p(q), _p(k), _p(v), _p(r),
-                   _p(u), _p(vb), _p(o), _p(lse), nthreads or default_threads())
+    if mem_visible is None:
+        lib.oracle_fwd(B, H, L, m, dh, float(scale), int(pos0), _p(q), _p(k), _p(v), _p(r),
+                       _p(u), _p(vb), _p(o), _p(lse), nthreads or default_threads())
+    else:
+        mv = _mvis(mem_visible, B, m)
+        lib.oracle_fwd_reset(B, H, L, m, dh, float(scale), int(pos0), _p(q), _p(k), _p(v), _p(r),
+                             _p(u), _p(vb), mv.ctypes.data_as(_I), _p(o), _p(lse),
+                             nthreads or default_threads())
     return o, lse
 
 
@@ -146,9 +165,10 @@ def logits(q, k, r, u, vb, scale, pos0=0, nthreads=None, lib=None):
     return z
 
 
-def bwd(q, k, v, r, u, vb, dout, scale, pos0=0, nthreads=None, lib=None):
+def bwd(q, k, v, r, u, vb, dout, scale, pos0=0, nthreads=None, lib=None, mem_visible=None):
     """Gradients of sum(O * dout): dict with dq [B,H,L,dh], dk, dv [B,H,m+L,dh]
-    (logical order), dr [H,m+L,dh], du, dvb [H,dh]; all float64."""
+    (logical order), dr [H,m+L,dh], du, dvb [H,dh]; all float64. mem_visible
+    as in fwd."""
     lib = lib or load()
     B, H, L, m, dh = _shapes(q, k, r)
     q, k, v, u, vb, dout = map(_f64, (q, k, v, u, vb, dout))
@@ -158,10 +178,15 @@ def bwd(q, k, v, r, u, vb, dout, scale, pos0=0, nthreads=None, lib=None):
         "dv": np.zeros((B, H, m + L, dh)), "dr": np.zeros((H, m + L, dh)),
         "du": np.zeros((H, dh)), "dvb": np.zeros((H, dh)),
     }
-    rc = lib.oracle_bwd(B, H, L, m, dh, float(scale), int(pos0), _p(q), _p(k), _p(v), _p(r),
-                        _p(u), _p(vb), _p(dout), _p(out["dq"]), _p(out["dk"]), _p(out["dv"]),
-                        _p(out["dr"]), _p(out["du"]), _p(out["dvb"]),
-                        nthreads or default_threads())
+    outs = (_p(out["dq"]), _p(out["dk"]), _p(out["dv"]), _p(out["dr"]), _p(out["du"]), _p(out["dvb"]))
+    if mem_visible is None:
+        rc = lib.oracle_bwd(B, H, L, m, dh, float(scale), int(pos0), _p(q), _p(k), _p(v), _p(r),
+                            _p(u), _p(vb), _p(dout), *outs, nthreads or default_threads())
+    else:
+        mv = _mvis(mem_visible, B, m)
+        rc = lib.oracle_bwd_reset(B, H, L, m, dh, float(scale), int(pos0), _p(q), _p(k), _p(v),
+                                  _p(r), _p(u), _p(vb), mv.ctypes.data_as(_I), _p(dout), *outs,
+                                  nthreads or default_threads())
     if rc != 0:
         raise MemoryError("oracle_bwd: allocation failed")
     return out

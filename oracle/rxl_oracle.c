@@ -12,6 +12,11 @@
  *  - key positions: memory -m..-1, current 0..L-1; query positions 0..L-1
  *    (Transformer-XL page, "Causal Mask With Memory");
  *  - allow(i,j) = 1 if j<0, 1 if 0<=j<=i, else 0 (same section, eq. allow);
+ *  - per-row document reset: a batch row that entered a new document must
+ *    not see the previous document's memory (same section, the note after the
+ *    mask picture; "Batched Streams": the reset is per row). Read here as a
+ *    mask: batch row b sees only its newest mvis[b] memory rows, i.e. memory
+ *    key j is visible iff j >= -mvis[b] (mvis NULL: every row sees all m);
  *  - A_ij = q_i.k_j + q_i.r_{i-j} + u.k_j + v.r_{i-j}
  *         = (q_i+u).k_j + (q_i+v).r_{i-j}
  *    (Transformer-XL page, "Relative Positional Encoding", four-term score;
@@ -54,6 +59,7 @@ typedef struct {
   double *dq, *dk, *dv;            /* backward outputs per unit */
   double *dr_part, *du_part, *dvb_part; /* per-unit partials */
   const int *sel;                  /* row subset: (b,h,i) triples */
+  const int *mvis;                 /* per batch row: newest memory rows visible (or NULL) */
   int nsel;
   int next;                        /* work counter */
   int nunits;
@@ -65,6 +71,13 @@ typedef struct {
 static int allow(long long pi, long long pj, long long pos0) {
   if (pj < pos0) return 1;
   return pj <= pi;
+}
+
+/* allow(i,j) for batch row b, with the row's document reset: of the memory
+ * keys only the newest mvis[b] are visible. */
+static int allow_b(const problem *P, int b, int i, int j) {
+  if (P->mvis && j < 0 && j < -P->mvis[b]) return 0;
+  return allow(P->pos0 + i, P->pos0 + j, P->pos0);
 }
 
 /* scaled score s*A_ij of query row i against key position j (j in [-m, L)). */
@@ -88,7 +101,7 @@ static void row_stats(const problem *P, int b, int h, int i, double *z, double *
                       double *l_out) {
   double mx = -INFINITY;
   for (int j = -P->m; j < P->L; ++j) {
-    if (allow(P->pos0 + i, P->pos0 + j, P->pos0)) {
+    if (allow_b(P, b, i, j)) {
       z[j + P->m] = scaled_score(P, b, h, i, j);
       if (z[j + P->m] > mx) mx = z[j + P->m];
     } else {
@@ -157,7 +170,7 @@ static void *logits_worker(void *arg) {
     for (int i = 0; i < P->L; ++i)
       for (int j = -P->m; j < P->L; ++j) {
         double *dst = P->logits + ((((size_t)b * P->H + h) * P->L + i) * mL + (P->m + j));
-        *dst = allow(P->pos0 + i, P->pos0 + j, P->pos0) ? scaled_score(P, b, h, i, j) : -INFINITY;
+        *dst = allow_b(P, b, i, j) ? scaled_score(P, b, h, i, j) : -INFINITY;
       }
   }
   return NULL;
@@ -279,12 +292,14 @@ void oracle_logits(int B, int H, int L, int m, int dh, double scale, long long p
 
 /* Backward: all outputs are overwritten. dk/dv cover memory rows too (the
  * K/V gradient of cached rows); nothing is returned for the cached states. */
-int oracle_bwd(int B, int H, int L, int m, int dh, double scale, long long pos0,
-               const double *q, const double *k, const double *v, const double *r,
-               const double *u, const double *vb, const double *dout, double *dq, double *dk,
-               double *dv, double *dr, double *du, double *dvb, int nthreads) {
+static int bwd_impl(int B, int H, int L, int m, int dh, double scale, long long pos0,
+                    const double *q, const double *k, const double *v, const double *r,
+                    const double *u, const double *vb, const int *mvis, const double *dout,
+                    double *dq, double *dk, double *dv, double *dr, double *du, double *dvb,
+                    int nthreads) {
   problem P;
   setup(&P, B, H, L, m, dh, scale, pos0, q, k, v, r, u, vb);
+  P.mvis = mvis;
   const int mL = m + L;
   const size_t units = (size_t)B * H;
   P.dout = dout; P.dq = dq; P.dk = dk; P.dv = dv;
@@ -315,4 +330,34 @@ int oracle_bwd(int B, int H, int L, int m, int dh, double scale, long long pos0,
     }
   free(P.dr_part); free(P.du_part); free(P.dvb_part);
   return 0;
+}
+
+int oracle_bwd(int B, int H, int L, int m, int dh, double scale, long long pos0,
+               const double *q, const double *k, const double *v, const double *r,
+               const double *u, const double *vb, const double *dout, double *dq, double *dk,
+               double *dv, double *dr, double *du, double *dvb, int nthreads) {
+  return bwd_impl(B, H, L, m, dh, scale, pos0, q, k, v, r, u, vb, NULL, dout, dq, dk, dv, dr, du,
+                  dvb, nthreads);
+}
+
+/* The same with a per-batch-row document reset: mvis[b] in [0, m] is the
+ * number of newest memory rows batch row b may attend to. */
+void oracle_fwd_reset(int B, int H, int L, int m, int dh, double scale, long long pos0,
+                      const double *q, const double *k, const double *v, const double *r,
+                      const double *u, const double *vb, const int *mvis, double *o, double *lse,
+                      int nthreads) {
+  problem P;
+  setup(&P, B, H, L, m, dh, scale, pos0, q, k, v, r, u, vb);
+  P.mvis = mvis;
+  P.o = o; P.lse = lse;
+  run(&P, fwd_worker, nthreads);
+}
+
+int oracle_bwd_reset(int B, int H, int L, int m, int dh, double scale, long long pos0,
+                     const double *q, const double *k, const double *v, const double *r,
+                     const double *u, const double *vb, const int *mvis, const double *dout,
+                     double *dq, double *dk, double *dv, double *dr, double *du, double *dvb,
+                     int nthreads) {
+  return bwd_impl(B, H, L, m, dh, scale, pos0, q, k, v, r, u, vb, mvis, dout, dq, dk, dv, dr, du,
+                  dvb, nthreads);
 }

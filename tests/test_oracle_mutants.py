@@ -15,7 +15,7 @@ import torch.nn.functional as F
 
 import oracle
 from tests import _golden
-from tests.test_oracle_pins import make_txl_mask, reference_rel_ids, distance_probe
+from tests.test_oracle_pins import make_txl_mask, reference_rel_ids, distance_probe, reset_vs_sliced
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "rxl_oracle.c")
 
@@ -34,6 +34,10 @@ MUTANTS = {
     "dr_wrong_bias": ("drd[c] += dA * (qi[c] + vb[c]);", "drd[c] += dA * (qi[c] + u[c]);"),
     "dq_content_only": ("dqi[c] += dA * (kj[c] + rd[c]);", "dqi[c] += dA * kj[c];"),
     "du_uses_r": ("du[c] += dA * kj[c];", "du[c] += dA * rd[c];"),
+    "reset_keeps_oldest": ("if (P->mvis && j < 0 && j < -P->mvis[b]) return 0;",
+                           "if (P->mvis && j < 0 && j >= P->mvis[b] - P->m) return 0;"),
+    "reset_off_by_one": ("if (P->mvis && j < 0 && j < -P->mvis[b]) return 0;",
+                         "if (P->mvis && j < 0 && j <= -P->mvis[b]) return 0;"),
 }
 
 
@@ -126,6 +130,10 @@ def battery(lib):
             if abs(fd - an) > 1e-6 * max(1.0, np.max(np.abs(g[gk[n]]))):
                 failed.append("grad_" + n)
                 break
+
+    # per-row document reset: each row equals the row alone with its newest memory
+    if reset_vs_sliced((7, 0, 3), lib=lib):
+        failed.append("reset")
     return failed
 
 

@@ -363,3 +363,48 @@ def test_row_subset_and_threads_agree_with_full_forward():
     o, l = oracle.fwd_rows(*args, s, sel, nthreads=2)
     for n, (b, h, i) in enumerate(sel):
         assert np.array_equal(o[n], o1[b, h, i]) and l[n] == l1[b, h, i]
+
+
+# ------------------------------------------------ per-row document reset
+
+def reset_vs_sliced(mvis, B=3, H=2, L=6, m=7, dh=16, seed=11, lib=None):
+    """Per-row reset ("Causal Mask With Memory", the note after the picture;
+    "Batched Streams"): batch row b that sees only its newest mvis[b] memory
+    rows must give exactly what the plain oracle gives on that row alone with
+    only those memory rows (masking a key = removing it). Returns the names
+    of the outputs that differ."""
+    rng = np.random.default_rng(seed)
+    q, k, v = rand(rng, B, H, L, dh), rand(rng, B, H, m + L, dh), rand(rng, B, H, m + L, dh)
+    r, u, vb = rand(rng, H, m + L, dh), rand(rng, H, dh, std=0.3), rand(rng, H, dh, std=0.3)
+    do = rand(rng, B, H, L, dh)
+    o, lse = oracle.fwd(q, k, v, r, u, vb, 0.4, mem_visible=mvis, nthreads=1, lib=lib)
+    g = oracle.bwd(q, k, v, r, u, vb, do, 0.4, mem_visible=mvis, nthreads=1, lib=lib)
+    bad = []
+    dr = np.zeros((H, m + L, dh))
+    du, dvb = np.zeros((H, dh)), np.zeros((H, dh))
+    for b in range(B):
+        mb = int(mvis[b])
+        keep = np.r_[m - mb:m + L]                    # newest mb memory rows, then the segment
+        ob, lb = oracle.fwd(q[b:b + 1], k[b:b + 1][:, :, keep], v[b:b + 1][:, :, keep], r, u, vb, 0.4,
+                            nthreads=1, lib=lib)
+        gb = oracle.bwd(q[b:b + 1], k[b:b + 1][:, :, keep], v[b:b + 1][:, :, keep], r, u, vb,
+                        do[b:b + 1], 0.4, nthreads=1, lib=lib)
+        if not np.array_equal(o[b], ob[0]) or not np.array_equal(lse[b], lb[0]):
+            bad.append(f"fwd[{b}]")
+        if not np.array_equal(g["dq"][b], gb["dq"][0]):
+            bad.append(f"dq[{b}]")
+        for n in ("dk", "dv"):
+            if not np.array_equal(g[n][b][:, keep], gb[n][0]) or np.any(g[n][b][:, :m - mb] != 0):
+                bad.append(f"{n}[{b}]")
+        dr[:, :mb + L] += gb["dr"]
+        du += gb["du"]
+        dvb += gb["dvb"]
+    for n, ref in (("dr", dr), ("du", du), ("dvb", dvb)):
+        if not np.array_equal(g[n], ref):
+            bad.append(n)
+    return bad
+
+
+@pytest.mark.parametrize("mvis", [(7, 0, 3), (0, 0, 0), (7, 7, 7), (1, 6, 2)])
+def test_document_reset_equals_the_row_alone(mvis):
+    assert reset_vs_sliced(mvis) == []
