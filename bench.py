@@ -281,6 +281,7 @@ def run_ours(args, rank, world):
         out["stream_cfg5"] = stream
         out["mem_update_roofline"] = mu
         out["window_recompute"] = window_recompute()
+        out["reset_cfg3"] = reset_cfg3()
     if world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         dt, fl = cpu_sample(x, (0, 4), nthreads)
@@ -352,6 +353,47 @@ def stream_cfg5(segments=32, layers=16, reps_update=200):
             "note": "per segment and layer: K/V current rows copied in (torch), rxl_attn_fwd, 2 x rxl_mem_update"}, \
            {"kernel": "mem_update_kernel", "bound": "hbm", "unit": "GB/s", "us_per_call": us,
             "bytes_per_call": bytes_call, "achieved": bytes_call / (us * 1e-6) / 1e9}
+
+
+def reset_cfg3(reps=10):
+    """The cfg3 training pair under a per-row document reset: a quarter of the
+    batch rows has just started a new document (no memory), a quarter sees
+    128, a quarter 384 and a quarter all 512 memory rows. Throughput counts
+    the visible pairs of each row. L2 flushed between steps as in the main
+    measurement."""
+    import numpy as np
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    from tests._harness import AttnCall, place_kv
+    x = make_inputs()
+    cap = m = M
+    mvis = [(0, 128, 384, 512)[b % 4] for b in range(B)]
+    c = AttnCall(x["q"], place_kv(x["k_mem"], x["k_cur"], cap, 0), place_kv(x["v_mem"], x["v_cur"], cap, 0),
+                 x["r"], x["u"], x["vb"], cap=cap, m=m, head=0, dtype="bf16", scale=SCALE)
+    c.fwd_reset(mvis)
+    c.alloc_bwd(x["do"])
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        c.fwd_reset(mvis, stream=stream)
+        c.bwd_reset(stream)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for e in ev:
+        flush.zero_()
+        e[0].record(stream)
+        rxl.rxl_attn_fwd_reset(c.desc, c.mvis, c.q, c.k, c.v, c.r, c.u, c.vb, c.o, c.o_lo, c.lse, stream)
+        e[1].record(stream)
+        c.bwd_reset(stream)
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / reps
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / reps
+    pairs = sum(H * (L * mb + L * (L + 1) // 2) for mb in mvis)
+    flop = pairs * (FLOP_FWD_PAIR + FLOP_BWD_PAIR)
+    return {"workload": "cfg3 with per-row reset, mem_visible = 0/128/384/512 by b mod 4",
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "visible_pairs": pairs,
+            "tflops": flop / ((fwd_ms + bwd_ms) * 1e-3) / 1e12}
 
 
 def window_recompute(reps=20):

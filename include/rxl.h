@@ -176,6 +176,35 @@ rxl_status rxl_attn_bwd_ex(const rxl_attn_desc *desc, const void *q, const void 
                            void *workspace, size_t workspace_bytes, rxl_stream_t stream);
 
 /*
+ * Per-row document reset (Transformer-XL page, "Causal Mask With Memory",
+ * the note after the mask picture, and "Batched Streams": a batch row that
+ * has just entered a new document must not take the previous document as
+ * its context, and the reset is per row, not per batch).
+ *   mem_visible  DEVICE int32 [B] (4-byte aligned): batch row b attends only
+ *                to its newest mem_visible[b] memory rows, i.e. logical
+ *                memory rows m - mem_visible[b] .. m-1 (key positions
+ *                -mem_visible[b] .. -1); the older ones are masked as if
+ *                absent. A row that starts a new document passes 0 and its
+ *                count grows again as that document's segments arrive.
+ *                Values are clamped into [0, mem_len] on the device.
+ * The ring itself is shared by all rows (rxl_mem_update is unchanged). In
+ * the backward, the masked memory rows of a batch row get dk = dv = 0 and
+ * contribute nothing to dr, du, dvbias. All other arguments, outputs and
+ * checks as in rxl_attn_fwd_ex / rxl_attn_bwd_ex (o_lo may be NULL).
+ */
+rxl_status rxl_attn_fwd_reset(const rxl_attn_desc *desc, const int32_t *mem_visible, const void *q,
+                              const void *k, const void *v, const void *r, const void *u,
+                              const void *vbias, void *o, void *o_lo, float *lse,
+                              rxl_stream_t stream);
+
+rxl_status rxl_attn_bwd_reset(const rxl_attn_desc *desc, const int32_t *mem_visible, const void *q,
+                              const void *k, const void *v, const void *r, const void *u,
+                              const void *vbias, const void *o, const void *o_lo, const float *lse,
+                              const void *dout, void *dq, void *dk, void *dv, float *dr, float *du,
+                              float *dvbias, void *workspace, size_t workspace_bytes,
+                              rxl_stream_t stream);
+
+/*
  * FIFO memory ring (eq. Tail_M; update_mems with mem_len == cap).
  *   data         device pointer to plane 0, row 0
  *   planes       independent rings (e.g. B*H), >= 1

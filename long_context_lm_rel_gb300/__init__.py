@@ -76,6 +76,10 @@ def lib():
             L.rxl_attn_fwd_ex.restype = ctypes.c_int
             L.rxl_attn_bwd_ex.argtypes = [P(rxl_attn_desc)] + [vp] * 17 + [ctypes.c_size_t, vp]
             L.rxl_attn_bwd_ex.restype = ctypes.c_int
+            L.rxl_attn_fwd_reset.argtypes = [P(rxl_attn_desc)] + [vp] * 10 + [vp]
+            L.rxl_attn_fwd_reset.restype = ctypes.c_int
+            L.rxl_attn_bwd_reset.argtypes = [P(rxl_attn_desc)] + [vp] * 18 + [ctypes.c_size_t, vp]
+            L.rxl_attn_bwd_reset.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc.argtypes = [P(rxl_attn_desc)] + [vp] * 15 + [vp]
             L.rxl_attn_bwd_noalloc.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc_max_scratch_bytes.argtypes = []
@@ -126,6 +130,20 @@ def rxl_attn_bwd_ex(desc, q, k, v, r, u, vbias, o, o_lo, lse, dout, dq, dk, dv, 
                                  *map(_ptr, (q, k, v, r, u, vbias, o, o_lo, lse, dout, dq, dk, dv, dr,
                                              du, dvbias, workspace)),
                                  int(workspace_bytes), _stream(stream)), "rxl_attn_bwd_ex")
+
+
+def rxl_attn_fwd_reset(desc, mem_visible, q, k, v, r, u, vbias, o, o_lo, lse, stream=None):
+    _check(lib().rxl_attn_fwd_reset(ctypes.byref(desc),
+                                    *map(_ptr, (mem_visible, q, k, v, r, u, vbias, o, o_lo, lse)),
+                                    _stream(stream)), "rxl_attn_fwd_reset")
+
+
+def rxl_attn_bwd_reset(desc, mem_visible, q, k, v, r, u, vbias, o, o_lo, lse, dout, dq, dk, dv, dr,
+                       du, dvbias, workspace, workspace_bytes, stream=None):
+    _check(lib().rxl_attn_bwd_reset(ctypes.byref(desc),
+                                    *map(_ptr, (mem_visible, q, k, v, r, u, vbias, o, o_lo, lse, dout,
+                                                dq, dk, dv, dr, du, dvbias, workspace)),
+                                    int(workspace_bytes), _stream(stream)), "rxl_attn_bwd_reset")
 
 
 def rxl_attn_bwd_workspace_bytes(desc) -> int:

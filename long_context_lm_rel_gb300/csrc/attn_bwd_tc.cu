@@ -62,6 +62,7 @@ __device__ int g_bwd_error;
 
 struct BwdParams {
   int B, H, L, cap, m, head, nq, kv_rows, nitems;
+  const int *mvis;  // per-row document reset (nullable): newest memory rows per batch row
   float scale, scale_log2;
   const float *lse, *delta;
   __nv_bfloat16 *dk, *dv;
@@ -113,46 +114,65 @@ constexpr uint32_t TM_QC = 256, TM_QP = 320, TM_R0 = 384;
 
 // A work item is one (b, h, key tile); items are numbered key tile major, so
 // that the memory tiles and the early current tiles (seen by the most query
-// tiles) come first. CTA c of G takes one item per round, snake order.
+// tiles) come first. CTA c of G takes one item per round, snake order. Under
+// a per-row document reset a batch row may have fewer key tiles than the
+// item numbering allows for; its surplus items are empty (NQ = 0).
 struct FItem {
   int bh, h, qlo, NQ;
   KeyTile x;
 };
 
-__device__ __forceinline__ FItem fitem(const BwdParams &p, const KeyTiles &tiles, int w) {
+__device__ __forceinline__ FItem fitem(const BwdParams &p, int w) {
   const int BH = p.B * p.H;
   FItem it;
   it.bh = w % BH;
   it.h = it.bh % p.H;
-  it.x = tiles.get(w / BH);
+  const RowMemory rm = row_memory(p.mvis, it.bh / p.H, p.m, p.cap, p.head);
+  const KeyTiles tiles(rm.m, p.cap, rm.head, p.L);
+  const int t = w / BH;
+  if (t >= tiles.count()) {
+    it.x.phys0 = it.x.jlog0 = it.x.nvalid = 0;
+    it.qlo = it.NQ = 0;
+    return it;
+  }
+  it.x = tiles.get(t);
   it.qlo = it.x.jlog0 >= 0 ? it.x.jlog0 / BQ : 0;
   it.NQ = p.nq - it.qlo;
   return it;
 }
 
-// Walks this CTA's (item, query tile) pairs: k counts items, n query tiles.
+// Walks this CTA's (item, query tile) pairs: r counts rounds, k the items
+// with work, n the query tiles of the current item.
 struct PairCursor {
-  int k, n;
+  int r, k, n;
   bool valid;
   FItem it;
   __device__ __forceinline__ static int item_of_round(int r) {
     const int G = gridDim.x, c = blockIdx.x;
     return r * G + ((r & 1) ? G - 1 - c : c);
   }
-  __device__ void init(const BwdParams &p, const KeyTiles &tiles) {
+  // from round r on, the first item that has work
+  __device__ void seek(const BwdParams &p) {
+    for (;; ++r) {
+      const int w = item_of_round(r);
+      valid = w < p.nitems;
+      if (!valid) return;
+      it = fitem(p, w);
+      if (it.NQ > 0) return;
+    }
+  }
+  __device__ void init(const BwdParams &p) {
+    r = 0;
     k = 0;
     n = 0;
-    const int w = item_of_round(0);
-    valid = w < p.nitems;
-    if (valid) it = fitem(p, tiles, w);
+    seek(p);
   }
-  __device__ void next(const BwdParams &p, const KeyTiles &tiles) {
+  __device__ void next(const BwdParams &p) {
     if (++n == it.NQ) {
       n = 0;
       ++k;
-      const int w = item_of_round(k);
-      valid = w < p.nitems;
-      if (valid) it = fitem(p, tiles, w);
+      ++r;
+      seek(p);
     }
   }
   __device__ int i0() const { return (it.qlo + n) * BQ; }
@@ -168,7 +188,6 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint8_t *smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const KeyTiles tiles(p.m, p.cap, p.head, p.L);
 
   const uint32_t b0 = sb + F_BAR;
   const uint32_t bar_kv = b0, bar_ld = b0 + 8, bar_sg = b0 + 16, bar_p = b0 + 24;
@@ -243,7 +262,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       };
       bool ok = true;
       PairCursor c;
-      c.init(p, tiles);
+      c.init(p);
       if (c.valid) {
         load_qu(c);
         load_do(c);
@@ -252,7 +271,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       for (int g = 0; ok && c.valid; ++g) {
         const bool first = c.n == 0;
         PairCursor nx = c;
-        nx.next(p, tiles);
+        nx.next(p);
         if (first && !(ok = mbar_wait(bar_kv, (c.k & 1), abort_flag))) break;
         if (!(ok = mbar_wait(bar_qu, g & 1, abort_flag) && mbar_wait(bar_ld, g & 1, abort_flag))) break;
         // G's columns hold the previous pair's dQ / dR until it was flushed
@@ -339,7 +358,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     if (lane == 0) {
       bool ok = true;
       PairCursor c;
-      c.init(p, tiles);
+      c.init(p);
       for (int g = 0; c.valid; ++g) {
         if (!(ok = mbar_wait(bar_staged, g & 1, abort_flag))) break;
         const int i0 = c.i0();
@@ -360,7 +379,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         bulk_commit();
         bulk_wait_read();
         mbar_arrive(bar_sfree);
-        c.next(p, tiles);
+        c.next(p);
       }
       // the reductions must be complete before shared memory goes away
       bulk_wait_all();
@@ -378,7 +397,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     float dvp = 0.f;  // sum over this warp's rows of dQp, column 32*hf + lane
     bool ok = true;
     PairCursor c;
-    c.init(p, tiles);
+    c.init(p);
     for (int g = 0; c.valid; ++g) {
       const FItem it = c.it;
       const int i0 = c.i0();
@@ -561,7 +580,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         dvp += v[0];
       }
-      c.next(p, tiles);
+      c.next(p);
       if (c.valid && c.n != 0) continue;
       // ---- end of the item: dV (half 0) and dK (half 1) rows, dv sums
       {
@@ -606,9 +625,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 // The dR and dQ accumulators and the du/dv sums <- 0; dK/dV rows of ring
 // slots that hold no valid memory <- 0; R16 <- fp16(R) (satfinite).
 __global__ void bwd_zero_kernel(float *dr, size_t n_dr, float *dq_acc, size_t n_dq, float *sums,
-                                int n_sums, __nv_bfloat16 *dk, __nv_bfloat16 *dv, int BH, int cap,
-                                int m, int head, int kv_rows, const __nv_bfloat16 *r, __half *r16,
-                                size_t n_r) {
+                                int n_sums, __nv_bfloat16 *dk, __nv_bfloat16 *dv, int BH, int H,
+                                int cap, int m, int head, int kv_rows, const __nv_bfloat16 *r,
+                                __half *r16, size_t n_r, const int *mvis) {
   const size_t tid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -624,12 +643,15 @@ __global__ void bwd_zero_kernel(float *dr, size_t n_dr, float *dq_acc, size_t n_
       o[f] = pack_f16(__uint_as_float(w[f] << 16), __uint_as_float(w[f] & 0xFFFF0000u));
     ((uint4 *)r16)[e] = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  const int empty = cap - m;
-  const size_t n_rows = (size_t)BH * empty * 8;
+  // ring slots whose rows the row does not see: logical slots t < m - mb
+  // (masked by a document reset) and t >= m (no valid memory); 8 x 16 B per row
+  const size_t n_rows = (size_t)BH * cap * 8;
   for (size_t e = tid; e < n_rows; e += stride) {
     const int c = (int)(e & 7);
     const size_t rr = e >> 3;
-    const int bh = (int)(rr / empty), t = m + (int)(rr % empty);  // logical slot t >= m
+    const int bh = (int)(rr / cap), t = (int)(rr % cap);
+    const int mb = row_memory(mvis, bh / H, m, cap, head).m;
+    if (t >= m - mb && t < m) continue;
     int pr = head + t;
     if (pr >= cap) pr -= cap;
     const size_t off = ((size_t)bh * kv_rows + pr) * DH;
@@ -834,9 +856,9 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   bwd_zero_kernel<<<sms * 4, 256, 0, st>>>(dr_acc, n_dr_acc, dq_acc, rows * DH, sums,
                                            2 * s.H * DH, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv,
-                                           s.B * s.H, s.cap, s.m, s.head, s.kv_rows,
+                                           s.B * s.H, s.H, s.cap, s.m, s.head, s.kv_rows,
                                            (const __nv_bfloat16 *)r, r16,
-                                           (size_t)s.H * s.kv_rows * DH);
+                                           (size_t)s.H * s.kv_rows * DH, s.mvis);
   ++*launches;
   if (o_lo) {
     long long blocks = ((long long)rows * 8 + 255) / 256;
@@ -854,6 +876,7 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   BwdParams p;
   p.B = s.B; p.H = s.H; p.L = s.L; p.cap = s.cap; p.m = s.m; p.head = s.head; p.nq = nq;
   p.kv_rows = s.kv_rows;
+  p.mvis = s.mvis;
   {
     // key tiles per (b,h): ring runs A and B, then the current rows
     const int lenA = s.m < s.cap - s.head ? s.m : s.cap - s.head;

@@ -49,6 +49,8 @@ using tc::DH;
 using tc::NB;
 using tc::KeyTile;
 using tc::KeyTiles;
+using tc::RowMemory;
+using tc::row_memory;
 
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
@@ -85,6 +87,7 @@ struct Params {
   float *delta;
   __nv_bfloat16 *qu_out;
   __half *qv_out;  // (Q+v) rows in fp16 for the backward's position products
+  const int *mvis;  // per-row document reset (nullable): newest memory rows per batch row
 };
 
 constexpr int kFwd = 0, kPrep = 1;
@@ -110,6 +113,7 @@ __device__ __forceinline__ bool pair_exchange(float mine, float *out, volatile f
 // ones, so that the CTAs' total key-tile counts stay within about one tile.
 struct Item {
   int bh, h, i0, T;
+  int m, head;  // the memory this batch row sees (all of it unless reset)
 };
 
 __device__ __forceinline__ Item item_at(const Params &p, int w) {
@@ -118,7 +122,10 @@ __device__ __forceinline__ Item item_at(const Params &p, int w) {
   it.bh = w % BH;
   it.h = it.bh % p.H;
   it.i0 = (p.nq - 1 - w / BH) * BQ;
-  it.T = KeyTiles(p.m, p.cap, p.head, min(it.i0 + BQ, p.L)).count();
+  const RowMemory rm = row_memory(p.mvis, it.bh / p.H, p.m, p.cap, p.head);
+  it.m = rm.m;
+  it.head = rm.head;
+  it.T = KeyTiles(it.m, p.cap, it.head, min(it.i0 + BQ, p.L)).count();
   return it;
 }
 
@@ -255,7 +262,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       int g_tma = 0;
       auto issue_tma = [&]() {
         const int s = g_tma & 1;
-        const KeyTile x = KeyTiles(p.m, p.cap, p.head, min(tc_.it.i0 + BQ, p.L)).get(tc_.t);
+        const KeyTile x = KeyTiles(tc_.it.m, p.cap, tc_.it.head, min(tc_.it.i0 + BQ, p.L)).get(tc_.t);
         const uint32_t bar = s ? bar_full1 : bar_full0;
         mbar_expect_tx(bar, STAGE_TX);
         tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, tc_.it.bh, bar);
@@ -375,7 +382,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       // tcgen05.ld/st below are warp-collective: keep every decision warp-uniform
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      const KeyTile x = KeyTiles(p.m, p.cap, p.head, min(it.i0 + BQ, p.L)).get(t);
+      const KeyTile x = KeyTiles(it.m, p.cap, it.head, min(it.i0 + BQ, p.L)).get(t);
       float y[64];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -585,6 +592,7 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   p.dout = (const __nv_bfloat16 *)dout; p.delta = delta;
   p.qu_out = (__nv_bfloat16 *)qu_out; p.qv_out = (__half *)qv_out;
   p.B = s.B; p.H = s.H; p.L = s.L; p.cap = s.cap; p.m = s.m; p.head = s.head;
+  p.mvis = s.mvis;
   p.nq = (s.L + BQ - 1) / BQ;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.q = (const __nv_bfloat16 *)q; p.u = (const __nv_bfloat16 *)u; p.vb = (const __nv_bfloat16 *)vb;

@@ -55,6 +55,14 @@ __device__ __forceinline__ int phys_row(const AttnShape &s, int j) {
   return t >= s.cap ? t - s.cap : t;
 }
 
+// Memory rows batch row b sees: all m, or under a per-row document reset its
+// newest mvis[b] (clamped into [0, m]); they are logical positions -mb..-1.
+__device__ __forceinline__ int row_m(const AttnShape &s, long long b) {
+  if (!s.mvis) return s.m;
+  const int mb = s.mvis[b];
+  return mb < 0 ? 0 : (mb > s.m ? s.m : mb);
+}
+
 constexpr int kDh = 64;
 constexpr int kWarps = 4;
 
@@ -77,7 +85,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(
   const T *rh = r + (long long)h * s.kv_rows * kDh;
   float mx = -INFINITY, l = 0.f;
   float2 acc = make_float2(0.f, 0.f);
-  for (int j = -s.m; j <= i; ++j) {
+  for (int j = -row_m(s, bh / s.H); j <= i; ++j) {
     const long long pr = phys_row(s, j);
     const float a = warp_sum(dot2(qu, ld2(kb + pr * kDh + 2 * lane)) +
                              dot2(qv, ld2(rh + (long long)(i - j) * kDh + 2 * lane)));
@@ -119,7 +127,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_d_kernel(
   const T *kb = k + bh * s.kv_rows * kDh, *vbase = v + bh * s.kv_rows * kDh;
   const T *rh = r + (long long)h * s.kv_rows * kDh;
   float2 acc = make_float2(0.f, 0.f);
-  for (int j = -s.m; j <= i; ++j) {
+  for (int j = -row_m(s, bh / s.H); j <= i; ++j) {
     const long long pr = phys_row(s, j);
     const float a = warp_sum(dot2(qu, ld2(kb + pr * kDh + 2 * lane)) +
                              dot2(qv, ld2(rh + (long long)(i - j) * kDh + 2 * lane)));
@@ -167,7 +175,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dq_kernel(
   const T *kb = k + bh * s.kv_rows * kDh, *vbase = v + bh * s.kv_rows * kDh;
   const T *rh = r + (long long)h * s.kv_rows * kDh;
   float2 gu = make_float2(0.f, 0.f), gv = make_float2(0.f, 0.f);
-  for (int j = -s.m; j <= i; ++j) {
+  for (int j = -row_m(s, bh / s.H); j <= i; ++j) {
     const long long pr = phys_row(s, j);
     const T *rrow = rh + (long long)(i - j) * kDh;
     float p;
@@ -199,7 +207,9 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dkv_kernel(
   if (pr < s.cap) {
     int t = pr - s.head;
     if (t < 0) t += s.cap;
-    if (t >= s.m) {  // ring row that holds no valid memory
+    // ring rows that hold no valid memory, or that this batch row's document
+    // reset masks, get zeros
+    if (t >= s.m || t - s.m < -row_m(s, bh / s.H)) {
       st2(dk + krow * kDh + 2 * lane, make_float2(0.f, 0.f));
       st2(dv + krow * kDh + 2 * lane, make_float2(0.f, 0.f));
       return;
@@ -246,7 +256,8 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dr_kernel(
     for (int b = 0; b < s.B; ++b) {
       const long long bh = (long long)b * s.H + h;
       const T *kb = k + bh * s.kv_rows * kDh, *vbase = v + bh * s.kv_rows * kDh;
-      for (int i = d - s.m > 0 ? d - s.m : 0; i < s.L; ++i) {
+      const int mb = row_m(s, b);  // keys j = i - d >= -mb
+      for (int i = d - mb > 0 ? d - mb : 0; i < s.L; ++i) {
         const int j = i - d;
         const long long qrow = bh * s.L + i;
         const long long pr = phys_row(s, j);

@@ -18,6 +18,9 @@ struct AttnShape {
   int head;       // physical row of the oldest memory row
   float scale;
   int kv_rows;    // cap + L
+  // per-row document reset (nullable device pointer, B entries): batch row b
+  // sees only its newest mvis[b] memory rows (clamped into [0, m])
+  const int *mvis = nullptr;
 };
 
 // Workspace layout of the backward (offsets in bytes from the base).

@@ -78,12 +78,18 @@ int rxl_device_error_flags(void) {
   return (fwd ? 1 : 0) | (bwd ? 2 : 0);
 }
 
-rxl_status rxl_attn_fwd_ex(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
-                           const void *r, const void *u, const void *vbias, void *o, void *o_lo,
-                           float *lse, rxl_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward with an optional per-row document reset (mvis: device int32 [B]).
+rxl_status attn_fwd(const rxl_attn_desc *desc, const int32_t *mvis, const void *q, const void *k,
+                    const void *v, const void *r, const void *u, const void *vbias, void *o,
+                    void *o_lo, float *lse, rxl_stream_t stream) {
   rxl::AttnShape s;
   rxl_status st = check_desc(desc, &s);
   if (st != RXL_OK) return st;
+  s.mvis = mvis;
   if ((st = check_ptrs({q, k, v, r, u, vbias, o, lse})) != RXL_OK) return st;
   if (o_lo && desc->dtype != RXL_DTYPE_BF16) return RXL_ERR_INVALID_ARGUMENT;
   if (o_lo && !aligned16(o_lo)) return RXL_ERR_MISALIGNED;
@@ -95,6 +101,25 @@ rxl_status rxl_attn_fwd_ex(const rxl_attn_desc *desc, const void *q, const void 
                                  (cudaStream_t)stream, &launches);
   g_last_launches = launches;
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+rxl_status rxl_attn_fwd_ex(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                           const void *r, const void *u, const void *vbias, void *o, void *o_lo,
+                           float *lse, rxl_stream_t stream) {
+  return attn_fwd(desc, nullptr, q, k, v, r, u, vbias, o, o_lo, lse, stream);
+}
+
+rxl_status rxl_attn_fwd_reset(const rxl_attn_desc *desc, const int32_t *mem_visible, const void *q,
+                              const void *k, const void *v, const void *r, const void *u,
+                              const void *vbias, void *o, void *o_lo, float *lse,
+                              rxl_stream_t stream) {
+  if (!mem_visible) return RXL_ERR_INVALID_ARGUMENT;
+  if ((uintptr_t)mem_visible % 4) return RXL_ERR_MISALIGNED;
+  return attn_fwd(desc, mem_visible, q, k, v, r, u, vbias, o, o_lo, lse, stream);
 }
 
 rxl_status rxl_attn_fwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
@@ -110,14 +135,20 @@ size_t rxl_attn_bwd_workspace_bytes(const rxl_attn_desc *desc) {
                                        : rxl::simt_bwd_workspace(s).total;
 }
 
-rxl_status rxl_attn_bwd_ex(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
-                           const void *r, const void *u, const void *vbias, const void *o,
-                           const void *o_lo, const float *lse, const void *dout, void *dq,
-                           void *dk, void *dv, float *dr, float *du, float *dvbias,
-                           void *workspace, size_t workspace_bytes, rxl_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward with an optional per-row document reset (mvis: device int32 [B]).
+rxl_status attn_bwd(const rxl_attn_desc *desc, const int32_t *mvis, const void *q, const void *k,
+                    const void *v, const void *r, const void *u, const void *vbias, const void *o,
+                    const void *o_lo, const float *lse, const void *dout, void *dq, void *dk,
+                    void *dv, float *dr, float *du, float *dvbias, void *workspace,
+                    size_t workspace_bytes, rxl_stream_t stream) {
   rxl::AttnShape s;
   rxl_status st = check_desc(desc, &s);
   if (st != RXL_OK) return st;
+  s.mvis = mvis;
   if (o_lo && desc->dtype != RXL_DTYPE_BF16) return RXL_ERR_INVALID_ARGUMENT;
   if (o_lo && !aligned16(o_lo)) return RXL_ERR_MISALIGNED;
   if ((st = check_ptrs({q, k, v, r, u, vbias, o, lse, dout, dq, dk, dv, dr, du, dvbias,
@@ -134,6 +165,31 @@ rxl_status rxl_attn_bwd_ex(const rxl_attn_desc *desc, const void *q, const void 
                                 du, dvbias, workspace, (cudaStream_t)stream, &launches);
   g_last_launches = launches;
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+rxl_status rxl_attn_bwd_ex(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
+                           const void *r, const void *u, const void *vbias, const void *o,
+                           const void *o_lo, const float *lse, const void *dout, void *dq,
+                           void *dk, void *dv, float *dr, float *du, float *dvbias,
+                           void *workspace, size_t workspace_bytes, rxl_stream_t stream) {
+  return attn_bwd(desc, nullptr, q, k, v, r, u, vbias, o, o_lo, lse, dout, dq, dk, dv, dr, du,
+                  dvbias, workspace, workspace_bytes, stream);
+}
+
+rxl_status rxl_attn_bwd_reset(const rxl_attn_desc *desc, const int32_t *mem_visible, const void *q,
+                              const void *k, const void *v, const void *r, const void *u,
+                              const void *vbias, const void *o, const void *o_lo, const float *lse,
+                              const void *dout, void *dq, void *dk, void *dv, float *dr, float *du,
+                              float *dvbias, void *workspace, size_t workspace_bytes,
+                              rxl_stream_t stream) {
+  if (!mem_visible) return RXL_ERR_INVALID_ARGUMENT;
+  if ((uintptr_t)mem_visible % 4) return RXL_ERR_MISALIGNED;
+  return attn_bwd(desc, mem_visible, q, k, v, r, u, vbias, o, o_lo, lse, dout, dq, dk, dv, dr, du,
+                  dvbias, workspace, workspace_bytes, stream);
 }
 
 rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,

@@ -58,6 +58,23 @@ struct KeyTiles {
   }
 };
 
+// Memory seen by batch row b under a per-row document reset: its newest
+// mb = clamp(mvis[b], 0, m) rows, which are themselves a ring run starting
+// at physical row (head + m - mb) mod cap. mvis == nullptr: all m rows.
+struct RowMemory {
+  int m, head;
+};
+__device__ __forceinline__ RowMemory row_memory(const int *mvis, int b, int m, int cap, int head) {
+  RowMemory r{m, head};
+  if (mvis) {
+    int mb = mvis[b];
+    mb = mb < 0 ? 0 : (mb > m ? m : mb);
+    r.m = mb;
+    r.head = cap > 0 ? (head + m - mb) % cap : 0;
+  }
+  return r;
+}
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }

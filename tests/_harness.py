@@ -147,3 +147,18 @@ class AttnCall:
                               self.lse, self.do, self.dq, self.dk, self.dv, self.dr, self.du,
                               self.dvb, self.ws, self.ws_bytes, stream)
         return self
+
+    # per-row document reset: mem_visible [B] int32 on the device
+    def fwd_reset(self, mem_visible, keep_low=True, stream=None):
+        self.mvis = self.torch.tensor(np.asarray(mem_visible, dtype=np.int32), device="cuda")
+        self.o_lo = self.torch.empty_like(self.o) if keep_low else None
+        self.rxl.rxl_attn_fwd_reset(self.desc, self.mvis, self.q, self.k, self.v, self.r, self.u,
+                                    self.vb, self.o, self.o_lo, self.lse, stream)
+        return self
+
+    def bwd_reset(self, stream=None):
+        self.rxl.rxl_attn_bwd_reset(self.desc, self.mvis, self.q, self.k, self.v, self.r, self.u,
+                                    self.vb, self.o, self.o_lo, self.lse, self.do, self.dq, self.dk,
+                                    self.dv, self.dr, self.du, self.dvb, self.ws, self.ws_bytes,
+                                    stream)
+        return self
