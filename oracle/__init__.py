@@ -192,6 +192,22 @@ def bwd(q, k, v, r, u, vb, dout, scale, pos0=0, nthreads=None, lib=None, mem_vis
     return out
 
 
+def proj(h_mem, h_cur, w_q, w_k, w_v, H):
+    """The projection front-end ("Segment-Level Recurrence": Q = H W^Q,
+    K = [SG(M); H] W^K, V = [SG(M); H] W^V; "Batched Tensor Contract" for
+    the shapes). h_mem [B,m,d] is the layer's hidden-state memory in logical
+    order (oldest first), h_cur [B,L,d]; w_* [d, H*dh]; projected column
+    h*dh + e is element e of head h. Returns q [B,H,L,dh] and k, v
+    [B,H,m+L,dh] (logical order), float64; a matrix product is the step."""
+    h_mem, h_cur = _f64(h_mem), _f64(h_cur)
+    w_q, w_k, w_v = _f64(w_q), _f64(w_k), _f64(w_v)
+    B, L, d = h_cur.shape
+    dh = w_q.shape[1] // H
+    h_t = np.concatenate([h_mem, h_cur], axis=1)           # H~ = [SG(M); H]
+    split = lambda x: x.reshape(B, x.shape[1], H, dh).transpose(0, 2, 1, 3).copy()
+    return split(h_cur @ w_q), split(h_t @ w_k), split(h_t @ w_v)
+
+
 def tail_m(mem: np.ndarray, hids: np.ndarray, mem_len: int) -> np.ndarray:
     """Memory update along axis -2 (sequence axis, d innermost):
     cat([mem, hids]) then keep the last mem_len rows; mem_len == 0 keeps an

@@ -408,3 +408,43 @@ def reset_vs_sliced(mvis, B=3, H=2, L=6, m=7, dh=16, seed=11, lib=None):
 @pytest.mark.parametrize("mvis", [(7, 0, 3), (0, 0, 0), (7, 7, 7), (1, 6, 2)])
 def test_document_reset_equals_the_row_alone(mvis):
     assert reset_vs_sliced(mvis) == []
+
+
+# ------------------------------------------------ projection front-end
+
+def test_projection_matches_brute_force_and_head_split():
+    """Q = H W^Q, K/V = [SG(M); H] W^{K,V} ("Segment-Level Recurrence"), head h
+    taking columns h*dh .. h*dh+dh-1: checked element by element with loops."""
+    rng = np.random.default_rng(5)
+    B, m, L, d, H, dh = 2, 3, 4, 8, 2, 3
+    hm, hc = rand(rng, B, m, d), rand(rng, B, L, d)
+    wq, wk, wv = rand(rng, d, H * dh), rand(rng, d, H * dh), rand(rng, d, H * dh)
+    q, k, v = oracle.proj(hm, hc, wq, wk, wv, H)
+    assert q.shape == (B, H, L, dh) and k.shape == (B, H, m + L, dh) and v.shape == k.shape
+    for b in range(B):
+        for h in range(H):
+            for e in range(dh):
+                col = h * dh + e
+                for i in range(L):
+                    assert abs(q[b, h, i, e] - sum(hc[b, i, c] * wq[c, col] for c in range(d))) < 1e-12
+                for j in range(m + L):
+                    row = hm[b, j] if j < m else hc[b, j - m]
+                    assert abs(k[b, h, j, e] - sum(row[c] * wk[c, col] for c in range(d))) < 1e-12
+                    assert abs(v[b, h, j, e] - sum(row[c] * wv[c, col] for c in range(d))) < 1e-12
+
+
+def test_projection_identity_weights_split_the_hidden_state():
+    rng = np.random.default_rng(6)
+    B, m, L, H, dh = 2, 5, 3, 4, 2
+    d = H * dh
+    hm, hc = rand(rng, B, m, d), rand(rng, B, L, d)
+    eye = np.eye(d)
+    q, k, v = oracle.proj(hm, hc, eye, eye, eye, H)
+    ht = np.concatenate([hm, hc], 1)
+    for h in range(H):
+        assert np.array_equal(q[:, h], hc[:, :, h * dh:(h + 1) * dh])
+        assert np.array_equal(k[:, h], ht[:, :, h * dh:(h + 1) * dh])
+        assert np.array_equal(v[:, h], ht[:, :, h * dh:(h + 1) * dh])
+    # queries come from the current segment only: the memory never changes q
+    q2, _, _ = oracle.proj(hm * 0 + 7.0, hc, eye, eye, eye, H)
+    assert np.array_equal(q, q2)
