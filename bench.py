@@ -282,6 +282,7 @@ def run_ours(args, rank, world):
         out["mem_update_roofline"] = mu
         out["window_recompute"] = window_recompute()
         out["reset_cfg3"] = reset_cfg3()
+        out["proj_cfg3"] = proj_cfg3()
     if world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         dt, fl = cpu_sample(x, (0, 4), nthreads)
@@ -394,6 +395,45 @@ def reset_cfg3(reps=10):
     return {"workload": "cfg3 with per-row reset, mem_visible = 0/128/384/512 by b mod 4",
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "visible_pairs": pairs,
             "tflops": flop / ((fwd_ms + bwd_ms) * 1e-3) / 1e12}
+
+
+def proj_cfg3(reps=20):
+    """The projection front-end at the cfg3 shape with a hidden-state memory:
+    d = 1024, H*dh = 1024; Q from the 512 current rows, K and V from the 512
+    memory + 512 current rows of each of the 16 batch rows (2 * 16 * (512 +
+    2 * 1024) * 1024 * 1024 flop). Warm L2, back-to-back calls (the weights
+    are 6 MB, the hidden states 32 MB)."""
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    d, Hh = 1024, H
+    g = torch.Generator(device="cuda").manual_seed(11)
+    bf = torch.bfloat16
+    mk = lambda *s, std=1.0: (torch.randn(*s, generator=g, device="cuda") * std).to(bf)
+    hm, hc = mk(B, M, d), mk(B, L, d)
+    w = [mk(d, Hh * DH, std=d ** -0.5) for _ in range(3)]
+    q = torch.empty(B, Hh, L, DH, device="cuda", dtype=bf)
+    k = torch.empty(B, Hh, M + L, DH, device="cuda", dtype=bf)
+    v = torch.empty_like(k)
+    desc = rxl.make_desc(B, Hh, L, M, M, 0, SCALE, rxl.RXL_DTYPE_BF16)
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        rxl.rxl_qkv_proj(desc, d, hm, hc, *w, q, k, v, st)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        rxl.rxl_qkv_proj(desc, d, hm, hc, *w, q, k, v, st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flop = 2 * B * (L + 2 * (M + L)) * d * Hh * DH
+    peak_tf, _, kind = peaks()
+    tf = flop / (ms * 1e-3) / 1e12
+    return {"workload": "cfg3 shape, d=1024, hidden-state memory of 512 rows; Q, K, V in one launch",
+            "ms": ms, "tflops": tf, "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf,
+                                                  "unit": "TFLOP/s", "frac": tf / peak_tf,
+                                                  "peak_kind": f"{kind} bf16 burst"},
+            "note": "warm L2, back-to-back calls"}
 
 
 def window_recompute(reps=20):

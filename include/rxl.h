@@ -205,6 +205,28 @@ rxl_status rxl_attn_bwd_reset(const rxl_attn_desc *desc, const int32_t *mem_visi
                               rxl_stream_t stream);
 
 /*
+ * Projection front-end (Transformer-XL page, "Segment-Level Recurrence":
+ * Q = H W^Q, K = [SG(M); H] W^K, V = [SG(M); H] W^V; shapes as in "Batched
+ * Tensor Contract"). The memory holds the layer's input hidden states, as the
+ * pages define it, in a ring with the same mapping as K/V.
+ *   d_model   hidden width d: a multiple of 64 (bf16 only)
+ *   h_mem     [B, M, d] hidden-state ring: logical memory row t at physical
+ *             row (mem_head + t) mod M; NULL allowed when M == 0
+ *   h_cur     [B, L, d] the current segment's hidden states
+ *   w_q, w_k, w_v  [d, H*dh] row-major; column h*dh + e feeds element e of head h
+ *   q         [B, H, L, dh] written
+ *   k, v      [B, H, M+L, dh] written in the attention's layout: ring slot p
+ *             of h_mem projects to physical row p, current row i to row M+i.
+ *             Rows of ring slots without valid memory are not written.
+ * The ring of hidden states is advanced with rxl_mem_update (D = d_model).
+ * Errors: RXL_ERR_UNSUPPORTED for f32 or a width that is not a multiple of
+ * 64; the usual argument, alignment and device-error rules otherwise.
+ */
+rxl_status rxl_qkv_proj(const rxl_attn_desc *desc, int d_model, const void *h_mem,
+                        const void *h_cur, const void *w_q, const void *w_k, const void *w_v,
+                        void *q, void *k, void *v, rxl_stream_t stream);
+
+/*
  * FIFO memory ring (eq. Tail_M; update_mems with mem_len == cap).
  *   data         device pointer to plane 0, row 0
  *   planes       independent rings (e.g. B*H), >= 1
@@ -250,7 +272,8 @@ int rxl_last_launch_count(void);
  * word instead of hanging, drains its in-flight copies, frees its tensor
  * memory and exits with its outputs undefined. This call synchronises the
  * current device, returns the recorded bits (bit 0: forward kernel, bit 1:
- * backward kernels) and clears them; -1 if the device could not be read.
+ * backward kernels, bit 2: projection kernel) and clears them; -1 if the
+ * device could not be read.
  */
 int rxl_device_error_flags(void);
 

@@ -80,6 +80,8 @@ def lib():
             L.rxl_attn_fwd_reset.restype = ctypes.c_int
             L.rxl_attn_bwd_reset.argtypes = [P(rxl_attn_desc)] + [vp] * 18 + [ctypes.c_size_t, vp]
             L.rxl_attn_bwd_reset.restype = ctypes.c_int
+            L.rxl_qkv_proj.argtypes = [P(rxl_attn_desc), ctypes.c_int] + [vp] * 8 + [vp]
+            L.rxl_qkv_proj.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc.argtypes = [P(rxl_attn_desc)] + [vp] * 15 + [vp]
             L.rxl_attn_bwd_noalloc.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc_max_scratch_bytes.argtypes = []
@@ -144,6 +146,12 @@ def rxl_attn_bwd_reset(desc, mem_visible, q, k, v, r, u, vbias, o, o_lo, lse, do
                                     *map(_ptr, (mem_visible, q, k, v, r, u, vbias, o, o_lo, lse, dout,
                                                 dq, dk, dv, dr, du, dvbias, workspace)),
                                     int(workspace_bytes), _stream(stream)), "rxl_attn_bwd_reset")
+
+
+def rxl_qkv_proj(desc, d_model, h_mem, h_cur, w_q, w_k, w_v, q, k, v, stream=None):
+    _check(lib().rxl_qkv_proj(ctypes.byref(desc), int(d_model),
+                              *map(_ptr, (h_mem, h_cur, w_q, w_k, w_v, q, k, v)), _stream(stream)),
+           "rxl_qkv_proj")
 
 
 def rxl_attn_bwd_workspace_bytes(desc) -> int:

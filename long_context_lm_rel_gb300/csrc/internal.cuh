@@ -72,4 +72,11 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
                           float *dvb, void *ws, cudaStream_t st, int *launches);
 cudaError_t tc_bwd_read_error(int *flag);
 
+// Projection front-end (bf16): q, k, v from the hidden-state memory ring and
+// the current hidden states.
+cudaError_t launch_tc_proj(const AttnShape &s, int d, const void *h_mem, const void *h_cur,
+                           const void *wq, const void *wk, const void *wv, void *q, void *k, void *v,
+                           cudaStream_t st, int *launches);
+cudaError_t tc_proj_read_error(int *flag);
+
 }  // namespace rxl

@@ -72,10 +72,28 @@ int rxl_last_cuda_error(void) { return g_last_cuda_error; }
 int rxl_last_launch_count(void) { return g_last_launches; }
 
 int rxl_device_error_flags(void) {
-  int fwd = 0, bwd = 0;
-  if (rxl::tc_fwd_read_error(&fwd) != cudaSuccess || rxl::tc_bwd_read_error(&bwd) != cudaSuccess)
+  int fwd = 0, bwd = 0, proj = 0;
+  if (rxl::tc_fwd_read_error(&fwd) != cudaSuccess || rxl::tc_bwd_read_error(&bwd) != cudaSuccess ||
+      rxl::tc_proj_read_error(&proj) != cudaSuccess)
     return -1;
-  return (fwd ? 1 : 0) | (bwd ? 2 : 0);
+  return (fwd ? 1 : 0) | (bwd ? 2 : 0) | (proj ? 4 : 0);
+}
+
+rxl_status rxl_qkv_proj(const rxl_attn_desc *desc, int d_model, const void *h_mem,
+                        const void *h_cur, const void *w_q, const void *w_k, const void *w_v,
+                        void *q, void *k, void *v, rxl_stream_t stream) {
+  rxl::AttnShape s;
+  rxl_status st = check_desc(desc, &s);
+  if (st != RXL_OK) return st;
+  if (desc->dtype != RXL_DTYPE_BF16) return RXL_ERR_UNSUPPORTED;
+  if (d_model < 64 || d_model % 64 != 0 || d_model > (1 << 16)) return RXL_ERR_UNSUPPORTED;
+  if ((st = check_ptrs({h_cur, w_q, w_k, w_v, q, k, v})) != RXL_OK) return st;
+  if (s.cap > 0 && (st = check_ptrs({h_mem})) != RXL_OK) return st;
+  int launches = 0;
+  const cudaError_t e = rxl::launch_tc_proj(s, d_model, h_mem, h_cur, w_q, w_k, w_v, q, k, v,
+                                            (cudaStream_t)stream, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
 }
 
 }  // extern "C"
