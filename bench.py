@@ -39,6 +39,9 @@ WORKLOAD = "cfg3_bf16_B16H16_L512M512_dh64_fwd+bwd"
 B, H, L, M, DH = 16, 16, 512, 512, 64
 SCALE = 1.0 / math.sqrt(DH)
 FLOP_FWD_PAIR, FLOP_BWD_PAIR = 6 * DH, 12 * DH
+# dram__bytes_read.sum + dram__bytes_write.sum of one rxl_bwd_main_kernel
+# launch at cfg3: 45.06 MB at B=4 (profiles/bwd_main_kernel_B4H16L512M512.md) x 4
+TRAFFIC_BWD_MAIN = 4 * 45.06e6
 
 
 def visible_pairs(b, h, l, m):
@@ -267,8 +270,12 @@ def run_ours(args, rank, world):
         "config": {"workload": WORKLOAD, "B": B, "H": H, "L": L, "M": M, "mem_len": m, "dh": DH,
                    "flop_per_step": flop_step, "l2": "flushed between steps (256 MiB write, outside events)",
                    "parallelism": f"{world} independent replicas (one per GPU)"},
-        "roofline": {"bound": "tensor", "kernel": "rxl_attn_bwd_ex", "achieved": achieved, "peak": peak_tf,
-                     "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+        "roofline": {"bound": "tensor",
+                     "kernel": "rxl_attn_bwd_ex call (5 launches; rxl_bwd_main_kernel is 88 % of it)",
+                     "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                     "traffic": TRAFFIC_BWD_MAIN if B == 16 else None,
+                     "traffic_note": "rxl_bwd_main_kernel dram read+write per launch: ncu capture at "
+                                     "B=4 (profiles/) x 4, the items scaling with B",
                      "peak_kind": f"{peak_kind} bf16 burst"},
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -285,10 +292,10 @@ def run_ours(args, rank, world):
         out["proj_cfg3"] = proj_cfg3()
     if world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
-        dt, fl = cpu_sample(x, (0, 4), nthreads)
-        out["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": min(nthreads, 4 * B),
+        dt, fl = cpu_sample(x, (0, H), nthreads)
+        out["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": min(nthreads, H * B),
                                "kind": "oracle",
-                               "sample": f"fwd+bwd of 4 heads x {B} batch rows (64 of 256 (b,h) units), {dt:.1f} s"}
+                               "sample": f"fwd+bwd of the whole workload ({H * B} (b,h) units), {dt:.1f} s"}
     print(json.dumps(out), flush=True)
 
 

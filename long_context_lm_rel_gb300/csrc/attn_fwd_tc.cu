@@ -116,21 +116,28 @@ struct Item {
   int m, head;  // the memory this batch row sees (all of it unless reset)
 };
 
+template <bool RESET>
 __device__ __forceinline__ Item item_at(const Params &p, int w) {
   const int BH = p.B * p.H;
   Item it;
   it.bh = w % BH;
   it.h = it.bh % p.H;
   it.i0 = (p.nq - 1 - w / BH) * BQ;
-  const RowMemory rm = row_memory(p.mvis, it.bh / p.H, p.m, p.cap, p.head);
-  it.m = rm.m;
-  it.head = rm.head;
+  if (RESET) {
+    const RowMemory rm = row_memory(p.mvis, it.bh / p.H, p.m, p.cap, p.head);
+    it.m = rm.m;
+    it.head = rm.head;
+  } else {
+    it.m = p.m;
+    it.head = p.head;
+  }
   it.T = KeyTiles(it.m, p.cap, it.head, min(it.i0 + BQ, p.L)).count();
   return it;
 }
 
 // Walks this CTA's tiles across its items: k counts the CTA's items, t the
 // key tiles of the current item.
+template <bool RESET>
 struct Cursor {
   int k, w, t, nitems;
   bool valid;
@@ -145,7 +152,7 @@ struct Cursor {
     t = 0;
     w = item_of_round(0);
     valid = w < nitems;
-    if (valid) it = item_at(p, w);
+    if (valid) it = item_at<RESET>(p, w);
   }
   __device__ void next(const Params &p) {
     if (++t == it.T) {
@@ -153,7 +160,7 @@ struct Cursor {
       ++k;
       w = item_of_round(k);
       valid = w < nitems;
-      if (valid) it = item_at(p, w);
+      if (valid) it = item_at<RESET>(p, w);
     }
   }
 };
@@ -202,7 +209,7 @@ __device__ __forceinline__ void q_prep(const Params &p, const Item &it, uint32_t
 // Persistent kernel: gridDim.x CTAs walk all work items. Per CTA, tiles are
 // numbered g = 0, 1, ... across its items; every barrier phase follows g
 // (tile barriers) or the item counter k (q_ready, o_free).
-template <int MODE>
+template <int MODE, bool RESET>
 __global__ void __launch_bounds__(kThreads, 1)
 rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_r, const Params p, int nitems) {
@@ -257,7 +264,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (lane == 0) {
       bool pending[2] = {false, false};
       int nissued[2] = {0, 0};
-      Cursor tc_;  // next tile to load
+      Cursor<RESET> tc_;  // next tile to load
       tc_.init(p, nitems);
       int g_tma = 0;
       auto issue_tma = [&]() {
@@ -296,7 +303,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         return r;
       };
       bool ok = true;
-      Cursor mc;  // tile whose P.V is next
+      Cursor<RESET> mc;  // tile whose P.V is next
       mc.init(p, nitems);
       if (tc_.valid) issue_tma();
       if (tc_.valid) issue_tma();
@@ -305,7 +312,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (ok) issue_sg(0);
       }
       for (int g = 0; ok && mc.valid; ++g) {
-        Cursor nx = mc;
+        Cursor<RESET> nx = mc;
         nx.next(p);
         const bool new_item = nx.valid && nx.t == 0;
         // S/G of tile g+1 as soon as the softmax released S/G of tile g
@@ -363,7 +370,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint32_t xphase = 0;
     float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's part of the row sum
     bool ok = true;
-    Cursor cur;
+    Cursor<RESET> cur;
     cur.init(p, nitems);
     if (cur.valid) {
       q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
@@ -584,8 +591,11 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(rxl_fwd_tc_kernel<MODE>,
+    attr_err = cudaFuncSetAttribute(rxl_fwd_tc_kernel<MODE, false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(rxl_fwd_tc_kernel<MODE, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   Params p;
@@ -602,7 +612,11 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const unsigned grid = (unsigned)(nitems < sms ? nitems : sms);
-  rxl_fwd_tc_kernel<MODE><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
+  // the per-row reset is a separate instantiation: the plain call pays nothing for it
+  if (s.mvis)
+    rxl_fwd_tc_kernel<MODE, true><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
+  else
+    rxl_fwd_tc_kernel<MODE, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
   ++*launches;
   return cudaGetLastError();
 }
