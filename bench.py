@@ -40,7 +40,8 @@ B, H, L, M, DH = 16, 16, 512, 512, 64
 SCALE = 1.0 / math.sqrt(DH)
 FLOP_FWD_PAIR, FLOP_BWD_PAIR = 6 * DH, 12 * DH
 # dram__bytes_read.sum + dram__bytes_write.sum of one rxl_bwd_main_kernel
-# launch at cfg3: 45.06 MB at B=4 (profiles/bwd_main_kernel_B4H16L512M512.md) x 4
+# launch at cfg3: 45.06 MB measured by ncu at B=4, times 4 (the work items
+# scale with the batch)
 TRAFFIC_BWD_MAIN = 4 * 45.06e6
 
 
@@ -275,7 +276,7 @@ def run_ours(args, rank, world):
                      "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
                      "traffic": TRAFFIC_BWD_MAIN if B == 16 else None,
                      "traffic_note": "rxl_bwd_main_kernel dram read+write per launch: ncu capture at "
-                                     "B=4 (profiles/) x 4, the items scaling with B",
+                                     "B=4, times 4 (the items scale with B)",
                      "peak_kind": f"{peak_kind} bf16 burst"},
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
