@@ -208,6 +208,35 @@ def proj(h_mem, h_cur, w_q, w_k, w_v, H):
     return split(h_cur @ w_q), split(h_t @ w_k), split(h_t @ w_v)
 
 
+def layer_norm(x, gamma, beta, eps=1e-5):
+    """(x - mean) / sqrt(var + eps) * gamma + beta over the last axis, with the
+    biased variance (float64)."""
+    x = _f64(x)
+    mu = x.mean(-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * _f64(gamma) + _f64(beta)
+
+
+def layer_fwd(h_mem, h_in, w, H, scale, eps=1e-5, nthreads=None):
+    """One evaluation layer (float64): the attention sublayer of "Segment-Level
+    Recurrence" (Q = H W^Q, K/V = [SG(M); H] W^{K,V}, the relative-position
+    attention) and a feed-forward sublayer, in the post-norm arrangement
+    (the pages leave the layer's remaining steps open):
+        x1 = h_in + Attn . W_O,  x1n = LN1(x1),
+        h_out = LN2(x1n + ReLU(x1n W_1 + b_1) W_2 + b_2).
+    h_mem [B,m,d] logical order, h_in [B,L,d]; w: dict of the weights named as
+    the fields of rxl_layer_weights. Returns h_out [B,L,d]."""
+    q, k, v = proj(h_mem, h_in, w["w_q"], w["w_k"], w["w_v"], H)
+    o, _ = fwd(q, k, v, w["r"], w["u"], w["vbias"], scale, nthreads=nthreads)
+    B, _, L, dh = o.shape
+    om = o.transpose(0, 2, 1, 3).reshape(B, L, H * dh)      # heads merged: column h*dh + e
+    x1 = _f64(h_in) + om @ _f64(w["w_o"])
+    x1n = layer_norm(x1, w["ln1_gamma"], w["ln1_beta"], eps)
+    z = np.maximum(x1n @ _f64(w["w_1"]) + _f64(w["b_1"]), 0.0)
+    x2 = x1n + z @ _f64(w["w_2"]) + _f64(w["b_2"])
+    return layer_norm(x2, w["ln2_gamma"], w["ln2_beta"], eps)
+
+
 def tail_m(mem: np.ndarray, hids: np.ndarray, mem_len: int) -> np.ndarray:
     """Memory update along axis -2 (sequence axis, d innermost):
     cat([mem, hids]) then keep the last mem_len rows; mem_len == 0 keeps an

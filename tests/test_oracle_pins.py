@@ -448,3 +448,57 @@ def test_projection_identity_weights_split_the_hidden_state():
     # queries come from the current segment only: the memory never changes q
     q2, _, _ = oracle.proj(hm * 0 + 7.0, hc, eye, eye, eye, H)
     assert np.array_equal(q, q2)
+
+
+# ------------------------------------------------ evaluation layer
+
+def _layer_weights(rng, H, dh, d, dff, m, L):
+    return dict(w_q=rand(rng, d, H * dh, std=d ** -0.5), w_k=rand(rng, d, H * dh, std=d ** -0.5),
+                w_v=rand(rng, d, H * dh, std=d ** -0.5), w_o=rand(rng, H * dh, d, std=(H * dh) ** -0.5),
+                r=rand(rng, H, m + L, dh), u=rand(rng, H, dh, std=0.1), vbias=rand(rng, H, dh, std=0.1),
+                ln1_gamma=1 + rand(rng, d, std=0.1), ln1_beta=rand(rng, d, std=0.1),
+                w_1=rand(rng, d, dff, std=d ** -0.5), b_1=rand(rng, dff, std=0.1),
+                w_2=rand(rng, dff, d, std=dff ** -0.5), b_2=rand(rng, d, std=0.1),
+                ln2_gamma=1 + rand(rng, d, std=0.1), ln2_beta=rand(rng, d, std=0.1))
+
+
+def test_layer_norm_matches_torch():
+    rng = np.random.default_rng(8)
+    x, g, b = rand(rng, 3, 5, 16), rand(rng, 16), rand(rng, 16)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (16,), torch.from_numpy(g),
+                                         torch.from_numpy(b), eps=1e-5).numpy()
+    assert np.allclose(oracle.layer_norm(x, g, b), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_layer_with_silent_sublayers_is_two_norms():
+    """W_O = 0 and a zero FFN leave only the residual path: LN2(LN1(h))."""
+    rng = np.random.default_rng(9)
+    B, H, dh, L, m = 2, 2, 4, 3, 5
+    d, dff = H * dh, 12
+    w = _layer_weights(rng, H, dh, d, dff, m, L)
+    for n in ("w_o", "w_1", "b_1", "w_2", "b_2"):
+        w[n] = np.zeros_like(w[n])
+    hm, hi = rand(rng, B, m, d), rand(rng, B, L, d)
+    out = oracle.layer_fwd(hm, hi, w, H, 0.5, nthreads=1)
+    ref = oracle.layer_norm(oracle.layer_norm(hi, w["ln1_gamma"], w["ln1_beta"]),
+                            w["ln2_gamma"], w["ln2_beta"])
+    assert np.allclose(out, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_layer_merges_heads_in_column_order():
+    """With W_O = I and the FFN silent, LN1's input is h + [o_head0 | o_head1 | ...]."""
+    rng = np.random.default_rng(10)
+    B, H, dh, L, m = 2, 3, 4, 5, 6
+    d, dff = H * dh, 8
+    w = _layer_weights(rng, H, dh, d, dff, m, L)
+    w["w_o"] = np.eye(d)
+    for n in ("w_1", "b_1", "w_2", "b_2"):
+        w[n] = np.zeros_like(w[n])
+    w["ln1_gamma"], w["ln1_beta"] = np.ones(d), np.zeros(d)
+    w["ln2_gamma"], w["ln2_beta"] = np.ones(d), np.zeros(d)
+    hm, hi = rand(rng, B, m, d), rand(rng, B, L, d)
+    q, k, v = oracle.proj(hm, hi, w["w_q"], w["w_k"], w["w_v"], H)
+    o, _ = oracle.fwd(q, k, v, w["r"], w["u"], w["vbias"], 0.5, nthreads=1)
+    x1 = hi + np.concatenate([o[:, h] for h in range(H)], axis=-1)
+    ref = oracle.layer_norm(oracle.layer_norm(x1, np.ones(d), np.zeros(d)), np.ones(d), np.zeros(d))
+    assert np.allclose(oracle.layer_fwd(hm, hi, w, H, 0.5, nthreads=1), ref, rtol=1e-12, atol=1e-12)
