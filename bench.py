@@ -291,6 +291,7 @@ def run_ours(args, rank, world):
         out["window_recompute"] = window_recompute()
         out["reset_cfg3"] = reset_cfg3()
         out["proj_cfg3"] = proj_cfg3()
+        out["stack_cfg5"] = stack_cfg5()
     if world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         dt, fl = cpu_sample(x, (0, H), nthreads)
@@ -442,6 +443,71 @@ def proj_cfg3(reps=20):
                                                   "unit": "TFLOP/s", "frac": tf / peak_tf,
                                                   "peak_kind": f"{kind} bf16 burst"},
             "note": "warm L2, back-to-back calls"}
+
+
+def stack_cfg5(segments=3, layers=16):
+    """The full evaluation stack at the cfg5 shape: 16 layers (d = 1024,
+    d_ff = 4096, H = 16) over B4 L128 segments, each layer's hidden-state
+    memory already holding M = 1600 rows (steady state; the ring head moves
+    by L per segment). Per segment and layer: rxl_layer_fwd (projections of
+    the 1728 memory + current rows, attention, W_O, two LayerNorms, the
+    feed-forward sublayer) and rxl_mem_update of that layer's input states.
+    Seeded device normals (timing only; parity is in the tests)."""
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    B5, H5, L5, M5, d, dff = 4, 16, 128, 1600, 1024, 4096
+    g = torch.Generator(device="cuda").manual_seed(13)
+    bf = torch.bfloat16
+    mk = lambda *s, std=1.0: (torch.randn(*s, generator=g, device="cuda") * std).to(bf)
+    Ws, keep = [], []
+    for _ in range(layers):
+        t = dict(w_q=mk(d, H5 * DH, std=d ** -0.5), w_k=mk(d, H5 * DH, std=d ** -0.5),
+                 w_v=mk(d, H5 * DH, std=d ** -0.5), w_o=mk(H5 * DH, d, std=(H5 * DH) ** -0.5),
+                 r=mk(H5, M5 + L5, DH, std=0.7), u=mk(H5, DH, std=0.02), vbias=mk(H5, DH, std=0.02),
+                 ln1_gamma=torch.ones(d, device="cuda", dtype=bf), ln1_beta=torch.zeros(d, device="cuda", dtype=bf),
+                 w_1=mk(d, dff, std=d ** -0.5), b_1=mk(dff, std=0.1), w_2=mk(dff, d, std=dff ** -0.5),
+                 b_2=mk(d, std=0.1), ln2_gamma=torch.ones(d, device="cuda", dtype=bf),
+                 ln2_beta=torch.zeros(d, device="cuda", dtype=bf))
+        keep.append(t)
+        Ws.append(rxl.make_layer_weights(**t))
+    rings = [mk(B5, M5, d) for _ in range(layers)]
+    state = [rxl.rxl_ring(rings[n].data_ptr(), B5, M5, d, M5 * d, rxl.RXL_DTYPE_BF16, 0, M5)
+             for n in range(layers)]
+    hs = [mk(B5, L5, d) for _ in range(layers + 1)]
+    desc0 = rxl.make_desc(B5, H5, L5, M5, M5, 0, SCALE, rxl.RXL_DTYPE_BF16)
+    wsb = rxl.rxl_layer_fwd_workspace_bytes(desc0, d, dff)
+    ws = torch.empty(wsb, device="cuda", dtype=torch.uint8)
+    st = torch.cuda.current_stream()
+    launches = 0
+
+    def segment():
+        nonlocal launches
+        for n in range(layers):
+            desc = rxl.make_desc(B5, H5, L5, M5, state[n].len, state[n].head, SCALE, rxl.RXL_DTYPE_BF16)
+            rxl.rxl_layer_fwd(desc, d, dff, Ws[n], rings[n], hs[n], hs[n + 1], ws, wsb, st)
+            launches += rxl.rxl_last_launch_count()
+            rxl.rxl_mem_update(state[n], hs[n], L5 * d, L5, st)
+            launches += rxl.rxl_last_launch_count()
+
+    segment()
+    torch.cuda.synchronize()
+    launches = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(segments):
+        segment()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / segments
+    rows_kv = M5 + L5
+    flop_layer = (2 * B5 * (L5 + 2 * rows_kv) * d * H5 * DH              # Q, K, V projections
+                  + visible_pairs(B5, H5, L5, M5) * FLOP_FWD_PAIR           # attention
+                  + 2 * B5 * L5 * H5 * DH * d                             # W_O
+                  + 2 * 2 * B5 * L5 * d * dff)                            # feed-forward
+    return {"workload": "cfg5 shape, 16-layer stack: B4 H16 L128, hidden-state memory 1600 rows, d 1024, d_ff 4096, fwd",
+            "ms_per_segment": ms, "tokens_per_s": B5 * L5 / (ms * 1e-3),
+            "tflops": layers * flop_layer / (ms * 1e-3) / 1e12, "gpu_launches_per_segment": launches // segments,
+            "note": "steady state (memory full); each segment re-projects K/V of the 1728 memory + current rows per layer"}
 
 
 def window_recompute(reps=20):

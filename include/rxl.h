@@ -227,6 +227,42 @@ rxl_status rxl_qkv_proj(const rxl_attn_desc *desc, int d_model, const void *h_me
                         void *q, void *k, void *v, rxl_stream_t stream);
 
 /*
+ * One Transformer-XL layer for evaluation streams (forward only): the
+ * attention sublayer over [SG(memory); current] (projections, the
+ * relative-position attention above, output projection) and a feed-forward
+ * sublayer. The pages define the attention and the memory; they leave the
+ * rest of the layer open ("obtain the layer's new representation"). Read
+ * here as the original post-norm block:
+ *   x1  = h_in + Attn([SG(h_mem); h_in]) . W_O
+ *   x1n = LayerNorm1(x1)
+ *   x2  = x1n + ReLU(x1n . W_1 + b_1) . W_2 + b_2
+ *   h_out = LayerNorm2(x2)           (LayerNorm: biased variance, eps 1e-5)
+ * Weights (bf16, row-major, device): w_q, w_k, w_v [d, H*dh]; w_o [H*dh, d];
+ * r [H, M+L, dh], u, vbias [H, dh] as for the attention; w_1 [d, d_ff], b_1
+ * [d_ff]; w_2 [d_ff, d], b_2 [d]; ln*_gamma, ln*_beta [d].
+ *   h_mem  [B, M, d] the layer's hidden-state memory ring (as in rxl_qkv_proj)
+ *   h_in   [B, L, d] the layer's input; h_out [B, L, d] written
+ *   workspace  rxl_layer_fwd_workspace_bytes(desc, d_model, d_ff) bytes
+ * The caller advances the memory afterwards with rxl_mem_update(ring over
+ * h_mem with D = d, src = h_in): the layer's input states are what the next
+ * segment's layer attends to (eq. Tail_M). bf16 only; d_model a multiple of
+ * 256, d_ff a multiple of 64 (else RXL_ERR_UNSUPPORTED).
+ */
+typedef struct {
+  const void *w_q, *w_k, *w_v, *w_o;
+  const void *r, *u, *vbias;
+  const void *ln1_gamma, *ln1_beta;
+  const void *w_1, *b_1, *w_2, *b_2;
+  const void *ln2_gamma, *ln2_beta;
+} rxl_layer_weights;
+
+size_t rxl_layer_fwd_workspace_bytes(const rxl_attn_desc *desc, int d_model, int d_ff);
+
+rxl_status rxl_layer_fwd(const rxl_attn_desc *desc, int d_model, int d_ff, const rxl_layer_weights *w,
+                         const void *h_mem, const void *h_in, void *h_out, void *workspace,
+                         size_t workspace_bytes, rxl_stream_t stream);
+
+/*
  * FIFO memory ring (eq. Tail_M; update_mems with mem_len == cap).
  *   data         device pointer to plane 0, row 0
  *   planes       independent rings (e.g. B*H), >= 1
@@ -272,8 +308,8 @@ int rxl_last_launch_count(void);
  * word instead of hanging, drains its in-flight copies, frees its tensor
  * memory and exits with its outputs undefined. This call synchronises the
  * current device, returns the recorded bits (bit 0: forward kernel, bit 1:
- * backward kernels, bit 2: projection kernel) and clears them; -1 if the
- * device could not be read.
+ * backward kernels, bit 2: projection kernel, bit 3: dense-layer kernel) and
+ * clears them; -1 if the device could not be read.
  */
 int rxl_device_error_flags(void);
 

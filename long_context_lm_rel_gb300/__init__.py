@@ -36,6 +36,17 @@ class rxl_ring(ctypes.Structure):
                 ("head", ctypes.c_int), ("len", ctypes.c_int)]
 
 
+class rxl_layer_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "w_q", "w_k", "w_v", "w_o", "r", "u", "vbias", "ln1_gamma", "ln1_beta",
+        "w_1", "b_1", "w_2", "b_2", "ln2_gamma", "ln2_beta")]
+
+
+def make_layer_weights(**tensors) -> rxl_layer_weights:
+    """rxl_layer_weights from tensors (or addresses) named as its fields."""
+    return rxl_layer_weights(**{k: _ptr(v) for k, v in tensors.items()})
+
+
 class RxlError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -82,6 +93,11 @@ def lib():
             L.rxl_attn_bwd_reset.restype = ctypes.c_int
             L.rxl_qkv_proj.argtypes = [P(rxl_attn_desc), ctypes.c_int] + [vp] * 8 + [vp]
             L.rxl_qkv_proj.restype = ctypes.c_int
+            L.rxl_layer_fwd_workspace_bytes.argtypes = [P(rxl_attn_desc), ctypes.c_int, ctypes.c_int]
+            L.rxl_layer_fwd_workspace_bytes.restype = ctypes.c_size_t
+            L.rxl_layer_fwd.argtypes = [P(rxl_attn_desc), ctypes.c_int, ctypes.c_int, P(rxl_layer_weights)] \
+                + [vp] * 4 + [ctypes.c_size_t, vp]
+            L.rxl_layer_fwd.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc.argtypes = [P(rxl_attn_desc)] + [vp] * 15 + [vp]
             L.rxl_attn_bwd_noalloc.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc_max_scratch_bytes.argtypes = []
@@ -152,6 +168,17 @@ def rxl_qkv_proj(desc, d_model, h_mem, h_cur, w_q, w_k, w_v, q, k, v, stream=Non
     _check(lib().rxl_qkv_proj(ctypes.byref(desc), int(d_model),
                               *map(_ptr, (h_mem, h_cur, w_q, w_k, w_v, q, k, v)), _stream(stream)),
            "rxl_qkv_proj")
+
+
+def rxl_layer_fwd_workspace_bytes(desc, d_model, d_ff) -> int:
+    return int(lib().rxl_layer_fwd_workspace_bytes(ctypes.byref(desc), int(d_model), int(d_ff)))
+
+
+def rxl_layer_fwd(desc, d_model, d_ff, weights, h_mem, h_in, h_out, workspace, workspace_bytes,
+                  stream=None):
+    _check(lib().rxl_layer_fwd(ctypes.byref(desc), int(d_model), int(d_ff), ctypes.byref(weights),
+                               *map(_ptr, (h_mem, h_in, h_out, workspace)), int(workspace_bytes),
+                               _stream(stream)), "rxl_layer_fwd")
 
 
 def rxl_attn_bwd_workspace_bytes(desc) -> int:

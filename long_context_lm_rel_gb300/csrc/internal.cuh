@@ -79,4 +79,13 @@ cudaError_t launch_tc_proj(const AttnShape &s, int d, const void *h_mem, const v
                            cudaStream_t st, int *launches);
 cudaError_t tc_proj_read_error(int *flag);
 
+// Dense layer out = act(A . W + bias) + residual over B groups of R rows
+// (bf16); A is [B, R, K] or, with a_heads, the attention output [B, K/64, R, 64].
+cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_heads, const void *w,
+                           const void *bias, const void *residual, bool relu, void *out,
+                           cudaStream_t st, int *launches);
+cudaError_t launch_layernorm(const void *x, const void *gamma, const void *beta, void *y, long long rows,
+                             int d, float eps, cudaStream_t st, int *launches);
+cudaError_t tc_gemm_read_error(int *flag);
+
 }  // namespace rxl

@@ -72,11 +72,89 @@ int rxl_last_cuda_error(void) { return g_last_cuda_error; }
 int rxl_last_launch_count(void) { return g_last_launches; }
 
 int rxl_device_error_flags(void) {
-  int fwd = 0, bwd = 0, proj = 0;
+  int fwd = 0, bwd = 0, proj = 0, gemm = 0;
   if (rxl::tc_fwd_read_error(&fwd) != cudaSuccess || rxl::tc_bwd_read_error(&bwd) != cudaSuccess ||
-      rxl::tc_proj_read_error(&proj) != cudaSuccess)
+      rxl::tc_proj_read_error(&proj) != cudaSuccess || rxl::tc_gemm_read_error(&gemm) != cudaSuccess)
     return -1;
-  return (fwd ? 1 : 0) | (bwd ? 2 : 0) | (proj ? 4 : 0);
+  return (fwd ? 1 : 0) | (bwd ? 2 : 0) | (proj ? 4 : 0) | (gemm ? 8 : 0);
+}
+
+namespace {
+struct LayerWs {
+  size_t q, k, v, o, lse, x1, x1n, z, x2, total;
+};
+size_t up256_(size_t x) { return (x + 255) & ~(size_t)255; }
+LayerWs layer_ws(const rxl::AttnShape &s, int d, int dff) {
+  const size_t rows = (size_t)s.B * s.L, bh = (size_t)s.B * s.H;
+  LayerWs w;
+  w.q = 0;
+  w.k = w.q + up256_(bh * s.L * 64 * 2);
+  w.v = w.k + up256_(bh * s.kv_rows * 64 * 2);
+  w.o = w.v + up256_(bh * s.kv_rows * 64 * 2);
+  w.lse = w.o + up256_(bh * s.L * 64 * 2);
+  w.x1 = w.lse + up256_(bh * s.L * 4);
+  w.x1n = w.x1 + up256_(rows * d * 2);
+  w.z = w.x1n + up256_(rows * d * 2);
+  w.x2 = w.z + up256_(rows * dff * 2);
+  w.total = w.x2 + up256_(rows * d * 2);
+  return w;
+}
+rxl_status check_layer(const rxl_attn_desc *desc, int d, int dff, rxl::AttnShape *s) {
+  rxl_status st = check_desc(desc, s);
+  if (st != RXL_OK) return st;
+  if (desc->dtype != RXL_DTYPE_BF16) return RXL_ERR_UNSUPPORTED;
+  if (d < 256 || d % 256 != 0 || d > (1 << 16) || dff < 64 || dff % 64 != 0 || dff > (1 << 17))
+    return RXL_ERR_UNSUPPORTED;
+  return RXL_OK;
+}
+}  // namespace
+
+size_t rxl_layer_fwd_workspace_bytes(const rxl_attn_desc *desc, int d_model, int d_ff) {
+  rxl::AttnShape s;
+  if (check_layer(desc, d_model, d_ff, &s) != RXL_OK) return 0;
+  return layer_ws(s, d_model, d_ff).total;
+}
+
+rxl_status rxl_layer_fwd(const rxl_attn_desc *desc, int d_model, int d_ff, const rxl_layer_weights *w,
+                         const void *h_mem, const void *h_in, void *h_out, void *workspace,
+                         size_t workspace_bytes, rxl_stream_t stream) {
+  rxl::AttnShape s;
+  rxl_status st = check_layer(desc, d_model, d_ff, &s);
+  if (st != RXL_OK) return st;
+  if (!w) return RXL_ERR_INVALID_ARGUMENT;
+  if ((st = check_ptrs({w->w_q, w->w_k, w->w_v, w->w_o, w->r, w->u, w->vbias, w->ln1_gamma,
+                        w->ln1_beta, w->w_1, w->b_1, w->w_2, w->b_2, w->ln2_gamma, w->ln2_beta,
+                        h_in, h_out, workspace})) != RXL_OK)
+    return st;
+  if (s.cap > 0 && (st = check_ptrs({h_mem})) != RXL_OK) return st;
+  const LayerWs lw = layer_ws(s, d_model, d_ff);
+  if (workspace_bytes < lw.total) return RXL_ERR_WORKSPACE_TOO_SMALL;
+  char *ws = (char *)workspace;
+  void *q = ws + lw.q, *k = ws + lw.k, *v = ws + lw.v, *o = ws + lw.o;
+  float *lse = (float *)(ws + lw.lse);
+  void *x1 = ws + lw.x1, *x1n = ws + lw.x1n, *z = ws + lw.z, *x2 = ws + lw.x2;
+  cudaStream_t cs = (cudaStream_t)stream;
+  const long long rows = (long long)s.B * s.L;
+  int launches = 0;
+  cudaError_t e = rxl::launch_tc_proj(s, d_model, h_mem, h_in, w->w_q, w->w_k, w->w_v, q, k, v, cs,
+                                      &launches);
+  if (e == cudaSuccess)
+    e = rxl::launch_tc_fwd(s, q, k, v, w->r, w->u, w->vbias, o, nullptr, lse, cs, &launches);
+  if (e == cudaSuccess)  // x1 = h + attention . W_O (heads merged by the A operand's layout)
+    e = rxl::launch_tc_gemm(s.B, s.L, s.H * 64, d_model, o, true, w->w_o, nullptr, h_in, false, x1,
+                            cs, &launches);
+  if (e == cudaSuccess)
+    e = rxl::launch_layernorm(x1, w->ln1_gamma, w->ln1_beta, x1n, rows, d_model, 1e-5f, cs, &launches);
+  if (e == cudaSuccess)  // z = ReLU(x1n . W_1 + b_1)
+    e = rxl::launch_tc_gemm(s.B, s.L, d_model, d_ff, x1n, false, w->w_1, w->b_1, nullptr, true, z, cs,
+                            &launches);
+  if (e == cudaSuccess)  // x2 = x1n + z . W_2 + b_2
+    e = rxl::launch_tc_gemm(s.B, s.L, d_ff, d_model, z, false, w->w_2, w->b_2, x1n, false, x2, cs,
+                            &launches);
+  if (e == cudaSuccess)
+    e = rxl::launch_layernorm(x2, w->ln2_gamma, w->ln2_beta, h_out, rows, d_model, 1e-5f, cs, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
 }
 
 rxl_status rxl_qkv_proj(const rxl_attn_desc *desc, int d_model, const void *h_mem,
