@@ -244,21 +244,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return r;
 }
 
-// In place: 8 bf16 of a 16-byte shared-memory chunk become 8 fp16.
-__device__ __forceinline__ void chunk_bf16_to_f16(uint32_t addr) {
-  uint32_t a, b, c, d;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-               : "r"(addr));
-  auto cv = [](uint32_t x) {
-    const float lo = __uint_as_float(x << 16), hi = __uint_as_float(x & 0xFFFF0000u);
-    return pack_f16(lo, hi);
-  };
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(cv(a)), "r"(cv(b)),
-               "r"(cv(c)), "r"(cv(d))
-               : "memory");
-}
-
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

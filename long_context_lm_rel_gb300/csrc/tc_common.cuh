@@ -79,49 +79,7 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
-// Scaled logits (log2 domain) of one 128x128 tile for the calling thread's
-// query row ii = 32*warp + lane, key jj = 0..127:
-//   y[jj] = (S[ii][jj] + G[ii][ii - jj + 127]) * scale_log2, -inf if masked.
-// S sits at TMEM columns s_col.., the 256-column band G at g_col.. of the
-// warp's lane quadrant `trow`. Warp-collective (TMEM loads).
-__device__ __forceinline__ void tile_logits(uint32_t trow, uint32_t s_col, uint32_t g_col,
-                                            int warp, int lane, int i, const KeyTile &x,
-                                            float scale_log2, float (&y)[BK]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t sr[32], w0[32], w1[32];
-    tmem_ld32(trow + s_col + 32 * c, sr);
-    const uint32_t gcol = g_col + 32 * warp + 96 - 32 * c;
-    tmem_ld32(trow + gcol, w0);
-    tmem_ld32(trow + gcol + 32, w1);
-    tmem_wait_ld();
-    float win[64];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      win[e] = __uint_as_float(w0[e]);
-      win[32 + e] = __uint_as_float(w1[e]);
-    }
-    // win[x] <- win[x + lane] (5 predicated stages; fixed trip counts keep
-    // the array in registers)
-#pragma unroll
-    for (int b = 4; b >= 0; --b) {
-      const int sh = 1 << b;
-      const bool take = (lane >> b) & 1;
-#pragma unroll
-      for (int e = 0; e < 63; ++e)
-        if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
-    }
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int jj = 32 * c + k;
-      const float a = __uint_as_float(sr[k]) + win[31 - k];
-      const bool valid = jj < x.nvalid && x.jlog0 + jj <= i;
-      y[jj] = valid ? a * scale_log2 : -INFINITY;
-    }
-  }
-}
-
-// Half-tile variant for two warps per TMEM lane quadrant: the calling thread
+// Logits of half a 128x128 tile for two warps per TMEM lane quadrant: the calling thread
 // (quadrant `quad`, half `hf`) produces the logits of keys jj = 64*hf + k,
 // k = 0..63, of its row ii = 32*quad + lane: y[k] = (S + G_skewed) * scale,
 // -inf where masked. kScaled = false skips the multiply (operands prescaled).
@@ -161,13 +119,6 @@ __device__ __forceinline__ void half_tile_logits(uint32_t trow, uint32_t s_col, 
       y[32 * cc + k] = k <= lim ? a : -INFINITY;
     }
   }
-}
-
-// Vector float atomic add (sm_90+): 4 consecutive floats, 16-byte aligned.
-__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
 }
 
 }  // namespace tc
