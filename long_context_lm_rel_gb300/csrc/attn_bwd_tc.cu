@@ -404,15 +404,27 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const int i = i0 + ii;
       const bool row_ok = i < p.L;
       const size_t row = (size_t)it.bh * p.L + (row_ok ? i : 0);
-      const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.f;
+      // rows past L: lse = +inf makes P = 0 without a select per key
+      const float lse2 = row_ok ? p.lse[row] * kLog2e : INFINITY;
       const float Di = row_ok ? p.delta[row] : 0.f;
       ok = mbar_wait(bar_sg, g & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
+      if (c.n == 0 && ii >= it.x.nvalid) {
+        // rows of K and V past the run hold another run's (or junk) data:
+        // zero them so that 0 * junk cannot leak into dP or dQc (the
+        // logits of those keys are masked, the S products of later pairs
+        // then read zeros)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          st_shared_v4(sb + F_K + sw128_offset(ii, 4 * hf + cc), 0, 0, 0, 0);
+          st_shared_v4(sb + F_V + sw128_offset(ii, 4 * hf + cc), 0, 0, 0, 0);
+        }
+      }
       float y[64];
       half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, y);
 #pragma unroll
-      for (int k = 0; k < 64; ++k) y[k] = row_ok ? ex2(y[k] - lse2) : 0.f;  // P
+      for (int k = 0; k < 64; ++k) y[k] = ex2(y[k] - lse2);  // P
       // the P/dA and dG buffers held the previous pair's staging
       if (g > 0) {
         ok = mbar_wait(bar_sfree, (g - 1) & 1, abort_flag);
@@ -431,10 +443,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         tmem_ld32(trow + TM_S + 64 * hf + 32 * cc, dp);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float pv = y[32 * cc + k];
-          y[32 * cc + k] = pv != 0.f ? p.scale * pv * (__uint_as_float(dp[k]) - Di) : 0.f;  // dA
-        }
+        for (int k = 0; k < 32; ++k)  // dA (P = 0 and finite dP off the allowed pairs)
+          y[32 * cc + k] = p.scale * y[32 * cc + k] * (__uint_as_float(dp[k]) - Di);
       }
       // P is no longer read: dP and dV were committed together
       store_half_bf16(sb + F_PA, ii, hf, y);
@@ -458,18 +468,26 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const float sig = am > 0.f ? exp2f(14.f - ceilf(log2f(am))) : 1.f;  // max |sig dA| <= 2^14
       // Sheared dG row ii: key jj sits at column ii + 127 - jj. This half's
       // keys fill columns s .. s+63 (s = ii + 64 - 64 hf) in reverse key
-      // order; z = those values shifted right by s mod 8 = ii mod 8 lines
-      // them up with 16-byte chunks (s >> 3) .. (s >> 3) + 8.
+      // order; shifted right by s mod 8 = ii mod 8 elements they line up
+      // with 16-byte chunks (s >> 3) .. (s >> 3) + 8. w holds them as fp16
+      // pairs (element x in half x & 1 of word x >> 1).
       {
         const int r = ii & 7;
-        float z[72];
+        uint32_t w[36];
 #pragma unroll
-        for (int x = 0; x < 72; ++x) z[x] = x < 64 ? sig * y[63 - (x < 64 ? x : 0)] : 0.f;
+        for (int m = 0; m < 32; ++m) w[m] = pack_f16(sig * y[63 - 2 * m], sig * y[62 - 2 * m]);
 #pragma unroll
-        for (int b = 4; b >= 1; b >>= 1) {
-          const bool take = (r & b) != 0;
+        for (int m = 32; m < 36; ++m) w[m] = 0u;
+        // odd part of the shift: element x <- x - 1 by a byte permute of
+        // neighbouring words; then whole words by 2 and 1
+        const uint32_t sel = (r & 1) ? 0x5432u : 0x7654u;
 #pragma unroll
-          for (int x = 71; x >= 0; --x) z[x] = take ? (x >= b ? z[x >= b ? x - b : 0] : 0.f) : z[x];
+        for (int m = 35; m >= 0; --m) w[m] = __byte_perm(m > 0 ? w[m > 0 ? m - 1 : 0] : 0u, w[m], sel);
+#pragma unroll
+        for (int b = 2; b >= 1; b >>= 1) {
+          const bool take = ((r >> 1) & b) != 0;
+#pragma unroll
+          for (int m = 35; m >= 0; --m) w[m] = take ? (m >= b ? w[m >= b ? m - b : 0] : 0u) : w[m];
         }
         const int cbase = c0 + (hf ? 0 : 8);
         const uint32_t xrow = sb + F_X + ii * 16;
@@ -483,22 +501,19 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         if (hf == 1) {
           // chunk cbase + 8 is shared with the other half: hand it over
-          st_shared_v4(xrow, pack_f16(z[64], z[65]), pack_f16(z[66], z[67]), pack_f16(z[68], z[69]),
-                       pack_f16(z[70], z[71]));
+          st_shared_v4(xrow, w[32], w[33], w[34], w[35]);
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
             const int C = cbase + t;
-            st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7),
-                         pack_f16(z[8 * t + 0], z[8 * t + 1]), pack_f16(z[8 * t + 2], z[8 * t + 3]),
-                         pack_f16(z[8 * t + 4], z[8 * t + 5]), pack_f16(z[8 * t + 6], z[8 * t + 7]));
+            st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), w[4 * t],
+                         w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
           }
         } else {
 #pragma unroll
           for (int t = 1; t < 9; ++t) {
             const int C = cbase + t;
-            st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7),
-                         pack_f16(z[8 * t + 0], z[8 * t + 1]), pack_f16(z[8 * t + 2], z[8 * t + 3]),
-                         pack_f16(z[8 * t + 4], z[8 * t + 5]), pack_f16(z[8 * t + 6], z[8 * t + 7]));
+            st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), w[4 * t],
+                         w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
           }
         }
         if (!(ok = pair_sync(bar_x, lane, xphase, abort_flag))) break;
@@ -511,8 +526,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                        : "r"(xrow));
           const int C = cbase;
           st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7),
-                       a | pack_f16(z[0], z[1]), b | pack_f16(z[2], z[3]), cc | pack_f16(z[4], z[5]),
-                       d | pack_f16(z[6], z[7]));
+                       a | w[0], b | w[1], cc | w[2], d | w[3]);
         }
       }
       fence_proxy_async_smem();

@@ -110,13 +110,23 @@ __device__ __forceinline__ void half_tile_logits(uint32_t trow, uint32_t s_col, 
       for (int e = 0; e < 63; ++e)
         if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
     }
-    // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i
+    // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i; the
+    // warp skips the mask where all 32 keys are visible to all its rows
     const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
+    if (__all_sync(0xffffffffu, lim >= 31)) {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      float a = __uint_as_float(sr[k]) + win[31 - k];
-      if (kScaled) a *= scale;
-      y[32 * cc + k] = k <= lim ? a : -INFINITY;
+      for (int k = 0; k < 32; ++k) {
+        float a = __uint_as_float(sr[k]) + win[31 - k];
+        if (kScaled) a *= scale;
+        y[32 * cc + k] = a;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        float a = __uint_as_float(sr[k]) + win[31 - k];
+        if (kScaled) a *= scale;
+        y[32 * cc + k] = k <= lim ? a : -INFINITY;
+      }
     }
   }
 }

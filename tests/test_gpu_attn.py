@@ -34,10 +34,11 @@ def make_inputs(B, H, L, cap, m, dtype, seed=0, tid0=900000, D_model=1024):
         r=gen.round_to(gen.rel_table(cap + L, D_model, H, dh, seed, tid0 + 9), dtype))
 
 
-def run_gpu(x, cap, m, head, dtype, bwd=True, scale=0.125, ex=False):
-    """ex=True runs the training pair (forward keeps the low part of O)."""
-    k_phys = place_kv(x["k_mem"], x["k_cur"], cap, head, fill=7.0)   # junk in unused ring rows
-    v_phys = place_kv(x["v_mem"], x["v_cur"], cap, head, fill=-7.0)
+def run_gpu(x, cap, m, head, dtype, bwd=True, scale=0.125, ex=False, fill=(7.0, -7.0)):
+    """ex=True runs the training pair (forward keeps the low part of O);
+    `fill` is the junk written to the K and V ring rows that hold no memory."""
+    k_phys = place_kv(x["k_mem"], x["k_cur"], cap, head, fill=fill[0])
+    v_phys = place_kv(x["v_mem"], x["v_cur"], cap, head, fill=fill[1])
     c = AttnCall(x["q"], k_phys, v_phys, x["r"], x["u"], x["vb"], cap=cap, m=m, head=head,
                  dtype=dtype, scale=scale)
     c.fwd_ex() if ex else c.fwd()
@@ -93,6 +94,17 @@ SMALL = [  # B, H, L, cap, m, head
 def test_small_bf16_full_parity(B, H, L, cap, m, head, ex):
     x = make_inputs(B, H, L, cap, m, "bf16", seed=B * 1000 + L + m)
     c = run_gpu(x, cap, m, head, "bf16", ex=ex)
+    compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head, ex)))
+
+
+@pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
+@pytest.mark.parametrize("B,H,L,cap,m,head", [(2, 2, 200, 300, 250, 123), (2, 2, 128, 256, 0, 0),
+                                              (1, 2, 130, 200, 70, 190)])
+def test_nan_in_ring_rows_without_memory_does_not_leak(B, H, L, cap, m, head, ex):
+    # ring rows past the memory are never read as keys: whatever they hold
+    # (here NaN) must not reach O or any gradient, even through a 0 weight
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=77 + m)
+    c = run_gpu(x, cap, m, head, "bf16", ex=ex, fill=(float("nan"), float("nan")))
     compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head, ex)))
 
 
