@@ -454,7 +454,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       // CTA-wide max |dA| of this pair -> power-of-two fp16 scale of dG
       float am = 0.f;
 #pragma unroll
-      for (int k = 0; k < 64; ++k) am = fmaxf(am, fabsf(y[k]));
+      for (int k = 0; k < 64; k += 2) am = fmax3(am, fabsf(y[k]), fabsf(y[k + 1]));
       am = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(am)));
       if (lane == 0) {
         wmax[(g & 1) * 8 + warp] = am;

@@ -50,6 +50,7 @@ using tc::NB;
 using tc::KeyTile;
 using tc::KeyTiles;
 using tc::RowMemory;
+using tc::lane_shift_window;
 using tc::row_memory;
 
 constexpr int kSoftmaxWarps = 8;
@@ -411,26 +412,24 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           win[e] = __uint_as_float(w0[e]);
           win[32 + e] = __uint_as_float(w1[e]);
         }
-        // win[x] <- win[x + lane] (5 predicated stages)
-#pragma unroll
-        for (int b = 4; b >= 0; --b) {
-          const int sh = 1 << b;
-          const bool take = (lane >> b) & 1;
-#pragma unroll
-          for (int e = 0; e < 63; ++e)
-            if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
-        }
-        // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i
+        lane_shift_window(win, lane);  // win[x] <- win[x + lane]
+        // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i;
+        // the warp skips the mask where all 32 keys are visible to all its rows
         const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
+        if (__all_sync(0xffffffffu, lim >= 31)) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float a = __uint_as_float(sr[k]) + win[31 - k];
-          y[32 * cc + k] = k <= lim ? a : -INFINITY;
+          for (int k = 0; k < 32; ++k) y[32 * cc + k] = __uint_as_float(sr[k]) + win[31 - k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float a = __uint_as_float(sr[k]) + win[31 - k];
+            y[32 * cc + k] = k <= lim ? a : -INFINITY;
+          }
         }
       }
       float mt = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 64; ++k) mt = fmaxf(mt, y[k]);
+      for (int k = 0; k < 64; k += 2) mt = fmax3(mt, y[k], y[k + 1]);
       float other;
       if (!(ok = pair_exchange(mt, &other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
       // the exponent reference only moves when the row max outgrows it by 2^8

@@ -79,6 +79,20 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
+// win[x] <- win[x + lane] for x = 0..31: a 63-value window shifted left by
+// the lane index in 5 predicated stages, largest shift first (selects; the
+// same stages as t*a + (1-t)*b on the FMA pipe measured slower).
+__device__ __forceinline__ void lane_shift_window(float (&win)[64], int lane) {
+#pragma unroll
+  for (int b = 4; b >= 0; --b) {
+    const int sh = 1 << b;
+    const bool take = (lane >> b) & 1;
+#pragma unroll
+    for (int e = 0; e < 63; ++e)
+      if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
+  }
+}
+
 // Logits of half a 128x128 tile for two warps per TMEM lane quadrant: the calling thread
 // (quadrant `quad`, half `hf`) produces the logits of keys jj = 64*hf + k,
 // k = 0..63, of its row ii = 32*quad + lane: y[k] = (S + G_skewed) * scale,
@@ -102,14 +116,7 @@ __device__ __forceinline__ void half_tile_logits(uint32_t trow, uint32_t s_col, 
       win[e] = __uint_as_float(w0[e]);
       win[32 + e] = __uint_as_float(w1[e]);
     }
-#pragma unroll
-    for (int b = 4; b >= 0; --b) {
-      const int sh = 1 << b;
-      const bool take = (lane >> b) & 1;
-#pragma unroll
-      for (int e = 0; e < 63; ++e)
-        if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
-    }
+    lane_shift_window(win, lane);
     // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i; the
     // warp skips the mask where all 32 keys are visible to all its rows
     const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
