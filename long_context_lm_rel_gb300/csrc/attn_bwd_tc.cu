@@ -194,7 +194,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const uint32_t bar_dp = b0 + 32, bar_ds = b0 + 40, bar_fin = b0 + 48, bar_fl = b0 + 56;
   const uint32_t bar_acc = b0 + 64, bar_red = b0 + 72, bar_drain = b0 + 80, bar_x0 = b0 + 88;
   const uint32_t bar_staged = b0 + 120;  // each softmax warp staged its rows of a pair (8)
-  const uint32_t bar_sfree = b0 + 128;   // the staging of a pair has been read (1)
+  const uint32_t bar_sfree = b0 + 128;   // the dQ staging of a pair has been read (1)
+  const uint32_t bar_gfree = b0 + 240;   // the dR staging of a pair has been read (1)
   const uint32_t bar_da = b0 + 136;      // softmax warps (256): dA written
   const uint32_t bar_f0 = b0 + 144;      // dK and dQc done (commit)
   const uint32_t bar_do = b0 + 152, bar_qu = b0 + 160;  // TMA: dO, (Q+u) of a pair
@@ -210,6 +211,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     mbar_init(bar_staged, kSoftmaxWarps);
     mbar_init(bar_sfree, 1);
+    mbar_init(bar_gfree, 1);
     mbar_init(bar_da, kSoftmaxWarps * 32);
     mbar_init(bar_f0, 1);
     mbar_init(bar_do, 1);
@@ -363,22 +365,32 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (!(ok = mbar_wait(bar_staged, g & 1, abort_flag))) break;
         const int i0 = c.i0();
         const int d0 = kDrPad + i0 - c.it.x.jlog0 - (BK - 1);  // >= 1
+        // warp (quad, hf) staged its dQ box in the P/dA buffer and its dR
+        // block-hf rows in dG atoms 2hf, 2hf+1. The dQ boxes go first, in a
+        // bulk group of their own: the next pair's P needs that buffer
+        // soon, its dG not before the dA of that pair.
 #pragma unroll 1
         for (int w = 0; w < kSoftmaxWarps; ++w) {
-          // warp (quad, hf) staged its dQ box in the P/dA buffer and its dR
-          // block-hf rows in dG atoms 2hf, 2hf+1
           const int quad = w & 3, hf = w >> 2;
-          const int qrow = i0 + 32 * quad, drow = d0 + 128 * hf + 32 * quad;
+          const int qrow = i0 + 32 * quad;
           if (qrow < p.L)
             tma_reduce_add_3d(&tm_dq, 32 * hf, qrow, c.it.bh, sb + F_PA + hf * 16384 + quad * 4096);
+        }
+        bulk_commit();
+#pragma unroll 1
+        for (int w = 0; w < kSoftmaxWarps; ++w) {
+          const int quad = w & 3, hf = w >> 2;
+          const int drow = d0 + 128 * hf + 32 * quad;
           if (drow < kDrPad + p.kv_rows) {
             tma_reduce_add_3d(&tm_dr, 0, drow, c.it.h, sb + F_DG + 2 * hf * 16384 + quad * 4096);
             tma_reduce_add_3d(&tm_dr, 32, drow, c.it.h, sb + F_DG + (2 * hf + 1) * 16384 + quad * 4096);
           }
         }
         bulk_commit();
-        bulk_wait_read();
+        bulk_wait_read_but_latest();
         mbar_arrive(bar_sfree);
+        bulk_wait_read();
+        mbar_arrive(bar_gfree);
         c.next(p);
       }
       // the reductions must be complete before shared memory goes away
@@ -425,7 +437,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, y);
 #pragma unroll
       for (int k = 0; k < 64; ++k) y[k] = ex2(y[k] - lse2);  // P
-      // the P/dA and dG buffers held the previous pair's staging
+      // the P/dA buffer held the previous pair's dQ staging
       if (g > 0) {
         ok = mbar_wait(bar_sfree, (g - 1) & 1, abort_flag);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
@@ -466,6 +478,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
       for (int w = 0; w < kSoftmaxWarps; ++w) am = fmaxf(am, wmax[(g & 1) * 8 + w]);
       const float sig = am > 0.f ? exp2f(14.f - ceilf(log2f(am))) : 1.f;  // max |sig dA| <= 2^14
+      // the dG buffer held the previous pair's dR staging
+      if (g > 0) {
+        ok = mbar_wait(bar_gfree, (g - 1) & 1, abort_flag);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      }
       // Sheared dG row ii: key jj sits at column ii + 127 - jj. This half's
       // keys fill columns s .. s+63 (s = ii + 64 - 64 hf) in reverse key
       // order; shifted right by s mod 8 = ii mod 8 elements they line up
