@@ -385,8 +385,6 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       const int s = g & 1;
       ok = mbar_wait(bar_sg, g & 1, abort_flag) &&
            mbar_wait(s ? bar_full1 : bar_full0, (g >> 1) & 1, abort_flag);
-      // P buffer and O: P.V(g-1) must be done
-      if (ok && g > 0) ok = mbar_wait(bar_pv, (g - 1) & 1, abort_flag);
       // tcgen05.ld/st below are warp-collective: keep every decision warp-uniform
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
@@ -448,6 +446,13 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       }
       l_run = l_run * alpha + sum;
       m_run = m_new;
+      // the P buffer and O: P.V(g-1), which ran while this tile's logits
+      // were formed, must be done
+      if (g > 0) {
+        ok = mbar_wait(bar_pv, (g - 1) & 1, abort_flag);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        tc_fence_after();
+      }
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         st_shared_v4(sbase + SM_P + hf * 16384 + sw128_offset(ii, c), pk[4 * c], pk[4 * c + 1],
