@@ -304,7 +304,7 @@ def run_ours(args, rank, world):
                    "flop_per_step": flop_step, "l2": "flushed between steps (256 MiB write, outside events)",
                    "parallelism": f"{world} independent replicas (one per GPU)"},
         "roofline": {"bound": "tensor",
-                     "kernel": "rxl_attn_bwd_ex call (5 launches; rxl_bwd_main_kernel is 88 % of it)",
+                     "kernel": "rxl_attn_bwd_ex call (3 launches; rxl_bwd_main_kernel is most of it)",
                      "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
                      "traffic": TRAFFIC_BWD_MAIN if B == 16 else None,
                      "traffic_note": "rxl_bwd_main_kernel dram read+write per launch: ncu capture at "

@@ -32,7 +32,9 @@
 //            two chosen per pair from max |dA|: R rows are several times
 //            larger than K rows, and bf16 rounding of dA in that term alone
 //            can exceed 1% of max|dQ| on short contexts.
-//   finish : dQ -> bf16 with per-head column sums; then dR copied out, du, dv
+//   finish : dQ -> bf16 with per-head column sums, dR copied out; the last
+//            block forms du and dv
+// (zero and prep share one launch when the forward kept the low part of O)
 #include <math.h>
 
 #include <mutex>
@@ -653,49 +655,64 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
 // ---------------------------------------------------------- small kernels
 
-// The dR and dQ accumulators and the du/dv sums <- 0; dK/dV rows of ring
-// slots that hold no valid memory <- 0; R16 <- fp16(R) (satfinite).
-__global__ void bwd_zero_kernel(float *dr, size_t n_dr, float *dq_acc, size_t n_dq, float *sums,
-                                int n_sums, __nv_bfloat16 *dk, __nv_bfloat16 *dv, int BH, int H,
-                                int cap, int m, int head, int kv_rows, const __nv_bfloat16 *r,
-                                __half *r16, size_t n_r, const int *mvis) {
-  const size_t tid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
+// The dR and dQ accumulators and the du/dv sums (with the finish kernel's
+// block counter) <- 0; dK/dV rows of ring slots that hold no valid memory
+// <- 0; R16 <- fp16(R) (satfinite).
+struct ZeroArgs {
+  float *dr;
+  size_t n_dr;
+  float *dq_acc;
+  size_t n_dq;
+  float *sums;
+  int n_sums;
+  __nv_bfloat16 *dk, *dv;
+  int BH, H, cap, m, head, kv_rows;
+  const __nv_bfloat16 *r;
+  __half *r16;
+  size_t n_r;
+  const int *mvis;
+};
+
+__device__ void zero_work(const ZeroArgs &z, size_t tid, size_t stride) {
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (size_t e = tid; e < n_dr / 4; e += stride) ((float4 *)dr)[e] = z4;
-  for (size_t e = tid; e < n_dq / 4; e += stride) ((float4 *)dq_acc)[e] = z4;
-  for (size_t e = tid; e < (size_t)n_sums; e += stride) sums[e] = 0.f;
-  for (size_t e = tid; e < n_r / 8; e += stride) {
-    const uint4 a = ((const uint4 *)r)[e];
+  for (size_t e = tid; e < z.n_dr / 4; e += stride) ((float4 *)z.dr)[e] = z4;
+  for (size_t e = tid; e < z.n_dq / 4; e += stride) ((float4 *)z.dq_acc)[e] = z4;
+  for (size_t e = tid; e < (size_t)z.n_sums; e += stride) z.sums[e] = 0.f;
+  for (size_t e = tid; e < z.n_r / 8; e += stride) {
+    const uint4 a = ((const uint4 *)z.r)[e];
     const uint32_t w[4] = {a.x, a.y, a.z, a.w};
     uint32_t o[4];
 #pragma unroll
     for (int f = 0; f < 4; ++f)
       o[f] = pack_f16(__uint_as_float(w[f] << 16), __uint_as_float(w[f] & 0xFFFF0000u));
-    ((uint4 *)r16)[e] = make_uint4(o[0], o[1], o[2], o[3]);
+    ((uint4 *)z.r16)[e] = make_uint4(o[0], o[1], o[2], o[3]);
   }
   // ring slots whose rows the row does not see: logical slots t < m - mb
   // (masked by a document reset) and t >= m (no valid memory); 8 x 16 B per row
-  const size_t n_rows = (size_t)BH * cap * 8;
+  const size_t n_rows = (size_t)z.BH * z.cap * 8;
   for (size_t e = tid; e < n_rows; e += stride) {
     const int c = (int)(e & 7);
     const size_t rr = e >> 3;
-    const int bh = (int)(rr / cap), t = (int)(rr % cap);
-    const int mb = row_memory(mvis, bh / H, m, cap, head).m;
-    if (t >= m - mb && t < m) continue;
-    int pr = head + t;
-    if (pr >= cap) pr -= cap;
-    const size_t off = ((size_t)bh * kv_rows + pr) * DH;
-    ((uint4 *)(dk + off))[c] = make_uint4(0, 0, 0, 0);
-    ((uint4 *)(dv + off))[c] = make_uint4(0, 0, 0, 0);
+    const int bh = (int)(rr / z.cap), t = (int)(rr % z.cap);
+    const int mb = row_memory(z.mvis, bh / z.H, z.m, z.cap, z.head).m;
+    if (t >= z.m - mb && t < z.m) continue;
+    int pr = z.head + t;
+    if (pr >= z.cap) pr -= z.cap;
+    const size_t off = ((size_t)bh * z.kv_rows + pr) * DH;
+    ((uint4 *)(z.dk + off))[c] = make_uint4(0, 0, 0, 0);
+    ((uint4 *)(z.dv + off))[c] = make_uint4(0, 0, 0, 0);
   }
 }
 
+__global__ void bwd_zero_kernel(const ZeroArgs z) {
+  zero_work(z, blockIdx.x * (size_t)blockDim.x + threadIdx.x, (size_t)gridDim.x * blockDim.x);
+}
+
 // Streaming preparation when the forward kept the low part of O: per row,
-// (Q+u) in bf16, (Q+v) in fp16 and D_i = dO_i . (o_i + o_lo_i). Eight
-// threads per row, 16 bytes each.
+// (Q+u) in bf16, (Q+v) in fp16 and D_i = dO_i . (o_i + o_lo_i), eight
+// threads per row, 16 bytes each; then the zeroing above, in the same launch.
 __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
-    long long rows, int L, int H, const __nv_bfloat16 *__restrict__ q,
+    const ZeroArgs z, long long rows, int L, int H, const __nv_bfloat16 *__restrict__ q,
     const __nv_bfloat16 *__restrict__ u, const __nv_bfloat16 *__restrict__ vb,
     const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ o_lo,
     const __nv_bfloat16 *__restrict__ dout, __nv_bfloat16 *__restrict__ qu,
@@ -730,16 +747,21 @@ __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
     for (int w = 4; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
     if (sub == 0) delta[row] = acc;
   }
+  zero_work(z, blockIdx.x * (size_t)blockDim.x + threadIdx.x, (size_t)gridDim.x * blockDim.x);
 }
 
 // dq = bf16(dQ accumulator); per-head column sums of dQ into colsum[H][64].
 // Block (bh, chunk) covers 128 rows of one (b, h) plane: 8 threads per row,
-// 8 columns each.
-__global__ void __launch_bounds__(256) bwd_dq_finish_kernel(const float *__restrict__ dq_acc,
-                                                            __nv_bfloat16 *__restrict__ dq,
-                                                            float *colsum, int L, int H,
-                                                            int chunks) {
+// 8 columns each. Every block also copies its slice of the dR rows out of
+// the padded accumulator; the last block to finish (a counter the zeroing
+// reset) forms du = (column sums of dQ) - dv and dv = the column sums of
+// the position part.
+__global__ void __launch_bounds__(256) bwd_dq_finish_kernel(
+    const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq, float *colsum,
+    const float *dv_acc, unsigned *counter, float *du, float *dvb, const float *dr_acc, float *dr,
+    int L, int H, int kv_rows, int chunks) {
   __shared__ float part[32][65];
+  __shared__ bool last;
   const int bh = blockIdx.x / chunks, ch = blockIdx.x % chunks;
   const int sub = threadIdx.x & 7, slot = threadIdx.x >> 3;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -761,22 +783,24 @@ __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(const float *__restr
     for (int k = 0; k < 32; ++k) s += part[k][threadIdx.x];
     atomicAdd(colsum + (bh % H) * DH + threadIdx.x, s);
   }
-}
-
-// dR rows out of the padded accumulator; du = (column sums of dQ) - dv,
-// dv = column sums of the position part.
-__global__ void bwd_tail_kernel(const float *colsum, const float *dv_acc, float *du, float *dvb,
-                                int n, const float *dr_acc, float *dr, int H, int kv_rows) {
-  const size_t tid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t e = tid; e < (size_t)n; e += stride) {
-    dvb[e] = dv_acc[e];
-    du[e] = colsum[e] - dv_acc[e];
+  {
+    const size_t per_h = (size_t)kv_rows * DH / 4, n = (size_t)H * per_h;
+    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+      const size_t h = e / per_h, o = e % per_h;
+      ((float4 *)dr)[e] = ((const float4 *)(dr_acc + (h * (kv_rows + kDrPad) + kDrPad) * DH))[o];
+    }
   }
-  const size_t per_h = (size_t)kv_rows * DH / 4;
-  for (size_t e = tid; e < (size_t)H * per_h; e += stride) {
-    const size_t h = e / per_h, o = e % per_h;
-    ((float4 *)dr)[e] = ((const float4 *)(dr_acc + (h * (kv_rows + kDrPad) + kDrPad) * DH))[o];
+  // the column sums of every block are in place before the counter moves
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < H * DH; e += blockDim.x) {
+    const float cs = __ldcg(colsum + e), pv = __ldcg(dv_acc + e);
+    dvb[e] = pv;
+    du[e] = cs - pv;
   }
 }
 
@@ -832,7 +856,8 @@ size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 }  // namespace
 
 // Workspace: D [rows] f32 | (Q+u) [rows][64] bf16 | (Q+v) [rows][64] fp16 |
-// R fp16 [H][kv_rows][64] | dQ accumulator [rows][64] f32 | dv, colsum [H][64] f32 |
+// R fp16 [H][kv_rows][64] | dQ accumulator [rows][64] f32 | dv, colsum [H][64] f32,
+// finish counter u32 |
 // dR accumulator [H][kDrPad + kv_rows][64] f32
 BwdWorkspace tc_bwd_workspace(const AttnShape &s) {
   const size_t rows = (size_t)s.B * s.H * s.L;
@@ -843,7 +868,7 @@ BwdWorkspace tc_bwd_workspace(const AttnShape &s) {
   const size_t r16_off = w.dqv_off + up256(rows * DH * 2);
   const size_t dq_off = r16_off + up256((size_t)s.H * s.kv_rows * DH * 2);
   const size_t sums_off = dq_off + up256(rows * DH * 4);
-  const size_t dr_off = sums_off + up256((size_t)2 * s.H * DH * 4);
+  const size_t dr_off = sums_off + up256((size_t)2 * s.H * DH * 4 + 4);
   w.total = dr_off + up256((size_t)s.H * (kDrPad + s.kv_rows) * DH * 4);
   return w;
 }
@@ -862,8 +887,8 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   __half *r16 = (__half *)((char *)ws + r16_off);
   const size_t dq_off = r16_off + up256((size_t)s.H * s.kv_rows * DH * 2);
   float *dq_acc = (float *)((char *)ws + dq_off);
-  float *sums = (float *)((char *)ws + dq_off + up256(rows * DH * 4));  // dv_acc | colsum
-  float *dr_acc = (float *)((char *)sums + up256((size_t)2 * s.H * DH * 4));
+  float *sums = (float *)((char *)ws + dq_off + up256(rows * DH * 4));  // dv_acc | colsum | counter
+  float *dr_acc = (float *)((char *)sums + up256((size_t)2 * s.H * DH * 4 + 4));
   const size_t n_dr_acc = (size_t)s.H * (kDrPad + s.kv_rows) * DH;
   const int nq = (s.L + BQ - 1) / BQ;
 
@@ -885,21 +910,25 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  bwd_zero_kernel<<<sms * 4, 256, 0, st>>>(dr_acc, n_dr_acc, dq_acc, rows * DH, sums,
-                                           2 * s.H * DH, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv,
-                                           s.B * s.H, s.H, s.cap, s.m, s.head, s.kv_rows,
-                                           (const __nv_bfloat16 *)r, r16,
-                                           (size_t)s.H * s.kv_rows * DH, s.mvis);
-  ++*launches;
+  ZeroArgs z;
+  z.dr = dr_acc; z.n_dr = n_dr_acc; z.dq_acc = dq_acc; z.n_dq = rows * DH;
+  z.sums = sums; z.n_sums = 2 * s.H * DH + 1;  // the counter is zero as a float too
+  z.dk = (__nv_bfloat16 *)dk; z.dv = (__nv_bfloat16 *)dv;
+  z.BH = s.B * s.H; z.H = s.H; z.cap = s.cap; z.m = s.m; z.head = s.head; z.kv_rows = s.kv_rows;
+  z.r = (const __nv_bfloat16 *)r; z.r16 = r16; z.n_r = (size_t)s.H * s.kv_rows * DH;
+  z.mvis = s.mvis;
   if (o_lo) {
     long long blocks = ((long long)rows * 8 + 255) / 256;
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+    if (blocks < (long long)sms * 4) blocks = (long long)sms * 4;  // enough for the zeroing
     bwd_light_prep_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-        (long long)rows, s.L, s.H, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)u,
+        z, (long long)rows, s.L, s.H, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)u,
         (const __nv_bfloat16 *)vb, (const __nv_bfloat16 *)o, (const __nv_bfloat16 *)o_lo,
         (const __nv_bfloat16 *)dout, (__nv_bfloat16 *)qu, (__half *)qv, delta);
     ++*launches;
   } else {
+    bwd_zero_kernel<<<sms * 4, 256, 0, st>>>(z);
+    ++*launches;
     cudaError_t e = launch_tc_bwd_prep(s, q, k, v, r, u, vb, dout, delta, qu, qv, st, launches);
     if (e != cudaSuccess) return e;
   }
@@ -924,11 +953,9 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   rxl_bwd_main_kernel<<<grid, kThreads, F_SMEM, st>>>(tk, tv, tr16, tqu, tqv, tdo, tdq, tdr, p);
   ++*launches;
   const int chunks = (s.L + 127) / 128;
-  bwd_dq_finish_kernel<<<(unsigned)(s.B * s.H * chunks), 256, 0, st>>>(dq_acc, (__nv_bfloat16 *)dq,
-                                                                        sums + s.H * DH, s.L, s.H, chunks);
-  ++*launches;
-  bwd_tail_kernel<<<sms * 2, 256, 0, st>>>(sums + s.H * DH, sums, du, dvb, s.H * DH, dr_acc, dr, s.H,
-                                           s.kv_rows);
+  bwd_dq_finish_kernel<<<(unsigned)(s.B * s.H * chunks), 256, 0, st>>>(
+      dq_acc, (__nv_bfloat16 *)dq, sums + s.H * DH, sums, (unsigned *)(sums + 2 * s.H * DH), du, dvb,
+      dr_acc, dr, s.L, s.H, s.kv_rows, chunks);
   ++*launches;
   return cudaGetLastError();
 }
