@@ -436,9 +436,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
       }
       float y[64];
-      half_tile_logits<true>(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, y);
+      half_tile_exponents(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, -lse2, y);
 #pragma unroll
-      for (int k = 0; k < 64; ++k) y[k] = ex2(y[k] - lse2);  // P
+      for (int k = 0; k < 64; ++k) y[k] = ex2(y[k]);  // P
       // the P/dA buffer held the previous pair's dQ staging
       if (g > 0) {
         ok = mbar_wait(bar_sfree, (g - 1) & 1, abort_flag);
@@ -456,9 +456,14 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         uint32_t dp[32];
         tmem_ld32(trow + TM_S + 64 * hf + 32 * cc, dp);
         tmem_wait_ld();
+        const float2 scale2 = make_float2(p.scale, p.scale), ndi2 = make_float2(-Di, -Di);
 #pragma unroll
-        for (int k = 0; k < 32; ++k)  // dA (P = 0 and finite dP off the allowed pairs)
-          y[32 * cc + k] = p.scale * y[32 * cc + k] * (__uint_as_float(dp[k]) - Di);
+        for (int k = 0; k < 32; k += 2) {  // dA (P = 0 and finite dP off the allowed pairs)
+          const float2 d = __fadd2_rn(make_float2(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])), ndi2);
+          const float2 t = __fmul2_rn(__fmul2_rn(make_float2(y[32 * cc + k], y[32 * cc + k + 1]), scale2), d);
+          y[32 * cc + k] = t.x;
+          y[32 * cc + k + 1] = t.y;
+        }
       }
       // P is no longer read: dP and dV were committed together
       store_half_bf16(sb + F_PA, ii, hf, y);
@@ -493,8 +498,12 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       {
         const int r = ii & 7;
         uint32_t w[36];
+        const float2 sig2 = make_float2(sig, sig);
 #pragma unroll
-        for (int m = 0; m < 32; ++m) w[m] = pack_f16(sig * y[63 - 2 * m], sig * y[62 - 2 * m]);
+        for (int m = 0; m < 32; ++m) {
+          const float2 t = __fmul2_rn(make_float2(y[63 - 2 * m], y[62 - 2 * m]), sig2);
+          w[m] = pack_f16(t.x, t.y);
+        }
 #pragma unroll
         for (int m = 32; m < 36; ++m) w[m] = 0u;
         // odd part of the shift: element x <- x - 1 by a byte permute of
@@ -565,15 +574,22 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           tmem_ld32(trow + TM_QC + 32 * hf, qc);
           tmem_ld32(trow + TM_QP + 32 * hf, qp);
           tmem_wait_ld();
+          const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(qp[e]) * inv;
+          for (int e = 0; e < 32; e += 2) {
+            const float2 t = __fmul2_rn(make_float2(__uint_as_float(qp[e]), __uint_as_float(qp[e + 1])), inv2);
+            v[e] = t.x;
+            v[e + 1] = t.y;
+          }
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            st_shared_v4(sb + F_PA + hf * 16384 + sw128_offset(ii, e),
-                         __float_as_uint(__uint_as_float(qc[4 * e]) + v[4 * e]),
-                         __float_as_uint(__uint_as_float(qc[4 * e + 1]) + v[4 * e + 1]),
-                         __float_as_uint(__uint_as_float(qc[4 * e + 2]) + v[4 * e + 2]),
-                         __float_as_uint(__uint_as_float(qc[4 * e + 3]) + v[4 * e + 3]));
+          for (int e = 0; e < 8; ++e) {
+            const float2 lo = __fadd2_rn(make_float2(__uint_as_float(qc[4 * e]), __uint_as_float(qc[4 * e + 1])),
+                                         make_float2(v[4 * e], v[4 * e + 1]));
+            const float2 hi = __fadd2_rn(make_float2(__uint_as_float(qc[4 * e + 2]), __uint_as_float(qc[4 * e + 3])),
+                                         make_float2(v[4 * e + 2], v[4 * e + 3]));
+            st_shared_v4(sb + F_PA + hf * 16384 + sw128_offset(ii, e), __float_as_uint(lo.x),
+                         __float_as_uint(lo.y), __float_as_uint(hi.x), __float_as_uint(hi.y));
+          }
         }
         {
           uint32_t ra[32], rb[32];
@@ -582,18 +598,18 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar_fl);  // the G columns may take the next pair's logits
+          const float2 inv2 = make_float2(inv, inv);
+          auto scaled = [&](const uint32_t(&src)[32], int e) {
+            return __fmul2_rn(make_float2(__uint_as_float(src[e]), __uint_as_float(src[e + 1])), inv2);
+          };
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            st_shared_v4(sb + F_DG + 2 * hf * 16384 + sw128_offset(ii, e),
-                         __float_as_uint(inv * __uint_as_float(ra[4 * e])),
-                         __float_as_uint(inv * __uint_as_float(ra[4 * e + 1])),
-                         __float_as_uint(inv * __uint_as_float(ra[4 * e + 2])),
-                         __float_as_uint(inv * __uint_as_float(ra[4 * e + 3])));
-            st_shared_v4(sb + F_DG + (2 * hf + 1) * 16384 + sw128_offset(ii, e),
-                         __float_as_uint(inv * __uint_as_float(rb[4 * e])),
-                         __float_as_uint(inv * __uint_as_float(rb[4 * e + 1])),
-                         __float_as_uint(inv * __uint_as_float(rb[4 * e + 2])),
-                         __float_as_uint(inv * __uint_as_float(rb[4 * e + 3])));
+            const float2 a0 = scaled(ra, 4 * e), a1 = scaled(ra, 4 * e + 2);
+            const float2 b0 = scaled(rb, 4 * e), b1 = scaled(rb, 4 * e + 2);
+            st_shared_v4(sb + F_DG + 2 * hf * 16384 + sw128_offset(ii, e), __float_as_uint(a0.x),
+                         __float_as_uint(a0.y), __float_as_uint(a1.x), __float_as_uint(a1.y));
+            st_shared_v4(sb + F_DG + (2 * hf + 1) * 16384 + sw128_offset(ii, e), __float_as_uint(b0.x),
+                         __float_as_uint(b0.y), __float_as_uint(b1.x), __float_as_uint(b1.y));
           }
         }
         fence_proxy_async_smem();

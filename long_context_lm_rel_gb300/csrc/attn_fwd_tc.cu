@@ -414,15 +414,17 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i;
         // the warp skips the mask where all 32 keys are visible to all its rows
         const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
-        if (__all_sync(0xffffffffu, lim >= 31)) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) y[32 * cc + k] = __uint_as_float(sr[k]) + win[31 - k];
-        } else {
+        for (int k = 0; k < 32; k += 2) {
+          const float2 a = __fadd2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])),
+                                      make_float2(win[31 - k], win[30 - k]));
+          y[32 * cc + k] = a.x;
+          y[32 * cc + k + 1] = a.y;
+        }
+        if (!__all_sync(0xffffffffu, lim >= 31)) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float a = __uint_as_float(sr[k]) + win[31 - k];
-            y[32 * cc + k] = k <= lim ? a : -INFINITY;
-          }
+          for (int k = 0; k < 32; ++k)
+            if (k > lim) y[32 * cc + k] = -INFINITY;
         }
       }
       float mt = -INFINITY;
@@ -436,14 +438,17 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       const float m_new = move ? mrow : m_run;
       const float ref = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = move ? ex2(m_run - ref) : 1.f;  // 0 on the first visible tile
-      float sum = 0.f;
+      float2 sum2 = make_float2(0.f, 0.f);
+      const float2 nref2 = make_float2(-ref, -ref);
       uint32_t pk[32];
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
-        const float p0 = ex2(y[k] - ref), p1 = ex2(y[k + 1] - ref);
-        sum += p0 + p1;
-        pk[k / 2] = pack_bf16(p0, p1);
+        const float2 e = __fadd2_rn(make_float2(y[k], y[k + 1]), nref2);
+        const float2 pp = make_float2(ex2(e.x), ex2(e.y));
+        sum2 = __fadd2_rn(sum2, pp);
+        pk[k / 2] = pack_bf16(pp.x, pp.y);
       }
+      const float sum = sum2.x + sum2.y;
       l_run = l_run * alpha + sum;
       m_run = m_new;
       // the P buffer and O: P.V(g-1), which ran while this tile's logits

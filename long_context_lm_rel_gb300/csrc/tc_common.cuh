@@ -93,14 +93,16 @@ __device__ __forceinline__ void lane_shift_window(float (&win)[64], int lane) {
   }
 }
 
-// Logits of half a 128x128 tile for two warps per TMEM lane quadrant: the calling thread
-// (quadrant `quad`, half `hf`) produces the logits of keys jj = 64*hf + k,
-// k = 0..63, of its row ii = 32*quad + lane: y[k] = (S + G_skewed) * scale,
-// -inf where masked. kScaled = false skips the multiply (operands prescaled).
-template <bool kScaled>
-__device__ __forceinline__ void half_tile_logits(uint32_t trow, uint32_t s_col, uint32_t g_col,
-                                                 int quad, int lane, int hf, int i,
-                                                 const KeyTile &x, float scale, float (&y)[64]) {
+// Base-2 exponents of P for half a 128x128 tile, two warps per TMEM lane
+// quadrant: the calling thread (quadrant `quad`, half `hf`) produces, for
+// keys jj = 64*hf + k (k = 0..63) of its row ii = 32*quad + lane,
+// y[k] = (S + G_skewed) * scale + bias, -inf where masked. Pairs of keys go
+// through the packed fp32x2 add and fma.
+__device__ __forceinline__ void half_tile_exponents(uint32_t trow, uint32_t s_col, uint32_t g_col,
+                                                    int quad, int lane, int hf, int i,
+                                                    const KeyTile &x, float scale, float bias,
+                                                    float (&y)[64]) {
+  const float2 scale2 = make_float2(scale, scale), bias2 = make_float2(bias, bias);
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
     const int c = 2 * hf + cc;
@@ -117,23 +119,21 @@ __device__ __forceinline__ void half_tile_logits(uint32_t trow, uint32_t s_col, 
       win[32 + e] = __uint_as_float(w1[e]);
     }
     lane_shift_window(win, lane);
+#pragma unroll
+    for (int k = 0; k < 32; k += 2) {
+      const float2 a = __fadd2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])),
+                                  make_float2(win[31 - k], win[30 - k]));
+      const float2 t = __ffma2_rn(a, scale2, bias2);
+      y[32 * cc + k] = t.x;
+      y[32 * cc + k + 1] = t.y;
+    }
     // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i; the
     // warp skips the mask where all 32 keys are visible to all its rows
     const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
-    if (__all_sync(0xffffffffu, lim >= 31)) {
+    if (!__all_sync(0xffffffffu, lim >= 31)) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        float a = __uint_as_float(sr[k]) + win[31 - k];
-        if (kScaled) a *= scale;
-        y[32 * cc + k] = a;
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        float a = __uint_as_float(sr[k]) + win[31 - k];
-        if (kScaled) a *= scale;
-        y[32 * cc + k] = k <= lim ? a : -INFINITY;
-      }
+      for (int k = 0; k < 32; ++k)
+        if (k > lim) y[32 * cc + k] = -INFINITY;
     }
   }
 }
