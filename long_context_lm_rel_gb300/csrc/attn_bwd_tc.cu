@@ -86,11 +86,11 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {
 }
 
 // 64 fp32 values (keys 64*hf ..) of row ii as bf16 into column block hf of a
-// [128][128] K-major 128-byte-swizzled tile pair (blocks 16 KB apart).
-__device__ __forceinline__ void store_half_bf16(uint32_t base, int ii, int hf, const float (&a)[64]) {
+// [128][128] K-major 128-byte-swizzled tile pair; row = sw128_row(block hf, ii).
+__device__ __forceinline__ void store_half_bf16(uint32_t row, const float (&a)[64]) {
 #pragma unroll
   for (int c = 0; c < 8; ++c)
-    st_shared_v4(base + hf * 16384 + sw128_offset(ii, c), pack_bf16(a[8 * c + 0], a[8 * c + 1]),
+    st_shared_v4(sw128_at(row, c), pack_bf16(a[8 * c + 0], a[8 * c + 1]),
                  pack_bf16(a[8 * c + 2], a[8 * c + 3]), pack_bf16(a[8 * c + 4], a[8 * c + 5]),
                  pack_bf16(a[8 * c + 6], a[8 * c + 7]));
 }
@@ -407,6 +407,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t bar_x = bar_x0 + 8 * quad;
     const int c0 = ii >> 3;  // first 16-byte chunk of row ii's sheared values
+    // row ii in the P/dA block hf (also dQ staging), in the dG tile (chunk C
+    // at sw128_at(row_dg, C & 7) + (C >> 3) * 16384) and in dR staging atom 2hf
+    const uint32_t row_pa = sw128_row(sb + F_PA + hf * 16384, ii);
+    const uint32_t row_dg = sw128_row(sb + F_DG, ii);
+    const uint32_t row_dr = sw128_row(sb + F_DG + 2 * hf * 16384, ii);
     uint32_t xphase = 0;
     float dvp = 0.f;  // sum over this warp's rows of dQp, column 32*hf + lane
     bool ok = true;
@@ -444,7 +449,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         ok = mbar_wait(bar_sfree, (g - 1) & 1, abort_flag);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
       }
-      store_half_bf16(sb + F_PA, ii, hf, y);
+      store_half_bf16(row_pa, y);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_p);
@@ -466,7 +471,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
       }
       // P is no longer read: dP and dV were committed together
-      store_half_bf16(sb + F_PA, ii, hf, y);
+      store_half_bf16(row_pa, y);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_da);
@@ -522,10 +527,10 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         // columns outside [ii, ii + 127] are zero (staging overwrote them)
         if (hf == 1) {
           for (int C = 0; C < 15; ++C)
-            if (C < c0) st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), 0, 0, 0, 0);
+            if (C < c0) st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384, 0, 0, 0, 0);
         } else {
           for (int C = 17; C < 32; ++C)
-            if (C > c0 + 16) st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), 0, 0, 0, 0);
+            if (C > c0 + 16) st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384, 0, 0, 0, 0);
         }
         if (hf == 1) {
           // chunk cbase + 8 is shared with the other half: hand it over
@@ -533,14 +538,14 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
             const int C = cbase + t;
-            st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), w[4 * t],
+            st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384, w[4 * t],
                          w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
           }
         } else {
 #pragma unroll
           for (int t = 1; t < 9; ++t) {
             const int C = cbase + t;
-            st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7), w[4 * t],
+            st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384, w[4 * t],
                          w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
           }
         }
@@ -553,7 +558,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                        : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
                        : "r"(xrow));
           const int C = cbase;
-          st_shared_v4(sb + F_DG + (C >> 3) * 16384 + sw128_offset(ii, C & 7),
+          st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384,
                        a | w[0], b | w[1], cc | w[2], d | w[3]);
         }
       }
@@ -587,7 +592,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                                          make_float2(v[4 * e], v[4 * e + 1]));
             const float2 hi = __fadd2_rn(make_float2(__uint_as_float(qc[4 * e + 2]), __uint_as_float(qc[4 * e + 3])),
                                          make_float2(v[4 * e + 2], v[4 * e + 3]));
-            st_shared_v4(sb + F_PA + hf * 16384 + sw128_offset(ii, e), __float_as_uint(lo.x),
+            st_shared_v4(sw128_at(row_pa, e), __float_as_uint(lo.x),
                          __float_as_uint(lo.y), __float_as_uint(hi.x), __float_as_uint(hi.y));
           }
         }
@@ -606,9 +611,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           for (int e = 0; e < 8; ++e) {
             const float2 a0 = scaled(ra, 4 * e), a1 = scaled(ra, 4 * e + 2);
             const float2 b0 = scaled(rb, 4 * e), b1 = scaled(rb, 4 * e + 2);
-            st_shared_v4(sb + F_DG + 2 * hf * 16384 + sw128_offset(ii, e), __float_as_uint(a0.x),
+            st_shared_v4(sw128_at(row_dr, e), __float_as_uint(a0.x),
                          __float_as_uint(a0.y), __float_as_uint(a1.x), __float_as_uint(a1.y));
-            st_shared_v4(sb + F_DG + (2 * hf + 1) * 16384 + sw128_offset(ii, e), __float_as_uint(b0.x),
+            st_shared_v4(sw128_at(row_dr, e) + 16384, __float_as_uint(b0.x),
                          __float_as_uint(b0.y), __float_as_uint(b1.x), __float_as_uint(b1.y));
           }
         }

@@ -367,6 +367,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const int quad = warp & 3, hf = warp >> 2;
     const int ii = quad * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t row_p = sw128_row(sbase + SM_P + hf * 16384, ii);  // row ii of P block hf
     const uint32_t bar_x = bar_x0 + 8 * quad;
     uint32_t xphase = 0;
     float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's part of the row sum
@@ -460,7 +461,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       }
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        st_shared_v4(sbase + SM_P + hf * 16384 + sw128_offset(ii, c), pk[4 * c], pk[4 * c + 1],
+        st_shared_v4(sw128_at(row_p, c), pk[4 * c], pk[4 * c + 1],
                      pk[4 * c + 2], pk[4 * c + 3]);
       // rows of V past the run hold another run's (or junk) data: zero them
       // so that 0 * junk cannot leak into O

@@ -273,6 +273,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
+// The same for a whole row of a tile whose base is 1024-byte aligned: with
+// r = sw128_row(base, row), chunk c of the row sits at sw128_at(r, c) =
+// r ^ (c << 4) (row * 128 leaves bits 4-6 clear, so the swizzle is one xor).
+__device__ __forceinline__ uint32_t sw128_row(uint32_t base, int row) {
+  return base + (uint32_t)(row * 128) + ((uint32_t)(row & 7) << 4);
+}
+__device__ __forceinline__ uint32_t sw128_at(uint32_t row_addr, int chunk) {
+  return row_addr ^ ((uint32_t)chunk << 4);
+}
 
 }  // namespace sm103
 }  // namespace rxl
