@@ -19,12 +19,16 @@
 //     already the base-2 logit;
 //   * 8 softmax warps, two per TMEM lane quadrant: the thread of (row ii,
 //     half hf) handles keys 64*hf .. 64*hf+63 of row ii. It loads S and its
-//     skewed G window, masks, and runs the fp32 online softmax (exp2); the two
-//     halves of a row exchange their maxima (and at the end their sums)
-//     through shared memory. P goes to shared memory (bf16). The running
-//     maximum used as the exponent reference only moves when the row max
-//     grows by more than 2^8 (then O is rescaled in TMEM), so P <= 256;
-//   * tcgen05: O += P V -> TMEM cols [384,448)          (M=128, N=64)
+//     skewed G window, masks, and runs the fp32 online softmax (exp2) over
+//     its half on its own: each half keeps its own exponent reference, sum
+//     and O accumulator, so the two warps of a row never wait on each other
+//     within an item. P goes to shared memory (bf16). A half's running
+//     maximum, used as its exponent reference, only moves when the half's
+//     max grows by more than 2^8 (then its O is rescaled in TMEM), so
+//     P <= 256;
+//   * tcgen05: O_h += P_h V_h -> TMEM cols [384,448), [448,512) for the key
+//     halves h (M=128, N=64, K=64 each); the epilogue combines the halves
+//     with their references (one exchange through shared memory per item)
 // Warp 8 is the producer: one thread issues the TMA loads (two stages) and
 // every MMA; tcgen05.commit signals completion through mbarriers.
 //
@@ -67,6 +71,7 @@ constexpr uint32_t SM_X = SM_BAR + 128;        // row-half exchange: [2][2][128]
 constexpr uint32_t SMEM_BYTES = SM_X + 2048 + 1024;  // + alignment slack
 constexpr float kRescaleThreshold = 8.f;       // log2 units
 constexpr uint32_t STAGE_TX = 16384 + 16384 + 32768;
+// O accumulators: keys 0-63 of every tile into TM_O, keys 64-127 into TM_O + 64
 constexpr uint32_t TM_S = 0, TM_G = 128, TM_O = 384, TM_COLS = 512;
 
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
@@ -328,10 +333,10 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         tc_fence_after();
         const int s = g & 1;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 8; ++k) {  // O_h += P_h V_h for the key halves h = k / 4
           const uint64_t a = sdesc_sw128(sbase + SM_P + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
           const uint64_t b = sdesc_sw128(sbase + SM_V + s * 16384 + k * 2048, 16, 1024);
-          mma_bf16(tmem + TM_O, a, b, IDESC_O, (mc.t > 0 || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + TM_O + 64 * (k >> 2), a, b, IDESC_O, (mc.t > 0 || (k & 3) > 0) ? 1u : 0u);
         }
         mma_commit(bar_pv);
         if (new_item) {
@@ -431,12 +436,10 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       float mt = -INFINITY;
 #pragma unroll
       for (int k = 0; k < 64; k += 2) mt = fmax3(mt, y[k], y[k + 1]);
-      float other;
-      if (!(ok = pair_exchange(mt, &other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
-      // the exponent reference only moves when the row max outgrows it by 2^8
-      const float mrow = fmaxf(mt, other);
-      const bool move = mrow > m_run + kRescaleThreshold;
-      const float m_new = move ? mrow : m_run;
+      // this half's exponent reference only moves when its max outgrows it
+      // by 2^8 (each half keeps its own reference, sum and O accumulator)
+      const bool move = mt > m_run + kRescaleThreshold;
+      const float m_new = move ? mt : m_run;
       const float ref = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = move ? ex2(m_run - ref) : 1.f;  // 0 on the first visible tile
       float2 sum2 = make_float2(0.f, 0.f);
@@ -471,13 +474,16 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         for (int c = 0; c < 4; ++c) st_shared_v4(vrow + 16 * (4 * hf + c), 0, 0, 0, 0);
       }
       if (__any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
-        uint32_t o[32];
-        tmem_ld32(trow + TM_O + 32 * hf, o);
-        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-        tmem_st32(trow + TM_O + 32 * hf, o);
-        tmem_wait_st();
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(trow + TM_O + 64 * hf + 32 * cc, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(trow + TM_O + 64 * hf + 32 * cc, o);
+          tmem_wait_st();
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -493,16 +499,32 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         mbar_arrive(bar_qready);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, g & 1, abort_flag));
-      float l_other = 0.f;
+      // the two halves' references and sums; O_h and l_h are relative to
+      // 2^(reference of half h), which is -inf for a half that saw no key
+      float m_other = -INFINITY, l_other = 0.f;
+      if (ok) ok = pair_exchange(m_run, &m_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
       if (ok) ok = pair_exchange(l_run, &l_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      const float inv = 1.f / (l_run + l_other);
+      const float m_row = fmaxf(m_run, m_other);
+      const float a_own = m_run == -INFINITY ? 0.f : ex2(m_run - m_row);
+      const float a_oth = m_other == -INFINITY ? 0.f : ex2(m_other - m_row);
+      const float l_row = l_run * a_own + l_other * a_oth;
+      const float inv = 1.f / l_row;
       uint32_t o[32];
-      tmem_ld32(trow + TM_O + 32 * hf, o);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar_ofree);
+      {
+        // this warp's 32 output columns: both halves' accumulators, scaled
+        uint32_t o1[32];
+        tmem_ld32(trow + TM_O + 32 * hf, o);
+        tmem_ld32(trow + TM_O + 64 + 32 * hf, o1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_ofree);
+        const float a0 = hf ? a_oth : a_own, a1 = hf ? a_own : a_oth;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          o[e] = __float_as_uint(__uint_as_float(o[e]) * a0 + __uint_as_float(o1[e]) * a1);
+      }
       if (MODE == kPrep) {
         // D_i = dO_i . O_i with O_i still in fp32
         const uint4 *drow = (const uint4 *)(p.dout + ((size_t)it.bh * p.L + (i < p.L ? i : 0)) * DH);
@@ -542,7 +564,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           }
         }
         if (hf == 0 && i < p.L)
-          p.lse[(size_t)it.bh * p.L + i] = (m_run + log2f(l_run + l_other)) * 0.69314718055994531f;
+          p.lse[(size_t)it.bh * p.L + i] = (m_row + log2f(l_row)) * 0.69314718055994531f;
       }
       m_run = -INFINITY;
       l_run = 0.f;
