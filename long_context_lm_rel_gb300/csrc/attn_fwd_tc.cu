@@ -32,6 +32,14 @@
 // Warp 8 is the producer: one thread issues the TMA loads (two stages) and
 // every MMA; tcgen05.commit signals completion through mbarriers.
 //
+// Few items (at most half as many as SMs: short segments, few heads): the
+// kernel runs as clusters of two CTAs per item instead of persistently, each
+// CTA over half of the item's key tiles. Rank 1 hands its O (fp32,
+// relative to its own reference), reference and sum to rank 0 through
+// distributed shared memory once rank 0 has finished with its K/V stages;
+// rank 0 merges the two and writes the output. Every cross-CTA wait is a
+// bounded mbarrier wait.
+//
 // The skew: thread of row ii = 32*quad + lane needs G columns ii..ii+127. Per
 // chunk of 32 keys it loads a warp-uniform 64-column window and shifts it by
 // its lane with a 5-stage predicated barrel shift.
@@ -142,10 +150,12 @@ __device__ __forceinline__ Item item_at(const Params &p, int w) {
 }
 
 // Walks this CTA's tiles across its items: k counts the CTA's items, t the
-// key tiles of the current item.
-template <bool RESET>
+// key tiles of the current item, which this CTA takes from t0 up to t1.
+// SPLIT: a cluster of two CTAs per item, the first (rank 0) taking the first
+// half of its key tiles, rank 1 the rest; one item per cluster.
+template <bool RESET, bool SPLIT>
 struct Cursor {
-  int k, w, t, nitems;
+  int k, w, t, t0, t1, nitems;
   bool valid;
   Item it;
   __device__ __forceinline__ int item_of_round(int r) const {
@@ -155,18 +165,34 @@ struct Cursor {
   __device__ void init(const Params &p, int n) {
     nitems = n;
     k = 0;
-    t = 0;
-    w = item_of_round(0);
+    w = SPLIT ? (int)(blockIdx.x >> 1) : item_of_round(0);
     valid = w < nitems;
-    if (valid) it = item_at<RESET>(p, w);
+    if (!valid) return;
+    it = item_at<RESET>(p, w);
+    t0 = 0;
+    t1 = it.T;
+    if (SPLIT) {
+      const int half = (it.T + 1) >> 1;
+      if (blockIdx.x & 1) t0 = half; else t1 = half;
+      valid = t0 < t1;
+    }
+    t = t0;
   }
   __device__ void next(const Params &p) {
-    if (++t == it.T) {
+    if (++t == t1) {
+      if (SPLIT) {
+        valid = false;
+        return;
+      }
       t = 0;
       ++k;
       w = item_of_round(k);
       valid = w < nitems;
-      if (valid) it = item_at<RESET>(p, w);
+      if (valid) {
+        it = item_at<RESET>(p, w);
+        t0 = 0;
+        t1 = it.T;
+      }
     }
   }
 };
@@ -215,7 +241,7 @@ __device__ __forceinline__ void q_prep(const Params &p, const Item &it, uint32_t
 // Persistent kernel: gridDim.x CTAs walk all work items. Per CTA, tiles are
 // numbered g = 0, 1, ... across its items; every barrier phase follows g
 // (tile barriers) or the item counter k (q_ready, o_free).
-template <int MODE, bool RESET>
+template <int MODE, bool RESET, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_r, const Params p, int nitems) {
@@ -234,6 +260,9 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   const uint32_t bar_ofree = b0 + 56;    // epilogue of an item read O (256)
   const uint32_t bar_drain = b0 + 64;
   const uint32_t bar_x0 = b0 + 72;       // 4 quadrant exchange barriers
+  // SPLIT: rank 0's K/V stages are free for rank 1's half (rank 1, count 1);
+  // rank 1's half has landed in them (rank 0, count 256)
+  const uint32_t bar_peer = b0 + 112, bar_data = b0 + 120;
   uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 104);
   volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 108);
   volatile float *xbuf = (volatile float *)(smem + SM_X);
@@ -249,9 +278,15 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     mbar_init(bar_ofree, kSoftmaxWarps * 32);
     mbar_init(bar_drain, 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
+    if (SPLIT) {
+      mbar_init(bar_peer, 1);
+      mbar_init(bar_data, kSoftmaxWarps * 32);
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
+  // the peer CTA arrives on this CTA's barriers: they must be initialised first
+  if (SPLIT) cluster_sync();
   if (warp == kProducerWarp) {
     tmem_alloc(smem_u32(tmem_slot), TM_COLS);
     if (lane == 0) {
@@ -270,7 +305,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (lane == 0) {
       bool pending[2] = {false, false};
       int nissued[2] = {0, 0};
-      Cursor<RESET> tc_;  // next tile to load
+      Cursor<RESET, SPLIT> tc_;  // next tile to load
       tc_.init(p, nitems);
       int g_tma = 0;
       auto issue_tma = [&]() {
@@ -309,7 +344,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         return r;
       };
       bool ok = true;
-      Cursor<RESET> mc;  // tile whose P.V is next
+      Cursor<RESET, SPLIT> mc;  // tile whose P.V is next
       mc.init(p, nitems);
       if (tc_.valid) issue_tma();
       if (tc_.valid) issue_tma();
@@ -318,9 +353,9 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (ok) issue_sg(0);
       }
       for (int g = 0; ok && mc.valid; ++g) {
-        Cursor<RESET> nx = mc;
+        Cursor<RESET, SPLIT> nx = mc;
         nx.next(p);
-        const bool new_item = nx.valid && nx.t == 0;
+        const bool new_item = nx.valid && nx.t == nx.t0;
         // S/G of tile g+1 as soon as the softmax released S/G of tile g
         // (same item: the Q tiles are unchanged)
         if (nx.valid && !new_item) {
@@ -329,14 +364,14 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
         if (!(ok = mbar_wait(bar_pr, g & 1, abort_flag))) break;
         // the first P.V of an item overwrites O: its epilogue must have read it
-        if (mc.t == 0 && mc.k > 0 && !(ok = mbar_wait(bar_ofree, (mc.k - 1) & 1, abort_flag))) break;
+        if (mc.t == mc.t0 && mc.k > 0 && !(ok = mbar_wait(bar_ofree, (mc.k - 1) & 1, abort_flag))) break;
         tc_fence_after();
         const int s = g & 1;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // O_h += P_h V_h for the key halves h = k / 4
           const uint64_t a = sdesc_sw128(sbase + SM_P + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
           const uint64_t b = sdesc_sw128(sbase + SM_V + s * 16384 + k * 2048, 16, 1024);
-          mma_bf16(tmem + TM_O + 64 * (k >> 2), a, b, IDESC_O, (mc.t > 0 || (k & 3) > 0) ? 1u : 0u);
+          mma_bf16(tmem + TM_O + 64 * (k >> 2), a, b, IDESC_O, (mc.t > mc.t0 || (k & 3) > 0) ? 1u : 0u);
         }
         mma_commit(bar_pv);
         if (new_item) {
@@ -377,7 +412,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint32_t xphase = 0;
     float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's part of the row sum
     bool ok = true;
-    Cursor<RESET> cur;
+    Cursor<RESET, SPLIT> cur;
     cur.init(p, nitems);
     if (cur.valid) {
       q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
@@ -386,7 +421,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
     for (int g = 0; cur.valid; ++g) {
       const Item it = cur.it;
-      const int t = cur.t;
+      const int t = cur.t, t0 = cur.t0, t1 = cur.t1;
       const int i = it.i0 + ii;
       const int s = g & 1;
       ok = mbar_wait(bar_sg, g & 1, abort_flag) &&
@@ -473,7 +508,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
         for (int c = 0; c < 4; ++c) st_shared_v4(vrow + 16 * (4 * hf + c), 0, 0, 0, 0);
       }
-      if (__any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
+      if (__any_sync(0xffffffffu, t > t0 && alpha != 1.f)) {
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t o[32];
@@ -490,7 +525,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       mbar_arrive(bar_pr);
 
       cur.next(p);
-      if (t + 1 < it.T) continue;
+      if (t + 1 < t1) continue;
       // ---- last tile of the item: Q tiles of the next item, then epilogue
       if (cur.valid) {
         // the S/G MMAs of this item are all done (bar_sg waited above)
@@ -506,11 +541,10 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       if (ok) ok = pair_exchange(l_run, &l_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      const float m_row = fmaxf(m_run, m_other);
+      float m_row = fmaxf(m_run, m_other);
       const float a_own = m_run == -INFINITY ? 0.f : ex2(m_run - m_row);
       const float a_oth = m_other == -INFINITY ? 0.f : ex2(m_other - m_row);
-      const float l_row = l_run * a_own + l_other * a_oth;
-      const float inv = 1.f / l_row;
+      float l_row = l_run * a_own + l_other * a_oth;
       uint32_t o[32];
       {
         // this warp's 32 output columns: both halves' accumulators, scaled
@@ -525,6 +559,51 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         for (int e = 0; e < 32; ++e)
           o[e] = __float_as_uint(__uint_as_float(o[e]) * a0 + __uint_as_float(o1[e]) * a1);
       }
+      if (SPLIT) {
+        // rank 1 hands its part of the item (O relative to 2^m_row, m_row,
+        // l_row) to rank 0 through distributed shared memory: O rows into
+        // rank 0's K stages ([128][64] fp32, 16-byte chunks swizzled by
+        // row), m and l into its V stage; rank 0 merges the two parts
+        const uint32_t orow = ii * 256 + hf * 128;
+        if (blockIdx.x & 1) {
+          ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_peer, 0, abort_flag));
+          if (!ok) break;
+          const uint32_t ob = mapa_shared(sbase + SM_K + orow, 0);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_cluster_v4(ob + ((c ^ (ii & 7)) << 4), o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+          if (hf == 0) {
+            st_cluster_u32(mapa_shared(sbase + SM_V + 4 * ii, 0), __float_as_uint(m_row));
+            st_cluster_u32(mapa_shared(sbase + SM_V + 512 + 4 * ii, 0), __float_as_uint(l_row));
+          }
+          mbar_arrive_remote(mapa_shared(bar_data, 0));
+          break;  // this CTA's only item is done
+        }
+        if (it.T >= 2) {  // rank 1 has tiles: its stages were read (P.V done above)
+          if (threadIdx.x == 0) mbar_arrive_remote(mapa_shared(bar_peer, 1));
+          ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_data, 0, abort_flag));
+          if (!ok) break;
+          const float m1 = *(volatile float *)(smem + SM_V + 4 * ii);
+          const float l1 = *(volatile float *)(smem + SM_V + 512 + 4 * ii);
+          const float mm = fmaxf(m_row, m1);
+          const float as = m_row == -INFINITY ? 0.f : ex2(m_row - mm);
+          const float ap = m1 == -INFINITY ? 0.f : ex2(m1 - mm);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t a, b, cc, d;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
+                         : "r"(sbase + SM_K + orow + ((c ^ (ii & 7)) << 4)));
+            const uint32_t w[4] = {a, b, cc, d};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o[4 * c + e] = __float_as_uint(__uint_as_float(o[4 * c + e]) * as + __uint_as_float(w[e]) * ap);
+          }
+          l_row = l_row * as + l1 * ap;
+          m_row = mm;
+        }
+      }
+      const float inv = 1.f / l_row;
       if (MODE == kPrep) {
         // D_i = dO_i . O_i with O_i still in fp32
         const uint4 *drow = (const uint4 *)(p.dout + ((size_t)it.bh * p.L + (i < p.L ? i : 0)) * DH);
@@ -623,11 +702,12 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(rxl_fwd_tc_kernel<MODE, false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(rxl_fwd_tc_kernel<MODE, true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const void *fns[4] = {(const void *)rxl_fwd_tc_kernel<MODE, false, false>,
+                          (const void *)rxl_fwd_tc_kernel<MODE, true, false>,
+                          (const void *)rxl_fwd_tc_kernel<MODE, false, true>,
+                          (const void *)rxl_fwd_tc_kernel<MODE, true, true>};
+    for (int f = 0; f < 4 && attr_err == cudaSuccess; ++f)
+      attr_err = cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   Params p;
@@ -643,12 +723,32 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const unsigned grid = (unsigned)(nitems < sms ? nitems : sms);
   // the per-row reset is a separate instantiation: the plain call pays nothing for it
+  if (MODE == kFwd && 2 * nitems <= sms) {
+    // few items (short segments, few heads): two CTAs per item, each over
+    // half of its key tiles, merged through distributed shared memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * nitems));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = s.mvis ? cudaLaunchKernelEx(&cfg, rxl_fwd_tc_kernel<MODE, true, true>, tk, tv, tr, p, nitems)
+                           : cudaLaunchKernelEx(&cfg, rxl_fwd_tc_kernel<MODE, false, true>, tk, tv, tr, p, nitems);
+    ++*launches;
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  const unsigned grid = (unsigned)(nitems < sms ? nitems : sms);
   if (s.mvis)
-    rxl_fwd_tc_kernel<MODE, true><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
+    rxl_fwd_tc_kernel<MODE, true, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
   else
-    rxl_fwd_tc_kernel<MODE, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
+    rxl_fwd_tc_kernel<MODE, false, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
   ++*launches;
   return cudaGetLastError();
 }
