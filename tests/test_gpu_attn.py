@@ -8,6 +8,9 @@ float64 oracle on the same seeded inputs.
   (all batch rows), cfg5 as the 32-segment stream on its first and last layer
   with sampled rows at fill, wrap and steady-state segments;
 * skew-sensitive closed-form probes (distance labels) on tile boundaries;
+* calls with at most half as many (b, h, query tile) items as SMs, which the
+  forward runs as 2-CTA clusters (the small cases too, one of them with a
+  single key tile per item, i.e. an empty second half);
 * stop-gradient: the cache is never written by the backward.
 """
 import math
@@ -106,6 +109,18 @@ def test_nan_in_ring_rows_without_memory_does_not_leak(B, H, L, cap, m, head, ex
     x = make_inputs(B, H, L, cap, m, "bf16", seed=77 + m)
     c = run_gpu(x, cap, m, head, "bf16", ex=ex, fill=(float("nan"), float("nan")))
     compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head, ex)))
+
+
+@pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
+def test_few_items_two_cta_clusters(ex):
+    # 4 x 16 heads x one 128-row query tile = 64 items, at most half the SMs:
+    # the forward runs as 2-CTA clusters, each CTA over half of an item's key
+    # tiles (here 5 memory tiles on a wrapping ring + 1 current), merged
+    # through distributed shared memory
+    B, H, L, cap, m, head = 4, 16, 128, 640, 600, 500
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=4242)
+    c = run_gpu(x, cap, m, head, "bf16", ex=ex)
+    compare_full(x, c, cap, m, head, "bf16", tag=f"split {ex}")
 
 
 def test_low_part_of_o_restores_the_unrounded_output():
