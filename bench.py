@@ -357,36 +357,68 @@ def stream_cfg5(segments=32, layers=16, reps_update=200):
     cur = mk(B5, H5, L5, DH)
     rings = [[rxl.rxl_ring(t.data_ptr(), B5 * H5, M5, DH, kv * DH, rxl.RXL_DTYPE_BF16, 0, 0) for t in (K[n], V[n])]
              for n in range(layers)]
-    st = torch.cuda.current_stream()
-    launches = 0
-    pairs = 0
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for seg in range(segments):
-        for n in range(layers):
-            rk, rv = rings[n]
-            K[n][:, :, M5:].copy_(cur)
-            V[n][:, :, M5:].copy_(cur)
-            m = rk.len
-            pairs += B5 * H5 * (L5 * m + L5 * (L5 + 1) // 2)
-            d = rxl.make_desc(B5, H5, L5, M5, m, rk.head, SCALE, rxl.RXL_DTYPE_BF16)
-            rxl.rxl_attn_fwd(d, Q, K[n], V[n], R[n], U[n], VB[n], o, lse, st)
-            launches += rxl.rxl_last_launch_count()
-            for r_, t in ((rk, K[n]), (rv, V[n])):
-                rxl.rxl_mem_update(r_, t.data_ptr() + M5 * DH * 2, kv * DH, L5, st)
+    def run_stream(st):
+        """One pass of the stream from empty memory; returns (launches, visible pairs)."""
+        rings = [[rxl.rxl_ring(t.data_ptr(), B5 * H5, M5, DH, kv * DH, rxl.RXL_DTYPE_BF16, 0, 0)
+                  for t in (K[n], V[n])] for n in range(layers)]
+        launches = pairs = 0
+        for seg in range(segments):
+            for n in range(layers):
+                rk, rv = rings[n]
+                K[n][:, :, M5:].copy_(cur)
+                V[n][:, :, M5:].copy_(cur)
+                m = rk.len
+                pairs += B5 * H5 * (L5 * m + L5 * (L5 + 1) // 2)
+                d = rxl.make_desc(B5, H5, L5, M5, m, rk.head, SCALE, rxl.RXL_DTYPE_BF16)
+                rxl.rxl_attn_fwd(d, Q, K[n], V[n], R[n], U[n], VB[n], o, lse, st)
                 launches += rxl.rxl_last_launch_count()
+                for r_, t in ((rk, K[n]), (rv, V[n])):
+                    rxl.rxl_mem_update(r_, t.data_ptr() + M5 * DH * 2, kv * DH, L5, st)
+                    launches += rxl.rxl_last_launch_count()
+        return launches, pairs
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # eager: the calls issued from Python one by one
+    st = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    e0.record(st)
+    launches, pairs = run_stream(st)
     e1.record(st)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    # the memory update alone: back-to-back calls on a full ring
+    ms_eager = e0.elapsed_time(e1)
+    # the same 32 x 16 sequence (same ring positions) captured once as a CUDA
+    # graph and replayed: what the GPU takes without the host issuing every call
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            run_stream(torch.cuda.current_stream())
+    torch.cuda.current_stream().wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = 3
+    e0.record(st)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    # the memory update alone: back-to-back calls on a full ring, as a graph
     rk = rxl.rxl_ring(K[0].data_ptr(), B5 * H5, M5, DH, kv * DH, rxl.RXL_DTYPE_BF16, 0, M5)
     for _ in range(10):
         rxl.rxl_mem_update(rk, K[0].data_ptr() + M5 * DH * 2, kv * DH, L5, st)
     torch.cuda.synchronize()
+    g_up = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_up, stream=side):
+            for _ in range(reps_update):
+                rxl.rxl_mem_update(rk, K[0].data_ptr() + M5 * DH * 2, kv * DH, L5, torch.cuda.current_stream())
+    torch.cuda.current_stream().wait_stream(side)
+    g_up.replay()
+    torch.cuda.synchronize()
     e0.record(st)
-    for _ in range(reps_update):
-        rxl.rxl_mem_update(rk, K[0].data_ptr() + M5 * DH * 2, kv * DH, L5, st)
+    g_up.replay()
     e1.record(st)
     torch.cuda.synchronize()
     us = 1e3 * e0.elapsed_time(e1) / reps_update
@@ -394,9 +426,13 @@ def stream_cfg5(segments=32, layers=16, reps_update=200):
     return {"workload": "cfg5_bf16_B4H16_L128M1600_16layer_32seg_fwd", "segments": segments, "layers": layers,
             "ms": ms, "tokens_per_s": B5 * L5 * segments / (ms * 1e-3),
             "attn_tflops": pairs * FLOP_FWD_PAIR / (ms * 1e-3) / 1e12, "gpu_launches": launches,
-            "note": "per segment and layer: K/V current rows copied in (torch), rxl_attn_fwd, 2 x rxl_mem_update"}, \
+            "ms_eager": ms_eager, "tokens_per_s_eager": B5 * L5 * segments / (ms_eager * 1e-3),
+            "note": "per segment and layer: K/V current rows copied in (torch), rxl_attn_fwd, "
+                    "2 x rxl_mem_update; ms = the whole stream captured once as a CUDA graph and "
+                    "replayed, ms_eager = the same calls issued one by one from Python"}, \
            {"kernel": "mem_update_kernel", "bound": "hbm", "unit": "GB/s", "us_per_call": us,
-            "bytes_per_call": bytes_call, "achieved": bytes_call / (us * 1e-6) / 1e9}
+            "bytes_per_call": bytes_call, "achieved": bytes_call / (us * 1e-6) / 1e9,
+            "note": f"{reps_update} back-to-back calls on a full ring, replayed as a CUDA graph"}
 
 
 def reset_cfg3(reps=10):
