@@ -9,6 +9,9 @@
 // 128 x 256 output block with K streamed in 64-wide steps through a 4-stage
 // TMA pipeline (the structure of the projection kernel), then four epilogue
 // warps add the bias, apply ReLU, add the residual and store bf16 rows.
+// With fewer output blocks than half the SMs (few rows: short segments) the
+// K range is split over S CTAs per block: each stores its fp32 partial block
+// and a finalize kernel sums the S partials before bias, ReLU and residual.
 #include <math.h>
 
 #include <mutex>
@@ -35,6 +38,8 @@ __device__ int g_gemm_error;
 struct GemmParams {
   int B, R, K, N;
   int Tr, Tn;  // row tiles per group, 256-column tiles
+  int splits;       // K split over this many CTAs per output block (1: no split)
+  float *partials;  // splits > 1: [splits][B * R][N] fp32 partial sums
   const __nv_bfloat16 *bias;      // [N] or null
   const __nv_bfloat16 *residual;  // [B, R, N] or null
   __nv_bfloat16 *out;             // [B, R, N]
@@ -49,9 +54,11 @@ rxl_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   uint8_t *smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = blockIdx.x % p.Tn;
-  const int rt = (blockIdx.x / p.Tn) % p.Tr;
-  const int b = blockIdx.x / (p.Tn * p.Tr);
+  const int tiles = p.B * p.Tr * p.Tn;
+  const int z = blockIdx.x / tiles, tile = blockIdx.x % tiles;  // K split, output block
+  const int nt = tile % p.Tn;
+  const int rt = (tile / p.Tn) % p.Tr;
+  const int b = tile / (p.Tn * p.Tr);
   const int row0 = rt * 128, nrows = min(128, p.R - row0);
   const int col0 = nt * 256, ncols = min(256, p.N - col0), nbox = (ncols + 63) / 64;
 
@@ -73,21 +80,24 @@ rxl_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nk = p.K / 64;
+  // this CTA's 64-wide k-steps [kb, ke)
+  const int nk_all = p.K / 64;
+  const int kb = z * nk_all / p.splits, ke = (z + 1) * nk_all / p.splits, nk = ke - kb;
 
   if (warp == 4) {
     if (lane == 0) {
       int issued[G_STAGES] = {0, 0, 0, 0};
-      auto load = [&](int kt) {
+      auto load = [&](int kt) {  // kt counts from kb
         const int s = kt % G_STAGES;
+        const int kg = kb + kt;
         const uint32_t a = sb + s * G_STAGE, bb = a + G_A_BYTES;
         mbar_expect_tx(bar_full + 8 * s, G_A_BYTES + nbox * 8192);
-        if (A_HEADS)  // k-step kt is head kt of O [B, H, R, 64]
-          tma_load_4d(a, &tm_a, 0, row0, kt, b, bar_full + 8 * s);
+        if (A_HEADS)  // k-step kg is head kg of O [B, H, R, 64]
+          tma_load_4d(a, &tm_a, 0, row0, kg, b, bar_full + 8 * s);
         else
-          tma_load_3d(a, &tm_a, kt * 64, row0, b, bar_full + 8 * s);
+          tma_load_3d(a, &tm_a, kg * 64, row0, b, bar_full + 8 * s);
         for (int j = 0; j < nbox; ++j)
-          tma_load_3d(bb + j * 8192, &tm_w, col0 + 64 * j, kt * 64, 0, bar_full + 8 * s);
+          tma_load_3d(bb + j * 8192, &tm_w, col0 + 64 * j, kg * 64, 0, bar_full + 8 * s);
         ++issued[s];
       };
       const uint32_t idesc = idesc_bf16(128, 64 * nbox, false, true);
@@ -133,6 +143,14 @@ rxl_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         tmem_ld32(trow + 32 * c, acc);
         tmem_wait_ld();
         if (r >= nrows || 32 * c >= ncols) continue;
+        if (p.splits > 1) {  // this split's fp32 partial; the finalize kernel does the rest
+          float4 *dst = (float4 *)(p.partials + (size_t)z * p.B * p.R * p.N + orow + 32 * c);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(acc[4 * q]), __uint_as_float(acc[4 * q + 1]),
+                                 __uint_as_float(acc[4 * q + 2]), __uint_as_float(acc[4 * q + 3]));
+          continue;
+        }
         float f[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(acc[e]);
@@ -180,6 +198,54 @@ rxl_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   if (warp == 4) tmem_dealloc(tmem, 256);
+}
+
+// Split K: out = act(sum of the partials + bias) + residual, 8 columns per thread.
+__global__ void __launch_bounds__(256) gemm_finalize_kernel(const float *__restrict__ partials, int splits,
+                                                            long long rows, int N,
+                                                            const __nv_bfloat16 *__restrict__ bias, int relu,
+                                                            const __nv_bfloat16 *__restrict__ residual,
+                                                            __nv_bfloat16 *__restrict__ out) {
+  const long long n8 = rows * (N / 8), plane = rows * N;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n8;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long off = e * 8;
+    const int col = (int)(off % N);
+    float f[8];
+    {
+      const float4 a = *(const float4 *)(partials + off), b = *(const float4 *)(partials + off + 4);
+      f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+    for (int zz = 1; zz < splits; ++zz) {
+      const float4 a = *(const float4 *)(partials + zz * plane + off);
+      const float4 b = *(const float4 *)(partials + zz * plane + off + 4);
+      f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w; f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
+    }
+    if (bias) {
+      const uint4 w = *(const uint4 *)(bias + col);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        f[2 * t] += __uint_as_float(ww[t] << 16);
+        f[2 * t + 1] += __uint_as_float(ww[t] & 0xFFFF0000u);
+      }
+    }
+    if (relu) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) f[t] = fmaxf(f[t], 0.f);
+    }
+    if (residual) {
+      const uint4 w = *(const uint4 *)(residual + off);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        f[2 * t] += __uint_as_float(ww[t] << 16);
+        f[2 * t + 1] += __uint_as_float(ww[t] & 0xFFFF0000u);
+      }
+    }
+    *(uint4 *)(out + off) = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                                       pack_bf16(f[6], f[7]));
+  }
 }
 
 // LayerNorm over the last dimension (one warp per row, statistics in fp32):
@@ -276,7 +342,7 @@ bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims
 
 cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_heads, const void *w,
                            const void *bias, const void *residual, bool relu, void *out,
-                           cudaStream_t st, int *launches) {
+                           float *partials, size_t partial_floats, cudaStream_t st, int *launches) {
   CUtensorMap ta, tw;
   bool ok;
   if (a_heads) {  // O [B, K/64, R, 64]
@@ -304,12 +370,37 @@ cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_hea
   p.residual = (const __nv_bfloat16 *)residual;
   p.out = (__nv_bfloat16 *)out;
   p.relu = relu ? 1 : 0;
-  const unsigned grid = (unsigned)((long long)B * p.Tr * p.Tn);
+  const long long tiles = (long long)B * p.Tr * p.Tn;
+  // split K when the blocks fill less than half of the SMs: as many splits as
+  // fit the SMs, at least two k-steps each, at most 8, within the partial budget
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long per_split = (long long)B * R * N;
+  long long S = 1;
+  if (partials && 2 * tiles <= sms) {
+    S = sms / tiles;
+    if (S > K / 128) S = K / 128;
+    if (S > 8) S = 8;
+    if (S > (long long)(partial_floats / per_split)) S = (long long)(partial_floats / per_split);
+    if (S < 2) S = 1;
+  }
+  p.splits = (int)S;
+  p.partials = partials;
+  const unsigned grid = (unsigned)(tiles * S);
   if (a_heads)
     rxl_gemm_kernel<true><<<grid, G_THREADS, G_SMEM, st>>>(ta, tw, p);
   else
     rxl_gemm_kernel<false><<<grid, G_THREADS, G_SMEM, st>>>(ta, tw, p);
   ++*launches;
+  if (S > 1) {
+    long long blocks = (per_split / 8 + 255) / 256;
+    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+    gemm_finalize_kernel<<<(unsigned)blocks, 256, 0, st>>>(partials, (int)S, (long long)B * R, N,
+                                                          (const __nv_bfloat16 *)bias, relu ? 1 : 0,
+                                                          (const __nv_bfloat16 *)residual, (__nv_bfloat16 *)out);
+    ++*launches;
+  }
   return cudaGetLastError();
 }
 

@@ -81,7 +81,7 @@ int rxl_device_error_flags(void) {
 
 namespace {
 struct LayerWs {
-  size_t q, k, v, o, lse, x1, x1n, z, x2, total;
+  size_t q, k, v, o, lse, x1, x1n, z, x2, part, part_floats, total;
 };
 size_t up256_(size_t x) { return (x + 255) & ~(size_t)255; }
 LayerWs layer_ws(const rxl::AttnShape &s, int d, int dff) {
@@ -96,7 +96,11 @@ LayerWs layer_ws(const rxl::AttnShape &s, int d, int dff) {
   w.x1n = w.x1 + up256_(rows * d * 2);
   w.z = w.x1n + up256_(rows * d * 2);
   w.x2 = w.z + up256_(rows * dff * 2);
-  w.total = w.x2 + up256_(rows * d * 2);
+  // fp32 partial sums of the dense layers when their K range is split
+  // (short segments): up to 8 splits of a [rows][d] output
+  w.part = w.x2 + up256_(rows * d * 2);
+  w.part_floats = rows * 8 * (size_t)d;
+  w.total = w.part + up256_(w.part_floats * 4);
   return w;
 }
 rxl_status check_layer(const rxl_attn_desc *desc, int d, int dff, rxl::AttnShape *s) {
@@ -133,6 +137,7 @@ rxl_status rxl_layer_fwd(const rxl_attn_desc *desc, int d_model, int d_ff, const
   void *q = ws + lw.q, *k = ws + lw.k, *v = ws + lw.v, *o = ws + lw.o;
   float *lse = (float *)(ws + lw.lse);
   void *x1 = ws + lw.x1, *x1n = ws + lw.x1n, *z = ws + lw.z, *x2 = ws + lw.x2;
+  float *part = (float *)(ws + lw.part);
   cudaStream_t cs = (cudaStream_t)stream;
   const long long rows = (long long)s.B * s.L;
   int launches = 0;
@@ -142,15 +147,15 @@ rxl_status rxl_layer_fwd(const rxl_attn_desc *desc, int d_model, int d_ff, const
     e = rxl::launch_tc_fwd(s, q, k, v, w->r, w->u, w->vbias, o, nullptr, lse, cs, &launches);
   if (e == cudaSuccess)  // x1 = h + attention . W_O (heads merged by the A operand's layout)
     e = rxl::launch_tc_gemm(s.B, s.L, s.H * 64, d_model, o, true, w->w_o, nullptr, h_in, false, x1,
-                            cs, &launches);
+                            part, lw.part_floats, cs, &launches);
   if (e == cudaSuccess)
     e = rxl::launch_layernorm(x1, w->ln1_gamma, w->ln1_beta, x1n, rows, d_model, 1e-5f, cs, &launches);
   if (e == cudaSuccess)  // z = ReLU(x1n . W_1 + b_1)
-    e = rxl::launch_tc_gemm(s.B, s.L, d_model, d_ff, x1n, false, w->w_1, w->b_1, nullptr, true, z, cs,
-                            &launches);
+    e = rxl::launch_tc_gemm(s.B, s.L, d_model, d_ff, x1n, false, w->w_1, w->b_1, nullptr, true, z,
+                            part, lw.part_floats, cs, &launches);
   if (e == cudaSuccess)  // x2 = x1n + z . W_2 + b_2
-    e = rxl::launch_tc_gemm(s.B, s.L, d_ff, d_model, z, false, w->w_2, w->b_2, x1n, false, x2, cs,
-                            &launches);
+    e = rxl::launch_tc_gemm(s.B, s.L, d_ff, d_model, z, false, w->w_2, w->b_2, x1n, false, x2,
+                            part, lw.part_floats, cs, &launches);
   if (e == cudaSuccess)
     e = rxl::launch_layernorm(x2, w->ln2_gamma, w->ln2_beta, h_out, rows, d_model, 1e-5f, cs, &launches);
   g_last_launches = launches;
