@@ -9,8 +9,8 @@
 // 128 x 256 output block with K streamed in 64-wide steps through a 4-stage
 // TMA pipeline (the structure of the projection kernel), then four epilogue
 // warps add the bias, apply ReLU, add the residual and store bf16 rows.
-// With fewer output blocks than half the SMs (few rows: short segments) the
-// K range is split over S CTAs per block: each stores its fp32 partial block
+// With at most a quarter as many output blocks as SMs (few rows: short
+// segments) the K range is split over S CTAs per block: each stores its fp32 partial block
 // and a finalize kernel sums the S partials before bias, ReLU and residual.
 #include <math.h>
 
@@ -216,7 +216,9 @@ __global__ void __launch_bounds__(256) gemm_finalize_kernel(const float *__restr
       const float4 a = *(const float4 *)(partials + off), b = *(const float4 *)(partials + off + 4);
       f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
     }
-    for (int zz = 1; zz < splits; ++zz) {
+#pragma unroll
+    for (int zz = 1; zz < 8; ++zz) {  // splits <= 8: every load of the row group in flight at once
+      if (zz >= splits) break;
       const float4 a = *(const float4 *)(partials + zz * plane + off);
       const float4 b = *(const float4 *)(partials + zz * plane + off + 4);
       f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w; f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
@@ -371,19 +373,20 @@ cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_hea
   p.out = (__nv_bfloat16 *)out;
   p.relu = relu ? 1 : 0;
   const long long tiles = (long long)B * p.Tr * p.Tn;
-  // split K when the blocks fill less than half of the SMs: as many splits as
-  // fit the SMs, at least two k-steps each, at most 8, within the partial budget
+  // split K when the blocks fill at most a quarter of the SMs: as many
+  // splits as fit the SMs, at least two k-steps each, at most 8, within the
+  // partial budget; fewer than 4 splits do not repay the finalize pass
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long per_split = (long long)B * R * N;
   long long S = 1;
-  if (partials && 2 * tiles <= sms) {
+  if (partials && 4 * tiles <= sms) {
     S = sms / tiles;
     if (S > K / 128) S = K / 128;
     if (S > 8) S = 8;
     if (S > (long long)(partial_floats / per_split)) S = (long long)(partial_floats / per_split);
-    if (S < 2) S = 1;
+    if (S < 4) S = 1;
   }
   p.splits = (int)S;
   p.partials = partials;
