@@ -75,8 +75,9 @@ constexpr uint32_t SM_V = 65536;               // 2 stages x 16 KB
 constexpr uint32_t SM_R = 98304;               // 2 stages x 32 KB
 constexpr uint32_t SM_P = 163840;              // 2 x [128][64] bf16 (keys 0-63, 64-127)
 constexpr uint32_t SM_BAR = 196608;            // mbarriers, TMEM slot, abort flag
-constexpr uint32_t SM_X = SM_BAR + 128;        // row-half exchange: [2][2][128] floats
-constexpr uint32_t SMEM_BYTES = SM_X + 2048 + 1024;  // + alignment slack
+constexpr uint32_t SM_X = SM_BAR + 256;        // row-half exchange: [2][2][128] floats
+constexpr uint32_t SM_QRAW = 199680;           // the next item's Q rows [128][64] bf16 (TMA, sw128)
+constexpr uint32_t SMEM_BYTES = SM_QRAW + 16384 + 1024;  // + alignment slack
 constexpr float kRescaleThreshold = 8.f;       // log2 units
 constexpr uint32_t STAGE_TX = 16384 + 16384 + 32768;
 // O accumulators: keys 0-63 of every tile into TM_O, keys 64-127 into TM_O + 64
@@ -198,21 +199,24 @@ struct Cursor {
 };
 
 // (Q+u)*c and (Q+v)*c in bf16, c = scale*log2(e), as 128-byte swizzled
-// K-major tiles for the item's query rows; the row's two warps split its 8
-// chunks. In kPrep mode the unscaled rows also go to global memory ((Q+v) in fp16).
+// K-major tiles for the item's query rows, from the raw Q tile the producer
+// loaded ahead; the row's two warps split its 8 chunks. In kPrep mode the unscaled rows also go to global memory ((Q+v) in fp16).
 template <int MODE>
 __device__ __forceinline__ void q_prep(const Params &p, const Item &it, uint32_t sbase, int quad,
                                        int hf, int lane) {
   const int ii = quad * 32 + lane;
   const int i = it.i0 + ii;
   const float c2 = p.scale_log2;
-  const uint4 *qrow = (const uint4 *)(p.q + ((size_t)it.bh * p.L + (i < p.L ? i : 0)) * DH);
   const uint4 *urow = (const uint4 *)(p.u + (size_t)it.h * DH);
   const uint4 *vrow = (const uint4 *)(p.vb + (size_t)it.h * DH);
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
     const int c = 4 * hf + cc;
-    uint4 qv4 = i < p.L ? qrow[c] : make_uint4(0, 0, 0, 0);
+    // the raw Q rows were loaded by TMA (rows past L read as zero)
+    uint4 qv4;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(qv4.x), "=r"(qv4.y), "=r"(qv4.z), "=r"(qv4.w)
+                 : "r"(sbase + SM_QRAW + sw128_offset(ii, c)));
     const uint4 u4 = urow[c], v4 = vrow[c];
     const uint32_t qw[4] = {qv4.x, qv4.y, qv4.z, qv4.w};
     const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
@@ -244,7 +248,8 @@ __device__ __forceinline__ void q_prep(const Params &p, const Item &it, uint32_t
 template <int MODE, bool RESET, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_r, const Params p, int nitems) {
+                  const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_q,
+                  const Params p, int nitems) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = tc::align1024(smem_raw);
   const uint32_t sbase = smem_u32(smem);
@@ -263,6 +268,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   // SPLIT: rank 0's K/V stages are free for rank 1's half (rank 1, count 1);
   // rank 1's half has landed in them (rank 0, count 256)
   const uint32_t bar_peer = b0 + 112, bar_data = b0 + 120;
+  const uint32_t bar_q = b0 + 128;  // TMA: the raw Q rows of the next item
   uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 104);
   volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 108);
   volatile float *xbuf = (volatile float *)(smem + SM_X);
@@ -277,6 +283,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     mbar_init(bar_qready, kSoftmaxWarps * 32);
     mbar_init(bar_ofree, kSoftmaxWarps * 32);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_q, 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     if (SPLIT) {
       mbar_init(bar_peer, 1);
@@ -293,6 +300,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_r);
+      tma_prefetch_desc(&tm_q);
     }
   }
   tc_fence_before();
@@ -343,14 +351,35 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         pending[s] = false;
         return r;
       };
+      // the raw Q rows of this CTA's item k (round k of the item order)
+      int nq_loads = 0;
+      auto load_q = [&](int k) {
+        int w;
+        if (SPLIT) {
+          if (k > 0) return;
+          w = (int)(blockIdx.x >> 1);
+        } else {
+          const int G = gridDim.x, c = blockIdx.x;
+          w = k * G + ((k & 1) ? G - 1 - c : c);
+        }
+        if (w >= nitems) return;
+        const Item qi = item_at<RESET>(p, w);
+        mbar_expect_tx(bar_q, 16384);
+        tma_load_3d(sbase + SM_QRAW, &tm_q, 0, qi.i0, qi.bh, bar_q);
+        ++nq_loads;
+      };
       bool ok = true;
       Cursor<RESET, SPLIT> mc;  // tile whose P.V is next
       mc.init(p, nitems);
+      if (mc.valid) load_q(0);
       if (tc_.valid) issue_tma();
       if (tc_.valid) issue_tma();
       if (mc.valid) {
         ok = mbar_wait(bar_qready, 0, abort_flag) && wait_full(0);
-        if (ok) issue_sg(0);
+        if (ok) {
+          load_q(1);  // the softmax has read item 0's raw rows
+          issue_sg(0);
+        }
       }
       for (int g = 0; ok && mc.valid; ++g) {
         Cursor<RESET, SPLIT> nx = mc;
@@ -380,6 +409,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           if (!(ok = mbar_wait(bar_sgfree, g & 1, abort_flag) &&
                      mbar_wait(bar_qready, nx.k & 1, abort_flag) && wait_full(g + 1)))
             break;
+          load_q(nx.k + 1);  // the softmax has read item nx.k's raw rows
           tc_fence_after();
           issue_sg(g + 1);
         }
@@ -396,6 +426,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         volatile int no_abort = 0;
         for (int s = 0; s < 2; ++s)
           if (pending[s]) mbar_wait(s ? bar_full1 : bar_full0, (nissued[s] - 1) & 1, &no_abort);
+        if (nq_loads > 0) mbar_wait(bar_q, (nq_loads - 1) & 1, &no_abort);
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0, &no_abort);
         atomicExch(&g_fwd_error, 1);
@@ -415,9 +446,14 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     Cursor<RESET, SPLIT> cur;
     cur.init(p, nitems);
     if (cur.valid) {
-      q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
-      fence_proxy_async_smem();
-      mbar_arrive(bar_qready);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag));
+      if (ok) {
+        q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
+        fence_proxy_async_smem();
+        mbar_arrive(bar_qready);
+      } else {
+        cur.valid = false;
+      }
     }
     for (int g = 0; cur.valid; ++g) {
       const Item it = cur.it;
@@ -529,6 +565,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       // ---- last tile of the item: Q tiles of the next item, then epilogue
       if (cur.valid) {
         // the S/G MMAs of this item are all done (bar_sg waited above)
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_q, cur.k & 1, abort_flag)))) break;
         q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
         fence_proxy_async_smem();
         mbar_arrive(bar_qready);
@@ -695,9 +732,9 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
                         const void *r, const void *u, const void *vb, void *o, void *o_lo, float *lse,
                         const void *dout, float *delta, void *qu_out, void *qv_out,
                         cudaStream_t st, int *launches) {
-  CUtensorMap tk, tv, tr;
+  CUtensorMap tk, tv, tr, tq;
   if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
-      !make_map(&tr, r, s.H, s.kv_rows, NB))
+      !make_map(&tr, r, s.H, s.kv_rows, NB) || !make_map(&tq, q, s.B * s.H, s.L, BQ))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -739,16 +776,16 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = s.mvis ? cudaLaunchKernelEx(&cfg, rxl_fwd_tc_kernel<MODE, true, true>, tk, tv, tr, p, nitems)
-                           : cudaLaunchKernelEx(&cfg, rxl_fwd_tc_kernel<MODE, false, true>, tk, tv, tr, p, nitems);
+    cudaError_t e = s.mvis ? cudaLaunchKernelEx(&cfg, rxl_fwd_tc_kernel<MODE, true, true>, tk, tv, tr, tq, p, nitems)
+                           : cudaLaunchKernelEx(&cfg, rxl_fwd_tc_kernel<MODE, false, true>, tk, tv, tr, tq, p, nitems);
     ++*launches;
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   const unsigned grid = (unsigned)(nitems < sms ? nitems : sms);
   if (s.mvis)
-    rxl_fwd_tc_kernel<MODE, true, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
+    rxl_fwd_tc_kernel<MODE, true, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, tq, p, nitems);
   else
-    rxl_fwd_tc_kernel<MODE, false, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, p, nitems);
+    rxl_fwd_tc_kernel<MODE, false, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, tq, p, nitems);
   ++*launches;
   return cudaGetLastError();
 }
