@@ -62,7 +62,7 @@ using tc::NB;
 using tc::KeyTile;
 using tc::KeyTiles;
 using tc::RowMemory;
-using tc::lane_shift_window;
+using tc::lane_shift_window96;
 using tc::row_memory;
 
 constexpr int kSoftmaxWarps = 8;
@@ -467,41 +467,55 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       tc_fence_after();
       const KeyTile x = KeyTiles(it.m, p.cap, it.head, min(it.i0 + BQ, p.L)).get(t);
       float y[64];
+      {
+        // One 96-column window of G serves both 32-key chunks of this half:
+        // chunk 2hf reads columns W .. W+63 and chunk 2hf+1 columns W-32 ..
+        // W+31 (W = 32 quad + 96 - 64 hf). Shifted left by the lane, the
+        // keys 32 c + k sit at win[63 - k] (c = 2hf) and win[31 - k] (2hf+1).
+        float win[96];
+        {
+          uint32_t w0[32], w1[32], w2[32];
+          const uint32_t gcol = TM_G + 32 * quad + 64 - 64 * hf;
+          tmem_ld32(trow + gcol, w0);
+          tmem_ld32(trow + gcol + 32, w1);
+          tmem_ld32(trow + gcol + 64, w2);
+          tmem_wait_ld();
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * hf + cc;
-        uint32_t sr[32], w0[32], w1[32];
-        tmem_ld32(trow + TM_S + 32 * c, sr);
-        const uint32_t gcol = TM_G + 32 * quad + 96 - 32 * c;
-        tmem_ld32(trow + gcol, w0);
-        tmem_ld32(trow + gcol + 32, w1);
+          for (int e = 0; e < 32; ++e) {
+            win[e] = __uint_as_float(w0[e]);
+            win[32 + e] = __uint_as_float(w1[e]);
+            win[64 + e] = __uint_as_float(w2[e]);
+          }
+        }
+        lane_shift_window96(win, lane);  // win[x] <- win[x + lane]
+        uint32_t s0[32], s1[32];
+        tmem_ld32(trow + TM_S + 64 * hf, s0);
+        tmem_ld32(trow + TM_S + 64 * hf + 32, s1);
         tmem_wait_ld();
-        if (cc == 1) {
-          // done reading S and G: the next tile's S/G MMAs may start
-          tc_fence_before();
-          mbar_arrive(bar_sgfree);
-        }
-        float win[64];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          win[e] = __uint_as_float(w0[e]);
-          win[32 + e] = __uint_as_float(w1[e]);
-        }
-        lane_shift_window(win, lane);  // win[x] <- win[x + lane]
-        // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i;
-        // the warp skips the mask where all 32 keys are visible to all its rows
-        const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
+        // done reading S and G: the next tile's S/G MMAs may start
+        tc_fence_before();
+        mbar_arrive(bar_sgfree);
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          const float2 a = __fadd2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])),
-                                      make_float2(win[31 - k], win[30 - k]));
-          y[32 * cc + k] = a.x;
-          y[32 * cc + k + 1] = a.y;
+          const float2 a0 = __fadd2_rn(make_float2(__uint_as_float(s0[k]), __uint_as_float(s0[k + 1])),
+                                       make_float2(win[63 - k], win[62 - k]));
+          const float2 a1 = __fadd2_rn(make_float2(__uint_as_float(s1[k]), __uint_as_float(s1[k + 1])),
+                                       make_float2(win[31 - k], win[30 - k]));
+          y[k] = a0.x;
+          y[k + 1] = a0.y;
+          y[32 + k] = a1.x;
+          y[32 + k + 1] = a1.y;
         }
-        if (!__all_sync(0xffffffffu, lim >= 31)) {
+        // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i;
+        // the warp skips the mask where all 32 keys are visible to all its rows
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (k > lim) y[32 * cc + k] = -INFINITY;
+        for (int cc = 0; cc < 2; ++cc) {
+          const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * (2 * hf + cc);
+          if (!__all_sync(0xffffffffu, lim >= 31)) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (k > lim) y[32 * cc + k] = -INFINITY;
+          }
         }
       }
       float mt = -INFINITY;

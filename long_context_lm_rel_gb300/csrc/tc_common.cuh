@@ -93,6 +93,19 @@ __device__ __forceinline__ void lane_shift_window(float (&win)[64], int lane) {
   }
 }
 
+// The same over a 96-value window, keeping 64 results: win[x] <- win[x +
+// lane] for x = 0..63 (one window serving two adjacent 32-key chunks).
+__device__ __forceinline__ void lane_shift_window96(float (&win)[96], int lane) {
+#pragma unroll
+  for (int b = 4; b >= 0; --b) {
+    const int sh = 1 << b;
+    const bool take = (lane >> b) & 1;
+#pragma unroll
+    for (int e = 0; e < 95; ++e)
+      if (e < 64 + sh - 1) win[e] = take ? win[e + sh] : win[e];
+  }
+}
+
 // Base-2 exponents of P for half a 128x128 tile, two warps per TMEM lane
 // quadrant: the calling thread (quadrant `quad`, half `hf`) produces, for
 // keys jj = 64*hf + k (k = 0..63) of its row ii = 32*quad + lane,
