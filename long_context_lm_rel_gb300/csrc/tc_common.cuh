@@ -79,22 +79,10 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
-// win[x] <- win[x + lane] for x = 0..31: a 63-value window shifted left by
-// the lane index in 5 predicated stages, largest shift first (selects; the
-// same stages as t*a + (1-t)*b on the FMA pipe measured slower).
-__device__ __forceinline__ void lane_shift_window(float (&win)[64], int lane) {
-#pragma unroll
-  for (int b = 4; b >= 0; --b) {
-    const int sh = 1 << b;
-    const bool take = (lane >> b) & 1;
-#pragma unroll
-    for (int e = 0; e < 63; ++e)
-      if (e < 32 + sh - 1) win[e] = take ? win[e + sh] : win[e];
-  }
-}
-
-// The same over a 96-value window, keeping 64 results: win[x] <- win[x +
-// lane] for x = 0..63 (one window serving two adjacent 32-key chunks).
+// win[x] <- win[x + lane] for x = 0..63: a 96-value window (serving two
+// adjacent 32-key chunks) shifted left by the lane index in 5 predicated
+// stages, largest shift first (selects; the same stages as t*a + (1-t)*b on
+// the FMA pipe measured slower).
 __device__ __forceinline__ void lane_shift_window96(float (&win)[96], int lane) {
 #pragma unroll
   for (int b = 4; b >= 0; --b) {
@@ -109,40 +97,54 @@ __device__ __forceinline__ void lane_shift_window96(float (&win)[96], int lane) 
 // Base-2 exponents of P for half a 128x128 tile, two warps per TMEM lane
 // quadrant: the calling thread (quadrant `quad`, half `hf`) produces, for
 // keys jj = 64*hf + k (k = 0..63) of its row ii = 32*quad + lane,
-// y[k] = (S + G_skewed) * scale + bias, -inf where masked. Pairs of keys go
-// through the packed fp32x2 add and fma.
+// y[k] = (S + G_skewed) * scale + bias, -inf where masked. One 96-column G
+// window serves both 32-key chunks of the half: chunk 2hf reads columns W ..
+// W+63 and chunk 2hf+1 columns W-32 .. W+31 (W = 32 quad + 96 - 64 hf), so
+// after the lane shift keys 32c + k sit at win[63 - k] (c = 2hf) and
+// win[31 - k] (c = 2hf+1). Pairs of keys go through the packed fp32x2 add
+// and fma.
 __device__ __forceinline__ void half_tile_exponents(uint32_t trow, uint32_t s_col, uint32_t g_col,
                                                     int quad, int lane, int hf, int i,
                                                     const KeyTile &x, float scale, float bias,
                                                     float (&y)[64]) {
   const float2 scale2 = make_float2(scale, scale), bias2 = make_float2(bias, bias);
-#pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {
-    const int c = 2 * hf + cc;
-    uint32_t sr[32], w0[32], w1[32];
-    tmem_ld32(trow + s_col + 32 * c, sr);
-    const uint32_t gcol = g_col + 32 * quad + 96 - 32 * c;
+  float win[96];
+  {
+    uint32_t w0[32], w1[32], w2[32];
+    const uint32_t gcol = g_col + 32 * quad + 64 - 64 * hf;
     tmem_ld32(trow + gcol, w0);
     tmem_ld32(trow + gcol + 32, w1);
+    tmem_ld32(trow + gcol + 64, w2);
     tmem_wait_ld();
-    float win[64];
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       win[e] = __uint_as_float(w0[e]);
       win[32 + e] = __uint_as_float(w1[e]);
+      win[64 + e] = __uint_as_float(w2[e]);
     }
-    lane_shift_window(win, lane);
+  }
+  lane_shift_window96(win, lane);
+  uint32_t s0[32], s1[32];
+  tmem_ld32(trow + s_col + 64 * hf, s0);
+  tmem_ld32(trow + s_col + 64 * hf + 32, s1);
+  tmem_wait_ld();
 #pragma unroll
-    for (int k = 0; k < 32; k += 2) {
-      const float2 a = __fadd2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])),
-                                  make_float2(win[31 - k], win[30 - k]));
-      const float2 t = __ffma2_rn(a, scale2, bias2);
-      y[32 * cc + k] = t.x;
-      y[32 * cc + k + 1] = t.y;
-    }
-    // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i; the
-    // warp skips the mask where all 32 keys are visible to all its rows
-    const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * c;
+  for (int k = 0; k < 32; k += 2) {
+    const float2 a0 = __fadd2_rn(make_float2(__uint_as_float(s0[k]), __uint_as_float(s0[k + 1])),
+                                 make_float2(win[63 - k], win[62 - k]));
+    const float2 a1 = __fadd2_rn(make_float2(__uint_as_float(s1[k]), __uint_as_float(s1[k + 1])),
+                                 make_float2(win[31 - k], win[30 - k]));
+    const float2 t0 = __ffma2_rn(a0, scale2, bias2), t1 = __ffma2_rn(a1, scale2, bias2);
+    y[k] = t0.x;
+    y[k + 1] = t0.y;
+    y[32 + k] = t1.x;
+    y[32 + k + 1] = t1.y;
+  }
+  // key jj = 32c + k is visible iff jj < nvalid and jlog0 + jj <= i; the
+  // warp skips the mask where all 32 keys are visible to all its rows
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int lim = min(x.nvalid - 1, i - x.jlog0) - 32 * (2 * hf + cc);
     if (!__all_sync(0xffffffffu, lim >= 31)) {
 #pragma unroll
       for (int k = 0; k < 32; ++k)
