@@ -526,9 +526,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const uint32_t xrow = sb + F_X + ii * 16;
         // columns outside [ii, ii + 127] are zero (staging overwrote them)
         if (hf == 1) {
+#pragma unroll
           for (int C = 0; C < 15; ++C)
             if (C < c0) st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384, 0, 0, 0, 0);
         } else {
+#pragma unroll
           for (int C = 17; C < 32; ++C)
             if (C > c0 + 16) st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384, 0, 0, 0, 0);
         }
@@ -625,11 +627,21 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
         for (int h2 = 16; h2 >= 1; h2 >>= 1) {
           const bool upper = (lane & h2) != 0;
+          if (h2 == 1) {
+            const float send = upper ? v[0] : v[1];
+            const float keep = upper ? v[1] : v[0];
+            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+          } else {
 #pragma unroll
-          for (int k = 0; k < h2; ++k) {
-            const float send = upper ? v[k] : v[k + h2];
-            const float keep = upper ? v[k + h2] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, h2);
+            for (int k = 0; k < h2; k += 2) {  // pairs of columns through the packed add
+              const float s0 = upper ? v[k] : v[k + h2], s1 = upper ? v[k + 1] : v[k + 1 + h2];
+              const float k0 = upper ? v[k + h2] : v[k], k1 = upper ? v[k + 1 + h2] : v[k + 1];
+              const float2 t = __fadd2_rn(make_float2(k0, k1),
+                                          make_float2(__shfl_xor_sync(0xffffffffu, s0, h2),
+                                                      __shfl_xor_sync(0xffffffffu, s1, h2)));
+              v[k] = t.x;
+              v[k + 1] = t.y;
+            }
           }
         }
         dvp += v[0];
