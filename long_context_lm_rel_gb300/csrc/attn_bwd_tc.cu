@@ -9,7 +9,9 @@
 //   du   = sum dA_ij k_j               dv   = sum dA_ij r_{i-j}
 //
 // One pass over the visible (query tile, key tile) pairs computes every
-// gradient; the logits are formed once per pair.
+// gradient; the logits are formed once per pair. Internally the softmax
+// carries scale * P (log2(scale) folded into the exponent), so dA is one
+// product away and dV is divided by scale once per item.
 //
 // Kernels (all on the caller's stream):
 //   zero   : dR, the fp32 dQ accumulator and the du/dv sums <- 0; dK/dV rows
@@ -414,6 +416,10 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const uint32_t row_dr = sw128_row(sb + F_DG + 2 * hf * 16384, ii);
     uint32_t xphase = 0;
     float dvp = 0.f;  // sum over this warp's rows of dQp, column 32*hf + lane
+    // the exponent bias carries log2(scale): the softmax handles scale * P
+    // throughout (dA = (scale P)(dP - D) in two packed ops); the P tile of
+    // the dV product holds scale * P, so dV is divided by scale at the end
+    const float log2_scale = log2f(p.scale), inv_scale = 1.f / p.scale;
     bool ok = true;
     PairCursor c;
     c.init(p);
@@ -441,9 +447,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
       }
       float y[64];
-      half_tile_exponents(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, -lse2, y);
+      half_tile_exponents(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, log2_scale - lse2, y);
 #pragma unroll
-      for (int k = 0; k < 64; ++k) y[k] = ex2(y[k]);  // P
+      for (int k = 0; k < 64; ++k) y[k] = ex2(y[k]);  // scale * P
       // the P/dA buffer held the previous pair's dQ staging
       if (g > 0) {
         ok = mbar_wait(bar_sfree, (g - 1) & 1, abort_flag);
@@ -461,11 +467,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         uint32_t dp[32];
         tmem_ld32(trow + TM_S + 64 * hf + 32 * cc, dp);
         tmem_wait_ld();
-        const float2 scale2 = make_float2(p.scale, p.scale), ndi2 = make_float2(-Di, -Di);
+        const float2 ndi2 = make_float2(-Di, -Di);
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {  // dA (P = 0 and finite dP off the allowed pairs)
           const float2 d = __fadd2_rn(make_float2(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])), ndi2);
-          const float2 t = __fmul2_rn(__fmul2_rn(make_float2(y[32 * cc + k], y[32 * cc + k + 1]), scale2), d);
+          const float2 t = __fmul2_rn(make_float2(y[32 * cc + k], y[32 * cc + k + 1]), d);
           y[32 * cc + k] = t.x;
           y[32 * cc + k + 1] = t.y;
         }
@@ -660,18 +666,18 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         tc_fence_before();
         mbar_arrive(bar_acc);
         if (kk < it.x.nvalid) {
+          const float gs = hf ? 1.f : inv_scale;  // dV accumulated (scale P)^T dO
+          auto f = [&](const uint32_t(&a)[32], int e) { return __uint_as_float(a[e]) * gs; };
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            ((uint4 *)dst)[e] = make_uint4(
-                pack_bf16(__uint_as_float(ga[8 * e + 0]), __uint_as_float(ga[8 * e + 1])),
-                pack_bf16(__uint_as_float(ga[8 * e + 2]), __uint_as_float(ga[8 * e + 3])),
-                pack_bf16(__uint_as_float(ga[8 * e + 4]), __uint_as_float(ga[8 * e + 5])),
-                pack_bf16(__uint_as_float(ga[8 * e + 6]), __uint_as_float(ga[8 * e + 7])));
-            ((uint4 *)dst)[4 + e] = make_uint4(
-                pack_bf16(__uint_as_float(gb[8 * e + 0]), __uint_as_float(gb[8 * e + 1])),
-                pack_bf16(__uint_as_float(gb[8 * e + 2]), __uint_as_float(gb[8 * e + 3])),
-                pack_bf16(__uint_as_float(gb[8 * e + 4]), __uint_as_float(gb[8 * e + 5])),
-                pack_bf16(__uint_as_float(gb[8 * e + 6]), __uint_as_float(gb[8 * e + 7])));
+            ((uint4 *)dst)[e] = make_uint4(pack_bf16(f(ga, 8 * e + 0), f(ga, 8 * e + 1)),
+                                           pack_bf16(f(ga, 8 * e + 2), f(ga, 8 * e + 3)),
+                                           pack_bf16(f(ga, 8 * e + 4), f(ga, 8 * e + 5)),
+                                           pack_bf16(f(ga, 8 * e + 6), f(ga, 8 * e + 7)));
+            ((uint4 *)dst)[4 + e] = make_uint4(pack_bf16(f(gb, 8 * e + 0), f(gb, 8 * e + 1)),
+                                               pack_bf16(f(gb, 8 * e + 2), f(gb, 8 * e + 3)),
+                                               pack_bf16(f(gb, 8 * e + 4), f(gb, 8 * e + 5)),
+                                               pack_bf16(f(gb, 8 * e + 6), f(gb, 8 * e + 7)));
           }
         }
         atomicAdd(p.dv_acc + it.h * DH + 32 * hf + lane, dvp);
