@@ -242,7 +242,10 @@ rxl_status rxl_qkv_proj(const rxl_attn_desc *desc, int d_model, const void *h_me
  * [d_ff]; w_2 [d_ff, d], b_2 [d]; ln*_gamma, ln*_beta [d].
  *   h_mem  [B, M, d] the layer's hidden-state memory ring (as in rxl_qkv_proj)
  *   h_in   [B, L, d] the layer's input; h_out [B, L, d] written
- *   workspace  rxl_layer_fwd_workspace_bytes(desc, d_model, d_ff) bytes
+ *   workspace  rxl_layer_fwd_workspace_bytes(desc, d_model, d_ff) bytes:
+ *              projected Q/K/V, the attention output, the sublayer
+ *              intermediates and fp32 partial sums of the dense layers (when
+ *              few output blocks split their K range over several CTAs)
  * The caller advances the memory afterwards with rxl_mem_update(ring over
  * h_mem with D = d, src = h_in): the layer's input states are what the next
  * segment's layer attends to (eq. Tail_M). bf16 only; d_model a multiple of
