@@ -495,7 +495,17 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       am = 0.f;
 #pragma unroll
       for (int w = 0; w < kSoftmaxWarps; ++w) am = fmaxf(am, wmax[(g & 1) * 8 + w]);
-      const float sig = am > 0.f ? exp2f(14.f - ceilf(log2f(am))) : 1.f;  // max |sig dA| <= 2^14
+      // sig = 2^(14 - ceil(log2 max|dA|)), so max |sig dA| <= 2^14, and
+      // inv = 1/sig, both read off the exponent bits of max|dA| (1 for 0)
+      float sig, inv;
+      {
+        const uint32_t ab = __float_as_uint(am);
+        int ce = (int)(ab >> 23) - 127 + ((ab & 0x7FFFFFu) != 0u);  // ceil(log2 am), am normal
+        int e = am > 0.f ? 14 - ce : 0;
+        e = e < -126 ? -126 : (e > 126 ? 126 : e);
+        sig = __uint_as_float((uint32_t)(e + 127) << 23);
+        inv = __uint_as_float((uint32_t)(127 - e) << 23);
+      }
       // the dG buffer held the previous pair's dR staging
       if (g > 0) {
         ok = mbar_wait(bar_gfree, (g - 1) & 1, abort_flag);
@@ -580,7 +590,6 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         // flush: this half's 32 dQ columns of row ii and row ii of dR block
         // hf, staged in fp32 (128-byte swizzled 32-column boxes) in the P/dA
         // and dG buffers, then added into the accumulators by TMA
-        const float inv = 1.f / sig;
         float v[32];
         {
           uint32_t qc[32], qp[32];
