@@ -40,9 +40,9 @@ B, H, L, M, DH = 16, 16, 512, 512, 64
 SCALE = 1.0 / math.sqrt(DH)
 FLOP_FWD_PAIR, FLOP_BWD_PAIR = 6 * DH, 12 * DH
 # dram__bytes_read.sum + dram__bytes_write.sum of one rxl_bwd_main_kernel
-# launch at cfg3: 45.12 MB measured by ncu at B=4, times 4 (the work items
+# launch at cfg3: 45.15 MB measured by ncu at B=4, times 4 (the work items
 # scale with the batch)
-TRAFFIC_BWD_MAIN = 4 * 45.12e6
+TRAFFIC_BWD_MAIN = 4 * 45.15e6
 
 
 def visible_pairs(b, h, l, m):
