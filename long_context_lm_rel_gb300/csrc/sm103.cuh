@@ -75,11 +75,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 
 // ----------------------------------------------------- thread-block clusters
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 // All threads of every CTA of the cluster (once, right after the barriers of
 // each CTA are initialised: the CTAs of a cluster start together).
 __device__ __forceinline__ void cluster_sync() {
