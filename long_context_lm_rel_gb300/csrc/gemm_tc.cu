@@ -113,9 +113,14 @@ rxl_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
           mma_bf16(tmem, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bb + k * 2048, 8192, 1024), idesc,
                    (kt > 0 || k > 0) ? 1u : 0u);
         mma_commit(bar_empty + 8 * s);
-        if (kt + G_STAGES < nk) {
-          if (!(ok = mbar_wait(bar_empty + 8 * s, (kt / G_STAGES) & 1, abort_flag))) break;
-          load(kt + G_STAGES);
+        // refill the previous k-step's stage once its MMAs are done: they
+        // finish while this step's are queued, so the tensor pipe does not
+        // run dry during the wait
+        const int kp = kt - 1;
+        if (kp >= 0 && kp + G_STAGES < nk) {
+          const int sp = kp % G_STAGES;
+          if (!(ok = mbar_wait(bar_empty + 8 * sp, (kp / G_STAGES) & 1, abort_flag))) break;
+          load(kp + G_STAGES);
         }
       }
       if (!ok) {

@@ -138,10 +138,14 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
           mma_bf16(tmem, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bb + k * 2048, 8192, 1024), idesc,
                    (kt > 0 || k > 0) ? 1u : 0u);
         mma_commit(bar_empty + 8 * s);
-        if (kt + P_STAGES < nk) {
-          // the stage is free once its MMAs are done
-          if (!(ok = mbar_wait(bar_empty + 8 * s, (kt / P_STAGES) & 1, abort_flag))) break;
-          load(kt + P_STAGES);
+        // refill the previous k-step's stage once its MMAs are done: they
+        // finish while this step's are queued, so the tensor pipe does not
+        // run dry during the wait
+        const int kp = kt - 1;
+        if (kp >= 0 && kp + P_STAGES < nk) {
+          const int sp = kp % P_STAGES;
+          if (!(ok = mbar_wait(bar_empty + 8 * sp, (kp / P_STAGES) & 1, abort_flag))) break;
+          load(kp + P_STAGES);
         }
       }
       if (!ok) {
