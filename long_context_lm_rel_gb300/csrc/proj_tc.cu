@@ -10,13 +10,16 @@
 // projected (their rows are walked as the attention walks its key tiles);
 // rows of empty slots are not written.
 //
-// One CTA computes one output block: 128 hidden-state rows of one batch row
-// times up to 4 heads (N <= 256 columns) of one of Q, K, V, with the hidden
-// width d streamed in 64-wide steps through a 4-stage TMA pipeline:
+// An output block is 128 hidden-state rows of one batch row times up to 4
+// heads (N <= 256 columns) of one of Q, K, V, with the hidden width d
+// streamed in 64-wide steps through a 4-stage TMA pipeline:
 //   A = hidden rows [128][64] bf16 (K-major, 128-byte swizzle)
 //   B = W rows [64][N] bf16 (MN-major: 64x64 swizzled boxes, 8 KB apart)
 //   D = TMEM [128 lanes][N] fp32; four epilogue warps write bf16 rows of
 //   64 columns per head.
+// The kernel is persistent (one CTA per SM walks its share of the blocks)
+// with one producer warp, one MMA warp and two accumulators, so pipeline
+// fill and epilogue of one block overlap the main loop of the next.
 #include <math.h>
 
 #include <mutex>
@@ -31,12 +34,14 @@ using namespace sm103;
 using namespace tc;
 
 constexpr int P_STAGES = 4;
-constexpr int P_THREADS = 160;  // warps 0-3 epilogue (TMEM lane quadrants), warp 4 TMA + MMA
+// warps 0-3 epilogue (TMEM lane quadrants), warp 4 TMA producer, warp 5 MMA issuer
+constexpr int P_THREADS = 192;
 constexpr uint32_t P_A_BYTES = 128 * 64 * 2;  // 16 KB
 constexpr uint32_t P_B_BYTES = 4 * 64 * 64 * 2;  // 32 KB (up to four 64-column boxes)
 constexpr uint32_t P_STAGE = P_A_BYTES + P_B_BYTES;
 constexpr uint32_t P_BAR = P_STAGES * P_STAGE;
-constexpr uint32_t P_SMEM = P_BAR + 128 + 1024;
+constexpr uint32_t P_STG = P_BAR + 256;  // epilogue staging: 4 warps x 32 rows x 128 B
+constexpr uint32_t P_SMEM = P_STG + 4 * 4096 + 1024;
 
 __device__ int g_proj_error;
 
@@ -47,19 +52,20 @@ struct ProjParams {
   __nv_bfloat16 *out[3];  // q, k, v
 };
 
-__global__ void __launch_bounds__(P_THREADS, 1)
-rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_constant__ CUtensorMap tm_hcur,
-                const __grid_constant__ CUtensorMap tm_wq, const __grid_constant__ CUtensorMap tm_wk,
-                const __grid_constant__ CUtensorMap tm_wv, const ProjParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = align1024(smem_raw);
-  const uint32_t sb = smem_u32(smem);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// One output block: which of Q, K, V, its batch row, heads and rows.
+struct ProjItem {
+  const CUtensorMap *amap, *wmap;
+  __nv_bfloat16 *out;
+  int b, h0, nh, arow, orow0, nvalid, orows;
+};
 
-  // ---- which output block
+__device__ __forceinline__ ProjItem proj_item(const ProjParams &p, int w, const CUtensorMap *tm_hmem,
+                                              const CUtensorMap *tm_hcur, const CUtensorMap *tm_wq,
+                                              const CUtensorMap *tm_wk, const CUtensorMap *tm_wv) {
+  ProjItem it;
   const int per_b = p.NT * (p.Tq + 2 * p.Tkv);
-  const int b = blockIdx.x / per_b;
-  int rest = blockIdx.x % per_b;
+  it.b = w / per_b;
+  int rest = w % per_b;
   const int nt = rest % p.NT;
   rest /= p.NT;
   int which, tile;  // 0 q, 1 k, 2 v
@@ -71,83 +77,101 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
     which = 1 + rest / p.Tkv;
     tile = rest % p.Tkv;
   }
-  const int h0 = 4 * nt, nh = min(4, p.H - h0), N = 64 * nh;
-  // source rows and output rows of the block
-  const CUtensorMap *amap = &tm_hcur;
-  int arow, orow0, nvalid, orows;
+  it.h0 = 4 * nt;
+  it.nh = min(4, p.H - it.h0);
+  it.amap = tm_hcur;
   if (which == 0) {
-    arow = tile * BQ;
-    orow0 = arow;
-    nvalid = min(BQ, p.L - arow);
-    orows = p.L;
+    it.arow = tile * BQ;
+    it.orow0 = it.arow;
+    it.nvalid = min(BQ, p.L - it.arow);
+    it.orows = p.L;
   } else {
     const KeyTiles tiles(p.m, p.cap, p.head, p.L);
     const KeyTile x = tiles.get(tile);
     const bool mem = x.jlog0 < 0;
-    amap = mem ? &tm_hmem : &tm_hcur;
-    arow = mem ? x.phys0 : x.jlog0;
-    orow0 = x.phys0;
-    nvalid = x.nvalid;
-    orows = p.cap + p.L;
+    it.amap = mem ? tm_hmem : tm_hcur;
+    it.arow = mem ? x.phys0 : x.jlog0;
+    it.orow0 = x.phys0;
+    it.nvalid = x.nvalid;
+    it.orows = p.cap + p.L;
   }
-  const CUtensorMap *wmap = which == 0 ? &tm_wq : (which == 1 ? &tm_wk : &tm_wv);
-  __nv_bfloat16 *out = p.out[which];
+  it.wmap = which == 0 ? tm_wq : (which == 1 ? tm_wk : tm_wv);
+  it.out = p.out[which];
+  return it;
+}
+
+// Persistent: CTA c takes output blocks c, c + G, c + 2G, ... (G CTAs) as
+// one stream of 64-wide k-steps through the stage ring. Block j accumulates
+// in TMEM columns 256 (j & 1) .. +255, so its epilogue runs while the MMAs
+// of block j+1 do, and the producer fills the stages of block j+1 while the
+// MMAs of block j finish.
+__global__ void __launch_bounds__(P_THREADS, 1)
+rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_constant__ CUtensorMap tm_hcur,
+                const __grid_constant__ CUtensorMap tm_wq, const __grid_constant__ CUtensorMap tm_wk,
+                const __grid_constant__ CUtensorMap tm_wv, const ProjParams p, int nblocks) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  const int nj = (int)blockIdx.x < nblocks ? (nblocks - 1 - (int)blockIdx.x) / G + 1 : 0;
+  auto item = [&](int j) {
+    return proj_item(p, (int)blockIdx.x + j * G, &tm_hmem, &tm_hcur, &tm_wq, &tm_wk, &tm_wv);
+  };
 
   const uint32_t bar_full = sb + P_BAR, bar_empty = bar_full + 8 * P_STAGES;
-  const uint32_t bar_done = bar_empty + 8 * P_STAGES;
-  uint32_t *tmem_slot = (uint32_t *)(smem + P_BAR + 16 * P_STAGES + 8);
-  volatile int *abort_flag = (volatile int *)(smem + P_BAR + 16 * P_STAGES + 12);
+  const uint32_t bar_accf = bar_empty + 8 * P_STAGES;  // [2] accumulator written (MMA commit)
+  const uint32_t bar_acce = bar_accf + 16;             // [2] accumulator read (4 epilogue warps)
+  const uint32_t bar_drain = bar_acce + 16;            // MMAs drained after an abort
+  uint32_t *tmem_slot = (uint32_t *)(smem + P_BAR + 16 * P_STAGES + 40);
+  volatile int *abort_flag = (volatile int *)(smem + P_BAR + 16 * P_STAGES + 44);
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_done, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_accf + 8 * a, 1);
+      mbar_init(bar_acce + 8 * a, 4);
+    }
+    mbar_init(bar_drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 4) tmem_alloc(smem_u32(tmem_slot), 256);
+  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nk = p.d / 64;
+  const int total = nj * nk;  // k-steps of this CTA
 
   if (warp == 4) {
+    // ---- producer: k-step g of the CTA's stream goes to stage g % P_STAGES
     if (lane == 0) {
       int issued[P_STAGES] = {0, 0, 0, 0};
-      auto load = [&](int kt) {
-        const int s = kt % P_STAGES;
-        const uint32_t a = sb + s * P_STAGE, bb = a + P_A_BYTES;
-        mbar_expect_tx(bar_full + 8 * s, P_A_BYTES + nh * 8192);
-        tma_load_3d(a, amap, kt * 64, arow, b, bar_full + 8 * s);
-        for (int j = 0; j < nh; ++j)
-          tma_load_3d(bb + j * 8192, wmap, (h0 + j) * 64, kt * 64, 0, bar_full + 8 * s);
-        ++issued[s];
-      };
-      const uint32_t idesc = idesc_bf16(128, N, false, true);
       bool ok = true;
-      for (int kt = 0; kt < nk && kt < P_STAGES; ++kt) load(kt);
-      for (int kt = 0; kt < nk; ++kt) {
-        const int s = kt % P_STAGES;
-        if (!(ok = mbar_wait(bar_full + 8 * s, (kt / P_STAGES) & 1, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t a = sb + s * P_STAGE, bb = a + P_A_BYTES;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bb + k * 2048, 8192, 1024), idesc,
-                   (kt > 0 || k > 0) ? 1u : 0u);
-        mma_commit(bar_empty + 8 * s);
-        // refill the previous k-step's stage once its MMAs are done: they
-        // finish while this step's are queued, so the tensor pipe does not
-        // run dry during the wait
-        const int kp = kt - 1;
-        if (kp >= 0 && kp + P_STAGES < nk) {
-          const int sp = kp % P_STAGES;
-          if (!(ok = mbar_wait(bar_empty + 8 * sp, (kp / P_STAGES) & 1, abort_flag))) break;
-          load(kp + P_STAGES);
+      int lj = -1;
+      ProjItem li;
+      for (int g = 0; g < total; ++g) {
+        const int j = g / nk, kt = g - j * nk, s = g % P_STAGES;
+        // the stage's previous k-step must have been consumed by its MMAs
+        if (g >= P_STAGES && !(ok = mbar_wait(bar_empty + 8 * s, ((g / P_STAGES) - 1) & 1, abort_flag)))
+          break;
+        if (j != lj) {
+          li = item(j);
+          lj = j;
         }
+        const uint32_t a = sb + s * P_STAGE, bb = a + P_A_BYTES;
+        mbar_expect_tx(bar_full + 8 * s, P_A_BYTES + li.nh * 8192);
+        tma_load_3d(a, li.amap, kt * 64, li.arow, li.b, bar_full + 8 * s);
+        for (int jj = 0; jj < li.nh; ++jj)
+          tma_load_3d(bb + jj * 8192, li.wmap, (li.h0 + jj) * 64, kt * 64, 0, bar_full + 8 * s);
+        ++issued[s];
       }
+      // the last stages' releases arrive before the CTA may exit
+      for (int g = total > P_STAGES ? total - P_STAGES : 0; ok && g < total; ++g)
+        ok = mbar_wait(bar_empty + 8 * (g % P_STAGES), (g / P_STAGES) & 1, abort_flag);
       if (!ok) {
         // let in-flight copies land before shared memory is released
         volatile int no_abort = 0;
@@ -155,48 +179,94 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
           if (issued[s] > 0) mbar_wait(bar_full + 8 * s, (issued[s] - 1) & 1, &no_abort);
         atomicExch(&g_proj_error, 1);
       }
-      mma_commit(bar_done);
-      if (!ok) {  // the epilogue gives up at once: wait for the MMAs here
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      for (int j = 0; ok && j < nj; ++j) {
+        const uint32_t acc = tmem + 256 * (j & 1);
+        // the accumulator last held block j-2: its epilogue must have read it
+        if (j >= 2 && !(ok = mbar_wait(bar_acce + 8 * (j & 1), ((j >> 1) - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16(128, 64 * item(j).nh, false, true);
+        for (int kt = 0; kt < nk; ++kt) {
+          const int g = j * nk + kt, s = g % P_STAGES;
+          if (!(ok = mbar_wait(bar_full + 8 * s, (g / P_STAGES) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t a = sb + s * P_STAGE, bb = a + P_A_BYTES;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(acc, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bb + k * 2048, 8192, 1024), idesc,
+                     (kt > 0 || k > 0) ? 1u : 0u);
+          mma_commit(bar_empty + 8 * s);
+        }
+        if (ok) mma_commit(bar_accf + 8 * (j & 1));
+      }
+      if (!ok) {  // the MMAs in flight finish before TMEM and shared memory are released
         volatile int no_abort = 0;
-        mbar_wait(bar_done, 0, &no_abort);
+        mma_commit(bar_drain);
+        mbar_wait(bar_drain, 0, &no_abort);
+        atomicExch(&g_proj_error, 1);
       }
     }
     __syncwarp();
   } else {
-    // ---- epilogue: TMEM lane = row of the block
-    const int r = warp * 32 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort_flag));
-    if (ok) {
+    // ---- epilogue: TMEM lane = row of the block. Each warp turns its 32
+    // rows around in shared memory (16-byte chunks xor-swizzled by row), so
+    // one store instruction writes 4 whole 128-byte head rows.
+    const uint32_t stg = sb + P_STG + warp * 4096;
+    const uint32_t srow = stg + lane * 128;
+    const int rr0 = lane >> 3, c = lane & 7;
+    bool ok = true;
+    for (int j = 0; j < nj; ++j) {
+      const ProjItem it = item(j);
+      const uint32_t trow = tmem + 256 * (j & 1) + ((uint32_t)(warp * 32) << 16);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_accf + 8 * (j & 1), (j >> 1) & 1, abort_flag));
+      if (!ok) break;
       tc_fence_after();
-      for (int hh = 0; hh < nh; ++hh) {
+      for (int hh = 0; hh < it.nh; ++hh) {
         uint32_t lo[32], hi[32];
         tmem_ld32(trow + 64 * hh, lo);
         tmem_ld32(trow + 64 * hh + 32, hi);
         tmem_wait_ld();
-        if (r < nvalid) {
-          uint4 *dst = (uint4 *)(out + (((size_t)b * p.H + h0 + hh) * orows + orow0 + r) * DH);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            dst[e] = make_uint4(pack_bf16(__uint_as_float(lo[8 * e]), __uint_as_float(lo[8 * e + 1])),
-                                pack_bf16(__uint_as_float(lo[8 * e + 2]), __uint_as_float(lo[8 * e + 3])),
-                                pack_bf16(__uint_as_float(lo[8 * e + 4]), __uint_as_float(lo[8 * e + 5])),
-                                pack_bf16(__uint_as_float(lo[8 * e + 6]), __uint_as_float(lo[8 * e + 7])));
-            dst[4 + e] = make_uint4(pack_bf16(__uint_as_float(hi[8 * e]), __uint_as_float(hi[8 * e + 1])),
-                                    pack_bf16(__uint_as_float(hi[8 * e + 2]), __uint_as_float(hi[8 * e + 3])),
-                                    pack_bf16(__uint_as_float(hi[8 * e + 4]), __uint_as_float(hi[8 * e + 5])),
-                                    pack_bf16(__uint_as_float(hi[8 * e + 6]), __uint_as_float(hi[8 * e + 7])));
-          }
+        if (hh == it.nh - 1) {  // the accumulator may take block j+2
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acce + 8 * (j & 1));
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          st_shared_v4(srow + ((e ^ (lane & 7)) << 4),
+                       pack_bf16(__uint_as_float(lo[8 * e]), __uint_as_float(lo[8 * e + 1])),
+                       pack_bf16(__uint_as_float(lo[8 * e + 2]), __uint_as_float(lo[8 * e + 3])),
+                       pack_bf16(__uint_as_float(lo[8 * e + 4]), __uint_as_float(lo[8 * e + 5])),
+                       pack_bf16(__uint_as_float(lo[8 * e + 6]), __uint_as_float(lo[8 * e + 7])));
+          st_shared_v4(srow + (((4 + e) ^ (lane & 7)) << 4),
+                       pack_bf16(__uint_as_float(hi[8 * e]), __uint_as_float(hi[8 * e + 1])),
+                       pack_bf16(__uint_as_float(hi[8 * e + 2]), __uint_as_float(hi[8 * e + 3])),
+                       pack_bf16(__uint_as_float(hi[8 * e + 4]), __uint_as_float(hi[8 * e + 5])),
+                       pack_bf16(__uint_as_float(hi[8 * e + 6]), __uint_as_float(hi[8 * e + 7])));
+        }
+        __syncwarp();
+        __nv_bfloat16 *obase =
+            it.out + (((size_t)it.b * p.H + it.h0 + hh) * it.orows + it.orow0 + warp * 32) * DH + c * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + rr0;
+          const uint4 v = ld_shared_v4(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
+          if (warp * 32 + rr < it.nvalid) *(uint4 *)(obase + rr * DH) = v;
+        }
+        __syncwarp();
       }
-    } else {
-      atomicExch(&g_proj_error, 2);
     }
+    if (!ok) atomicExch(&g_proj_error, 2);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, 256);
+  if (warp == 5) tmem_dealloc(tmem, 512);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -260,7 +330,12 @@ cudaError_t launch_tc_proj(const AttnShape &s, int d, const void *h_mem, const v
   }
   p.out[0] = (__nv_bfloat16 *)q; p.out[1] = (__nv_bfloat16 *)k; p.out[2] = (__nv_bfloat16 *)v;
   const long long blocks = (long long)s.B * p.NT * (p.Tq + 2 * p.Tkv);
-  rxl_proj_kernel<<<(unsigned)blocks, P_THREADS, P_SMEM, st>>>(thm, thc, twq, twk, twv, p);
+  if (blocks == 0) return cudaSuccess;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const unsigned grid = (unsigned)(blocks < sms ? blocks : sms);
+  rxl_proj_kernel<<<grid, P_THREADS, P_SMEM, st>>>(thm, thc, twq, twk, twv, p, (int)blocks);
   ++*launches;
   return cudaGetLastError();
 }
