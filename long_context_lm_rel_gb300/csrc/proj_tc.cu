@@ -33,11 +33,12 @@ namespace {
 using namespace sm103;
 using namespace tc;
 
-constexpr int P_STAGES = 4;
-// warps 0-3 epilogue (TMEM lane quadrants), warp 4 TMA producer, warp 5 MMA issuer
+constexpr int P_STAGES = 5;
+// warps 0-3 epilogue (TMEM lane quadrants), warp 4 TMA producer, warp 5 MMA
+// issuer (first CTA of the pair; TMEM allocation only in the second)
 constexpr int P_THREADS = 192;
-constexpr uint32_t P_A_BYTES = 128 * 64 * 2;  // 16 KB
-constexpr uint32_t P_B_BYTES = 4 * 64 * 64 * 2;  // 32 KB (up to four 64-column boxes)
+constexpr uint32_t P_A_BYTES = 128 * 64 * 2;     // 16 KB: this CTA's 128 rows
+constexpr uint32_t P_B_BYTES = 2 * 64 * 64 * 2;  // 16 KB: this CTA's 128 of the pair's 256 columns
 constexpr uint32_t P_STAGE = P_A_BYTES + P_B_BYTES;
 constexpr uint32_t P_BAR = P_STAGES * P_STAGE;
 constexpr uint32_t P_STG = P_BAR + 256;  // epilogue staging: 4 warps x 32 rows x 128 B
@@ -47,36 +48,46 @@ __device__ int g_proj_error;
 
 struct ProjParams {
   int B, H, L, cap, m, head, d;
-  int NT;        // column tiles of up to 4 heads
-  int Tq, Tkv;   // row tiles of Q and of K/V per batch row
+  int NT;              // column tiles of up to 4 heads
+  int Tq, Tkv;         // row tiles of Q and of K/V per batch row
+  int pairs_q, pairs_kv;  // pairs of row tiles of Q and of K (or V), over all batch rows
   __nv_bfloat16 *out[3];  // q, k, v
 };
 
-// One output block: which of Q, K, V, its batch row, heads and rows.
+// One CTA's output block of a pair unit: which of Q, K, V, its batch row,
+// heads and rows; `store` is false for the second CTA of a pair whose list
+// has an odd number of row tiles (it repeats the first CTA's rows).
 struct ProjItem {
   const CUtensorMap *amap, *wmap;
   __nv_bfloat16 *out;
   int b, h0, nh, arow, orow0, nvalid, orows;
+  bool store;
 };
 
-__device__ __forceinline__ ProjItem proj_item(const ProjParams &p, int w, const CUtensorMap *tm_hmem,
+// Unit u = (column tile nt, pair of row tiles): the row tiles of Q over all
+// batch rows in order, then those of K, then those of V, two per unit, so
+// both CTAs of a pair use the same W columns.
+__device__ __forceinline__ ProjItem proj_item(const ProjParams &p, int u, int rank, const CUtensorMap *tm_hmem,
                                               const CUtensorMap *tm_hcur, const CUtensorMap *tm_wq,
                                               const CUtensorMap *tm_wk, const CUtensorMap *tm_wv) {
   ProjItem it;
-  const int per_b = p.NT * (p.Tq + 2 * p.Tkv);
-  it.b = w / per_b;
-  int rest = w % per_b;
-  const int nt = rest % p.NT;
-  rest /= p.NT;
-  int which, tile;  // 0 q, 1 k, 2 v
-  if (rest < p.Tq) {
+  const int nt = u % p.NT;
+  int q = u / p.NT;
+  int which, T;
+  if (q < p.pairs_q) {
     which = 0;
-    tile = rest;
+    T = p.Tq;
   } else {
-    rest -= p.Tq;
-    which = 1 + rest / p.Tkv;
-    tile = rest % p.Tkv;
+    q -= p.pairs_q;
+    which = 1 + q / p.pairs_kv;
+    q %= p.pairs_kv;
+    T = p.Tkv;
   }
+  int idx = 2 * q + rank;
+  it.store = idx < p.B * T;
+  if (!it.store) idx = 2 * q;
+  it.b = idx / T;
+  const int tile = idx % T;
   it.h0 = 4 * nt;
   it.nh = min(4, p.H - it.h0);
   it.amap = tm_hcur;
@@ -100,28 +111,31 @@ __device__ __forceinline__ ProjItem proj_item(const ProjParams &p, int w, const 
   return it;
 }
 
-// Persistent: CTA c takes output blocks c, c + G, c + 2G, ... (G CTAs) as
-// one stream of 64-wide k-steps through the stage ring. Block j accumulates
-// in TMEM columns 256 (j & 1) .. +255, so its epilogue runs while the MMAs
-// of block j+1 do, and the producer fills the stages of block j+1 while the
-// MMAs of block j finish.
+// Persistent CTA pairs (clusters of two): pair c takes units c, c + P, ...
+// (P pairs) as one stream of 64-wide k-steps through the stage ring. Each
+// CTA loads its own 128 hidden-state rows and its half (two heads) of the
+// unit's W columns; the first CTA issues one M = 256, N = 256 MMA chain per
+// unit into TMEM columns 256 (j & 1) .. +255 of both CTAs, so the epilogue
+// of unit j runs while the MMAs of unit j+1 do. Heads past H load a valid
+// head's columns and are not stored.
 __global__ void __launch_bounds__(P_THREADS, 1)
 rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_constant__ CUtensorMap tm_hcur,
                 const __grid_constant__ CUtensorMap tm_wq, const __grid_constant__ CUtensorMap tm_wk,
-                const __grid_constant__ CUtensorMap tm_wv, const ProjParams p, int nblocks) {
+                const __grid_constant__ CUtensorMap tm_wv, const ProjParams p, int nunits) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x;
-  const int nj = (int)blockIdx.x < nblocks ? (nblocks - 1 - (int)blockIdx.x) / G + 1 : 0;
+  const int rank = (int)(blockIdx.x & 1), pair = (int)(blockIdx.x >> 1), P = (int)(gridDim.x >> 1);
+  const int nj = pair < nunits ? (nunits - 1 - pair) / P + 1 : 0;
   auto item = [&](int j) {
-    return proj_item(p, (int)blockIdx.x + j * G, &tm_hmem, &tm_hcur, &tm_wq, &tm_wk, &tm_wv);
+    return proj_item(p, pair + j * P, rank, &tm_hmem, &tm_hcur, &tm_wq, &tm_wk, &tm_wv);
   };
 
-  const uint32_t bar_full = sb + P_BAR, bar_empty = bar_full + 8 * P_STAGES;
-  const uint32_t bar_accf = bar_empty + 8 * P_STAGES;  // [2] accumulator written (MMA commit)
-  const uint32_t bar_acce = bar_accf + 16;             // [2] accumulator read (4 epilogue warps)
+  const uint32_t bar_full = sb + P_BAR;                // [S] (first CTA) the stage landed in both CTAs
+  const uint32_t bar_empty = bar_full + 8 * P_STAGES;  // [S] the stage's MMAs are done
+  const uint32_t bar_accf = bar_empty + 8 * P_STAGES;  // [2] accumulator written
+  const uint32_t bar_acce = bar_accf + 16;             // [2] (first CTA) accumulator read by 8 warps
   const uint32_t bar_drain = bar_acce + 16;            // MMAs drained after an abort
   uint32_t *tmem_slot = (uint32_t *)(smem + P_BAR + 16 * P_STAGES + 40);
   volatile int *abort_flag = (volatile int *)(smem + P_BAR + 16 * P_STAGES + 44);
@@ -132,98 +146,115 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_accf + 8 * a, 1);
-      mbar_init(bar_acce + 8 * a, 4);
+      mbar_init(bar_acce + 8 * a, 8);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == 5) tmem_alloc_pair(smem_u32(tmem_slot), 512);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers and TMEM are ready
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nk = p.d / 64;
-  const int total = nj * nk;  // k-steps of this CTA
+  const int total = nj * nk;  // k-steps of this pair
 
   if (warp == 4) {
-    // ---- producer: k-step g of the CTA's stream goes to stage g % P_STAGES
+    // ---- producer: k-step g of the pair's stream goes to stage g % P_STAGES
+    // of both CTAs; every copy counts on the first CTA's full barrier, which
+    // expects both CTAs' bytes
     if (lane == 0) {
-      int issued[P_STAGES] = {0, 0, 0, 0};
+      const uint32_t full0 = mapa_shared(bar_full, 0);
+      int issued[P_STAGES] = {};
       bool ok = true;
       int lj = -1;
       ProjItem li;
       for (int g = 0; g < total; ++g) {
         const int j = g / nk, kt = g - j * nk, s = g % P_STAGES;
-        // the stage's previous k-step must have been consumed by its MMAs
-        if (g >= P_STAGES && !(ok = mbar_wait(bar_empty + 8 * s, ((g / P_STAGES) - 1) & 1, abort_flag)))
+        // the stage's previous k-step must have been consumed by the pair's MMAs
+        if (g >= P_STAGES &&
+            !(ok = mbar_wait_cluster(bar_empty + 8 * s, ((g / P_STAGES) - 1) & 1, abort_flag)))
           break;
         if (j != lj) {
           li = item(j);
           lj = j;
         }
         const uint32_t a = sb + s * P_STAGE, bb = a + P_A_BYTES;
-        mbar_expect_tx(bar_full + 8 * s, P_A_BYTES + li.nh * 8192);
-        tma_load_3d(a, li.amap, kt * 64, li.arow, li.b, bar_full + 8 * s);
-        for (int jj = 0; jj < li.nh; ++jj)
-          tma_load_3d(bb + jj * 8192, li.wmap, (li.h0 + jj) * 64, kt * 64, 0, bar_full + 8 * s);
+        if (rank == 0) mbar_expect_tx(bar_full + 8 * s, 2 * P_STAGE);
+        tma_load_3d_pair(a, li.amap, kt * 64, li.arow, li.b, full0 + 8 * s);
+        for (int jj = 0; jj < 2; ++jj) {
+          const int h = min(li.h0 + 2 * rank + jj, p.H - 1);
+          tma_load_3d_pair(bb + jj * 8192, li.wmap, h * 64, kt * 64, 0, full0 + 8 * s);
+        }
         ++issued[s];
       }
-      // the last stages' releases arrive before the CTA may exit
+      // the last stages' releases arrive before the pair may exit
       for (int g = total > P_STAGES ? total - P_STAGES : 0; ok && g < total; ++g)
-        ok = mbar_wait(bar_empty + 8 * (g % P_STAGES), (g / P_STAGES) & 1, abort_flag);
+        ok = mbar_wait_cluster(bar_empty + 8 * (g % P_STAGES), (g / P_STAGES) & 1, abort_flag);
       if (!ok) {
-        // let in-flight copies land before shared memory is released
+        // let in-flight copies land before shared memory is released: the
+        // first CTA sees its full barriers complete (they count both CTAs'
+        // bytes); the second CTA, which has no barrier of its own to watch,
+        // gives its copies a bounded grace period
         volatile int no_abort = 0;
-        for (int s = 0; s < P_STAGES; ++s)
-          if (issued[s] > 0) mbar_wait(bar_full + 8 * s, (issued[s] - 1) & 1, &no_abort);
+        if (rank == 0) {
+          for (int s = 0; s < P_STAGES; ++s)
+            if (issued[s] > 0) mbar_wait(bar_full + 8 * s, (issued[s] - 1) & 1, &no_abort);
+        } else {
+          const long long t0 = clock64();
+          while (clock64() - t0 < 20000000LL) {
+          }
+        }
         atomicExch(&g_proj_error, 1);
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
-    // ---- MMA issuer
+  } else if (warp == 5 && rank == 0) {
+    // ---- first CTA: MMA issuer for the pair
     if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(256, 256, false, true);
       bool ok = true;
       for (int j = 0; ok && j < nj; ++j) {
         const uint32_t acc = tmem + 256 * (j & 1);
-        // the accumulator last held block j-2: its epilogue must have read it
-        if (j >= 2 && !(ok = mbar_wait(bar_acce + 8 * (j & 1), ((j >> 1) - 1) & 1, abort_flag))) break;
+        // the accumulator last held unit j-2: both epilogues must have read it
+        if (j >= 2 && !(ok = mbar_wait_cluster(bar_acce + 8 * (j & 1), ((j >> 1) - 1) & 1, abort_flag)))
+          break;
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16(128, 64 * item(j).nh, false, true);
         for (int kt = 0; kt < nk; ++kt) {
           const int g = j * nk + kt, s = g % P_STAGES;
-          if (!(ok = mbar_wait(bar_full + 8 * s, (g / P_STAGES) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait_cluster(bar_full + 8 * s, (g / P_STAGES) & 1, abort_flag))) break;
           tc_fence_after();
           const uint32_t a = sb + s * P_STAGE, bb = a + P_A_BYTES;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(acc, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bb + k * 2048, 8192, 1024), idesc,
-                     (kt > 0 || k > 0) ? 1u : 0u);
-          mma_commit(bar_empty + 8 * s);
+            mma_bf16_pair(acc, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bb + k * 2048, 8192, 1024), idesc,
+                          (kt > 0 || k > 0) ? 1u : 0u);
+          mma_commit_pair(bar_empty + 8 * s, 3);
         }
-        if (ok) mma_commit(bar_accf + 8 * (j & 1));
+        if (ok) mma_commit_pair(bar_accf + 8 * (j & 1), 3);
       }
       if (!ok) {  // the MMAs in flight finish before TMEM and shared memory are released
         volatile int no_abort = 0;
-        mma_commit(bar_drain);
+        mma_commit_pair(bar_drain, 1);
         mbar_wait(bar_drain, 0, &no_abort);
         atomicExch(&g_proj_error, 1);
       }
     }
     __syncwarp();
-  } else {
-    // ---- epilogue: TMEM lane = row of the block. Each warp turns its 32
-    // rows around in shared memory (16-byte chunks xor-swizzled by row), so
-    // one store instruction writes 4 whole 128-byte head rows.
+  } else if (warp < 4) {
+    // ---- epilogue: TMEM lane = row of this CTA's block. Each warp turns its
+    // 32 rows around in shared memory (16-byte chunks xor-swizzled by row),
+    // so one store instruction writes 4 whole 128-byte head rows.
     const uint32_t stg = sb + P_STG + warp * 4096;
     const uint32_t srow = stg + lane * 128;
+    const uint32_t acce0 = mapa_shared(bar_acce, 0);
     const int rr0 = lane >> 3, c = lane & 7;
     bool ok = true;
     for (int j = 0; j < nj; ++j) {
       const ProjItem it = item(j);
       const uint32_t trow = tmem + 256 * (j & 1) + ((uint32_t)(warp * 32) << 16);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_accf + 8 * (j & 1), (j >> 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_accf + 8 * (j & 1), (j >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       for (int hh = 0; hh < it.nh; ++hh) {
@@ -231,11 +262,12 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
         tmem_ld32(trow + 64 * hh, lo);
         tmem_ld32(trow + 64 * hh + 32, hi);
         tmem_wait_ld();
-        if (hh == it.nh - 1) {  // the accumulator may take block j+2
+        if (hh == it.nh - 1) {  // the accumulator may take unit j+2
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_acce + 8 * (j & 1));
+          if (lane == 0) mbar_arrive_remote(acce0 + 8 * (j & 1));
         }
+        if (!it.store) continue;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           st_shared_v4(srow + ((e ^ (lane & 7)) << 4),
@@ -265,8 +297,9 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // neither CTA leaves while the other may still touch its shared memory or TMEM
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == 5) tmem_dealloc_pair(tmem, 512);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -328,16 +361,36 @@ cudaError_t launch_tc_proj(const AttnShape &s, int d, const void *h_mem, const v
     const int lenB = s.m - lenA;
     p.Tkv = (lenA + BK - 1) / BK + (lenB + BK - 1) / BK + (s.L + BK - 1) / BK;
   }
+  p.pairs_q = (s.B * p.Tq + 1) / 2;
+  p.pairs_kv = (s.B * p.Tkv + 1) / 2;
   p.out[0] = (__nv_bfloat16 *)q; p.out[1] = (__nv_bfloat16 *)k; p.out[2] = (__nv_bfloat16 *)v;
-  const long long blocks = (long long)s.B * p.NT * (p.Tq + 2 * p.Tkv);
-  if (blocks == 0) return cudaSuccess;
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const unsigned grid = (unsigned)(blocks < sms ? blocks : sms);
-  rxl_proj_kernel<<<grid, P_THREADS, P_SMEM, st>>>(thm, thc, twq, twk, twv, p, (int)blocks);
+  const long long units = (long long)p.NT * (p.pairs_q + 2LL * p.pairs_kv);
+  if (units == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(P_THREADS);
+  cfg.dynamicSmemBytes = P_SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent pairs: as many as can be resident at once
+  static std::once_flag occ_once;
+  static int max_pairs = 0;
+  std::call_once(occ_once, [&] {
+    cudaLaunchConfig_t one = cfg;
+    one.gridDim = dim3(2);
+    if (cudaOccupancyMaxActiveClusters(&max_pairs, rxl_proj_kernel, &one) != cudaSuccess) max_pairs = 0;
+  });
+  if (max_pairs <= 0) return cudaErrorLaunchOutOfResources;
+  const long long pairs = units < max_pairs ? units : max_pairs;
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, rxl_proj_kernel, thm, thc, twq, twk, twv, p, (int)units);
   ++*launches;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t tc_proj_read_error(int *flag) {
