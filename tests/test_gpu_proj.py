@@ -69,6 +69,7 @@ CASES = [  # B, H, L, cap, m, head, d
     (2, 16, 64, 1600, 1600, 1550, 128),  # long ring wrapping mid-tile
     (3, 3, 1, 5, 5, 2, 64),              # one current row
     (2, 2, 130, 256, 100, 200, 256),     # ring not full: empty slots stay untouched
+    (1, 5, 300, 130, 130, 60, 128),      # a 1-head column tile; odd row-tile lists (a CTA pair with one block)
 ]
 
 
