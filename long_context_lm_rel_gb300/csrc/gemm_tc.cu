@@ -255,6 +255,93 @@ __global__ void __launch_bounds__(256) gemm_finalize_kernel(const float *__restr
   }
 }
 
+// Split K followed by the block's LayerNorm, one CTA per row and 8 columns
+// per thread (N / 8 <= 1024 threads, so a row is read once and stays in
+// registers): x = act(sum of the partials + bias) + residual, rounded to
+// bf16 (what the separate pass would store), then y = LayerNorm(x) with fp32
+// statistics: mean, then the mean squared deviation, each summed per thread,
+// per warp and over the CTA.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();  // red may still be read from the previous sum
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int w = 0; w < nw; ++w) s += red[w];
+  return s;
+}
+
+__global__ void __launch_bounds__(1024) gemm_finalize_ln_kernel(const float *__restrict__ partials, int splits,
+                                                                long long rows, int N,
+                                                                const __nv_bfloat16 *__restrict__ bias, int relu,
+                                                                const __nv_bfloat16 *__restrict__ residual,
+                                                                const __nv_bfloat16 *__restrict__ gamma,
+                                                                const __nv_bfloat16 *__restrict__ beta, float eps,
+                                                                __nv_bfloat16 *__restrict__ y) {
+  __shared__ float red[32];
+  const long long row = blockIdx.x;
+  const int c = threadIdx.x;  // 16-byte chunk of the row; blockDim.x == N / 8
+  const long long plane = rows * N, off = row * N + 8 * c;
+  float f[8];
+  {
+    const float4 a = *(const float4 *)(partials + off), b = *(const float4 *)(partials + off + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+#pragma unroll
+  for (int zz = 1; zz < 8; ++zz) {  // splits <= 8: every load of the row group in flight at once
+    if (zz >= splits) break;
+    const float4 a = *(const float4 *)(partials + zz * plane + off);
+    const float4 b = *(const float4 *)(partials + zz * plane + off + 4);
+    f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w; f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
+  }
+  if (bias) {
+    const uint4 w = *(const uint4 *)(bias + 8 * c);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      f[2 * t] += __uint_as_float(ww[t] << 16);
+      f[2 * t + 1] += __uint_as_float(ww[t] & 0xFFFF0000u);
+    }
+  }
+  if (relu) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) f[t] = fmaxf(f[t], 0.f);
+  }
+  if (residual) {
+    const uint4 w = *(const uint4 *)(residual + off);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      f[2 * t] += __uint_as_float(ww[t] << 16);
+      f[2 * t + 1] += __uint_as_float(ww[t] & 0xFFFF0000u);
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {  // the bf16 value the separate pass would read
+    const uint32_t w = pack_bf16(f[2 * t], f[2 * t + 1]);
+    f[2 * t] = __uint_as_float(w << 16);
+    f[2 * t + 1] = __uint_as_float(w & 0xFFFF0000u);
+    s += f[2 * t] + f[2 * t + 1];
+  }
+  const float mean = block_sum(s, red) / N;
+  float v = 0.f;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) v += (f[t] - mean) * (f[t] - mean);
+  const float rstd = rsqrtf(block_sum(v, red) / N + eps);
+  const uint4 g = *(const uint4 *)(gamma + 8 * c), bt = *(const uint4 *)(beta + 8 * c);
+  const uint32_t gg[4] = {g.x, g.y, g.z, g.w}, bb[4] = {bt.x, bt.y, bt.z, bt.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    o[t] = pack_bf16((f[2 * t] - mean) * rstd * __uint_as_float(gg[t] << 16) + __uint_as_float(bb[t] << 16),
+                     (f[2 * t + 1] - mean) * rstd * __uint_as_float(gg[t] & 0xFFFF0000u) +
+                         __uint_as_float(bb[t] & 0xFFFF0000u));
+  *(uint4 *)(y + off) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // LayerNorm over the last dimension (one warp per row, statistics in fp32):
 // y = (x - mean) / sqrt(var + eps) * gamma + beta, var the biased variance.
 __global__ void __launch_bounds__(256) layernorm_kernel(const __nv_bfloat16 *__restrict__ x,
@@ -349,7 +436,8 @@ bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims
 
 cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_heads, const void *w,
                            const void *bias, const void *residual, bool relu, void *out,
-                           float *partials, size_t partial_floats, cudaStream_t st, int *launches) {
+                           float *partials, size_t partial_floats, const void *ln_gamma, const void *ln_beta,
+                           float ln_eps, void *ln_out, cudaStream_t st, int *launches) {
   CUtensorMap ta, tw;
   bool ok;
   if (a_heads) {  // O [B, K/64, R, 64]
@@ -404,20 +492,28 @@ cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_hea
   if (S > 1) {
     long long blocks = (per_split / 8 + 255) / 256;
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-    gemm_finalize_kernel<<<(unsigned)blocks, 256, 0, st>>>(partials, (int)S, (long long)B * R, N,
-                                                          (const __nv_bfloat16 *)bias, relu ? 1 : 0,
-                                                          (const __nv_bfloat16 *)residual, (__nv_bfloat16 *)out);
+    if (ln_out && N / 8 <= 1024)  // the sum of the partials and the LayerNorm in one pass over the rows
+      gemm_finalize_ln_kernel<<<(unsigned)((long long)B * R), (unsigned)(N / 8), 0, st>>>(
+          partials, (int)S, (long long)B * R, N, (const __nv_bfloat16 *)bias, relu ? 1 : 0,
+          (const __nv_bfloat16 *)residual, (const __nv_bfloat16 *)ln_gamma, (const __nv_bfloat16 *)ln_beta,
+          ln_eps, (__nv_bfloat16 *)ln_out);
+    else
+      gemm_finalize_kernel<<<(unsigned)blocks, 256, 0, st>>>(partials, (int)S, (long long)B * R, N,
+                                                            (const __nv_bfloat16 *)bias, relu ? 1 : 0,
+                                                            (const __nv_bfloat16 *)residual, (__nv_bfloat16 *)out);
+    ++*launches;
+    if (ln_out && N / 8 > 1024) {
+      layernorm_kernel<<<(unsigned)(((long long)B * R + 7) / 8), 256, 0, st>>>(
+          (const __nv_bfloat16 *)out, (const __nv_bfloat16 *)ln_gamma, (const __nv_bfloat16 *)ln_beta,
+          (__nv_bfloat16 *)ln_out, (long long)B * R, N, ln_eps);
+      ++*launches;
+    }
+  } else if (ln_out) {
+    layernorm_kernel<<<(unsigned)(((long long)B * R + 7) / 8), 256, 0, st>>>(
+        (const __nv_bfloat16 *)out, (const __nv_bfloat16 *)ln_gamma, (const __nv_bfloat16 *)ln_beta,
+        (__nv_bfloat16 *)ln_out, (long long)B * R, N, ln_eps);
     ++*launches;
   }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_layernorm(const void *x, const void *gamma, const void *beta, void *y, long long rows,
-                             int d, float eps, cudaStream_t st, int *launches) {
-  layernorm_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
-      (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)gamma, (const __nv_bfloat16 *)beta,
-      (__nv_bfloat16 *)y, rows, d, eps);
-  ++*launches;
   return cudaGetLastError();
 }
 

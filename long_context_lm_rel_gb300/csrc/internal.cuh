@@ -77,18 +77,21 @@ cudaError_t tc_bwd_read_error(int *flag);
 cudaError_t launch_tc_proj(const AttnShape &s, int d, const void *h_mem, const void *h_cur,
                            const void *wq, const void *wk, const void *wv, void *q, void *k, void *v,
                            cudaStream_t st, int *launches);
-cudaError_t tc_proj_read_error(int *flag);
 
 // Dense layer out = act(A . W + bias) + residual over B groups of R rows
 // (bf16); A is [B, R, K] or, with a_heads, the attention output [B, K/64, R, 64].
 // partials (nullable): fp32 scratch of partial_floats floats that lets the
 // K range be split over several CTAs per output block when there are few
-// blocks (each split needs B * R * N floats)
+// blocks (each split needs B * R * N floats).
+// ln_out (nullable): the result then goes on through the LayerNorm
+// (ln_gamma, ln_beta, ln_eps) into ln_out; out is written only when K is not
+// split (the split's finalize pass applies the LayerNorm itself).
 cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_heads, const void *w,
                            const void *bias, const void *residual, bool relu, void *out,
-                           float *partials, size_t partial_floats, cudaStream_t st, int *launches);
-cudaError_t launch_layernorm(const void *x, const void *gamma, const void *beta, void *y, long long rows,
-                             int d, float eps, cudaStream_t st, int *launches);
+                           float *partials, size_t partial_floats, const void *ln_gamma, const void *ln_beta,
+                           float ln_eps, void *ln_out, cudaStream_t st, int *launches);
+
+cudaError_t tc_proj_read_error(int *flag);
 cudaError_t tc_gemm_read_error(int *flag);
 
 }  // namespace rxl

@@ -139,25 +139,20 @@ rxl_status rxl_layer_fwd(const rxl_attn_desc *desc, int d_model, int d_ff, const
   void *x1 = ws + lw.x1, *x1n = ws + lw.x1n, *z = ws + lw.z, *x2 = ws + lw.x2;
   float *part = (float *)(ws + lw.part);
   cudaStream_t cs = (cudaStream_t)stream;
-  const long long rows = (long long)s.B * s.L;
   int launches = 0;
   cudaError_t e = rxl::launch_tc_proj(s, d_model, h_mem, h_in, w->w_q, w->w_k, w->w_v, q, k, v, cs,
                                       &launches);
   if (e == cudaSuccess)
     e = rxl::launch_tc_fwd(s, q, k, v, w->r, w->u, w->vbias, o, nullptr, lse, cs, &launches);
-  if (e == cudaSuccess)  // x1 = h + attention . W_O (heads merged by the A operand's layout)
+  if (e == cudaSuccess)  // x1n = LayerNorm(h + attention . W_O) (heads merged by the A operand's layout)
     e = rxl::launch_tc_gemm(s.B, s.L, s.H * 64, d_model, o, true, w->w_o, nullptr, h_in, false, x1,
-                            part, lw.part_floats, cs, &launches);
-  if (e == cudaSuccess)
-    e = rxl::launch_layernorm(x1, w->ln1_gamma, w->ln1_beta, x1n, rows, d_model, 1e-5f, cs, &launches);
+                            part, lw.part_floats, w->ln1_gamma, w->ln1_beta, 1e-5f, x1n, cs, &launches);
   if (e == cudaSuccess)  // z = ReLU(x1n . W_1 + b_1)
     e = rxl::launch_tc_gemm(s.B, s.L, d_model, d_ff, x1n, false, w->w_1, w->b_1, nullptr, true, z,
-                            part, lw.part_floats, cs, &launches);
-  if (e == cudaSuccess)  // x2 = x1n + z . W_2 + b_2
+                            part, lw.part_floats, nullptr, nullptr, 0.f, nullptr, cs, &launches);
+  if (e == cudaSuccess)  // h_out = LayerNorm(x1n + z . W_2 + b_2)
     e = rxl::launch_tc_gemm(s.B, s.L, d_ff, d_model, z, false, w->w_2, w->b_2, x1n, false, x2,
-                            part, lw.part_floats, cs, &launches);
-  if (e == cudaSuccess)
-    e = rxl::launch_layernorm(x2, w->ln2_gamma, w->ln2_beta, h_out, rows, d_model, 1e-5f, cs, &launches);
+                            part, lw.part_floats, w->ln2_gamma, w->ln2_beta, 1e-5f, h_out, cs, &launches);
   g_last_launches = launches;
   return cuda_status(e);
 }
