@@ -6,7 +6,8 @@
 // never straddles two groups. A is either a row-major [B, R, K] activation or
 // the attention output O [B, H, R, 64] read as [B, R, H*64] (heads merged by
 // the TMA box coordinates, no copy). W is [K, N] row-major. One CTA computes a
-// 128 x 256 output block with K streamed in 64-wide steps through a 4-stage
+// 128 x 256 output block (128 x 128 when the 256-wide blocks would leave half
+// the SMs idle) with K streamed in 64-wide steps through a 4-stage
 // TMA pipeline (the structure of the projection kernel), then four epilogue
 // warps add the bias, apply ReLU, add the residual and store bf16 rows.
 // With at most a quarter as many output blocks as SMs (few rows: short
@@ -37,7 +38,8 @@ __device__ int g_gemm_error;
 
 struct GemmParams {
   int B, R, K, N;
-  int Tr, Tn;  // row tiles per group, 256-column tiles
+  int Tr, Tn;  // row tiles per group, column tiles of TN columns
+  int TN;      // 256, or 128 when the 256-wide blocks would fill at most half the SMs
   int splits;       // K split over this many CTAs per output block (1: no split)
   float *partials;  // splits > 1: [splits][B * R][N] fp32 partial sums
   const __nv_bfloat16 *bias;      // [N] or null
@@ -60,7 +62,7 @@ rxl_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   const int rt = (tile / p.Tn) % p.Tr;
   const int b = tile / (p.Tn * p.Tr);
   const int row0 = rt * 128, nrows = min(128, p.R - row0);
-  const int col0 = nt * 256, ncols = min(256, p.N - col0), nbox = (ncols + 63) / 64;
+  const int col0 = nt * p.TN, ncols = min(p.TN, p.N - col0), nbox = (ncols + 63) / 64;
 
   const uint32_t bar_full = sb + G_BAR, bar_empty = bar_full + 8 * G_STAGES;
   const uint32_t bar_done = bar_empty + 8 * G_STAGES;
@@ -460,7 +462,13 @@ cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_hea
   GemmParams p;
   p.B = B; p.R = R; p.K = K; p.N = N;
   p.Tr = (R + 127) / 128;
-  p.Tn = (N + 255) / 256;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // 128-column blocks when the 256-column ones would fill at most half the
+  // SMs: twice the CTAs, each streaming a third less per k-step
+  p.TN = 2LL * B * p.Tr * ((N + 255) / 256) <= sms ? 128 : 256;
+  p.Tn = (N + p.TN - 1) / p.TN;
   p.bias = (const __nv_bfloat16 *)bias;
   p.residual = (const __nv_bfloat16 *)residual;
   p.out = (__nv_bfloat16 *)out;
@@ -469,9 +477,6 @@ cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_hea
   // split K when the blocks fill at most a quarter of the SMs: as many
   // splits as fit the SMs, at least two k-steps each, at most 8, within the
   // partial budget; fewer than 4 splits do not repay the finalize pass
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long per_split = (long long)B * R * N;
   long long S = 1;
   if (partials && 4 * tiles <= sms) {

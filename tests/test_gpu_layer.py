@@ -65,6 +65,7 @@ class Layer:
     (2, 16, 128, 256, 256, 0, 1024, 4096),     # model width of the benchmark configurations
     (1, 2, 64, 0, 0, 0, 256, 256),             # no memory
     (2, 8, 100, 130, 120, 20, 512, 320),       # W_O and W_1 split over 4 CTAs, W_1's last column tile 64 wide
+    (2, 4, 512, 0, 0, 0, 256, 4096),           # W_1 in 256-wide blocks without a split, W_2 split with its LayerNorm
 ])
 def test_layer_parity(B, H, L, cap, m, head, d, dff):
     import torch
