@@ -12,14 +12,18 @@
 //
 // An output block is 128 hidden-state rows of one batch row times up to 4
 // heads (N <= 256 columns) of one of Q, K, V, with the hidden width d
-// streamed in 64-wide steps through a 4-stage TMA pipeline:
+// streamed in 64-wide steps through a 5-stage TMA pipeline:
 //   A = hidden rows [128][64] bf16 (K-major, 128-byte swizzle)
-//   B = W rows [64][N] bf16 (MN-major: 64x64 swizzled boxes, 8 KB apart)
+//   B = W rows [64][N] bf16 (MN-major: 64x64 swizzled boxes, 8 KB apart;
+//       each CTA of a pair holds its two heads' boxes)
 //   D = TMEM [128 lanes][N] fp32; four epilogue warps write bf16 rows of
 //   64 columns per head.
-// The kernel is persistent (one CTA per SM walks its share of the blocks)
-// with one producer warp, one MMA warp and two accumulators, so pipeline
-// fill and epilogue of one block overlap the main loop of the next.
+// The kernel runs on persistent CTA pairs (tcgen05 cta_group::2: one
+// M = 256, N = 256 MMA per k-step over two blocks that share their W columns,
+// each SM loading its own rows and half of the columns), with one producer
+// warp, one MMA warp and two accumulators, so pipeline fill and epilogue of
+// one unit overlap the main loop of the next; the epilogue turns rows around
+// in shared memory so that each store writes whole 128-byte head rows.
 #include <math.h>
 
 #include <mutex>
