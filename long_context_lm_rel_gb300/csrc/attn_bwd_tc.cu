@@ -235,6 +235,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // inputs written by the previous kernel on the stream
+  griddep_launch_dependents();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------ producer / MMA issuer
@@ -753,6 +755,8 @@ __device__ void zero_work(const ZeroArgs &z, size_t tid, size_t stride) {
 }
 
 __global__ void bwd_zero_kernel(const ZeroArgs z) {
+  griddep_wait();
+  griddep_launch_dependents();
   zero_work(z, blockIdx.x * (size_t)blockDim.x + threadIdx.x, (size_t)gridDim.x * blockDim.x);
 }
 
@@ -765,6 +769,8 @@ __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
     const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ o_lo,
     const __nv_bfloat16 *__restrict__ dout, __nv_bfloat16 *__restrict__ qu,
     __half *__restrict__ qv, float *__restrict__ delta) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int sub = threadIdx.x & 7;
   for (long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 3; row < rows;
        row += ((long long)gridDim.x * blockDim.x) >> 3) {
@@ -808,6 +814,8 @@ __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(
     const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq, float *colsum,
     const float *dv_acc, unsigned *counter, float *du, float *dvb, const float *dr_acc, float *dr,
     int L, int H, int kv_rows, int chunks) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float part[32][65];
   __shared__ bool last;
   const int bh = blockIdx.x / chunks, ch = blockIdx.x % chunks;
@@ -969,15 +977,17 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
     long long blocks = ((long long)rows * 8 + 255) / 256;
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
     if (blocks < (long long)sms * 4) blocks = (long long)sms * 4;  // enough for the zeroing
-    bwd_light_prep_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-        z, (long long)rows, s.L, s.H, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)u,
-        (const __nv_bfloat16 *)vb, (const __nv_bfloat16 *)o, (const __nv_bfloat16 *)o_lo,
-        (const __nv_bfloat16 *)dout, (__nv_bfloat16 *)qu, (__half *)qv, delta);
+    const cudaError_t e = launch_ex(
+        bwd_light_prep_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, z, (long long)rows, s.L, s.H,
+        (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)u, (const __nv_bfloat16 *)vb, (const __nv_bfloat16 *)o,
+        (const __nv_bfloat16 *)o_lo, (const __nv_bfloat16 *)dout, (__nv_bfloat16 *)qu, (__half *)qv, delta);
     ++*launches;
+    if (e != cudaSuccess) return e;
   } else {
-    bwd_zero_kernel<<<sms * 4, 256, 0, st>>>(z);
+    cudaError_t e = launch_ex(bwd_zero_kernel, dim3((unsigned)(sms * 4)), dim3(256), 0, st, 1, z);
     ++*launches;
-    cudaError_t e = launch_tc_bwd_prep(s, q, k, v, r, u, vb, dout, delta, qu, qv, st, launches);
+    if (e != cudaSuccess) return e;
+    e = launch_tc_bwd_prep(s, q, k, v, r, u, vb, dout, delta, qu, qv, st, launches);
     if (e != cudaSuccess) return e;
   }
 
@@ -998,14 +1008,16 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   p.dk = (__nv_bfloat16 *)dk; p.dv = (__nv_bfloat16 *)dv;
   p.dv_acc = sums;
   const unsigned grid = (unsigned)(p.nitems < sms ? p.nitems : sms);
-  rxl_bwd_main_kernel<<<grid, kThreads, F_SMEM, st>>>(tk, tv, tr16, tqu, tqv, tdo, tdq, tdr, p);
+  cudaError_t e = launch_ex(rxl_bwd_main_kernel, dim3(grid), dim3(kThreads), F_SMEM, st, 1, tk, tv, tr16, tqu, tqv,
+                            tdo, tdq, tdr, p);
   ++*launches;
+  if (e != cudaSuccess) return e;
   const int chunks = (s.L + 127) / 128;
-  bwd_dq_finish_kernel<<<(unsigned)(s.B * s.H * chunks), 256, 0, st>>>(
-      dq_acc, (__nv_bfloat16 *)dq, sums + s.H * DH, sums, (unsigned *)(sums + 2 * s.H * DH), du, dvb,
-      dr_acc, dr, s.L, s.H, s.kv_rows, chunks);
+  e = launch_ex(bwd_dq_finish_kernel, dim3((unsigned)(s.B * s.H * chunks)), dim3(256), 0, st, 1,
+                (const float *)dq_acc, (__nv_bfloat16 *)dq, sums + s.H * DH, (const float *)sums,
+                (unsigned *)(sums + 2 * s.H * DH), du, dvb, (const float *)dr_acc, dr, s.L, s.H, s.kv_rows, chunks);
   ++*launches;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t tc_bwd_read_error(int *flag) {

@@ -307,6 +307,8 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // inputs written by the previous kernel on the stream
+  griddep_launch_dependents();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------ producer / MMA issuer
@@ -778,30 +780,22 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   if (MODE == kFwd && 2 * nitems <= sms) {
     // few items (short segments, few heads): two CTAs per item, each over
     // half of its key tiles, merged through distributed shared memory
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * nitems));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = s.mvis ? cudaLaunchKernelEx(&cfg, rxl_fwd_tc_kernel<MODE, true, true>, tk, tv, tr, tq, p, nitems)
-                           : cudaLaunchKernelEx(&cfg, rxl_fwd_tc_kernel<MODE, false, true>, tk, tv, tr, tq, p, nitems);
+    cudaError_t e =
+        s.mvis ? launch_ex(rxl_fwd_tc_kernel<MODE, true, true>, dim3((unsigned)(2 * nitems)), dim3(kThreads),
+                           SMEM_BYTES, st, 2, tk, tv, tr, tq, p, nitems)
+               : launch_ex(rxl_fwd_tc_kernel<MODE, false, true>, dim3((unsigned)(2 * nitems)), dim3(kThreads),
+                           SMEM_BYTES, st, 2, tk, tv, tr, tq, p, nitems);
     ++*launches;
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   const unsigned grid = (unsigned)(nitems < sms ? nitems : sms);
-  if (s.mvis)
-    rxl_fwd_tc_kernel<MODE, true, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, tq, p, nitems);
-  else
-    rxl_fwd_tc_kernel<MODE, false, false><<<grid, kThreads, SMEM_BYTES, st>>>(tk, tv, tr, tq, p, nitems);
+  const cudaError_t e =
+      s.mvis ? launch_ex(rxl_fwd_tc_kernel<MODE, true, false>, dim3(grid), dim3(kThreads), SMEM_BYTES, st, 1, tk, tv,
+                         tr, tq, p, nitems)
+             : launch_ex(rxl_fwd_tc_kernel<MODE, false, false>, dim3(grid), dim3(kThreads), SMEM_BYTES, st, 1, tk,
+                         tv, tr, tq, p, nitems);
   ++*launches;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -82,6 +82,8 @@ rxl_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // inputs written by the previous kernel on the stream
+  griddep_launch_dependents();
   // this CTA's 64-wide k-steps [kb, ke)
   const int nk_all = p.K / 64;
   const int kb = z * nk_all / p.splits, ke = (z + 1) * nk_all / p.splits, nk = ke - kb;
@@ -213,6 +215,8 @@ __global__ void __launch_bounds__(256) gemm_finalize_kernel(const float *__restr
                                                             const __nv_bfloat16 *__restrict__ bias, int relu,
                                                             const __nv_bfloat16 *__restrict__ residual,
                                                             __nv_bfloat16 *__restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
   const long long n8 = rows * (N / 8), plane = rows * N;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n8;
        e += (long long)gridDim.x * blockDim.x) {
@@ -282,6 +286,8 @@ __global__ void __launch_bounds__(1024) gemm_finalize_ln_kernel(const float *__r
                                                                 const __nv_bfloat16 *__restrict__ gamma,
                                                                 const __nv_bfloat16 *__restrict__ beta, float eps,
                                                                 __nv_bfloat16 *__restrict__ y) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[32];
   const long long row = blockIdx.x;
   const int c = threadIdx.x;  // 16-byte chunk of the row; blockDim.x == N / 8
@@ -351,6 +357,8 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const __nv_bfloat16 *__r
                                                         const __nv_bfloat16 *__restrict__ beta,
                                                         __nv_bfloat16 *__restrict__ y, long long rows,
                                                         int d, float eps) {
+  griddep_wait();
+  griddep_launch_dependents();
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -489,35 +497,32 @@ cudaError_t launch_tc_gemm(int B, int R, int K, int N, const void *a, bool a_hea
   p.splits = (int)S;
   p.partials = partials;
   const unsigned grid = (unsigned)(tiles * S);
-  if (a_heads)
-    rxl_gemm_kernel<true><<<grid, G_THREADS, G_SMEM, st>>>(ta, tw, p);
-  else
-    rxl_gemm_kernel<false><<<grid, G_THREADS, G_SMEM, st>>>(ta, tw, p);
+  const long long rows = (long long)B * R;
+  cudaError_t e = a_heads ? launch_ex(rxl_gemm_kernel<true>, dim3(grid), dim3(G_THREADS), G_SMEM, st, 1, ta, tw, p)
+                          : launch_ex(rxl_gemm_kernel<false>, dim3(grid), dim3(G_THREADS), G_SMEM, st, 1, ta, tw, p);
   ++*launches;
+  if (e != cudaSuccess) return e;
+  const __nv_bfloat16 *bias16 = (const __nv_bfloat16 *)bias, *res16 = (const __nv_bfloat16 *)residual;
+  const __nv_bfloat16 *g16 = (const __nv_bfloat16 *)ln_gamma, *b16 = (const __nv_bfloat16 *)ln_beta;
+  const bool fused_ln = ln_out && S > 1 && N / 8 <= 1024;
   if (S > 1) {
     long long blocks = (per_split / 8 + 255) / 256;
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-    if (ln_out && N / 8 <= 1024)  // the sum of the partials and the LayerNorm in one pass over the rows
-      gemm_finalize_ln_kernel<<<(unsigned)((long long)B * R), (unsigned)(N / 8), 0, st>>>(
-          partials, (int)S, (long long)B * R, N, (const __nv_bfloat16 *)bias, relu ? 1 : 0,
-          (const __nv_bfloat16 *)residual, (const __nv_bfloat16 *)ln_gamma, (const __nv_bfloat16 *)ln_beta,
-          ln_eps, (__nv_bfloat16 *)ln_out);
+    if (fused_ln)  // the sum of the partials and the LayerNorm in one pass over the rows
+      e = launch_ex(gemm_finalize_ln_kernel, dim3((unsigned)rows), dim3((unsigned)(N / 8)), 0, st, 1,
+                    (const float *)partials, (int)S, rows, N, bias16, relu ? 1 : 0, res16, g16, b16, ln_eps,
+                    (__nv_bfloat16 *)ln_out);
     else
-      gemm_finalize_kernel<<<(unsigned)blocks, 256, 0, st>>>(partials, (int)S, (long long)B * R, N,
-                                                            (const __nv_bfloat16 *)bias, relu ? 1 : 0,
-                                                            (const __nv_bfloat16 *)residual, (__nv_bfloat16 *)out);
+      e = launch_ex(gemm_finalize_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, (const float *)partials,
+                    (int)S, rows, N, bias16, relu ? 1 : 0, res16, (__nv_bfloat16 *)out);
     ++*launches;
-    if (ln_out && N / 8 > 1024) {
-      layernorm_kernel<<<(unsigned)(((long long)B * R + 7) / 8), 256, 0, st>>>(
-          (const __nv_bfloat16 *)out, (const __nv_bfloat16 *)ln_gamma, (const __nv_bfloat16 *)ln_beta,
-          (__nv_bfloat16 *)ln_out, (long long)B * R, N, ln_eps);
-      ++*launches;
-    }
-  } else if (ln_out) {
-    layernorm_kernel<<<(unsigned)(((long long)B * R + 7) / 8), 256, 0, st>>>(
-        (const __nv_bfloat16 *)out, (const __nv_bfloat16 *)ln_gamma, (const __nv_bfloat16 *)ln_beta,
-        (__nv_bfloat16 *)ln_out, (long long)B * R, N, ln_eps);
+    if (e != cudaSuccess) return e;
+  }
+  if (ln_out && !fused_ln) {
+    e = launch_ex(layernorm_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, 1,
+                  (const __nv_bfloat16 *)out, g16, b16, (__nv_bfloat16 *)ln_out, rows, N, ln_eps);
     ++*launches;
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

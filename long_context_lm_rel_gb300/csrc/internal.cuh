@@ -10,6 +10,34 @@
 
 namespace rxl {
 
+// Launches k (optionally as clusters of `cluster` CTAs) with programmatic
+// dependent launch allowed: its CTAs may start their setup while the previous
+// kernel on the stream finishes; the kernels wait for it (griddep_wait)
+// before their first global-memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             unsigned cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  unsigned n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 // Validated shape of one attention call, as the kernels see it.
 struct AttnShape {
   int B, H, L;

@@ -10,6 +10,7 @@
 // move consecutive vectors of a row, so each warp reads and writes whole
 // 128-byte lines. The grid is a grid-stride loop sized to the SM count.
 #include "internal.cuh"
+#include "sm103.cuh"
 
 namespace rxl {
 
@@ -17,6 +18,8 @@ __global__ void __launch_bounds__(256) mem_update_kernel(
     int4 *__restrict__ data, long long plane_stride_v, int cap, int vpr,
     const int4 *__restrict__ src, long long src_plane_stride_v, int src_row0, int nrows,
     int dst_row0, long long total_v) {
+  sm103::griddep_wait();
+  sm103::griddep_launch_dependents();
   const long long per_plane = (long long)nrows * vpr;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total_v;
        e += (long long)gridDim.x * blockDim.x) {
@@ -44,11 +47,12 @@ cudaError_t launch_mem_update(void *data, int planes, int cap, int D, long long 
   long long blocks = (total + 255) / 256;
   const long long cap_blocks = (long long)sms * 8;  // 8 resident 256-thread blocks per SM
   if (blocks > cap_blocks) blocks = cap_blocks;
-  mem_update_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-      (int4 *)data, plane_stride * elem_bytes / 16, cap, vpr, (const int4 *)src,
-      src_plane_stride * elem_bytes / 16, src_row0, nrows, dst_row0, total);
+  const cudaError_t e = launch_ex(mem_update_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, (int4 *)data,
+                                  (long long)(plane_stride * elem_bytes / 16), cap, vpr, (const int4 *)src,
+                                  (long long)(src_plane_stride * elem_bytes / 16), src_row0, nrows, dst_row0,
+                                  total);
   ++*launches;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace rxl

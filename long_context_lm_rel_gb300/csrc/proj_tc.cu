@@ -161,6 +161,8 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
   cluster_sync();  // both CTAs' barriers and TMEM are ready
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // inputs written by the previous kernel on the stream
+  griddep_launch_dependents();
   const int nk = p.d / 64;
   const int total = nj * nk;  // k-steps of this pair
 
@@ -391,8 +393,8 @@ cudaError_t launch_tc_proj(const AttnShape &s, int d, const void *h_mem, const v
   });
   if (max_pairs <= 0) return cudaErrorLaunchOutOfResources;
   const long long pairs = units < max_pairs ? units : max_pairs;
-  cfg.gridDim = dim3((unsigned)(2 * pairs));
-  cudaError_t e = cudaLaunchKernelEx(&cfg, rxl_proj_kernel, thm, thc, twq, twk, twv, p, (int)units);
+  cudaError_t e = launch_ex(rxl_proj_kernel, dim3((unsigned)(2 * pairs)), dim3(P_THREADS), P_SMEM, st, 2, thm, thc,
+                            twq, twk, twv, p, (int)units);
   ++*launches;
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -25,6 +25,20 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start its
+// setup while the previous kernel on the stream finishes. griddep_wait()
+// returns once that kernel (and so every earlier one) has completed and its
+// memory is visible; without the launch attribute it returns at once. Every
+// kernel here calls it before its first global-memory access.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream launch once every CTA of this grid has
+// called it (or exited): its CTAs take free SMs and run their setup, then
+// wait in griddep_wait() for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
