@@ -42,7 +42,7 @@ FLOP_FWD_PAIR, FLOP_BWD_PAIR = 6 * DH, 12 * DH
 # dram__bytes_read.sum + dram__bytes_write.sum of one rxl_bwd_main_kernel
 # launch at cfg3: 45.15 MB measured by ncu at B=4, times 4 (the work items
 # scale with the batch)
-TRAFFIC_BWD_MAIN = 4 * 45.15e6
+TRAFFIC_BWD_MAIN = 4 * 45.17e6
 
 
 def visible_pairs(b, h, l, m):
