@@ -32,6 +32,10 @@
  *     and never synchronise. Arguments are checked before anything is
  *     launched; on any error nothing is launched and no output is touched.
  *     Device faults surface at the caller's next synchronisation.
+ *   - Stream order is kept. The sm_103a kernels are launched with
+ *     programmatic dependent launch: a kernel may start its on-chip setup
+ *     while the previous kernel on the stream finishes, and touches no
+ *     device memory before that kernel has completed.
  *   - Thread safety: calls may be made from several host threads; the only
  *     shared host state is a cache of TMA descriptors guarded by a mutex.
  */
