@@ -22,8 +22,9 @@
 // M = 256, N = 256 MMA per k-step over two blocks that share their W columns,
 // each SM loading its own rows and half of the columns), with one producer
 // warp, one MMA warp and two accumulators, so pipeline fill and epilogue of
-// one unit overlap the main loop of the next; the epilogue turns rows around
-// in shared memory so that each store writes whole 128-byte head rows.
+// one unit overlap the main loop of the next; the epilogue stages each head's
+// 32 rows per warp as a 128-byte-swizzled box and writes it with one TMA
+// store.
 #include <math.h>
 
 #include <mutex>
@@ -45,8 +46,10 @@ constexpr uint32_t P_A_BYTES = 128 * 64 * 2;     // 16 KB: this CTA's 128 rows
 constexpr uint32_t P_B_BYTES = 2 * 64 * 64 * 2;  // 16 KB: this CTA's 128 of the pair's 256 columns
 constexpr uint32_t P_STAGE = P_A_BYTES + P_B_BYTES;
 constexpr uint32_t P_BAR = P_STAGES * P_STAGE;
-constexpr uint32_t P_STG = P_BAR + 256;  // epilogue staging: 4 warps x 32 rows x 128 B
-constexpr uint32_t P_SMEM = P_STG + 4 * 4096 + 1024;
+// epilogue staging: 4 warps x 2 buffers x 32 rows x 128 B, 1024-byte aligned
+// (the layout of a 128-byte-swizzled TMA box)
+constexpr uint32_t P_STG = P_BAR + 1024;
+constexpr uint32_t P_SMEM = P_STG + 4 * 8192 + 1024;
 
 __device__ int g_proj_error;
 
@@ -62,10 +65,10 @@ struct ProjParams {
 // heads and rows; `store` is false for the second CTA of a pair whose list
 // has an odd number of row tiles (it repeats the first CTA's rows).
 struct ProjItem {
-  const CUtensorMap *amap, *wmap;
+  const CUtensorMap *amap, *wmap, *omap;
   __nv_bfloat16 *out;
   int b, h0, nh, arow, orow0, nvalid, orows;
-  bool store;
+  bool store, kv;
 };
 
 // Unit u = (column tile nt, pair of row tiles): the row tiles of Q over all
@@ -73,7 +76,9 @@ struct ProjItem {
 // both CTAs of a pair use the same W columns.
 __device__ __forceinline__ ProjItem proj_item(const ProjParams &p, int u, int rank, const CUtensorMap *tm_hmem,
                                               const CUtensorMap *tm_hcur, const CUtensorMap *tm_wq,
-                                              const CUtensorMap *tm_wk, const CUtensorMap *tm_wv) {
+                                              const CUtensorMap *tm_wk, const CUtensorMap *tm_wv,
+                                              const CUtensorMap *tm_oq, const CUtensorMap *tm_ok,
+                                              const CUtensorMap *tm_ov) {
   ProjItem it;
   const int nt = u % p.NT;
   int q = u / p.NT;
@@ -111,6 +116,8 @@ __device__ __forceinline__ ProjItem proj_item(const ProjParams &p, int u, int ra
     it.orows = p.cap + p.L;
   }
   it.wmap = which == 0 ? tm_wq : (which == 1 ? tm_wk : tm_wv);
+  it.omap = which == 0 ? tm_oq : (which == 1 ? tm_ok : tm_ov);
+  it.kv = which != 0;
   it.out = p.out[which];
   return it;
 }
@@ -125,7 +132,9 @@ __device__ __forceinline__ ProjItem proj_item(const ProjParams &p, int u, int ra
 __global__ void __launch_bounds__(P_THREADS, 1)
 rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_constant__ CUtensorMap tm_hcur,
                 const __grid_constant__ CUtensorMap tm_wq, const __grid_constant__ CUtensorMap tm_wk,
-                const __grid_constant__ CUtensorMap tm_wv, const ProjParams p, int nunits) {
+                const __grid_constant__ CUtensorMap tm_wv, const __grid_constant__ CUtensorMap tm_oq,
+                const __grid_constant__ CUtensorMap tm_ok, const __grid_constant__ CUtensorMap tm_ov,
+                const ProjParams p, int nunits) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -133,7 +142,7 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
   const int rank = (int)(blockIdx.x & 1), pair = (int)(blockIdx.x >> 1), P = (int)(gridDim.x >> 1);
   const int nj = pair < nunits ? (nunits - 1 - pair) / P + 1 : 0;
   auto item = [&](int j) {
-    return proj_item(p, pair + j * P, rank, &tm_hmem, &tm_hcur, &tm_wq, &tm_wk, &tm_wv);
+    return proj_item(p, pair + j * P, rank, &tm_hmem, &tm_hcur, &tm_wq, &tm_wk, &tm_wv, &tm_oq, &tm_ok, &tm_ov);
   };
 
   const uint32_t bar_full = sb + P_BAR;                // [S] (first CTA) the stage landed in both CTAs
@@ -250,12 +259,15 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
     __syncwarp();
   } else if (warp < 4) {
     // ---- epilogue: TMEM lane = row of this CTA's block. Each warp turns its
-    // 32 rows around in shared memory (16-byte chunks xor-swizzled by row),
-    // so one store instruction writes 4 whole 128-byte head rows.
-    const uint32_t stg = sb + P_STG + warp * 4096;
-    const uint32_t srow = stg + lane * 128;
+    // 32 rows of a head around in shared memory (16-byte chunks xor-swizzled
+    // by row: a 128-byte-swizzled box) and one lane stores the box with the
+    // TMA; two buffers per warp, so a head is staged while the previous
+    // head's box is read out. A K/V box that reaches past the block's valid
+    // rows (their successors belong to another block) is stored row by row.
+    const uint32_t stg0 = sb + P_STG + warp * 8192;
     const uint32_t acce0 = mapa_shared(bar_acce, 0);
     const int rr0 = lane >> 3, c = lane & 7;
+    int nst = 0;  // boxes this warp handed to the TMA
     bool ok = true;
     for (int j = 0; j < nj; ++j) {
       const ProjItem it = item(j);
@@ -263,6 +275,9 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
       ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_accf + 8 * (j & 1), (j >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
+      // Q rows past the block are past L (the box is clipped); K/V rows are not
+      const bool any = warp * 32 < it.nvalid;
+      const bool by_tma = any && (!it.kv || warp * 32 + 32 <= it.nvalid);
       for (int hh = 0; hh < it.nh; ++hh) {
         uint32_t lo[32], hi[32];
         tmem_ld32(trow + 64 * hh, lo);
@@ -273,7 +288,11 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(acce0 + 8 * (j & 1));
         }
-        if (!it.store) continue;
+        if (!it.store || !any) continue;
+        const uint32_t stg = stg0 + (nst & 1) * 4096, srow = stg + lane * 128;
+        // the box stored from this buffer two boxes ago has been read
+        if (lane == 0) bulk_wait_read_but_latest();
+        __syncwarp();
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           st_shared_v4(srow + ((e ^ (lane & 7)) << 4),
@@ -287,18 +306,30 @@ rxl_proj_kernel(const __grid_constant__ CUtensorMap tm_hmem, const __grid_consta
                        pack_bf16(__uint_as_float(hi[8 * e + 4]), __uint_as_float(hi[8 * e + 5])),
                        pack_bf16(__uint_as_float(hi[8 * e + 6]), __uint_as_float(hi[8 * e + 7])));
         }
-        __syncwarp();
-        __nv_bfloat16 *obase =
-            it.out + (((size_t)it.b * p.H + it.h0 + hh) * it.orows + it.orow0 + warp * 32) * DH + c * 8;
+        if (by_tma) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(it.omap, 0, it.orow0 + warp * 32, it.b * p.H + it.h0 + hh, stg);
+            bulk_commit();
+          }
+          ++nst;
+        } else {
+          __syncwarp();
+          __nv_bfloat16 *obase =
+              it.out + (((size_t)it.b * p.H + it.h0 + hh) * it.orows + it.orow0 + warp * 32) * DH + c * 8;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + rr0;
-          const uint4 v = ld_shared_v4(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
-          if (warp * 32 + rr < it.nvalid) *(uint4 *)(obase + rr * DH) = v;
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + rr0;
+            const uint4 v = ld_shared_v4(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
+            if (warp * 32 + rr < it.nvalid) *(uint4 *)(obase + rr * DH) = v;
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
+    if (lane == 0) bulk_wait_all();  // every box written before the CTA leaves
+    __syncwarp();
     if (!ok) atomicExch(&g_proj_error, 2);
   }
   tc_fence_before();
@@ -345,9 +376,10 @@ bool make_map(CUtensorMap *m, const void *base, int planes, int rows, int inner,
 cudaError_t launch_tc_proj(const AttnShape &s, int d, const void *h_mem, const void *h_cur,
                            const void *wq, const void *wk, const void *wv, void *q, void *k, void *v,
                            cudaStream_t st, int *launches) {
-  CUtensorMap thm, thc, twq, twk, twv;
+  CUtensorMap thm, thc, twq, twk, twv, toq, tok, tov;
   const int n = s.H * DH;
-  if (!make_map(&thc, h_cur, s.B, s.L, d, BQ) ||
+  if (!make_map(&toq, q, s.B * s.H, s.L, DH, 32) || !make_map(&tok, k, s.B * s.H, s.cap + s.L, DH, 32) ||
+      !make_map(&tov, v, s.B * s.H, s.cap + s.L, DH, 32) || !make_map(&thc, h_cur, s.B, s.L, d, BQ) ||
       !make_map(&thm, s.cap > 0 ? h_mem : h_cur, s.B, s.cap > 0 ? s.cap : s.L, d, BQ) ||
       !make_map(&twq, wq, 1, d, n, 64) || !make_map(&twk, wk, 1, d, n, 64) ||
       !make_map(&twv, wv, 1, d, n, 64))
@@ -394,7 +426,7 @@ cudaError_t launch_tc_proj(const AttnShape &s, int d, const void *h_mem, const v
   if (max_pairs <= 0) return cudaErrorLaunchOutOfResources;
   const long long pairs = units < max_pairs ? units : max_pairs;
   cudaError_t e = launch_ex(rxl_proj_kernel, dim3((unsigned)(2 * pairs)), dim3(P_THREADS), P_SMEM, st, 2, thm, thc,
-                            twq, twk, twv, p, (int)units);
+                            twq, twk, twv, toq, tok, tov, p, (int)units);
   ++*launches;
   return e != cudaSuccess ? e : cudaGetLastError();
 }

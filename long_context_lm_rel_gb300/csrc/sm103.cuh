@@ -181,6 +181,15 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, int c0
       "r"(c0), "r"(c1), "r"(c2), "r"(src)
       : "memory");
 }
+// Shared-memory box into global memory (bulk group); the box must not start
+// at a negative coordinate.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int c0, int c1, int c2, uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk group has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() {
