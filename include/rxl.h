@@ -55,7 +55,7 @@ typedef struct CUstream_st *rxl_stream_t;
 typedef enum {
   RXL_OK = 0,
   RXL_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative or inconsistent size */
-  RXL_ERR_UNSUPPORTED = 2,        /* valid request this build does not implement (d_h != 64, dtype) */
+  RXL_ERR_UNSUPPORTED = 2,        /* a valid request the library does not implement (d_h != 64, dtype) */
   RXL_ERR_MISALIGNED = 3,         /* pointer or row stride not 16-byte aligned */
   RXL_ERR_WORKSPACE_TOO_SMALL = 4,
   RXL_ERR_CUDA = 5                /* a CUDA call or launch failed (see rxl_last_cuda_error) */
