@@ -145,3 +145,69 @@ def test_unmodified_oracle_passes_battery(tmp_path):
 def test_mutant_is_caught(tmp_path, name):
     failed = battery(_build(tmp_path, name, MUTANTS[name]))
     assert failed, f"mutant {name} slipped through every pin"
+
+
+# ------------------------------------- the evaluation layer (Python oracle)
+# The same idea for oracle.layer_fwd: a copy of the oracle package's source
+# with one mistake in the feed-forward sublayer, loaded as its own module, must
+# fail one of the feed-forward pins.
+
+PY_SRC = oracle.__file__
+LAYER_MUTANTS = {
+    "ffn_no_relu": ("z = np.maximum(x1n @ _f64(w[\"w_1\"]) + _f64(w[\"b_1\"]), 0.0)",
+                    "z = x1n @ _f64(w[\"w_1\"]) + _f64(w[\"b_1\"])"),
+    "ffn_bias_after_relu": ("z = np.maximum(x1n @ _f64(w[\"w_1\"]) + _f64(w[\"b_1\"]), 0.0)",
+                            "z = np.maximum(x1n @ _f64(w[\"w_1\"]), 0.0) + _f64(w[\"b_1\"])"),
+    "ffn_w1_w2_swapped": ("z = np.maximum(x1n @ _f64(w[\"w_1\"]) + _f64(w[\"b_1\"]), 0.0)\n"
+                          "    x2 = x1n + z @ _f64(w[\"w_2\"]) + _f64(w[\"b_2\"])",
+                          "z = np.maximum(x1n @ _f64(w[\"w_2\"]) + _f64(w[\"b_1\"]), 0.0)\n"
+                          "    x2 = x1n + z @ _f64(w[\"w_1\"]) + _f64(w[\"b_2\"])"),
+    "ffn_relu_after_w2": ("z = np.maximum(x1n @ _f64(w[\"w_1\"]) + _f64(w[\"b_1\"]), 0.0)\n"
+                          "    x2 = x1n + z @ _f64(w[\"w_2\"]) + _f64(w[\"b_2\"])",
+                          "z = x1n @ _f64(w[\"w_1\"]) + _f64(w[\"b_1\"])\n"
+                          "    x2 = x1n + np.maximum(z @ _f64(w[\"w_2\"]), 0.0) + _f64(w[\"b_2\"])"),
+    "ffn_no_residual": ("x2 = x1n + z @ _f64(w[\"w_2\"]) + _f64(w[\"b_2\"])",
+                        "x2 = z @ _f64(w[\"w_2\"]) + _f64(w[\"b_2\"])"),
+}
+
+
+def _py_oracle(tmp_path, name, edit):
+    import importlib.util
+    with open(PY_SRC) as f:
+        src = f.read()
+    if edit is not None:
+        old, new = edit
+        assert src.count(old) == 1, f"mutation anchor not found: {old}"
+        src = src.replace(old, new)
+    pkg = tmp_path / f"oracle_{name}"
+    pkg.mkdir()
+    (pkg / "__init__.py").write_text(src)
+    spec = importlib.util.spec_from_file_location(f"oracle_{name}", pkg / "__init__.py")
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod._lib = oracle.load()  # the C part is unchanged: reuse the built library
+    return mod
+
+
+def layer_battery(mod):
+    from tests.test_oracle_pins import ffn_pin_absolute_value, ffn_pin_bias_before_relu, ffn_pin_w1_then_w2
+    pins = {"abs": ffn_pin_absolute_value, "bias": ffn_pin_bias_before_relu, "order": ffn_pin_w1_then_w2}
+    failed = []
+    for n, f in pins.items():
+        try:
+            ok = f(mod)
+        except ValueError:  # shapes that no longer fit (d != d_ff) also expose the mistake
+            ok = False
+        if not ok:
+            failed.append(n)
+    return failed
+
+
+def test_unmodified_layer_passes_ffn_pins(tmp_path):
+    assert layer_battery(_py_oracle(tmp_path, "control", None)) == []
+
+
+@pytest.mark.parametrize("name", sorted(LAYER_MUTANTS))
+def test_layer_mutant_is_caught(tmp_path, name):
+    failed = layer_battery(_py_oracle(tmp_path, name, LAYER_MUTANTS[name]))
+    assert failed, f"layer mutant {name} slipped through every feed-forward pin"

@@ -502,3 +502,109 @@ def test_layer_merges_heads_in_column_order():
     x1 = hi + np.concatenate([o[:, h] for h in range(H)], axis=-1)
     ref = oracle.layer_norm(oracle.layer_norm(x1, np.ones(d), np.zeros(d)), np.ones(d), np.zeros(d))
     assert np.allclose(oracle.layer_fwd(hm, hi, w, H, 0.5, nthreads=1), ref, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------- the feed-forward sublayer
+# With W_O = 0 the attention sublayer contributes nothing (x1 = h_in), so
+# x1n = LN1(h_in) is known without the attention and the feed-forward
+# sublayer x2 = x1n + ReLU(x1n W_1 + b_1) W_2 + b_2 can be pinned to closed
+# forms; LN2 (gamma = 1, beta = 0) of x2 is what the layer returns. Each pin
+# takes the oracle module, so that the mutant tests can run it on a copy.
+
+def _ffn_layer(mod, rng, d, dff, H=2):
+    dh = d // H
+    m, L = 3, 4
+    w = _layer_weights(rng, H, dh, d, dff, m, L)
+    w["w_o"] = np.zeros_like(w["w_o"])
+    w["ln2_gamma"], w["ln2_beta"] = np.ones(d), np.zeros(d)
+    hm, hi = rand(rng, 2, m, d), rand(rng, 2, L, d)
+    x1n = mod.layer_norm(hi, w["ln1_gamma"], w["ln1_beta"])
+    return w, hm, hi, x1n, H
+
+
+def _ln_plain(x):
+    mu = x.mean(-1, keepdims=True)
+    return (x - mu) / np.sqrt(((x - mu) ** 2).mean(-1, keepdims=True) + 1e-5)
+
+
+def ffn_pin_absolute_value(mod) -> bool:
+    """W_1 = [I | -I], b_1 = 0, W_2 = [I ; I], b_2 = 0: ReLU(x) + ReLU(-x) = |x|,
+    so x2 = x1n + |x1n| = 2 max(x1n, 0). Without the ReLU the pair cancels
+    (x2 = x1n); a ReLU after W_2 instead of after W_1 gives ReLU(x - x) = 0."""
+    rng = np.random.default_rng(21)
+    d = 8
+    w, hm, hi, x1n, H = _ffn_layer(mod, rng, d, 2 * d)
+    eye = np.eye(d)
+    w["w_1"], w["b_1"] = np.concatenate([eye, -eye], 1), np.zeros(2 * d)
+    w["w_2"], w["b_2"] = np.concatenate([eye, eye], 0), np.zeros(d)
+    assert (x1n < 0).any() and (x1n > 0).any()  # the ReLU clips somewhere
+    out = mod.layer_fwd(hm, hi, w, H, 0.5, nthreads=1)
+    return bool(np.allclose(out, _ln_plain(2 * np.maximum(x1n, 0)), rtol=0, atol=1e-12))
+
+
+def ffn_pin_bias_before_relu(mod) -> bool:
+    """W_1 = 0, b_1 = c with both signs: the hidden units are ReLU(c) (a bias
+    added after the ReLU would give c); W_2 = I, b_2 = e: x2 = x1n + ReLU(c) + e."""
+    rng = np.random.default_rng(22)
+    d = 8
+    w, hm, hi, x1n, H = _ffn_layer(mod, rng, d, d)
+    c = np.array([1.5, -2.0, 0.25, -0.5, 3.0, -1.0, 0.75, -4.0])
+    e = rand(rng, d, std=0.3)
+    w["w_1"], w["b_1"] = np.zeros((d, d)), c
+    w["w_2"], w["b_2"] = np.eye(d), e
+    out = mod.layer_fwd(hm, hi, w, H, 0.5, nthreads=1)
+    return bool(np.allclose(out, _ln_plain(x1n + np.maximum(c, 0) + e), rtol=0, atol=1e-12))
+
+
+def ffn_pin_w1_then_w2(mod) -> bool:
+    """d = d_ff, W_1 = diag(a) with a of both signs, W_2 = a cyclic shift S
+    (column k of x S is column k-1 of x): x2 = x1n + ReLU(x1n diag(a)) S.
+    Swapped products (ReLU(x1n S) diag(a)) differ: S is not diagonal and a
+    is not constant."""
+    rng = np.random.default_rng(23)
+    d = 8
+    w, hm, hi, x1n, H = _ffn_layer(mod, rng, d, d)
+    a = np.array([1.0, -1.0, 2.0, 0.5, -3.0, 1.5, -0.25, 4.0])
+    S = np.roll(np.eye(d), 1, axis=1)
+    w["w_1"], w["b_1"] = np.diag(a), np.zeros(d)
+    w["w_2"], w["b_2"] = S, np.zeros(d)
+    want = _ln_plain(x1n + np.roll(np.maximum(x1n * a, 0), 1, axis=-1))
+    swapped = _ln_plain(x1n + np.maximum(np.roll(x1n, 1, axis=-1), 0) * a)
+    assert not np.allclose(want, swapped, atol=1e-3)
+    out = mod.layer_fwd(hm, hi, w, H, 0.5, nthreads=1)
+    return bool(np.allclose(out, want, rtol=0, atol=1e-12))
+
+
+def test_ffn_relu_pair_gives_absolute_value():
+    assert ffn_pin_absolute_value(oracle)
+
+
+def test_ffn_bias_enters_before_the_relu():
+    assert ffn_pin_bias_before_relu(oracle)
+
+
+def test_ffn_applies_w1_then_w2():
+    assert ffn_pin_w1_then_w2(oracle)
+
+
+def test_ffn_random_weights_against_elementwise_loops():
+    """Random weights (ReLU clipping part of the hidden units): every element
+    of x2 against a plain loop over the hidden units."""
+    rng = np.random.default_rng(24)
+    d, dff = 8, 12
+    w, hm, hi, x1n, H = _ffn_layer(oracle, rng, d, dff)
+    B, L = x1n.shape[:2]
+    x2 = np.zeros_like(x1n)
+    clipped = 0
+    for b in range(B):
+        for i in range(L):
+            for o_ in range(d):
+                acc = x1n[b, i, o_] + w["b_2"][o_]
+                for f in range(dff):
+                    pre = w["b_1"][f] + sum(x1n[b, i, k] * w["w_1"][k, f] for k in range(d))
+                    clipped += pre < 0
+                    acc += max(pre, 0.0) * w["w_2"][f, o_]
+                x2[b, i, o_] = acc
+    assert clipped > 0
+    out = oracle.layer_fwd(hm, hi, w, H, 0.5, nthreads=1)
+    assert np.allclose(out, _ln_plain(x2), rtol=0, atol=1e-11)
