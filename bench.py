@@ -39,10 +39,37 @@ WORKLOAD = "cfg3_bf16_B16H16_L512M512_dh64_fwd+bwd"
 B, H, L, M, DH = 16, 16, 512, 512, 64
 SCALE = 1.0 / math.sqrt(DH)
 FLOP_FWD_PAIR, FLOP_BWD_PAIR = 6 * DH, 12 * DH
-# dram__bytes_read.sum + dram__bytes_write.sum of one rxl_bwd_main_kernel
-# launch at cfg3: 45.15 MB measured by ncu at B=4, times 4 (the work items
-# scale with the batch)
-TRAFFIC_BWD_MAIN = 4 * 45.17e6
+# The backward main kernel's sources: a DRAM-traffic record in its profile
+# summary counts only while these files are unchanged since the capture.
+BWD_MAIN_SOURCES = ("long_context_lm_rel_gb300/csrc/attn_bwd_tc.cu", "long_context_lm_rel_gb300/csrc/tc_common.cuh",
+                    "long_context_lm_rel_gb300/csrc/sm103.cuh")
+BWD_MAIN_PROFILE = "profiles/bwd_main_kernel_B4H16L512M512.md"
+
+
+def sources_sha256(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_record(profile, sources):
+    """(bytes per launch at the profile's batch, batch) from the profile's
+    'traffic-record:' line if its source hash matches the current sources,
+    else (None, reason)."""
+    try:
+        with open(os.path.join(ROOT, profile)) as f:
+            lines = [ln for ln in f if ln.startswith("traffic-record:")]
+    except OSError:
+        return None, "no profile"
+    if not lines:
+        return None, "no traffic record in the profile"
+    rec = dict(kv.split("=", 1) for kv in lines[-1].split(":", 1)[1].split())
+    if rec.get("sha256") != sources_sha256(sources):
+        return None, "the kernel changed since the capture"
+    return (float(rec["bytes_per_launch"]), int(rec["batch"])), None
 
 
 def visible_pairs(b, h, l, m):
@@ -177,7 +204,7 @@ def run_ours(args, rank, world):
 
     import long_context_lm_rel_gb300 as rxl
     from long_context_lm_rel_gb300.multirank import max_over_ranks, replica_seed, whole_job_rate
-    from tests._harness import AttnCall, place_kv
+    from long_context_lm_rel_gb300.calls import AttnCall, place_kv
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -282,6 +309,23 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         return start.elapsed_time(end)
 
+    # the dominant kernel alone: the same steps again with the library's
+    # event pairs around each launch of the forward kernel and of the
+    # backward's main kernel (kept out of the headline pass: an event between
+    # two kernels stops the second from overlapping the first one's tail)
+    rxl.rxl_kernel_timing(True)
+    rxl.rxl_kernel_timing_read(rxl.RXL_KERNEL_FWD)
+    rxl.rxl_kernel_timing_read(rxl.RXL_KERNEL_BWD_MAIN)
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    rxl.rxl_kernel_timing(False)
+    kfwd_ms, kfwd_n = rxl.rxl_kernel_timing_read(rxl.RXL_KERNEL_FWD)
+    kbwd_ms, kbwd_n = rxl.rxl_kernel_timing_read(rxl.RXL_KERNEL_BWD_MAIN)
+    kernel_ms = {"rxl_fwd_tc_kernel": kfwd_ms / max(kfwd_n, 1), "rxl_bwd_main_kernel": kbwd_ms / max(kbwd_n, 1)}
+    kernel_ms = {k: max_over_ranks(v, world, device="cuda") for k, v in kernel_ms.items()}
+
     e2e_value = None
     if not args.no_e2e:
         e2e_run(max(args.warmup, 2))
@@ -293,7 +337,10 @@ def run_ours(args, rank, world):
     peak_tf, _, peak_kind = peaks()
     bwd_avg = sum(bwd_ms) / len(bwd_ms)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    achieved = pairs * FLOP_BWD_PAIR / (bwd_avg * 1e-3) / 1e12
+    kb = kernel_ms["rxl_bwd_main_kernel"]
+    achieved = pairs * FLOP_BWD_PAIR / (kb * 1e-3) / 1e12
+    rec, why = traffic_record(BWD_MAIN_PROFILE, BWD_MAIN_SOURCES)
+    traffic = rec[0] * B / rec[1] if rec else None
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True,
@@ -303,13 +350,18 @@ def run_ours(args, rank, world):
         "config": {"workload": WORKLOAD, "B": B, "H": H, "L": L, "M": M, "mem_len": m, "dh": DH,
                    "flop_per_step": flop_step, "l2": "flushed between steps (256 MiB write, outside events)",
                    "parallelism": f"{world} independent replicas (one per GPU)"},
-        "roofline": {"bound": "tensor",
-                     "kernel": "rxl_attn_bwd_ex call (3 launches; rxl_bwd_main_kernel is most of it)",
+        "roofline": {"bound": "tensor", "kernel": "rxl_bwd_main_kernel",
                      "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
-                     "traffic": TRAFFIC_BWD_MAIN if B == 16 else None,
-                     "traffic_note": "rxl_bwd_main_kernel dram read+write per launch: ncu capture at "
-                                     "B=4, times 4 (the items scale with B)",
+                     "traffic": traffic,
+                     "kernel_ms": kb, "algorithmic_flop_per_launch": pairs * FLOP_BWD_PAIR,
+                     "traffic_note": (f"dram read+write per launch from the ncu record in {BWD_MAIN_PROFILE} "
+                                      f"(batch {rec[1]}), scaled by the batch (the items scale with B)")
+                     if rec else f"null: {why}",
+                     "timing_note": "CUDA events around each launch of the kernel on its stream, in a second "
+                                    "pass of the same steps (L2 flushed between steps)",
                      "peak_kind": f"{peak_kind} bf16 burst"},
+        "kernels_ms": kernel_ms,
+        "fwd_kernel_tflops": pairs * FLOP_FWD_PAIR / (kernel_ms["rxl_fwd_tc_kernel"] * 1e-3) / 1e12,
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "pinned host buffers; inputs of step n+1 and outputs of step n-1 are copied on two copy "
@@ -318,10 +370,11 @@ def run_ours(args, rank, world):
     }
     if world == 1 and not args.no_stream:
         stream, mu = stream_cfg5()
-        _, hbm, kind = peaks()
-        mu.update({"peak": hbm, "frac": mu["achieved"] / hbm, "peak_kind": f"{kind} copy"})
         out["stream_cfg5"] = stream
-        out["mem_update_roofline"] = mu
+        out["mem_update_roofline"] = mem_update_hbm()
+        out["mem_update_l2_resident"] = mu
+        out["cfg2_stream"] = cfg2_stream(cpu=not args.no_cpu_baseline)
+        out["cfg4_pair"] = cfg4_pair(cpu=not args.no_cpu_baseline)
         out["window_recompute"] = window_recompute()
         out["reset_cfg3"] = reset_cfg3()
         out["proj_cfg3"] = proj_cfg3()
@@ -372,9 +425,9 @@ def stream_cfg5(segments=32, layers=16, reps_update=200):
                 d = rxl.make_desc(B5, H5, L5, M5, m, rk.head, SCALE, rxl.RXL_DTYPE_BF16)
                 rxl.rxl_attn_fwd(d, Q, K[n], V[n], R[n], U[n], VB[n], o, lse, st)
                 launches += rxl.rxl_last_launch_count()
-                for r_, t in ((rk, K[n]), (rv, V[n])):
-                    rxl.rxl_mem_update(r_, t.data_ptr() + M5 * DH * 2, kv * DH, L5, st)
-                    launches += rxl.rxl_last_launch_count()
+                rxl.rxl_mem_update_rings([rk, rv], [K[n].data_ptr() + M5 * DH * 2, V[n].data_ptr() + M5 * DH * 2],
+                                         [kv * DH, kv * DH], L5, st)
+                launches += rxl.rxl_last_launch_count()
         return launches, pairs
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -404,16 +457,20 @@ def stream_cfg5(segments=32, layers=16, reps_update=200):
     e1.record(st)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
-    # the memory update alone: back-to-back calls on a full ring, as a graph
+    # the memory update alone at the stream's call size (K and V rings of a
+    # layer in one launch, 2 MiB appended per ring): back-to-back calls on full
+    # rings, replayed as a graph. The 28 MB of rings stay in L2 here.
     rk = rxl.rxl_ring(K[0].data_ptr(), B5 * H5, M5, DH, kv * DH, rxl.RXL_DTYPE_BF16, 0, M5)
+    rv = rxl.rxl_ring(V[0].data_ptr(), B5 * H5, M5, DH, kv * DH, rxl.RXL_DTYPE_BF16, 0, M5)
+    srcs = [K[0].data_ptr() + M5 * DH * 2, V[0].data_ptr() + M5 * DH * 2]
     for _ in range(10):
-        rxl.rxl_mem_update(rk, K[0].data_ptr() + M5 * DH * 2, kv * DH, L5, st)
+        rxl.rxl_mem_update_rings([rk, rv], srcs, [kv * DH] * 2, L5, st)
     torch.cuda.synchronize()
     g_up = torch.cuda.CUDAGraph()
     with torch.cuda.stream(side):
         with torch.cuda.graph(g_up, stream=side):
             for _ in range(reps_update):
-                rxl.rxl_mem_update(rk, K[0].data_ptr() + M5 * DH * 2, kv * DH, L5, torch.cuda.current_stream())
+                rxl.rxl_mem_update_rings([rk, rv], srcs, [kv * DH] * 2, L5, torch.cuda.current_stream())
     torch.cuda.current_stream().wait_stream(side)
     g_up.replay()
     torch.cuda.synchronize()
@@ -422,17 +479,237 @@ def stream_cfg5(segments=32, layers=16, reps_update=200):
     e1.record(st)
     torch.cuda.synchronize()
     us = 1e3 * e0.elapsed_time(e1) / reps_update
-    bytes_call = 2 * B5 * H5 * min(L5, M5) * DH * 2   # read + write of the appended rows
+    bytes_call = 2 * 2 * B5 * H5 * min(L5, M5) * DH * 2   # K and V: read + write of the appended rows
     return {"workload": "cfg5_bf16_B4H16_L128M1600_16layer_32seg_fwd", "segments": segments, "layers": layers,
             "ms": ms, "tokens_per_s": B5 * L5 * segments / (ms * 1e-3),
             "attn_tflops": pairs * FLOP_FWD_PAIR / (ms * 1e-3) / 1e12, "gpu_launches": launches,
             "ms_eager": ms_eager, "tokens_per_s_eager": B5 * L5 * segments / (ms_eager * 1e-3),
             "note": "per segment and layer: K/V current rows copied in (torch), rxl_attn_fwd, "
-                    "2 x rxl_mem_update; ms = the whole stream captured once as a CUDA graph and "
-                    "replayed, ms_eager = the same calls issued one by one from Python"}, \
-           {"kernel": "mem_update_kernel", "bound": "hbm", "unit": "GB/s", "us_per_call": us,
+                    "rxl_mem_update_rings (K and V in one launch); ms = the whole stream captured once as a "
+                    "CUDA graph and replayed, ms_eager = the same calls issued one by one from Python"}, \
+           {"kernel": "mem_update_kernel", "residency": "l2", "unit": "GB/s", "us_per_call": us,
             "bytes_per_call": bytes_call, "achieved": bytes_call / (us * 1e-6) / 1e9,
-            "note": f"{reps_update} back-to-back calls on a full ring, replayed as a CUDA graph"}
+            "note": f"cfg5 call size (K+V of a layer, 4 MiB appended), {reps_update} back-to-back calls as a "
+                    "CUDA graph; the rings stay L2-resident, so this is launch/latency-bound, not an HBM figure"}
+
+
+def mem_update_hbm(reps=10):
+    """The memory-update kernel where HBM bounds it: the K and V rings of a
+    B16 H16 layer (256 planes, 128-byte rows) with 8192 rows of memory,
+    appending 4096 rows per ring per call (268 MB read + 268 MB written per
+    call), the L2 flushed (256 MiB write) before each timed call."""
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    planes, cap, Lm = 256, 8192, 4096
+    bf = torch.bfloat16
+    rings = [torch.zeros(planes, cap, DH, device="cuda", dtype=bf) for _ in range(2)]
+    srcs = [torch.randn(planes, Lm, DH, device="cuda").to(bf) for _ in range(2)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    rr = [rxl.rxl_ring(t.data_ptr(), planes, cap, DH, cap * DH, rxl.RXL_DTYPE_BF16, 0, cap) for t in rings]
+    for _ in range(3):
+        rxl.rxl_mem_update_rings(rr, srcs, [Lm * DH] * 2, Lm, st)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(st)
+        rxl.rxl_mem_update_rings(rr, srcs, [Lm * DH] * 2, Lm, st)
+        e1.record(st)
+    torch.cuda.synchronize()
+    us = 1e3 * sum(a.elapsed_time(b) for a, b in ev) / reps
+    bytes_call = 2 * 2 * planes * Lm * DH * 2
+    _, hbm, kind = peaks()
+    gbs = bytes_call / (us * 1e-6) / 1e9
+    return {"kernel": "mem_update_kernel", "residency": "hbm", "bound": "hbm", "unit": "GB/s",
+            "us_per_call": us, "bytes_per_call": bytes_call, "achieved": gbs, "peak": hbm, "frac": gbs / hbm,
+            "peak_kind": f"{kind} copy",
+            "workload": "K and V rings, 256 planes x 8192 rows x 64 bf16, 4096 rows appended per ring per call",
+            "note": "L2 flushed (256 MiB write) before each call, outside the events; bytes = read + write of the "
+                    "appended rows"}
+
+
+def pair_bytes(b, h, l, cap):
+    """Compulsory HBM bytes of one fwd_ex + bwd_ex pair (bf16 tensors, fp32
+    LSE and position gradients): every input read once, every output written
+    once: forward Q, K, V, R in, O, O_lo, LSE out; backward Q, K, V, R, O,
+    O_lo, LSE, dO in, dQ, dK, dV, dR, du, dv out."""
+    q = b * h * l * DH * 2
+    kv = b * h * (cap + l) * DH * 2
+    r = h * (cap + l) * DH * 2
+    lse = b * h * l * 4
+    fwd = q + 2 * kv + r + 2 * q + lse
+    bwd = (q + 2 * kv + r + 2 * q + lse + q) + (q + 2 * kv + 2 * r + 2 * h * DH * 4)
+    return fwd, bwd
+
+
+def cfg4_pair(reps=10, cpu=True):
+    """Configuration 4 (long memory, M = 5L): B8 H16 L256 M1280, the training
+    pair (fwd_ex + bwd_ex), seeded inputs of the configuration's
+    distributions, L2 flushed between steps. Near the ridge of the tensor and
+    HBM roofs, so both fractions are reported; the oracle is timed on the
+    whole workload on the host cores."""
+    import numpy as np
+    import torch
+    import long_context_lm_rel_gb300 as rxl  # noqa: F401
+    import rxl_inputs as gen
+    from long_context_lm_rel_gb300.calls import AttnCall, place_kv
+    w = gen.CFG4
+    p, sg, mem = gen.layer_params(w), gen.segment_inputs(w), gen.initial_memory(w)
+    cap = m = w.M
+    c = AttnCall(sg["q"], place_kv(mem["k_mem"], sg["k_cur"], cap, 0), place_kv(mem["v_mem"], sg["v_cur"], cap, 0),
+                 p["r"], p["u"], p["vb"], cap=cap, m=m, head=0, dtype="bf16", scale=w.scale)
+    c.fwd_ex().alloc_bwd(sg["do"])
+    st = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        c.fwd_ex(st).bwd_ex(st)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for e in ev:
+        flush.zero_()
+        e[0].record(st)
+        c.fwd_ex(st)
+        e[1].record(st)
+        c.bwd_ex(st)
+        e[2].record(st)
+    torch.cuda.synchronize()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / reps
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / reps
+    pairs = visible_pairs(w.B, w.H, w.L, m)
+    flop = pairs * (FLOP_FWD_PAIR + FLOP_BWD_PAIR)
+    tot = (fwd_ms + bwd_ms) * 1e-3
+    peak_tf, hbm, kind = peaks()
+    fb, bb = pair_bytes(w.B, w.H, w.L, cap)
+    tf = flop / tot / 1e12
+    out = {"workload": "cfg4_bf16_B8H16_L256M1280_dh64_fwd+bwd", "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+           "tokens_per_s": w.B * w.L / tot, "tflops": tf, "visible_pairs": pairs,
+           "roofline": {"tensor": {"achieved": tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf,
+                                   "peak_kind": f"{kind} bf16 burst"},
+                        "hbm": {"achieved": (fb + bb) / tot / 1e9, "peak": hbm, "unit": "GB/s",
+                                "frac": (fb + bb) / tot / 1e9 / hbm, "compulsory_bytes": fb + bb,
+                                "peak_kind": f"{kind} copy"}},
+           "note": "L2 flushed between steps; compulsory bytes = every input read and every output written once"}
+    if cpu:
+        import oracle
+        k = np.concatenate([mem["k_mem"], sg["k_cur"]], 2)
+        v = np.concatenate([mem["v_mem"], sg["v_cur"]], 2)
+        nthreads = os.cpu_count() or 1
+        t0 = time.perf_counter()
+        oracle.fwd(sg["q"], k, v, p["r"], p["u"], p["vb"], w.scale, nthreads=nthreads)
+        oracle.bwd(sg["q"], k, v, p["r"], p["u"], p["vb"], sg["do"], w.scale, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": flop / dt / 1e12, "unit": "TFLOP/s", "seconds": dt, "kind": "oracle",
+                               "cores": min(nthreads, w.B * w.H), "sample": "the whole workload, fwd+bwd"}
+    return out
+
+
+def cfg2_stream(reps=20, cpu=True):
+    """Configuration 2: one layer over 4 consecutive segments, B8 H8 L128
+    M128, memory empty at the start and rolled with Tail_M (K and V rings in
+    one launch) after each segment; per segment the training pair (fwd_ex +
+    bwd_ex). Device-generated normals (timing only; parity is in the tests).
+    The whole workload is L2-resident and small (64 query tiles per call), so
+    it is launch- and latency-bound: reported eager and as a CUDA graph."""
+    import numpy as np
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    B2, H2, L2, M2, segs = 8, 8, 128, 128, 4
+    kv = M2 + L2
+    g = torch.Generator(device="cuda").manual_seed(2)
+    bf = torch.bfloat16
+    mk = lambda *sh, std=0.125: (torch.randn(*sh, generator=g, device="cuda") * std).to(bf)
+    K, V = mk(B2, H2, kv, DH), mk(B2, H2, kv, DH)
+    R, U, VB = mk(H2, kv, DH, std=0.7), mk(H2, DH, std=0.02), mk(H2, DH, std=0.02)
+    seg_in = [dict(q=mk(B2, H2, L2, DH), k=mk(B2, H2, L2, DH), v=mk(B2, H2, L2, DH), do=mk(B2, H2, L2, DH, std=1.0))
+              for _ in range(segs)]
+    o, o_lo = torch.empty(B2, H2, L2, DH, device="cuda", dtype=bf), torch.empty(B2, H2, L2, DH, device="cuda", dtype=bf)
+    lse = torch.empty(B2, H2, L2, device="cuda", dtype=torch.float32)
+    dq = torch.empty_like(o)
+    dk, dv = torch.empty_like(K), torch.empty_like(V)
+    dr = torch.empty(H2, kv, DH, device="cuda", dtype=torch.float32)
+    du, dvb = torch.empty(H2, DH, device="cuda", dtype=torch.float32), torch.empty(H2, DH, device="cuda",
+                                                                                  dtype=torch.float32)
+    d0 = rxl.make_desc(B2, H2, L2, M2, M2, 0, SCALE, rxl.RXL_DTYPE_BF16)
+    wsb = rxl.rxl_attn_bwd_workspace_bytes(d0)
+    ws = torch.empty(wsb, device="cuda", dtype=torch.uint8)
+
+    def run(st):
+        rk = rxl.rxl_ring(K.data_ptr(), B2 * H2, M2, DH, kv * DH, rxl.RXL_DTYPE_BF16, 0, 0)
+        rv = rxl.rxl_ring(V.data_ptr(), B2 * H2, M2, DH, kv * DH, rxl.RXL_DTYPE_BF16, 0, 0)
+        pairs = launches = 0
+        for x in seg_in:
+            K[:, :, M2:].copy_(x["k"])
+            V[:, :, M2:].copy_(x["v"])
+            m = rk.len
+            d = rxl.make_desc(B2, H2, L2, M2, m, rk.head, SCALE, rxl.RXL_DTYPE_BF16)
+            rxl.rxl_attn_fwd_ex(d, x["q"], K, V, R, U, VB, o, o_lo, lse, st)
+            launches += rxl.rxl_last_launch_count()
+            rxl.rxl_attn_bwd_ex(d, x["q"], K, V, R, U, VB, o, o_lo, lse, x["do"], dq, dk, dv, dr, du, dvb, ws, wsb, st)
+            launches += rxl.rxl_last_launch_count()
+            rxl.rxl_mem_update_rings([rk, rv], [K.data_ptr() + M2 * DH * 2, V.data_ptr() + M2 * DH * 2],
+                                     [kv * DH] * 2, L2, st)
+            launches += rxl.rxl_last_launch_count()
+            pairs += visible_pairs(B2, H2, L2, m)
+        return pairs, launches
+
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        run(st)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        pairs, launches = run(st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms_eager = e0.elapsed_time(e1) / reps
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(st)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            run(torch.cuda.current_stream())
+    st.wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flop = pairs * (FLOP_FWD_PAIR + FLOP_BWD_PAIR)
+    peak_tf, _, kind = peaks()
+    tf = flop / (ms * 1e-3) / 1e12
+    out = {"workload": "cfg2_bf16_B8H8_L128M128_4seg_fwd+bwd", "ms": ms, "ms_eager": ms_eager,
+           "tokens_per_s": segs * B2 * L2 / (ms * 1e-3), "tflops": tf,
+           "tflops_eager": flop / (ms_eager * 1e-3) / 1e12, "visible_pairs": pairs, "gpu_launches": launches,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf,
+                        "peak_kind": f"{kind} bf16 burst"},
+           "note": "4 segments from empty memory, per segment: K/V current rows copied in, fwd_ex, bwd_ex, K+V ring "
+                   "update; ms = captured once as a CUDA graph and replayed, ms_eager = issued from Python; warm L2 "
+                   "(the whole workload is ~10 MB)"}
+    if cpu:
+        import oracle
+        import rxl_inputs as gen
+        wk = gen.CFG2
+        prm = gen.layer_params(wk)
+        mk_, mv_ = np.zeros((wk.B, wk.H, 0, wk.dh)), np.zeros((wk.B, wk.H, 0, wk.dh))
+        nthreads = os.cpu_count() or 1
+        t_cpu = 0.0
+        for sgi in range(wk.segments):
+            x = gen.segment_inputs(wk, sgi)
+            k = np.concatenate([mk_, x["k_cur"]], 2)
+            v = np.concatenate([mv_, x["v_cur"]], 2)
+            t0 = time.perf_counter()
+            oracle.fwd(x["q"], k, v, prm["r"], prm["u"], prm["vb"], wk.scale, nthreads=nthreads)
+            oracle.bwd(x["q"], k, v, prm["r"], prm["u"], prm["vb"], x["do"], wk.scale, nthreads=nthreads)
+            mk_, mv_ = oracle.tail_m(mk_, x["k_cur"], wk.M), oracle.tail_m(mv_, x["v_cur"], wk.M)
+            t_cpu += time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": flop / t_cpu / 1e12, "unit": "TFLOP/s", "seconds": t_cpu, "kind": "oracle",
+                               "cores": min(nthreads, wk.B * wk.H), "sample": "the whole 4-segment stream, fwd+bwd"}
+    return out
 
 
 def reset_cfg3(reps=10):
@@ -444,7 +721,7 @@ def reset_cfg3(reps=10):
     import numpy as np
     import torch
     import long_context_lm_rel_gb300 as rxl
-    from tests._harness import AttnCall, place_kv
+    from long_context_lm_rel_gb300.calls import AttnCall, place_kv
     x = make_inputs()
     cap = m = M
     mvis = [(0, 128, 384, 512)[b % 4] for b in range(B)]

@@ -141,10 +141,14 @@ rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k,
  *  - Same arguments, outputs and checks as rxl_attn_bwd minus the workspace.
  *  - Shapes whose backward needs more than the fixed scratch
  *    (rxl_attn_bwd_workspace_bytes(desc) > max) return
- *    RXL_ERR_WORKSPACE_TOO_SMALL without launching anything.
+ *    RXL_ERR_WORKSPACE_TOO_SMALL without launching anything. In bf16 the
+ *    need is about 516*B*H*L + 384*H*(M+L) + 32768*H bytes, so long memory
+ *    reaches the limit first (B=4, H=16, L=128, M=1600 needs ~15.4 MiB);
+ *    in f32 it is about 516*B*H*L bytes.
  *  - The first call on each device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    that device current) and caches it per context; make that first call
+ *    before any stream capture. After a device reset the next call looks the
+ *    address up again.
  *  - All calls share the one array per device and it keeps the last call's
  *    contents (nothing in it has to start at zero). Calls that overlap on the
  *    GPU, e.g. on two streams, race on it: serialise them.
@@ -300,6 +304,20 @@ typedef struct {
 rxl_status rxl_mem_update(rxl_ring *ring, const void *src, long long src_plane_stride, int L,
                           rxl_stream_t stream);
 
+/*
+ * The same update for n rings (1 <= n <= 8) in one launch, e.g. the K and V
+ * rings of a layer, which the recurrence advances together (eq. Tail_M is
+ * applied per layer to the states it caches). rings[r] is appended the L rows
+ * of srcs[r] (plane stride src_plane_strides[r] elements). All rings must
+ * share planes, cap, D, dtype, head and len (else RXL_ERR_INVALID_ARGUMENT)
+ * and be distinct structs; data pointers and strides may differ. On success
+ * every ring's head and len advance as in rxl_mem_update; on any error
+ * nothing is launched and no ring changes.
+ */
+rxl_status rxl_mem_update_rings(rxl_ring *const *rings, const void *const *srcs,
+                                const long long *src_plane_strides, int n, int L,
+                                rxl_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char *rxl_status_string(rxl_status status);
 
@@ -319,6 +337,41 @@ int rxl_last_launch_count(void);
  * clears them; -1 if the device could not be read.
  */
 int rxl_device_error_flags(void);
+
+/*
+ * Measurement hook (no counterpart in the paper). With timing enabled, every
+ * launch of the forward kernel (kernel 0: rxl_attn_fwd*, not the backward's
+ * recomputation) and of the backward's main kernel (kernel 1: the fused
+ * pass over the (query tile, key tile) pairs) is bracketed by a CUDA event
+ * pair recorded on the call's stream; up to 1024 launches per kernel are kept.
+ * rxl_kernel_timing_read waits for the recorded events, returns the summed
+ * device time in milliseconds and the number of timed launches, and clears
+ * them. The events sit between kernels, so a timed launch does not overlap
+ * the previous kernel's tail (programmatic dependent launch): timing is for
+ * measurement runs, off by default. Both return 0 or a cudaError_t value.
+ */
+int rxl_kernel_timing(int enable);
+int rxl_kernel_timing_read(int kernel, double *total_ms, int *launches);
+
+/*
+ * Testing hooks (no counterpart in the paper): they let a test exercise the
+ * failure paths above without faulting, trapping or hanging a GPU.
+ *
+ * rxl_test_fail_next_launch: the next kernel launch of any entry point (on
+ * any thread) is not made; it reports cuda_error instead (a cudaError_t
+ * value, 0 disarms), so that call returns RXL_ERR_CUDA with
+ * rxl_last_cuda_error() == cuda_error. One-shot.
+ *
+ * rxl_test_forward_wait_timeout: every bounded wait of the forward kernel
+ * gives up after wait_cycles SM clock cycles (<= 0 restores the default,
+ * about two seconds), and with withhold != 0 the kernel's softmax warps do
+ * not signal that the first item's query tiles are ready, so the producer's
+ * wait for it runs out: the kernel drains its copies, frees its tensor memory,
+ * exits and sets bit 0 of rxl_device_error_flags(). Stays in force until
+ * called again with (0, 0). Synchronous; returns 0 or a cudaError_t value.
+ */
+void rxl_test_fail_next_launch(int cuda_error);
+int rxl_test_forward_wait_timeout(long long wait_cycles, int withhold);
 
 #ifdef __cplusplus
 }

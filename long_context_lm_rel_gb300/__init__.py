@@ -75,6 +75,9 @@ def lib():
             L.rxl_attn_bwd.restype = ctypes.c_int
             L.rxl_mem_update.argtypes = [P(rxl_ring), vp, ctypes.c_longlong, ctypes.c_int, vp]
             L.rxl_mem_update.restype = ctypes.c_int
+            L.rxl_mem_update_rings.argtypes = [P(P(rxl_ring)), P(vp), P(ctypes.c_longlong), ctypes.c_int,
+                                               ctypes.c_int, vp]
+            L.rxl_mem_update_rings.restype = ctypes.c_int
             L.rxl_status_string.argtypes = [ctypes.c_int]
             L.rxl_status_string.restype = ctypes.c_char_p
             L.rxl_last_cuda_error.argtypes = []
@@ -98,6 +101,14 @@ def lib():
             L.rxl_layer_fwd.argtypes = [P(rxl_attn_desc), ctypes.c_int, ctypes.c_int, P(rxl_layer_weights)] \
                 + [vp] * 4 + [ctypes.c_size_t, vp]
             L.rxl_layer_fwd.restype = ctypes.c_int
+            L.rxl_kernel_timing.argtypes = [ctypes.c_int]
+            L.rxl_kernel_timing.restype = ctypes.c_int
+            L.rxl_kernel_timing_read.argtypes = [ctypes.c_int, P(ctypes.c_double), P(ctypes.c_int)]
+            L.rxl_kernel_timing_read.restype = ctypes.c_int
+            L.rxl_test_fail_next_launch.argtypes = [ctypes.c_int]
+            L.rxl_test_fail_next_launch.restype = None
+            L.rxl_test_forward_wait_timeout.argtypes = [ctypes.c_longlong, ctypes.c_int]
+            L.rxl_test_forward_wait_timeout.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc.argtypes = [P(rxl_attn_desc)] + [vp] * 15 + [vp]
             L.rxl_attn_bwd_noalloc.restype = ctypes.c_int
             L.rxl_attn_bwd_noalloc_max_scratch_bytes.argtypes = []
@@ -210,6 +221,35 @@ def rxl_attn_bwd_noalloc_max_scratch_bytes() -> int:
 def rxl_mem_update(ring: rxl_ring, src, src_plane_stride: int, L: int, stream=None):
     _check(lib().rxl_mem_update(ctypes.byref(ring), _ptr(src), int(src_plane_stride), int(L),
                                 _stream(stream)), "rxl_mem_update")
+
+
+def rxl_mem_update_rings(rings, srcs, src_plane_strides, L: int, stream=None):
+    """rxl_mem_update of several rings of one geometry in one launch; the
+    rxl_ring structs in `rings` are advanced in place."""
+    n = len(rings)
+    ring_ptrs = (ctypes.POINTER(rxl_ring) * n)(*[ctypes.pointer(r) for r in rings])
+    src_arr = (ctypes.c_void_p * n)(*[_ptr(x) for x in srcs])
+    str_arr = (ctypes.c_longlong * n)(*[int(x) for x in src_plane_strides])
+    _check(lib().rxl_mem_update_rings(ring_ptrs, src_arr, str_arr, n, int(L), _stream(stream)),
+           "rxl_mem_update_rings")
+
+
+RXL_KERNEL_FWD, RXL_KERNEL_BWD_MAIN = 0, 1
+
+
+def rxl_kernel_timing(enable: bool):
+    rc = lib().rxl_kernel_timing(1 if enable else 0)
+    if rc:
+        raise RuntimeError(f"rxl_kernel_timing: cuda error {rc}")
+
+
+def rxl_kernel_timing_read(kernel: int):
+    """(summed device ms, timed launches) of kernel since the last read."""
+    ms, n = ctypes.c_double(0.0), ctypes.c_int(0)
+    rc = lib().rxl_kernel_timing_read(int(kernel), ctypes.byref(ms), ctypes.byref(n))
+    if rc:
+        raise RuntimeError(f"rxl_kernel_timing_read: cuda error {rc}")
+    return ms.value, n.value
 
 
 def rxl_status_string(status: int) -> str:

@@ -1008,8 +1008,10 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   p.dk = (__nv_bfloat16 *)dk; p.dv = (__nv_bfloat16 *)dv;
   p.dv_acc = sums;
   const unsigned grid = (unsigned)(p.nitems < sms ? p.nitems : sms);
+  const int slot = timing_begin(1, st);
   cudaError_t e = launch_ex(rxl_bwd_main_kernel, dim3(grid), dim3(kThreads), F_SMEM, st, 1, tk, tv, tr16, tqu, tqv,
                             tdo, tdq, tdr, p);
+  timing_end(1, slot, st);
   ++*launches;
   if (e != cudaSuccess) return e;
   const int chunks = (s.L + 127) / 128;

@@ -88,6 +88,9 @@ constexpr uint32_t IDESC_G = idesc_bf16(128, 256, false, false);
 constexpr uint32_t IDESC_O = idesc_bf16(128, 64, false, true);   // V is MN-major (d contiguous)
 
 __device__ int g_fwd_error;
+// Testing hook (tc_fwd_test_hooks): non-zero makes the softmax warps withhold
+// their arrival on bar_qready for the CTA's first item.
+__device__ int g_fwd_withhold;
 
 struct Params {
   int B, H, L, cap, m, head, nq;
@@ -452,7 +455,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       if (ok) {
         q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
         fence_proxy_async_smem();
-        mbar_arrive(bar_qready);
+        if (!*(volatile int *)&g_fwd_withhold) mbar_arrive(bar_qready);
       } else {
         cur.valid = false;
       }
@@ -780,20 +783,24 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   if (MODE == kFwd && 2 * nitems <= sms) {
     // few items (short segments, few heads): two CTAs per item, each over
     // half of its key tiles, merged through distributed shared memory
+    const int slot = timing_begin(0, st);
     cudaError_t e =
         s.mvis ? launch_ex(rxl_fwd_tc_kernel<MODE, true, true>, dim3((unsigned)(2 * nitems)), dim3(kThreads),
                            SMEM_BYTES, st, 2, tk, tv, tr, tq, p, nitems)
                : launch_ex(rxl_fwd_tc_kernel<MODE, false, true>, dim3((unsigned)(2 * nitems)), dim3(kThreads),
                            SMEM_BYTES, st, 2, tk, tv, tr, tq, p, nitems);
+    timing_end(0, slot, st);
     ++*launches;
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   const unsigned grid = (unsigned)(nitems < sms ? nitems : sms);
+  const int slot = MODE == kFwd ? timing_begin(0, st) : -1;
   const cudaError_t e =
       s.mvis ? launch_ex(rxl_fwd_tc_kernel<MODE, true, false>, dim3(grid), dim3(kThreads), SMEM_BYTES, st, 1, tk, tv,
                          tr, tq, p, nitems)
              : launch_ex(rxl_fwd_tc_kernel<MODE, false, false>, dim3(grid), dim3(kThreads), SMEM_BYTES, st, 1, tk,
                          tv, tr, tq, p, nitems);
+  timing_end(0, slot, st);
   ++*launches;
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -813,6 +820,14 @@ cudaError_t launch_tc_bwd_prep(const AttnShape &s, const void *q, const void *k,
                                int *launches) {
   return launch_mode<kPrep>(s, q, k, v, r, u, vb, nullptr, nullptr, nullptr, dout, delta, qu_out, qv_out,
                             st, launches);
+}
+
+cudaError_t tc_fwd_test_hooks(long long wait_cycles, int withhold) {
+  const long long cycles = wait_cycles > 0 ? wait_cycles : sm103::kWaitCycles;
+  const int w = withhold ? 1 : 0;
+  cudaError_t e = cudaMemcpyToSymbol(sm103::g_wait_cycles, &cycles, sizeof(cycles));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fwd_withhold, &w, sizeof(w));
+  return e;
 }
 
 cudaError_t tc_fwd_read_error(int *flag) {

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/rxl.h"
 
 namespace rxl {
@@ -14,9 +16,14 @@ namespace rxl {
 // dependent launch allowed: its CTAs may start their setup while the previous
 // kernel on the stream finishes; the kernels wait for it (griddep_wait)
 // before their first global-memory access.
+// Testing hook: a non-zero value is returned, once, by the next launch_ex
+// instead of launching (rxl_test_fail_next_launch).
+extern std::atomic<int> g_fail_next_launch;
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                              unsigned cluster, Args... args) {
+  if (const int injected = g_fail_next_launch.exchange(0)) return (cudaError_t)injected;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -37,6 +44,14 @@ inline cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t 
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, k, args...);
 }
+
+// Opt-in device timing (rxl_kernel_timing): timing_begin records a start event
+// on st and returns a slot (-1 when timing is off or full); timing_end records
+// the matching stop event.
+constexpr int kTimedKernels = 2;  // 0: forward kernel, 1: backward main kernel
+bool timing_enabled();
+int timing_begin(int kernel, cudaStream_t st);
+void timing_end(int kernel, int slot, cudaStream_t st);
 
 // Validated shape of one attention call, as the kernels see it.
 struct AttnShape {
@@ -59,10 +74,19 @@ BwdWorkspace simt_bwd_workspace(const AttnShape &s);
 
 // Launchers return cudaSuccess or the launch error; `launches` is
 // incremented by the number of kernels put on the stream.
-cudaError_t launch_mem_update(void *data, int planes, int cap, int D, long long plane_stride,
-                              int elem_bytes, const void *src, long long src_plane_stride,
-                              int src_row0, int nrows, int dst_row0, cudaStream_t st,
-                              int *launches);
+// One FIFO update of up to kMaxRingsPerUpdate rings of the same geometry
+// (planes, cap, D, element size, head, len): rows src_row0 .. src_row0+nrows-1
+// of every source plane go to ring rows dst_row0 .. (mod cap).
+constexpr int kMaxRingsPerUpdate = 8;
+struct MemUpdateArgs {
+  void *data[kMaxRingsPerUpdate];
+  const void *src[kMaxRingsPerUpdate];
+  long long plane_stride[kMaxRingsPerUpdate];      // elements
+  long long src_plane_stride[kMaxRingsPerUpdate];  // elements
+  int nrings, planes, cap, D, elem_bytes;
+  int src_row0, nrows, dst_row0;
+};
+cudaError_t launch_mem_update(const MemUpdateArgs &a, cudaStream_t st, int *launches);
 
 cudaError_t launch_simt_fwd(const AttnShape &s, rxl_dtype dt, const void *q, const void *k,
                             const void *v, const void *r, const void *u, const void *vb,
@@ -81,6 +105,11 @@ cudaError_t launch_tc_fwd(const AttnShape &s, const void *q, const void *k, cons
                           float *lse, cudaStream_t st, int *launches);
 // Reads and clears the forward kernel's wait-timeout flag (synchronous).
 cudaError_t tc_fwd_read_error(int *flag);
+// Testing hook of the forward kernel: its bounded waits give up after
+// wait_cycles (<= 0: the default), and with withhold != 0 its softmax warps
+// withhold the arrival that tells the producer a new item's query tiles are
+// ready, so that the producer's wait on it runs out.
+cudaError_t tc_fwd_test_hooks(long long wait_cycles, int withhold);
 
 // Forward kernel in backward-preparation mode: D = dO.O (fp32 O) and the
 // (Q+u) rows in bf16 and (Q+v) rows in fp16.

@@ -7,6 +7,10 @@
 
 #include "internal.cuh"
 
+namespace rxl {
+std::atomic<int> g_fail_next_launch{0};
+}  // namespace rxl
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
@@ -70,6 +74,12 @@ const char *rxl_status_string(rxl_status s) {
 int rxl_last_cuda_error(void) { return g_last_cuda_error; }
 
 int rxl_last_launch_count(void) { return g_last_launches; }
+
+void rxl_test_fail_next_launch(int cuda_error) { rxl::g_fail_next_launch.store(cuda_error); }
+
+int rxl_test_forward_wait_timeout(long long wait_cycles, int withhold) {
+  return (int)rxl::tc_fwd_test_hooks(wait_cycles, withhold);
+}
 
 int rxl_device_error_flags(void) {
   int fwd = 0, bwd = 0, proj = 0, gemm = 0;
@@ -297,42 +307,76 @@ rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k,
                          dvbias, workspace, workspace_bytes, stream);
 }
 
-rxl_status rxl_mem_update(rxl_ring *ring, const void *src, long long src_plane_stride, int L,
-                          rxl_stream_t stream) {
-  if (!ring || L < 0) return RXL_ERR_INVALID_ARGUMENT;
-  if (ring->dtype != RXL_DTYPE_F32 && ring->dtype != RXL_DTYPE_BF16) return RXL_ERR_UNSUPPORTED;
-  if (ring->planes < 1 || ring->cap < 0 || ring->D < 1) return RXL_ERR_INVALID_ARGUMENT;
-  if (ring->len < 0 || ring->len > ring->cap) return RXL_ERR_INVALID_ARGUMENT;
-  if (ring->cap == 0 ? ring->head != 0 : (ring->head < 0 || ring->head >= ring->cap))
-    return RXL_ERR_INVALID_ARGUMENT;
-  const int es = ring->dtype == RXL_DTYPE_F32 ? 4 : 2;
-  if (ring->plane_stride < (long long)ring->cap * ring->D) return RXL_ERR_INVALID_ARGUMENT;
-  if (src_plane_stride < (long long)L * ring->D) return RXL_ERR_INVALID_ARGUMENT;
+rxl_status rxl_mem_update_rings(rxl_ring *const *rings, const void *const *srcs,
+                                const long long *src_plane_strides, int n, int L, rxl_stream_t stream) {
+  if (!rings || !srcs || !src_plane_strides || L < 0) return RXL_ERR_INVALID_ARGUMENT;
+  if (n < 1 || n > rxl::kMaxRingsPerUpdate) return RXL_ERR_INVALID_ARGUMENT;
+  for (int r = 0; r < n; ++r)
+    if (!rings[r]) return RXL_ERR_INVALID_ARGUMENT;
+  const rxl_ring &g = *rings[0];  // the shared geometry
+  if (g.dtype != RXL_DTYPE_F32 && g.dtype != RXL_DTYPE_BF16) return RXL_ERR_UNSUPPORTED;
+  if (g.planes < 1 || g.cap < 0 || g.D < 1) return RXL_ERR_INVALID_ARGUMENT;
+  if (g.len < 0 || g.len > g.cap) return RXL_ERR_INVALID_ARGUMENT;
+  if (g.cap == 0 ? g.head != 0 : (g.head < 0 || g.head >= g.cap)) return RXL_ERR_INVALID_ARGUMENT;
+  const int es = g.dtype == RXL_DTYPE_F32 ? 4 : 2;
+  for (int r = 0; r < n; ++r) {
+    const rxl_ring &x = *rings[r];
+    if (x.planes != g.planes || x.cap != g.cap || x.D != g.D || x.dtype != g.dtype || x.head != g.head ||
+        x.len != g.len)
+      return RXL_ERR_INVALID_ARGUMENT;
+    for (int t = 0; t < r; ++t)
+      if (rings[t] == rings[r]) return RXL_ERR_INVALID_ARGUMENT;  // each ring advances once
+    if (x.plane_stride < (long long)x.cap * x.D) return RXL_ERR_INVALID_ARGUMENT;
+    if (src_plane_strides[r] < (long long)L * x.D) return RXL_ERR_INVALID_ARGUMENT;
+  }
   g_last_launches = 0;
-  if (ring->cap == 0 || L == 0) return RXL_OK;  // nothing kept / nothing appended
-  if (!ring->data || !src) return RXL_ERR_INVALID_ARGUMENT;
-  if (!aligned16(ring->data) || !aligned16(src) || ((long long)ring->D * es) % 16 != 0 ||
-      (ring->plane_stride * es) % 16 != 0 || (src_plane_stride * es) % 16 != 0)
-    return RXL_ERR_MISALIGNED;
-  const int cap = ring->cap;
+  if (g.cap == 0 || L == 0) return RXL_OK;  // nothing kept / nothing appended
+  for (int r = 0; r < n; ++r) {
+    const rxl_ring &x = *rings[r];
+    if (!x.data || !srcs[r]) return RXL_ERR_INVALID_ARGUMENT;
+    if (!aligned16(x.data) || !aligned16(srcs[r]) || ((long long)x.D * es) % 16 != 0 ||
+        (x.plane_stride * es) % 16 != 0 || (src_plane_strides[r] * es) % 16 != 0)
+      return RXL_ERR_MISALIGNED;
+  }
+  const int cap = g.cap;
   const int nwrite = L < cap ? L : cap;          // only the last min(L, cap) rows survive
-  const int src_row0 = L - nwrite;
-  const int dst_row0 = (int)(((long long)ring->head + ring->len + src_row0) % cap);
+  rxl::MemUpdateArgs a;
+  for (int r = 0; r < n; ++r) {
+    a.data[r] = rings[r]->data;
+    a.src[r] = srcs[r];
+    a.plane_stride[r] = rings[r]->plane_stride;
+    a.src_plane_stride[r] = src_plane_strides[r];
+  }
+  a.nrings = n;
+  a.planes = g.planes;
+  a.cap = cap;
+  a.D = g.D;
+  a.elem_bytes = es;
+  a.src_row0 = L - nwrite;
+  a.nrows = nwrite;
+  a.dst_row0 = (int)(((long long)g.head + g.len + a.src_row0) % cap);
   int launches = 0;
-  const cudaError_t e = rxl::launch_mem_update(ring->data, ring->planes, cap, ring->D,
-                                               ring->plane_stride, es, src, src_plane_stride,
-                                               src_row0, nwrite, dst_row0,
-                                               (cudaStream_t)stream, &launches);
+  const cudaError_t e = rxl::launch_mem_update(a, (cudaStream_t)stream, &launches);
   g_last_launches = launches;
   if (e != cudaSuccess) return cuda_status(e);
-  const long long total = (long long)ring->len + L;
+  const long long total = (long long)g.len + L;
+  int head = g.head, len;
   if (total > cap) {
-    ring->head = (int)(((long long)ring->head + total - cap) % cap);
-    ring->len = cap;
+    head = (int)(((long long)g.head + total - cap) % cap);
+    len = cap;
   } else {
-    ring->len = (int)total;
+    len = (int)total;
+  }
+  for (int r = 0; r < n; ++r) {
+    rings[r]->head = head;
+    rings[r]->len = len;
   }
   return RXL_OK;
+}
+
+rxl_status rxl_mem_update(rxl_ring *ring, const void *src, long long src_plane_stride, int L,
+                          rxl_stream_t stream) {
+  return rxl_mem_update_rings(&ring, &src, &src_plane_stride, 1, L, stream);
 }
 
 }  // extern "C"

@@ -13,39 +13,87 @@
 //  * shapes whose backward needs more scratch than that are rejected;
 //  * all calls share the one array per device, so calls that overlap on the
 //    GPU (different streams, or different host threads) race on it.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.cuh"
 
 namespace {
 
-// 16 MiB: enough for B*H*L up to about 32,000 query rows (the backward needs
-// about 520 bytes of scratch per query row, plus 128 bytes per head and K/V
-// row for an fp16 copy of R).
+// 16 MiB. The backward's scratch is, with rows = B*H*L query rows and
+// kv = M+L key rows per head (bf16; the f32 path needs only the first term):
+//   516*rows + 384*H*kv + 32,768*H bytes (+ at most 2 KB of alignment),
+// i.e. per query row D (4 B), (Q+u) and (Q+v) (2 x 128 B) and the fp32 dQ
+// accumulator (256 B); per head and key row the fp16 copy of R (128 B) and
+// the fp32 dR accumulator (256 B, with 128 extra rows per head). Long memory
+// reaches the limit well before many query rows do: B4 H16 L128 with 1600
+// memory rows already needs about 15.4 MiB.
 constexpr size_t kScratchBytes = 16u << 20;
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 128;
 std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+struct Cached {
+  unsigned long long ctx_id;  // the context the address belongs to (0: none yet)
+  void *addr;
+};
+Cached g_scratch[kMaxDevices] = {};
 
-// Device address of g_bwd_scratch on the current device. The name is only a
-// host-side stand-in for the array, so the address is looked up once per
-// device, with that device current, and cached.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+template <typename Fn>
+Fn driver_fn(const char *name) {
+  void *f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return (Fn)f;
+  return nullptr;
+}
+
+// Unique id of the calling thread's current context, 0 if unknown.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_bwd_scratch on the current device. The array's name is
+// only a host-side stand-in, so the address is looked up with the device
+// current, at the first call on that device, and cached. The cache is keyed
+// by the context's unique id as well: after a device reset the module is
+// loaded again in a new context, the array may move, and the next call looks
+// the address up again instead of using a stale one. (When the id cannot be
+// read, e.g. before the runtime has made a context current, the address is
+// looked up on every call.)
 cudaError_t scratch_on_current_device(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  Cached &c = g_scratch[dev];
+  if (!c.addr || id == 0 || c.ctx_id != id) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_bwd_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    c.addr = p;
+    c.ctx_id = current_context_id();  // the lookup made the device's context current
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return cudaSuccess;
 }
 

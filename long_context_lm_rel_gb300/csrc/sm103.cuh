@@ -7,7 +7,7 @@
 //    (128 B) per tile row, 16-byte chunk c of row r stored at chunk c^(r&7),
 //    8-row atoms of 1024 B, tile base 1024-byte aligned. TMA with
 //    CU_TENSOR_MAP_SWIZZLE_128B writes exactly this layout.
-//  * every wait on an mbarrier gives up after kWaitCycles; the kernel then
+//  * every wait on an mbarrier gives up after g_wait_cycles; the kernel then
 //    records the failure in the library's device error word and winds down.
 #pragma once
 
@@ -20,6 +20,9 @@ namespace sm103 {
 
 // ~2 s at 2 GHz: far beyond any legitimate wait in these kernels.
 constexpr long long kWaitCycles = 4000000000LL;
+// The limit the waits use: kWaitCycles unless a test shortened it for the
+// kernels of this translation unit (one variable per translation unit).
+static __device__ long long g_wait_cycles = kWaitCycles;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -70,7 +73,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of the given parity; false after kWaitCycles (or when
+// Waits for the phase of the given parity; false after g_wait_cycles (or when
 // another thread of the CTA already gave up: *abort != 0).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -79,7 +82,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (clock64() - t0 > kWaitCycles) {
+      if (clock64() - t0 > g_wait_cycles) {
         *abort = 1;
         return false;
       }
@@ -116,7 +119,7 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                : "memory");
 }
 // Bounded wait on a local mbarrier that other CTAs of the cluster arrive on
-// (acquire at cluster scope): false after kWaitCycles or an abort.
+// (acquire at cluster scope): false after g_wait_cycles or an abort.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort) {
   const long long t0 = clock64();
   for (uint32_t it = 0;; ++it) {
@@ -131,7 +134,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     if (ok) return true;
     if ((it & 63u) == 63u) {
       if (*abort) return false;
-      if (clock64() - t0 > kWaitCycles) {
+      if (clock64() - t0 > g_wait_cycles) {
         *abort = 1;
         return false;
       }

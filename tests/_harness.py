@@ -43,21 +43,7 @@ def to_host(t) -> np.ndarray:
         else t.detach().cpu().numpy().astype(np.float64)
 
 
-def ring_rows(cap: int, head: int, m: int) -> np.ndarray:
-    """Physical ring row of each logical memory row t = 0..m-1."""
-    return (head + np.arange(m)) % cap if m else np.zeros(0, dtype=np.int64)
-
-
-def place_kv(mem: np.ndarray, cur: np.ndarray, cap: int, head: int, fill=0.0) -> np.ndarray:
-    """Physical [B,H,cap+L,dh] K or V: logical memory rows into the ring at
-    head, current rows after the ring. Unused ring rows get `fill`."""
-    B, H, m, dh = mem.shape
-    L = cur.shape[2]
-    out = np.full((B, H, cap + L, dh), fill, dtype=np.float32)
-    if m:
-        out[:, :, ring_rows(cap, head, m)] = mem
-    out[:, :, cap:] = cur
-    return out
+from long_context_lm_rel_gb300.calls import place_kv, ring_rows  # noqa: E402,F401
 
 
 def logical_kv(phys: np.ndarray, cap: int, head: int, m: int) -> np.ndarray:
@@ -87,78 +73,8 @@ def assert_close(name: str, got: np.ndarray, ref: np.ndarray, dtype: str, extra=
     return float(err.max())
 
 
-class AttnCall:
-    """Device buffers and one fwd (+bwd) call through the C ABI."""
-
-    def __init__(self, q, k_phys, v_phys, r, u, vb, *, cap, m, head, dtype, scale):
-        import torch
-        import long_context_lm_rel_gb300 as rxl
-        self.torch = torch
-        self.rxl = rxl
-        B, H, L, dh = q.shape
-        self.shape = (B, H, L, dh)
-        self.dtype = dtype
-        self.cap, self.m, self.head = cap, m, head
-        self.desc = rxl.make_desc(B, H, L, cap, m, head, scale, rxl_dtype(dtype))
-        self.q, self.k, self.v = to_dev(q, dtype), to_dev(k_phys, dtype), to_dev(v_phys, dtype)
-        rr = np.zeros((H, cap + L, dh), dtype=np.float32)
-        rr[:, :min(r.shape[1], cap + L)] = r[:, :cap + L]
-        self.r, self.u, self.vb = to_dev(rr, dtype), to_dev(u, dtype), to_dev(vb, dtype)
-        td = torch_dtype(dtype)
-        self.o = torch.empty((B, H, L, dh), device="cuda", dtype=td)
-        self.lse = torch.empty((B, H, L), device="cuda", dtype=torch.float32)
-
-    def fwd(self, stream=None):
-        self.rxl.rxl_attn_fwd(self.desc, self.q, self.k, self.v, self.r, self.u, self.vb, self.o,
-                              self.lse, stream)
-        return self
-
-    def fwd_ex(self, stream=None):
-        """Forward of the training pair: also keeps the low part of O."""
-        if not hasattr(self, "o_lo"):
-            self.o_lo = self.torch.empty_like(self.o)
-        self.rxl.rxl_attn_fwd_ex(self.desc, self.q, self.k, self.v, self.r, self.u, self.vb, self.o,
-                                 self.o_lo, self.lse, stream)
-        return self
-
-    def bwd_ex(self, stream=None):
-        self.rxl.rxl_attn_bwd_ex(self.desc, self.q, self.k, self.v, self.r, self.u, self.vb, self.o,
-                                 self.o_lo, self.lse, self.do, self.dq, self.dk, self.dv, self.dr,
-                                 self.du, self.dvb, self.ws, self.ws_bytes, stream)
-        return self
-
-    def alloc_bwd(self, dout):
-        torch = self.torch
-        B, H, L, dh = self.shape
-        td = torch_dtype(self.dtype)
-        self.do = to_dev(dout, self.dtype)
-        self.dq = torch.empty((B, H, L, dh), device="cuda", dtype=td)
-        self.dk = torch.empty_like(self.k)
-        self.dv = torch.empty_like(self.v)
-        self.dr = torch.empty((H, self.cap + L, dh), device="cuda", dtype=torch.float32)
-        self.du = torch.empty((H, dh), device="cuda", dtype=torch.float32)
-        self.dvb = torch.empty((H, dh), device="cuda", dtype=torch.float32)
-        self.ws_bytes = self.rxl.rxl_attn_bwd_workspace_bytes(self.desc)
-        self.ws = torch.empty(max(self.ws_bytes, 16), device="cuda", dtype=torch.uint8)
-        return self
-
-    def bwd(self, stream=None):
-        self.rxl.rxl_attn_bwd(self.desc, self.q, self.k, self.v, self.r, self.u, self.vb, self.o,
-                              self.lse, self.do, self.dq, self.dk, self.dv, self.dr, self.du,
-                              self.dvb, self.ws, self.ws_bytes, stream)
-        return self
-
-    # per-row document reset: mem_visible [B] int32 on the device
-    def fwd_reset(self, mem_visible, keep_low=True, stream=None):
-        self.mvis = self.torch.tensor(np.asarray(mem_visible, dtype=np.int32), device="cuda")
-        self.o_lo = self.torch.empty_like(self.o) if keep_low else None
-        self.rxl.rxl_attn_fwd_reset(self.desc, self.mvis, self.q, self.k, self.v, self.r, self.u,
-                                    self.vb, self.o, self.o_lo, self.lse, stream)
-        return self
-
-    def bwd_reset(self, stream=None):
-        self.rxl.rxl_attn_bwd_reset(self.desc, self.mvis, self.q, self.k, self.v, self.r, self.u,
-                                    self.vb, self.o, self.o_lo, self.lse, self.do, self.dq, self.dk,
-                                    self.dv, self.dr, self.du, self.dvb, self.ws, self.ws_bytes,
-                                    stream)
-        return self
+def AttnCall(*args, **kw):
+    """The package's AttnCall with the test side's bit-exact device copies."""
+    from long_context_lm_rel_gb300.calls import AttnCall as _AttnCall
+    kw.setdefault("to_dev", to_dev)
+    return _AttnCall(*args, **kw)

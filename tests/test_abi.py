@@ -98,3 +98,24 @@ def test_mem_update_validation_and_noops(lib):
     assert lib.rxl_mem_update(ctypes.byref(r), A + 2, 64 * 4, 4, None) == rxl.RXL_ERR_MISALIGNED
     assert lib.rxl_mem_update(ctypes.byref(r), A, 64 * 4, -1, None) == rxl.RXL_ERR_INVALID_ARGUMENT
     assert (r.head, r.len) == (3, 5)
+
+
+def test_mem_update_rings_rejects_mismatched_rings(lib):
+    mk = lambda head=0, length=0, D=64, cap=8: rxl.rxl_ring(A, 2, cap, D, cap * D, rxl.RXL_DTYPE_BF16, head, length)
+    P = ctypes.POINTER(rxl.rxl_ring)
+
+    def call(rings, n=None):
+        n = len(rings) if n is None else n
+        arr = (P * max(n, 1))(*[ctypes.pointer(r) for r in rings])
+        srcs = (ctypes.c_void_p * max(n, 1))(*([A] * max(n, 1)))
+        strides = (ctypes.c_longlong * max(n, 1))(*([4 * 64] * max(n, 1)))
+        return lib.rxl_mem_update_rings(arr, srcs, strides, n, 4, None)
+
+    a = mk()
+    assert call([a, mk(head=1)]) == rxl.RXL_ERR_INVALID_ARGUMENT      # other head
+    assert call([a, mk(length=3)]) == rxl.RXL_ERR_INVALID_ARGUMENT    # other len
+    assert call([a, mk(D=128)]) == rxl.RXL_ERR_INVALID_ARGUMENT       # other width
+    assert call([a, a]) == rxl.RXL_ERR_INVALID_ARGUMENT               # the same ring twice
+    assert call([], n=0) == rxl.RXL_ERR_INVALID_ARGUMENT
+    assert call([mk() for _ in range(9)]) == rxl.RXL_ERR_INVALID_ARGUMENT
+    assert (a.head, a.len) == (0, 0)                                  # nothing advanced

@@ -3,10 +3,10 @@ float64 oracle on the same seeded inputs.
 
 * every element at sizes the oracle finishes in seconds (several tiles,
   ragged tails, rotated and wrapping rings, empty memory);
-* the five configurations of the path at full size: cfg1 and cfg2 in full,
-  cfg3/cfg4 on sampled forward rows plus the whole backward of one head
-  (all batch rows), cfg5 as the 32-segment stream on its first and last layer
-  with sampled rows at fill, wrap and steady-state segments;
+* the five configurations of the path at full size, every element: cfg1,
+  cfg2 (4-segment stream), cfg3/cfg4 (forward and backward, all (b, h)),
+  cfg5 as the 32-segment stream of all 16 layers, every row at the fill,
+  wrap and steady-state segments;
 * skew-sensitive closed-form probes (distance labels) on tile boundaries;
 * calls with at most half as many (b, h, query tile) items as SMs, which the
   forward runs as 2-CTA clusters (the small cases too, one of them with a
@@ -202,23 +202,28 @@ def test_cfg2_stream_fwd_bwd():
         k_dev, v_dev = c.k.clone(), c.v.clone()
 
 
-# ---------------------------------- configurations 3 and 4 (full size, sampled)
+# ------------------------------------ configurations 3 and 4 (full size)
 
-def sample_rows(B, H, L, n, rng):
-    fixed = [0, 1, 63, 64, 127, 128, L - 1]
-    sel = set()
-    for b, h in [(0, 0), (B - 1, H - 1), (B // 2, H // 3)]:
-        for i in fixed:
-            if i < L:
-                sel.add((b, h, i))
-    while len(sel) < n:
-        sel.add((int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(L))))
-    return np.array(sorted(sel), dtype=np.int32)
+_FULL_SIZE_REF = {}
+
+
+def _full_size_reference(cfg, x, scale):
+    """The oracle's forward and backward of the whole configuration (every
+    (b, h)), computed once per configuration and shared by both call modes."""
+    if cfg not in _FULL_SIZE_REF:
+        k, v = logical(x)
+        o, lse = oracle.fwd(x["q"], k, v, x["r"], x["u"], x["vb"], scale)
+        g = oracle.bwd(x["q"], k, v, x["r"], x["u"], x["vb"], x["do"], scale)
+        _FULL_SIZE_REF.clear()
+        _FULL_SIZE_REF[cfg] = (o, lse, g)
+    return _FULL_SIZE_REF[cfg]
 
 
 @pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
 @pytest.mark.parametrize("cfg", [3, 4])
 def test_full_size_config(cfg, ex):
+    """Every element of every output (O, LSE, dQ, dK, dV, dR, du, dv) over all
+    (b, h) at the full size of the configuration."""
     import torch
     w = gen.CONFIGS[cfg]
     p = gen.layer_params(w)
@@ -230,24 +235,16 @@ def test_full_size_config(cfg, ex):
     c = run_gpu(x, cap, m, 0, "bf16", scale=w.scale, ex=ex)
     torch.cuda.synchronize()
     assert_no_device_error()
-    k, v = logical(x)
-    rng = np.random.default_rng(cfg)
-    sel = sample_rows(w.B, w.H, w.L, 96, rng)
-    o_ref, lse_ref = oracle.fwd_rows(x["q"], k, v, x["r"], x["u"], x["vb"], w.scale, sel)
-    o, lse = to_host(c.o), to_host(c.lse)
-    assert_close("O(sampled)", o[sel[:, 0], sel[:, 1], sel[:, 2]], o_ref, "bf16")
-    assert_close("LSE(sampled)", lse[sel[:, 0], sel[:, 1], sel[:, 2]], lse_ref, "bf16")
-    # the whole backward of one head, all batch rows (dR/du/dv sum over b)
-    h = w.H // 2
-    hs = slice(h, h + 1)
-    g = oracle.bwd(x["q"][:, hs], k[:, hs], v[:, hs], x["r"][hs], x["u"][hs], x["vb"][hs],
-                   x["do"][:, hs], w.scale)
-    assert_close("dQ", to_host(c.dq)[:, hs], g["dq"], "bf16")
-    assert_close("dK", logical_kv(to_host(c.dk)[:, hs], cap, 0, m), g["dk"], "bf16")
-    assert_close("dV", logical_kv(to_host(c.dv)[:, hs], cap, 0, m), g["dv"], "bf16")
-    assert_close("dR", to_host(c.dr)[hs], g["dr"], "bf16")
-    assert_close("du", to_host(c.du)[hs], g["du"], "bf16")
-    assert_close("dv", to_host(c.dvb)[hs], g["dvb"], "bf16")
+    o_ref, lse_ref, g = _full_size_reference(cfg, x, w.scale)
+    tag = f"cfg{cfg} {'training pair' if ex else 'plain'}"
+    assert_close("O", to_host(c.o), o_ref, "bf16", tag)
+    assert_close("LSE", to_host(c.lse), lse_ref, "bf16", tag)
+    assert_close("dQ", to_host(c.dq), g["dq"], "bf16", tag)
+    assert_close("dK", logical_kv(to_host(c.dk), cap, 0, m), g["dk"], "bf16", tag)
+    assert_close("dV", logical_kv(to_host(c.dv), cap, 0, m), g["dv"], "bf16", tag)
+    assert_close("dR", to_host(c.dr), g["dr"], "bf16", tag)
+    assert_close("du", to_host(c.du), g["du"], "bf16", tag)
+    assert_close("dv", to_host(c.dvb), g["dvb"], "bf16", tag)
 
 
 # -------------------- recompute-the-window evaluation baseline (forward)
@@ -255,7 +252,7 @@ def test_full_size_config(cfg, ex):
 def test_window_recompute_case():
     """The evaluation baseline without a memory: every step recomputes causal
     attention over the whole window of cfg5 (M + L = 1728 positions, m = 0),
-    B4 H16; sampled rows against the oracle."""
+    B4 H16; every row against the oracle."""
     import torch
     B, H, W = 4, 16, 1728
     x = make_inputs(B, H, W, 0, 0, "bf16", seed=1728)
@@ -263,24 +260,24 @@ def test_window_recompute_case():
     torch.cuda.synchronize()
     assert_no_device_error()
     k, v = logical(x)
-    rng = np.random.default_rng(1728)
-    sel = sample_rows(B, H, W, 64, rng)
-    o_ref, lse_ref = oracle.fwd_rows(x["q"], k, v, x["r"], x["u"], x["vb"], 0.125, sel)
-    o, lse = to_host(c.o), to_host(c.lse)
-    assert_close("O(sampled)", o[sel[:, 0], sel[:, 1], sel[:, 2]], o_ref, "bf16")
-    assert_close("LSE(sampled)", lse[sel[:, 0], sel[:, 1], sel[:, 2]], lse_ref, "bf16")
+    o_ref, lse_ref = oracle.fwd(x["q"], k, v, x["r"], x["u"], x["vb"], 0.125)
+    assert_close("O", to_host(c.o), o_ref, "bf16")
+    assert_close("LSE", to_host(c.lse), lse_ref, "bf16")
 
 
 # ------------------------- configuration 5 (16-layer evaluation stream, fwd)
 
-def test_cfg5_stream_first_and_last_layer():
+def test_cfg5_stream_all_layers():
+    """The 32-segment stream of every one of the 16 layers: every row of O and
+    LSE against the oracle at the segments where the memory is empty,
+    partial, last partial, wraps, is full for the first time, and steady."""
     import torch
     import long_context_lm_rel_gb300 as rxl
+    from tests._harness import to_dev
     w = gen.CFG5
     cap, L, dh = w.M, w.L, w.dh
     check_at = {0, 1, 11, 12, 13, 31}   # empty, partial, last partial, wrap, full, steady
-    rng = np.random.default_rng(55)
-    for layer in (0, w.layers - 1):
+    for layer in range(w.layers):
         p = gen.layer_params(w, layer)
         k = torch.zeros((w.B, w.H, cap + L, dh), device="cuda", dtype=torch.bfloat16)
         v = torch.zeros_like(k)
@@ -291,7 +288,6 @@ def test_cfg5_stream_first_and_last_layer():
         rv = rxl.rxl_ring(v.data_ptr(), w.B * w.H, cap, dh, (cap + L) * dh, rxl.RXL_DTYPE_BF16, 0, 0)
         mem_k = np.zeros((w.B, w.H, 0, dh), np.float32)
         mem_v = mem_k.copy()
-        from tests._harness import to_dev
         for seg in range(w.segments):
             s = gen.segment_inputs(w, seg, layer)
             k[:, :, cap:] = to_dev(s["k_cur"], "bf16")
@@ -303,17 +299,16 @@ def test_cfg5_stream_first_and_last_layer():
                 torch.cuda.synchronize()
                 kl = np.concatenate([mem_k, s["k_cur"]], 2)
                 vl = np.concatenate([mem_v, s["v_cur"]], 2)
-                sel = sample_rows(w.B, w.H, L, 48, rng)
-                o_ref, lse_ref = oracle.fwd_rows(s["q"], kl, vl, p["r"], p["u"], p["vb"], w.scale, sel)
-                o, lse = to_host(r_dev.o), to_host(r_dev.lse)
+                o_ref, lse_ref = oracle.fwd(s["q"], kl, vl, p["r"], p["u"], p["vb"], w.scale)
                 tag = f"layer {layer} segment {seg} m={rk.len} head={rk.head}"
-                assert_close("O", o[sel[:, 0], sel[:, 1], sel[:, 2]], o_ref, "bf16", tag)
-                assert_close("LSE", lse[sel[:, 0], sel[:, 1], sel[:, 2]], lse_ref, "bf16", tag)
+                assert_close("O", to_host(r_dev.o), o_ref, "bf16", tag)
+                assert_close("LSE", to_host(r_dev.lse), lse_ref, "bf16", tag)
             rxl.rxl_mem_update(rk, k.data_ptr() + cap * dh * 2, (cap + L) * dh, L)
             rxl.rxl_mem_update(rv, v.data_ptr() + cap * dh * 2, (cap + L) * dh, L)
             mem_k = oracle.tail_m(mem_k, s["k_cur"], cap)
             mem_v = oracle.tail_m(mem_v, s["v_cur"], cap)
         assert (rk.len, rk.head) == (cap, (32 * L - cap) % cap)
+    assert_no_device_error()
 
 
 # ------------------------------------------- skew-sensitive closed-form probes

@@ -86,3 +86,51 @@ def test_ring_checkpoint_restore_continues_identically():
     torch.cuda.synchronize()
     assert (ring_a.head, ring_a.len) == (ring_b.head, ring_b.len)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("cap,L,steps,head0", [(1600, 128, 15, 1536), (5, 2, 7, 3), (3, 7, 3, 2), (512, 512, 3, 100)])
+def test_rings_updated_together_bit_exact(cap, L, steps, head0):
+    """rxl_mem_update_rings advances K and V rings of one geometry (different
+    buffers and source strides) in one launch, each bit-exact to Tail_M."""
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    rng = np.random.default_rng(cap + 17 * L)
+    planes, D = 5, 64
+    k = _dev(_bits(rng, (planes, cap + L, D), "bf16"))
+    v_ring = _dev(_bits(rng, (planes, cap, D), "bf16"))      # a ring without current rows
+    v_src = _dev(_bits(rng, (planes, L + 3, D), "bf16"))     # a source with another plane stride
+    rk = rxl.rxl_ring(k.data_ptr(), planes, cap, D, (cap + L) * D, rxl.RXL_DTYPE_BF16, head0, 0)
+    rv = rxl.rxl_ring(v_ring.data_ptr(), planes, cap, D, cap * D, rxl.RXL_DTYPE_BF16, head0, 0)
+    mk = np.zeros((planes, 0, D), np.uint16)
+    mv = mk.copy()
+    for step in range(steps):
+        nk, nv = _bits(rng, (planes, L, D), "bf16"), _bits(rng, (planes, L, D), "bf16")
+        k[:, cap:] = _dev(nk)
+        v_src[:, :L] = _dev(nv)
+        rxl.rxl_mem_update_rings([rk, rv], [k.data_ptr() + cap * D * 2, v_src], [(cap + L) * D, (L + 3) * D], L)
+        assert rxl.rxl_last_launch_count() == 1
+        torch.cuda.synchronize()
+        mk, mv = oracle.tail_m(mk, nk, cap), oracle.tail_m(mv, nv, cap)
+        assert (rk.head, rk.len) == (rv.head, rv.len) and rk.len == mk.shape[1]
+        assert np.array_equal(_host(k, "bf16")[:, ring_rows(cap, rk.head, rk.len)], mk), f"K step {step}"
+        assert np.array_equal(_host(v_ring, "bf16")[:, ring_rows(cap, rv.head, rv.len)], mv), f"V step {step}"
+
+
+def test_wide_plane_wrapping_copy():
+    """One wide plane (D = 8192 bf16 elements, 16 KB rows; 4096 rows appended
+    to a full ring of 8192 at head 6000): the copy of 4 M vectors crosses the
+    ring's wrap inside one plane and lands row for row."""
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    planes, cap, L, D = 1, 8192, 4096, 8192
+    head0 = 6000
+    k = torch.zeros((planes, cap + L, D), device="cuda", dtype=torch.int16)
+    src = torch.arange(L, device="cuda", dtype=torch.int16).view(1, L, 1).expand(planes, L, D).contiguous()
+    k[:, cap:] = src
+    ring = rxl.rxl_ring(k.data_ptr(), planes, cap, D, (cap + L) * D, rxl.RXL_DTYPE_BF16, head0, cap)
+    rxl.rxl_mem_update(ring, k.data_ptr() + cap * D * 2, (cap + L) * D, L)
+    torch.cuda.synchronize()
+    assert (ring.head, ring.len) == ((head0 + L) % cap, cap)
+    dst = (head0 + np.arange(L)) % cap                # where the appended rows went
+    got = k[0, torch.from_numpy(dst).cuda(), :].cpu().numpy()
+    assert np.array_equal(got, np.broadcast_to(np.arange(L, dtype=np.int16)[:, None], (L, D)))
