@@ -60,18 +60,18 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
 
 
 def test_noalloc_shape_whose_scratch_ends_at_the_limit():
-    """B4 H16 L128 with a full 1600-row memory: the workspace ends within a
-    MiB of the fixed array's end, so the fp32 dR accumulator and its TMA
+    """B4 H16 L128 with a full 1780-row memory: the workspace ends within
+    300 KB of the fixed array's end, so the fp32 dR accumulator and its TMA
     descriptor sit at the end of the array. Every output matches the
     workspace backward."""
     import torch
-    B, H, L, cap, m, head = 4, 16, 128, 1600, 1600, 1500
+    B, H, L, cap, m, head = 4, 16, 128, 1780, 1780, 1700
     limit = __import__("long_context_lm_rel_gb300").rxl_attn_bwd_noalloc_max_scratch_bytes()
     x = make_inputs(B, H, L, cap, m, "bf16", seed=99)
     c = AttnCall(x["q"], place_kv(x["k_mem"], x["k_cur"], cap, head), place_kv(x["v_mem"], x["v_cur"], cap, head),
                  x["r"], x["u"], x["vb"], cap=cap, m=m, head=head, dtype="bf16", scale=0.125)
     c.fwd().alloc_bwd(x["do"])
-    assert limit - (1 << 20) < c.ws_bytes <= limit, (c.ws_bytes, limit)
+    assert limit - (300 << 10) < c.ws_bytes <= limit, (c.ws_bytes, limit)
     c.bwd()
     torch.cuda.synchronize()
     ref = {n: to_host(getattr(c, n)) for n in OUTS}
