@@ -78,14 +78,16 @@ struct BwdParams {
 // start at distance >= -127; their rows below 0 only ever receive zeros).
 constexpr int kDrPad = 128;
 
-// K-major operand: 128-byte swizzled [rows][64] tile, k-step kk of 16 elements.
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk) {
-  return sdesc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+// K-major operand: 128-byte swizzled [rows][64] tile, k-step kk of 16 elements
+// (kk >= 4: the next [rows][64] tile, 16 KB on). kd0 = kdesc0(tile base).
+__device__ __forceinline__ uint64_t kdesc0(uint32_t base) { return sdesc_sw128(base, 16, 1024); }
+__device__ __forceinline__ uint64_t kdesc(uint64_t kd0, int kk) {
+  return sdesc_add(kd0, (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32));
 }
-// MN-major operand: [K rows][MN] tiles of 64 MN columns (16 KB apart), k-step of 16 rows.
-__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {
-  return sdesc_sw128(base + kk * 2048, 16384, 1024);
-}
+// MN-major operand: [K rows][MN] tiles of 64 MN columns (16 KB apart), k-step
+// of 16 rows. md0 = mndesc0(tile base).
+__device__ __forceinline__ uint64_t mndesc0(uint32_t base) { return sdesc_sw128(base, 16384, 1024); }
+__device__ __forceinline__ uint64_t mndesc(uint64_t md0, int kk) { return sdesc_add(md0, (uint32_t)(kk * 2048)); }
 
 // 64 fp32 values (keys 64*hf ..) of row ii as bf16 into column block hf of a
 // [128][128] K-major 128-byte-swizzled tile pair; row = sw128_row(block hf, ii).
@@ -109,9 +111,12 @@ __device__ __forceinline__ bool pair_sync(uint32_t bar, int lane, uint32_t &phas
 
 // ------------------------------------------------------------ main kernel
 
-constexpr uint32_t F_K = 0, F_V = 16384, F_QU = 32768, F_QV = 49152, F_DO = 65536;
-constexpr uint32_t F_R = 81920, F_PA = 114688, F_DG = 147456, F_X = 212992, F_BAR = 215040;
-constexpr uint32_t F_SMEM = F_BAR + 256 + 1024;
+// Shared memory: K, V, (Q+u), two (Q+v) buffers (the next pair's rows load
+// while the current pair still reads its own), dO, the 256-row R band, P/dA
+// (bf16, then the pair's dQ staging), dG (fp16, then its dR staging), barriers.
+constexpr uint32_t F_K = 0, F_V = 16384, F_QU = 32768, F_QV0 = 49152, F_QV1 = 65536, F_DO = 81920;
+constexpr uint32_t F_R = 98304, F_PA = 131072, F_DG = 163840, F_BAR = 229376;
+constexpr uint32_t F_SMEM = F_BAR + 512 + 1024;
 // TMEM columns: dV, dK accumulators; S (then dP); G (then dQc, dQp, dR blocks)
 constexpr uint32_t TM_DV = 0, TM_DK = 64, TM_S = 128, TM_G = 256;
 constexpr uint32_t TM_QC = 256, TM_QP = 320, TM_R0 = 384;
@@ -194,32 +199,38 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const uint32_t b0 = sb + F_BAR;
-  const uint32_t bar_kv = b0, bar_ld = b0 + 8, bar_sg = b0 + 16, bar_p = b0 + 24;
-  const uint32_t bar_dp = b0 + 32, bar_ds = b0 + 40, bar_fin = b0 + 48, bar_fl = b0 + 56;
-  const uint32_t bar_acc = b0 + 64, bar_red = b0 + 72, bar_drain = b0 + 80, bar_x0 = b0 + 88;
-  const uint32_t bar_staged = b0 + 120;  // each softmax warp staged its rows of a pair (8)
-  const uint32_t bar_sfree = b0 + 128;   // the dQ staging of a pair has been read (1)
-  const uint32_t bar_gfree = b0 + 240;   // the dR staging of a pair has been read (1)
-  const uint32_t bar_da = b0 + 136;      // softmax warps (256): dA written
-  const uint32_t bar_f0 = b0 + 144;      // dK and dQc done (commit)
-  const uint32_t bar_do = b0 + 152, bar_qu = b0 + 160;  // TMA: dO, (Q+u) of a pair
-  uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 168);
-  volatile int *abort_flag = (volatile int *)(smem + F_BAR + 172);
-  volatile float *wmax = (volatile float *)(smem + F_BAR + 176);  // [2][8]
+  // TMA: K/V of an item; (Q+v) of a pair into buffer 0 / 1; the R band;
+  // dO and (Q+u) of a pair
+  const uint32_t bar_kv = b0, bar_qv0 = b0 + 8, bar_qv1 = b0 + 16, bar_r = b0 + 24;
+  const uint32_t bar_do = b0 + 32, bar_qu = b0 + 40;
+  // MMA commits: S and G; dP; dV; dK and dQc; dQp; dR (the pair's last)
+  const uint32_t bar_sg = b0 + 48, bar_dp = b0 + 56, bar_dv = b0 + 64, bar_f0 = b0 + 72;
+  const uint32_t bar_dq = b0 + 80, bar_fin = b0 + 88, bar_drain = b0 + 96;
+  // softmax warps (256 arrivals): P, dA, dG written; TMEM G columns read;
+  // dV/dK of an item read
+  const uint32_t bar_p = b0 + 104, bar_da = b0 + 112, bar_ds = b0 + 120, bar_fl = b0 + 128;
+  const uint32_t bar_acc = b0 + 136;
+  const uint32_t bar_red = b0 + 144;     // max |dA| of each softmax warp (8)
+  const uint32_t bar_x0 = b0 + 152;      // 4 lane-quadrant rendezvous (2 each)
+  const uint32_t bar_stq = b0 + 184;     // each softmax warp staged its dQ rows (8)
+  const uint32_t bar_str = b0 + 192;     // each softmax warp staged its dR rows (8)
+  const uint32_t bar_sfree = b0 + 200;   // the dQ staging has been read (1)
+  const uint32_t bar_gfree = b0 + 208;   // the dR staging has been read (1)
+  uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 216);
+  volatile int *abort_flag = (volatile int *)(smem + F_BAR + 220);
+  volatile float *wmax = (volatile float *)(smem + F_BAR + 224);  // [2][8]
   if (threadIdx.x == 0) {
-    mbar_init(bar_kv, 1); mbar_init(bar_ld, 1); mbar_init(bar_sg, 1);
-    mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_dp, 1);
-    mbar_init(bar_ds, kSoftmaxWarps * 32); mbar_init(bar_fin, 1);
-    mbar_init(bar_fl, kSoftmaxWarps * 32); mbar_init(bar_acc, kSoftmaxWarps * 32);
-    mbar_init(bar_red, kSoftmaxWarps); mbar_init(bar_drain, 1);
+    mbar_init(bar_kv, 1); mbar_init(bar_qv0, 1); mbar_init(bar_qv1, 1); mbar_init(bar_r, 1);
+    mbar_init(bar_do, 1); mbar_init(bar_qu, 1);
+    mbar_init(bar_sg, 1); mbar_init(bar_dp, 1); mbar_init(bar_dv, 1); mbar_init(bar_f0, 1);
+    mbar_init(bar_dq, 1); mbar_init(bar_fin, 1); mbar_init(bar_drain, 1);
+    mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_da, kSoftmaxWarps * 32);
+    mbar_init(bar_ds, kSoftmaxWarps * 32); mbar_init(bar_fl, kSoftmaxWarps * 32);
+    mbar_init(bar_acc, kSoftmaxWarps * 32);
+    mbar_init(bar_red, kSoftmaxWarps);
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
-    mbar_init(bar_staged, kSoftmaxWarps);
-    mbar_init(bar_sfree, 1);
-    mbar_init(bar_gfree, 1);
-    mbar_init(bar_da, kSoftmaxWarps * 32);
-    mbar_init(bar_f0, 1);
-    mbar_init(bar_do, 1);
-    mbar_init(bar_qu, 1);
+    mbar_init(bar_stq, kSoftmaxWarps); mbar_init(bar_str, kSoftmaxWarps);
+    mbar_init(bar_sfree, 1); mbar_init(bar_gfree, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -240,127 +251,183 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------ producer / MMA issuer
-    if (lane == 0) {
-      int n_kv = 0, n_ld = 0, n_do = 0, n_qu = 0;  // copies issued per barrier
-      // dO of a pair is loaded once the previous pair's dP and dV are done,
-      // (Q+u) once its dK and dQc are done; the rest at the end of the pair
-      auto load_do = [&](const PairCursor &c) {
+    // Pair g reads (Q+v) buffer g & 1. Each operand is reloaded as soon as
+    // its last reader of the previous pair is done: dO after dV, (Q+u) after
+    // dK, the R band after dQp, K/V of a new item after dQc; the next pair's
+    // (Q+v) goes into the other buffer right after this pair's G is issued.
+    // The whole warp runs the schedule (uniform control flow, so that the
+    // descriptors stay in uniform registers); one elected thread issues.
+    int n_kv = 0, n_qv[2] = {0, 0}, n_r = 0, n_do = 0, n_qu = 0;  // copies issued per barrier
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+    };
+    auto load_do = [&](const PairCursor &c) {
+      if (elect_one()) {
         mbar_expect_tx(bar_do, 16384);
         tma_load_3d(sb + F_DO, &tm_do, 0, c.i0(), c.it.bh, bar_do);
-        ++n_do;
-      };
-      auto load_qu = [&](const PairCursor &c) {
+      }
+      __syncwarp();
+      ++n_do;
+    };
+    auto load_qu = [&](const PairCursor &c) {
+      if (elect_one()) {
         mbar_expect_tx(bar_qu, 16384);
         tma_load_3d(sb + F_QU, &tm_qu, 0, c.i0(), c.it.bh, bar_qu);
-        ++n_qu;
-      };
-      auto issue_loads = [&](const PairCursor &c) {
-        const FItem &it = c.it;
+      }
+      __syncwarp();
+      ++n_qu;
+    };
+    auto load_qv = [&](const PairCursor &c, int buf) {
+      if (elect_one()) {
+        const uint32_t bar = buf ? bar_qv1 : bar_qv0;
+        mbar_expect_tx(bar, 16384);
+        tma_load_3d(sb + (buf ? F_QV1 : F_QV0), &tm_qv16, 0, c.i0(), c.it.bh, bar);
+      }
+      __syncwarp();
+      ++n_qv[buf];
+    };
+    auto load_r_kv = [&](const PairCursor &c) {
+      const FItem &it = c.it;
+      if (elect_one()) {
         if (c.n == 0) {
           mbar_expect_tx(bar_kv, 2 * 16384);
           tma_load_3d(sb + F_K, &tm_k, 0, it.x.phys0, it.bh, bar_kv);
           tma_load_3d(sb + F_V, &tm_v, 0, it.x.phys0, it.bh, bar_kv);
-          ++n_kv;
         }
-        const int i0 = c.i0();
-        mbar_expect_tx(bar_ld, 16384 + 32768);
-        tma_load_3d(sb + F_QV, &tm_qv16, 0, i0, it.bh, bar_ld);
-        tma_load_3d(sb + F_R, &tm_r16, 0, i0 - it.x.jlog0 - (BK - 1), it.h, bar_ld);
-        ++n_ld;
-      };
-      bool ok = true;
-      PairCursor c;
-      c.init(p);
-      if (c.valid) {
-        load_qu(c);
-        load_do(c);
-        issue_loads(c);
+        mbar_expect_tx(bar_r, 32768);
+        tma_load_3d(sb + F_R, &tm_r16, 0, c.i0() - it.x.jlog0 - (BK - 1), it.h, bar_r);
       }
-      for (int g = 0; ok && c.valid; ++g) {
-        const bool first = c.n == 0;
-        PairCursor nx = c;
-        nx.next(p);
-        if (first && !(ok = mbar_wait(bar_kv, (c.k & 1), abort_flag))) break;
-        if (!(ok = mbar_wait(bar_qu, g & 1, abort_flag) && mbar_wait(bar_ld, g & 1, abort_flag))) break;
-        // G's columns hold the previous pair's dQ / dR until it was flushed
-        if (g > 0 && !(ok = mbar_wait(bar_fl, (g - 1) & 1, abort_flag))) break;
+      __syncwarp();
+      if (c.n == 0) ++n_kv;
+      ++n_r;
+    };
+    // operand descriptors: two bases built once (K-major and MN-major
+    // layouts at the start of shared memory); a tile, k-step or buffer is
+    // a constant added to them
+    const uint64_t kb = kdesc0(sb), mb0 = mndesc0(sb);
+    const uint64_t k_qu = sdesc_add(kb, F_QU), k_k = sdesc_add(kb, F_K), k_do = sdesc_add(kb, F_DO);
+    const uint64_t k_v = sdesc_add(kb, F_V), k_r = sdesc_add(kb, F_R), k_pa = sdesc_add(kb, F_PA);
+    const uint64_t k_dg = sdesc_add(kb, F_DG);
+    const uint64_t m_pa = sdesc_add(mb0, F_PA), m_do = sdesc_add(mb0, F_DO), m_qu = sdesc_add(mb0, F_QU);
+    const uint64_t m_k = sdesc_add(mb0, F_K), m_r = sdesc_add(mb0, F_R), m_dg = sdesc_add(mb0, F_DG);
+    bool ok = true;
+    PairCursor c;
+    c.init(p);
+    if (c.valid) {
+      load_qu(c);
+      load_qv(c, 0);
+      load_do(c);
+      load_r_kv(c);
+    }
+    for (int g = 0; ok && c.valid; ++g) {
+      const bool first = c.n == 0;
+      const int buf = g & 1;
+      const uint32_t f_qv = buf ? F_QV1 : F_QV0;
+      const uint64_t k_qv = sdesc_add(kb, f_qv), m_qv = sdesc_add(mb0, f_qv);
+      PairCursor nx = c;
+      nx.next(p);
+      if (first && !(ok = wait(bar_kv, (c.k & 1)))) break;
+      if (!(ok = wait(bar_qu, g & 1) && wait(buf ? bar_qv1 : bar_qv0, (g >> 1) & 1) && wait(bar_r, g & 1))) break;
+      // G's columns hold the previous pair's dQ / dR until it was flushed
+      if (g > 0 && !(ok = wait(bar_fl, (g - 1) & 1))) break;
+      if (elect_one()) {
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_S, kdesc(sb + F_QU, k), kdesc(sb + F_K, k), IDESC_S, k > 0);
+          mma_bf16(tmem + TM_S, kdesc(k_qu, k), kdesc(k_k, k), IDESC_S, k > 0);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_G, kdesc(sb + F_QV, k), kdesc(sb + F_R, k), IDESC_G_F16, k > 0);
+          mma_bf16(tmem + TM_G, kdesc(k_qv, k), kdesc(k_r, k), IDESC_G_F16, k > 0);
         mma_commit(bar_sg);
-        if (!(ok = mbar_wait(bar_p, g & 1, abort_flag))) break;
-        // the first dV of an item overwrites the accumulators: the previous
-        // item's epilogue must have read them
-        if (first && c.k > 0 && !(ok = mbar_wait(bar_acc, (c.k - 1) & 1, abort_flag))) break;
-        if (!(ok = mbar_wait(bar_do, g & 1, abort_flag))) break;
+      }
+      __syncwarp();
+      // the other (Q+v) buffer was last read by the previous pair's dR,
+      // which completed before its flush released the G columns
+      if (nx.valid) load_qv(nx, buf ^ 1);
+      if (!(ok = wait(bar_p, g & 1))) break;
+      // the first dV of an item overwrites the accumulators: the previous
+      // item's epilogue must have read them
+      if (first && c.k > 0 && !(ok = wait(bar_acc, (c.k - 1) & 1))) break;
+      if (!(ok = wait(bar_do, g & 1))) break;
+      if (elect_one()) {
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_S, kdesc(sb + F_DO, k), kdesc(sb + F_V, k), IDESC_S, k > 0);
+          mma_bf16(tmem + TM_S, kdesc(k_do, k), kdesc(k_v, k), IDESC_S, k > 0);
+        mma_commit(bar_dp);  // dA needs only dP
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // dV += P^T dO
-          mma_bf16(tmem + TM_DV, mndesc(sb + F_PA, k), mndesc(sb + F_DO, k), IDESC_MN_MN,
-                   (!first || k > 0) ? 1u : 0u);
-        mma_commit(bar_dp);
-        if (nx.valid) {  // dO is free once dP and dV are done
-          if (!(ok = mbar_wait(bar_dp, g & 1, abort_flag))) break;
-          load_do(nx);
-        }
-        // dK and dQc as soon as dA is written, while the softmax warps
-        // shear dG; then dQp and the dR blocks
-        if (!(ok = mbar_wait(bar_da, g & 1, abort_flag))) break;
+          mma_bf16(tmem + TM_DV, mndesc(m_pa, k), mndesc(m_do, k), IDESC_MN_MN, (!first || k > 0) ? 1u : 0u);
+        mma_commit(bar_dv);
+      }
+      __syncwarp();
+      if (nx.valid) {  // dO is free once dP and dV are done
+        if (!(ok = wait(bar_dv, g & 1))) break;
+        load_do(nx);
+      }
+      // dK and dQc as soon as dA is written, while the softmax warps
+      // shear dG; then dQp and the dR blocks
+      if (!(ok = wait(bar_da, g & 1))) break;
+      if (elect_one()) {
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // dK += dA^T (Q+u)
-          mma_bf16(tmem + TM_DK, mndesc(sb + F_PA, k), mndesc(sb + F_QU, k), IDESC_MN_MN,
-                   (!first || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + TM_DK, mndesc(m_pa, k), mndesc(m_qu, k), IDESC_MN_MN, (!first || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // dQc = dA K
-          mma_bf16(tmem + TM_QC, kdesc(sb + F_PA, k), mndesc(sb + F_K, k), IDESC_K_MN, k > 0);
+          mma_bf16(tmem + TM_QC, kdesc(k_pa, k), mndesc(m_k, k), IDESC_K_MN, k > 0);
         mma_commit(bar_f0);
-        if (nx.valid) {  // (Q+u) is free once dK is done
-          if (!(ok = mbar_wait(bar_f0, g & 1, abort_flag))) break;
-          load_qu(nx);
-        }
-        if (!(ok = mbar_wait(bar_ds, g & 1, abort_flag))) break;
+      }
+      __syncwarp();
+      if (nx.valid) {  // (Q+u) is free once dK is done
+        if (!(ok = wait(bar_f0, g & 1))) break;
+        load_qu(nx);
+      }
+      if (!(ok = wait(bar_ds, g & 1))) break;
+      if (elect_one()) {
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 16; ++k)  // dQp = dG Rband (fp16)
-          mma_bf16(tmem + TM_QP, kdesc(sb + F_DG, k), mndesc(sb + F_R, k), IDESC_K_MN_F16, k > 0);
+          mma_bf16(tmem + TM_QP, kdesc(k_dg, k), mndesc(m_r, k), IDESC_K_MN_F16, k > 0);
+        mma_commit(bar_dq);
+      }
+      __syncwarp();
+      if (nx.valid) {
+        // the R band is free once dQp is done, K and V once dQc and dP are
+        if (!(ok = wait(bar_dq, g & 1))) break;
+        load_r_kv(nx);
+      }
+      if (elect_one()) {
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb)  // dR band = dG^T (Q+v), two 128-distance blocks (fp16)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_bf16(tmem + TM_R0 + 64 * mb, mndesc(sb + F_DG + 2 * mb * 16384, k),
-                     mndesc(sb + F_QV, k), IDESC_MN_MN_F16, k > 0);
+            mma_bf16(tmem + TM_R0 + 64 * mb, mndesc(sdesc_add(m_dg, 2 * mb * 16384), k), mndesc(m_qv, k),
+                     IDESC_MN_MN_F16, k > 0);
         mma_commit(bar_fin);
-        if (nx.valid) {
-          // every operand of this pair has been consumed once its MMAs are done
-          if (!(ok = mbar_wait(bar_fin, g & 1, abort_flag))) break;
-          issue_loads(nx);
-        }
-        c = nx;
       }
-      if (!ok) {
-        // wind down: let in-flight copies and MMAs land before TMEM and
-        // shared memory are released
-        // (the latest copy of each barrier; an earlier one completed before
-        // the latest was issued, and a completed phase returns at once)
+      __syncwarp();
+      c = nx;
+    }
+    if (!ok) {
+      // wind down: let in-flight copies and MMAs land before TMEM and
+      // shared memory are released
+      // (the latest copy of each barrier; an earlier one completed before
+      // the latest was issued, and a completed phase returns at once)
+      if (elect_one()) {
         volatile int no_abort = 0;
         if (n_kv > 0) mbar_wait(bar_kv, (n_kv - 1) & 1, &no_abort);
-        if (n_ld > 0) mbar_wait(bar_ld, (n_ld - 1) & 1, &no_abort);
+        if (n_qv[0] > 0) mbar_wait(bar_qv0, (n_qv[0] - 1) & 1, &no_abort);
+        if (n_qv[1] > 0) mbar_wait(bar_qv1, (n_qv[1] - 1) & 1, &no_abort);
+        if (n_r > 0) mbar_wait(bar_r, (n_r - 1) & 1, &no_abort);
         if (n_do > 0) mbar_wait(bar_do, (n_do - 1) & 1, &no_abort);
         if (n_qu > 0) mbar_wait(bar_qu, (n_qu - 1) & 1, &no_abort);
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0, &no_abort);
         atomicExch(&g_bwd_error, 1);
       }
+      __syncwarp();
     }
-    __syncwarp();
   } else if (warp == kStoreWarp) {
     // --------------------------------------------------- reduction issuer
     if (lane == 0) {
@@ -368,13 +435,12 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       PairCursor c;
       c.init(p);
       for (int g = 0; c.valid; ++g) {
-        if (!(ok = mbar_wait(bar_staged, g & 1, abort_flag))) break;
         const int i0 = c.i0();
         const int d0 = kDrPad + i0 - c.it.x.jlog0 - (BK - 1);  // >= 1
         // warp (quad, hf) staged its dQ box in the P/dA buffer and its dR
-        // block-hf rows in dG atoms 2hf, 2hf+1. The dQ boxes go first, in a
-        // bulk group of their own: the next pair's P needs that buffer
-        // soon, its dG not before the dA of that pair.
+        // block-hf rows in dG atoms 2hf, 2hf+1; dQ is staged first (while
+        // the dR MMAs run)
+        if (!(ok = mbar_wait(bar_stq, g & 1, abort_flag))) break;
 #pragma unroll 1
         for (int w = 0; w < kSoftmaxWarps; ++w) {
           const int quad = w & 3, hf = w >> 2;
@@ -383,6 +449,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             tma_reduce_add_3d(&tm_dq, 32 * hf, qrow, c.it.bh, sb + F_PA + hf * 16384 + quad * 4096);
         }
         bulk_commit();
+        if (!(ok = mbar_wait(bar_str, g & 1, abort_flag))) break;
 #pragma unroll 1
         for (int w = 0; w < kSoftmaxWarps; ++w) {
           const int quad = w & 3, hf = w >> 2;
@@ -478,12 +545,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           y[32 * cc + k + 1] = t.y;
         }
       }
-      // P is no longer read: dP and dV were committed together
-      store_half_bf16(row_pa, y);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar_da);
-      // CTA-wide max |dA| of this pair -> power-of-two fp16 scale of dG
+      // CTA-wide max |dA| of this pair -> power-of-two fp16 scale of dG;
+      // this warp's part is published while the dV product may still run
       float am = 0.f;
 #pragma unroll
       for (int k = 0; k < 64; k += 2) am = fmax3(am, fabsf(y[k]), fabsf(y[k + 1]));
@@ -492,6 +555,13 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         wmax[(g & 1) * 8 + warp] = am;
         mbar_arrive(bar_red);
       }
+      // P is no longer read once dV is done
+      ok = mbar_wait(bar_dv, g & 1, abort_flag);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      store_half_bf16(row_pa, y);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_da);
       ok = mbar_wait(bar_red, g & 1, abort_flag);  // bounded, unlike a named barrier
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       am = 0.f;
@@ -541,7 +611,6 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           for (int m = 35; m >= 0; --m) w[m] = take ? (m >= b ? w[m >= b ? m - b : 0] : 0u) : w[m];
         }
         const int cbase = c0 + (hf ? 0 : 8);
-        const uint32_t xrow = sb + F_X + ii * 16;
         // columns outside [ii, ii + 127] are zero (staging overwrote them)
         if (hf == 1) {
 #pragma unroll
@@ -552,15 +621,18 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           for (int C = 17; C < 32; ++C)
             if (C > c0 + 16) st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384, 0, 0, 0, 0);
         }
+        // chunk c0 + 8 is shared by the two halves: the upper half (hf 1)
+        // writes its part there (zeros in the other half's positions), the
+        // lower half ORs its part in after the rendezvous
+        const uint32_t shared_chunk = sw128_at(row_dg, (c0 + 8) & 7) + ((c0 + 8) >> 3) * 16384;
         if (hf == 1) {
-          // chunk cbase + 8 is shared with the other half: hand it over
-          st_shared_v4(xrow, w[32], w[33], w[34], w[35]);
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
             const int C = cbase + t;
             st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384, w[4 * t],
                          w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
           }
+          st_shared_v4(shared_chunk, w[32], w[33], w[34], w[35]);
         } else {
 #pragma unroll
           for (int t = 1; t < 9; ++t) {
@@ -573,72 +645,75 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (hf == 0) {
           // the two halves' values occupy complementary positions of the
           // shared chunk (+0 elsewhere): OR merges them exactly
-          uint32_t a, b, cc, d;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
-                       : "r"(xrow));
-          const int C = cbase;
-          st_shared_v4(sw128_at(row_dg, C & 7) + (C >> 3) * 16384,
-                       a | w[0], b | w[1], cc | w[2], d | w[3]);
+          const uint4 o = ld_shared_v4(shared_chunk);
+          st_shared_v4(shared_chunk, o.x | w[0], o.y | w[1], o.z | w[2], o.w | w[3]);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_ds);
+      float v[32];
+      ok = mbar_wait(bar_dq, g & 1, abort_flag);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      tc_fence_after();
+      {
+        // flush, dQ part (while the dR MMAs run): this half's 32 dQ columns
+        // of row ii staged in fp32 (a 128-byte swizzled 32-column box) in the
+        // P/dA buffer, whose dA the finished dK/dQc products no longer read
+        uint32_t qc[32], qp[32];
+        tmem_ld32(trow + TM_QC + 32 * hf, qc);
+        tmem_ld32(trow + TM_QP + 32 * hf, qp);
+        tmem_wait_ld();
+        const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float2 t = __fmul2_rn(make_float2(__uint_as_float(qp[e]), __uint_as_float(qp[e + 1])), inv2);
+          v[e] = t.x;
+          v[e + 1] = t.y;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 lo = __fadd2_rn(make_float2(__uint_as_float(qc[4 * e]), __uint_as_float(qc[4 * e + 1])),
+                                       make_float2(v[4 * e], v[4 * e + 1]));
+          const float2 hi = __fadd2_rn(make_float2(__uint_as_float(qc[4 * e + 2]), __uint_as_float(qc[4 * e + 3])),
+                                       make_float2(v[4 * e + 2], v[4 * e + 3]));
+          st_shared_v4(sw128_at(row_pa, e), __float_as_uint(lo.x),
+                       __float_as_uint(lo.y), __float_as_uint(hi.x), __float_as_uint(hi.y));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_stq);
+      }
       ok = mbar_wait(bar_fin, g & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       {
-        // flush: this half's 32 dQ columns of row ii and row ii of dR block
-        // hf, staged in fp32 (128-byte swizzled 32-column boxes) in the P/dA
-        // and dG buffers, then added into the accumulators by TMA
-        float v[32];
-        {
-          uint32_t qc[32], qp[32];
-          tmem_ld32(trow + TM_QC + 32 * hf, qc);
-          tmem_ld32(trow + TM_QP + 32 * hf, qp);
-          tmem_wait_ld();
-          const float2 inv2 = make_float2(inv, inv);
+        // flush, dR part: row ii of dR block hf, staged in fp32 in dG atoms
+        // 2hf, 2hf+1 (the dG products are done)
+        uint32_t ra[32], rb[32];
+        tmem_ld32(trow + TM_R0 + 64 * hf, ra);
+        tmem_ld32(trow + TM_R0 + 64 * hf + 32, rb);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_fl);  // the G columns may take the next pair's logits
+        const float2 inv2 = make_float2(inv, inv);
+        auto scaled = [&](const uint32_t(&src)[32], int e) {
+          return __fmul2_rn(make_float2(__uint_as_float(src[e]), __uint_as_float(src[e + 1])), inv2);
+        };
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 t = __fmul2_rn(make_float2(__uint_as_float(qp[e]), __uint_as_float(qp[e + 1])), inv2);
-            v[e] = t.x;
-            v[e + 1] = t.y;
-          }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float2 lo = __fadd2_rn(make_float2(__uint_as_float(qc[4 * e]), __uint_as_float(qc[4 * e + 1])),
-                                         make_float2(v[4 * e], v[4 * e + 1]));
-            const float2 hi = __fadd2_rn(make_float2(__uint_as_float(qc[4 * e + 2]), __uint_as_float(qc[4 * e + 3])),
-                                         make_float2(v[4 * e + 2], v[4 * e + 3]));
-            st_shared_v4(sw128_at(row_pa, e), __float_as_uint(lo.x),
-                         __float_as_uint(lo.y), __float_as_uint(hi.x), __float_as_uint(hi.y));
-          }
-        }
-        {
-          uint32_t ra[32], rb[32];
-          tmem_ld32(trow + TM_R0 + 64 * hf, ra);
-          tmem_ld32(trow + TM_R0 + 64 * hf + 32, rb);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(bar_fl);  // the G columns may take the next pair's logits
-          const float2 inv2 = make_float2(inv, inv);
-          auto scaled = [&](const uint32_t(&src)[32], int e) {
-            return __fmul2_rn(make_float2(__uint_as_float(src[e]), __uint_as_float(src[e + 1])), inv2);
-          };
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float2 a0 = scaled(ra, 4 * e), a1 = scaled(ra, 4 * e + 2);
-            const float2 b0 = scaled(rb, 4 * e), b1 = scaled(rb, 4 * e + 2);
-            st_shared_v4(sw128_at(row_dr, e), __float_as_uint(a0.x),
-                         __float_as_uint(a0.y), __float_as_uint(a1.x), __float_as_uint(a1.y));
-            st_shared_v4(sw128_at(row_dr, e) + 16384, __float_as_uint(b0.x),
-                         __float_as_uint(b0.y), __float_as_uint(b1.x), __float_as_uint(b1.y));
-          }
+        for (int e = 0; e < 8; ++e) {
+          const float2 a0 = scaled(ra, 4 * e), a1 = scaled(ra, 4 * e + 2);
+          const float2 b0 = scaled(rb, 4 * e), b1 = scaled(rb, 4 * e + 2);
+          st_shared_v4(sw128_at(row_dr, e), __float_as_uint(a0.x),
+                       __float_as_uint(a0.y), __float_as_uint(a1.x), __float_as_uint(a1.y));
+          st_shared_v4(sw128_at(row_dr, e) + 16384, __float_as_uint(b0.x),
+                       __float_as_uint(b0.y), __float_as_uint(b1.x), __float_as_uint(b1.y));
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_staged);
+        if (lane == 0) mbar_arrive(bar_str);
+      }
+      {
         // column sums of dQp over the warp's 32 rows (recursive halving):
         // afterwards lane l holds column 32*hf + l
 #pragma unroll

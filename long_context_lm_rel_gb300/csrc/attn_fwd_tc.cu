@@ -315,44 +315,55 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------ producer / MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the schedule (uniform control flow, so that the
+    // descriptors stay in uniform registers); one elected thread issues.
+    {
       bool pending[2] = {false, false};
       int nissued[2] = {0, 0};
       Cursor<RESET, SPLIT> tc_;  // next tile to load
       tc_.init(p, nitems);
       int g_tma = 0;
+      auto wait = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+      };
       auto issue_tma = [&]() {
         const int s = g_tma & 1;
         const KeyTile x = KeyTiles(tc_.it.m, p.cap, tc_.it.head, min(tc_.it.i0 + BQ, p.L)).get(tc_.t);
-        const uint32_t bar = s ? bar_full1 : bar_full0;
-        mbar_expect_tx(bar, STAGE_TX);
-        tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, tc_.it.bh, bar);
-        tma_load_3d(sbase + SM_V + s * 16384, &tm_v, 0, x.phys0, tc_.it.bh, bar);
-        tma_load_3d(sbase + SM_R + s * 32768, &tm_r, 0, tc_.it.i0 - x.jlog0 - (BK - 1), tc_.it.h, bar);
+        if (elect_one()) {
+          const uint32_t bar = s ? bar_full1 : bar_full0;
+          mbar_expect_tx(bar, STAGE_TX);
+          tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, tc_.it.bh, bar);
+          tma_load_3d(sbase + SM_V + s * 16384, &tm_v, 0, x.phys0, tc_.it.bh, bar);
+          tma_load_3d(sbase + SM_R + s * 32768, &tm_r, 0, tc_.it.i0 - x.jlog0 - (BK - 1), tc_.it.h, bar);
+        }
+        __syncwarp();
         pending[s] = true;
         ++nissued[s];
         ++g_tma;
         tc_.next(p);
       };
+      // operand descriptors, built once; a k-step or a stage is an add
+      const uint64_t d_qu = sdesc_sw128(sbase + SM_QU, 16, 1024), d_qv = sdesc_sw128(sbase + SM_QV, 16, 1024);
+      const uint64_t d_k = sdesc_sw128(sbase + SM_K, 16, 1024), d_r = sdesc_sw128(sbase + SM_R, 16, 1024);
+      const uint64_t d_p = sdesc_sw128(sbase + SM_P, 16, 1024), d_v = sdesc_sw128(sbase + SM_V, 16, 1024);
       auto issue_sg = [&](int g) {
         const int s = g & 1;
+        const uint64_t dk_s = sdesc_add(d_k, s * 16384), dr_s = sdesc_add(d_r, s * 32768);
+        if (elect_one()) {
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t a = sdesc_sw128(sbase + SM_QU + k * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(sbase + SM_K + s * 16384 + k * 32, 16, 1024);
-          mma_bf16(tmem + TM_S, a, b, IDESC_S, k > 0);
-        }
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + TM_S, sdesc_add(d_qu, k * 32), sdesc_add(dk_s, k * 32), IDESC_S, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t a = sdesc_sw128(sbase + SM_QV + k * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(sbase + SM_R + s * 32768 + k * 32, 16, 1024);
-          mma_bf16(tmem + TM_G, a, b, IDESC_G, k > 0);
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + TM_G, sdesc_add(d_qv, k * 32), sdesc_add(dr_s, k * 32), IDESC_G, k > 0);
+          mma_commit(bar_sg);
         }
-        mma_commit(bar_sg);
+        __syncwarp();
       };
       auto wait_full = [&](int g) {
         const int s = g & 1;
-        const bool r = mbar_wait(s ? bar_full1 : bar_full0, (g >> 1) & 1, abort_flag);
+        const bool r = wait(s ? bar_full1 : bar_full0, (g >> 1) & 1);
         pending[s] = false;
         return r;
       };
@@ -369,8 +380,11 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
         if (w >= nitems) return;
         const Item qi = item_at<RESET>(p, w);
-        mbar_expect_tx(bar_q, 16384);
-        tma_load_3d(sbase + SM_QRAW, &tm_q, 0, qi.i0, qi.bh, bar_q);
+        if (elect_one()) {
+          mbar_expect_tx(bar_q, 16384);
+          tma_load_3d(sbase + SM_QRAW, &tm_q, 0, qi.i0, qi.bh, bar_q);
+        }
+        __syncwarp();
         ++nq_loads;
       };
       bool ok = true;
@@ -380,7 +394,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       if (tc_.valid) issue_tma();
       if (tc_.valid) issue_tma();
       if (mc.valid) {
-        ok = mbar_wait(bar_qready, 0, abort_flag) && wait_full(0);
+        ok = wait(bar_qready, 0) && wait_full(0);
         if (ok) {
           load_q(1);  // the softmax has read item 0's raw rows
           issue_sg(0);
@@ -393,34 +407,34 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // S/G of tile g+1 as soon as the softmax released S/G of tile g
         // (same item: the Q tiles are unchanged)
         if (nx.valid && !new_item) {
-          if (!(ok = mbar_wait(bar_sgfree, g & 1, abort_flag) && wait_full(g + 1))) break;
+          if (!(ok = wait(bar_sgfree, g & 1) && wait_full(g + 1))) break;
           issue_sg(g + 1);
         }
-        if (!(ok = mbar_wait(bar_pr, g & 1, abort_flag))) break;
+        if (!(ok = wait(bar_pr, g & 1))) break;
         // the first P.V of an item overwrites O: its epilogue must have read it
-        if (mc.t == mc.t0 && mc.k > 0 && !(ok = mbar_wait(bar_ofree, (mc.k - 1) & 1, abort_flag))) break;
-        tc_fence_after();
+        if (mc.t == mc.t0 && mc.k > 0 && !(ok = wait(bar_ofree, (mc.k - 1) & 1))) break;
         const int s = g & 1;
+        const uint64_t dv_s = sdesc_add(d_v, s * 16384);
+        const uint32_t acc0 = mc.t > mc.t0 ? 1u : 0u;
+        if (elect_one()) {
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // O_h += P_h V_h for the key halves h = k / 4
-          const uint64_t a = sdesc_sw128(sbase + SM_P + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(sbase + SM_V + s * 16384 + k * 2048, 16, 1024);
-          mma_bf16(tmem + TM_O + 64 * (k >> 2), a, b, IDESC_O, (mc.t > mc.t0 || (k & 3) > 0) ? 1u : 0u);
+          for (int k = 0; k < 8; ++k)  // O_h += P_h V_h for the key halves h = k / 4
+            mma_bf16(tmem + TM_O + 64 * (k >> 2), sdesc_add(d_p, (k >> 2) * 16384 + (k & 3) * 32),
+                     sdesc_add(dv_s, k * 2048), IDESC_O, ((k & 3) > 0) ? 1u : acc0);
+          mma_commit(bar_pv);
         }
-        mma_commit(bar_pv);
+        __syncwarp();
         if (new_item) {
           // next item: its Q tiles are written once the softmax finished
           // this item's last tile
-          if (!(ok = mbar_wait(bar_sgfree, g & 1, abort_flag) &&
-                     mbar_wait(bar_qready, nx.k & 1, abort_flag) && wait_full(g + 1)))
-            break;
+          if (!(ok = wait(bar_sgfree, g & 1) && wait(bar_qready, nx.k & 1) && wait_full(g + 1))) break;
           load_q(nx.k + 1);  // the softmax has read item nx.k's raw rows
-          tc_fence_after();
           issue_sg(g + 1);
         }
         if (tc_.valid) {
           // stage g&1 is free once P.V(g) (and with it S/G(g)) completed
-          if (!(ok = mbar_wait(bar_pv, g & 1, abort_flag))) break;
+          if (!(ok = wait(bar_pv, g & 1))) break;
           issue_tma();
         }
         mc = nx;
@@ -428,13 +442,16 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       if (!ok) {
         // wind down: let in-flight copies and MMAs land before TMEM and
         // shared memory are released
-        volatile int no_abort = 0;
-        for (int s = 0; s < 2; ++s)
-          if (pending[s]) mbar_wait(s ? bar_full1 : bar_full0, (nissued[s] - 1) & 1, &no_abort);
-        if (nq_loads > 0) mbar_wait(bar_q, (nq_loads - 1) & 1, &no_abort);
-        mma_commit(bar_drain);
-        mbar_wait(bar_drain, 0, &no_abort);
-        atomicExch(&g_fwd_error, 1);
+        if (elect_one()) {
+          volatile int no_abort = 0;
+          for (int s = 0; s < 2; ++s)
+            if (pending[s]) mbar_wait(s ? bar_full1 : bar_full0, (nissued[s] - 1) & 1, &no_abort);
+          if (nq_loads > 0) mbar_wait(bar_q, (nq_loads - 1) & 1, &no_abort);
+          mma_commit(bar_drain);
+          mbar_wait(bar_drain, 0, &no_abort);
+          atomicExch(&g_fwd_error, 1);
+        }
+        __syncwarp();
       }
     }
     __syncwarp();

@@ -42,6 +42,20 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// One thread of the (converged) warp, the same one every time: the warp runs
+// a schedule in uniform control flow and this thread issues its copies and
+// MMAs, so that warp-uniform values (operand descriptors, coordinates) stay
+// in uniform registers.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred P;\n"
+      " elect.sync _|P, 0xffffffff;\n"
+      " selp.b32 %0, 1, 0, P;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -237,6 +251,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;
+}
+
+// The descriptor of the same tile layout byte_offset bytes further on (a
+// k-step inside a tile, another tile): the start address sits in the low
+// 14 bits as address / 16, and shared-memory addresses stay below 256 KB, so
+// the sum never carries out of that field. One 64-bit add per operand
+// instead of rebuilding the descriptor.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_offset) {
+  return desc + (uint64_t)(byte_offset >> 4);
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator,
