@@ -55,7 +55,7 @@ constexpr int kProducerWarp = kSoftmaxWarps;   // TMA loads and MMA issue
 constexpr int kStoreWarp = kSoftmaxWarps + 1;  // TMA reductions of the staged dQ / dR rows
 constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
-constexpr uint32_t IDESC_G_F16 = idesc_f16(128, 256, false, false);
+constexpr uint32_t IDESC_G_F16 = idesc_f16(128, 128, false, false);  // one 128-distance half of G
 constexpr uint32_t IDESC_MN_MN = idesc_bf16(128, 64, true, true);   // A^T . B, both d/row-major tiles
 constexpr uint32_t IDESC_K_MN = idesc_bf16(128, 64, false, true);
 constexpr uint32_t IDESC_K_MN_F16 = idesc_f16(128, 64, false, true);
@@ -199,10 +199,12 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const uint32_t b0 = sb + F_BAR;
-  // TMA: K/V of an item; (Q+v) of a pair into buffer 0 / 1; the R band;
-  // dO and (Q+u) of a pair
-  const uint32_t bar_kv = b0, bar_qv0 = b0 + 8, bar_qv1 = b0 + 16, bar_r = b0 + 24;
-  const uint32_t bar_do = b0 + 32, bar_qu = b0 + 40;
+  // TMA: every operand of pair g but dO ((Q+u), (Q+v), the R band and, for
+  // an item's first pair, K/V) completes one phase of bar_nx0 / bar_nx1 (by
+  // the parity of g), so that the producer waits once per pair for them; dO
+  // of a pair
+  const uint32_t bar_nx0 = b0 + 8, bar_nx1 = b0 + 16;
+  const uint32_t bar_do = b0 + 32;
   // MMA commits: S and G; dP; dV; dK and dQc; dQp; dR (the pair's last)
   const uint32_t bar_sg = b0 + 48, bar_dp = b0 + 56, bar_dv = b0 + 64, bar_f0 = b0 + 72;
   const uint32_t bar_dq = b0 + 80, bar_fin = b0 + 88, bar_drain = b0 + 96;
@@ -220,8 +222,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   volatile int *abort_flag = (volatile int *)(smem + F_BAR + 220);
   volatile float *wmax = (volatile float *)(smem + F_BAR + 224);  // [2][8]
   if (threadIdx.x == 0) {
-    mbar_init(bar_kv, 1); mbar_init(bar_qv0, 1); mbar_init(bar_qv1, 1); mbar_init(bar_r, 1);
-    mbar_init(bar_do, 1); mbar_init(bar_qu, 1);
+    mbar_init(bar_nx0, 1); mbar_init(bar_nx1, 1); mbar_init(bar_do, 1);
     mbar_init(bar_sg, 1); mbar_init(bar_dp, 1); mbar_init(bar_dv, 1); mbar_init(bar_f0, 1);
     mbar_init(bar_dq, 1); mbar_init(bar_fin, 1); mbar_init(bar_drain, 1);
     mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_da, kSoftmaxWarps * 32);
@@ -257,7 +258,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // (Q+v) goes into the other buffer right after this pair's G is issued.
     // The whole warp runs the schedule (uniform control flow, so that the
     // descriptors stay in uniform registers); one elected thread issues.
-    int n_kv = 0, n_qv[2] = {0, 0}, n_r = 0, n_do = 0, n_qu = 0;  // copies issued per barrier
+    // A phase of bar_nx{b} is opened by the copies issued without arrival
+    // ((Q+v), (Q+u)) and closed by the last one (the R band, with K/V), which
+    // arrives; the phase then completes when all of its bytes have landed.
+    int n_do = 0, nx_closed0 = 0, nx_closed1 = 0;
+    bool nx_open0 = false, nx_open1 = false;
     auto wait = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
     };
@@ -269,37 +274,55 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       __syncwarp();
       ++n_do;
     };
-    auto load_qu = [&](const PairCursor &c) {
+    // pb: the parity of the pair the copy is for
+    auto load_qu = [&](const PairCursor &c, int pb) {
       if (elect_one()) {
-        mbar_expect_tx(bar_qu, 16384);
-        tma_load_3d(sb + F_QU, &tm_qu, 0, c.i0(), c.it.bh, bar_qu);
+        const uint32_t bar = pb ? bar_nx1 : bar_nx0;
+        mbar_expect_tx_noarrive(bar, 16384);
+        tma_load_3d(sb + F_QU, &tm_qu, 0, c.i0(), c.it.bh, bar);
       }
       __syncwarp();
-      ++n_qu;
+      if (pb) nx_open1 = true; else nx_open0 = true;
     };
-    auto load_qv = [&](const PairCursor &c, int buf) {
+    auto load_qv = [&](const PairCursor &c, int pb) {
       if (elect_one()) {
-        const uint32_t bar = buf ? bar_qv1 : bar_qv0;
-        mbar_expect_tx(bar, 16384);
-        tma_load_3d(sb + (buf ? F_QV1 : F_QV0), &tm_qv16, 0, c.i0(), c.it.bh, bar);
+        const uint32_t bar = pb ? bar_nx1 : bar_nx0;
+        mbar_expect_tx_noarrive(bar, 16384);
+        tma_load_3d(sb + (pb ? F_QV1 : F_QV0), &tm_qv16, 0, c.i0(), c.it.bh, bar);
       }
       __syncwarp();
-      ++n_qv[buf];
+      if (pb) nx_open1 = true; else nx_open0 = true;
     };
-    auto load_r_kv = [&](const PairCursor &c) {
+    // The R band of a pair is two 128-row halves (distances d0 .. d0+127 and
+    // d0+128 .. d0+255) in two 16 KB slots. The next query tile of the same
+    // item needs d0+128 .. d0+383: its lower half is this pair's upper half,
+    // already resident, so only its upper half is loaded, into the slot of
+    // this pair's lower half. r_lo: the slot holding the lower half.
+    int r_lo = 0;
+    auto load_r_kv = [&](const PairCursor &c, int next_lo, int pb) {
       const FItem &it = c.it;
+      const int d0 = c.i0() - it.x.jlog0 - (BK - 1);
       if (elect_one()) {
+        const uint32_t bar = pb ? bar_nx1 : bar_nx0;
         if (c.n == 0) {
-          mbar_expect_tx(bar_kv, 2 * 16384);
-          tma_load_3d(sb + F_K, &tm_k, 0, it.x.phys0, it.bh, bar_kv);
-          tma_load_3d(sb + F_V, &tm_v, 0, it.x.phys0, it.bh, bar_kv);
+          mbar_expect_tx(bar, 4 * 16384);
+          tma_load_3d(sb + F_K, &tm_k, 0, it.x.phys0, it.bh, bar);
+          tma_load_3d(sb + F_V, &tm_v, 0, it.x.phys0, it.bh, bar);
+          tma_load_3d(sb + F_R, &tm_r16, 0, d0, it.h, bar);
+          tma_load_3d(sb + F_R + 16384, &tm_r16, 0, d0 + 128, it.h, bar);
+        } else {
+          mbar_expect_tx(bar, 16384);
+          tma_load_3d(sb + F_R + (next_lo ^ 1) * 16384, &tm_r16, 0, d0 + 128, it.h, bar);
         }
-        mbar_expect_tx(bar_r, 32768);
-        tma_load_3d(sb + F_R, &tm_r16, 0, c.i0() - it.x.jlog0 - (BK - 1), it.h, bar_r);
       }
       __syncwarp();
-      if (c.n == 0) ++n_kv;
-      ++n_r;
+      if (pb) {
+        nx_open1 = false;
+        ++nx_closed1;
+      } else {
+        nx_open0 = false;
+        ++nx_closed0;
+      }
     };
     // operand descriptors: two bases built once (K-major and MN-major
     // layouts at the start of shared memory); a tile, k-step or buffer is
@@ -314,10 +337,10 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     PairCursor c;
     c.init(p);
     if (c.valid) {
-      load_qu(c);
       load_qv(c, 0);
+      load_qu(c, 0);
       load_do(c);
-      load_r_kv(c);
+      load_r_kv(c, 0, 0);
     }
     for (int g = 0; ok && c.valid; ++g) {
       const bool first = c.n == 0;
@@ -326,24 +349,41 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const uint64_t k_qv = sdesc_add(kb, f_qv), m_qv = sdesc_add(mb0, f_qv);
       PairCursor nx = c;
       nx.next(p);
-      if (first && !(ok = wait(bar_kv, (c.k & 1)))) break;
-      if (!(ok = wait(bar_qu, g & 1) && wait(buf ? bar_qv1 : bar_qv0, (g >> 1) & 1) && wait(bar_r, g & 1))) break;
+      if (!(ok = wait(buf ? bar_nx1 : bar_nx0, (g >> 1) & 1))) break;  // (Q+u), (Q+v), R, K/V
       // G's columns hold the previous pair's dQ / dR until it was flushed
       if (g > 0 && !(ok = wait(bar_fl, (g - 1) & 1))) break;
+      const uint64_t k_rlo = sdesc_add(k_r, r_lo * 16384), k_rhi = sdesc_add(k_r, (r_lo ^ 1) * 16384);
+      const uint64_t m_rlo = sdesc_add(m_r, r_lo * 16384), m_rhi = sdesc_add(m_r, (r_lo ^ 1) * 16384);
       if (elect_one()) {
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_bf16(tmem + TM_S, kdesc(k_qu, k), kdesc(k_k, k), IDESC_S, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_G, kdesc(k_qv, k), kdesc(k_r, k), IDESC_G_F16, k > 0);
+        for (int k = 0; k < 4; ++k) {  // G columns 0-127 from the lower half, 128-255 from the upper
+          mma_bf16(tmem + TM_G, kdesc(k_qv, k), kdesc(k_rlo, k), IDESC_G_F16, k > 0);
+          mma_bf16(tmem + TM_G + 128, kdesc(k_qv, k), kdesc(k_rhi, k), IDESC_G_F16, k > 0);
+        }
         mma_commit(bar_sg);
       }
       __syncwarp();
       // the other (Q+v) buffer was last read by the previous pair's dR,
       // which completed before its flush released the G columns
       if (nx.valid) load_qv(nx, buf ^ 1);
+      // the next pair's other operands come from HBM on first touch (about
+      // 2.5k cycles): pull them into L2 now, a pair ahead of their loads
+      if (nx.valid && elect_one()) {
+        const int i0n = nx.i0(), d0n = i0n - nx.it.x.jlog0 - (BK - 1);
+        tma_prefetch_l2_3d(&tm_qu, 0, i0n, nx.it.bh);
+        tma_prefetch_l2_3d(&tm_do, 0, i0n, nx.it.bh);
+        tma_prefetch_l2_3d(&tm_r16, 0, d0n + 128, nx.it.h);
+        if (nx.n == 0) {
+          tma_prefetch_l2_3d(&tm_r16, 0, d0n, nx.it.h);
+          tma_prefetch_l2_3d(&tm_k, 0, nx.it.x.phys0, nx.it.bh);
+          tma_prefetch_l2_3d(&tm_v, 0, nx.it.x.phys0, nx.it.bh);
+        }
+      }
+      __syncwarp();
       if (!(ok = wait(bar_p, g & 1))) break;
       // the first dV of an item overwrites the accumulators: the previous
       // item's epilogue must have read them
@@ -381,21 +421,24 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       __syncwarp();
       if (nx.valid) {  // (Q+u) is free once dK is done
         if (!(ok = wait(bar_f0, g & 1))) break;
-        load_qu(nx);
+        load_qu(nx, buf ^ 1);
       }
       if (!(ok = wait(bar_ds, g & 1))) break;
       if (elect_one()) {
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 16; ++k)  // dQp = dG Rband (fp16)
-          mma_bf16(tmem + TM_QP, kdesc(k_dg, k), mndesc(m_r, k), IDESC_K_MN_F16, k > 0);
+        for (int k = 0; k < 16; ++k)  // dQp = dG Rband (fp16), band rows 16k .. 16k+15
+          mma_bf16(tmem + TM_QP, kdesc(k_dg, k), mndesc(k < 8 ? m_rlo : m_rhi, k & 7), IDESC_K_MN_F16, k > 0);
         mma_commit(bar_dq);
       }
       __syncwarp();
       if (nx.valid) {
-        // the R band is free once dQp is done, K and V once dQc and dP are
+        // the R band's lower half is free once dQp is done, K and V once dQc
+        // and dP are
         if (!(ok = wait(bar_dq, g & 1))) break;
-        load_r_kv(nx);
+        const int next_lo = nx.n == 0 ? 0 : (r_lo ^ 1);
+        load_r_kv(nx, next_lo, buf ^ 1);
+        r_lo = next_lo;
       }
       if (elect_one()) {
 #pragma unroll
@@ -416,12 +459,14 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       // the latest was issued, and a completed phase returns at once)
       if (elect_one()) {
         volatile int no_abort = 0;
-        if (n_kv > 0) mbar_wait(bar_kv, (n_kv - 1) & 1, &no_abort);
-        if (n_qv[0] > 0) mbar_wait(bar_qv0, (n_qv[0] - 1) & 1, &no_abort);
-        if (n_qv[1] > 0) mbar_wait(bar_qv1, (n_qv[1] - 1) & 1, &no_abort);
-        if (n_r > 0) mbar_wait(bar_r, (n_r - 1) & 1, &no_abort);
+        // a phase whose closing copy was not issued yet is closed here, so
+        // that it completes once the copies issued for it have landed
+        if (nx_open0) mbar_arrive(bar_nx0);
+        if (nx_open1) mbar_arrive(bar_nx1);
+        const int ph0 = nx_closed0 + (nx_open0 ? 1 : 0), ph1 = nx_closed1 + (nx_open1 ? 1 : 0);
+        if (ph0 > 0) mbar_wait(bar_nx0, (ph0 - 1) & 1, &no_abort);
+        if (ph1 > 0) mbar_wait(bar_nx1, (ph1 - 1) & 1, &no_abort);
         if (n_do > 0) mbar_wait(bar_do, (n_do - 1) & 1, &no_abort);
-        if (n_qu > 0) mbar_wait(bar_qu, (n_qu - 1) & 1, &no_abort);
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0, &no_abort);
         atomicExch(&g_bwd_error, 1);
@@ -1025,7 +1070,7 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
 
   CUtensorMap tk, tv, tr16, tqu, tqv, tdo, tdq, tdr;
   if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
-      !make_map(&tr16, r16, s.H, s.kv_rows, NB) || !make_map(&tqu, qu, s.B * s.H, s.L, BQ) ||
+      !make_map(&tr16, r16, s.H, s.kv_rows, 128) || !make_map(&tqu, qu, s.B * s.H, s.L, BQ) ||
       !make_map(&tqv, qv, s.B * s.H, s.L, BQ) || !make_map(&tdo, dout, s.B * s.H, s.L, BQ) ||
       !make_map_f32(&tdq, dq_acc, s.B * s.H, s.L) ||
       !make_map_f32(&tdr, dr_acc, s.H, kDrPad + s.kv_rows))

@@ -318,8 +318,10 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // The whole warp runs the schedule (uniform control flow, so that the
     // descriptors stay in uniform registers); one elected thread issues.
     {
-      bool pending[2] = {false, false};
-      int nissued[2] = {0, 0};
+      // per stage: a copy in flight, copies issued (scalars: a runtime-indexed
+      // array would live in local memory)
+      bool pending0 = false, pending1 = false;
+      int nissued0 = 0, nissued1 = 0;
       Cursor<RESET, SPLIT> tc_;  // next tile to load
       tc_.init(p, nitems);
       int g_tma = 0;
@@ -337,8 +339,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           tma_load_3d(sbase + SM_R + s * 32768, &tm_r, 0, tc_.it.i0 - x.jlog0 - (BK - 1), tc_.it.h, bar);
         }
         __syncwarp();
-        pending[s] = true;
-        ++nissued[s];
+        if (s) { pending1 = true; ++nissued1; } else { pending0 = true; ++nissued0; }
         ++g_tma;
         tc_.next(p);
       };
@@ -364,7 +365,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       auto wait_full = [&](int g) {
         const int s = g & 1;
         const bool r = wait(s ? bar_full1 : bar_full0, (g >> 1) & 1);
-        pending[s] = false;
+        if (s) pending1 = false; else pending0 = false;
         return r;
       };
       // the raw Q rows of this CTA's item k (round k of the item order)
@@ -444,8 +445,8 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // shared memory are released
         if (elect_one()) {
           volatile int no_abort = 0;
-          for (int s = 0; s < 2; ++s)
-            if (pending[s]) mbar_wait(s ? bar_full1 : bar_full0, (nissued[s] - 1) & 1, &no_abort);
+          if (pending0) mbar_wait(bar_full0, (nissued0 - 1) & 1, &no_abort);
+          if (pending1) mbar_wait(bar_full1, (nissued1 - 1) & 1, &no_abort);
           if (nq_loads > 0) mbar_wait(bar_q, (nq_loads - 1) & 1, &no_abort);
           mma_commit(bar_drain);
           mbar_wait(bar_drain, 0, &no_abort);
