@@ -326,6 +326,14 @@ def run_ours(args, rank, world):
     kernel_ms = {"rxl_fwd_tc_kernel": kfwd_ms / max(kfwd_n, 1), "rxl_bwd_main_kernel": kbwd_ms / max(kbwd_n, 1)}
     kernel_ms = {k: max_over_ranks(v, world, device="cuda") for k, v in kernel_ms.items()}
 
+    # run-to-run variation of the backward: dQ/dR/du/dv are summed by
+    # hardware reductions in a varying order (dK/dV are reproducible)
+    ref = {n: getattr(c, n).float().clone() for n in ("dq", "dr", "du", "dvb", "dk", "dv")}
+    step()
+    torch.cuda.synchronize()
+    variation = {n: {"max_abs_diff": (getattr(c, n).float() - t).abs().max().item(),
+                     "max_abs": t.abs().max().item()} for n, t in ref.items()}
+
     e2e_value = None
     if not args.no_e2e:
         e2e_run(max(args.warmup, 2))
@@ -361,6 +369,7 @@ def run_ours(args, rank, world):
                                     "pass of the same steps (L2 flushed between steps)",
                      "peak_kind": f"{peak_kind} bf16 burst"},
         "kernels_ms": kernel_ms,
+        "bwd_run_to_run": variation,
         "fwd_kernel_tflops": pairs * FLOP_FWD_PAIR / (kernel_ms["rxl_fwd_tc_kernel"] * 1e-3) / 1e12,
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

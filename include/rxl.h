@@ -120,6 +120,12 @@ size_t rxl_attn_bwd_workspace_bytes(const rxl_attn_desc *desc);
  * do dr rows d >= m+L. k and v are read-only here.
  * workspace: device scratch of at least rxl_attn_bwd_workspace_bytes(desc)
  * bytes (16-byte aligned), owned by the caller; contents on entry ignored.
+ * Range (bf16): the position products run on fp16 operands, so r and
+ * q + vbias must stay within |x| <= 65504; larger elements are clamped and
+ * reported through bit 4 of rxl_device_error_flags().
+ * The fp32 sums over tiles (dq, dr, du, dvbias) are accumulated with
+ * hardware reductions in an order that varies from run to run: results agree
+ * to rounding, not bit for bit (dk, dv and the forward are reproducible).
  */
 rxl_status rxl_attn_bwd(const rxl_attn_desc *desc, const void *q, const void *k, const void *v,
                         const void *r, const void *u, const void *vbias, const void *o,
@@ -335,6 +341,11 @@ int rxl_last_launch_count(void);
  * current device, returns the recorded bits (bit 0: forward kernel, bit 1:
  * backward kernels, bit 2: projection kernel, bit 3: dense-layer kernel) and
  * clears them; -1 if the device could not be read.
+ * Bit 4 is a range report, not a wait timeout: the bf16 backward runs its
+ * position products (dq's r_{i-j} term and dr) on fp16 operands: r, q + vbias
+ * and dA (the latter scaled by a power of two so that it stays in range). An
+ * r or q + vbias element beyond the fp16 range (|x| > 65504) is clamped to
+ * +-65504 and sets bit 4; the gradients of that call are then inexact.
  */
 int rxl_device_error_flags(void);
 

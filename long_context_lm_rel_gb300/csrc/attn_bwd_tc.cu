@@ -63,6 +63,9 @@ constexpr uint32_t IDESC_MN_MN_F16 = idesc_f16(128, 64, true, true);
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ int g_bwd_error;
+// set when an operand converted to fp16 for the position products (R, Q+v)
+// was beyond the fp16 range and clamped (reported, not silent)
+__device__ int g_bwd_range;
 
 struct BwdParams {
   int B, H, L, cap, m, head, nq, kv_rows, nitems;
@@ -848,15 +851,20 @@ __device__ void zero_work(const ZeroArgs &z, size_t tid, size_t stride) {
   for (size_t e = tid; e < z.n_dr / 4; e += stride) ((float4 *)z.dr)[e] = z4;
   for (size_t e = tid; e < z.n_dq / 4; e += stride) ((float4 *)z.dq_acc)[e] = z4;
   for (size_t e = tid; e < (size_t)z.n_sums; e += stride) z.sums[e] = 0.f;
+  float rmax = 0.f;  // largest |R| converted by this thread
   for (size_t e = tid; e < z.n_r / 8; e += stride) {
     const uint4 a = ((const uint4 *)z.r)[e];
     const uint32_t w[4] = {a.x, a.y, a.z, a.w};
     uint32_t o[4];
 #pragma unroll
-    for (int f = 0; f < 4; ++f)
-      o[f] = pack_f16(__uint_as_float(w[f] << 16), __uint_as_float(w[f] & 0xFFFF0000u));
+    for (int f = 0; f < 4; ++f) {
+      const float lo = __uint_as_float(w[f] << 16), hi = __uint_as_float(w[f] & 0xFFFF0000u);
+      rmax = fmax3(rmax, fabsf(lo), fabsf(hi));
+      o[f] = pack_f16(lo, hi);
+    }
     ((uint4 *)z.r16)[e] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  if (__any_sync(0xffffffffu, rmax > 65504.f) && (threadIdx.x & 31) == 0) atomicOr(&g_bwd_range, 1);
   // ring slots whose rows the row does not see: logical slots t < m - mb
   // (masked by a document reset) and t >= m (no valid memory); 8 x 16 B per row
   const size_t n_rows = (size_t)z.BH * z.cap * 8;
@@ -892,6 +900,7 @@ __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
   griddep_wait();
   griddep_launch_dependents();
   const int sub = threadIdx.x & 7;
+  float qvmax = 0.f;  // largest |q + v| converted to fp16 by this thread
   for (long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 3; row < rows;
        row += ((long long)gridDim.x * blockDim.x) >> 3) {
     const int h = (int)((row / L) % H);
@@ -912,15 +921,21 @@ __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       a[e] = pack_bf16(lo(qw[e]) + lo(uw[e]), hi(qw[e]) + hi(uw[e]));
-      b[e] = pack_f16(lo(qw[e]) + lo(vw[e]), hi(qw[e]) + hi(vw[e]));
+      const float v0 = lo(qw[e]) + lo(vw[e]), v1 = hi(qw[e]) + hi(vw[e]);
+      qvmax = fmax3(qvmax, fabsf(v0), fabsf(v1));
+      b[e] = pack_f16(v0, v1);
       acc += lo(dw[e]) * (lo(ow[e]) + lo(lw[e])) + hi(dw[e]) * (hi(ow[e]) + hi(lw[e]));
     }
     ((uint4 *)(qu + off))[sub] = make_uint4(a[0], a[1], a[2], a[3]);
     ((uint4 *)(qv + off))[sub] = make_uint4(b[0], b[1], b[2], b[3]);
+    // the row's 8 lanes (a warp's last rows may leave other groups outside
+    // the loop, so the mask names this group only)
+    const unsigned group = 0xFFu << (threadIdx.x & 24);
 #pragma unroll
-    for (int w = 4; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    for (int w = 4; w > 0; w >>= 1) acc += __shfl_xor_sync(group, acc, w);
     if (sub == 0) delta[row] = acc;
   }
+  if (__any_sync(0xffffffffu, qvmax > 65504.f) && (threadIdx.x & 31) == 0) atomicOr(&g_bwd_range, 1);
   zero_work(z, blockIdx.x * (size_t)blockDim.x + threadIdx.x, (size_t)gridDim.x * blockDim.x);
 }
 
@@ -1140,6 +1155,13 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
                 (unsigned *)(sums + 2 * s.H * DH), du, dvb, (const float *)dr_acc, dr, s.L, s.H, s.kv_rows, chunks);
   ++*launches;
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t tc_bwd_read_range(int *flag) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_bwd_range, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_bwd_range, &zero, sizeof(int));
+  return e;
 }
 
 cudaError_t tc_bwd_read_error(int *flag) {

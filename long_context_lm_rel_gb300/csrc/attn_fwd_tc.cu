@@ -88,6 +88,9 @@ constexpr uint32_t IDESC_G = idesc_bf16(128, 256, false, false);
 constexpr uint32_t IDESC_O = idesc_bf16(128, 64, false, true);   // V is MN-major (d contiguous)
 
 __device__ int g_fwd_error;
+// set when the backward preparation mode converted a (q + v) element beyond
+// the fp16 range (clamped)
+__device__ int g_fwd_range;
 // Testing hook (tc_fwd_test_hooks): non-zero makes the softmax warps withhold
 // their arrival on bar_qready for the CTA's first item.
 __device__ int g_fwd_withhold;
@@ -234,6 +237,7 @@ __device__ __forceinline__ void q_prep(const Params &p, const Item &it, uint32_t
       b[e] = pack_bf16((q0 + v0) * c2, (q1 + v1) * c2);
       a1[e] = pack_bf16(q0 + u0, q1 + u1);
       b1[e] = pack_f16(q0 + v0, q1 + v1);
+      if (MODE == kPrep && fmaxf(fabsf(q0 + v0), fabsf(q1 + v1)) > 65504.f) atomicOr(&g_fwd_range, 1);
     }
     st_shared_v4(sbase + SM_QU + sw128_offset(ii, c), a[0], a[1], a[2], a[3]);
     st_shared_v4(sbase + SM_QV + sw128_offset(ii, c), b[0], b[1], b[2], b[3]);
@@ -845,6 +849,13 @@ cudaError_t tc_fwd_test_hooks(long long wait_cycles, int withhold) {
   const int w = withhold ? 1 : 0;
   cudaError_t e = cudaMemcpyToSymbol(sm103::g_wait_cycles, &cycles, sizeof(cycles));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fwd_withhold, &w, sizeof(w));
+  return e;
+}
+
+cudaError_t tc_fwd_read_range(int *flag) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_fwd_range, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fwd_range, &zero, sizeof(int));
   return e;
 }
 

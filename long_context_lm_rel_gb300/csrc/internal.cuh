@@ -128,6 +128,10 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
                           const void *dout, void *dq, void *dk, void *dv, float *dr, float *du,
                           float *dvb, void *ws, cudaStream_t st, int *launches);
 cudaError_t tc_bwd_read_error(int *flag);
+// Read and clear the fp16 range words (an R or q + v element beyond 65504 in
+// magnitude reached the backward's fp16 position products and was clamped).
+cudaError_t tc_bwd_read_range(int *flag);
+cudaError_t tc_fwd_read_range(int *flag);
 
 // Projection front-end (bf16): q, k, v from the hidden-state memory ring and
 // the current hidden states.

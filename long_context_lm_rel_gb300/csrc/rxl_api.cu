@@ -82,11 +82,12 @@ int rxl_test_forward_wait_timeout(long long wait_cycles, int withhold) {
 }
 
 int rxl_device_error_flags(void) {
-  int fwd = 0, bwd = 0, proj = 0, gemm = 0;
+  int fwd = 0, bwd = 0, proj = 0, gemm = 0, range_b = 0, range_f = 0;
   if (rxl::tc_fwd_read_error(&fwd) != cudaSuccess || rxl::tc_bwd_read_error(&bwd) != cudaSuccess ||
-      rxl::tc_proj_read_error(&proj) != cudaSuccess || rxl::tc_gemm_read_error(&gemm) != cudaSuccess)
+      rxl::tc_proj_read_error(&proj) != cudaSuccess || rxl::tc_gemm_read_error(&gemm) != cudaSuccess ||
+      rxl::tc_bwd_read_range(&range_b) != cudaSuccess || rxl::tc_fwd_read_range(&range_f) != cudaSuccess)
     return -1;
-  return (fwd ? 1 : 0) | (bwd ? 2 : 0) | (proj ? 4 : 0) | (gemm ? 8 : 0);
+  return (fwd ? 1 : 0) | (bwd ? 2 : 0) | (proj ? 4 : 0) | (gemm ? 8 : 0) | ((range_b || range_f) ? 16 : 0);
 }
 
 namespace {

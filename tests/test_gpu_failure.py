@@ -82,3 +82,25 @@ def test_forward_wait_that_runs_out_is_reported_and_the_context_survives():
     o_ref, lse_ref = oracle.fwd(x["q"], k, v, x["r"], x["u"], x["vb"], 0.125)
     assert_close("O", to_host(c.o), o_ref, "bf16")
     assert_close("LSE", to_host(c.lse), lse_ref, "bf16")
+
+
+@pytest.mark.parametrize("where", ["r", "vbias"])
+def test_fp16_range_of_the_position_products_is_reported(where):
+    """The backward's position products take r and q + vbias in fp16: an
+    element beyond 65504 in magnitude is clamped and reported (bit 4 of
+    rxl_device_error_flags), never silently."""
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    lib = rxl.lib()
+    B, H, L, cap, m = 1, 2, 64, 64, 32
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=8)
+    c = run_gpu(x, cap, m, 0, "bf16")
+    torch.cuda.synchronize()
+    assert lib.rxl_device_error_flags() == 0          # in range: nothing reported
+    if where == "r":
+        c.r[1, 5, 3] = 1.0e5                          # a distance row the call reads
+    else:
+        c.vb[0, 7] = -7.0e4
+    c.alloc_bwd(x["do"]).bwd()
+    torch.cuda.synchronize()
+    assert lib.rxl_device_error_flags() == 16
