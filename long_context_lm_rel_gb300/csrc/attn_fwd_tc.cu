@@ -273,8 +273,9 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   const uint32_t bar_drain = b0 + 64;
   const uint32_t bar_x0 = b0 + 72;       // 4 quadrant exchange barriers
   // SPLIT: rank 0's K/V stages are free for rank 1's half (rank 1, count 1);
-  // rank 1's half has landed in them (rank 0, count 256)
-  const uint32_t bar_peer = b0 + 112, bar_data = b0 + 120;
+  // rank 1's half has landed in them (rank 0, count 1 + the copy's bytes);
+  // rank 1's softmax warps staged their part in its own stages (rank 1, 256)
+  const uint32_t bar_peer = b0 + 112, bar_data = b0 + 120, bar_staged = b0 + 136;
   const uint32_t bar_q = b0 + 128;  // TMA: the raw Q rows of the next item
   uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 104);
   volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 108);
@@ -294,7 +295,8 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     if (SPLIT) {
       mbar_init(bar_peer, 1);
-      mbar_init(bar_data, kSoftmaxWarps * 32);
+      mbar_init(bar_data, 1);
+      mbar_init(bar_staged, kSoftmaxWarps * 32);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -639,27 +641,46 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       }
       if (SPLIT) {
         // rank 1 hands its part of the item (O relative to 2^m_row, m_row,
-        // l_row) to rank 0 through distributed shared memory: O rows into
-        // rank 0's K stages ([128][64] fp32, 16-byte chunks swizzled by
-        // row), m and l into its V stage; rank 0 merges the two parts
+        // l_row) to rank 0: it stages the O rows in its own K stages
+        // ([128][64] fp32, 16-byte chunks swizzled by row) and m, l in its V
+        // stage, then one thread moves the 33 KB into the same places of rank
+        // 0 with one bulk copy over distributed shared memory (per-thread
+        // remote stores took 2.1 us at the cfg5 shape); rank 0 merges the two
         const uint32_t orow = ii * 256 + hf * 128;
+        constexpr uint32_t kHandBytes = 32768, kMlBytes = 1024;
         if (blockIdx.x & 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_peer, 0, abort_flag));
-          if (!ok) break;
-          const uint32_t ob = mapa_shared(sbase + SM_K + orow, 0);
+          // this CTA's stages were last read by its final P.V (done above)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            st_cluster_v4(ob + ((c ^ (ii & 7)) << 4), o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            st_shared_v4(sbase + SM_K + orow + ((c ^ (ii & 7)) << 4), o[4 * c], o[4 * c + 1], o[4 * c + 2],
+                         o[4 * c + 3]);
           if (hf == 0) {
-            st_cluster_u32(mapa_shared(sbase + SM_V + 4 * ii, 0), __float_as_uint(m_row));
-            st_cluster_u32(mapa_shared(sbase + SM_V + 512 + 4 * ii, 0), __float_as_uint(l_row));
+            *(volatile float *)(smem + SM_V + 4 * ii) = m_row;
+            *(volatile float *)(smem + SM_V + 512 + 4 * ii) = l_row;
           }
-          mbar_arrive_remote(mapa_shared(bar_data, 0));
+          fence_proxy_async_smem();
+          mbar_arrive(bar_staged);
+          if (warp == 0) {
+            if (lane == 0) {
+              ok = mbar_wait(bar_staged, 0, abort_flag) && mbar_wait_cluster(bar_peer, 0, abort_flag);
+              if (ok) {
+                const uint32_t bar0 = mapa_shared(bar_data, 0);
+                bulk_copy_to_cluster(mapa_shared(sbase + SM_K, 0), sbase + SM_K, kHandBytes, bar0);
+                bulk_copy_to_cluster(mapa_shared(sbase + SM_V, 0), sbase + SM_V, kMlBytes, bar0);
+                bulk_commit();
+                bulk_wait_read();  // the source stays valid until the copy has read it
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          }
           break;  // this CTA's only item is done
         }
         if (it.T >= 2) {  // rank 1 has tiles: its stages were read (P.V done above)
-          if (threadIdx.x == 0) mbar_arrive_remote(mapa_shared(bar_peer, 1));
-          ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_data, 0, abort_flag));
+          if (threadIdx.x == 0) {
+            mbar_expect_tx(bar_data, kHandBytes + kMlBytes);  // the arrival of this phase
+            mbar_arrive_remote(mapa_shared(bar_peer, 1));
+          }
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_data, 0, abort_flag));
           if (!ok) break;
           const float m1 = *(volatile float *)(smem + SM_V + 4 * ii);
           const float l1 = *(volatile float *)(smem + SM_V + 512 + 4 * ii);
