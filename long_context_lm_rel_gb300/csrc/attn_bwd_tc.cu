@@ -202,12 +202,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const uint32_t b0 = sb + F_BAR;
-  // TMA: every operand of pair g but dO ((Q+u), (Q+v), the R band and, for
-  // an item's first pair, K/V) completes one phase of bar_nx0 / bar_nx1 (by
-  // the parity of g), so that the producer waits once per pair for them; dO
-  // of a pair
+  // TMA: (Q+v), the R band and, for an item's first pair, K/V of pair g
+  // complete one phase of bar_nx0 / bar_nx1 (by the parity of g), so that the
+  // producer waits once per pair for them; dO and (Q+u) of a pair
   const uint32_t bar_nx0 = b0 + 8, bar_nx1 = b0 + 16;
-  const uint32_t bar_do = b0 + 32;
+  const uint32_t bar_do = b0 + 32, bar_qu = b0 + 40;
   // MMA commits: S and G; dP; dV; dK and dQc; dQp; dR (the pair's last)
   const uint32_t bar_sg = b0 + 48, bar_dp = b0 + 56, bar_dv = b0 + 64, bar_f0 = b0 + 72;
   const uint32_t bar_dq = b0 + 80, bar_fin = b0 + 88, bar_drain = b0 + 96;
@@ -225,7 +224,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   volatile int *abort_flag = (volatile int *)(smem + F_BAR + 220);
   volatile float *wmax = (volatile float *)(smem + F_BAR + 224);  // [2][8]
   if (threadIdx.x == 0) {
-    mbar_init(bar_nx0, 1); mbar_init(bar_nx1, 1); mbar_init(bar_do, 1);
+    mbar_init(bar_nx0, 1); mbar_init(bar_nx1, 1); mbar_init(bar_do, 1); mbar_init(bar_qu, 1);
     mbar_init(bar_sg, 1); mbar_init(bar_dp, 1); mbar_init(bar_dv, 1); mbar_init(bar_f0, 1);
     mbar_init(bar_dq, 1); mbar_init(bar_fin, 1); mbar_init(bar_drain, 1);
     mbar_init(bar_p, kSoftmaxWarps * 32); mbar_init(bar_da, kSoftmaxWarps * 32);
@@ -261,10 +260,10 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // (Q+v) goes into the other buffer right after this pair's G is issued.
     // The whole warp runs the schedule (uniform control flow, so that the
     // descriptors stay in uniform registers); one elected thread issues.
-    // A phase of bar_nx{b} is opened by the copies issued without arrival
-    // ((Q+v), (Q+u)) and closed by the last one (the R band, with K/V), which
+    // A phase of bar_nx{b} is opened by the copy issued without arrival
+    // ((Q+v)) and closed by the last one (the R band, with K/V), which
     // arrives; the phase then completes when all of its bytes have landed.
-    int n_do = 0, nx_closed0 = 0, nx_closed1 = 0;
+    int n_do = 0, n_qu = 0, nx_closed0 = 0, nx_closed1 = 0;
     bool nx_open0 = false, nx_open1 = false;
     auto wait = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
@@ -277,16 +276,15 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       __syncwarp();
       ++n_do;
     };
-    // pb: the parity of the pair the copy is for
-    auto load_qu = [&](const PairCursor &c, int pb) {
+    auto load_qu = [&](const PairCursor &c) {
       if (elect_one()) {
-        const uint32_t bar = pb ? bar_nx1 : bar_nx0;
-        mbar_expect_tx_noarrive(bar, 16384);
-        tma_load_3d(sb + F_QU, &tm_qu, 0, c.i0(), c.it.bh, bar);
+        mbar_expect_tx(bar_qu, 16384);
+        tma_load_3d(sb + F_QU, &tm_qu, 0, c.i0(), c.it.bh, bar_qu);
       }
       __syncwarp();
-      if (pb) nx_open1 = true; else nx_open0 = true;
+      ++n_qu;
     };
+    // pb: the parity of the pair the copy is for
     auto load_qv = [&](const PairCursor &c, int pb) {
       if (elect_one()) {
         const uint32_t bar = pb ? bar_nx1 : bar_nx0;
@@ -341,10 +339,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     c.init(p);
     if (c.valid) {
       load_qv(c, 0);
-      load_qu(c, 0);
+      load_qu(c);
       load_do(c);
       load_r_kv(c, 0, 0);
     }
+    bool s_issued = false;  // this pair's S product was issued during the previous pair
     for (int g = 0; ok && c.valid; ++g) {
       const bool first = c.n == 0;
       const int buf = g & 1;
@@ -352,16 +351,19 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const uint64_t k_qv = sdesc_add(kb, f_qv), m_qv = sdesc_add(mb0, f_qv);
       PairCursor nx = c;
       nx.next(p);
-      if (!(ok = wait(buf ? bar_nx1 : bar_nx0, (g >> 1) & 1))) break;  // (Q+u), (Q+v), R, K/V
+      if (!(ok = wait(buf ? bar_nx1 : bar_nx0, (g >> 1) & 1))) break;  // (Q+v), R, K/V
+      if (!s_issued && !(ok = wait(bar_qu, g & 1))) break;
       // G's columns hold the previous pair's dQ / dR until it was flushed
       if (g > 0 && !(ok = wait(bar_fl, (g - 1) & 1))) break;
       const uint64_t k_rlo = sdesc_add(k_r, r_lo * 16384), k_rhi = sdesc_add(k_r, (r_lo ^ 1) * 16384);
       const uint64_t m_rlo = sdesc_add(m_r, r_lo * 16384), m_rhi = sdesc_add(m_r, (r_lo ^ 1) * 16384);
       if (elect_one()) {
         tc_fence_after();
+        if (!s_issued) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_S, kdesc(k_qu, k), kdesc(k_k, k), IDESC_S, k > 0);
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + TM_S, kdesc(k_qu, k), kdesc(k_k, k), IDESC_S, k > 0);
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // G columns 0-127 from the lower half, 128-255 from the upper
           mma_bf16(tmem + TM_G, kdesc(k_qv, k), kdesc(k_rlo, k), IDESC_G_F16, k > 0);
@@ -424,7 +426,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       __syncwarp();
       if (nx.valid) {  // (Q+u) is free once dK is done
         if (!(ok = wait(bar_f0, g & 1))) break;
-        load_qu(nx, buf ^ 1);
+        load_qu(nx);
       }
       if (!(ok = wait(bar_ds, g & 1))) break;
       if (elect_one()) {
@@ -435,15 +437,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         mma_commit(bar_dq);
       }
       __syncwarp();
-      if (nx.valid) {
-        // the R band's lower half is free once dQp is done, K and V once dQc
-        // and dP are
-        if (!(ok = wait(bar_dq, g & 1))) break;
-        const int next_lo = nx.n == 0 ? 0 : (r_lo ^ 1);
-        load_r_kv(nx, next_lo, buf ^ 1);
-        r_lo = next_lo;
-      }
       if (elect_one()) {
+        // dR right behind dQp (it does not read the R band): the tensor pipe
+        // runs the two chains back to back
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb)  // dR band = dG^T (Q+v), two 128-distance blocks (fp16)
 #pragma unroll
@@ -453,6 +449,29 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         mma_commit(bar_fin);
       }
       __syncwarp();
+      // the next pair's S, when it is of the same item (same K), into the S
+      // columns (free since dA was formed): only its G is then left between
+      // this pair's flush and the next pair's softmax
+      s_issued = false;
+      if (nx.valid && nx.n != 0) {
+        if (!(ok = wait(bar_qu, (g + 1) & 1))) break;
+        if (elect_one()) {
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + TM_S, kdesc(k_qu, k), kdesc(k_k, k), IDESC_S, k > 0);
+        }
+        __syncwarp();
+        s_issued = true;
+      }
+      if (nx.valid) {
+        // the R band's lower half is free once dQp is done, K and V once dQc
+        // and dP are
+        if (!(ok = wait(bar_dq, g & 1))) break;
+        const int next_lo = nx.n == 0 ? 0 : (r_lo ^ 1);
+        load_r_kv(nx, next_lo, buf ^ 1);
+        r_lo = next_lo;
+      }
       c = nx;
     }
     if (!ok) {
@@ -470,6 +489,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (ph0 > 0) mbar_wait(bar_nx0, (ph0 - 1) & 1, &no_abort);
         if (ph1 > 0) mbar_wait(bar_nx1, (ph1 - 1) & 1, &no_abort);
         if (n_do > 0) mbar_wait(bar_do, (n_do - 1) & 1, &no_abort);
+        if (n_qu > 0) mbar_wait(bar_qu, (n_qu - 1) & 1, &no_abort);
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0, &no_abort);
         atomicExch(&g_bwd_error, 1);
