@@ -79,7 +79,6 @@ constexpr uint32_t SM_X = SM_BAR + 256;        // row-half exchange: [2][2][128]
 constexpr uint32_t SM_QRAW = 199680;           // the next item's Q rows [128][64] bf16 (TMA, sw128)
 constexpr uint32_t SMEM_BYTES = SM_QRAW + 16384 + 1024;  // + alignment slack
 constexpr float kRescaleThreshold = 8.f;       // log2 units
-constexpr uint32_t STAGE_TX = 16384 + 16384 + 32768;
 // O accumulators: keys 0-63 of every tile into TM_O, keys 64-127 into TM_O + 64
 constexpr uint32_t TM_S = 0, TM_G = 128, TM_O = 384, TM_COLS = 512;
 
@@ -263,7 +262,8 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const uint32_t b0 = sbase + SM_BAR;
-  const uint32_t bar_full0 = b0, bar_full1 = b0 + 8;
+  // TMA per stage: K and R of a tile (bar_kr*), its V (bar_v*)
+  const uint32_t bar_kr0 = b0, bar_kr1 = b0 + 8, bar_v0 = b0 + 152, bar_v1 = b0 + 160;
   const uint32_t bar_sg = b0 + 16;       // S/G MMAs of a tile done (commit)
   const uint32_t bar_sgfree = b0 + 24;   // softmax finished reading S/G of a tile (256)
   const uint32_t bar_pr = b0 + 32;       // softmax finished a tile: P written (256)
@@ -277,15 +277,19 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   // rank 1's softmax warps staged their part in its own stages (rank 1, 256)
   const uint32_t bar_peer = b0 + 112, bar_data = b0 + 120, bar_staged = b0 + 136;
   const uint32_t bar_q = b0 + 128;  // TMA: the raw Q rows of the next item
+  const uint32_t bar_gread = b0 + 144;   // softmax finished reading G of a tile (256)
   uint32_t *tmem_slot = (uint32_t *)(smem + SM_BAR + 104);
   volatile int *abort_flag = (volatile int *)(smem + SM_BAR + 108);
   volatile float *xbuf = (volatile float *)(smem + SM_X);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_full0, 1);
-    mbar_init(bar_full1, 1);
+    mbar_init(bar_kr0, 1);
+    mbar_init(bar_kr1, 1);
+    mbar_init(bar_v0, 1);
+    mbar_init(bar_v1, 1);
     mbar_init(bar_sg, 1);
     mbar_init(bar_sgfree, kSoftmaxWarps * 32);
+    mbar_init(bar_gread, kSoftmaxWarps * 32);
     mbar_init(bar_pr, kSoftmaxWarps * 32);
     mbar_init(bar_pv, 1);
     mbar_init(bar_qready, kSoftmaxWarps * 32);
@@ -323,57 +327,76 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // ------------------------------------------------ producer / MMA issuer
     // The whole warp runs the schedule (uniform control flow, so that the
     // descriptors stay in uniform registers); one elected thread issues.
+    // Stage s of tile g = g & 1 holds its K and R (bar_kr{s}) and its V
+    // (bar_v{s}): K and R are reloaded for tile g+2 as soon as the S/G
+    // products of tile g are done, V once its P.V is, so each copy has about
+    // two tiles of lead.
     {
-      // per stage: a copy in flight, copies issued (scalars: a runtime-indexed
-      // array would live in local memory)
-      bool pending0 = false, pending1 = false;
-      int nissued0 = 0, nissued1 = 0;
-      Cursor<RESET, SPLIT> tc_;  // next tile to load
-      tc_.init(p, nitems);
-      int g_tma = 0;
+      int n_kr0 = 0, n_kr1 = 0, n_v0 = 0, n_v1 = 0;  // copies issued per barrier
+      Cursor<RESET, SPLIT> kc, vc;  // next tile whose K/R, whose V to load
+      kc.init(p, nitems);
+      vc.init(p, nitems);
+      int g_kr = 0, g_v = 0;
       auto wait = [&](uint32_t bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
       };
-      auto issue_tma = [&]() {
-        const int s = g_tma & 1;
-        const KeyTile x = KeyTiles(tc_.it.m, p.cap, tc_.it.head, min(tc_.it.i0 + BQ, p.L)).get(tc_.t);
+      auto issue_kr = [&]() {
+        const int s = g_kr & 1;
+        const KeyTile x = KeyTiles(kc.it.m, p.cap, kc.it.head, min(kc.it.i0 + BQ, p.L)).get(kc.t);
         if (elect_one()) {
-          const uint32_t bar = s ? bar_full1 : bar_full0;
-          mbar_expect_tx(bar, STAGE_TX);
-          tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, tc_.it.bh, bar);
-          tma_load_3d(sbase + SM_V + s * 16384, &tm_v, 0, x.phys0, tc_.it.bh, bar);
-          tma_load_3d(sbase + SM_R + s * 32768, &tm_r, 0, tc_.it.i0 - x.jlog0 - (BK - 1), tc_.it.h, bar);
+          const uint32_t bar = s ? bar_kr1 : bar_kr0;
+          mbar_expect_tx(bar, 16384 + 32768);
+          tma_load_3d(sbase + SM_K + s * 16384, &tm_k, 0, x.phys0, kc.it.bh, bar);
+          tma_load_3d(sbase + SM_R + s * 32768, &tm_r, 0, kc.it.i0 - x.jlog0 - (BK - 1), kc.it.h, bar);
         }
         __syncwarp();
-        if (s) { pending1 = true; ++nissued1; } else { pending0 = true; ++nissued0; }
-        ++g_tma;
-        tc_.next(p);
+        if (s) ++n_kr1; else ++n_kr0;
+        ++g_kr;
+        kc.next(p);
+      };
+      auto issue_v = [&]() {
+        const int s = g_v & 1;
+        const KeyTile x = KeyTiles(vc.it.m, p.cap, vc.it.head, min(vc.it.i0 + BQ, p.L)).get(vc.t);
+        if (elect_one()) {
+          const uint32_t bar = s ? bar_v1 : bar_v0;
+          mbar_expect_tx(bar, 16384);
+          tma_load_3d(sbase + SM_V + s * 16384, &tm_v, 0, x.phys0, vc.it.bh, bar);
+        }
+        __syncwarp();
+        if (s) ++n_v1; else ++n_v0;
+        ++g_v;
+        vc.next(p);
       };
       // operand descriptors, built once; a k-step or a stage is an add
       const uint64_t d_qu = sdesc_sw128(sbase + SM_QU, 16, 1024), d_qv = sdesc_sw128(sbase + SM_QV, 16, 1024);
       const uint64_t d_k = sdesc_sw128(sbase + SM_K, 16, 1024), d_r = sdesc_sw128(sbase + SM_R, 16, 1024);
       const uint64_t d_p = sdesc_sw128(sbase + SM_P, 16, 1024), d_v = sdesc_sw128(sbase + SM_V, 16, 1024);
-      auto issue_sg = [&](int g) {
-        const int s = g & 1;
-        const uint64_t dk_s = sdesc_add(d_k, s * 16384), dr_s = sdesc_add(d_r, s * 32768);
+      // G of a tile (two thirds of its S/G work) goes as soon as the softmax
+      // has read the previous tile's G, while it still skews it; S once it
+      // has read S; one commit covers both
+      auto issue_g = [&](int g) {
+        const uint64_t dr_s = sdesc_add(d_r, (g & 1) * 32768);
+        if (elect_one()) {
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + TM_G, sdesc_add(d_qv, k * 32), sdesc_add(dr_s, k * 32), IDESC_G, k > 0);
+        }
+        __syncwarp();
+      };
+      auto issue_s_commit = [&](int g) {
+        const uint64_t dk_s = sdesc_add(d_k, (g & 1) * 16384);
         if (elect_one()) {
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_bf16(tmem + TM_S, sdesc_add(d_qu, k * 32), sdesc_add(dk_s, k * 32), IDESC_S, k > 0);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + TM_G, sdesc_add(d_qv, k * 32), sdesc_add(dr_s, k * 32), IDESC_G, k > 0);
           mma_commit(bar_sg);
         }
         __syncwarp();
       };
-      auto wait_full = [&](int g) {
-        const int s = g & 1;
-        const bool r = wait(s ? bar_full1 : bar_full0, (g >> 1) & 1);
-        if (s) pending1 = false; else pending0 = false;
-        return r;
-      };
+      auto wait_kr = [&](int g) { return wait((g & 1) ? bar_kr1 : bar_kr0, (g >> 1) & 1); };
+      auto wait_v = [&](int g) { return wait((g & 1) ? bar_v1 : bar_v0, (g >> 1) & 1); };
       // the raw Q rows of this CTA's item k (round k of the item order)
       int nq_loads = 0;
       auto load_q = [&](int k) {
@@ -398,13 +421,17 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       Cursor<RESET, SPLIT> mc;  // tile whose P.V is next
       mc.init(p, nitems);
       if (mc.valid) load_q(0);
-      if (tc_.valid) issue_tma();
-      if (tc_.valid) issue_tma();
+      for (int t = 0; t < 2 && kc.valid; ++t) {
+        issue_kr();
+        issue_v();
+      }
+      // later V copies: the one of tile g+1 during tile g (g >= 1)
       if (mc.valid) {
-        ok = wait(bar_qready, 0) && wait_full(0);
+        ok = wait(bar_qready, 0) && wait_kr(0);
         if (ok) {
           load_q(1);  // the softmax has read item 0's raw rows
-          issue_sg(0);
+          issue_g(0);
+          issue_s_commit(0);
         }
       }
       for (int g = 0; ok && mc.valid; ++g) {
@@ -414,10 +441,22 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // S/G of tile g+1 as soon as the softmax released S/G of tile g
         // (same item: the Q tiles are unchanged)
         if (nx.valid && !new_item) {
-          if (!(ok = wait(bar_sgfree, g & 1) && wait_full(g + 1))) break;
-          issue_sg(g + 1);
+          if (!(ok = wait(bar_gread, g & 1) && wait_kr(g + 1))) break;
+          issue_g(g + 1);
         }
-        if (!(ok = wait(bar_pr, g & 1))) break;
+        if (g > 0 && vc.valid) {
+          // the V stage of tile g-1 is free once its P.V completed: tile g+1
+          if (!(ok = wait(bar_pv, (g - 1) & 1))) break;
+          issue_v();
+        }
+        if (nx.valid && !new_item) {
+          if (!(ok = wait(bar_sgfree, g & 1))) break;
+          issue_s_commit(g + 1);
+          // the S/G products of tile g are done (the softmax has read them):
+          // its K and R stage takes tile g+2
+          if (kc.valid) issue_kr();
+        }
+        if (!(ok = wait(bar_pr, g & 1) && wait_v(g))) break;
         // the first P.V of an item overwrites O: its epilogue must have read it
         if (mc.t == mc.t0 && mc.k > 0 && !(ok = wait(bar_ofree, (mc.k - 1) & 1))) break;
         const int s = g & 1;
@@ -435,24 +474,24 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (new_item) {
           // next item: its Q tiles are written once the softmax finished
           // this item's last tile
-          if (!(ok = wait(bar_sgfree, g & 1) && wait(bar_qready, nx.k & 1) && wait_full(g + 1))) break;
+          if (!(ok = wait(bar_sgfree, g & 1) && wait(bar_qready, nx.k & 1) && wait_kr(g + 1))) break;
           load_q(nx.k + 1);  // the softmax has read item nx.k's raw rows
-          issue_sg(g + 1);
-        }
-        if (tc_.valid) {
-          // stage g&1 is free once P.V(g) (and with it S/G(g)) completed
-          if (!(ok = wait(bar_pv, g & 1))) break;
-          issue_tma();
+          issue_g(g + 1);
+          issue_s_commit(g + 1);
+          if (kc.valid) issue_kr();  // tile g's S/G are done (read by the softmax)
         }
         mc = nx;
       }
       if (!ok) {
         // wind down: let in-flight copies and MMAs land before TMEM and
-        // shared memory are released
+        // shared memory are released (the latest copy of each barrier; an
+        // earlier one completed before it, and a completed phase returns at once)
         if (elect_one()) {
           volatile int no_abort = 0;
-          if (pending0) mbar_wait(bar_full0, (nissued0 - 1) & 1, &no_abort);
-          if (pending1) mbar_wait(bar_full1, (nissued1 - 1) & 1, &no_abort);
+          if (n_kr0 > 0) mbar_wait(bar_kr0, (n_kr0 - 1) & 1, &no_abort);
+          if (n_kr1 > 0) mbar_wait(bar_kr1, (n_kr1 - 1) & 1, &no_abort);
+          if (n_v0 > 0) mbar_wait(bar_v0, (n_v0 - 1) & 1, &no_abort);
+          if (n_v1 > 0) mbar_wait(bar_v1, (n_v1 - 1) & 1, &no_abort);
           if (nq_loads > 0) mbar_wait(bar_q, (nq_loads - 1) & 1, &no_abort);
           mma_commit(bar_drain);
           mbar_wait(bar_drain, 0, &no_abort);
@@ -489,8 +528,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       const int t = cur.t, t0 = cur.t0, t1 = cur.t1;
       const int i = it.i0 + ii;
       const int s = g & 1;
-      ok = mbar_wait(bar_sg, g & 1, abort_flag) &&
-           mbar_wait(s ? bar_full1 : bar_full0, (g >> 1) & 1, abort_flag);
+      ok = mbar_wait(bar_sg, g & 1, abort_flag);
       // tcgen05.ld/st below are warp-collective: keep every decision warp-uniform
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
@@ -509,6 +547,9 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           tmem_ld32(trow + gcol + 32, w1);
           tmem_ld32(trow + gcol + 64, w2);
           tmem_wait_ld();
+          // done reading G: the next tile's G products may start
+          tc_fence_before();
+          mbar_arrive(bar_gread);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             win[e] = __uint_as_float(w0[e]);
@@ -521,7 +562,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         tmem_ld32(trow + TM_S + 64 * hf, s0);
         tmem_ld32(trow + TM_S + 64 * hf + 32, s1);
         tmem_wait_ld();
-        // done reading S and G: the next tile's S/G MMAs may start
+        // done reading S: the next tile's S products may start
         tc_fence_before();
         mbar_arrive(bar_sgfree);
 #pragma unroll
@@ -581,7 +622,11 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         st_shared_v4(sw128_at(row_p, c), pk[4 * c], pk[4 * c + 1],
                      pk[4 * c + 2], pk[4 * c + 3]);
       // rows of V past the run hold another run's (or junk) data: zero them
-      // so that 0 * junk cannot leak into O
+      // so that 0 * junk cannot leak into O (once the tile's V has landed)
+      if (x.nvalid < BK) {
+        ok = __all_sync(0xffffffffu, mbar_wait(s ? bar_v1 : bar_v0, (g >> 1) & 1, abort_flag));
+        if (!ok) break;
+      }
       if (ii >= x.nvalid) {
         const uint32_t vrow = sbase + SM_V + s * 16384 + ii * 128;
 #pragma unroll
