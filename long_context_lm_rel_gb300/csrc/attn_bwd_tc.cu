@@ -977,27 +977,14 @@ __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(
   const int sub = threadIdx.x & 7, slot = threadIdx.x >> 3;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   const int r_end = min(L, (ch + 1) * 128);
-  // the chunk's 4 rows of this thread: all loads first (8 x 16 B in flight)
-  float4 a[4], b[4];
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int i = ch * 128 + slot + 32 * t;
-    if (i < r_end) {
-      const size_t off = ((size_t)bh * L + i) * DH + 8 * sub;
-      a[t] = __ldcs((const float4 *)(dq_acc + off));
-      b[t] = __ldcs((const float4 *)(dq_acc + off + 4));
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int i = ch * 128 + slot + 32 * t;
-    if (i < r_end) {
-      const size_t off = ((size_t)bh * L + i) * DH + 8 * sub;
-      acc[0] += a[t].x; acc[1] += a[t].y; acc[2] += a[t].z; acc[3] += a[t].w;
-      acc[4] += b[t].x; acc[5] += b[t].y; acc[6] += b[t].z; acc[7] += b[t].w;
-      *(uint4 *)(dq + off) = make_uint4(pack_bf16(a[t].x, a[t].y), pack_bf16(a[t].z, a[t].w),
-                                        pack_bf16(b[t].x, b[t].y), pack_bf16(b[t].z, b[t].w));
-    }
+  for (int i = ch * 128 + slot; i < r_end; i += 32) {
+    const size_t off = ((size_t)bh * L + i) * DH + 8 * sub;
+    const float4 a = *(const float4 *)(dq_acc + off);
+    const float4 b = *(const float4 *)(dq_acc + off + 4);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    *(uint4 *)(dq + off) = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
+                                      pack_bf16(b.z, b.w));
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) part[slot][8 * sub + e] = acc[e];
