@@ -115,10 +115,11 @@ __device__ __forceinline__ bool pair_sync(uint32_t bar, int lane, uint32_t &phas
 // ------------------------------------------------------------ main kernel
 
 // Shared memory: K, V, (Q+u), two (Q+v) buffers (the next pair's rows load
-// while the current pair still reads its own), dO, the 256-row R band, P/dA
-// (bf16, then the pair's dQ staging), dG (fp16, then its dR staging), barriers.
-constexpr uint32_t F_K = 0, F_V = 16384, F_QU = 32768, F_QV0 = 49152, F_QV1 = 65536, F_DO = 81920;
-constexpr uint32_t F_R = 98304, F_PA = 131072, F_DG = 163840, F_BAR = 229376;
+// while the current pair still reads its own), three 16 KB slots that hold
+// dO and the two 128-row halves of the R band in turn, P/dA (bf16, then the
+// pair's dQ staging), dG (fp16, then its dR staging), barriers.
+constexpr uint32_t F_K = 0, F_V = 16384, F_QU = 32768, F_QV0 = 49152, F_QV1 = 65536, F_SLOT = 81920;
+constexpr uint32_t F_PA = 131072, F_DG = 163840, F_BAR = 229376;
 constexpr uint32_t F_SMEM = F_BAR + 512 + 1024;
 // TMEM columns: dV, dK accumulators; S (then dP); G (then dQc, dQp, dR blocks)
 constexpr uint32_t TM_DV = 0, TM_DK = 64, TM_S = 128, TM_G = 256;
@@ -195,6 +196,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const __grid_constant__ CUtensorMap tm_r16, const __grid_constant__ CUtensorMap tm_qu,
                     const __grid_constant__ CUtensorMap tm_qv16, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dr,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -220,6 +222,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const uint32_t bar_str = b0 + 192;     // each softmax warp staged its dR rows (8)
   const uint32_t bar_sfree = b0 + 200;   // the dQ staging has been read (1)
   const uint32_t bar_gfree = b0 + 208;   // the dR staging has been read (1)
+  const uint32_t bar_sread = b0 + 288;   // each softmax warp read its S / G columns (8)
+  const uint32_t bar_rlo = b0 + 296;     // MMA commit: dQp's products with the band's lower half
   uint32_t *tmem_slot = (uint32_t *)(smem + F_BAR + 216);
   volatile int *abort_flag = (volatile int *)(smem + F_BAR + 220);
   volatile float *wmax = (volatile float *)(smem + F_BAR + 224);  // [2][8]
@@ -233,7 +237,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     mbar_init(bar_red, kSoftmaxWarps);
     for (int q = 0; q < 4; ++q) mbar_init(bar_x0 + 8 * q, 2);
     mbar_init(bar_stq, kSoftmaxWarps); mbar_init(bar_str, kSoftmaxWarps);
-    mbar_init(bar_sfree, 1); mbar_init(bar_gfree, 1);
+    mbar_init(bar_sfree, 1); mbar_init(bar_gfree, 1); mbar_init(bar_sread, kSoftmaxWarps);
+    mbar_init(bar_rlo, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -243,6 +248,7 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v); tma_prefetch_desc(&tm_r16);
       tma_prefetch_desc(&tm_qu); tma_prefetch_desc(&tm_qv16); tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_dq); tma_prefetch_desc(&tm_dr);
+      tma_prefetch_desc(&tm_dk); tma_prefetch_desc(&tm_dv);
     }
   }
   tc_fence_before();
@@ -255,9 +261,12 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   if (warp == kProducerWarp) {
     // ------------------------------------------------ producer / MMA issuer
     // Pair g reads (Q+v) buffer g & 1. Each operand is reloaded as soon as
-    // its last reader of the previous pair is done: dO after dV, (Q+u) after
-    // dK, the R band after dQp, K/V of a new item after dQc; the next pair's
-    // (Q+v) goes into the other buffer right after this pair's G is issued.
+    // its last reader of the previous pair is done: (Q+u), and K and V of a
+    // new item, once dK and dQc are; dO and the R band by the slot rotation
+    // below; the next pair's (Q+v) goes into the other buffer right after
+    // this pair's G is issued. So the next pair's S is issued right behind
+    // this pair's dR, for a new item too, and the tensor pipe does not idle
+    // between items.
     // The whole warp runs the schedule (uniform control flow, so that the
     // descriptors stay in uniform registers); one elected thread issues.
     // A phase of bar_nx{b} is opened by the copy issued without arrival
@@ -268,80 +277,79 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     auto wait = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
     };
-    auto load_do = [&](const PairCursor &c) {
+    // The R band of a pair is two 128-row halves (distances d0 .. d0+127 and
+    // d0+128 .. d0+255). The next query tile of the same item needs
+    // d0+128 .. d0+383: its lower half is this pair's upper half, already
+    // resident. Three slots rotate among dO and the two halves, each refilled
+    // as soon as its last reader is done: dO's once dV is done, the lower
+    // half's once dQp's products with it are, the upper half's once dQp is.
+    //   same item: next upper half -> dO's slot, next dO -> lower half's
+    //   new item : next lower half -> dO's slot, next upper half -> lower
+    //              half's, next dO -> upper half's
+    // s_lo, s_hi, s_do: slot of each operand.
+    int s_do = 0, s_lo = 1, s_hi = 2;
+    auto slot = [](int k) { return F_SLOT + (uint32_t)k * 16384u; };
+    auto load_do = [&](const PairCursor &c, int k) {
       if (elect_one()) {
         mbar_expect_tx(bar_do, 16384);
-        tma_load_3d(sb + F_DO, &tm_do, 0, c.i0(), c.it.bh, bar_do);
+        tma_load_3d(sb + slot(k), &tm_do, 0, c.i0(), c.it.bh, bar_do);
       }
       __syncwarp();
       ++n_do;
     };
+    // (Q+u) of a pair, with K for the first pair of an item (S reads both)
     auto load_qu = [&](const PairCursor &c) {
+      const bool with_k = c.n == 0;
       if (elect_one()) {
-        mbar_expect_tx(bar_qu, 16384);
+        mbar_expect_tx(bar_qu, with_k ? 2 * 16384 : 16384);
         tma_load_3d(sb + F_QU, &tm_qu, 0, c.i0(), c.it.bh, bar_qu);
+        if (with_k) tma_load_3d(sb + F_K, &tm_k, 0, c.it.x.phys0, c.it.bh, bar_qu);
       }
       __syncwarp();
       ++n_qu;
     };
-    // pb: the parity of the pair the copy is for
-    auto load_qv = [&](const PairCursor &c, int pb) {
+    // one 16 KB tile into the phase of bar_nx{pb} (pb: the parity of the
+    // pair it is for); the phase's last copy closes it (arrives)
+    auto load_nx = [&](uint32_t dst, const CUtensorMap *tm, int y, int z, int pb, bool close) {
       if (elect_one()) {
         const uint32_t bar = pb ? bar_nx1 : bar_nx0;
-        mbar_expect_tx_noarrive(bar, 16384);
-        tma_load_3d(sb + (pb ? F_QV1 : F_QV0), &tm_qv16, 0, c.i0(), c.it.bh, bar);
-      }
-      __syncwarp();
-      if (pb) nx_open1 = true; else nx_open0 = true;
-    };
-    // The R band of a pair is two 128-row halves (distances d0 .. d0+127 and
-    // d0+128 .. d0+255) in two 16 KB slots. The next query tile of the same
-    // item needs d0+128 .. d0+383: its lower half is this pair's upper half,
-    // already resident, so only its upper half is loaded, into the slot of
-    // this pair's lower half. r_lo: the slot holding the lower half.
-    int r_lo = 0;
-    auto load_r_kv = [&](const PairCursor &c, int next_lo, int pb) {
-      const FItem &it = c.it;
-      const int d0 = c.i0() - it.x.jlog0 - (BK - 1);
-      if (elect_one()) {
-        const uint32_t bar = pb ? bar_nx1 : bar_nx0;
-        if (c.n == 0) {
-          mbar_expect_tx(bar, 4 * 16384);
-          tma_load_3d(sb + F_K, &tm_k, 0, it.x.phys0, it.bh, bar);
-          tma_load_3d(sb + F_V, &tm_v, 0, it.x.phys0, it.bh, bar);
-          tma_load_3d(sb + F_R, &tm_r16, 0, d0, it.h, bar);
-          tma_load_3d(sb + F_R + 16384, &tm_r16, 0, d0 + 128, it.h, bar);
-        } else {
+        if (close)
           mbar_expect_tx(bar, 16384);
-          tma_load_3d(sb + F_R + (next_lo ^ 1) * 16384, &tm_r16, 0, d0 + 128, it.h, bar);
-        }
+        else
+          mbar_expect_tx_noarrive(bar, 16384);
+        tma_load_3d(dst, tm, 0, y, z, bar);
       }
       __syncwarp();
-      if (pb) {
-        nx_open1 = false;
-        ++nx_closed1;
+      bool &open = pb ? nx_open1 : nx_open0;
+      if (close) {
+        open = false;
+        ++(pb ? nx_closed1 : nx_closed0);
       } else {
-        nx_open0 = false;
-        ++nx_closed0;
+        open = true;
       }
     };
+    auto load_qv = [&](const PairCursor &c, int pb) {
+      load_nx(sb + (pb ? F_QV1 : F_QV0), &tm_qv16, c.i0(), c.it.bh, pb, false);
+    };
+    auto band0 = [](const PairCursor &c) { return c.i0() - c.it.x.jlog0 - (BK - 1); };
     // operand descriptors: two bases built once (K-major and MN-major
     // layouts at the start of shared memory); a tile, k-step or buffer is
     // a constant added to them
     const uint64_t kb = kdesc0(sb), mb0 = mndesc0(sb);
-    const uint64_t k_qu = sdesc_add(kb, F_QU), k_k = sdesc_add(kb, F_K), k_do = sdesc_add(kb, F_DO);
-    const uint64_t k_v = sdesc_add(kb, F_V), k_r = sdesc_add(kb, F_R), k_pa = sdesc_add(kb, F_PA);
-    const uint64_t k_dg = sdesc_add(kb, F_DG);
-    const uint64_t m_pa = sdesc_add(mb0, F_PA), m_do = sdesc_add(mb0, F_DO), m_qu = sdesc_add(mb0, F_QU);
-    const uint64_t m_k = sdesc_add(mb0, F_K), m_r = sdesc_add(mb0, F_R), m_dg = sdesc_add(mb0, F_DG);
+    const uint64_t k_qu = sdesc_add(kb, F_QU), k_k = sdesc_add(kb, F_K), k_slot = sdesc_add(kb, F_SLOT);
+    const uint64_t k_v = sdesc_add(kb, F_V), k_pa = sdesc_add(kb, F_PA), k_dg = sdesc_add(kb, F_DG);
+    const uint64_t m_pa = sdesc_add(mb0, F_PA), m_slot = sdesc_add(mb0, F_SLOT), m_qu = sdesc_add(mb0, F_QU);
+    const uint64_t m_k = sdesc_add(mb0, F_K), m_dg = sdesc_add(mb0, F_DG);
     bool ok = true;
     PairCursor c;
     c.init(p);
     if (c.valid) {
       load_qv(c, 0);
       load_qu(c);
-      load_do(c);
-      load_r_kv(c, 0, 0);
+      load_do(c, s_do);
+      load_nx(sb + F_V, &tm_v, c.it.x.phys0, c.it.bh, 0, false);
+      load_nx(sb + slot(s_lo), &tm_r16, band0(c), c.it.h, 0, false);
+      load_nx(sb + slot(s_hi), &tm_r16, band0(c) + 128, c.it.h, 0, true);
     }
     bool s_issued = false;  // this pair's S product was issued during the previous pair
     for (int g = 0; ok && c.valid; ++g) {
@@ -351,12 +359,13 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const uint64_t k_qv = sdesc_add(kb, f_qv), m_qv = sdesc_add(mb0, f_qv);
       PairCursor nx = c;
       nx.next(p);
-      if (!(ok = wait(buf ? bar_nx1 : bar_nx0, (g >> 1) & 1))) break;  // (Q+v), R, K/V
+      if (!(ok = wait(buf ? bar_nx1 : bar_nx0, (g >> 1) & 1))) break;  // (Q+v), R, V
       if (!s_issued && !(ok = wait(bar_qu, g & 1))) break;
       // G's columns hold the previous pair's dQ / dR until it was flushed
       if (g > 0 && !(ok = wait(bar_fl, (g - 1) & 1))) break;
-      const uint64_t k_rlo = sdesc_add(k_r, r_lo * 16384), k_rhi = sdesc_add(k_r, (r_lo ^ 1) * 16384);
-      const uint64_t m_rlo = sdesc_add(m_r, r_lo * 16384), m_rhi = sdesc_add(m_r, (r_lo ^ 1) * 16384);
+      const uint64_t k_rlo = sdesc_add(k_slot, s_lo * 16384), k_rhi = sdesc_add(k_slot, s_hi * 16384);
+      const uint64_t m_rlo = sdesc_add(m_slot, s_lo * 16384), m_rhi = sdesc_add(m_slot, s_hi * 16384);
+      const uint64_t k_do = sdesc_add(k_slot, s_do * 16384), m_do = sdesc_add(m_slot, s_do * 16384);
       if (elect_one()) {
         tc_fence_after();
         if (!s_issued) {
@@ -389,10 +398,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
       }
       __syncwarp();
-      if (!(ok = wait(bar_p, g & 1))) break;
-      // the first dV of an item overwrites the accumulators: the previous
-      // item's epilogue must have read them
-      if (first && c.k > 0 && !(ok = wait(bar_acc, (c.k - 1) & 1))) break;
+      // dP into the S columns as soon as the softmax warps have read S: it
+      // runs while they form P
+      if (!(ok = wait(bar_sread, g & 1))) break;
       if (!(ok = wait(bar_do, g & 1))) break;
       if (elect_one()) {
         tc_fence_after();
@@ -400,15 +408,26 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int k = 0; k < 4; ++k)
           mma_bf16(tmem + TM_S, kdesc(k_do, k), kdesc(k_v, k), IDESC_S, k > 0);
         mma_commit(bar_dp);  // dA needs only dP
+      }
+      __syncwarp();
+      if (!(ok = wait(bar_p, g & 1))) break;
+      // the first dV of an item overwrites the accumulators: the previous
+      // item's epilogue must have read them
+      if (first && c.k > 0 && !(ok = wait(bar_acc, (c.k - 1) & 1))) break;
+      if (elect_one()) {
+        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // dV += P^T dO
           mma_bf16(tmem + TM_DV, mndesc(m_pa, k), mndesc(m_do, k), IDESC_MN_MN, (!first || k > 0) ? 1u : 0u);
         mma_commit(bar_dv);
       }
       __syncwarp();
-      if (nx.valid) {  // dO is free once dP and dV are done
+      // dO's slot is free once dP and dV are done: the next pair's upper
+      // half (same item; the last copy of its phase) or lower half (new item)
+      const bool same = nx.valid && nx.n != 0;
+      if (nx.valid) {
         if (!(ok = wait(bar_dv, g & 1))) break;
-        load_do(nx);
+        load_nx(sb + slot(s_do), &tm_r16, band0(nx) + (same ? 128 : 0), nx.it.h, buf ^ 1, same);
       }
       // dK and dQc as soon as dA is written, while the softmax warps
       // shear dG; then dQp and the dR blocks
@@ -424,16 +443,21 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         mma_commit(bar_f0);
       }
       __syncwarp();
-      if (nx.valid) {  // (Q+u) is free once dK is done
+      if (nx.valid) {  // (Q+u), K and V are free once dK and dQc are done
         if (!(ok = wait(bar_f0, g & 1))) break;
         load_qu(nx);
+        if (!same) load_nx(sb + F_V, &tm_v, nx.it.x.phys0, nx.it.bh, buf ^ 1, false);
       }
       if (!(ok = wait(bar_ds, g & 1))) break;
       if (elect_one()) {
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 16; ++k)  // dQp = dG Rband (fp16), band rows 16k .. 16k+15
-          mma_bf16(tmem + TM_QP, kdesc(k_dg, k), mndesc(k < 8 ? m_rlo : m_rhi, k & 7), IDESC_K_MN_F16, k > 0);
+        for (int k = 0; k < 8; ++k)  // dQp = dG Rband (fp16), band rows 16k .. 16k+15: lower half
+          mma_bf16(tmem + TM_QP, kdesc(k_dg, k), mndesc(m_rlo, k), IDESC_K_MN_F16, k > 0);
+        mma_commit(bar_rlo);
+#pragma unroll
+        for (int k = 8; k < 16; ++k)  // upper half
+          mma_bf16(tmem + TM_QP, kdesc(k_dg, k), mndesc(m_rhi, k & 7), IDESC_K_MN_F16, 1u);
         mma_commit(bar_dq);
       }
       __syncwarp();
@@ -449,11 +473,26 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         mma_commit(bar_fin);
       }
       __syncwarp();
-      // the next pair's S, when it is of the same item (same K), into the S
-      // columns (free since dA was formed): only its G is then left between
-      // this pair's flush and the next pair's softmax
+      // the lower half's slot is free once dQp's products with it are done
+      // (and with them every earlier product of the pair): the next dO (same
+      // item) or the next upper half (new item; the last copy of its phase)
+      if (nx.valid) {
+        if (!(ok = wait(bar_rlo, g & 1))) break;
+        if (same) {
+          load_do(nx, s_lo);
+          const int t = s_lo;
+          s_lo = s_hi;
+          s_hi = s_do;
+          s_do = t;
+        } else {
+          load_nx(sb + slot(s_lo), &tm_r16, band0(nx) + 128, nx.it.h, buf ^ 1, true);
+        }
+      }
+      // the next pair's S into the S columns (free since dA was formed):
+      // only its G is then left between this pair's flush and the next
+      // pair's softmax
       s_issued = false;
-      if (nx.valid && nx.n != 0) {
+      if (nx.valid) {
         if (!(ok = wait(bar_qu, (g + 1) & 1))) break;
         if (elect_one()) {
           tc_fence_after();
@@ -464,13 +503,14 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         __syncwarp();
         s_issued = true;
       }
-      if (nx.valid) {
-        // the R band's lower half is free once dQp is done, K and V once dQc
-        // and dP are
+      if (nx.valid && !same) {
+        // new item: the next dO into the upper half's slot once dQp is done
         if (!(ok = wait(bar_dq, g & 1))) break;
-        const int next_lo = nx.n == 0 ? 0 : (r_lo ^ 1);
-        load_r_kv(nx, next_lo, buf ^ 1);
-        r_lo = next_lo;
+        load_do(nx, s_hi);
+        const int t = s_lo;
+        s_lo = s_do;
+        s_do = s_hi;
+        s_hi = t;
       }
       c = nx;
     }
@@ -585,13 +625,21 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
       float y[64];
       half_tile_exponents(trow, TM_S, TM_G, quad, lane, hf, i, it.x, p.scale_log2, log2_scale - lse2, y);
+      // S is read: dP may take its columns (and read the zeroed V rows)
+      if (c.n == 0 && it.x.nvalid < BK) fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sread);
 #pragma unroll
       for (int k = 0; k < 64; ++k) y[k] = ex2(y[k]);  // scale * P
-      // the P/dA buffer held the previous pair's dQ staging
+      // the P/dA buffer held the previous pair's dQ staging (and, after an
+      // item's last pair, this warp's dK or dV rows on their way out)
       if (g > 0) {
         ok = mbar_wait(bar_sfree, (g - 1) & 1, abort_flag);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
       }
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
       store_half_bf16(row_pa, y);
       fence_proxy_async_smem();
       tc_fence_before();
@@ -808,36 +856,60 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
       c.next(p);
       if (c.valid && c.n != 0) continue;
-      // ---- end of the item: dV (half 0) and dK (half 1) rows, dv sums
+      // ---- end of the item: dV (half 0) and dK (half 1) rows, dv sums.
+      // A warp's 32 rows (consecutive in dK / dV: a key tile never straddles
+      // the ring's wrap) leave as one TMA store from its own 4 KB box of the
+      // P/dA buffer, free once this pair's dQ reductions have read it; row
+      // per thread global stores are 32 partial sectors per instruction and
+      // slow the whole SM down. A quadrant with rows past the tile's run
+      // writes its valid rows directly.
       {
         const int kk = ii;
-        const size_t krow = (size_t)it.bh * p.kv_rows + it.x.phys0 + (kk < it.x.nvalid ? kk : 0);
-        __nv_bfloat16 *dst = (hf ? p.dk : p.dv) + krow * DH;
         uint32_t ga[32], gb[32];
         tmem_ld32(trow + (hf ? TM_DK : TM_DV), ga);
         tmem_ld32(trow + (hf ? TM_DK : TM_DV) + 32, gb);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar_acc);
-        if (kk < it.x.nvalid) {
-          const float gs = hf ? 1.f : inv_scale;  // dV accumulated (scale P)^T dO
-          auto f = [&](const uint32_t(&a)[32], int e) { return __uint_as_float(a[e]) * gs; };
+        const float gs = hf ? 1.f : inv_scale;  // dV accumulated (scale P)^T dO
+        auto f = [&](const uint32_t(&a)[32], int e) { return __uint_as_float(a[e]) * gs; };
+        auto pack8 = [&](const uint32_t(&a)[32], int e) {
+          return make_uint4(pack_bf16(f(a, 8 * e + 0), f(a, 8 * e + 1)), pack_bf16(f(a, 8 * e + 2), f(a, 8 * e + 3)),
+                            pack_bf16(f(a, 8 * e + 4), f(a, 8 * e + 5)), pack_bf16(f(a, 8 * e + 6), f(a, 8 * e + 7)));
+        };
+        if (quad * 32 + 32 <= it.x.nvalid) {
+          ok = mbar_wait(bar_sfree, g & 1, abort_flag);
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          const uint32_t box = sb + F_PA + hf * 16384 + quad * 4096;
+          const uint32_t row = sw128_row(box, lane);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            ((uint4 *)dst)[e] = make_uint4(pack_bf16(f(ga, 8 * e + 0), f(ga, 8 * e + 1)),
-                                           pack_bf16(f(ga, 8 * e + 2), f(ga, 8 * e + 3)),
-                                           pack_bf16(f(ga, 8 * e + 4), f(ga, 8 * e + 5)),
-                                           pack_bf16(f(ga, 8 * e + 6), f(ga, 8 * e + 7)));
-            ((uint4 *)dst)[4 + e] = make_uint4(pack_bf16(f(gb, 8 * e + 0), f(gb, 8 * e + 1)),
-                                               pack_bf16(f(gb, 8 * e + 2), f(gb, 8 * e + 3)),
-                                               pack_bf16(f(gb, 8 * e + 4), f(gb, 8 * e + 5)),
-                                               pack_bf16(f(gb, 8 * e + 6), f(gb, 8 * e + 7)));
+            const uint4 a = pack8(ga, e), b = pack8(gb, e);
+            st_shared_v4(sw128_at(row, e), a.x, a.y, a.z, a.w);
+            st_shared_v4(sw128_at(row, 4 + e), b.x, b.y, b.z, b.w);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(hf ? &tm_dk : &tm_dv, 0, it.x.phys0 + quad * 32, it.bh, box);
+            bulk_commit();
+          }
+        } else if (kk < it.x.nvalid) {
+          const size_t krow = (size_t)it.bh * p.kv_rows + it.x.phys0 + kk;
+          uint4 *dst = (uint4 *)((hf ? p.dk : p.dv) + krow * DH);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dst[e] = pack8(ga, e);
+            dst[4 + e] = pack8(gb, e);
           }
         }
         atomicAdd(p.dv_acc + it.h * DH + 32 * hf + lane, dvp);
         dvp = 0.f;
       }
     }
+    // the dK / dV stores must have completed before shared memory goes away
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     if (!ok) atomicExch(&g_bwd_error, 2);
   }
   tc_fence_before();
@@ -1103,12 +1175,13 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   const size_t n_dr_acc = (size_t)s.H * (kDrPad + s.kv_rows) * DH;
   const int nq = (s.L + BQ - 1) / BQ;
 
-  CUtensorMap tk, tv, tr16, tqu, tqv, tdo, tdq, tdr;
+  CUtensorMap tk, tv, tr16, tqu, tqv, tdo, tdq, tdr, tdk, tdv;
   if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
       !make_map(&tr16, r16, s.H, s.kv_rows, 128) || !make_map(&tqu, qu, s.B * s.H, s.L, BQ) ||
       !make_map(&tqv, qv, s.B * s.H, s.L, BQ) || !make_map(&tdo, dout, s.B * s.H, s.L, BQ) ||
       !make_map_f32(&tdq, dq_acc, s.B * s.H, s.L) ||
-      !make_map_f32(&tdr, dr_acc, s.H, kDrPad + s.kv_rows))
+      !make_map_f32(&tdr, dr_acc, s.H, kDrPad + s.kv_rows) ||
+      !make_map(&tdk, dk, s.B * s.H, s.kv_rows, 32) || !make_map(&tdv, dv, s.B * s.H, s.kv_rows, 32))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1165,7 +1238,7 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   const unsigned grid = (unsigned)(p.nitems < sms ? p.nitems : sms);
   const int slot = timing_begin(1, st);
   cudaError_t e = launch_ex(rxl_bwd_main_kernel, dim3(grid), dim3(kThreads), F_SMEM, st, 1, tk, tv, tr16, tqu, tqv,
-                            tdo, tdq, tdr, p);
+                            tdo, tdq, tdr, tdk, tdv, p);
   timing_end(1, slot, st);
   ++*launches;
   if (e != cudaSuccess) return e;
