@@ -196,7 +196,6 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const __grid_constant__ CUtensorMap tm_r16, const __grid_constant__ CUtensorMap tm_qu,
                     const __grid_constant__ CUtensorMap tm_qv16, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dr,
-                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -248,7 +247,6 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v); tma_prefetch_desc(&tm_r16);
       tma_prefetch_desc(&tm_qu); tma_prefetch_desc(&tm_qv16); tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_dq); tma_prefetch_desc(&tm_dr);
-      tma_prefetch_desc(&tm_dk); tma_prefetch_desc(&tm_dv);
     }
   }
   tc_fence_before();
@@ -600,15 +598,28 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     bool ok = true;
     PairCursor c;
     c.init(p);
+    // lse and D of row ii of a pair's query tile, loaded a pair ahead (for
+    // a new (b, h) they come from HBM); rows past L: lse = +inf makes P = 0
+    // without a select per key
+    float lse_n = INFINITY, d_n = 0.f;
+    auto load_stats = [&](const PairCursor &cc) {
+      const int i = cc.i0() + ii;
+      if (i < p.L) {
+        const size_t row = (size_t)cc.it.bh * p.L + i;
+        lse_n = p.lse[row];
+        d_n = p.delta[row];
+      } else {
+        lse_n = INFINITY;
+        d_n = 0.f;
+      }
+    };
+    if (c.valid) load_stats(c);
     for (int g = 0; c.valid; ++g) {
       const FItem it = c.it;
       const int i0 = c.i0();
       const int i = i0 + ii;
-      const bool row_ok = i < p.L;
-      const size_t row = (size_t)it.bh * p.L + (row_ok ? i : 0);
-      // rows past L: lse = +inf makes P = 0 without a select per key
-      const float lse2 = row_ok ? p.lse[row] * kLog2e : INFINITY;
-      const float Di = row_ok ? p.delta[row] : 0.f;
+      const float lse2 = lse_n * kLog2e;
+      const float Di = d_n;
       ok = mbar_wait(bar_sg, g & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
@@ -632,14 +643,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       if (lane == 0) mbar_arrive(bar_sread);
 #pragma unroll
       for (int k = 0; k < 64; ++k) y[k] = ex2(y[k]);  // scale * P
-      // the P/dA buffer held the previous pair's dQ staging (and, after an
-      // item's last pair, this warp's dK or dV rows on their way out)
+      // the P/dA buffer held the previous pair's dQ staging
       if (g > 0) {
         ok = mbar_wait(bar_sfree, (g - 1) & 1, abort_flag);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
       }
-      if (lane == 0) bulk_wait_read();
-      __syncwarp();
       store_half_bf16(row_pa, y);
       fence_proxy_async_smem();
       tc_fence_before();
@@ -855,16 +863,17 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         dvp += v[0];
       }
       c.next(p);
+      if (c.valid) load_stats(c);
       if (c.valid && c.n != 0) continue;
       // ---- end of the item: dV (half 0) and dK (half 1) rows, dv sums.
-      // A warp's 32 rows (consecutive in dK / dV: a key tile never straddles
-      // the ring's wrap) leave as one TMA store from its own 4 KB box of the
-      // P/dA buffer, free once this pair's dQ reductions have read it; row
-      // per thread global stores are 32 partial sectors per instruction and
-      // slow the whole SM down. A quadrant with rows past the tile's run
-      // writes its valid rows directly.
+      // Thread ii holds row ii (128 bytes); stored as they are, each store
+      // instruction would write 32 partial sectors, which slows the whole SM
+      // down. An 8 x 8 transpose of 16-byte chunks within each group of 8
+      // lanes (three shuffle butterflies) leaves lane 8k + r with chunk r of
+      // the group's rows 8k .. 8k+7, so that each store instruction writes
+      // four whole 128-byte rows (a key tile's rows are consecutive in dK /
+      // dV: it never straddles the ring's wrap).
       {
-        const int kk = ii;
         uint32_t ga[32], gb[32];
         tmem_ld32(trow + (hf ? TM_DK : TM_DV), ga);
         tmem_ld32(trow + (hf ? TM_DK : TM_DV) + 32, gb);
@@ -877,39 +886,39 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           return make_uint4(pack_bf16(f(a, 8 * e + 0), f(a, 8 * e + 1)), pack_bf16(f(a, 8 * e + 2), f(a, 8 * e + 3)),
                             pack_bf16(f(a, 8 * e + 4), f(a, 8 * e + 5)), pack_bf16(f(a, 8 * e + 6), f(a, 8 * e + 7)));
         };
-        if (quad * 32 + 32 <= it.x.nvalid) {
-          ok = mbar_wait(bar_sfree, g & 1, abort_flag);
-          if (!(ok = __all_sync(0xffffffffu, ok))) break;
-          const uint32_t box = sb + F_PA + hf * 16384 + quad * 4096;
-          const uint32_t row = sw128_row(box, lane);
+        uint4 m[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint4 a = pack8(ga, e), b = pack8(gb, e);
-            st_shared_v4(sw128_at(row, e), a.x, a.y, a.z, a.w);
-            st_shared_v4(sw128_at(row, 4 + e), b.x, b.y, b.z, b.w);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(hf ? &tm_dk : &tm_dv, 0, it.x.phys0 + quad * 32, it.bh, box);
-            bulk_commit();
-          }
-        } else if (kk < it.x.nvalid) {
-          const size_t krow = (size_t)it.bh * p.kv_rows + it.x.phys0 + kk;
-          uint4 *dst = (uint4 *)((hf ? p.dk : p.dv) + krow * DH);
+        for (int e = 0; e < 4; ++e) {
+          m[e] = pack8(ga, e);
+          m[4 + e] = pack8(gb, e);
+        }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            dst[e] = pack8(ga, e);
-            dst[4 + e] = pack8(gb, e);
+        for (int sx = 4; sx >= 1; sx >>= 1) {
+          const bool up = (lane & sx) != 0;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            if (cc & sx) continue;
+            const uint4 snd = up ? m[cc] : m[cc + sx];
+            uint4 rcv;
+            rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, sx);
+            rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, sx);
+            rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, sx);
+            rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, sx);
+            if (up)
+              m[cc] = rcv;
+            else
+              m[cc + sx] = rcv;
           }
         }
+        const int r0 = quad * 32 + 8 * (lane >> 3);  // the lane group's first row of the tile
+        uint4 *out = (uint4 *)((hf ? p.dk : p.dv) + ((size_t)it.bh * p.kv_rows + it.x.phys0 + r0) * DH) + (lane & 7);
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          if (r0 + t < it.x.nvalid) out[t * (DH / 8)] = m[t];
         atomicAdd(p.dv_acc + it.h * DH + 32 * hf + lane, dvp);
         dvp = 0.f;
       }
     }
-    // the dK / dV stores must have completed before shared memory goes away
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
     if (!ok) atomicExch(&g_bwd_error, 2);
   }
   tc_fence_before();
@@ -1175,13 +1184,12 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   const size_t n_dr_acc = (size_t)s.H * (kDrPad + s.kv_rows) * DH;
   const int nq = (s.L + BQ - 1) / BQ;
 
-  CUtensorMap tk, tv, tr16, tqu, tqv, tdo, tdq, tdr, tdk, tdv;
+  CUtensorMap tk, tv, tr16, tqu, tqv, tdo, tdq, tdr;
   if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
       !make_map(&tr16, r16, s.H, s.kv_rows, 128) || !make_map(&tqu, qu, s.B * s.H, s.L, BQ) ||
       !make_map(&tqv, qv, s.B * s.H, s.L, BQ) || !make_map(&tdo, dout, s.B * s.H, s.L, BQ) ||
       !make_map_f32(&tdq, dq_acc, s.B * s.H, s.L) ||
-      !make_map_f32(&tdr, dr_acc, s.H, kDrPad + s.kv_rows) ||
-      !make_map(&tdk, dk, s.B * s.H, s.kv_rows, 32) || !make_map(&tdv, dv, s.B * s.H, s.kv_rows, 32))
+      !make_map_f32(&tdr, dr_acc, s.H, kDrPad + s.kv_rows))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1238,7 +1246,7 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   const unsigned grid = (unsigned)(p.nitems < sms ? p.nitems : sms);
   const int slot = timing_begin(1, st);
   cudaError_t e = launch_ex(rxl_bwd_main_kernel, dim3(grid), dim3(kThreads), F_SMEM, st, 1, tk, tv, tr16, tqu, tqv,
-                            tdo, tdq, tdr, tdk, tdv, p);
+                            tdo, tdq, tdr, p);
   timing_end(1, slot, st);
   ++*launches;
   if (e != cudaSuccess) return e;
