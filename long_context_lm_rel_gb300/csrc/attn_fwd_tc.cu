@@ -765,9 +765,13 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (!(ok = pair_exchange(acc, &acc_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
         if (hf == 0 && i < p.L) p.delta[(size_t)it.bh * p.L + i] = (acc + acc_other) * inv;
       } else {
-        const size_t orow_off = ((size_t)it.bh * p.L + (i < p.L ? i : 0)) * DH;
-        uint4 *orow = (uint4 *)(p.o + orow_off);
-        uint4 *lorow = (uint4 *)(p.o_lo + orow_off);
+        // this thread's half row of O as four 16-byte chunks (and of the low
+        // part), then a 4 x 4 transpose of chunks within each group of 4
+        // lanes (two shuffle butterflies): lane 4k + r holds chunk r of the
+        // group's rows 4k .. 4k+3, so that each store instruction writes
+        // whole 32-byte sectors (64 contiguous bytes of 8 rows) instead of
+        // 32 half sectors
+        uint4 mh[4], ml[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           float f[8];
@@ -781,9 +785,38 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             lo[g2] = pack_bf16(f[2 * g2] - __uint_as_float(hi[g2] << 16),
                                f[2 * g2 + 1] - __uint_as_float(hi[g2] & 0xFFFF0000u));
           }
-          if (i < p.L) {
-            orow[4 * hf + e] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            if (p.o_lo) lorow[4 * hf + e] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          mh[e] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          ml[e] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        auto xchg = [&](uint4 &a, uint4 &b, bool up, int sx) {  // up: send a, receive into a
+          const uint4 snd = up ? a : b;
+          uint4 rcv;
+          rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, sx);
+          rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, sx);
+          rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, sx);
+          rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, sx);
+          if (up)
+            a = rcv;
+          else
+            b = rcv;
+        };
+#pragma unroll
+        for (int sx = 2; sx >= 1; sx >>= 1) {
+          const bool up = (lane & sx) != 0;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            if (cc & sx) continue;
+            xchg(mh[cc], mh[cc + sx], up, sx);
+            if (p.o_lo) xchg(ml[cc], ml[cc + sx], up, sx);
+          }
+        }
+        const int r0 = it.i0 + quad * 32 + 4 * (lane >> 2);  // the lane group's first row
+        const size_t c0 = ((size_t)it.bh * p.L + r0) * (DH / 8) + 4 * hf + (lane & 3);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (r0 + t < p.L) {
+            ((uint4 *)p.o)[c0 + t * (DH / 8)] = mh[t];
+            if (p.o_lo) ((uint4 *)p.o_lo)[c0 + t * (DH / 8)] = ml[t];
           }
         }
         if (hf == 0 && i < p.L)
