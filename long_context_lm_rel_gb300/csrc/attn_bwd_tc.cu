@@ -349,28 +349,27 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       load_nx(sb + slot(s_lo), &tm_r16, band0(c), c.it.h, 0, false);
       load_nx(sb + slot(s_hi), &tm_r16, band0(c) + 128, c.it.h, 0, true);
     }
-    bool s_issued = false;  // this pair's S product was issued during the previous pair
-    for (int g = 0; ok && c.valid; ++g) {
-      const bool first = c.n == 0;
-      const int buf = g & 1;
-      const uint32_t f_qv = buf ? F_QV1 : F_QV0;
-      const uint64_t k_qv = sdesc_add(kb, f_qv), m_qv = sdesc_add(mb0, f_qv);
-      PairCursor nx = c;
-      nx.next(p);
-      if (!(ok = wait(buf ? bar_nx1 : bar_nx0, (g >> 1) & 1))) break;  // (Q+v), R, V
-      if (!s_issued && !(ok = wait(bar_qu, g & 1))) break;
-      // G's columns hold the previous pair's dQ / dR until it was flushed
-      if (g > 0 && !(ok = wait(bar_fl, (g - 1) & 1))) break;
-      const uint64_t k_rlo = sdesc_add(k_slot, s_lo * 16384), k_rhi = sdesc_add(k_slot, s_hi * 16384);
-      const uint64_t m_rlo = sdesc_add(m_slot, s_lo * 16384), m_rhi = sdesc_add(m_slot, s_hi * 16384);
-      const uint64_t k_do = sdesc_add(k_slot, s_do * 16384), m_do = sdesc_add(m_slot, s_do * 16384);
+    // S of pair g, once its (Q+u) (and an item's K) have landed, into the S
+    // columns (free since the previous pair's dA was formed)
+    auto issue_s = [&](int g) {
+      if (!(ok = wait(bar_qu, g & 1))) return;
       if (elect_one()) {
         tc_fence_after();
-        if (!s_issued) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + TM_S, kdesc(k_qu, k), kdesc(k_k, k), IDESC_S, k > 0);
-        }
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(tmem + TM_S, kdesc(k_qu, k), kdesc(k_k, k), IDESC_S, k > 0);
+      }
+      __syncwarp();
+    };
+    // G of pair g, once its (Q+v), R band (and an item's V) have landed and
+    // the previous pair's flush has released the G columns; commits S and G
+    auto issue_g = [&](int g) {
+      if (!(ok = wait((g & 1) ? bar_nx1 : bar_nx0, (g >> 1) & 1))) return;
+      if (g > 0 && !(ok = wait(bar_fl, (g - 1) & 1))) return;
+      const uint64_t k_qv = sdesc_add(kb, (g & 1) ? F_QV1 : F_QV0);
+      const uint64_t k_rlo = sdesc_add(k_slot, s_lo * 16384), k_rhi = sdesc_add(k_slot, s_hi * 16384);
+      if (elect_one()) {
+        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // G columns 0-127 from the lower half, 128-255 from the upper
           mma_bf16(tmem + TM_G, kdesc(k_qv, k), kdesc(k_rlo, k), IDESC_G_F16, k > 0);
@@ -379,23 +378,45 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         mma_commit(bar_sg);
       }
       __syncwarp();
-      // the other (Q+v) buffer was last read by the previous pair's dR,
-      // which completed before its flush released the G columns
-      if (nx.valid) load_qv(nx, buf ^ 1);
-      // the next pair's other operands come from HBM on first touch (about
-      // 2.5k cycles): pull them into L2 now, a pair ahead of their loads
-      if (nx.valid && elect_one()) {
-        const int i0n = nx.i0(), d0n = i0n - nx.it.x.jlog0 - (BK - 1);
-        tma_prefetch_l2_3d(&tm_qu, 0, i0n, nx.it.bh);
-        tma_prefetch_l2_3d(&tm_do, 0, i0n, nx.it.bh);
-        tma_prefetch_l2_3d(&tm_r16, 0, d0n + 128, nx.it.h);
-        if (nx.n == 0) {
-          tma_prefetch_l2_3d(&tm_r16, 0, d0n, nx.it.h);
-          tma_prefetch_l2_3d(&tm_k, 0, nx.it.x.phys0, nx.it.bh);
-          tma_prefetch_l2_3d(&tm_v, 0, nx.it.x.phys0, nx.it.bh);
+    };
+    // after G of pair g: (Q+v) of the pair after it (cursor n2) into the
+    // other buffer, last read by pair g-1's dR, which completed before pair
+    // g-1's flush released the G columns; n2's other operands come from HBM
+    // on first touch (about 2.5k cycles): pulled into L2 now, ahead of their
+    // loads
+    auto after_g = [&](int g, const PairCursor &n2) {
+      if (!n2.valid) return;
+      load_qv(n2, (g + 1) & 1);
+      if (elect_one()) {
+        const int i0n = n2.i0(), d0n = band0(n2);
+        tma_prefetch_l2_3d(&tm_qu, 0, i0n, n2.it.bh);
+        tma_prefetch_l2_3d(&tm_do, 0, i0n, n2.it.bh);
+        tma_prefetch_l2_3d(&tm_r16, 0, d0n + 128, n2.it.h);
+        if (n2.n == 0) {
+          tma_prefetch_l2_3d(&tm_r16, 0, d0n, n2.it.h);
+          tma_prefetch_l2_3d(&tm_k, 0, n2.it.x.phys0, n2.it.bh);
+          tma_prefetch_l2_3d(&tm_v, 0, n2.it.x.phys0, n2.it.bh);
         }
       }
       __syncwarp();
+    };
+    PairCursor nx = c;
+    nx.next(p);
+    if (c.valid) {
+      issue_s(0);
+      if (ok) issue_g(0);
+      if (ok) after_g(0, nx);
+    }
+    // Pair g's S and G were issued at the end of the previous iteration (by
+    // the prologue for the first pair), right behind pair g-1's dR, so that
+    // only the latency of G lies between a pair's flush and the next pair's
+    // softmax.
+    for (int g = 0; ok && c.valid; ++g) {
+      const bool first = c.n == 0;
+      const int buf = g & 1;
+      const uint64_t m_qv = sdesc_add(mb0, buf ? F_QV1 : F_QV0);
+      const uint64_t m_rlo = sdesc_add(m_slot, s_lo * 16384), m_rhi = sdesc_add(m_slot, s_hi * 16384);
+      const uint64_t k_do = sdesc_add(k_slot, s_do * 16384), m_do = sdesc_add(m_slot, s_do * 16384);
       // dP into the S columns as soon as the softmax warps have read S: it
       // runs while they form P
       if (!(ok = wait(bar_sread, g & 1))) break;
@@ -471,46 +492,41 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         mma_commit(bar_fin);
       }
       __syncwarp();
+      if (!nx.valid) break;
       // the lower half's slot is free once dQp's products with it are done
       // (and with them every earlier product of the pair): the next dO (same
-      // item) or the next upper half (new item; the last copy of its phase)
-      if (nx.valid) {
-        if (!(ok = wait(bar_rlo, g & 1))) break;
-        if (same) {
-          load_do(nx, s_lo);
-          const int t = s_lo;
-          s_lo = s_hi;
-          s_hi = s_do;
-          s_do = t;
-        } else {
-          load_nx(sb + slot(s_lo), &tm_r16, band0(nx) + 128, nx.it.h, buf ^ 1, true);
-        }
-      }
-      // the next pair's S into the S columns (free since dA was formed):
-      // only its G is then left between this pair's flush and the next
-      // pair's softmax
-      s_issued = false;
-      if (nx.valid) {
-        if (!(ok = wait(bar_qu, (g + 1) & 1))) break;
-        if (elect_one()) {
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + TM_S, kdesc(k_qu, k), kdesc(k_k, k), IDESC_S, k > 0);
-        }
-        __syncwarp();
-        s_issued = true;
-      }
-      if (nx.valid && !same) {
-        // new item: the next dO into the upper half's slot once dQp is done
-        if (!(ok = wait(bar_dq, g & 1))) break;
-        load_do(nx, s_hi);
+      // item) or the next upper half (new item; the last copy of its phase).
+      // The slots rotate: the next pair's lower half is this pair's upper
+      // half (same item) or the band loaded into dO's slot (new item)
+      if (!(ok = wait(bar_rlo, g & 1))) break;
+      if (same) {
+        load_do(nx, s_lo);
+        const int t = s_lo;
+        s_lo = s_hi;
+        s_hi = s_do;
+        s_do = t;
+      } else {
+        load_nx(sb + slot(s_lo), &tm_r16, band0(nx) + 128, nx.it.h, buf ^ 1, true);
         const int t = s_lo;
         s_lo = s_do;
         s_do = s_hi;
         s_hi = t;
       }
+      // the next pair's S and G
+      issue_s(g + 1);
+      if (!ok) break;
+      issue_g(g + 1);
+      if (!ok) break;
+      PairCursor n2 = nx;
+      n2.next(p);
+      after_g(g + 1, n2);
+      // new item: the next dO into the old upper half's slot once dQp is done
+      if (!same) {
+        if (!(ok = wait(bar_dq, g & 1))) break;
+        load_do(nx, s_do);
+      }
       c = nx;
+      nx = n2;
     }
     if (!ok) {
       // wind down: let in-flight copies and MMAs land before TMEM and
