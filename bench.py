@@ -313,17 +313,20 @@ def run_ours(args, rank, world):
     # event pairs around each launch of the forward kernel and of the
     # backward's main kernel (kept out of the headline pass: an event between
     # two kernels stops the second from overlapping the first one's tail)
+    timed = {"rxl_fwd_tc_kernel": rxl.RXL_KERNEL_FWD, "rxl_bwd_main_kernel": rxl.RXL_KERNEL_BWD_MAIN,
+             "bwd_prep": rxl.RXL_KERNEL_BWD_PREP, "bwd_dq_finish_kernel": rxl.RXL_KERNEL_BWD_FINISH}
     rxl.rxl_kernel_timing(True)
-    rxl.rxl_kernel_timing_read(rxl.RXL_KERNEL_FWD)
-    rxl.rxl_kernel_timing_read(rxl.RXL_KERNEL_BWD_MAIN)
+    for k in timed.values():
+        rxl.rxl_kernel_timing_read(k)
     for _ in range(args.steps):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     rxl.rxl_kernel_timing(False)
-    kfwd_ms, kfwd_n = rxl.rxl_kernel_timing_read(rxl.RXL_KERNEL_FWD)
-    kbwd_ms, kbwd_n = rxl.rxl_kernel_timing_read(rxl.RXL_KERNEL_BWD_MAIN)
-    kernel_ms = {"rxl_fwd_tc_kernel": kfwd_ms / max(kfwd_n, 1), "rxl_bwd_main_kernel": kbwd_ms / max(kbwd_n, 1)}
+    kernel_ms = {}
+    for name, k in timed.items():
+        t_ms, n_launch = rxl.rxl_kernel_timing_read(k)
+        kernel_ms[name] = t_ms / max(n_launch, 1)
     kernel_ms = {k: max_over_ranks(v, world, device="cuda") for k, v in kernel_ms.items()}
 
     # run-to-run variation of the backward: dQ/dR/du/dv are summed by

@@ -352,8 +352,10 @@ int rxl_device_error_flags(void);
 /*
  * Measurement hook (no counterpart in the paper). With timing enabled, every
  * launch of the forward kernel (kernel 0: rxl_attn_fwd*, not the backward's
- * recomputation) and of the backward's main kernel (kernel 1: the fused
- * pass over the (query tile, key tile) pairs) is bracketed by a CUDA event
+ * recomputation), of the backward's main kernel (kernel 1: the fused pass
+ * over the (query tile, key tile) pairs), of the backward's preparation
+ * (kernel 2: zeroing and the (Q+u), (Q+v), D operands, one or two launches)
+ * and of the backward's finish kernel (kernel 3) is bracketed by a CUDA event
  * pair recorded on the call's stream; up to 1024 launches per kernel are kept.
  * rxl_kernel_timing_read waits for the recorded events, returns the summed
  * device time in milliseconds and the number of timed launches, and clears

@@ -234,7 +234,7 @@ def rxl_mem_update_rings(rings, srcs, src_plane_strides, L: int, stream=None):
            "rxl_mem_update_rings")
 
 
-RXL_KERNEL_FWD, RXL_KERNEL_BWD_MAIN = 0, 1
+RXL_KERNEL_FWD, RXL_KERNEL_BWD_MAIN, RXL_KERNEL_BWD_PREP, RXL_KERNEL_BWD_FINISH = 0, 1, 2, 3
 
 
 def rxl_kernel_timing(enable: bool):

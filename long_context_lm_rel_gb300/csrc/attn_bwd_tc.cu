@@ -493,30 +493,33 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
       __syncwarp();
       if (!nx.valid) break;
-      // the lower half's slot is free once dQp's products with it are done
+      // The lower half's slot is free once dQp's products with it are done
       // (and with them every earlier product of the pair): the next dO (same
       // item) or the next upper half (new item; the last copy of its phase).
       // The slots rotate: the next pair's lower half is this pair's upper
-      // half (same item) or the band loaded into dO's slot (new item)
-      if (!(ok = wait(bar_rlo, g & 1))) break;
+      // half (same item) or the band loaded into dO's slot (new item).
+      const int old_lo = s_lo;
       if (same) {
-        load_do(nx, s_lo);
-        const int t = s_lo;
         s_lo = s_hi;
         s_hi = s_do;
-        s_do = t;
+        s_do = old_lo;
       } else {
-        load_nx(sb + slot(s_lo), &tm_r16, band0(nx) + 128, nx.it.h, buf ^ 1, true);
-        const int t = s_lo;
+        if (!(ok = wait(bar_rlo, g & 1))) break;
+        load_nx(sb + slot(old_lo), &tm_r16, band0(nx) + 128, nx.it.h, buf ^ 1, true);
         s_lo = s_do;
         s_do = s_hi;
-        s_hi = t;
+        s_hi = old_lo;
       }
-      // the next pair's S and G
+      // the next pair's S and G (same item: nothing they read is still on
+      // its way, so they go first)
       issue_s(g + 1);
       if (!ok) break;
       issue_g(g + 1);
       if (!ok) break;
+      if (same) {
+        if (!(ok = wait(bar_rlo, g & 1))) break;
+        load_do(nx, s_do);
+      }
       PairCursor n2 = nx;
       n2.next(p);
       after_g(g + 1, n2);
@@ -1068,38 +1071,62 @@ __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(
     int L, int H, int kv_rows, int chunks) {
   griddep_wait();
   griddep_launch_dependents();
-  __shared__ float part[32][65];
+  __shared__ float part[8][64];  // column sums of each warp's rows
   __shared__ bool last;
   const int bh = blockIdx.x / chunks, ch = blockIdx.x % chunks;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = threadIdx.x & 7, slot = threadIdx.x >> 3;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   const int r_end = min(L, (ch + 1) * 128);
-  for (int i = ch * 128 + slot; i < r_end; i += 32) {
-    const size_t off = ((size_t)bh * L + i) * DH + 8 * sub;
-    const float4 a = *(const float4 *)(dq_acc + off);
-    const float4 b = *(const float4 *)(dq_acc + off + 4);
-    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-    *(uint4 *)(dq + off) = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
-                                      pack_bf16(b.z, b.w));
-  }
+  // the thread's four rows (slot, slot + 32, ..): all loads in flight first
+  float4 a[4], b[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) part[slot][8 * sub + e] = acc[e];
+  for (int t = 0; t < 4; ++t) {
+    const int i = ch * 128 + slot + 32 * t;
+    a[t] = b[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < r_end) {
+      const size_t off = ((size_t)bh * L + i) * DH + 8 * sub;
+      a[t] = *(const float4 *)(dq_acc + off);
+      b[t] = *(const float4 *)(dq_acc + off + 4);
+    }
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int i = ch * 128 + slot + 32 * t;
+    acc[0] += a[t].x; acc[1] += a[t].y; acc[2] += a[t].z; acc[3] += a[t].w;
+    acc[4] += b[t].x; acc[5] += b[t].y; acc[6] += b[t].z; acc[7] += b[t].w;
+    if (i < r_end) {
+      const size_t off = ((size_t)bh * L + i) * DH + 8 * sub;
+      *(uint4 *)(dq + off) = make_uint4(pack_bf16(a[t].x, a[t].y), pack_bf16(a[t].z, a[t].w),
+                                        pack_bf16(b[t].x, b[t].y), pack_bf16(b[t].z, b[t].w));
+    }
+  }
+  // lanes l, l+8, l+16, l+24 hold the same 8 columns: fold them, then the
+  // warps' partials through shared memory
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 8);
+    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
+  }
+  if (lane < 8) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[warp][8 * lane + e] = acc[e];
+  }
   __syncthreads();
   if (threadIdx.x < 64) {
-    float s = 0.f;
-    for (int k = 0; k < 32; ++k) s += part[k][threadIdx.x];
-    atomicAdd(colsum + (bh % H) * DH + threadIdx.x, s);
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += part[w][threadIdx.x];
+    atomicAdd(colsum + (bh % H) * DH + threadIdx.x, sum);
+    __threadfence();  // this block's column sums land before the counter moves
   }
   {
-    const size_t per_h = (size_t)kv_rows * DH / 4, n = (size_t)H * per_h;
-    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
-      const size_t h = e / per_h, o = e % per_h;
+    const size_t per_h = (size_t)kv_rows * (DH / 4), n = (size_t)H * per_h;
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+      const size_t h = e / per_h, o = e - h * per_h;
       ((float4 *)dr)[e] = ((const float4 *)(dr_acc + (h * (kv_rows + kDrPad) + kDrPad) * DH))[o];
     }
   }
-  // the column sums of every block are in place before the counter moves
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
   __syncthreads();
@@ -1225,6 +1252,7 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   z.BH = s.B * s.H; z.H = s.H; z.cap = s.cap; z.m = s.m; z.head = s.head; z.kv_rows = s.kv_rows;
   z.r = (const __nv_bfloat16 *)r; z.r16 = r16; z.n_r = (size_t)s.H * s.kv_rows * DH;
   z.mvis = s.mvis;
+  const int prep_slot = timing_begin(2, st);
   if (o_lo) {
     long long blocks = ((long long)rows * 8 + 255) / 256;
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
@@ -1234,14 +1262,24 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
         (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)u, (const __nv_bfloat16 *)vb, (const __nv_bfloat16 *)o,
         (const __nv_bfloat16 *)o_lo, (const __nv_bfloat16 *)dout, (__nv_bfloat16 *)qu, (__half *)qv, delta);
     ++*launches;
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      timing_end(2, prep_slot, st);
+      return e;
+    }
   } else {
     cudaError_t e = launch_ex(bwd_zero_kernel, dim3((unsigned)(sms * 4)), dim3(256), 0, st, 1, z);
     ++*launches;
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      timing_end(2, prep_slot, st);
+      return e;
+    }
     e = launch_tc_bwd_prep(s, q, k, v, r, u, vb, dout, delta, qu, qv, st, launches);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      timing_end(2, prep_slot, st);
+      return e;
+    }
   }
+  timing_end(2, prep_slot, st);
 
   BwdParams p;
   p.B = s.B; p.H = s.H; p.L = s.L; p.cap = s.cap; p.m = s.m; p.head = s.head; p.nq = nq;
@@ -1267,9 +1305,11 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   ++*launches;
   if (e != cudaSuccess) return e;
   const int chunks = (s.L + 127) / 128;
+  const int fin_slot = timing_begin(3, st);
   e = launch_ex(bwd_dq_finish_kernel, dim3((unsigned)(s.B * s.H * chunks)), dim3(256), 0, st, 1,
                 (const float *)dq_acc, (__nv_bfloat16 *)dq, sums + s.H * DH, (const float *)sums,
                 (unsigned *)(sums + 2 * s.H * DH), du, dvb, (const float *)dr_acc, dr, s.L, s.H, s.kv_rows, chunks);
+  timing_end(3, fin_slot, st);
   ++*launches;
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -48,7 +48,9 @@ inline cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t 
 // Opt-in device timing (rxl_kernel_timing): timing_begin records a start event
 // on st and returns a slot (-1 when timing is off or full); timing_end records
 // the matching stop event.
-constexpr int kTimedKernels = 2;  // 0: forward kernel, 1: backward main kernel
+// 0: forward kernel, 1: backward main kernel, 2: backward prep launches (zero and
+// operand prep), 3: backward finish kernel
+constexpr int kTimedKernels = 4;
 bool timing_enabled();
 int timing_begin(int kernel, cudaStream_t st);
 void timing_end(int kernel, int slot, cudaStream_t st);

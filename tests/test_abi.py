@@ -119,3 +119,15 @@ def test_mem_update_rings_rejects_mismatched_rings(lib):
     assert call([], n=0) == rxl.RXL_ERR_INVALID_ARGUMENT
     assert call([mk() for _ in range(9)]) == rxl.RXL_ERR_INVALID_ARGUMENT
     assert (a.head, a.len) == (0, 0)                                  # nothing advanced
+
+
+def test_kernel_timing_ids(lib):
+    """Kernels 0-3 (forward, backward main, backward prep, backward finish)
+    read back empty before anything was timed; other ids are refused with
+    cudaErrorInvalidValue. No device call is made on these paths."""
+    ms, n = ctypes.c_double(-1.0), ctypes.c_int(-1)
+    for k in range(4):
+        assert lib.rxl_kernel_timing_read(k, ctypes.byref(ms), ctypes.byref(n)) == 0
+        assert (ms.value, n.value) == (0.0, 0)
+    for k in (-1, 4):
+        assert lib.rxl_kernel_timing_read(k, ctypes.byref(ms), ctypes.byref(n)) == 1
