@@ -609,7 +609,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const uint32_t row_dg = sw128_row(sb + F_DG, ii);
     const uint32_t row_dr = sw128_row(sb + F_DG + 2 * hf * 16384, ii);
     uint32_t xphase = 0;
-    float dvp = 0.f;  // sum over this warp's rows of dQp, column 32*hf + lane
+    // this thread's dQp row values summed over the pairs of the item
+    // (columns 32*hf ..); summed over the warp's rows once per item
+    float dva[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) dva[e] = 0.f;
     // the exponent bias carries log2(scale): the softmax handles scale * P
     // throughout (dA = (scale P)(dP - D) in two packed ops); the P tile of
     // the dV product holds scale * P, so dV is divided by scale at the end
@@ -857,29 +861,12 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (lane == 0) mbar_arrive(bar_str);
       }
       {
-        // column sums of dQp over the warp's 32 rows (recursive halving):
-        // afterwards lane l holds column 32*hf + l
 #pragma unroll
-        for (int h2 = 16; h2 >= 1; h2 >>= 1) {
-          const bool upper = (lane & h2) != 0;
-          if (h2 == 1) {
-            const float send = upper ? v[0] : v[1];
-            const float keep = upper ? v[1] : v[0];
-            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-          } else {
-#pragma unroll
-            for (int k = 0; k < h2; k += 2) {  // pairs of columns through the packed add
-              const float s0 = upper ? v[k] : v[k + h2], s1 = upper ? v[k + 1] : v[k + 1 + h2];
-              const float k0 = upper ? v[k + h2] : v[k], k1 = upper ? v[k + 1 + h2] : v[k + 1];
-              const float2 t = __fadd2_rn(make_float2(k0, k1),
-                                          make_float2(__shfl_xor_sync(0xffffffffu, s0, h2),
-                                                      __shfl_xor_sync(0xffffffffu, s1, h2)));
-              v[k] = t.x;
-              v[k + 1] = t.y;
-            }
-          }
+        for (int e = 0; e < 32; e += 2) {
+          const float2 t = __fadd2_rn(make_float2(dva[e], dva[e + 1]), make_float2(v[e], v[e + 1]));
+          dva[e] = t.x;
+          dva[e + 1] = t.y;
         }
-        dvp += v[0];
       }
       c.next(p);
       if (c.valid) load_stats(c);
@@ -934,8 +921,31 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
         for (int t = 0; t < 8; ++t)
           if (r0 + t < it.x.nvalid) out[t * (DH / 8)] = m[t];
-        atomicAdd(p.dv_acc + it.h * DH + 32 * hf + lane, dvp);
-        dvp = 0.f;
+        // column sums of dQp over the warp's 32 rows (recursive halving):
+        // afterwards lane l holds column 32*hf + l
+#pragma unroll
+        for (int h2 = 16; h2 >= 1; h2 >>= 1) {
+          const bool upper = (lane & h2) != 0;
+          if (h2 == 1) {
+            const float send = upper ? dva[0] : dva[1];
+            const float keep = upper ? dva[1] : dva[0];
+            dva[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+          } else {
+#pragma unroll
+            for (int k = 0; k < h2; k += 2) {  // pairs of columns through the packed add
+              const float s0 = upper ? dva[k] : dva[k + h2], s1 = upper ? dva[k + 1] : dva[k + 1 + h2];
+              const float k0 = upper ? dva[k + h2] : dva[k], k1 = upper ? dva[k + 1 + h2] : dva[k + 1];
+              const float2 t = __fadd2_rn(make_float2(k0, k1),
+                                          make_float2(__shfl_xor_sync(0xffffffffu, s0, h2),
+                                                      __shfl_xor_sync(0xffffffffu, s1, h2)));
+              dva[k] = t.x;
+              dva[k + 1] = t.y;
+            }
+          }
+        }
+        atomicAdd(p.dv_acc + it.h * DH + 32 * hf + lane, dva[0]);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dva[e] = 0.f;
       }
     }
     if (!ok) atomicExch(&g_bwd_error, 2);
