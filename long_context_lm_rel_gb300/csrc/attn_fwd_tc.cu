@@ -46,6 +46,7 @@
 #include <math.h>
 #include <stdio.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "internal.cuh"
@@ -77,7 +78,8 @@ constexpr uint32_t SM_P = 163840;              // 2 x [128][64] bf16 (keys 0-63,
 constexpr uint32_t SM_BAR = 196608;            // mbarriers, TMEM slot, abort flag
 constexpr uint32_t SM_X = SM_BAR + 256;        // row-half exchange: [2][2][128] floats
 constexpr uint32_t SM_QRAW = 199680;           // the next item's Q rows [128][64] bf16 (TMA, sw128)
-constexpr uint32_t SMEM_BYTES = SM_QRAW + 16384 + 1024;  // + alignment slack
+constexpr uint32_t SM_UV = SM_QRAW + 16384;     // and its head's u and v rows (2 x 128 B)
+constexpr uint32_t SMEM_BYTES = SM_UV + 256 + 1024;  // + alignment slack
 constexpr float kRescaleThreshold = 8.f;       // log2 units
 // O accumulators: keys 0-63 of every tile into TM_O, keys 64-127 into TM_O + 64
 constexpr uint32_t TM_S = 0, TM_G = 128, TM_O = 384, TM_COLS = 512;
@@ -212,17 +214,16 @@ __device__ __forceinline__ void q_prep(const Params &p, const Item &it, uint32_t
   const int ii = quad * 32 + lane;
   const int i = it.i0 + ii;
   const float c2 = p.scale_log2;
-  const uint4 *urow = (const uint4 *)(p.u + (size_t)it.h * DH);
-  const uint4 *vrow = (const uint4 *)(p.vb + (size_t)it.h * DH);
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
     const int c = 4 * hf + cc;
-    // the raw Q rows were loaded by TMA (rows past L read as zero)
+    // the raw Q rows were loaded by TMA (rows past L read as zero), the
+    // head's u and v rows with them
     uint4 qv4;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(qv4.x), "=r"(qv4.y), "=r"(qv4.z), "=r"(qv4.w)
                  : "r"(sbase + SM_QRAW + sw128_offset(ii, c)));
-    const uint4 u4 = urow[c], v4 = vrow[c];
+    const uint4 u4 = ld_shared_v4(sbase + SM_UV + 16 * c), v4 = ld_shared_v4(sbase + SM_UV + 128 + 16 * c);
     const uint32_t qw[4] = {qv4.x, qv4.y, qv4.z, qv4.w};
     const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
     const uint32_t vw[4] = {v4.x, v4.y, v4.z, v4.w};
@@ -255,6 +256,7 @@ template <int MODE, bool RESET, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_olo,
                   const Params p, int nitems) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = tc::align1024(smem_raw);
@@ -411,8 +413,10 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (w >= nitems) return;
         const Item qi = item_at<RESET>(p, w);
         if (elect_one()) {
-          mbar_expect_tx(bar_q, 16384);
+          mbar_expect_tx(bar_q, 16384 + 256);
           tma_load_3d(sbase + SM_QRAW, &tm_q, 0, qi.i0, qi.bh, bar_q);
+          bulk_load(sbase + SM_UV, p.u + (size_t)qi.h * DH, 128, bar_q);
+          bulk_load(sbase + SM_UV + 128, p.vb + (size_t)qi.h * DH, 128, bar_q);
         }
         __syncwarp();
         ++nq_loads;
@@ -473,11 +477,11 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         __syncwarp();
         if (new_item) {
           // next item: its Q tiles are written once the softmax finished
-          // this item's last tile
+          // this item's last tile; its S/G first, then the copies
           if (!(ok = wait(bar_sgfree, g & 1) && wait(bar_qready, nx.k & 1) && wait_kr(g + 1))) break;
-          load_q(nx.k + 1);  // the softmax has read item nx.k's raw rows
           issue_g(g + 1);
           issue_s_commit(g + 1);
+          load_q(nx.k + 1);  // the softmax has read item nx.k's raw rows
           if (kc.valid) issue_kr();  // tile g's S/G are done (read by the softmax)
         }
         mc = nx;
@@ -616,6 +620,12 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         ok = mbar_wait(bar_pv, (g - 1) & 1, abort_flag);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
         tc_fence_after();
+      }
+      // the warp's part of the P buffer held the previous item's O rows on
+      // their way out
+      if (MODE != kPrep && t == t0 && cur.k > 0) {
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
       }
 #pragma unroll
       for (int c = 0; c < 8; ++c)
@@ -765,6 +775,8 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (!(ok = pair_exchange(acc, &acc_other, xbuf, bar_x, hf, ii, lane, xphase, abort_flag))) break;
         if (hf == 0 && i < p.L) p.delta[(size_t)it.bh * p.L + i] = (acc + acc_other) * inv;
       } else {
+        if (hf == 0 && i < p.L)
+          p.lse[(size_t)it.bh * p.L + i] = (m_row + log2f(l_row)) * 0.69314718055994531f;
         // this thread's half row of O as four 16-byte chunks (and of the low
         // part), then a 4 x 4 transpose of chunks within each group of 4
         // lanes (two shuffle butterflies): lane 4k + r holds chunk r of the
@@ -788,42 +800,35 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           mh[e] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           ml[e] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        auto xchg = [&](uint4 &a, uint4 &b, bool up, int sx) {  // up: send a, receive into a
-          const uint4 snd = up ? a : b;
-          uint4 rcv;
-          rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, sx);
-          rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, sx);
-          rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, sx);
-          rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, sx);
-          if (up)
-            a = rcv;
-          else
-            b = rcv;
-        };
+        // this warp's 32 rows x 32 columns of O (and of its low part) leave
+        // by TMA stores from the warp's own 4 KB of the P buffer (the last
+        // P.V has read P): 64-byte swizzled boxes, 2 KB each, so that the
+        // row-per-thread staging stores hit every bank; rows past L are
+        // clipped by the copy. The warp's next P store waits for the copies
+        // to have read the box.
+        const uint32_t obox = sbase + SM_P + hf * 16384 + quad * 4096;
+        const uint32_t orow = obox + lane * 64;
+        const int osw = (lane >> 1) & 3;  // 64-byte swizzle: chunk ^= (row >> 1) & 3
 #pragma unroll
-        for (int sx = 2; sx >= 1; sx >>= 1) {
-          const bool up = (lane & sx) != 0;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            if (cc & sx) continue;
-            xchg(mh[cc], mh[cc + sx], up, sx);
-            if (p.o_lo) xchg(ml[cc], ml[cc + sx], up, sx);
-          }
+        for (int e = 0; e < 4; ++e) {
+          st_shared_v4(orow + ((e ^ osw) << 4), mh[e].x, mh[e].y, mh[e].z, mh[e].w);
+          if (p.o_lo) st_shared_v4(orow + 2048 + ((e ^ osw) << 4), ml[e].x, ml[e].y, ml[e].z, ml[e].w);
         }
-        const int r0 = it.i0 + quad * 32 + 4 * (lane >> 2);  // the lane group's first row
-        const size_t c0 = ((size_t)it.bh * p.L + r0) * (DH / 8) + 4 * hf + (lane & 3);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (r0 + t < p.L) {
-            ((uint4 *)p.o)[c0 + t * (DH / 8)] = mh[t];
-            if (p.o_lo) ((uint4 *)p.o_lo)[c0 + t * (DH / 8)] = ml[t];
-          }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && it.i0 + 32 * quad < p.L) {
+          tma_store_3d(&tm_o, 32 * hf, it.i0 + 32 * quad, it.bh, obox);
+          if (p.o_lo) tma_store_3d(&tm_olo, 32 * hf, it.i0 + 32 * quad, it.bh, obox + 2048);
+          bulk_commit();
         }
-        if (hf == 0 && i < p.L)
-          p.lse[(size_t)it.bh * p.L + i] = (m_row + log2f(l_row)) * 0.69314718055994531f;
       }
       m_run = -INFINITY;
       l_run = 0.f;
+    }
+    // the O stores must have completed before shared memory goes away
+    if (MODE != kPrep) {
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
     if (!ok) atomicExch(&g_fwd_error, 1);
   }
@@ -854,6 +859,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// [planes][rows][64] bf16 output tensor, 32 x 32 boxes, 64-byte swizzle (the
+// O stores of the epilogue).
+bool make_map_out(CUtensorMap *m, const void *base, int planes, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)rows * 128};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [planes][rows][64] bf16 tensor, box of `box_rows` rows, 128-byte swizzle.
 bool make_map(CUtensorMap *m, const void *base, int planes, int rows, int box_rows) {
   EncodeTiledFn enc = encode_fn();
@@ -872,9 +891,14 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
                         const void *r, const void *u, const void *vb, void *o, void *o_lo, float *lse,
                         const void *dout, float *delta, void *qu_out, void *qv_out,
                         cudaStream_t st, int *launches) {
-  CUtensorMap tk, tv, tr, tq;
+  CUtensorMap tk, tv, tr, tq, to, tolo;
   if (!make_map(&tk, k, s.B * s.H, s.kv_rows, BK) || !make_map(&tv, v, s.B * s.H, s.kv_rows, BK) ||
       !make_map(&tr, r, s.H, s.kv_rows, NB) || !make_map(&tq, q, s.B * s.H, s.L, BQ))
+    return cudaErrorInvalidValue;
+  // the outputs' maps (the preparation pass writes no O: its maps are unused)
+  memset(&to, 0, sizeof(to));
+  memset(&tolo, 0, sizeof(tolo));
+  if (MODE == kFwd && (!make_map_out(&to, o, s.B * s.H, s.L) || (o_lo && !make_map_out(&tolo, o_lo, s.B * s.H, s.L))))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -907,9 +931,9 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
     const int slot = timing_begin(0, st);
     cudaError_t e =
         s.mvis ? launch_ex(rxl_fwd_tc_kernel<MODE, true, true>, dim3((unsigned)(2 * nitems)), dim3(kThreads),
-                           SMEM_BYTES, st, 2, tk, tv, tr, tq, p, nitems)
+                           SMEM_BYTES, st, 2, tk, tv, tr, tq, to, tolo, p, nitems)
                : launch_ex(rxl_fwd_tc_kernel<MODE, false, true>, dim3((unsigned)(2 * nitems)), dim3(kThreads),
-                           SMEM_BYTES, st, 2, tk, tv, tr, tq, p, nitems);
+                           SMEM_BYTES, st, 2, tk, tv, tr, tq, to, tolo, p, nitems);
     timing_end(0, slot, st);
     ++*launches;
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -918,9 +942,9 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   const int slot = MODE == kFwd ? timing_begin(0, st) : -1;
   const cudaError_t e =
       s.mvis ? launch_ex(rxl_fwd_tc_kernel<MODE, true, false>, dim3(grid), dim3(kThreads), SMEM_BYTES, st, 1, tk, tv,
-                         tr, tq, p, nitems)
+                         tr, tq, to, tolo, p, nitems)
              : launch_ex(rxl_fwd_tc_kernel<MODE, false, false>, dim3(grid), dim3(kThreads), SMEM_BYTES, st, 1, tk,
-                         tv, tr, tq, p, nitems);
+                         tv, tr, tq, to, tolo, p, nitems);
   timing_end(0, slot, st);
   ++*launches;
   return e != cudaSuccess ? e : cudaGetLastError();

@@ -154,6 +154,15 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint3
       : "memory");
 }
 
+// Global -> shared bulk copy (no tensor map) completing `bytes` of the
+// transaction count of the local mbarrier `bar`; src and dst 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // Bounded wait on a local mbarrier that other CTAs of the cluster arrive on
 // (acquire at cluster scope): false after g_wait_cycles or an abort.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort) {
