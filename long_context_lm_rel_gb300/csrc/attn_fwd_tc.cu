@@ -623,7 +623,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       }
       // the warp's part of the P buffer held the previous item's O rows on
       // their way out
-      if (MODE != kPrep && t == t0 && cur.k > 0) {
+      if (MODE != kPrep && !SPLIT && t == t0 && cur.k > 0) {
         if (lane == 0) bulk_wait_read();
         __syncwarp();
       }
@@ -800,33 +800,72 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           mh[e] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           ml[e] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        // this warp's 32 rows x 32 columns of O (and of its low part) leave
-        // by TMA stores from the warp's own 4 KB of the P buffer (the last
-        // P.V has read P): 64-byte swizzled boxes, 2 KB each, so that the
-        // row-per-thread staging stores hit every bank; rows past L are
-        // clipped by the copy. The warp's next P store waits for the copies
-        // to have read the box.
-        const uint32_t obox = sbase + SM_P + hf * 16384 + quad * 4096;
-        const uint32_t orow = obox + lane * 64;
-        const int osw = (lane >> 1) & 3;  // 64-byte swizzle: chunk ^= (row >> 1) & 3
+        if (SPLIT) {
+          // one item per CTA (2-CTA clusters): a 4 x 4 transpose of 16-byte
+          // chunks within each group of 4 lanes (two shuffle butterflies),
+          // so that each store writes whole 32-byte sectors; here the TMA
+          // stores below came out slower (their issue waits on the busy TMA
+          // engine and nothing follows to hide it)
+          auto xchg = [&](uint4 &a, uint4 &b, bool up, int sx) {  // up: send a, receive into a
+            const uint4 snd = up ? a : b;
+            uint4 rcv;
+            rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, sx);
+            rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, sx);
+            rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, sx);
+            rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, sx);
+            if (up)
+              a = rcv;
+            else
+              b = rcv;
+          };
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          st_shared_v4(orow + ((e ^ osw) << 4), mh[e].x, mh[e].y, mh[e].z, mh[e].w);
-          if (p.o_lo) st_shared_v4(orow + 2048 + ((e ^ osw) << 4), ml[e].x, ml[e].y, ml[e].z, ml[e].w);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && it.i0 + 32 * quad < p.L) {
-          tma_store_3d(&tm_o, 32 * hf, it.i0 + 32 * quad, it.bh, obox);
-          if (p.o_lo) tma_store_3d(&tm_olo, 32 * hf, it.i0 + 32 * quad, it.bh, obox + 2048);
-          bulk_commit();
+          for (int sx = 2; sx >= 1; sx >>= 1) {
+            const bool up = (lane & sx) != 0;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              if (cc & sx) continue;
+              xchg(mh[cc], mh[cc + sx], up, sx);
+              if (p.o_lo) xchg(ml[cc], ml[cc + sx], up, sx);
+            }
+          }
+          const int r0 = it.i0 + quad * 32 + 4 * (lane >> 2);  // the lane group's first row
+          const size_t c0 = ((size_t)it.bh * p.L + r0) * (DH / 8) + 4 * hf + (lane & 3);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            if (r0 + t < p.L) {
+              ((uint4 *)p.o)[c0 + t * (DH / 8)] = mh[t];
+              if (p.o_lo) ((uint4 *)p.o_lo)[c0 + t * (DH / 8)] = ml[t];
+            }
+          }
+        } else {
+          // this warp's 32 rows x 32 columns of O (and of its low part) leave
+          // by TMA stores from the warp's own 4 KB of the P buffer (the last
+          // P.V has read P): 64-byte swizzled boxes, 2 KB each, so that the
+          // row-per-thread staging stores hit every bank; rows past L are
+          // clipped by the copy. The warp's next P store waits for the copies
+          // to have read the box.
+          const uint32_t obox = sbase + SM_P + hf * 16384 + quad * 4096;
+          const uint32_t orow = obox + lane * 64;
+          const int osw = (lane >> 1) & 3;  // 64-byte swizzle: chunk ^= (row >> 1) & 3
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            st_shared_v4(orow + ((e ^ osw) << 4), mh[e].x, mh[e].y, mh[e].z, mh[e].w);
+            if (p.o_lo) st_shared_v4(orow + 2048 + ((e ^ osw) << 4), ml[e].x, ml[e].y, ml[e].z, ml[e].w);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && it.i0 + 32 * quad < p.L) {
+            tma_store_3d(&tm_o, 32 * hf, it.i0 + 32 * quad, it.bh, obox);
+            if (p.o_lo) tma_store_3d(&tm_olo, 32 * hf, it.i0 + 32 * quad, it.bh, obox + 2048);
+            bulk_commit();
+          }
         }
       }
       m_run = -INFINITY;
       l_run = 0.f;
     }
     // the O stores must have completed before shared memory goes away
-    if (MODE != kPrep) {
+    if (MODE != kPrep && !SPLIT) {
       if (lane == 0) bulk_wait_all();
       __syncwarp();
     }
