@@ -29,8 +29,11 @@
 //   * tcgen05: O_h += P_h V_h -> TMEM cols [384,448), [448,512) for the key
 //     halves h (M=128, N=64, K=64 each); the epilogue combines the halves
 //     with their references (one exchange through shared memory per item)
-// Warp 8 is the producer: one thread issues the TMA loads (two stages) and
-// every MMA; tcgen05.commit signals completion through mbarriers.
+//     and writes O (and its low part) by per-warp TMA stores staged in the
+//     free P buffer
+// Warp 8 is the producer: the whole warp runs the schedule and one elected
+// thread issues each TMA load (two stages ahead, across items) and each MMA;
+// tcgen05.commit signals completion through mbarriers.
 //
 // Few items (at most half as many as SMs: short segments, few heads): the
 // kernel runs as clusters of two CTAs per item instead of persistently, each
@@ -40,9 +43,9 @@
 // rank 0 merges the two and writes the output. Every cross-CTA wait is a
 // bounded mbarrier wait.
 //
-// The skew: thread of row ii = 32*quad + lane needs G columns ii..ii+127. Per
-// chunk of 32 keys it loads a warp-uniform 64-column window and shifts it by
-// its lane with a 5-stage predicated barrel shift.
+// The skew: thread of row ii = 32*quad + lane needs G columns ii..ii+127. For
+// its 64 keys it loads one warp-uniform 96-column window and shifts it by its
+// lane with a 5-stage predicated barrel shift.
 #include <math.h>
 #include <stdio.h>
 
