@@ -996,12 +996,16 @@ __device__ void zero_work(const ZeroArgs &z, size_t tid, size_t stride) {
   }
   if (__any_sync(0xffffffffu, rmax > 65504.f) && (threadIdx.x & 31) == 0) atomicOr(&g_bwd_range, 1);
   // ring slots whose rows the row does not see: logical slots t < m - mb
-  // (masked by a document reset) and t >= m (no valid memory); 8 x 16 B per row
-  const size_t n_rows = (size_t)z.BH * z.cap * 8;
+  // (masked by a document reset) and t >= m (no valid memory); 8 x 16 B per
+  // row. Without a reset only t >= m: the walk covers those slots alone (none
+  // when the ring is full)
+  const int t_lo = z.mvis ? 0 : z.m, n_t = z.cap - t_lo;
+  if (n_t <= 0) return;
+  const size_t n_rows = (size_t)z.BH * n_t * 8;
   for (size_t e = tid; e < n_rows; e += stride) {
     const int c = (int)(e & 7);
     const size_t rr = e >> 3;
-    const int bh = (int)(rr / z.cap), t = (int)(rr % z.cap);
+    const int bh = (int)(rr / n_t), t = t_lo + (int)(rr % n_t);
     const int mb = row_memory(z.mvis, bh / z.H, z.m, z.cap, z.head).m;
     if (t >= z.m - mb && t < z.m) continue;
     int pr = z.head + t;
