@@ -1037,7 +1037,8 @@ __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
   float qvmax = 0.f;  // largest |q + v| converted to fp16 by this thread
   for (long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 3; row < rows;
        row += ((long long)gridDim.x * blockDim.x) >> 3) {
-    const int h = (int)((row / L) % H);
+    // the row's head (32-bit division whenever the row count allows)
+    const int h = rows < (1ll << 32) ? (int)(((unsigned)row / (unsigned)L) % (unsigned)H) : (int)((row / L) % H);
     const size_t off = (size_t)row * DH;
     const uint4 q4 = ((const uint4 *)(q + off))[sub];
     const uint4 u4 = ((const uint4 *)(u + (size_t)h * DH))[sub];
