@@ -123,6 +123,27 @@ def test_few_items_two_cta_clusters(ex):
     compare_full(x, c, cap, m, head, "bf16", tag=f"split {ex}")
 
 
+@pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
+def test_persistent_forward_ragged_rows(ex):
+    # 4 x 16 heads x two query tiles = 128 items, more than half the SMs: the
+    # persistent forward, whose O (and low part) leave by TMA stores that
+    # must stop at each (b, h) plane's last row (L = 200: the second tile's
+    # last 56 rows do not exist); a wrapping ring; every element, and the low
+    # part against the unrounded output
+    import torch
+    B, H, L, cap, m, head = 4, 16, 200, 300, 250, 123
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=2002)
+    c = run_gpu(x, cap, m, head, "bf16", ex=ex)
+    compare_full(x, c, cap, m, head, "bf16", tag=f"persistent ragged {ex}")
+    if ex:
+        torch.cuda.synchronize()
+        k, v = logical(x)
+        o_ref, _ = oracle.fwd(x["q"], k, v, x["r"], x["u"], x["vb"], 0.125)
+        hi, lo = to_host(c.o), to_host(c.o_lo)
+        assert np.all(np.abs(lo) <= np.abs(hi) * 2.0 ** -8 + 1e-30)
+        assert np.abs(hi + lo - o_ref).mean() < 0.75 * np.abs(hi - o_ref).mean()
+
+
 def test_low_part_of_o_restores_the_unrounded_output():
     import torch
     B, H, L, cap, m = 2, 2, 150, 200, 180
