@@ -46,12 +46,37 @@ BWD_MAIN_SOURCES = ("long_context_lm_rel_gb300/csrc/attn_bwd_tc.cu", "long_conte
 BWD_MAIN_PROFILE = "profiles/bwd_main_kernel_B4H16L512M512.md"
 
 
+def code_of(text):
+    """C/CUDA source with its comments and blank space taken out (string
+    literals kept), so that the hash below follows the code alone."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def sources_sha256(paths):
+    """sha256 of the code (comments and blank space aside) of `paths`."""
     import hashlib
     h = hashlib.sha256()
     for rel in paths:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()
 
 

@@ -203,9 +203,10 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const uint32_t b0 = sb + F_BAR;
-  // TMA: (Q+v), the R band and, for an item's first pair, K/V of pair g
+  // TMA: (Q+v), the R band and, for an item's first pair, V of pair g
   // complete one phase of bar_nx0 / bar_nx1 (by the parity of g), so that the
-  // producer waits once per pair for them; dO and (Q+u) of a pair
+  // producer waits once per pair for them; dO of a pair; (Q+u) of a pair,
+  // with K for an item's first pair
   const uint32_t bar_nx0 = b0 + 8, bar_nx1 = b0 + 16;
   const uint32_t bar_do = b0 + 32, bar_qu = b0 + 40;
   // MMA commits: S and G; dP; dV; dK and dQc; dQp; dR (the pair's last)
@@ -267,9 +268,9 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // between items.
     // The whole warp runs the schedule (uniform control flow, so that the
     // descriptors stay in uniform registers); one elected thread issues.
-    // A phase of bar_nx{b} is opened by the copy issued without arrival
-    // ((Q+v)) and closed by the last one (the R band, with K/V), which
-    // arrives; the phase then completes when all of its bytes have landed.
+    // A phase of bar_nx{b} is opened by the first copy issued without
+    // arrival ((Q+v)) and closed by the last one (an R half), which arrives;
+    // the phase then completes when all of its bytes have landed.
     int n_do = 0, n_qu = 0, nx_closed0 = 0, nx_closed1 = 0;
     bool nx_open0 = false, nx_open1 = false;
     auto wait = [&](uint32_t bar, uint32_t parity) {
