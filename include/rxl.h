@@ -359,9 +359,10 @@ int rxl_device_error_flags(void);
  * pair recorded on the call's stream; up to 1024 launches per kernel are kept.
  * rxl_kernel_timing_read waits for the recorded events, returns the summed
  * device time in milliseconds and the number of timed launches, and clears
- * them. The events sit between kernels, so a timed launch does not overlap
- * the previous kernel's tail (programmatic dependent launch): timing is for
- * measurement runs, off by default. Both return 0 or a cudaError_t value.
+ * them. Launches captured into a CUDA graph are not timed. The events sit
+ * between kernels, so a timed launch does not overlap the previous kernel's
+ * tail (programmatic dependent launch): timing is for measurement runs, off
+ * by default. Both return 0 or a cudaError_t value.
  */
 int rxl_kernel_timing(int enable);
 int rxl_kernel_timing_read(int kernel, double *total_ms, int *launches);

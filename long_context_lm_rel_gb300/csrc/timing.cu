@@ -30,6 +30,10 @@ bool timing_enabled() { return g_enabled.load(std::memory_order_relaxed); }
 
 int timing_begin(int kernel, cudaStream_t st) {
   if (!timing_enabled() || kernel < 0 || kernel >= kTimedKernels) return -1;
+  // a launch being captured into a graph is not timed (its event records
+  // would become graph nodes)
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return -1;
   Timer &t = g_timers[kernel];
   std::lock_guard<std::mutex> lock(t.mu);
   if (t.used == kPairs) {

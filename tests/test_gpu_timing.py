@@ -34,3 +34,28 @@ def test_kernel_timing_covers_the_training_pair():
     torch.cuda.synchronize()
     for k in ids:
         assert rxl.rxl_kernel_timing_read(k) == (0.0, 0)
+
+
+def test_kernel_timing_skips_graph_capture():
+    import torch
+    import long_context_lm_rel_gb300 as rxl
+    ids = (rxl.RXL_KERNEL_FWD, rxl.RXL_KERNEL_BWD_MAIN, rxl.RXL_KERNEL_BWD_PREP, rxl.RXL_KERNEL_BWD_FINISH)
+    B, H, L, cap, m = 2, 4, 128, 128, 128
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=12)
+    c = run_gpu(x, cap, m, 0, "bf16", ex=True)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    try:
+        rxl.rxl_kernel_timing(True)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                c.fwd_ex().bwd_ex()
+        torch.cuda.current_stream().wait_stream(side)
+        graph.replay()
+        torch.cuda.synchronize()
+    finally:
+        rxl.rxl_kernel_timing(False)
+    for k in ids:
+        assert rxl.rxl_kernel_timing_read(k) == (0.0, 0)
