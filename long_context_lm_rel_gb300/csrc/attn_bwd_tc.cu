@@ -74,6 +74,7 @@ struct BwdParams {
   const float *lse, *delta;
   __nv_bfloat16 *dk, *dv;
   float *dv_acc;  // [H][64] column sums of the position part of dQ, zeroed
+  FastDiv fd_bh, fd_h;  // division by B*H and by H
 };
 
 // dR accumulates in [H][kDrPad + kv_rows][64] fp32 with kDrPad leading rows,
@@ -136,13 +137,13 @@ struct FItem {
 };
 
 __device__ __forceinline__ FItem fitem(const BwdParams &p, int w) {
-  const int BH = p.B * p.H;
   FItem it;
-  it.bh = w % BH;
-  it.h = it.bh % p.H;
-  const RowMemory rm = row_memory(p.mvis, it.bh / p.H, p.m, p.cap, p.head);
+  const int t = (int)p.fd_bh.div((uint32_t)w);  // w = t * B*H + bh
+  it.bh = w - t * (int)p.fd_bh.d;
+  const int b = (int)p.fd_h.div((uint32_t)it.bh);
+  it.h = it.bh - b * (int)p.fd_h.d;
+  const RowMemory rm = row_memory(p.mvis, b, p.m, p.cap, p.head);
   const KeyTiles tiles(rm.m, p.cap, rm.head, p.L);
-  const int t = w / BH;
   if (t >= tiles.count()) {
     it.x.phys0 = it.x.jlog0 = it.x.nvalid = 0;
     it.qlo = it.NQ = 0;
@@ -1301,6 +1302,8 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   p.B = s.B; p.H = s.H; p.L = s.L; p.cap = s.cap; p.m = s.m; p.head = s.head; p.nq = nq;
   p.kv_rows = s.kv_rows;
   p.mvis = s.mvis;
+  p.fd_bh.init((uint32_t)(s.B * s.H));
+  p.fd_h.init((uint32_t)s.H);
   {
     // key tiles per (b,h): ring runs A and B, then the current rows
     const int lenA = s.m < s.cap - s.head ? s.m : s.cap - s.head;

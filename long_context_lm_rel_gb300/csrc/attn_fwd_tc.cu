@@ -68,6 +68,7 @@ using tc::KeyTiles;
 using tc::RowMemory;
 using tc::lane_shift_window96;
 using tc::row_memory;
+using tc::FastDiv;
 
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
@@ -113,6 +114,7 @@ struct Params {
   __nv_bfloat16 *qu_out;
   __half *qv_out;  // (Q+v) rows in fp16 for the backward's position products
   const int *mvis;  // per-row document reset (nullable): newest memory rows per batch row
+  FastDiv fd_bh, fd_h;  // division by B*H and by H
 };
 
 constexpr int kFwd = 0, kPrep = 1;
@@ -143,13 +145,14 @@ struct Item {
 
 template <bool RESET>
 __device__ __forceinline__ Item item_at(const Params &p, int w) {
-  const int BH = p.B * p.H;
   Item it;
-  it.bh = w % BH;
-  it.h = it.bh % p.H;
-  it.i0 = (p.nq - 1 - w / BH) * BQ;
+  const uint32_t t = p.fd_bh.div((uint32_t)w);  // w = t * B*H + bh
+  it.bh = w - (int)(t * p.fd_bh.d);
+  const uint32_t b = p.fd_h.div((uint32_t)it.bh);
+  it.h = it.bh - (int)(b * p.fd_h.d);
+  it.i0 = (p.nq - 1 - (int)t) * BQ;
   if (RESET) {
-    const RowMemory rm = row_memory(p.mvis, it.bh / p.H, p.m, p.cap, p.head);
+    const RowMemory rm = row_memory(p.mvis, (int)b, p.m, p.cap, p.head);
     it.m = rm.m;
     it.head = rm.head;
   } else {
@@ -959,6 +962,8 @@ cudaError_t launch_mode(const AttnShape &s, const void *q, const void *k, const 
   p.B = s.B; p.H = s.H; p.L = s.L; p.cap = s.cap; p.m = s.m; p.head = s.head;
   p.mvis = s.mvis;
   p.nq = (s.L + BQ - 1) / BQ;
+  p.fd_bh.init((uint32_t)(s.B * s.H));
+  p.fd_h.init((uint32_t)s.H);
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.q = (const __nv_bfloat16 *)q; p.u = (const __nv_bfloat16 *)u; p.vb = (const __nv_bfloat16 *)vb;
   p.o = (__nv_bfloat16 *)o; p.o_lo = (__nv_bfloat16 *)o_lo; p.lse = lse;

@@ -15,6 +15,23 @@ using namespace sm103;
 
 constexpr int BQ = 128, BK = 128, DH = 64, NB = 256;
 
+// Unsigned division by a divisor fixed for a launch, for n, d < 2^31: with
+// s = ceil(log2 d) and m = floor(2^32 (2^s - d) / d) + 1 (computed on the
+// host), floor(n / d) = (umulhi(n, m) + n) >> s — the round-up reciprocal of
+// Granlund and Montgomery, "Division by invariant integers using
+// multiplication" (1994). The work cursors split item numbers with it.
+struct FastDiv {
+  uint32_t d, mul, shift;
+  __host__ void init(uint32_t divisor) {
+    d = divisor;
+    shift = 0;
+    while ((1ull << shift) < d) ++shift;
+    mul = (uint32_t)((((1ull << 32) * ((1ull << shift) - d)) / d) + 1);
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, mul) + n) >> shift; }
+  __device__ __forceinline__ uint32_t mod(uint32_t n) const { return n - div(n) * d; }
+};
+
 // A run of 128 physically contiguous K/V rows.
 struct KeyTile {
   int phys0;   // first physical K/V row
