@@ -14,7 +14,7 @@
 // product away and dV is divided by scale once per item.
 //
 // Kernels (all on the caller's stream):
-//   zero   : dR, the fp32 dQ accumulator and the du/dv sums <- 0; dK/dV rows
+//   zero   : dR, the fp32 dQ accumulator and the du/dv outputs <- 0; dK/dV rows
 //            of ring slots without valid memory <- 0; R -> fp16 copy
 //   prep   : D_i and the (Q+u) (bf16) and (Q+v) (fp16) rows, either from
 //            dO.(o + o_lo) in a streaming pass or, without o_lo, from the
@@ -29,13 +29,14 @@
 //            shared buffers its MMAs no longer need and added into fp32
 //            global accumulators by TMA tensor reductions, issued by a warp of
 //            their own while the next pair proceeds. The column sums of dQp over
-//            the rows give dv; du = (column sums of dQ) - dv.
+//            the rows give dv (added into dvbias, subtracted from du);
+//            du = (column sums of dQ) - dv.
 //            The position products run in fp16 with dG scaled by a power of
 //            two chosen per pair from max |dA|: R rows are several times
 //            larger than K rows, and bf16 rounding of dA in that term alone
 //            can exceed 1% of max|dQ| on short contexts.
-//   finish : dQ -> bf16 with per-head column sums, dR copied out; the last
-//            block forms du and dv
+//   finish : dQ -> bf16 with per-head column sums (added into du), dR
+//            copied out
 // (zero and prep share one launch when the forward kept the low part of O)
 #include <math.h>
 
@@ -73,7 +74,9 @@ struct BwdParams {
   float scale, scale_log2;
   const float *lse, *delta;
   __nv_bfloat16 *dk, *dv;
-  float *dv_acc;  // [H][64] column sums of the position part of dQ, zeroed
+  // [H][64] outputs, zeroed: dvb += the column sums of the position part of
+  // dQ, du -= them (the finish kernel adds the column sums of dQ into du)
+  float *du, *dvb;
   FastDiv fd_bh, fd_h;  // division by B*H and by H
 };
 
@@ -945,7 +948,8 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             }
           }
         }
-        atomicAdd(p.dv_acc + it.h * DH + 32 * hf + lane, dva[0]);
+        atomicAdd(p.dvb + it.h * DH + 32 * hf + lane, dva[0]);
+        atomicAdd(p.du + it.h * DH + 32 * hf + lane, -dva[0]);
 #pragma unroll
         for (int e = 0; e < 32; ++e) dva[e] = 0.f;
       }
@@ -960,16 +964,16 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
 // ---------------------------------------------------------- small kernels
 
-// The dR and dQ accumulators and the du/dv sums (with the finish kernel's
-// block counter) <- 0; dK/dV rows of ring slots that hold no valid memory
-// <- 0; R16 <- fp16(R) (satfinite).
+// The dR and dQ accumulators and the du/dv outputs (sums of atomic adds) <-
+// 0; dK/dV rows of ring slots that hold no valid memory <- 0; R16 <- fp16(R)
+// (satfinite).
 struct ZeroArgs {
   float *dr;
   size_t n_dr;
   float *dq_acc;
   size_t n_dq;
-  float *sums;
-  int n_sums;
+  float *du, *dvb;  // [H][64] each
+  int n_hd;
   __nv_bfloat16 *dk, *dv;
   int BH, H, cap, m, head, kv_rows;
   const __nv_bfloat16 *r;
@@ -982,7 +986,10 @@ __device__ void zero_work(const ZeroArgs &z, size_t tid, size_t stride) {
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   for (size_t e = tid; e < z.n_dr / 4; e += stride) ((float4 *)z.dr)[e] = z4;
   for (size_t e = tid; e < z.n_dq / 4; e += stride) ((float4 *)z.dq_acc)[e] = z4;
-  for (size_t e = tid; e < (size_t)z.n_sums; e += stride) z.sums[e] = 0.f;
+  for (size_t e = tid; e < (size_t)z.n_hd; e += stride) {
+    z.du[e] = 0.f;
+    z.dvb[e] = 0.f;
+  }
   float rmax = 0.f;  // largest |R| converted by this thread
   for (size_t e = tid; e < z.n_r / 8; e += stride) {
     const uint4 a = ((const uint4 *)z.r)[e];
@@ -1076,20 +1083,17 @@ __global__ void __launch_bounds__(256) bwd_light_prep_kernel(
   zero_work(z, blockIdx.x * (size_t)blockDim.x + threadIdx.x, (size_t)gridDim.x * blockDim.x);
 }
 
-// dq = bf16(dQ accumulator); per-head column sums of dQ into colsum[H][64].
-// Block (bh, chunk) covers 128 rows of one (b, h) plane: 8 threads per row,
-// 8 columns each. Every block also copies its slice of the dR rows out of
-// the padded accumulator; the last block to finish (a counter the zeroing
-// reset) forms du = (column sums of dQ) - dv and dv = the column sums of
-// the position part.
+// dq = bf16(dQ accumulator); the per-head column sums of dQ are added into
+// du (which the main kernel's atomics already hold -dv in), and the dR rows
+// are copied out of the padded accumulator. Block (bh, chunk) covers 128 rows
+// of one (b, h) plane: 8 threads per row, 8 columns each. No block waits on
+// another: every load is issued first, then the stores and the atomics.
 __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(
-    const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq, float *colsum,
-    const float *dv_acc, unsigned *counter, float *du, float *dvb, const float *dr_acc, float *dr,
-    int L, int H, int kv_rows, int chunks) {
+    const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq, float *du,
+    const float *__restrict__ dr_acc, float *__restrict__ dr, int L, int H, int kv_rows, int chunks) {
   griddep_wait();
   griddep_launch_dependents();
   __shared__ float part[8][64];  // column sums of each warp's rows
-  __shared__ bool last;
   const int bh = blockIdx.x / chunks, ch = blockIdx.x % chunks;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = threadIdx.x & 7, slot = threadIdx.x >> 3;
@@ -1104,6 +1108,14 @@ __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(
       const size_t off = ((size_t)bh * L + i) * DH + 8 * sub;
       a[t] = *(const float4 *)(dq_acc + off);
       b[t] = *(const float4 *)(dq_acc + off + 4);
+    }
+  }
+  {
+    // the block's share of the dR rows (16-byte chunks past the padding)
+    const size_t per_h = (size_t)kv_rows * (DH / 4), n = (size_t)H * per_h;
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+      const size_t h = e / per_h, o = e - h * per_h;
+      ((float4 *)dr)[e] = ((const float4 *)(dr_acc + (h * (kv_rows + kDrPad) + kDrPad) * DH))[o];
     }
   }
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -1134,25 +1146,7 @@ __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(
     float sum = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) sum += part[w][threadIdx.x];
-    atomicAdd(colsum + (bh % H) * DH + threadIdx.x, sum);
-    __threadfence();  // this block's column sums land before the counter moves
-  }
-  {
-    const size_t per_h = (size_t)kv_rows * (DH / 4), n = (size_t)H * per_h;
-    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
-      const size_t h = e / per_h, o = e - h * per_h;
-      ((float4 *)dr)[e] = ((const float4 *)(dr_acc + (h * (kv_rows + kDrPad) + kDrPad) * DH))[o];
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  for (int e = threadIdx.x; e < H * DH; e += blockDim.x) {
-    const float cs = __ldcg(colsum + e), pv = __ldcg(dv_acc + e);
-    dvb[e] = pv;
-    du[e] = cs - pv;
+    atomicAdd(du + (bh % H) * DH + threadIdx.x, sum);
   }
 }
 
@@ -1208,8 +1202,7 @@ size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 }  // namespace
 
 // Workspace: D [rows] f32 | (Q+u) [rows][64] bf16 | (Q+v) [rows][64] fp16 |
-// R fp16 [H][kv_rows][64] | dQ accumulator [rows][64] f32 | dv, colsum [H][64] f32,
-// finish counter u32 |
+// R fp16 [H][kv_rows][64] | dQ accumulator [rows][64] f32 |
 // dR accumulator [H][kDrPad + kv_rows][64] f32
 BwdWorkspace tc_bwd_workspace(const AttnShape &s) {
   const size_t rows = (size_t)s.B * s.H * s.L;
@@ -1219,8 +1212,7 @@ BwdWorkspace tc_bwd_workspace(const AttnShape &s) {
   w.dqv_off = w.dqu_off + up256(rows * DH * 2);
   const size_t r16_off = w.dqv_off + up256(rows * DH * 2);
   const size_t dq_off = r16_off + up256((size_t)s.H * s.kv_rows * DH * 2);
-  const size_t sums_off = dq_off + up256(rows * DH * 4);
-  const size_t dr_off = sums_off + up256((size_t)2 * s.H * DH * 4 + 4);
+  const size_t dr_off = dq_off + up256(rows * DH * 4);
   w.total = dr_off + up256((size_t)s.H * (kDrPad + s.kv_rows) * DH * 4);
   return w;
 }
@@ -1239,8 +1231,7 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   __half *r16 = (__half *)((char *)ws + r16_off);
   const size_t dq_off = r16_off + up256((size_t)s.H * s.kv_rows * DH * 2);
   float *dq_acc = (float *)((char *)ws + dq_off);
-  float *sums = (float *)((char *)ws + dq_off + up256(rows * DH * 4));  // dv_acc | colsum | counter
-  float *dr_acc = (float *)((char *)sums + up256((size_t)2 * s.H * DH * 4 + 4));
+  float *dr_acc = (float *)((char *)ws + dq_off + up256(rows * DH * 4));
   const size_t n_dr_acc = (size_t)s.H * (kDrPad + s.kv_rows) * DH;
   const int nq = (s.L + BQ - 1) / BQ;
 
@@ -1264,7 +1255,7 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   ZeroArgs z;
   z.dr = dr_acc; z.n_dr = n_dr_acc; z.dq_acc = dq_acc; z.n_dq = rows * DH;
-  z.sums = sums; z.n_sums = 2 * s.H * DH + 1;  // the counter is zero as a float too
+  z.du = du; z.dvb = dvb; z.n_hd = s.H * DH;
   z.dk = (__nv_bfloat16 *)dk; z.dv = (__nv_bfloat16 *)dv;
   z.BH = s.B * s.H; z.H = s.H; z.cap = s.cap; z.m = s.m; z.head = s.head; z.kv_rows = s.kv_rows;
   z.r = (const __nv_bfloat16 *)r; z.r16 = r16; z.n_r = (size_t)s.H * s.kv_rows * DH;
@@ -1315,7 +1306,7 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   p.scale_log2 = s.scale * kLog2e;
   p.lse = lse; p.delta = delta;
   p.dk = (__nv_bfloat16 *)dk; p.dv = (__nv_bfloat16 *)dv;
-  p.dv_acc = sums;
+  p.du = du; p.dvb = dvb;
   const unsigned grid = (unsigned)(p.nitems < sms ? p.nitems : sms);
   const int slot = timing_begin(1, st);
   cudaError_t e = launch_ex(rxl_bwd_main_kernel, dim3(grid), dim3(kThreads), F_SMEM, st, 1, tk, tv, tr16, tqu, tqv,
@@ -1326,8 +1317,8 @@ cudaError_t launch_tc_bwd(const AttnShape &s, const void *q, const void *k, cons
   const int chunks = (s.L + 127) / 128;
   const int fin_slot = timing_begin(3, st);
   e = launch_ex(bwd_dq_finish_kernel, dim3((unsigned)(s.B * s.H * chunks)), dim3(256), 0, st, 1,
-                (const float *)dq_acc, (__nv_bfloat16 *)dq, sums + s.H * DH, (const float *)sums,
-                (unsigned *)(sums + 2 * s.H * DH), du, dvb, (const float *)dr_acc, dr, s.L, s.H, s.kv_rows, chunks);
+                (const float *)dq_acc, (__nv_bfloat16 *)dq, du, (const float *)dr_acc, dr, s.L, s.H,
+                s.kv_rows, chunks);
   timing_end(3, fin_slot, st);
   ++*launches;
   return e != cudaSuccess ? e : cudaGetLastError();
