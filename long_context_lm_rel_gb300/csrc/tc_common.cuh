@@ -98,16 +98,34 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 // win[x] <- win[x + lane] for x = 0..63: a 96-value window (serving two
 // adjacent 32-key chunks) shifted left by the lane index in 5 predicated
-// stages, largest shift first (selects; the same stages as t*a + (1-t)*b on
-// the FMA pipe measured slower).
+// stages, largest shift first. Two of every three pairs of a stage are
+// selects on the ALU pipe and the third goes through the FMA pipe as
+// take * t + keep * (1 - t) with t in {0, 1}, which is exact for finite
+// values (the window holds position logits of finite operands): the stages
+// are the ALU pipe's main load, and this split measured fastest (all on the
+// ALU, half or a quarter on the FMA pipe were slower).
 __device__ __forceinline__ void lane_shift_window96(float (&win)[96], int lane) {
 #pragma unroll
   for (int b = 4; b >= 0; --b) {
     const int sh = 1 << b;
     const bool take = (lane >> b) & 1;
+    const float t = take ? 1.f : 0.f;
+    const float2 t2 = make_float2(t, t), nt2 = make_float2(1.f - t, 1.f - t);
+    const int n = 64 + sh - 1;  // window entries this stage still needs
 #pragma unroll
-    for (int e = 0; e < 95; ++e)
-      if (e < 64 + sh - 1) win[e] = take ? win[e + sh] : win[e];
+    for (int e = 0; e < 95; e += 2) {
+      if (e >= n) continue;
+      if ((e >> 1) % 3 == 2 && e + 1 < n) {
+        const float2 keep = make_float2(win[e], win[e + 1]);
+        const float2 tk = make_float2(win[e + sh], win[e + 1 + sh]);
+        const float2 r = __ffma2_rn(tk, t2, __fmul2_rn(keep, nt2));
+        win[e] = r.x;
+        win[e + 1] = r.y;
+      } else {
+        win[e] = take ? win[e + sh] : win[e];
+        if (e + 1 < n) win[e + 1] = take ? win[e + 1 + sh] : win[e + 1];
+      }
+    }
   }
 }
 
