@@ -11,7 +11,8 @@ float64 oracle on the same seeded inputs.
 * calls with at most half as many (b, h, query tile) items as SMs, which the
   forward runs as 2-CTA clusters (the small cases too, one of them with a
   single key tile per item, i.e. an empty second half);
-* stop-gradient: the cache is never written by the backward.
+* stop-gradient: the cache is never written by the backward;
+* NaN in every backward output and junk in the workspace on entry.
 """
 import math
 
@@ -98,6 +99,28 @@ def test_small_bf16_full_parity(B, H, L, cap, m, head, ex):
     x = make_inputs(B, H, L, cap, m, "bf16", seed=B * 1000 + L + m)
     c = run_gpu(x, cap, m, head, "bf16", ex=ex)
     compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head, ex)))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
+def test_backward_outputs_and_workspace_poisoned_on_entry(dtype, ex):
+    """The fp32 sums (dq, dr, du, dvbias) accumulate from zero inside the
+    call (du and dvbias by atomics from two kernels): NaN in every output and
+    0xFF bytes in the workspace on entry, twice in a row, must not reach the
+    results."""
+    import torch
+    if dtype == "f32" and ex:
+        pytest.skip("the training pair is the bf16 path")
+    B, H, L, cap, m, head = 2, 2, 200, 300, 250, 123
+    x = make_inputs(B, H, L, cap, m, dtype, seed=4242)
+    c = run_gpu(x, cap, m, head, dtype, bwd=False, ex=ex)
+    c.alloc_bwd(x["do"])
+    for rep in range(2):
+        for t in (c.dq, c.dk, c.dv, c.dr, c.du, c.dvb):
+            t.fill_(float("nan"))
+        c.ws.fill_(0xFF)
+        c.bwd_ex() if ex else c.bwd()
+        compare_full(x, c, cap, m, head, dtype, tag=f"poisoned, call {rep}")
 
 
 @pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
