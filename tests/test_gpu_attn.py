@@ -12,7 +12,9 @@ float64 oracle on the same seeded inputs.
   forward runs as 2-CTA clusters (the small cases too, one of them with a
   single key tile per item, i.e. an empty second half);
 * stop-gradient: the cache is never written by the backward;
-* NaN in every backward output and junk in the workspace on entry.
+* NaN in every backward output and junk in the workspace on entry;
+* seeded random shapes (tile edges, partly filled and wrapping rings, few
+  and many items).
 """
 import math
 
@@ -97,6 +99,61 @@ SMALL = [  # B, H, L, cap, m, head
 @pytest.mark.parametrize("B,H,L,cap,m,head", SMALL)
 def test_small_bf16_full_parity(B, H, L, cap, m, head, ex):
     x = make_inputs(B, H, L, cap, m, "bf16", seed=B * 1000 + L + m)
+    c = run_gpu(x, cap, m, head, "bf16", ex=ex)
+    compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head, ex)))
+
+
+def _random_shapes(n_small, n_wide, seed=2024):
+    """Seeded random shapes: small ones (few items: the forward's 2-CTA
+    clusters) and wide ones (many heads: the persistent forward), with
+    query lengths near tile edges, partly filled and wrapping rings."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n_small + n_wide):
+        wide = i >= n_small
+        B = int(rng.integers(1, 4)) if not wide else int(rng.integers(2, 5))
+        H = int(rng.integers(1, 4)) if not wide else int(rng.integers(12, 25))
+        L = int(rng.choice([1, 63, 127, 128, 129, 200, 255, 256, 257, 300]))
+        cap = int(rng.choice([0, 5, 127, 128, 200, 333, 400]))
+        m = int(rng.integers(0, cap + 1)) if cap else 0
+        head = int(rng.integers(0, cap)) if cap else 0
+        if L == 1 and m == 0:
+            continue  # one visible key per row: the degenerate case below
+        out.append((B, H, L, cap, m, head))
+    return out
+
+
+@pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
+def test_single_visible_key_gradients_vanish(ex):
+    """L = 1 without memory: each row sees only its own key, so P = 1,
+    O = v and D = dO.v = dP, and dA = scale P (dP - D) is identically zero
+    (the chain rule of "Dimension Walkthrough"). dq, dk, dr, du and dvbias are
+    then exactly zero, where a bound relative to max|ref| is zero too: the
+    kernel's dP and D are two fp32 sums of the same products (tensor core and
+    prep), so their difference leaves rounding residues, bounded here by
+    2^-16 of |dO| |v| scale |k|. dv = dO."""
+    import torch
+    B, H, L, cap, m, head = 2, 3, 1, 5, 0, 0
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=11)
+    c = run_gpu(x, cap, m, head, "bf16", ex=ex)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    k, v = logical(x)
+    assert_close("O", to_host(c.o), v[:, :, :L], "bf16")
+    g = oracle.bwd(x["q"], k, v, x["r"], x["u"], x["vb"], x["do"], 0.125)
+    for n in ("dq", "dk", "dr", "du", "dvb"):
+        assert np.all(g[n] == 0), n  # the definition's value
+    dv = logical_kv(to_host(c.dv), cap, head, m)
+    assert_close("dV", dv, g["dv"], "bf16")
+    scale_term = np.abs(x["do"]).max() * np.abs(v).max() * 0.125 * (np.abs(k).max() + np.abs(x["r"]).max()) * 64
+    for n, t in (("dq", c.dq), ("dk", c.dk), ("dr", c.dr), ("du", c.du), ("dvb", c.dvb)):
+        assert np.abs(to_host(t)).max() <= scale_term * 2.0 ** -16, n
+
+
+@pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
+@pytest.mark.parametrize("B,H,L,cap,m,head", _random_shapes(10, 3))
+def test_random_shapes_full_parity(B, H, L, cap, m, head, ex):
+    x = make_inputs(B, H, L, cap, m, "bf16", seed=7 * B + 13 * H + L + cap + m)
     c = run_gpu(x, cap, m, head, "bf16", ex=ex)
     compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head, ex)))
 
