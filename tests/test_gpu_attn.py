@@ -158,6 +158,13 @@ def test_random_shapes_full_parity(B, H, L, cap, m, head, ex):
     compare_full(x, c, cap, m, head, "bf16", tag=str((B, H, L, cap, m, head, ex)))
 
 
+@pytest.mark.parametrize("B,H,L,cap,m,head", _random_shapes(6, 0, seed=77))
+def test_random_shapes_f32_full_parity(B, H, L, cap, m, head):
+    x = make_inputs(B, H, L, cap, m, "f32", seed=5 * B + 11 * H + L + cap + m)
+    c = run_gpu(x, cap, m, head, "f32")
+    compare_full(x, c, cap, m, head, "f32", tag=str((B, H, L, cap, m, head)))
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("ex", [False, True], ids=["plain", "training_pair"])
 def test_backward_outputs_and_workspace_poisoned_on_entry(dtype, ex):

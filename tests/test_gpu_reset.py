@@ -4,14 +4,15 @@ Batch row b attends only to its newest mem_visible[b] memory rows
 (Transformer-XL page, "Causal Mask With Memory", the note after the mask
 picture; "Batched Streams": the reset is per row). Full forward and backward
 parity, including rows reset to 0, rows whose visible memory ends mid-tile,
-rings that wrap, out-of-range counts (clamped into [0, m]) and the fp32 path.
+rings that wrap, out-of-range counts (clamped into [0, m]), the fp32 path
+and seeded random shapes and counts.
 """
 import numpy as np
 import pytest
 
 import oracle
 from tests._harness import AttnCall, assert_close, assert_no_device_error, logical_kv, place_kv, to_host
-from tests.test_gpu_attn import make_inputs, logical
+from tests.test_gpu_attn import _random_shapes, make_inputs, logical
 
 pytestmark = pytest.mark.gpu
 
@@ -57,6 +58,25 @@ def _run(B, H, L, cap, m, head, mvis, dtype, keep_low, clamp_to=None, seed=None)
 @pytest.mark.parametrize("B,H,L,cap,m,head,mvis", CASES)
 def test_reset_bf16(B, H, L, cap, m, head, mvis, keep_low):
     _run(B, H, L, cap, m, head, mvis, "bf16", keep_low)
+
+
+def _random_reset_cases(seed=31):
+    """Seeded random shapes and mem_visible counts in [0, m] (partial tiles,
+    resets, wrapping rings); a one-row segment keeps at least one memory row
+    visible, so that no output is identically zero."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for B, H, L, cap, m, head in _random_shapes(8, 2, seed=seed):
+        if m == 0:
+            continue
+        lo = 1 if L == 1 else 0
+        out.append((B, H, L, cap, m, head, [int(rng.integers(lo, m + 1)) for _ in range(B)]))
+    return out
+
+
+@pytest.mark.parametrize("B,H,L,cap,m,head,mvis", _random_reset_cases())
+def test_reset_random_shapes(B, H, L, cap, m, head, mvis):
+    _run(B, H, L, cap, m, head, mvis, "bf16", keep_low=True)
 
 
 def test_reset_f32():
