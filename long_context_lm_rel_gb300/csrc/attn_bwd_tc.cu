@@ -277,8 +277,11 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // the phase then completes when all of its bytes have landed.
     int n_do = 0, n_qu = 0, nx_closed0 = 0, nx_closed1 = 0;
     bool nx_open0 = false, nx_open1 = false;
+    // (the polling loop out of line: the producer's code is the part of the
+    // kernel whose size costs time, while the softmax warps' waits stay
+    // inline, as a call there forces register saves)
     auto wait = [&](uint32_t bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+      return __all_sync(0xffffffffu, mbar_wait_lean(bar, parity, abort_flag));
     };
     // The R band of a pair is two 128-row halves (distances d0 .. d0+127 and
     // d0+128 .. d0+255). The next query tile of the same item needs
@@ -548,12 +551,12 @@ rxl_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (nx_open0) mbar_arrive(bar_nx0);
         if (nx_open1) mbar_arrive(bar_nx1);
         const int ph0 = nx_closed0 + (nx_open0 ? 1 : 0), ph1 = nx_closed1 + (nx_open1 ? 1 : 0);
-        if (ph0 > 0) mbar_wait(bar_nx0, (ph0 - 1) & 1, &no_abort);
-        if (ph1 > 0) mbar_wait(bar_nx1, (ph1 - 1) & 1, &no_abort);
-        if (n_do > 0) mbar_wait(bar_do, (n_do - 1) & 1, &no_abort);
-        if (n_qu > 0) mbar_wait(bar_qu, (n_qu - 1) & 1, &no_abort);
+        if (ph0 > 0) mbar_wait_lean(bar_nx0, (ph0 - 1) & 1, &no_abort);
+        if (ph1 > 0) mbar_wait_lean(bar_nx1, (ph1 - 1) & 1, &no_abort);
+        if (n_do > 0) mbar_wait_lean(bar_do, (n_do - 1) & 1, &no_abort);
+        if (n_qu > 0) mbar_wait_lean(bar_qu, (n_qu - 1) & 1, &no_abort);
         mma_commit(bar_drain);
-        mbar_wait(bar_drain, 0, &no_abort);
+        mbar_wait_lean(bar_drain, 0, &no_abort);
         atomicExch(&g_bwd_error, 1);
       }
       __syncwarp();

@@ -128,7 +128,7 @@ __device__ __forceinline__ bool pair_exchange(float mine, float *out, volatile f
   slot[hf * 128 + ii] = mine;
   __syncwarp();
   if (lane == 0) mbar_arrive(bar);
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, phase & 1, abort_flag));
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_lean(bar, phase & 1, abort_flag));
   ++phase;
   *out = slot[(1 - hf) * 128 + ii];
   return ok;
@@ -346,7 +346,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       vc.init(p, nitems);
       int g_kr = 0, g_v = 0;
       auto wait = [&](uint32_t bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+        return __all_sync(0xffffffffu, mbar_wait_lean(bar, parity, abort_flag));
       };
       auto issue_kr = [&]() {
         const int s = g_kr & 1;
@@ -498,13 +498,13 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // earlier one completed before it, and a completed phase returns at once)
         if (elect_one()) {
           volatile int no_abort = 0;
-          if (n_kr0 > 0) mbar_wait(bar_kr0, (n_kr0 - 1) & 1, &no_abort);
-          if (n_kr1 > 0) mbar_wait(bar_kr1, (n_kr1 - 1) & 1, &no_abort);
-          if (n_v0 > 0) mbar_wait(bar_v0, (n_v0 - 1) & 1, &no_abort);
-          if (n_v1 > 0) mbar_wait(bar_v1, (n_v1 - 1) & 1, &no_abort);
-          if (nq_loads > 0) mbar_wait(bar_q, (nq_loads - 1) & 1, &no_abort);
+          if (n_kr0 > 0) mbar_wait_lean(bar_kr0, (n_kr0 - 1) & 1, &no_abort);
+          if (n_kr1 > 0) mbar_wait_lean(bar_kr1, (n_kr1 - 1) & 1, &no_abort);
+          if (n_v0 > 0) mbar_wait_lean(bar_v0, (n_v0 - 1) & 1, &no_abort);
+          if (n_v1 > 0) mbar_wait_lean(bar_v1, (n_v1 - 1) & 1, &no_abort);
+          if (nq_loads > 0) mbar_wait_lean(bar_q, (nq_loads - 1) & 1, &no_abort);
           mma_commit(bar_drain);
-          mbar_wait(bar_drain, 0, &no_abort);
+          mbar_wait_lean(bar_drain, 0, &no_abort);
           atomicExch(&g_fwd_error, 1);
         }
         __syncwarp();
@@ -524,7 +524,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     Cursor<RESET, SPLIT> cur;
     cur.init(p, nitems);
     if (cur.valid) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait_lean(bar_q, 0, abort_flag));
       if (ok) {
         q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
         fence_proxy_async_smem();
@@ -538,7 +538,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       const int t = cur.t, t0 = cur.t0, t1 = cur.t1;
       const int i = it.i0 + ii;
       const int s = g & 1;
-      ok = mbar_wait(bar_sg, g & 1, abort_flag);
+      ok = mbar_wait_lean(bar_sg, g & 1, abort_flag);
       // tcgen05.ld/st below are warp-collective: keep every decision warp-uniform
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
@@ -623,7 +623,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       // the P buffer and O: P.V(g-1), which ran while this tile's logits
       // were formed, must be done
       if (g > 0) {
-        ok = mbar_wait(bar_pv, (g - 1) & 1, abort_flag);
+        ok = mbar_wait_lean(bar_pv, (g - 1) & 1, abort_flag);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
         tc_fence_after();
       }
@@ -640,7 +640,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       // rows of V past the run hold another run's (or junk) data: zero them
       // so that 0 * junk cannot leak into O (once the tile's V has landed)
       if (x.nvalid < BK) {
-        ok = __all_sync(0xffffffffu, mbar_wait(s ? bar_v1 : bar_v0, (g >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait_lean(s ? bar_v1 : bar_v0, (g >> 1) & 1, abort_flag));
         if (!ok) break;
       }
       if (ii >= x.nvalid) {
@@ -669,12 +669,12 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       // ---- last tile of the item: Q tiles of the next item, then epilogue
       if (cur.valid) {
         // the S/G MMAs of this item are all done (bar_sg waited above)
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_q, cur.k & 1, abort_flag)))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_lean(bar_q, cur.k & 1, abort_flag)))) break;
         q_prep<MODE>(p, cur.it, sbase, quad, hf, lane);
         fence_proxy_async_smem();
         mbar_arrive(bar_qready);
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, g & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait_lean(bar_pv, g & 1, abort_flag));
       // the two halves' references and sums; O_h and l_h are relative to
       // 2^(reference of half h), which is -inf for a half that saw no key
       float m_other = -INFINITY, l_other = 0.f;
@@ -723,7 +723,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           mbar_arrive(bar_staged);
           if (warp == 0) {
             if (lane == 0) {
-              ok = mbar_wait(bar_staged, 0, abort_flag) && mbar_wait_cluster(bar_peer, 0, abort_flag);
+              ok = mbar_wait_lean(bar_staged, 0, abort_flag) && mbar_wait_cluster(bar_peer, 0, abort_flag);
               if (ok) {
                 const uint32_t bar0 = mapa_shared(bar_data, 0);
                 bulk_copy_to_cluster(mapa_shared(sbase + SM_K, 0), sbase + SM_K, kHandBytes, bar0);
@@ -741,7 +741,7 @@ rxl_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             mbar_expect_tx(bar_data, kHandBytes + kMlBytes);  // the arrival of this phase
             mbar_arrive_remote(mapa_shared(bar_peer, 1));
           }
-          ok = __all_sync(0xffffffffu, mbar_wait(bar_data, 0, abort_flag));
+          ok = __all_sync(0xffffffffu, mbar_wait_lean(bar_data, 0, abort_flag));
           if (!ok) break;
           const float m1 = *(volatile float *)(smem + SM_V + 4 * ii);
           const float l1 = *(volatile float *)(smem + SM_V + 512 + 4 * ii);

@@ -112,6 +112,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same wait with its polling loop out of line: one probe inline, the
+// loop a call. Kernels with many wait sites keep their code smaller, which
+// the instruction cache rewards where the call's register saves cost little.
+static __device__ __noinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, volatile int *abort) {
+  return mbar_wait(bar, parity, abort);
+}
+__device__ __forceinline__ bool mbar_wait_lean(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_loop(bar, parity, abort);
+}
+
 // ----------------------------------------------------- thread-block clusters
 
 // All threads of every CTA of the cluster (once, right after the barriers of
