@@ -97,19 +97,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase of the given parity; false after g_wait_cycles (or when
 // another thread of the CTA already gave up: *abort != 0).
+// (Every probe after the first also checks the flag and the clock: the loop
+// stays a few instructions long at each of the kernels' many wait sites,
+// and a probe suspends the thread for a while when the phase is not done.)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (clock64() - t0 > g_wait_cycles) {
-        *abort = 1;
-        return false;
-      }
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort || clock64() - t0 > g_wait_cycles) {
+      *abort = 1;
+      return false;
     }
   }
+  return true;
 }
 
 // The same wait with its polling loop out of line: one probe inline, the
