@@ -41,7 +41,8 @@
 // relative to its own reference), reference and sum to rank 0 through
 // distributed shared memory once rank 0 has finished with its K/V stages;
 // rank 0 merges the two and writes the output. Every cross-CTA wait is a
-// bounded mbarrier wait.
+// bounded mbarrier wait. All waits here probe inline once and poll out of
+// line (mbar_wait_lean): the smaller code fetches faster.
 //
 // The skew: thread of row ii = 32*quad + lane needs G columns ii..ii+127. For
 // its 64 keys it loads one warp-uniform 96-column window and shifts it by its
